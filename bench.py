@@ -1,0 +1,387 @@
+#!/usr/bin/env python
+"""Throughput of one tensor-parallel forward step on GB300.
+
+A step is one pass of the whole hot path over one batch: vocab-parallel
+embedding of the step's token ids, the decoder layer(s) (every rank shard of
+the tensor-parallel layer, rank-sums in the row-parallel GEMM epilogues), the
+final norm, the vocab-parallel LM head and the argmax.  Default workload: one
+Qwen3-0.6B-shaped layer, prefill 1 x 2048 tokens, tp_size 2 emulated on one
+GPU.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--tp N]
+
+--impl reference times the CPU oracle (fp64, plain torch) on the host cores on
+a bounded sample of the same workload.  Under torchrun (N > 1) every rank runs
+an independent replica (the tensor-parallel ranks are emulated inside one GPU);
+rank 0 prints.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+import torch.distributed as dist  # noqa: E402
+
+import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "qwen3_0.6b_layer_prefill2048"
+METRIC = "tokens/sec per layer-forward (prefill & decode) on 1 GB300; % HBM BW / % TC peak"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def workload_config(w: synth.Workload, n: int) -> dict:
+    s = w.shape
+    return {"workload": w.name,
+            "shape": f"hidden {s.hidden}, {s.num_q_heads} q / {s.num_kv_heads} kv heads, head_dim {s.head_dim}, "
+                     f"intermediate {s.intermediate}, vocab {s.vocab}, {w.layers_run} layer(s)",
+            "batch": f"{len(w.prefill)} prefill seqs {[q for q, _ in w.prefill]} + {len(w.decode)} decode seqs",
+            "tokens_per_step": w.num_tokens, "tp_size": n, "tp_emulated_on_one_gpu": True,
+            "step": "embed(ids) + decoder layer(s) + final norm + LM head + argmax",
+            "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write, outside the step events)"}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work per launch of each kernel kind (emulated TP: all ranks' work)
+# ---------------------------------------------------------------------------
+
+def kernel_work(kind: str, w: synth.Workload, n: int):
+    s = w.shape
+    T, H, hd, I, V = w.num_tokens, s.hidden, s.head_dim, s.intermediate, s.vocab
+    nq_l = s.num_q_heads // n
+    nkv_l = s.num_kv_heads // n if s.num_kv_heads >= n else 1
+    B = w.num_seqs
+    if kind == "gemm_qkv":
+        return "tensor", 2.0 * T * H * n * (nq_l + 2 * nkv_l) * hd
+    if kind == "gemm_o":
+        return "tensor", 2.0 * T * H * s.num_q_heads * hd
+    if kind == "gemm_gate_up":
+        return "tensor", 2.0 * T * H * 2 * I
+    if kind == "gemm_down":
+        return "tensor", 2.0 * T * I * H
+    if kind == "attn_prefill":
+        f = 0.0
+        for q, c in w.prefill:
+            f += 4.0 * hd * s.num_q_heads * (q * c + q * (q + 1) / 2)
+        return "tensor", f
+    if kind == "attn_decode":
+        return "hbm", float(sum(c + 1 for c in w.decode)) * n * nkv_l * hd * 2 * 2
+    if kind == "gemm_lm_head":
+        return "hbm", float(V) * H * 2 + B * H * 2
+    if kind in ("embed", "rmsnorm"):
+        return "hbm", float(T) * H * 2 * 2
+    if kind == "rope":
+        return "hbm", float(T) * n * (nq_l + 2 * nkv_l) * hd * 2 * 2
+    return "hbm", 0.0
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            n += 1
+            for name, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+class OracleStep:
+    """The CPU oracle on a causal prefix of the workload's first sequence
+    (embed + layers + head): a bounded sample of the same workload."""
+
+    def __init__(self, w: synth.Workload):
+        from oracle import forward as of
+        from oracle import inputs as oi
+        self.of, self.w = of, w
+        s = w.shape
+        self.shape = oi.shape_of(s)
+        self.layers = [oi.layer_weights(s, li) for li in range(w.layers_run)]
+        self.head = oi.head_weights(s)
+        self.ids = torch.from_numpy(synth.step_token_ids(w.num_tokens, s.vocab))
+        self.cores = torch.get_num_threads()
+
+    def run(self, tokens: int) -> float:
+        of, s = self.of, self.w.shape
+        empty = torch.zeros(s.num_kv_heads, 0, s.head_dim, dtype=torch.float64)
+        seq = of.SeqInput(hidden=None, ids=self.ids[:tokens], k_cache=[empty] * len(self.layers),
+                          v_cache=[empty] * len(self.layers))
+        t0 = time.perf_counter()
+        of.run_sequence(seq, self.layers, self.head, self.shape, n=0)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(w: synth.Workload, budget_s: float = 15.0) -> dict:
+    o = OracleStep(w)
+    first = w.prefill[0][0] if w.prefill else 1
+    tokens, total_t, total_tok, runs = min(64, first), 0.0, 0, 0
+    while total_t < budget_s:
+        dt = o.run(tokens)
+        total_t += dt
+        total_tok += tokens
+        runs += 1
+        if dt < budget_s / 8 and tokens < first:
+            tokens = min(first, tokens * 2)
+    return {"value": total_tok / total_t, "unit": "tokens/s", "cores": o.cores, "kind": "oracle",
+            "sample": f"{runs} runs of the fp64 oracle (embed + {w.layers_run} layer(s) + head) on causal prefixes "
+                      f"of up to {tokens} of the first sequence's tokens, {total_t:.1f} s"}
+
+
+def run_reference(args, w: synth.Workload, n: int) -> dict:
+    o = OracleStep(w)
+    first = w.prefill[0][0] if w.prefill else 1
+    t16 = o.run(min(16, first))
+    budget = 150.0
+    per_step = budget / max(1, args.steps + args.warmup)
+    tokens = max(1, min(first, int(16 * per_step / max(t16, 1e-6))))
+    for _ in range(args.warmup):
+        o.run(tokens)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.run(tokens)
+    dt = time.perf_counter() - t0
+    value = tokens * args.steps / dt
+    sample = f"causal prefix of {tokens} of the {w.num_tokens} step tokens per step (embed + layers + head), fp64"
+    return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded counter generator)",
+            "config": workload_config(w, n), "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": o.cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def build_runner(w: synth.Workload, n: int):
+    import synth.device as sd
+    from tensor_transformer_forward_gb300 import ModelConfig
+    from tensor_transformer_forward_gb300.runner import TPRunner
+    s = w.shape
+    cfg = ModelConfig(s.hidden, s.num_q_heads, s.num_kv_heads, s.head_dim, s.intermediate, s.vocab, s.num_layers,
+                      s.rms_eps, s.rope_theta, n, s.tie_word_embeddings)
+    q, c = w.q_lens, w.ctx_lens
+    cap = (max(a + b for a, b in zip(q, c)) + 63) // 64 * 64
+    r = TPRunner(cfg, w.layers_run, w.num_seqs, cap, w.num_tokens)
+    for li in range(w.layers_run):
+        full = sd.layer_weights(s, li)
+        r.load_layer(li, full)
+        del full
+    r.load_head(sd.head_weights(s))
+    hmap = r.kv_head_map()
+    fill = max(c)
+    for li in range(w.layers_run):
+        if fill > 0:
+            sd.fill_kv_cache(r.kv[li], n, w.num_seqs, r.nkv_l, cap, s.head_dim, hmap, s.num_kv_heads, li,
+                             w.num_seqs, fill)
+    batch = r.make_batch(q, c, list(range(w.num_seqs)), num_prefill=len(w.prefill))
+    ids = sd.token_ids(w.num_tokens, s.vocab)
+    return r, batch, ids
+
+
+def run_ours(args, w: synth.Workload, n: int, rank: int, world: int) -> dict:
+    dev = torch.cuda.current_device()
+    r, batch, ids = build_runner(w, n)
+    ctx = r.ctx
+    T, H, B = w.num_tokens, w.shape.hidden, w.num_seqs
+    hidden = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    out_ids = torch.empty(B, dtype=torch.int32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def step():
+        r.step(batch, ids=ids, hidden=hidden, out_ids=out_ids)
+
+    # untimed: which kernel dominates the step
+    step()
+    torch.cuda.synchronize()
+    r.check_status()
+    ctx.profile_begin(list(__import__("tensor_transformer_forward_gb300").binding.KERNELS))
+    for _ in range(5):
+        flush.zero_()
+        step()
+    prof = ctx.profile_end()
+    dominant = max(prof, key=lambda k: prof[k][0])
+    breakdown = {k: round(v[0] / v[1] * 1e3, 2) for k, v in sorted(prof.items(), key=lambda kv: -kv[1][0])}
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(dev)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = ctx.launch_count()
+    ctx.profile_begin([dominant], max_launches=max(64, 8 * args.steps))
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record()
+        step()
+        ends[i].record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    dom = ctx.profile_end()
+    launches = ctx.launch_count() - launches0
+    clk = clocks.stop()
+    r.check_status()
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
+    ms_t = torch.tensor([ms], dtype=torch.float64, device="cuda" if world > 1 and dist.get_backend() == "nccl" else "cpu")
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+
+    # roofline of the dominant kernel, timed live in the timed region
+    pk = peaks()
+    bound, work = kernel_work(dominant, w, n)
+    dms, dcount = dom.get(dominant, (0.0, 0))
+    avg_s = dms / max(dcount, 1) / 1e3
+    if bound == "tensor":
+        achieved = work / avg_s / 1e12
+        peak = pk["bf16_tflops_sustained"]
+        unit = "TFLOP/s"
+    else:
+        achieved = work / avg_s / 1e9
+        peak = pk["hbm_gbs"]
+        unit = "GB/s"
+    roofline = {"bound": "tensor" if bound == "tensor" else "hbm", "kernel": dominant,
+                "achieved": round(achieved, 2), "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
+                "traffic": None, "peak_source": f"{pk['source']} ({'sustained bf16' if bound == 'tensor' else 'copy'})",
+                "algorithmic_per_launch": work, "avg_launch_ms": round(avg_s * 1e3, 4), "launches_timed": dcount}
+
+    # end to end through the public API: pinned host ids in, next ids out, every step
+    ids_host = ids.cpu().pin_memory()
+    out_host = torch.empty(B, dtype=torch.int32).pin_memory()
+    e2e_steps = min(args.steps, 200)
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    ids_dev = torch.empty_like(ids)
+    for i in range(e2e_steps):
+        flush.zero_()
+        e_s[i].record()
+        ids_dev.copy_(ids_host, non_blocking=True)
+        r.step(batch, ids=ids_dev, hidden=hidden, out_ids=out_ids)
+        out_host.copy_(out_ids, non_blocking=True)
+        e_e[i].record()
+    torch.cuda.synchronize()
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / e2e_steps
+
+    line = {"metric": METRIC, "value": world * T / (ms_max / 1e3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
+            "data": "synthetic (seeded counter generator; random-init weights of the named shape)",
+            "config": workload_config(w, n), "roofline": roofline,
+            "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": T * 4,
+                    "d2h_bytes_per_step": B * 4},
+            "gpu_launches": launches, "clocks": clk,
+            "kernel_ms_per_step": breakdown, "wall_s_timed_region": round(wall, 3)}
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--tp", type=int, default=None)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = synth.WORKLOADS[args.workload]
+    n = args.tp if args.tp is not None else max(w.tp_sizes)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, w, n)), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    line = run_ours(args, w, n, rank, world)
+    if rank == 0:
+        if world == 1:
+            line["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -36,7 +36,7 @@ DTYPE = torch.float64
 
 def from_bf16_bits(bits: np.ndarray, dtype=DTYPE) -> torch.Tensor:
     """Exact upcast of bf16 bit patterns (uint16) to ``dtype``."""
-    u32 = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    u32 = np.left_shift(np.asarray(bits, dtype=np.uint16).astype(np.uint32), np.uint32(16))
     return torch.from_numpy(u32.view(np.float32).copy()).to(dtype)
 
 
@@ -160,7 +160,7 @@ def argmax_first(logits: torch.Tensor) -> torch.Tensor:
 # ---------------------------------------------------------------------------
 
 def decoder_layer(x: torch.Tensor, w: LayerWeights, shape: Shape,
-                  k_cache: torch.Tensor, v_cache: torch.Tensor
+                  k_cache: torch.Tensor, v_cache: torch.Tensor, trace: Optional[dict] = None
                   ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """One decoder layer for one sequence, unsharded.
 
@@ -186,7 +186,10 @@ def decoder_layer(x: torch.Tensor, w: LayerWeights, shape: Shape,
     o = causal_gqa_attention(q, K, V)
     x = x + o.transpose(0, 1).reshape(T, nq * hd) @ w.o.T
     h2 = rms_norm(x, w.post_norm, shape.rms_eps)
-    x = x + (silu(h2 @ w.gate.T) * (h2 @ w.up.T)) @ w.down.T
+    act = silu(h2 @ w.gate.T) * (h2 @ w.up.T)
+    if trace is not None:  # intermediates, for diagnosis only
+        trace.update(h=h, q=q, k=k, v=v, attn=o.transpose(0, 1).reshape(T, nq * hd), x_mid=x, h2=h2, act=act)
+    x = x + act @ w.down.T
     return x, K, V
 
 
@@ -476,9 +479,9 @@ class SeqOutput:
 
 
 def run_sequence(seq: SeqInput, layers: Sequence[LayerWeights], hw: Optional[HeadWeights],
-                 shape: Shape, n: int = 0, comm: Optional[Comm] = None) -> SeqOutput:
-    """Embedding (if ids) -> layers -> (if hw) final norm, logits of the last
-    position, argmax.  n == 0 runs unsharded; n >= 1 runs the TP emulation."""
+                 shape: Shape, n: int = 0, comm: Optional[Comm] = None, head: bool = True) -> SeqOutput:
+    """Embedding (if ids) -> layers -> (if hw and head) final norm, logits of the
+    last position, argmax.  n == 0 runs unsharded; n >= 1 runs the TP emulation."""
     tp = n >= 1
     if tp:
         validate_tp(shape, n)
@@ -500,7 +503,7 @@ def run_sequence(seq: SeqInput, layers: Sequence[LayerWeights], hw: Optional[Hea
             ks.append(K)
             vs.append(V)
     out = SeqOutput(hidden=x, k_cache=ks, v_cache=vs)
-    if hw is not None:
+    if hw is not None and head:
         logits = tp_lm_head(x[-1], hw, shape, n, comm) if tp else lm_head(x[-1], hw, shape)
         out.logits = logits
         out.next_id = int(argmax_first(logits))

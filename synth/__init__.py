@@ -60,13 +60,18 @@ def mix64_int(z: int) -> int:
     return z ^ (z >> 31)
 
 
+# Bitwise work goes through the ufuncs explicitly (np.right_shift, ...): on some
+# NumPy builds the operator forms (>>, ^, &) on uint64 arrays are far slower.
+_RS, _XOR, _AND = np.right_shift, np.bitwise_xor, np.bitwise_and
+
+
 def _mix64(z: np.ndarray) -> np.ndarray:
     """SplitMix64 output function, in place on a uint64 array (wrapping)."""
-    z ^= z >> np.uint64(30)
-    z *= np.uint64(MIX1)
-    z ^= z >> np.uint64(27)
-    z *= np.uint64(MIX2)
-    z ^= z >> np.uint64(31)
+    _XOR(z, _RS(z, np.uint64(30)), out=z)
+    np.multiply(z, np.uint64(MIX1), out=z)
+    _XOR(z, _RS(z, np.uint64(27)), out=z)
+    np.multiply(z, np.uint64(MIX2), out=z)
+    _XOR(z, _RS(z, np.uint64(31)), out=z)
     return z
 
 
@@ -86,12 +91,12 @@ def bits(seed: int, stream: int, index: np.ndarray) -> np.ndarray:
 def _f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round fp32 to bf16 (nearest, ties to even); inputs here are finite."""
     u = x.astype(np.float32).view(np.uint32)
-    rounding = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
-    return ((u + rounding) >> np.uint32(16)).astype(np.uint16)
+    rounding = _AND(_RS(u, np.uint32(16)), np.uint32(1)) + np.uint32(0x7FFF)
+    return _RS(u + rounding, np.uint32(16)).astype(np.uint16)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
-    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return np.left_shift(np.asarray(b, dtype=np.uint16).astype(np.uint32), np.uint32(16)).view(np.float32)
 
 
 def normal_bf16_bits_at(seed: int, stream: int, index: np.ndarray, sigma: float,
@@ -99,7 +104,10 @@ def normal_bf16_bits_at(seed: int, stream: int, index: np.ndarray, sigma: float,
     """bf16 bit patterns of the approximately N(mean, sigma^2) draws at ``index``."""
     u = bits(seed, stream, index)
     m = np.uint64(0xFFFF)
-    s = (u & m) + ((u >> np.uint64(16)) & m) + ((u >> np.uint64(32)) & m) + (u >> np.uint64(48))
+    s = _AND(u, m)
+    s += _AND(_RS(u, np.uint64(16)), m)
+    s += _AND(_RS(u, np.uint64(32)), m)
+    s += _RS(u, np.uint64(48))
     x = (s.astype(np.int64) - IH_CENTER).astype(np.float32) * IH_SCALE
     y = x * np.float32(sigma)
     if mean is not None:
@@ -109,7 +117,7 @@ def normal_bf16_bits_at(seed: int, stream: int, index: np.ndarray, sigma: float,
 
 def normal_bf16_bits(seed: int, stream: int, count: int, sigma: float,
                      mean: Optional[float] = None, start: int = 0,
-                     chunk: int = 1 << 24) -> np.ndarray:
+                     chunk: int = 1 << 20) -> np.ndarray:
     """``count`` consecutive draws of a stream, as bf16 bit patterns (uint16)."""
     out = np.empty(count, dtype=np.uint16)
     for c0 in range(0, count, chunk):
@@ -122,7 +130,7 @@ def normal_bf16_bits(seed: int, stream: int, count: int, sigma: float,
 def token_ids(seed: int, stream: int, count: int, vocab: int, start: int = 0) -> np.ndarray:
     """Token ids uniform in ``[0, vocab)`` (int64)."""
     u = bits(seed, stream, np.arange(start, start + count, dtype=np.uint64))
-    return (((u >> np.uint64(32)) * np.uint64(vocab)) >> np.uint64(32)).astype(np.int64)
+    return _RS(_RS(u, np.uint64(32)) * np.uint64(vocab), np.uint64(32)).astype(np.int64)
 
 
 # ---------------------------------------------------------------------------

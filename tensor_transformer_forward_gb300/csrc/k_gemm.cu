@@ -1,0 +1,542 @@
+// tcgen05 / TMEM / TMA GEMM with the tensor-parallel epilogues.
+//
+// Computes, for every token row t and feature f,
+//     Y[t, f] = sum_r  X[t, r-th K segment] . W[r-th row block + f, :]
+// where the segments r are the tensor-parallel ranks of a row-split layer
+// (o_proj, down_proj) or a single segment for column-split layers (merged QKV,
+// merged gate/up, LM head with all ranks' vocab slices stacked).
+// ("Tensor parallelism from scratch", section "Two ways to split": a column
+// split gives each rank a slice of the output, a row split gives each rank a
+// partial sum that the all-reduce adds up; mini-SGLang linear.py:102-106.)
+//
+// Each rank's partial is accumulated by the tensor core in its own TMEM
+// accumulator (fp32) and the partials are added in fixed rank order in the
+// epilogue -- the all-reduce of the pages, done in HBM/registers on one GPU.
+//
+// Structure: persistent, warp-specialised, 192 threads per CTA.
+//   warp 0      TMA producer: X and W tiles (64-wide K blocks, 128-byte
+//               swizzle) into a STAGES-deep shared-memory ring.
+//   warp 1      TMEM allocator + MMA issuer (one thread): tcgen05.mma
+//               M=128 x N=BN x K=16, two TMEM accumulators so the epilogue of
+//               one segment overlaps the main loop of the next.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
+//               token row per thread), then the fused epilogue.
+// Split-K (for small token counts): a tile's K range is split over several
+// CTAs; each writes an fp32 partial, the last to arrive (atomic counter, no
+// spin-wait) adds the partials in split order and runs the epilogue.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cstdio>
+
+#include "kernels.h"
+#include "sm100.cuh"
+
+namespace tpk {
+
+struct GemmParams {
+  int T, n_seg, kb_seg, x_k_seg, w_row_seg;
+  int tiles_t, tiles_f, splits, total_kb;
+  void* out;
+  int ldo, out_cols;
+  float* partials;
+  int* counters;
+  float* amax_val;
+  int* amax_idx;
+  int amax_ld;
+  float* logits;
+  int ld_logits, vocab;
+  int* status;
+};
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int A_BYTES = 128 * 128;  // 128 rows x 64 bf16
+  static constexpr int B_BYTES = BN * 128;   // BN rows x 64 bf16
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);
+  static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64;
+};
+
+struct Unit {
+  int tt, tf, split, g0, g1;
+};
+
+__device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
+  Unit un;
+  un.split = u % p.splits;
+  const int tile = u / p.splits;
+  un.tf = tile % p.tiles_f;
+  un.tt = tile / p.tiles_f;
+  un.g0 = static_cast<int>((static_cast<long long>(un.split) * p.total_kb) / p.splits);
+  un.g1 = static_cast<int>((static_cast<long long>(un.split + 1) * p.total_kb) / p.splits);
+  return un;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+// ---- epilogue stores for one token row, 32 consecutive tile columns ----
+template <int EPI>
+__device__ __forceinline__ void store_chunk(const GemmParams& p, int t, int f, const float* v) {
+  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(t) * p.ldo + f;
+  if (f + 32 <= p.out_cols) {
+    uint4* o4 = reinterpret_cast<uint4*>(o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float x[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = v[j * 8 + i];
+      if (EPI == EPI_RESID) {
+        const uint4 r = o4[j];
+        x[0] += bf16lo(r.x); x[1] += bf16hi(r.x);
+        x[2] += bf16lo(r.y); x[3] += bf16hi(r.y);
+        x[4] += bf16lo(r.z); x[5] += bf16hi(r.z);
+        x[6] += bf16lo(r.w); x[7] += bf16hi(r.w);
+      }
+      uint4 w;
+      w.x = pack_bf16x2(x[0], x[1]);
+      w.y = pack_bf16x2(x[2], x[3]);
+      w.z = pack_bf16x2(x[4], x[5]);
+      w.w = pack_bf16x2(x[6], x[7]);
+      o4[j] = w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (f + i < p.out_cols) {
+        float x = v[i];
+        if (EPI == EPI_RESID) x += bf2f(o[i]);
+        o[i] = f2bf(x);
+      }
+    }
+  }
+}
+
+// SiLU(gate) * up for 32 output features starting at fo.
+__device__ __forceinline__ void store_silu(const GemmParams& p, int t, int fo, const float* g, const float* u) {
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = silu_f(g[i]) * u[i];
+  store_chunk<EPI_STORE>(p, t, fo, v);
+}
+
+__device__ __forceinline__ void argmax_scan(const GemmParams& p, int t, int f, const float* v, float& best,
+                                            int& bi) {
+  float* lg = p.logits ? p.logits + static_cast<size_t>(t) * p.ld_logits : nullptr;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int fi = f + i;
+    if (fi < p.vocab) {
+      const float x = v[i];
+      if (lg) lg[fi] = x;
+      const bool take = (bi < 0) || (x > best) || (x != x && best == best);
+      if (take) {
+        best = x;
+        bi = fi;
+      }
+    }
+  }
+}
+
+template <int BN, int EPI, bool ACC>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                   const GemmParams p) {
+  using C = GemmCfg<BN>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * C::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bar0 = smem_u32(bars);
+#define FULL(s) (bar0 + 8u * (s))
+#define EMPTY(s) (bar0 + 8u * (STAGES + (s)))
+#define TFULL(b) (bar0 + 8u * (2 * STAGES + (b)))
+#define TEMPTY(b) (bar0 + 8u * (2 * STAGES + 2 + (b)))
+#define DRAIN (bar0 + 8u * (2 * STAGES + 4))
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(FULL(s), 1);
+      mbar_init(EMPTY(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(TFULL(b), 1);
+      mbar_init(TEMPTY(b), 4);
+    }
+    mbar_init(DRAIN, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int units = p.tiles_t * p.tiles_f * p.splits;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        const Unit un = unit_of(p, u);
+        const int t0 = un.tt * 128, f0 = un.tf * BN;
+        for (int g = un.g0; g < un.g1; ++g) {
+          const int r = g / p.kb_seg, kb = g - r * p.kb_seg;
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(EMPTY(s), ph ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(FULL(s), C::STAGE_BYTES);
+          tma_load_2d(smem_u32(sA + s * C::A_BYTES), &tmX, FULL(s), r * p.x_k_seg + kb * 64, t0);
+          tma_load_2d(smem_u32(sB + s * C::B_BYTES), &tmW, FULL(s), kb * 64, r * p.w_row_seg + f0);
+          ++it;
+        }
+      }
+      // every load issued has landed before the CTA may exit
+      for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+        mbar_wait(FULL(j % STAGES), (j / STAGES) & 1, nullptr, p.status);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, BN);
+      int it = 0, seg = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        const Unit un = unit_of(p, u);
+        for (int g = un.g0; ok && g < un.g1;) {
+          const int gend = min(un.g1, (g / p.kb_seg + 1) * p.kb_seg);
+          const int b = seg & 1;
+          const uint32_t use = (seg >> 1) & 1;
+          if (!mbar_wait(TEMPTY(b), use ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+          const int gs = g;
+          for (; g < gend; ++g) {
+            const int s = it % STAGES;
+            const uint32_t ph = (it / STAGES) & 1;
+            if (!mbar_wait(FULL(s), ph, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t ad = sdesc_k_sw128(smem_u32(sA + s * C::A_BYTES));
+            const uint64_t bd = sdesc_k_sw128(smem_u32(sB + s * C::B_BYTES));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_bf16(d, ad + 2ull * kk, bd + 2ull * kk, idesc, (g > gs || kk > 0) ? 1u : 0u);
+            tc_commit(EMPTY(s));
+            ++it;
+          }
+          if (!ok) break;
+          tc_commit(TFULL(b));
+          ++seg;
+        }
+      }
+      tc_commit(DRAIN);
+      mbar_wait(DRAIN, 0, nullptr, p.status);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    int seg = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const Unit un = unit_of(p, u);
+      const int t = un.tt * 128 + row;
+      const int f0 = un.tf * BN;
+      const bool row_ok = t < p.T;
+      if constexpr (!ACC) {
+        const int b = seg & 1;
+        const uint32_t use = (seg >> 1) & 1;
+        if (!mbar_wait(TFULL(b), use, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t ta = lane_addr + static_cast<uint32_t>(b * BN);
+        if constexpr (EPI == EPI_SILU) {
+#pragma unroll 1
+          for (int qb = 0; qb < BN / 128; ++qb) {
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+              float gv[32], uv[32];
+              tc_ld32(ta + qb * 128 + h * 32, gv);
+              tc_ld32(ta + qb * 128 + 64 + h * 32, uv);
+              if (row_ok) store_silu(p, t, f0 / 2 + qb * 64 + h * 32, gv, uv);
+            }
+          }
+        } else if constexpr (EPI == EPI_ARGMAX) {
+          float best = -INFINITY;
+          int bi = -1;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tc_ld32(ta + c * 32, v);
+            if (row_ok) argmax_scan(p, t, f0 + c * 32, v, best, bi);
+          }
+          if (row_ok) {
+            p.amax_val[static_cast<size_t>(un.tf) * p.amax_ld + t] = best;
+            p.amax_idx[static_cast<size_t>(un.tf) * p.amax_ld + t] = bi < 0 ? INT_MAX : bi;
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tc_ld32(ta + c * 32, v);
+            if (row_ok) store_chunk<EPI>(p, t, f0 + c * 32, v);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(TEMPTY(b));
+        ++seg;
+      } else {
+        float acc[BN];
+#pragma unroll
+        for (int i = 0; i < BN; ++i) acc[i] = 0.0f;
+        bool ok = true;
+        for (int g = un.g0; g < un.g1;) {
+          g = min(un.g1, (g / p.kb_seg + 1) * p.kb_seg);
+          const int b = seg & 1;
+          const uint32_t use = (seg >> 1) & 1;
+          if (!mbar_wait(TFULL(b), use, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ta = lane_addr + static_cast<uint32_t>(b * BN);
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tc_ld32(ta + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[c * 32 + i] += v[i];
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(TEMPTY(b));
+          ++seg;
+        }
+        // every epilogue thread takes the same path from here (named barriers follow)
+        if (!named_bar_and(1, 128, ok)) break;
+        if (p.splits > 1) {
+          const int tile = un.tt * p.tiles_f + un.tf;
+          float* part = p.partials + (static_cast<size_t>(tile) * p.splits + un.split) * (BN * 128);
+#pragma unroll
+          for (int c = 0; c < BN; ++c) part[c * 128 + row] = acc[c];
+          __threadfence();
+          named_bar_sync(1, 128);
+          if (threadIdx.x == 64) {
+            const int old = atomicAdd(p.counters + tile, 1);
+            *last_flag = (old == p.splits - 1) ? 1 : 0;
+          }
+          named_bar_sync(1, 128);
+          const bool last = *last_flag != 0;
+          if (!last) continue;
+          __threadfence();
+          const float* base = p.partials + static_cast<size_t>(tile) * p.splits * (BN * 128);
+#pragma unroll
+          for (int c = 0; c < BN; ++c) acc[c] = __ldcg(base + c * 128 + row);
+          for (int s = 1; s < p.splits; ++s) {
+            const float* ps = base + static_cast<size_t>(s) * (BN * 128);
+#pragma unroll
+            for (int c = 0; c < BN; ++c) acc[c] += __ldcg(ps + c * 128 + row);
+          }
+          if (threadIdx.x == 64) p.counters[tile] = 0;
+        }
+        if (row_ok) {
+          if constexpr (EPI == EPI_SILU) {
+#pragma unroll
+            for (int qb = 0; qb < BN / 128; ++qb)
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                store_silu(p, t, f0 / 2 + qb * 64 + h * 32, acc + qb * 128 + h * 32, acc + qb * 128 + 64 + h * 32);
+          } else if constexpr (EPI == EPI_ARGMAX) {
+            float best = -INFINITY;
+            int bi = -1;
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) argmax_scan(p, t, f0 + c * 32, acc + c * 32, best, bi);
+            p.amax_val[static_cast<size_t>(un.tf) * p.amax_ld + t] = best;
+            p.amax_idx[static_cast<size_t>(un.tf) * p.amax_ld + t] = bi < 0 ? INT_MAX : bi;
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) store_chunk<EPI>(p, t, f0 + c * 32, acc + c * 32);
+          }
+        }
+      }
+    }
+  }
+#undef FULL
+#undef EMPTY
+#undef TFULL
+#undef TEMPTY
+#undef DRAIN
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2D bf16 row-major tensor [rows, cols] (row stride ld elements), box 64 x box_rows, 128 B swizzle.
+static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static inline int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
+  GemmPlan pl{};
+  pl.tiles_t = cdiv(pr.T, 128);
+  const int total_kb = pr.n_seg * (pr.k_seg / 64);
+  // tile width: wide tiles while there are enough of them to fill the GPU
+  int BN;
+  if (pr.epi == EPI_ARGMAX) {
+    BN = 64;  // weight streaming: small units balance the HBM-bound LM head
+  } else if (pr.epi == EPI_SILU) {
+    BN = (pl.tiles_t * cdiv(pr.N, 256) >= num_sms) ? 256 : 128;
+  } else if (pr.n_seg == 1 && pl.tiles_t * cdiv(pr.N, 256) >= num_sms) {
+    BN = 256;
+  } else if (pl.tiles_t * cdiv(pr.N, 128) >= num_sms / 2) {
+    BN = 128;
+  } else {
+    BN = 64;
+  }
+  pl.BN = BN;
+  pl.tiles_f = cdiv(pr.N, BN);
+  const int tiles = pl.tiles_t * pl.tiles_f;
+  int splits = 1;
+  if (pr.epi != EPI_ARGMAX && tiles < num_sms) {
+    splits = num_sms / tiles;
+    if (splits > total_kb / 2) splits = total_kb / 2;
+    if (splits < 1) splits = 1;
+  }
+  pl.splits = splits;
+  pl.acc = (pr.n_seg > 1) || (splits > 1);
+  if (pl.acc && BN > 128) {  // running sums need BN <= 128
+    pl.BN = 128;
+    pl.tiles_f = cdiv(pr.N, 128);
+  }
+  const int units = pl.tiles_t * pl.tiles_f * pl.splits;
+  pl.grid = units < num_sms ? units : num_sms;
+  pl.partial_floats = pl.splits > 1 ? static_cast<size_t>(pl.tiles_t) * pl.tiles_f * pl.splits * pl.BN * 128 : 0;
+  return pl;
+}
+
+int gemm_num_tiles_f(const GemmProblem& pr, const GemmPlan& plan) { return plan.tiles_f; }
+
+template <int BN, int EPI, bool ACC>
+static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, const GemmParams& gp, int grid,
+                                  cudaStream_t s) {
+  auto kern = gemm_tc_kernel<BN, EPI, ACC>;
+  constexpr int smem = GemmCfg<BN>::SMEM;
+  static bool attr_done = false;  // per instantiation
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  kern<<<grid, 192, smem, s>>>(mx, mw, gp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partials, int* counters, int* status,
+                        cudaStream_t stream) {
+  if (pr.T <= 0) return cudaSuccess;
+  if (pr.k_seg % 64 || pr.ldo % 8) return cudaErrorInvalidValue;
+  CUtensorMap mx, mw;
+  if (!make_map(&mx, pr.x, pr.x_rows, pr.x_cols, pr.x_ld, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&mw, pr.w, pr.w_rows, pr.w_cols, pr.w_ld, pl.BN)) return cudaErrorInvalidValue;
+  GemmParams gp{};
+  gp.T = pr.T;
+  gp.n_seg = pr.n_seg;
+  gp.kb_seg = pr.k_seg / 64;
+  gp.x_k_seg = pr.x_k_seg;
+  gp.w_row_seg = pr.w_row_seg;
+  gp.tiles_t = pl.tiles_t;
+  gp.tiles_f = pl.tiles_f;
+  gp.splits = pl.splits;
+  gp.total_kb = pr.n_seg * gp.kb_seg;
+  gp.out = pr.out;
+  gp.ldo = pr.ldo;
+  gp.out_cols = pr.out_cols;
+  gp.partials = partials;
+  gp.counters = counters;
+  gp.amax_val = pr.amax_val;
+  gp.amax_idx = pr.amax_idx;
+  gp.amax_ld = pr.amax_ld;
+  gp.logits = pr.logits;
+  gp.ld_logits = pr.ld_logits;
+  gp.vocab = pr.vocab;
+  gp.status = status;
+  const int g = pl.grid;
+#define TP_V(BN_, EPI_, ACC_) \
+  if (pl.BN == BN_ && pr.epi == EPI_ && pl.acc == ACC_) return launch_variant<BN_, EPI_, ACC_>(mx, mw, gp, g, stream);
+  TP_V(256, EPI_STORE, false)
+  TP_V(128, EPI_STORE, false)
+  TP_V(64, EPI_STORE, false)
+  TP_V(128, EPI_STORE, true)
+  TP_V(64, EPI_STORE, true)
+  TP_V(256, EPI_SILU, false)
+  TP_V(128, EPI_SILU, false)
+  TP_V(128, EPI_SILU, true)
+  TP_V(256, EPI_RESID, false)
+  TP_V(128, EPI_RESID, false)
+  TP_V(64, EPI_RESID, false)
+  TP_V(128, EPI_RESID, true)
+  TP_V(64, EPI_RESID, true)
+  TP_V(64, EPI_ARGMAX, false)
+#undef TP_V
+  return cudaErrorNotSupported;
+}
+
+}  // namespace tpk

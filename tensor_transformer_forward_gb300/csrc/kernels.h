@@ -1,0 +1,104 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+// Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace tpk {
+
+// ---------------- GEMM (tcgen05) ----------------
+enum GemmEpi : int { EPI_STORE = 0, EPI_SILU = 1, EPI_RESID = 2, EPI_ARGMAX = 3 };
+
+// Y[t, f] = sum over rank segments r of X[t, r*x_k_seg : +K_seg] . W[r*w_row_seg + f, 0 : K_seg]
+// X: [T, x_cols] bf16 row-major; W: [w_rows, K_seg] bf16 row-major ([out, in]).
+struct GemmProblem {
+  const void* x;
+  int64_t x_rows, x_cols, x_ld;   // elements
+  const void* w;
+  int64_t w_rows, w_cols, w_ld;
+  int T;            // valid token rows
+  int N;            // output features computed per segment (tile space, before SiLU folding)
+  int n_seg;        // rank segments along K (1 = column-parallel)
+  int k_seg;        // K per segment (multiple of 64)
+  int x_k_seg;      // X column offset between segments
+  int w_row_seg;    // W row offset between segments
+  int epi;          // GemmEpi
+  void* out;        // bf16 [T, ldo]
+  int ldo;
+  int out_cols;     // valid output columns
+  // argmax epilogue
+  float* amax_val;  // [tiles_f, amax_ld]
+  int* amax_idx;
+  int amax_ld;
+  float* logits;    // optional fp32 [T, ld_logits]
+  int ld_logits;
+  int vocab;        // features >= vocab are masked out of the argmax
+};
+
+struct GemmPlan {
+  int BN;
+  bool acc;         // running sum in registers (multi-segment or split-K)
+  int tiles_t, tiles_f, splits;
+  int grid;
+  size_t partial_floats;  // workspace floats for split-K partials
+};
+
+GemmPlan plan_gemm(const GemmProblem& pr, int num_sms);
+// workspace: partials (fp32) and per-tile counters (int, zeroed once, self-resetting)
+cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& plan, float* partials, int* counters,
+                        int* status, cudaStream_t stream);
+int gemm_num_tiles_f(const GemmProblem& pr, const GemmPlan& plan);
+
+// ---------------- small kernels ----------------
+cudaError_t launch_embed(const int32_t* ids, int T, const void* embed_stacked, int n, int64_t v_local,
+                         int64_t vocab, int H, void* out, int* status, cudaStream_t s);
+cudaError_t launch_rmsnorm(const void* x, int64_t rows, int H, const void* w, float eps, void* out,
+                           const int32_t* row_index, cudaStream_t s);
+struct RopeArgs {
+  void* qkv;                 // [T, n * w_rank] bf16, q rewritten in place
+  int T, n, nq_l, nkv_l, hd, w_rank;
+  const void* q_norm;        // [hd] bf16
+  const void* k_norm;
+  float eps;
+  const float2* rope;        // [max_pos, hd/2] (cos, sin)
+  int max_pos;
+  const int32_t* cu_q;       // [B+1]
+  const int32_t* ctx_len;    // [B]
+  const int32_t* slot;       // [B]
+  int B;
+  void* kv;                  // cache [n][2][max_seqs][nkv_l][cap][hd]
+  int max_seqs, cap;
+  int* status;
+};
+cudaError_t launch_qk_norm_rope(const RopeArgs& a, cudaStream_t s);
+
+struct AttnArgs {
+  const void* qkv;           // [T, n * w_rank] (q post-RoPE)
+  int n, nq_l, nkv_l, hd, w_rank;
+  const void* kv;            // cache [n][2][max_seqs][nkv_l][cap][hd]
+  int max_seqs, cap;
+  const int32_t* cu_q;
+  const int32_t* ctx_len;
+  const int32_t* slot;
+  int seq_begin, seq_end;    // sequences handled by this launch
+  int max_q_len, max_kv_len;
+  void* out;                 // [T, n * nq_l * hd]
+  float scale_log2;          // log2(e) / sqrt(hd)
+  float* part;               // split-KV partials (decode)
+  int* counters;
+  int splits;
+  int* status;
+};
+cudaError_t launch_attention_prefill(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s);
+int decode_splits(int max_kv_len, int num_units, int num_sms);
+
+cudaError_t launch_final_norm_select(const void* hidden, int H, const int32_t* cu_q, int B, const void* w,
+                                     float eps, void* out, int32_t* idx_scratch, cudaStream_t s);
+cudaError_t launch_argmax_reduce(const float* val, const int* idx, int tiles, int ld, int B, int32_t* out,
+                                 cudaStream_t s);
+cudaError_t launch_wait_probe(const int* flag, int* status, long long limit_ns, cudaStream_t s);
+
+}  // namespace tpk

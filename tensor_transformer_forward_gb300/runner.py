@@ -1,0 +1,100 @@
+"""A whole step through the C ABI: vocab-parallel embedding (or given hidden
+states), the decoder layers, and the vocab-parallel LM head with argmax.
+
+The runner owns (as torch device buffers) every rank's weight shards, one KV
+cache per layer, the workspace and the device status word; each method is one
+or a few C-ABI calls on the current stream.
+"""
+
+from __future__ import annotations
+
+from typing import Dict, List, Optional, Sequence
+
+import torch
+
+from .binding import (WEIGHTS_HEAD, WEIGHTS_LAYER, Batch, Context, ModelConfig, TP_OK, TPError,
+                      tp_decoder_layer_forward, tp_embed_vocab_parallel, tp_lm_head_argmax, tp_read_status,
+                      tp_shard_weights)
+
+
+class TPRunner:
+    def __init__(self, cfg: ModelConfig, num_layers: int, max_seqs: int, capacity: int, max_tokens: int):
+        self.cfg = cfg
+        self.ctx = Context(cfg)
+        self.num_layers = num_layers
+        self.max_seqs = max_seqs
+        self.capacity = capacity
+        self.max_tokens = max_tokens
+        self.layer_shards: List[Optional[torch.Tensor]] = [None] * num_layers
+        self.head_shards: Optional[torch.Tensor] = None
+        self.kv: List[torch.Tensor] = [self.ctx.alloc_kv_cache(max_seqs, capacity) for _ in range(num_layers)]
+        self.workspace = self.ctx.init_workspace(max_tokens, max(max_seqs, 1), capacity)
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        n = cfg.tp_size
+        self.nkv_l = cfg.num_kv_heads // n if cfg.num_kv_heads >= n else 1
+
+    # ---- weights ----
+    def load_layer(self, layer: int, full: Dict[str, torch.Tensor]) -> None:
+        dst = self.ctx.alloc_layer_shards()
+        tp_shard_weights(self.ctx, dst, layer=full)
+        self.layer_shards[layer] = dst
+
+    def load_head(self, full: Dict[str, torch.Tensor]) -> None:
+        dst = self.ctx.alloc_head_shards()
+        tp_shard_weights(self.ctx, dst, head=full)
+        self.head_shards = dst
+
+    def kv_head_map(self) -> List[int]:
+        """Global kv head stored at each (rank, local head) of the caches."""
+        hd = self.cfg.head_dim
+        out = []
+        for r in range(self.cfg.tp_size):
+            _, rows = self.ctx.shard_index_map("k", r)
+            out.extend(rows[j * hd] // hd for j in range(len(rows) // hd))
+        return out
+
+    def kv_view(self, layer: int) -> torch.Tensor:
+        """[n, 2, max_seqs, nkv_l, capacity, hd] bf16 view of a layer cache."""
+        c = self.cfg
+        return self.kv[layer].view(torch.bfloat16).view(c.tp_size, 2, self.max_seqs, self.nkv_l, self.capacity,
+                                                        c.head_dim)
+
+    # ---- one step ----
+    def make_batch(self, q_lens: Sequence[int], ctx_lens: Sequence[int], slots: Optional[Sequence[int]] = None,
+                   num_prefill: Optional[int] = None) -> Batch:
+        if slots is None:
+            slots = list(range(len(q_lens)))
+        if num_prefill is None:
+            num_prefill = sum(1 for q in q_lens if q > 1)
+        return Batch(q_lens, ctx_lens, slots, num_prefill)
+
+    def embed(self, ids: torch.Tensor, hidden_out: torch.Tensor) -> None:
+        tp_embed_vocab_parallel(self.ctx, self.head_shards, ids, hidden_out, self.status)
+
+    def layer(self, layer: int, batch: Batch, hidden: torch.Tensor) -> None:
+        tp_decoder_layer_forward(self.ctx, self.layer_shards[layer], batch, hidden, self.kv[layer], self.max_seqs,
+                                 self.capacity, self.status)
+
+    def head(self, batch: Batch, hidden: torch.Tensor, out_ids: torch.Tensor,
+             out_logits: Optional[torch.Tensor] = None) -> None:
+        tp_lm_head_argmax(self.ctx, self.head_shards, batch, hidden, out_ids, self.status, out_logits)
+
+    def step(self, batch: Batch, ids: Optional[torch.Tensor] = None, hidden: Optional[torch.Tensor] = None,
+             out_ids: Optional[torch.Tensor] = None, out_logits: Optional[torch.Tensor] = None,
+             layers: Optional[int] = None, run_head: bool = True) -> torch.Tensor:
+        """Embedding (when ids are given) -> layers -> head; returns hidden [T, H]."""
+        if hidden is None:
+            hidden = torch.empty(batch.num_tokens, self.cfg.hidden, dtype=torch.bfloat16, device="cuda")
+            self.embed(ids, hidden)
+        elif ids is not None:
+            self.embed(ids, hidden)
+        for li in range(self.num_layers if layers is None else layers):
+            self.layer(li, batch, hidden)
+        if run_head:
+            self.head(batch, hidden, out_ids, out_logits)
+        return hidden
+
+    def check_status(self) -> None:
+        st = tp_read_status(self.status)
+        if st != TP_OK:
+            raise TPError(st, "device status")

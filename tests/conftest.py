@@ -11,3 +11,11 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built extension")
     config.addinivalue_line("markers", "slow: takes more than a few seconds on the CPU")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _built_libraries():
+    """Build the native libraries in-tree (no-op when up to date)."""
+    from tensor_transformer_forward_gb300 import _build
+    _build.build()
+    yield

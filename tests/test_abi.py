@@ -1,0 +1,106 @@
+"""The C-ABI library without a GPU: it loads, exports every declared entry
+point, validates shard rules, and its host index maps equal the oracle's."""
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import forward as of
+from oracle import inputs as oi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "tpfwd.h")).read()
+    return sorted(set(re.findall(r"^(?:tp_status|const char\*)\s+(tp_\w+)\s*\(", text, re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    from tensor_transformer_forward_gb300 import binding
+    lib = binding.lib()
+    names = _declared()
+    assert len(names) >= 17
+    for name in names:
+        assert hasattr(lib, name), name
+    assert sorted(binding.EXPORTED) == names
+
+
+def _cfg(s: synth.ModelShape, n: int):
+    from tensor_transformer_forward_gb300 import ModelConfig
+    return ModelConfig(s.hidden, s.num_q_heads, s.num_kv_heads, s.head_dim, s.intermediate, s.vocab, s.num_layers,
+                       s.rms_eps, s.rope_theta, n, s.tie_word_embeddings)
+
+
+CASES = [(synth.TINY, 2), (synth.QWEN3_06B, 1), (synth.QWEN3_06B, 2), (synth.QWEN3_06B, 4),
+         (synth.QWEN3_06B, 8), (synth.QWEN3_32B, 16), (synth.QWEN3_32B, 8),
+         (synth.ModelShape(hidden=128, num_q_heads=8, num_kv_heads=2, head_dim=64, intermediate=96, vocab=1000,
+                           num_layers=1), 4)]
+
+
+@pytest.mark.parametrize("s,n", CASES)
+def test_index_maps_match_oracle_bit_exactly(s, n):
+    from tensor_transformer_forward_gb300 import Context
+    ctx = Context(_cfg(s, n))
+    shape = oi.shape_of(s)
+    for r in range(n):
+        for kind in ("q", "k", "v", "o", "gate", "up", "down", "embed", "lm_head"):
+            dim, idx = ctx.shard_index_map(kind, r)
+            odim, oidx = of.shard_index(kind, shape, n, r)
+            assert dim == odim and np.array_equal(np.asarray(idx, dtype=np.int64), oidx), (kind, r)
+
+
+def test_uneven_vocab_slices_and_replicated_heads():
+    from tensor_transformer_forward_gb300 import Context
+    s = synth.ModelShape(hidden=128, num_q_heads=8, num_kv_heads=2, head_dim=64, intermediate=96, vocab=1000,
+                         num_layers=1)
+    ctx = Context(_cfg(s, 3 if False else 4))
+    lens = [len(ctx.shard_index_map("embed", r)[1]) for r in range(4)]
+    assert lens == [250, 250, 250, 250]
+    s3 = synth.ModelShape(hidden=128, num_q_heads=6, num_kv_heads=3, head_dim=64, intermediate=96, vocab=1000,
+                          num_layers=1)
+    ctx3 = Context(_cfg(s3, 3))
+    assert [len(ctx3.shard_index_map("embed", r)[1]) for r in range(3)] == [334, 334, 332]
+    heads = [ctx.shard_index_map("k", r)[1][0] // 64 for r in range(4)]
+    assert heads == [0, 0, 1, 1]
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_q_heads=28, num_kv_heads=4), "TP_ERR_HEADS_NOT_DIVISIBLE"),
+    (dict(num_q_heads=24, num_kv_heads=12), "TP_ERR_KV_HEADS"),
+    (dict(num_q_heads=16, num_kv_heads=2, intermediate=100), "TP_ERR_INTERMEDIATE"),
+    (dict(vocab=13), "TP_ERR_VOCAB"),
+    (dict(head_dim=96), "TP_ERR_UNSUPPORTED"),
+])
+def test_create_rejects_what_the_pages_rule_out(kw, code):
+    import tensor_transformer_forward_gb300 as tpf
+    base = dict(hidden=256, num_q_heads=16, num_kv_heads=8, head_dim=64, intermediate=256, vocab=1000, num_layers=1)
+    base.update(kw)
+    s = synth.ModelShape(**base)
+    with pytest.raises(tpf.TPError) as e:
+        tpf.Context(_cfg(s, 8))
+    assert e.value.status == getattr(tpf, code)
+    # the oracle rejects the same shards (kernel coverage aside)
+    if code != "TP_ERR_UNSUPPORTED":
+        with pytest.raises(of.ShardError):
+            of.validate_tp(oi.shape_of(s), 8)
+
+
+def test_layout_sizes():
+    from tensor_transformer_forward_gb300 import WEIGHTS_HEAD, WEIGHTS_LAYER, Context
+    s, n = synth.QWEN3_32B, 16
+    ctx = Context(_cfg(s, n))
+    H, hd = s.hidden, s.head_dim
+    off, nb = ctx.weights_part("qkv")
+    assert nb == n * (4 + 2) * hd * H * 2          # 4 q heads + replicated k and v head per rank
+    assert ctx.weights_part("gate_up")[1] == n * 2 * 1600 * H * 2
+    assert ctx.weights_part("down")[1] == n * H * 1600 * 2
+    assert ctx.weights_part("lm_head")[0] != ctx.weights_part("embed")[0]  # untied
+    assert ctx.weights_bytes(WEIGHTS_LAYER) >= sum(ctx.weights_part(p)[1] for p in ("qkv", "o", "gate_up", "down"))
+    assert ctx.kv_cache_bytes(32, 2112) == n * 2 * 32 * 1 * 2112 * hd * 2
+    t = Context(_cfg(synth.QWEN3_06B, 2))
+    assert t.weights_part("lm_head")[0] == t.weights_part("embed")[0]       # tied
+    assert t.rank_sum_count() == 0

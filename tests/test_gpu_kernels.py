@@ -1,0 +1,172 @@
+"""GPU tests of the individual steps through the C ABI: generator parity,
+shard (A1) and embedding (A2) bit-exactness, the bounded wait, and the
+per-kernel intermediates of one layer against the oracle's trace."""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+import synth.device as sd
+from oracle import forward as of
+from oracle import inputs as oi
+from tests.gpu_harness import GpuStep, assert_close, model_config, oracle_layer
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def test_device_generator_matches_host_bit_for_bit():
+    t = torch.empty(100003, dtype=torch.bfloat16, device="cuda")
+    sd.fill_normal(t, 0, 77, 0.02)
+    assert np.array_equal(_bits(t), synth.normal_bf16_bits(0, 77, 100003, 0.02))
+    sd.fill_normal(t, 0, 78, 0.1, mean=1.0, start=12345)
+    assert np.array_equal(_bits(t), synth.normal_bf16_bits(0, 78, 100003, 0.1, mean=1.0, start=12345))
+    ids = sd.token_ids(5000, 151936)
+    assert np.array_equal(ids.cpu().numpy().astype(np.int64), synth.token_ids(synth.SEED_TOKENS, 0, 5000, 151936))
+    # KV cache fill: rank-local layout with an arbitrary head map
+    n, seqs, nkv_l, cap, hd, nkv = 2, 3, 2, 40, 64, 4
+    cache = torch.zeros(n * 2 * seqs * nkv_l * cap * hd, dtype=torch.bfloat16, device="cuda")
+    hmap = [3, 1, 0, 2]
+    sd.fill_kv_cache(cache, n, seqs, nkv_l, cap, hd, hmap, nkv, layer=5, num_slots=seqs, fill_len=33)
+    view = cache.view(n, 2, seqs, nkv_l, cap, hd)
+    for r in range(n):
+        for kv in range(2):
+            for b in range(seqs):
+                for j in range(nkv_l):
+                    ref = synth.kv_cache_bits(5, b, kv, hmap[r * nkv_l + j], 33, nkv, hd)
+                    assert np.array_equal(_bits(view[r, kv, b, j, :33]), ref)
+
+
+SHARD_CASES = [(synth.TINY, 2), (synth.TINY, 4),
+               (synth.ModelShape(hidden=256, num_q_heads=8, num_kv_heads=2, head_dim=128, intermediate=160,
+                                 vocab=1001, num_layers=1, tie_word_embeddings=False), 4),
+               (synth.QWEN3_06B, 2)]
+
+
+@pytest.mark.parametrize("s,n", SHARD_CASES)
+def test_shard_weights_bit_exact(s, n):
+    """A1 on the device equals the oracle's own shard-then-merge, bit for bit."""
+    from tensor_transformer_forward_gb300 import Context, tp_shard_weights
+    ctx = Context(model_config(s, n))
+    full = sd.layer_weights(s, 0, perturbed_norms=True)
+    dst = ctx.alloc_layer_shards()
+    tp_shard_weights(ctx, dst, layer=full)
+    hfull = sd.head_weights(s)
+    hdst = ctx.alloc_head_shards()
+    tp_shard_weights(ctx, hdst, head=hfull)
+    torch.cuda.synchronize()
+    w = oi.layer_weights(s, 0, perturbed_norms=True, dtype=torch.float32)
+    shape = oi.shape_of(s)
+    H, hd = s.hidden, s.head_dim
+    nq_l = s.num_q_heads // n
+    nkv_l = s.num_kv_heads // n if s.num_kv_heads >= n else 1
+    i_l = s.intermediate // n
+    i_p = (i_l + 63) // 64 * 64
+    wr = (nq_l + 2 * nkv_l) * hd
+    qkv = ctx.part_view(dst, "qkv", (n, wr, H)).float().cpu()
+    o = ctx.part_view(dst, "o", (n, H, nq_l * hd)).float().cpu()
+    gu = ctx.part_view(dst, "gate_up", (n, i_p // 64, 2, 64, H)).float().cpu()
+    down = ctx.part_view(dst, "down", (n, H, i_p)).float().cpu()
+    for r in range(n):
+        rl = of.shard_layer(w, shape, n, r)
+        assert torch.equal(qkv[r], rl.qkv)
+        assert torch.equal(o[r], rl.o)
+        g = gu[r, :, 0].reshape(i_p, H)
+        u = gu[r, :, 1].reshape(i_p, H)
+        assert torch.equal(g[:i_l], rl.gate_up[:i_l]) and torch.equal(u[:i_l], rl.gate_up[i_l:])
+        assert torch.count_nonzero(g[i_l:]) == 0 and torch.count_nonzero(u[i_l:]) == 0
+        assert torch.equal(down[r][:, :i_l], rl.down) and torch.count_nonzero(down[r][:, i_l:]) == 0
+    for name, ref in (("in_norm", w.in_norm), ("post_norm", w.post_norm), ("q_norm", w.q_norm), ("k_norm", w.k_norm)):
+        assert torch.equal(ctx.part_view(dst, name, (ref.numel(),)).float().cpu(), ref)
+    hw = oi.head_weights(s, dtype=torch.float32)
+    v_l = -(-s.vocab // n)
+    emb = ctx.part_view(hdst, "embed", (n, v_l, H)).float().cpu()
+    lm = ctx.part_view(hdst, "lm_head", (n, v_l, H)).float().cpu()
+    for r in range(n):
+        a, b = of.vocab_range(s.vocab, n, r)
+        assert torch.equal(emb[r, : b - a], hw.embed[a:b]) and torch.count_nonzero(emb[r, b - a:]) == 0
+        assert torch.equal(lm[r, : b - a], hw.lm_head[a:b])
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4])
+def test_embedding_bit_exact_and_bad_ids(n):
+    """A2: the rank-masked lookups summed over ranks equal the table rows exactly;
+    an id outside the vocab gives a zero row and the BAD_TOKEN status."""
+    from tensor_transformer_forward_gb300 import TP_ERR_BAD_TOKEN, TP_OK, Context, tp_embed_vocab_parallel, \
+        tp_read_status, tp_shard_weights
+    s = synth.ModelShape(hidden=128, num_q_heads=12, num_kv_heads=12, head_dim=64, intermediate=96, vocab=1000,
+                         num_layers=1)
+    ctx = Context(model_config(s, n))
+    hdst = ctx.alloc_head_shards()
+    tp_shard_weights(ctx, hdst, head=sd.head_weights(s))
+    ids_h = [0, 1, 333, 334, 335, 499, 500, 666, 667, 668, 999] + list(synth.token_ids(3, 9, 50, 1000))
+    ids = torch.tensor(ids_h, dtype=torch.int32, device="cuda")
+    out = torch.empty(len(ids_h), s.hidden, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tp_embed_vocab_parallel(ctx, hdst, ids, out, status)
+    assert tp_read_status(status) == TP_OK
+    ref = synth.global_weight_bits(s, synth.W_EMBED)[np.asarray(ids_h)]
+    assert np.array_equal(_bits(out), ref)
+    bad = torch.tensor([5, -1, 1000, 7], dtype=torch.int32, device="cuda")
+    out2 = torch.empty(4, s.hidden, dtype=torch.bfloat16, device="cuda")
+    tp_embed_vocab_parallel(ctx, hdst, bad, out2, status)
+    assert tp_read_status(status) == TP_ERR_BAD_TOKEN
+    assert torch.count_nonzero(out2[1:3]) == 0
+    assert np.array_equal(_bits(out2[0]), synth.global_weight_bits(s, synth.W_EMBED)[5])
+
+
+def test_bounded_wait_times_out_without_hanging():
+    from tensor_transformer_forward_gb300 import TP_ERR_TIMEOUT, TP_OK, tp_debug_wait_probe, tp_read_status
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    tp_debug_wait_probe(flag, status, 20_000_000)  # 20 ms
+    t1.record()
+    assert tp_read_status(status) == TP_ERR_TIMEOUT
+    assert 15.0 < t0.elapsed_time(t1) < 2000.0
+    flag.fill_(1)
+    status.zero_()
+    tp_debug_wait_probe(flag, status, 20_000_000)
+    assert tp_read_status(status) == TP_OK
+
+
+@pytest.mark.parametrize("n", [1, 2])
+def test_layer_intermediates_match_oracle_trace(n):
+    """Per kernel (A3-A10) on a 0.6B-shaped layer, 300 prefill tokens (two full
+    128-row tiles and a ragged tail): normed input, merged QKV with post-RoPE q,
+    attention output, SiLU*up, and the layer output."""
+    w = synth.Workload("prefill300", synth.QWEN3_06B, (n,), ((300, 0),), (), 1, False)
+    g = GpuStep(w, n, head=False, perturbed=True)
+    s = w.shape
+    T, H, hd = 300, s.hidden, s.head_dim
+    shape = oi.shape_of(s)
+    x = of.from_bf16_bits(synth.hidden_bits(T, H))
+    trace = {}
+    empty = torch.zeros(s.num_kv_heads, 0, hd, dtype=torch.float64)
+    y, K, V = of.decoder_layer(x, oracle_layer(s, 0, True), shape, empty, empty, trace)
+    ctx = g.runner.ctx
+    nq_l, nkv_l = s.num_q_heads // n, s.num_kv_heads // n
+    wr = (nq_l + 2 * nkv_l) * hd
+    qkv = ctx.workspace_view("qkv", T, n * wr).float().cpu().view(T, n, wr)
+    q_gpu = qkv[:, :, : nq_l * hd].reshape(T, n * nq_l, hd).transpose(0, 1)
+    assert_close(q_gpu, trace["q"], "post-RoPE q")
+    v_gpu = qkv[:, :, (nq_l + nkv_l) * hd:].reshape(T, n * nkv_l, hd).transpose(0, 1)
+    assert_close(v_gpu, trace["v"], "raw v")
+    attn = ctx.workspace_view("attn", T, s.num_q_heads * hd).float().cpu()
+    assert_close(attn, trace["attn"], "attention output")
+    assert_close(ctx.workspace_view("normed", T, H).float().cpu(), trace["h2"], "post-attention RMSNorm")
+    i_l = s.intermediate // n
+    i_p = (i_l + 63) // 64 * 64
+    act = ctx.workspace_view("act", T, n * i_p).float().cpu().view(T, n, i_p)[:, :, :i_l].reshape(T, n * i_l)
+    assert_close(act, trace["act"], "SiLU(gate)*up")
+    assert_close(g.hidden.float().cpu(), y, "layer output")
+    Kg, Vg = g.new_kv(0, 0)
+    assert_close(Kg, K, "cached K")
+    assert_close(Vg, V, "cached V")
+    assert g.runner.ctx.rank_sum_count() == 2

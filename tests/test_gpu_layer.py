@@ -1,0 +1,71 @@
+"""Whole-step parity on the GPU against the fp64 oracle at sizes the oracle
+finishes in seconds: prefill, decode, mixed batches, several layers, the
+vocab head with argmax, every tp size the shapes allow (incl. KV-head
+replication).  Tolerance: max |err| <= 2e-2 x RMS(reference) per tensor;
+greedy ids equal where the reference top-2 margin exceeds 0.05."""
+
+import pytest
+
+import synth
+from tests.gpu_harness import GpuStep, check_step
+
+pytestmark = pytest.mark.gpu
+
+S06 = synth.QWEN3_06B
+
+
+@pytest.mark.parametrize("n", [1, 2, 4])
+def test_tiny_workload_from_ids(n):
+    """The tiny workload: hidden 256, 4 q / 2 kv heads, 8 prefill tokens from ids,
+    one layer and the vocab head (n=4 replicates each kv head on 2 ranks)."""
+    w = synth.WORKLOADS["tiny_prefill8"]
+    g = GpuStep(w, n, perturbed=True)
+    check_step(g, [0])
+    assert g.runner.ctx.rank_sum_count() == 2 * 1 + 1
+
+
+@pytest.mark.parametrize("n", [1, 2, 4])
+def test_decode_varied_context_lengths(n):
+    """Decode: one new token for sequences with 0 .. 2047 cached positions
+    (several key splits, ragged tails), then the LM head."""
+    ctxs = (0, 1, 63, 64, 513, 1000, 2047, 77)
+    w = synth.Workload("decode_var", S06, (n,), (), ctxs, 1, False)
+    g = GpuStep(w, n)
+    check_step(g, list(range(len(ctxs))))
+
+
+@pytest.mark.parametrize("n", [1, 2])
+def test_prefill_with_cache_offset_and_ragged_lengths(n):
+    """Prefill sequences with cached context (mask tril(S - T)) and lengths that
+    are not multiples of the 64/128 tiles."""
+    w = synth.Workload("prefill_ctx", S06, (n,), ((130, 0), (70, 50), (1, 9), (65, 200)), (), 1, False)
+    g = GpuStep(w, n, perturbed=True)
+    check_step(g, [0, 1, 2, 3])
+
+
+def test_mixed_batch_two_layers_from_ids():
+    """Mixed step: two prefill sequences and five decode sequences, embedding
+    from ids, two layers, the vocab head."""
+    w = synth.Workload("mixed_small", S06, (2,), ((130, 0), (70, 0)), (5, 100, 300, 1, 700), 2, True)
+    g = GpuStep(w, 2)
+    check_step(g, list(range(7)))
+    assert g.runner.ctx.rank_sum_count() == 2 * 2 + 1
+
+
+def test_32b_layer_tp16_replicated_kv():
+    """32B-shaped layer at tp 16: 4 q heads and one replicated kv head per rank;
+    a prefill sequence and decode sequences (layer only: the untied 32B vocab
+    head is checked at the 0.6B shape)."""
+    w = synth.Workload("tp16_small", synth.QWEN3_32B, (16,), ((40, 0),), (33, 200), 1, False)
+    g = GpuStep(w, 16, head=False)
+    check_step(g, [0, 1, 2], head=False)
+
+
+def test_untied_head_uneven_vocab():
+    """Untied LM head with a vocab that leaves the last rank a shorter slice
+    (padded columns must never win the argmax)."""
+    s = synth.ModelShape(hidden=256, num_q_heads=6, num_kv_heads=3, head_dim=64, intermediate=384, vocab=1001,
+                         num_layers=1, tie_word_embeddings=False)
+    w = synth.Workload("untied_uneven", s, (3,), ((17, 0),), (5, 9), 1, True)
+    g = GpuStep(w, 3, perturbed=True)
+    check_step(g, [0, 1, 2])
