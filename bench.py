@@ -251,7 +251,7 @@ def run_ours(args, w: synth.Workload, n: int, rank: int, world: int) -> dict:
     r, batch, ids = build_runner(w, n)
     ctx = r.ctx
     T, H, B = w.num_tokens, w.shape.hidden, w.num_seqs
-    hidden = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    hidden = torch.empty(T, H, dtype=torch.float32, device="cuda")
     out_ids = torch.empty(B, dtype=torch.int32, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
@@ -359,6 +359,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--tp", type=int, default=None)
+    ap.add_argument("--quick", action="store_true",
+                    help="only warm-up + timed steps (no kernel breakdown, e2e or CPU baseline): for profilers")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -374,6 +376,17 @@ def main():
     if world > 1:
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
+    if args.quick:
+        r, batch, ids = build_runner(w, n)
+        hidden = torch.empty(w.num_tokens, w.shape.hidden, dtype=torch.float32, device="cuda")
+        out_ids = torch.empty(w.num_seqs, dtype=torch.int32, device="cuda")
+        for _ in range(args.warmup + args.steps):
+            r.step(batch, ids=ids, hidden=hidden, out_ids=out_ids)
+        torch.cuda.synchronize()
+        r.check_status()
+        print(json.dumps({"quick": True, "workload": w.name, "tp": n, "steps": args.steps,
+                          "launches": r.ctx.launch_count()}), flush=True)
+        return
     line = run_ours(args, w, n, rank, world)
     if rank == 0:
         if world == 1:

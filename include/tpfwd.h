@@ -98,8 +98,12 @@ tp_status tp_shard_index_map(const tp_ctx* ctx, int32_t kind, int32_t rank, int6
  *  TP_PART_IN_NORM, TP_PART_POST_NORM [H]; TP_PART_Q_NORM, TP_PART_K_NORM [hd] (one copy,
  *                                              identical on every rank)
  *  TP_PART_EMBED    [n][V_l][H]               : per rank its vocab rows, zero padded to V_l
- *  TP_PART_LM_HEAD  [n][V_l][H]               : same layout (absent when tied: offset == EMBED's)
+ *  TP_PART_LM_HEAD  [n][V_l][H]               : same layout; the embedding's rows when tied
  *  TP_PART_FINAL_NORM [H]
+ * The projection parts (QKV, O, GATE_UP, DOWN) and the LM head are tensor-core operands and
+ * are stored fp16 (converted from the bf16 inputs: exact for magnitudes in [2^-14, 65504],
+ * smaller ones rounded to fp16's subnormal grid, larger ones saturated); embedding rows and
+ * norm weights stay bf16.
  */
 #define TP_WEIGHTS_LAYER 0
 #define TP_WEIGHTS_HEAD 1
@@ -149,10 +153,11 @@ tp_status tp_workspace_init(tp_ctx* ctx, void* ws, size_t ws_bytes, int32_t max_
 
 /* Intermediates of the last tp_decoder_layer_forward, inside the workspace (for tests and
  * debugging; valid until the next call): byte offset and size of
- *  TP_WS_NORMED  bf16 [T, H]                  RMSNorm output (post-attention norm after the call)
- *  TP_WS_QKV     bf16 [T, n, (nq_l+2nkv_l) hd] merged projection; q heads hold post-RoPE q
- *  TP_WS_ATTN    bf16 [T, n * nq_l * hd]      attention output (o_proj input)
- *  TP_WS_ACT     bf16 [T, n * I_p]            SiLU(gate) * up (down_proj input) */
+ *  TP_WS_NORMED  fp16 [T, H]                  RMSNorm output (post-attention norm after the call)
+ *  TP_WS_QKV     fp16 [T, n, (nq_l+2nkv_l) hd] merged projection; its q heads hold post-RoPE q
+ *                                              (k and v go straight to the cache)
+ *  TP_WS_ATTN    fp16 [T, n * nq_l * hd]      attention output (o_proj input)
+ *  TP_WS_ACT     fp16 [T, n * I_p]            SiLU(gate) * up (down_proj input) */
 #define TP_WS_NORMED 0
 #define TP_WS_QKV 1
 #define TP_WS_ATTN 2
@@ -174,7 +179,8 @@ typedef struct {
 
 /* A2: vocab-parallel embedding ([TP] VocabParallelEmbedding): per rank, ids inside its slice
  * are looked up and the others give 0; the rank outputs are summed (fixed rank order).
- * ids: device int32 [T]; hidden_out: device bf16 [T, H].  Ids outside [0, V) give zero rows
+ * ids: device int32 [T]; hidden_out: device fp32 [T, H] (the residual stream is fp32; GEMM
+ * and attention operands are fp16, the KV cache bf16).  Ids outside [0, V) give zero rows
  * and set TP_ERR_BAD_TOKEN in *dev_status (device int32, sticky, read by tp_read_status). */
 tp_status tp_embed_vocab_parallel(tp_ctx* ctx, const void* head_shards, const int32_t* ids, int32_t num_tokens,
                                   void* hidden_out, int32_t* dev_status, void* stream);
@@ -182,7 +188,8 @@ tp_status tp_embed_vocab_parallel(tp_ctx* ctx, const void* head_shards, const in
 /* A3-A10: one decoder layer under tensor parallelism, all ranks ([TP] TPTransformer.forward loop
  * body, TPAttention, TPMLP): RMSNorm -> merged QKV (column) -> q/k RMSNorm + RoPE + KV write ->
  * per-rank GQA attention -> o_proj (row) + rank-sum + residual -> RMSNorm -> gate/up (column) with
- * SiLU*up -> down (row) + rank-sum + residual.  hidden: device bf16 [T, H], updated in place.
+ * SiLU*up -> down (row) + rank-sum + residual.  hidden: device fp32 [T, H] residual stream,
+ * updated in place.
  * kv_cache: this layer's cache (tp_kv_cache_bytes(kv_max_seqs, kv_capacity)); positions
  * [ctx_len, ctx_len + q_len) of each sequence are written.  Exactly two rank-sums. */
 tp_status tp_decoder_layer_forward(tp_ctx* ctx, const void* layer_shards, const tp_batch* batch, void* hidden,
@@ -192,7 +199,8 @@ tp_status tp_decoder_layer_forward(tp_ctx* ctx, const void* layer_shards, const 
 /* A11-A13: final RMSNorm of each sequence's last token, vocab-parallel logits (all ranks'
  * slices, padded columns masked) with a fused (max, first index) epilogue, and the argmax
  * reduction that replaces the all-gather ([TP] TPTransformer.forward; [CH9] ParallelLMHead).
- * out_ids: device int32 [num_seqs]; out_logits: device fp32 [num_seqs, V] or NULL. */
+ * hidden: device fp32 [T, H].  out_ids: device int32 [num_seqs]; out_logits: device fp32
+ * [num_seqs, V] or NULL. */
 tp_status tp_lm_head_argmax(tp_ctx* ctx, const void* head_shards, const tp_batch* batch, const void* hidden,
                             int32_t* out_ids, float* out_logits, int32_t* dev_status, void* stream);
 
@@ -209,7 +217,7 @@ tp_status tp_rank_sum_count(const tp_ctx* ctx, int64_t* count);
 #define TP_K_EMBED 0
 #define TP_K_RMSNORM 1
 #define TP_K_GEMM_QKV 2
-#define TP_K_ROPE 3
+#define TP_K_ROPE 3 /* q/k norm + RoPE + KV write: fused into TP_K_GEMM_QKV, never launched */
 #define TP_K_ATTN_PREFILL 4
 #define TP_K_ATTN_DECODE 5
 #define TP_K_GEMM_O 6

@@ -247,12 +247,12 @@ class Context:
         return ws
 
     def workspace_view(self, part: str, rows: int, cols: int) -> torch.Tensor:
-        """bf16 [rows, cols] view of an intermediate of the last layer call."""
+        """fp16 [rows, cols] view of an intermediate of the last layer call."""
         o, b = ctypes.c_size_t(), ctypes.c_size_t()
         _check(_lib.tp_workspace_part(self.handle, WS_PART[part], ctypes.byref(o), ctypes.byref(b)),
                "tp_workspace_part")
         assert rows * cols * 2 <= b.value
-        return self.workspace[o.value:o.value + rows * cols * 2].view(torch.bfloat16).view(rows, cols)
+        return self.workspace[o.value:o.value + rows * cols * 2].view(torch.float16).view(rows, cols)
 
     def part_view(self, shards: torch.Tensor, part: str, shape: Sequence[int], dtype=torch.bfloat16) -> torch.Tensor:
         off, nbytes = self.weights_part(part)
@@ -321,7 +321,7 @@ def tp_shard_weights(ctx: Context, dst: torch.Tensor, layer: Optional[Dict[str, 
 def tp_embed_vocab_parallel(ctx: Context, head_shards: torch.Tensor, ids: torch.Tensor, hidden_out: torch.Tensor,
                             status: torch.Tensor) -> None:
     _check(_lib.tp_embed_vocab_parallel(ctx.handle, _dev(head_shards, "head_shards"), _dev(ids, "ids", torch.int32),
-                                        ids.numel(), _dev(hidden_out, "hidden_out", torch.bfloat16),
+                                        ids.numel(), _dev(hidden_out, "hidden_out", torch.float32),
                                         _dev(status, "status", torch.int32), _stream()), "tp_embed_vocab_parallel")
 
 
@@ -329,7 +329,7 @@ def tp_decoder_layer_forward(ctx: Context, layer_shards: torch.Tensor, batch: Ba
                              kv_cache: torch.Tensor, kv_max_seqs: int, kv_capacity: int,
                              status: torch.Tensor) -> None:
     _check(_lib.tp_decoder_layer_forward(ctx.handle, _dev(layer_shards, "layer_shards"), ctypes.byref(batch.c),
-                                         _dev(hidden, "hidden", torch.bfloat16), _dev(kv_cache, "kv_cache"),
+                                         _dev(hidden, "hidden", torch.float32), _dev(kv_cache, "kv_cache"),
                                          kv_max_seqs, kv_capacity, _dev(status, "status", torch.int32), _stream()),
            "tp_decoder_layer_forward")
 
@@ -338,7 +338,7 @@ def tp_lm_head_argmax(ctx: Context, head_shards: torch.Tensor, batch: Batch, hid
                       out_ids: torch.Tensor, status: torch.Tensor, out_logits: Optional[torch.Tensor] = None) -> None:
     lg = _dev(out_logits, "out_logits", torch.float32) if out_logits is not None else None
     _check(_lib.tp_lm_head_argmax(ctx.handle, _dev(head_shards, "head_shards"), ctypes.byref(batch.c),
-                                  _dev(hidden, "hidden", torch.bfloat16), _dev(out_ids, "out_ids", torch.int32), lg,
+                                  _dev(hidden, "hidden", torch.float32), _dev(out_ids, "out_ids", torch.int32), lg,
                                   _dev(status, "status", torch.int32), _stream()), "tp_lm_head_argmax")
 
 

@@ -129,11 +129,7 @@ void lay_out(tp_ctx* x) {
   x->layer_bytes = off;
   off = 0;
   take(x->embed, n * x->v_l * H * 2);
-  if (x->c.tie_word_embeddings) {
-    x->lm_head = x->embed;
-  } else {
-    take(x->lm_head, n * x->v_l * H * 2);
-  }
+  take(x->lm_head, n * x->v_l * H * 2);  // fp16 operand copy, also when tied
   take(x->final_norm, H * 2);
   x->head_bytes = off;
 }
@@ -417,6 +413,11 @@ tp_status tp_shard_weights(tp_ctx* x, const tp_layer_full* L, const tp_head_full
     TP_CUDA(cudaMemcpyAsync(d + x->post_norm.off, L->post_norm, row, cudaMemcpyDeviceToDevice, s));
     TP_CUDA(cudaMemcpyAsync(d + x->q_norm.off, L->q_norm, hd * 2, cudaMemcpyDeviceToDevice, s));
     TP_CUDA(cudaMemcpyAsync(d + x->k_norm.off, L->k_norm, hd * 2, cudaMemcpyDeviceToDevice, s));
+    // the projection shards are tensor-core operands: stored fp16
+    for (const Region* r : {&x->qkv, &x->o, &x->gate_up, &x->down}) {
+      cudaError_t e = tpk::launch_bf16_to_f16(d + r->off, r->bytes / 2, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
     return TP_OK;
   }
   if (!Hd->embed || !Hd->final_norm || (!x->c.tie_word_embeddings && !Hd->lm_head)) return TP_ERR_INVALID_ARG;
@@ -426,12 +427,15 @@ tp_status tp_shard_weights(tp_ctx* x, const tp_layer_full* L, const tp_head_full
     TP_CUDA(cudaMemcpyAsync(d + x->embed.off + static_cast<size_t>(r) * x->v_l * row,
                             static_cast<const char*>(Hd->embed) + a * row, (b - a) * row, cudaMemcpyDeviceToDevice,
                             s));
-    if (!x->c.tie_word_embeddings)
-      TP_CUDA(cudaMemcpyAsync(d + x->lm_head.off + static_cast<size_t>(r) * x->v_l * row,
-                              static_cast<const char*>(Hd->lm_head) + a * row, (b - a) * row,
-                              cudaMemcpyDeviceToDevice, s));
+    const void* lm = x->c.tie_word_embeddings ? Hd->embed : Hd->lm_head;
+    TP_CUDA(cudaMemcpyAsync(d + x->lm_head.off + static_cast<size_t>(r) * x->v_l * row,
+                            static_cast<const char*>(lm) + a * row, (b - a) * row, cudaMemcpyDeviceToDevice, s));
   }
   TP_CUDA(cudaMemcpyAsync(d + x->final_norm.off, Hd->final_norm, row, cudaMemcpyDeviceToDevice, s));
+  {
+    cudaError_t e = tpk::launch_bf16_to_f16(d + x->lm_head.off, x->lm_head.bytes / 2, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   return TP_OK;
 }
 
@@ -522,27 +526,20 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   }
   if (e != cudaSuccess) return cuda_fail(e);
 
-  // A4: merged QKV of all ranks (column split: no exchange)
+  // A4 + A5: merged QKV of all ranks (column split: no exchange), with q/k RMSNorm,
+  // RoPE and the K/V cache write fused into the epilogue (fp32, no intermediate rounding)
   tpk::GemmProblem g{};
   g.x = xn; g.x_rows = T; g.x_cols = H; g.x_ld = H;
   g.w = w + x->qkv.off; g.w_rows = static_cast<int64_t>(n) * x->w_rank; g.w_cols = H; g.w_ld = H;
   g.T = T; g.N = n * x->w_rank; g.n_seg = 1; g.k_seg = H; g.x_k_seg = 0; g.w_row_seg = 0;
-  g.epi = tpk::EPI_STORE; g.out = qkv; g.ldo = n * x->w_rank; g.out_cols = n * x->w_rank;
+  g.epi = tpk::EPI_QKV; g.out = qkv; g.ldo = n * x->w_rank; g.out_cols = n * x->w_rank;
+  g.qkv.n = n; g.qkv.nq_l = x->nq_l; g.qkv.nkv_l = x->nkv_l; g.qkv.hd = x->hd; g.qkv.w_rank = x->w_rank;
+  g.qkv.q_norm = w + x->q_norm.off; g.qkv.k_norm = w + x->k_norm.off; g.qkv.eps = x->c.rms_eps;
+  g.qkv.rope = reinterpret_cast<const float2*>(x->ws + x->r_rope.off); g.qkv.max_pos = x->ws_pos;
+  g.qkv.cu_q = b->cu_q; g.qkv.ctx_len = b->ctx_len; g.qkv.slot = b->slot; g.qkv.B = b->num_seqs;
+  g.qkv.kv = kv; g.qkv.max_seqs = kv_max_seqs; g.qkv.cap = kv_cap;
   st = gemm(x, TP_K_GEMM_QKV, g, dev_status, s);
   if (st != TP_OK) return st;
-
-  // A5: q/k RMSNorm + RoPE + KV write
-  tpk::RopeArgs ra{};
-  ra.qkv = qkv; ra.T = T; ra.n = n; ra.nq_l = x->nq_l; ra.nkv_l = x->nkv_l; ra.hd = x->hd; ra.w_rank = x->w_rank;
-  ra.q_norm = w + x->q_norm.off; ra.k_norm = w + x->k_norm.off; ra.eps = x->c.rms_eps;
-  ra.rope = reinterpret_cast<const float2*>(x->ws + x->r_rope.off); ra.max_pos = x->ws_pos;
-  ra.cu_q = b->cu_q; ra.ctx_len = b->ctx_len; ra.slot = b->slot; ra.B = b->num_seqs;
-  ra.kv = kv; ra.max_seqs = kv_max_seqs; ra.cap = kv_cap; ra.status = dev_status;
-  {
-    Timed tm(x, TP_K_ROPE, s);
-    e = tpk::launch_qk_norm_rope(ra, s);
-  }
-  if (e != cudaSuccess) return cuda_fail(e);
 
   // A6: per-rank attention
   tpk::AttnArgs aa{};
@@ -636,15 +633,17 @@ tp_status tp_lm_head_argmax(tp_ctx* x, const void* head_shards, const tp_batch* 
   g.epi = tpk::EPI_ARGMAX; g.out = nullptr; g.ldo = 8; g.out_cols = 0;
   g.amax_val = reinterpret_cast<float*>(x->ws + x->r_amax_v.off);
   g.amax_idx = reinterpret_cast<int*>(x->ws + x->r_amax_i.off);
-  g.amax_ld = B; g.logits = out_logits; g.ld_logits = x->c.vocab; g.vocab = x->c.vocab;
+  g.amax_ld = B; g.logits = out_logits; g.ld_logits = x->c.vocab; g.vocab = x->c.vocab; g.out_ids = out_ids;
   tpk::GemmPlan pl = tpk::plan_gemm(g, x->num_sms);
-  if (pl.tiles_f > x->lm_tiles_max || pl.splits != 1) return TP_ERR_UNSUPPORTED;
+  if (pl.tiles_f > x->lm_tiles_max || pl.splits != 1 || (pl.swap && pl.grid > x->lm_tiles_max)) return TP_ERR_UNSUPPORTED;
   {
+    // few sequences: weights stream through the M side and the argmax over all
+    // ranks' vocab slices finishes inside the kernel (last CTA to arrive)
     Timed tm(x, TP_K_GEMM_LM_HEAD, s);
-    e = tpk::launch_gemm(g, pl, nullptr, nullptr, dev_status, s);
+    e = tpk::launch_gemm(g, pl, nullptr, at<int>(x->ws, x->r_gcnt), dev_status, s);
   }
   if (e != cudaSuccess) return cuda_fail(e);
-  {
+  if (!pl.swap) {
     Timed tm(x, TP_K_ARGMAX, s);
     e = tpk::launch_argmax_reduce(g.amax_val, g.amax_idx, pl.tiles_f, B, B, out_ids, s);
   }

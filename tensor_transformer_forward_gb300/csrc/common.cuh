@@ -1,7 +1,8 @@
-// Shared device helpers: status flags, bounded waits, bf16 conversion.
+// Shared device helpers: status flags, bounded waits, bf16 / fp16 conversion.
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -34,6 +35,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
 }
+
+#define TP_F16_MAX 65504.0f
+
+// fp16 operands (GEMM/attention inputs): saturate to the finite fp16 range.
+__device__ __forceinline__ float sat_f16(float x) { return fabsf(x) > TP_F16_MAX ? copysignf(TP_F16_MAX, x) : x; }
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  lo = sat_f16(lo);  // NaN passes through
+  hi = sat_f16(hi);
+  __half2 p = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+__device__ __forceinline__ float f16lo(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu))); }
+__device__ __forceinline__ float f16hi(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

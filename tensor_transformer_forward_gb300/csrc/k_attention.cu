@@ -6,8 +6,8 @@
 // tokens sees keys 0 .. ctx + j.  Softmax in fp32 (base-2, max-subtracted).
 //
 // Cache layout (per layer): [n][2 (K, V)][max_seqs][nkv_l][cap][hd] bf16.
-// Output layout: [T][n * nq_l * hd] bf16 (rank-major heads, the row-split
-// o_proj input).
+// q comes from the merged QKV buffer (fp16).  Output layout: [T][n * nq_l * hd]
+// fp16 (rank-major heads, the row-split o_proj operand).
 #include <climits>
 
 #include "kernels.h"
@@ -51,13 +51,13 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
 
   // this lane's 8 dims of each query head, pre-scaled into the exp2 domain
   float q[G][8];
-  const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(a.qkv) + static_cast<size_t>(t) * a.n * a.w_rank +
-                              static_cast<size_t>(r) * a.w_rank;
+  const __half* qrow = reinterpret_cast<const __half*>(a.qkv) + static_cast<size_t>(t) * a.n * a.w_rank +
+                       static_cast<size_t>(r) * a.w_rank;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     const uint4 u = *reinterpret_cast<const uint4*>(qrow + (g * G + h) * HD + dc * 8);
-    q[h][0] = bf16lo(u.x); q[h][1] = bf16hi(u.x); q[h][2] = bf16lo(u.y); q[h][3] = bf16hi(u.y);
-    q[h][4] = bf16lo(u.z); q[h][5] = bf16hi(u.z); q[h][6] = bf16lo(u.w); q[h][7] = bf16hi(u.w);
+    q[h][0] = f16lo(u.x); q[h][1] = f16hi(u.x); q[h][2] = f16lo(u.y); q[h][3] = f16hi(u.y);
+    q[h][4] = f16lo(u.z); q[h][5] = f16hi(u.z); q[h][6] = f16lo(u.w); q[h][7] = f16hi(u.w);
 #pragma unroll
     for (int i = 0; i < 8; ++i) q[h][i] *= a.scale_log2;
   }
@@ -165,9 +165,9 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
       }
     }
     if (a.splits == 1) {
-      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
-                         (static_cast<size_t>(r) * a.nq_l + g * G + h) * HD + d;
-      *o = f2bf(aa / ll);
+      __half* o = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
+                  (static_cast<size_t>(r) * a.nq_l + g * G + h) * HD + d;
+      *o = __float2half_rn(sat_f16(aa / ll));
     } else {
       part[h * (HD + 2) + d] = aa;
       if (d == 0) {
@@ -201,9 +201,9 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
         mm = mn;
       }
     }
-    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
-                       (static_cast<size_t>(r) * a.nq_l + g * G + h) * HD + d;
-    *o = f2bf(aa / ll);
+    __half* o = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
+                (static_cast<size_t>(r) * a.nq_l + g * G + h) * HD + d;
+    *o = __float2half_rn(sat_f16(aa / ll));
   }
   if (threadIdx.x == 0) a.counters[unit] = 0;
 }
@@ -232,10 +232,11 @@ cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s) {
 
 // ---------------------------------------------------------------------------
 // Prefill (several new tokens per sequence, causal with cache offset):
-// flash-attention style on the tensor cores with m16n8k16 bf16 MMA (fp32
+// flash-attention style on the tensor cores with m16n8k16 fp16 MMA (fp32
 // accumulate).  One CTA = 64 queries of one (sequence, rank, q head), 4 warps
 // x 16 query rows; K/V blocks of 64 keys double-buffered in shared memory by
-// cp.async (rows beyond the sequence zero-filled).
+// cp.async (rows beyond the sequence zero-filled), converted from the bf16
+// cache to fp16 in place (exact in fp16's normal range).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   const int n = valid ? 16 : 0;
@@ -258,7 +259,7 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 }
 __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -278,10 +279,10 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(AttnArgs a) {
   constexpr int BQ = C::BQ, BK = C::BK, LD = C::LD;
   constexpr int KSTEPS = HD / 16;  // k-steps of the QK^T product
   constexpr int NT_O = HD / 8;     // n-tiles of the output
-  extern __shared__ __align__(16) __nv_bfloat16 sm[];
-  __nv_bfloat16* sQ = sm;
-  __nv_bfloat16* sK = sm + BQ * LD;          // [2][BK][LD]
-  __nv_bfloat16* sV = sK + 2 * C::TILE;      // [2][BK][LD]
+  extern __shared__ __align__(16) __half sm[];
+  __half* sQ = sm;
+  __half* sK = sm + BQ * LD;          // [2][BK][LD]
+  __half* sV = sK + 2 * C::TILE;      // [2][BK][LD]
 
   const int b = a.seq_begin + blockIdx.z;
   const int qlen = a.cu_q[b + 1] - a.cu_q[b];
@@ -305,9 +306,9 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(AttnArgs a) {
   for (int c = threadIdx.x; c < BQ * CPR; c += 128) {
     const int row = c / CPR, col = (c % CPR) * 8;
     const int qi = q0 + row;
-    const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(a.qkv) +
-                               static_cast<size_t>(tbase + min(qi, qlen - 1)) * a.n * a.w_rank +
-                               static_cast<size_t>(r) * a.w_rank + h * HD + col;
+    const __half* src = reinterpret_cast<const __half*>(a.qkv) +
+                        static_cast<size_t>(tbase + min(qi, qlen - 1)) * a.n * a.w_rank +
+                        static_cast<size_t>(r) * a.w_rank + h * HD + col;
     cp_async16(smem_u32(sQ + row * LD + col), src, qi < qlen);
   }
   const int kend = ctx + min(q0 + BQ, qlen);  // keys needed by this CTA
@@ -320,6 +321,21 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(AttnArgs a) {
       const size_t off = static_cast<size_t>(ok ? key : 0) * HD + col;
       cp_async16(smem_u32(sK + buf * C::TILE + row * LD + col), Kc + off, ok);
       cp_async16(smem_u32(sV + buf * C::TILE + row * LD + col), Vc + off, ok);
+    }
+  };
+  // the chunks this thread loaded, turned from bf16 into fp16 in place once they landed
+  auto convert_kv = [&](int buf) {
+    for (int c = threadIdx.x; c < BK * CPR; c += 128) {
+      const int row = c / CPR, col = (c % CPR) * 8;
+      uint4* pk = reinterpret_cast<uint4*>(sK + buf * C::TILE + row * LD + col);
+      uint4* pv = reinterpret_cast<uint4*>(sV + buf * C::TILE + row * LD + col);
+      uint4 k = *pk, v = *pv;
+      k.x = pack_f16x2(bf16lo(k.x), bf16hi(k.x)); k.y = pack_f16x2(bf16lo(k.y), bf16hi(k.y));
+      k.z = pack_f16x2(bf16lo(k.z), bf16hi(k.z)); k.w = pack_f16x2(bf16lo(k.w), bf16hi(k.w));
+      v.x = pack_f16x2(bf16lo(v.x), bf16hi(v.x)); v.y = pack_f16x2(bf16lo(v.y), bf16hi(v.y));
+      v.z = pack_f16x2(bf16lo(v.z), bf16hi(v.z)); v.w = pack_f16x2(bf16lo(v.w), bf16hi(v.w));
+      *pk = k;
+      *pv = v;
     }
   };
   load_kv(0, 0);
@@ -337,6 +353,7 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(AttnArgs a) {
     if (blk + 1 < nblocks) load_kv(blk + 1, buf ^ 1);
     cp_async_commit();
     cp_async_wait<1>();
+    convert_kv(buf);
     __syncthreads();
     if (blk == 0) {
 #pragma unroll
@@ -349,7 +366,7 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(AttnArgs a) {
     float s[8][4];
 #pragma unroll
     for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.0f;
-    const __nv_bfloat16* kt = sK + buf * C::TILE;
+    const __half* kt = sK + buf * C::TILE;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
 #pragma unroll
@@ -393,8 +410,9 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(AttnArgs a) {
       const float p2 = exp2f(s[j][2] - mbase[1]), p3 = exp2f(s[j][3] - mbase[1]);
       psum[0] += p0 + p1;
       psum[1] += p2 + p3;
-      pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(p0, p1);
-      pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(p2, p3);
+      __half2 h01 = __floats2half2_rn(p0, p1), h23 = __floats2half2_rn(p2, p3);  // P in [0, 1]
+      pa[j >> 1][(j & 1) * 2 + 0] = *reinterpret_cast<uint32_t*>(&h01);
+      pa[j >> 1][(j & 1) * 2 + 1] = *reinterpret_cast<uint32_t*>(&h23);
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -410,7 +428,7 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(AttnArgs a) {
       o[i][3] *= corr[1];
     }
     // O += P V
-    const __nv_bfloat16* vt = sV + buf * C::TILE;
+    const __half* vt = sV + buf * C::TILE;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       uint32_t afr[4] = {pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3]};
@@ -432,12 +450,12 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(AttnArgs a) {
     const int qi = qrow0 + i * 8;
     if (qi >= qlen) continue;
     const float inv = 1.0f / lrow[i];
-    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(tbase + qi) * a.n * a.nq_l * HD +
-                          (static_cast<size_t>(r) * a.nq_l + h) * HD;
+    __half* orow = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(tbase + qi) * a.n * a.nq_l * HD +
+                   (static_cast<size_t>(r) * a.nq_l + h) * HD;
 #pragma unroll
     for (int nt = 0; nt < NT_O; ++nt) {
       const int d = nt * 8 + (lane & 3) * 2;
-      *reinterpret_cast<uint32_t*>(orow + d) = pack_bf16x2(o[nt][i * 2] * inv, o[nt][i * 2 + 1] * inv);
+      *reinterpret_cast<uint32_t*>(orow + d) = pack_f16x2(o[nt][i * 2] * inv, o[nt][i * 2 + 1] * inv);
     }
   }
 }

@@ -11,7 +11,7 @@
 //
 // Each rank's partial is accumulated by the tensor core in its own TMEM
 // accumulator (fp32) and the partials are added in fixed rank order in the
-// epilogue -- the all-reduce of the pages, done in HBM/registers on one GPU.
+// epilogue -- the all-reduce of the pages, done on one GPU.
 //
 // Structure: persistent, warp-specialised, 192 threads per CTA.
 //   warp 0      TMA producer: X and W tiles (64-wide K blocks, 128-byte
@@ -20,7 +20,11 @@
 //               M=128 x N=BN x K=16, two TMEM accumulators so the epilogue of
 //               one segment overlaps the main loop of the next.
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
-//               token row per thread), then the fused epilogue.
+//               row of the MMA's M side per thread), then the fused epilogue.
+// Orientation: tokens on the M side (tiles of 128 tokens x BN features), or,
+// for a handful of tokens against a long weight (the LM head), weights on the
+// M side (tiles of 128 features x BN tokens) so no shared-memory traffic is
+// spent on padding rows.
 // Split-K (for small token counts): a tile's K range is split over several
 // CTAs; each writes an fp32 partial, the last to arrive (atomic counter, no
 // spin-wait) adds the partials in split order and runs the epilogue.
@@ -36,7 +40,7 @@
 namespace tpk {
 
 struct GemmParams {
-  int T, n_seg, kb_seg, x_k_seg, w_row_seg;
+  int T, N, n_seg, kb_seg, x_k_seg, w_row_seg;
   int tiles_t, tiles_f, splits, total_kb;
   void* out;
   int ldo, out_cols;
@@ -47,18 +51,21 @@ struct GemmParams {
   int amax_ld;
   float* logits;
   int ld_logits, vocab;
+  int32_t* out_ids;
+  int* done_counter;
+  QkvEpi qkv;
   int* status;
 };
 
 template <int BN>
 struct GemmCfg {
-  static constexpr int A_BYTES = 128 * 128;  // 128 rows x 64 bf16
-  static constexpr int B_BYTES = BN * 128;   // BN rows x 64 bf16
+  static constexpr int A_BYTES = 128 * 128;  // 128 rows x 64 fp16
+  static constexpr int B_BYTES = BN * 128;   // BN rows x 64 fp16
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);
   static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int NUM_BARS = 2 * STAGES + 5;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64 + 1536;
 };
 
 struct Unit {
@@ -78,39 +85,65 @@ __device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
+// (value, index) order of torch.argmax: larger value first, NaN above all,
+// then the lower index.
+__device__ __forceinline__ bool amax_better(float v, int i, float bv, int bi) {
+  const bool vn = v != v, bn = bv != bv;
+  if (vn != bn) return vn;
+  if (!vn && v != bv) return v > bv;
+  return i < bi;
+}
+
+// 8 consecutive values as bf16 (the KV cache) or fp16 (GEMM / attention operands)
+__device__ __forceinline__ void store8(__nv_bfloat16* dst, const float* x) {
+  uint4 w;
+  w.x = pack_bf16x2(x[0], x[1]);
+  w.y = pack_bf16x2(x[2], x[3]);
+  w.z = pack_bf16x2(x[4], x[5]);
+  w.w = pack_bf16x2(x[6], x[7]);
+  *reinterpret_cast<uint4*>(dst) = w;
+}
+__device__ __forceinline__ void store8(__half* dst, const float* x) {
+  uint4 w;
+  w.x = pack_f16x2(x[0], x[1]);
+  w.y = pack_f16x2(x[2], x[3]);
+  w.z = pack_f16x2(x[4], x[5]);
+  w.w = pack_f16x2(x[6], x[7]);
+  *reinterpret_cast<uint4*>(dst) = w;
+}
+
 // ---- epilogue stores for one token row, 32 consecutive tile columns ----
+// EPI_STORE writes fp16 (the next GEMM's operand); EPI_RESID adds the
+// rank-summed row into the fp32 residual stream in place.
 template <int EPI>
 __device__ __forceinline__ void store_chunk(const GemmParams& p, int t, int f, const float* v) {
-  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(t) * p.ldo + f;
-  if (f + 32 <= p.out_cols) {
-    uint4* o4 = reinterpret_cast<uint4*>(o);
+  if constexpr (EPI == EPI_RESID) {
+    float* o = reinterpret_cast<float*>(p.out) + static_cast<size_t>(t) * p.ldo + f;
+    if (f + 32 <= p.out_cols) {
+      float4* o4 = reinterpret_cast<float4*>(o);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float x[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = v[j * 8 + i];
-      if (EPI == EPI_RESID) {
-        const uint4 r = o4[j];
-        x[0] += bf16lo(r.x); x[1] += bf16hi(r.x);
-        x[2] += bf16lo(r.y); x[3] += bf16hi(r.y);
-        x[4] += bf16lo(r.z); x[5] += bf16hi(r.z);
-        x[6] += bf16lo(r.w); x[7] += bf16hi(r.w);
+      for (int j = 0; j < 8; ++j) {
+        float4 r = o4[j];
+        r.x += v[j * 4 + 0];
+        r.y += v[j * 4 + 1];
+        r.z += v[j * 4 + 2];
+        r.w += v[j * 4 + 3];
+        o4[j] = r;
       }
-      uint4 w;
-      w.x = pack_bf16x2(x[0], x[1]);
-      w.y = pack_bf16x2(x[2], x[3]);
-      w.z = pack_bf16x2(x[4], x[5]);
-      w.w = pack_bf16x2(x[6], x[7]);
-      o4[j] = w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (f + i < p.out_cols) o[i] += v[i];
     }
   } else {
+    __half* o = reinterpret_cast<__half*>(p.out) + static_cast<size_t>(t) * p.ldo + f;
+    if (f + 32 <= p.out_cols) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (f + i < p.out_cols) {
-        float x = v[i];
-        if (EPI == EPI_RESID) x += bf2f(o[i]);
-        o[i] = f2bf(x);
-      }
+      for (int j = 0; j < 4; ++j) store8(o + j * 8, v + j * 8);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (f + i < p.out_cols) o[i] = __float2half_rn(sat_f16(v[i]));
     }
   }
 }
@@ -141,7 +174,99 @@ __device__ __forceinline__ void argmax_scan(const GemmParams& p, int t, int f, c
   }
 }
 
-template <int BN, int EPI, bool ACC>
+// Token row t -> its sequence, position and cache slot (binary search over cu_q).
+struct TokPos {
+  int pos, seq_slot;
+  bool ok;
+};
+__device__ __forceinline__ TokPos token_position(const QkvEpi& q, int t) {
+  int lo = 0, hi = q.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (q.cu_q[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  TokPos tp;
+  tp.pos = q.ctx_len[lo] + (t - q.cu_q[lo]);
+  tp.seq_slot = q.slot[lo];
+  tp.ok = tp.pos >= 0 && tp.pos < q.cap && tp.pos < q.max_pos;
+  return tp;
+}
+
+// One head of the merged QKV row of token t (fp32, straight from the
+// accumulator): q and k get RMSNorm over head_dim and rotate-half RoPE at the
+// token's position; q goes back to the QKV buffer, k and v to the rank's cache
+// (post-RoPE K, raw V).  ("Tensor parallelism from scratch", tp.py
+// TPAttention.forward: q_norm / k_norm, apply_rope, cache.update.)
+template <int HD>
+__device__ __forceinline__ void qkv_head(const GemmParams& p, int t, const TokPos& tp, int col0, const float* h) {
+  const QkvEpi& q = p.qkv;
+  constexpr int HALF = HD / 2;
+  const int r = col0 / q.w_rank;
+  const int sh = (col0 - r * q.w_rank) / HD;
+  const size_t plane = static_cast<size_t>(q.max_seqs) * q.nkv_l * q.cap * HD;
+  __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(q.kv);
+  if (sh >= q.nq_l + q.nkv_l) {  // v: raw into the cache
+    const int g = sh - q.nq_l - q.nkv_l;
+    __nv_bfloat16* dst = kv + (2 * static_cast<size_t>(r) + 1) * plane +
+                         ((static_cast<size_t>(tp.seq_slot) * q.nkv_l + g) * q.cap + tp.pos) * HD;
+#pragma unroll
+    for (int j = 0; j < HD / 8; ++j) store8(dst + j * 8, h + j * 8);
+    return;
+  }
+  const bool is_q = sh < q.nq_l;
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < HD; ++i) ss += h[i] * h[i];
+  const float inv = rsqrtf(ss / static_cast<float>(HD) + q.eps);
+  const __nv_bfloat16* nw = reinterpret_cast<const __nv_bfloat16*>(is_q ? q.q_norm : q.k_norm);
+  const float2* cs = q.rope + static_cast<size_t>(tp.pos) * HALF;
+  __half* qdst = reinterpret_cast<__half*>(p.out) + static_cast<size_t>(t) * p.ldo + col0;       // q: fp16 operand
+  __nv_bfloat16* kdst = kv + (2 * static_cast<size_t>(r)) * plane +                                // k: bf16 cache
+                        ((static_cast<size_t>(tp.seq_slot) * q.nkv_l + (sh - q.nq_l)) * q.cap + tp.pos) * HD;
+#pragma unroll
+  for (int j = 0; j < HALF / 8; ++j) {
+    float y0[8], y1[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int d = j * 8 + i;
+      const float u0 = h[d] * inv * bf2f(nw[d]);
+      const float u1 = h[d + HALF] * inv * bf2f(nw[d + HALF]);
+      const float2 c = cs[d];
+      y0[i] = u0 * c.x - u1 * c.y;
+      y1[i] = u1 * c.x + u0 * c.y;
+    }
+    if (is_q) {
+      store8(qdst + j * 8, y0);
+      store8(qdst + HALF + j * 8, y1);
+    } else {
+      store8(kdst + j * 8, y0);
+      store8(kdst + HALF + j * 8, y1);
+    }
+  }
+}
+
+// Streams the heads of one accumulator tile (tokens on the M side) through qkv_head.
+template <int BN, int HD>
+__device__ __forceinline__ void qkv_stream(const GemmParams& p, uint32_t ta, int t, const TokPos& tp, int f0,
+                                           bool row_ok) {
+#pragma unroll 1
+  for (int hb = 0; hb < BN / HD; ++hb) {
+    const int col0 = f0 + hb * HD;
+    if (col0 >= p.N) break;  // warp-uniform
+    float h[HD];
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) {
+      float v[32];
+      tc_ld32(ta + hb * HD + c * 32, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) h[c * 32 + i] = v[i];
+    }
+    if (row_ok && tp.ok) qkv_head<HD>(p, t, tp, col0, h);
+  }
+}
+
+template <int BN, int EPI, bool ACC, bool SWAP>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const GemmParams p) {
@@ -155,6 +280,11 @@ __global__ void __launch_bounds__(192, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  // weight-streaming argmax: per-column partials of the 4 epilogue warps and the CTA's running best
+  float* red_v = reinterpret_cast<float*>(tmem_slot + 16);  // [4][32]
+  int* red_i = reinterpret_cast<int*>(red_v + 128);          // [4][32]
+  float* best_v = reinterpret_cast<float*>(red_i + 128);     // [64]
+  int* best_i = reinterpret_cast<int*>(best_v + 64);         // [64]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bar0 = smem_u32(bars);
@@ -178,6 +308,10 @@ __global__ void __launch_bounds__(192, 1)
     *last_flag = 0;
     fence_barrier_init();
   }
+  if (SWAP && threadIdx.x >= 64 && threadIdx.x < 128) {
+    best_v[threadIdx.x - 64] = -INFINITY;
+    best_i[threadIdx.x - 64] = INT_MAX;
+  }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmW);
@@ -191,6 +325,9 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int units = p.tiles_t * p.tiles_f * p.splits;
+  // tile extents on the token and feature sides
+  constexpr int TM_T = SWAP ? BN : 128;  // tokens per tile
+  constexpr int TM_F = SWAP ? 128 : BN;  // features per tile
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -199,7 +336,7 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         const Unit un = unit_of(p, u);
-        const int t0 = un.tt * 128, f0 = un.tf * BN;
+        const int t0 = un.tt * TM_T, f0 = un.tf * TM_F;
         for (int g = un.g0; g < un.g1; ++g) {
           const int r = g / p.kb_seg, kb = g - r * p.kb_seg;
           const int s = it % STAGES;
@@ -209,8 +346,10 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           mbar_arrive_expect_tx(FULL(s), C::STAGE_BYTES);
-          tma_load_2d(smem_u32(sA + s * C::A_BYTES), &tmX, FULL(s), r * p.x_k_seg + kb * 64, t0);
-          tma_load_2d(smem_u32(sB + s * C::B_BYTES), &tmW, FULL(s), kb * 64, r * p.w_row_seg + f0);
+          const uint32_t xdst = smem_u32(SWAP ? sB + s * C::B_BYTES : sA + s * C::A_BYTES);
+          const uint32_t wdst = smem_u32(SWAP ? sA + s * C::A_BYTES : sB + s * C::B_BYTES);
+          tma_load_2d(xdst, &tmX, FULL(s), r * p.x_k_seg + kb * 64, t0);
+          tma_load_2d(wdst, &tmW, FULL(s), kb * 64, r * p.w_row_seg + f0);
           ++it;
         }
       }
@@ -221,7 +360,7 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, BN);
+      const uint32_t idesc = idesc_f16_f32(128, BN);
       int it = 0, seg = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
@@ -249,7 +388,7 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t bd = sdesc_k_sw128(smem_u32(sB + s * C::B_BYTES));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              tc_mma_bf16(d, ad + 2ull * kk, bd + 2ull * kk, idesc, (g > gs || kk > 0) ? 1u : 0u);
+              tc_mma_f16(d, ad + 2ull * kk, bd + 2ull * kk, idesc, (g > gs || kk > 0) ? 1u : 0u);
             tc_commit(EMPTY(s));
             ++it;
           }
@@ -261,8 +400,111 @@ __global__ void __launch_bounds__(192, 1)
       tc_commit(DRAIN);
       mbar_wait(DRAIN, 0, nullptr, p.status);
     }
+  } else if constexpr (SWAP) {
+    // ---------------- epilogue, weights on the M side: argmax over features ----------------
+    static_assert(EPI == EPI_ARGMAX && !ACC, "weight-streaming path implements the argmax epilogue");
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const int et = threadIdx.x - 64;  // epilogue thread 0..127
+    int seg = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const Unit un = unit_of(p, u);
+      const int f = un.tf * 128 + row;
+      const int t0 = un.tt * BN;
+      const bool f_ok = f < p.vocab;
+      const int b = seg & 1;
+      const uint32_t use = (seg >> 1) & 1;
+      ok = mbar_wait(TFULL(b), use, abort_flag, p.status);
+      if (!named_bar_and(1, 128, ok)) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        if constexpr (BN == 16) {
+          float v16[16];
+          tc_ld16(lane_addr + static_cast<uint32_t>(b * BN), v16);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = i < 16 ? v16[i] : 0.0f;
+        } else {
+          tc_ld32(lane_addr + static_cast<uint32_t>(b * BN + c0), v);
+        }
+        const int ncol = min(min(32, BN), p.T - (t0 + c0));  // valid token columns (warp-uniform)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (i >= ncol) break;
+          float bv = f_ok ? v[i] : -INFINITY;
+          int bi = f_ok ? f : INT_MAX;
+          if (p.logits && f_ok) p.logits[static_cast<size_t>(t0 + c0 + i) * p.ld_logits + f] = v[i];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (amax_better(ov, oi, bv, bi)) {
+              bv = ov;
+              bi = oi;
+            }
+          }
+          if (lane == 0) {
+            red_v[q * 32 + i] = bv;
+            red_i[q * 32 + i] = bi;
+          }
+        }
+        named_bar_sync(1, 128);
+        if (et < ncol) {
+          const int t = t0 + c0 + et;
+          float bv = best_v[t];
+          int bi = best_i[t];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const float ov = red_v[w * 32 + et];
+            const int oi = red_i[w * 32 + et];
+            if (amax_better(ov, oi, bv, bi)) {
+              bv = ov;
+              bi = oi;
+            }
+          }
+          best_v[t] = bv;
+          best_i[t] = bi;
+        }
+        named_bar_sync(1, 128);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(TEMPTY(b));
+      ++seg;
+    }
+    // CTA partials -> the last CTA to finish reduces them (no waiting)
+    if (named_bar_and(1, 128, ok)) {
+      for (int t = et; t < p.T; t += 128) {
+        p.amax_val[static_cast<size_t>(blockIdx.x) * p.amax_ld + t] = best_v[t];
+        p.amax_idx[static_cast<size_t>(blockIdx.x) * p.amax_ld + t] = best_i[t];
+      }
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (et == 0) *last_flag = (atomicAdd(p.done_counter, 1) == static_cast<int>(gridDim.x) - 1) ? 1 : 0;
+      named_bar_sync(1, 128);
+      if (*last_flag) {
+        __threadfence();
+        for (int t = et; t < p.T; t += 128) {
+          float bv = -INFINITY;
+          int bi = INT_MAX;
+          for (int c = 0; c < static_cast<int>(gridDim.x); ++c) {
+            const float ov = __ldcg(p.amax_val + static_cast<size_t>(c) * p.amax_ld + t);
+            const int oi = __ldcg(p.amax_idx + static_cast<size_t>(c) * p.amax_ld + t);
+            if (amax_better(ov, oi, bv, bi)) {
+              bv = ov;
+              bi = oi;
+            }
+          }
+          p.out_ids[t] = bi;
+        }
+        if (et == 0) *p.done_counter = 0;
+      }
+    }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (warps 2..5), tokens on the M side ----------------
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
@@ -272,13 +514,26 @@ __global__ void __launch_bounds__(192, 1)
       const int t = un.tt * 128 + row;
       const int f0 = un.tf * BN;
       const bool row_ok = t < p.T;
+      TokPos tp{0, 0, false};
+      if constexpr (EPI == EPI_QKV) {
+        if (row_ok) {
+          tp = token_position(p.qkv, t);
+          if (!tp.ok) raise_flag(p.status, TP_DEVFLAG_BAD_TOKEN);
+        }
+      }
       if constexpr (!ACC) {
         const int b = seg & 1;
         const uint32_t use = (seg >> 1) & 1;
         if (!mbar_wait(TFULL(b), use, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t ta = lane_addr + static_cast<uint32_t>(b * BN);
-        if constexpr (EPI == EPI_SILU) {
+        if constexpr (EPI == EPI_QKV) {
+          if (BN >= 128 && p.qkv.hd == 128) {
+            qkv_stream<BN, (BN >= 128 ? 128 : 64)>(p, ta, t, tp, f0, row_ok);
+          } else {
+            qkv_stream<BN, 64>(p, ta, t, tp, f0, row_ok);
+          }
+        } else if constexpr (EPI == EPI_SILU) {
 #pragma unroll 1
           for (int qb = 0; qb < BN / 128; ++qb) {
 #pragma unroll 1
@@ -369,7 +624,22 @@ __global__ void __launch_bounds__(192, 1)
           if (threadIdx.x == 64) p.counters[tile] = 0;
         }
         if (row_ok) {
-          if constexpr (EPI == EPI_SILU) {
+          if constexpr (EPI == EPI_QKV) {
+            if (tp.ok) {
+              if constexpr (BN >= 128) {
+                if (p.qkv.hd == 128) {
+#pragma unroll
+                  for (int hb = 0; hb < BN / 128; ++hb)
+                    if (f0 + hb * 128 < p.N) qkv_head<128>(p, t, tp, f0 + hb * 128, acc + hb * 128);
+                }
+              }
+              if (p.qkv.hd == 64) {
+#pragma unroll
+                for (int hb = 0; hb < BN / 64; ++hb)
+                  if (f0 + hb * 64 < p.N) qkv_head<64>(p, t, tp, f0 + hb * 64, acc + hb * 64);
+              }
+            }
+          } else if constexpr (EPI == EPI_SILU) {
 #pragma unroll
             for (int qb = 0; qb < BN / 128; ++qb)
 #pragma unroll
@@ -418,7 +688,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D bf16 row-major tensor [rows, cols] (row stride ld elements), box 64 x box_rows, 128 B swizzle.
+// 2D fp16 row-major tensor [rows, cols] (row stride ld elements), box 64 x box_rows, 128 B swizzle.
 static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -426,7 +696,7 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
   cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -436,10 +706,24 @@ static inline int cdiv(long long a, long long b) { return static_cast<int>((a + 
 
 GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
   GemmPlan pl{};
-  pl.tiles_t = cdiv(pr.T, 128);
   const int total_kb = pr.n_seg * (pr.k_seg / 64);
+  if (pr.epi == EPI_ARGMAX && pr.T <= 64) {
+    // few tokens against the whole vocab: weights on the M side, tokens as N
+    pl.swap = true;
+    pl.BN = pr.T <= 16 ? 16 : (pr.T <= 32 ? 32 : 64);
+    pl.tiles_t = 1;
+    pl.tiles_f = cdiv(pr.N, 128);
+    pl.splits = 1;
+    pl.acc = false;
+    const int units = pl.tiles_f;
+    pl.grid = units < num_sms ? units : num_sms;
+    pl.partial_floats = 0;
+    return pl;
+  }
+  pl.tiles_t = cdiv(pr.T, 128);
   // tile width: wide tiles while there are enough of them to fill the GPU
   int BN;
+  const int min_bn = pr.epi == EPI_QKV ? pr.qkv.hd : 64;
   if (pr.epi == EPI_ARGMAX) {
     BN = 64;  // weight streaming: small units balance the HBM-bound LM head
   } else if (pr.epi == EPI_SILU) {
@@ -451,6 +735,7 @@ GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
   } else {
     BN = 64;
   }
+  if (BN < min_bn) BN = min_bn;
   pl.BN = BN;
   pl.tiles_f = cdiv(pr.N, BN);
   const int tiles = pl.tiles_t * pl.tiles_f;
@@ -474,10 +759,10 @@ GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
 
 int gemm_num_tiles_f(const GemmProblem& pr, const GemmPlan& plan) { return plan.tiles_f; }
 
-template <int BN, int EPI, bool ACC>
+template <int BN, int EPI, bool ACC, bool SWAP>
 static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, const GemmParams& gp, int grid,
                                   cudaStream_t s) {
-  auto kern = gemm_tc_kernel<BN, EPI, ACC>;
+  auto kern = gemm_tc_kernel<BN, EPI, ACC, SWAP>;
   constexpr int smem = GemmCfg<BN>::SMEM;
   static bool attr_done = false;  // per instantiation
   if (!attr_done) {
@@ -494,10 +779,11 @@ cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partia
   if (pr.T <= 0) return cudaSuccess;
   if (pr.k_seg % 64 || pr.ldo % 8) return cudaErrorInvalidValue;
   CUtensorMap mx, mw;
-  if (!make_map(&mx, pr.x, pr.x_rows, pr.x_cols, pr.x_ld, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&mw, pr.w, pr.w_rows, pr.w_cols, pr.w_ld, pl.BN)) return cudaErrorInvalidValue;
+  if (!make_map(&mx, pr.x, pr.x_rows, pr.x_cols, pr.x_ld, pl.swap ? pl.BN : 128)) return cudaErrorInvalidValue;
+  if (!make_map(&mw, pr.w, pr.w_rows, pr.w_cols, pr.w_ld, pl.swap ? 128 : pl.BN)) return cudaErrorInvalidValue;
   GemmParams gp{};
   gp.T = pr.T;
+  gp.N = pr.N;
   gp.n_seg = pr.n_seg;
   gp.kb_seg = pr.k_seg / 64;
   gp.x_k_seg = pr.x_k_seg;
@@ -517,24 +803,36 @@ cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partia
   gp.logits = pr.logits;
   gp.ld_logits = pr.ld_logits;
   gp.vocab = pr.vocab;
+  gp.out_ids = pr.out_ids;
+  gp.done_counter = counters;
+  gp.qkv = pr.qkv;
   gp.status = status;
   const int g = pl.grid;
-#define TP_V(BN_, EPI_, ACC_) \
-  if (pl.BN == BN_ && pr.epi == EPI_ && pl.acc == ACC_) return launch_variant<BN_, EPI_, ACC_>(mx, mw, gp, g, stream);
-  TP_V(256, EPI_STORE, false)
-  TP_V(128, EPI_STORE, false)
-  TP_V(64, EPI_STORE, false)
-  TP_V(128, EPI_STORE, true)
-  TP_V(64, EPI_STORE, true)
-  TP_V(256, EPI_SILU, false)
-  TP_V(128, EPI_SILU, false)
-  TP_V(128, EPI_SILU, true)
-  TP_V(256, EPI_RESID, false)
-  TP_V(128, EPI_RESID, false)
-  TP_V(64, EPI_RESID, false)
-  TP_V(128, EPI_RESID, true)
-  TP_V(64, EPI_RESID, true)
-  TP_V(64, EPI_ARGMAX, false)
+#define TP_V(BN_, EPI_, ACC_, SW_)                                                           \
+  if (pl.BN == BN_ && pr.epi == EPI_ && pl.acc == ACC_ && pl.swap == SW_)                     \
+    return launch_variant<BN_, EPI_, ACC_, SW_>(mx, mw, gp, g, stream);
+  TP_V(256, EPI_STORE, false, false)
+  TP_V(128, EPI_STORE, false, false)
+  TP_V(64, EPI_STORE, false, false)
+  TP_V(128, EPI_STORE, true, false)
+  TP_V(64, EPI_STORE, true, false)
+  TP_V(256, EPI_QKV, false, false)
+  TP_V(128, EPI_QKV, false, false)
+  TP_V(64, EPI_QKV, false, false)
+  TP_V(128, EPI_QKV, true, false)
+  TP_V(64, EPI_QKV, true, false)
+  TP_V(256, EPI_SILU, false, false)
+  TP_V(128, EPI_SILU, false, false)
+  TP_V(128, EPI_SILU, true, false)
+  TP_V(256, EPI_RESID, false, false)
+  TP_V(128, EPI_RESID, false, false)
+  TP_V(64, EPI_RESID, false, false)
+  TP_V(128, EPI_RESID, true, false)
+  TP_V(64, EPI_RESID, true, false)
+  TP_V(64, EPI_ARGMAX, false, false)
+  TP_V(16, EPI_ARGMAX, false, true)
+  TP_V(32, EPI_ARGMAX, false, true)
+  TP_V(64, EPI_ARGMAX, false, true)
 #undef TP_V
   return cudaErrorNotSupported;
 }

@@ -1,7 +1,7 @@
 // Bandwidth-bound kernels of the tensor-parallel forward: vocab-parallel
-// embedding with its rank-sum, RMSNorm, q/k RMSNorm + RoPE + KV-cache write,
-// final RMSNorm of each sequence's last token, and the argmax reduction that
-// replaces the logits all-gather.  Plain coalesced 16-byte loads; no tensor
+// embedding with its rank-sum, RMSNorm, the final RMSNorm of each sequence's
+// last token, and the argmax reduction that replaces the logits all-gather.
+// (q/k RMSNorm + RoPE + KV-cache write run in the QKV GEMM epilogue.)  Plain coalesced 16-byte loads; no tensor
 // cores (none of this is a contraction).
 #include <climits>
 
@@ -22,7 +22,7 @@ namespace tpk {
 // ---------------------------------------------------------------------------
 __global__ void embed_vocab_parallel_kernel(const int32_t* __restrict__ ids, const uint4* __restrict__ table,
                                             int n, int64_t v_local, int64_t vocab, int H,
-                                            uint4* __restrict__ out, int* status) {
+                                            float4* __restrict__ out, int* status) {
   const int t = blockIdx.x;
   const int id = ids[t];
   if (threadIdx.x == 0 && (id < 0 || id >= vocab)) raise_flag(status, TP_DEVFLAG_BAD_TOKEN);
@@ -42,12 +42,8 @@ __global__ void embed_vocab_parallel_kernel(const int32_t* __restrict__ ids, con
         acc[6] += bf16lo(w.w); acc[7] += bf16hi(w.w);
       }
     }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    out[static_cast<int64_t>(t) * chunks + c] = o;
+    out[(static_cast<int64_t>(t) * chunks + c) * 2] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    out[(static_cast<int64_t>(t) * chunks + c) * 2 + 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
 }
 
@@ -56,16 +52,17 @@ cudaError_t launch_embed(const int32_t* ids, int T, const void* embed_stacked, i
   if (T <= 0) return cudaSuccess;
   const int threads = H / 8 < 128 ? 32 * ((H / 8 + 31) / 32) : 128;
   embed_vocab_parallel_kernel<<<T, threads, 0, s>>>(ids, reinterpret_cast<const uint4*>(embed_stacked), n, v_local,
-                                                    vocab, H, reinterpret_cast<uint4*>(out), status);
+                                                    vocab, H, reinterpret_cast<float4*>(out), status);
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
-// RMSNorm over the hidden dimension, fp32 math: y = x * rsqrt(mean(x^2)+eps) * w.
+// RMSNorm over the hidden dimension of the fp32 residual stream, fp32 math:
+// y = x * rsqrt(mean(x^2) + eps) * w, written as fp16 (the next GEMM's operand).
 // One warp per row; row_index (optional) picks the source row of each output row.
 // ---------------------------------------------------------------------------
-template <int VPL>  // 16-byte vectors per lane
-__global__ void rmsnorm_kernel(const uint4* __restrict__ x, int64_t rows, int H, const uint4* __restrict__ w,
+template <int VPL>  // 8-element groups per lane kept in registers
+__global__ void rmsnorm_kernel(const float4* __restrict__ x, int64_t rows, int H, const uint4* __restrict__ w,
                                float eps, uint4* __restrict__ out, const int32_t* __restrict__ row_index) {
   const int warps = blockDim.x / 32;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * warps + threadIdx.x / 32;
@@ -73,18 +70,16 @@ __global__ void rmsnorm_kernel(const uint4* __restrict__ x, int64_t rows, int H,
   if (row >= rows) return;
   const int64_t src = row_index ? row_index[row] : row;
   const int chunks = H / 8;
-  const uint4* xr = x + src * chunks;
+  const float4* xr = x + src * (H / 4);
   float v[VPL][8];
   float ss = 0.0f;
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
     const int c = lane + 32 * j;
     if (c < chunks) {
-      const uint4 u = xr[c];
-      v[j][0] = bf16lo(u.x); v[j][1] = bf16hi(u.x);
-      v[j][2] = bf16lo(u.y); v[j][3] = bf16hi(u.y);
-      v[j][4] = bf16lo(u.z); v[j][5] = bf16hi(u.z);
-      v[j][6] = bf16lo(u.w); v[j][7] = bf16hi(u.w);
+      const float4 a = xr[2 * c], b = xr[2 * c + 1];
+      v[j][0] = a.x; v[j][1] = a.y; v[j][2] = a.z; v[j][3] = a.w;
+      v[j][4] = b.x; v[j][5] = b.y; v[j][6] = b.z; v[j][7] = b.w;
 #pragma unroll
       for (int i = 0; i < 8; ++i) ss += v[j][i] * v[j][i];
     }
@@ -99,17 +94,17 @@ __global__ void rmsnorm_kernel(const uint4* __restrict__ x, int64_t rows, int H,
       const float wf[8] = {bf16lo(wu.x), bf16hi(wu.x), bf16lo(wu.y), bf16hi(wu.y),
                            bf16lo(wu.z), bf16hi(wu.z), bf16lo(wu.w), bf16hi(wu.w)};
       uint4 o;
-      o.x = pack_bf16x2(v[j][0] * inv * wf[0], v[j][1] * inv * wf[1]);
-      o.y = pack_bf16x2(v[j][2] * inv * wf[2], v[j][3] * inv * wf[3]);
-      o.z = pack_bf16x2(v[j][4] * inv * wf[4], v[j][5] * inv * wf[5]);
-      o.w = pack_bf16x2(v[j][6] * inv * wf[6], v[j][7] * inv * wf[7]);
+      o.x = pack_f16x2(v[j][0] * inv * wf[0], v[j][1] * inv * wf[1]);
+      o.y = pack_f16x2(v[j][2] * inv * wf[2], v[j][3] * inv * wf[3]);
+      o.z = pack_f16x2(v[j][4] * inv * wf[4], v[j][5] * inv * wf[5]);
+      o.w = pack_f16x2(v[j][6] * inv * wf[6], v[j][7] * inv * wf[7]);
       out[row * chunks + c] = o;
     }
   }
 }
 
 // Wide rows (H > 2048): one warp per row, two passes (the second re-reads the row from L1/L2).
-__global__ void rmsnorm_wide_kernel(const uint4* __restrict__ x, int64_t rows, int H, const uint4* __restrict__ w,
+__global__ void rmsnorm_wide_kernel(const float4* __restrict__ x, int64_t rows, int H, const uint4* __restrict__ w,
                                     float eps, uint4* __restrict__ out, const int32_t* __restrict__ row_index) {
   const int warps = blockDim.x / 32;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * warps + threadIdx.x / 32;
@@ -117,25 +112,22 @@ __global__ void rmsnorm_wide_kernel(const uint4* __restrict__ x, int64_t rows, i
   if (row >= rows) return;
   const int64_t src = row_index ? row_index[row] : row;
   const int chunks = H / 8;
-  const uint4* xr = x + src * chunks;
+  const float4* xr = x + src * (H / 4);
   float ss = 0.0f;
   for (int c = lane; c < chunks; c += 32) {
-    const uint4 u = xr[c];
-    const float f[8] = {bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y),
-                        bf16lo(u.z), bf16hi(u.z), bf16lo(u.w), bf16hi(u.w)};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ss += f[i] * f[i];
+    const float4 a = xr[2 * c], b = xr[2 * c + 1];
+    ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
   }
   ss = warp_sum(ss);
   const float inv = rsqrtf(ss / static_cast<float>(H) + eps);
   for (int c = lane; c < chunks; c += 32) {
-    const uint4 u = xr[c];
+    const float4 a = xr[2 * c], b = xr[2 * c + 1];
     const uint4 wu = w[c];
     uint4 o;
-    o.x = pack_bf16x2(bf16lo(u.x) * inv * bf16lo(wu.x), bf16hi(u.x) * inv * bf16hi(wu.x));
-    o.y = pack_bf16x2(bf16lo(u.y) * inv * bf16lo(wu.y), bf16hi(u.y) * inv * bf16hi(wu.y));
-    o.z = pack_bf16x2(bf16lo(u.z) * inv * bf16lo(wu.z), bf16hi(u.z) * inv * bf16hi(wu.z));
-    o.w = pack_bf16x2(bf16lo(u.w) * inv * bf16lo(wu.w), bf16hi(u.w) * inv * bf16hi(wu.w));
+    o.x = pack_f16x2(a.x * inv * bf16lo(wu.x), a.y * inv * bf16hi(wu.x));
+    o.y = pack_f16x2(a.z * inv * bf16lo(wu.y), a.w * inv * bf16hi(wu.y));
+    o.z = pack_f16x2(b.x * inv * bf16lo(wu.z), b.y * inv * bf16hi(wu.z));
+    o.w = pack_f16x2(b.z * inv * bf16lo(wu.w), b.w * inv * bf16hi(wu.w));
     out[row * chunks + c] = o;
   }
 }
@@ -146,7 +138,7 @@ cudaError_t launch_rmsnorm(const void* x, int64_t rows, int H, const void* w, fl
   const int vpl = (H / 8 + 31) / 32;
   const int warps = 4;
   const unsigned grid = static_cast<unsigned>((rows + warps - 1) / warps);
-  auto X = reinterpret_cast<const uint4*>(x);
+  auto X = reinterpret_cast<const float4*>(x);
   auto W = reinterpret_cast<const uint4*>(w);
   auto O = reinterpret_cast<uint4*>(out);
   if (vpl <= 1) rmsnorm_kernel<1><<<grid, 32 * warps, 0, s>>>(X, rows, H, W, eps, O, row_index);
@@ -173,101 +165,25 @@ cudaError_t launch_final_norm_select(const void* hidden, int H, const int32_t* c
 }
 
 // ---------------------------------------------------------------------------
-// q/k RMSNorm per head over head_dim, rotate-half RoPE at each token's
-// position, then K and V written to the rank's cache (post-RoPE K, raw V);
-// q is rewritten in place for the attention kernel.
-// ("Tensor parallelism from scratch", tp.py TPAttention.forward: q_norm/k_norm,
-// apply_rope at positions start..start+T, cache.update.)
-// One warp per (token, rank, head slot); the slot enumerates nq_l q heads,
-// nkv_l k heads and nkv_l v heads of the rank.
+// bf16 -> fp16, in place (weight shards used as tensor-core operands).  Exact
+// for magnitudes in fp16's normal range [2^-14, 65504]; smaller magnitudes
+// round to fp16's subnormal grid (absolute error <= 2^-25), larger ones
+// saturate.
 // ---------------------------------------------------------------------------
-template <int HD>
-__global__ void qk_norm_rope_kernel(RopeArgs a) {
-  constexpr int HALF = HD / 2;
-  constexpr int PER = HALF / 32;  // elements per lane in each half
-  const int warps = blockDim.x / 32;
-  const int64_t wid = static_cast<int64_t>(blockIdx.x) * warps + threadIdx.x / 32;
-  const int lane = threadIdx.x & 31;
-  const int slots = a.nq_l + 2 * a.nkv_l;
-  const int64_t total = static_cast<int64_t>(a.T) * a.n * slots;
-  if (wid >= total) return;
-  const int slot_h = static_cast<int>(wid % slots);
-  const int r = static_cast<int>((wid / slots) % a.n);
-  const int t = static_cast<int>(wid / (static_cast<int64_t>(slots) * a.n));
-  // sequence of token t: largest b with cu_q[b] <= t
-  int lo = 0, hi = a.B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (a.cu_q[mid] <= t) lo = mid;
-    else hi = mid - 1;
-  }
-  const int b = lo;
-  const int pos = a.ctx_len[b] + (t - a.cu_q[b]);
-  if (pos < 0 || pos >= a.cap || pos >= a.max_pos) {
-    if (lane == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
-    return;
-  }
-  __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(a.qkv) + static_cast<int64_t>(t) * a.n * a.w_rank +
-                       static_cast<int64_t>(r) * a.w_rank + static_cast<int64_t>(slot_h) * HD;
-  float x0[PER], x1[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    x0[i] = bf2f(row[lane + 32 * i]);
-    x1[i] = bf2f(row[HALF + lane + 32 * i]);
-  }
-  const int seq_slot = a.slot[b];
-  const size_t plane = static_cast<size_t>(a.max_seqs) * a.nkv_l * a.cap * HD;  // one of K or V for one rank
-  if (slot_h >= a.nq_l + a.nkv_l) {  // v: raw copy into the cache
-    const int g = slot_h - a.nq_l - a.nkv_l;
-    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.kv) + (2 * static_cast<size_t>(r) + 1) * plane +
-                         ((static_cast<size_t>(seq_slot) * a.nkv_l + g) * a.cap + pos) * HD;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      dst[lane + 32 * i] = f2bf(x0[i]);
-      dst[HALF + lane + 32 * i] = f2bf(x1[i]);
-    }
-    return;
-  }
-  const bool is_q = slot_h < a.nq_l;
-  const __nv_bfloat16* nw = reinterpret_cast<const __nv_bfloat16*>(is_q ? a.q_norm : a.k_norm);
-  float ss = 0.0f;
-#pragma unroll
-  for (int i = 0; i < PER; ++i) ss += x0[i] * x0[i] + x1[i] * x1[i];
-  ss = warp_sum(ss);
-  const float inv = rsqrtf(ss / static_cast<float>(HD) + a.eps);
-  const float2* cs = a.rope + static_cast<size_t>(pos) * HALF;
-  float y0[PER], y1[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int d = lane + 32 * i;
-    const float u0 = x0[i] * inv * bf2f(nw[d]);
-    const float u1 = x1[i] * inv * bf2f(nw[HALF + d]);
-    const float2 c = cs[d];
-    y0[i] = u0 * c.x - u1 * c.y;
-    y1[i] = u1 * c.x + u0 * c.y;
-  }
-  __nv_bfloat16* dst;
-  if (is_q) {
-    dst = row;
-  } else {
-    const int g = slot_h - a.nq_l;
-    dst = reinterpret_cast<__nv_bfloat16*>(a.kv) + (2 * static_cast<size_t>(r)) * plane +
-          ((static_cast<size_t>(seq_slot) * a.nkv_l + g) * a.cap + pos) * HD;
-  }
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    dst[lane + 32 * i] = f2bf(y0[i]);
-    dst[HALF + lane + 32 * i] = f2bf(y1[i]);
+__global__ void bf16_to_f16_kernel(uint32_t* __restrict__ w, size_t n_pairs) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n_pairs;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint32_t v = w[i];
+    w[i] = pack_f16x2(bf16lo(v), bf16hi(v));
   }
 }
 
-cudaError_t launch_qk_norm_rope(const RopeArgs& a, cudaStream_t s) {
-  if (a.T <= 0) return cudaSuccess;
-  const int64_t warps = static_cast<int64_t>(a.T) * a.n * (a.nq_l + 2 * a.nkv_l);
-  const unsigned grid = static_cast<unsigned>((warps + 7) / 8);
-  if (a.hd == 128) qk_norm_rope_kernel<128><<<grid, 256, 0, s>>>(a);
-  else if (a.hd == 64) qk_norm_rope_kernel<64><<<grid, 256, 0, s>>>(a);
-  else return cudaErrorInvalidValue;
+cudaError_t launch_bf16_to_f16(void* w, size_t elems, cudaStream_t s) {
+  if (elems == 0) return cudaSuccess;
+  const size_t pairs = elems / 2;
+  const size_t blocks = (pairs + 255) / 256;
+  bf16_to_f16_kernel<<<static_cast<unsigned>(blocks < 65536 ? blocks : 65536), 256, 0, s>>>(
+      reinterpret_cast<uint32_t*>(w), pairs);
   return cudaGetLastError();
 }
 

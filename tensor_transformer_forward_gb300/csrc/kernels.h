@@ -9,7 +9,24 @@
 namespace tpk {
 
 // ---------------- GEMM (tcgen05) ----------------
-enum GemmEpi : int { EPI_STORE = 0, EPI_SILU = 1, EPI_RESID = 2, EPI_ARGMAX = 3 };
+enum GemmEpi : int { EPI_STORE = 0, EPI_SILU = 1, EPI_RESID = 2, EPI_ARGMAX = 3, EPI_QKV = 4 };
+
+// Extra inputs of the merged-QKV epilogue: per-head RMSNorm of q and k, RoPE at
+// each token's position, K/V written to the rank's cache.
+struct QkvEpi {
+  int n, nq_l, nkv_l, hd, w_rank;
+  const void* q_norm;        // [hd] bf16
+  const void* k_norm;
+  float eps;
+  const float2* rope;        // [max_pos, hd/2] (cos, sin)
+  int max_pos;
+  const int32_t* cu_q;       // [B+1]
+  const int32_t* ctx_len;    // [B]
+  const int32_t* slot;       // [B]
+  int B;
+  void* kv;                  // cache [n][2][max_seqs][nkv_l][cap][hd]
+  int max_seqs, cap;
+};
 
 // Y[t, f] = sum over rank segments r of X[t, r*x_k_seg : +K_seg] . W[r*w_row_seg + f, 0 : K_seg]
 // X: [T, x_cols] bf16 row-major; W: [w_rows, K_seg] bf16 row-major ([out, in]).
@@ -35,10 +52,13 @@ struct GemmProblem {
   float* logits;    // optional fp32 [T, ld_logits]
   int ld_logits;
   int vocab;        // features >= vocab are masked out of the argmax
+  int32_t* out_ids; // argmax result per token (weight-streaming path: reduced in the kernel)
+  QkvEpi qkv;       // EPI_QKV only
 };
 
 struct GemmPlan {
   int BN;
+  bool swap;        // weights on the MMA's M side (few tokens): tiles of 128 features x BN tokens
   bool acc;         // running sum in registers (multi-segment or split-K)
   int tiles_t, tiles_f, splits;
   int grid;
@@ -56,23 +76,7 @@ cudaError_t launch_embed(const int32_t* ids, int T, const void* embed_stacked, i
                          int64_t vocab, int H, void* out, int* status, cudaStream_t s);
 cudaError_t launch_rmsnorm(const void* x, int64_t rows, int H, const void* w, float eps, void* out,
                            const int32_t* row_index, cudaStream_t s);
-struct RopeArgs {
-  void* qkv;                 // [T, n * w_rank] bf16, q rewritten in place
-  int T, n, nq_l, nkv_l, hd, w_rank;
-  const void* q_norm;        // [hd] bf16
-  const void* k_norm;
-  float eps;
-  const float2* rope;        // [max_pos, hd/2] (cos, sin)
-  int max_pos;
-  const int32_t* cu_q;       // [B+1]
-  const int32_t* ctx_len;    // [B]
-  const int32_t* slot;       // [B]
-  int B;
-  void* kv;                  // cache [n][2][max_seqs][nkv_l][cap][hd]
-  int max_seqs, cap;
-  int* status;
-};
-cudaError_t launch_qk_norm_rope(const RopeArgs& a, cudaStream_t s);
+
 
 struct AttnArgs {
   const void* qkv;           // [T, n * w_rank] (q post-RoPE)
@@ -100,5 +104,6 @@ cudaError_t launch_final_norm_select(const void* hidden, int H, const int32_t* c
 cudaError_t launch_argmax_reduce(const float* val, const int* idx, int tiles, int ld, int B, int32_t* out,
                                  cudaStream_t s);
 cudaError_t launch_wait_probe(const int* flag, int* status, long long limit_ns, cudaStream_t s);
+cudaError_t launch_bf16_to_f16(void* w, size_t elems, cudaStream_t s);
 
 }  // namespace tpk

@@ -82,9 +82,9 @@ class TPRunner:
     def step(self, batch: Batch, ids: Optional[torch.Tensor] = None, hidden: Optional[torch.Tensor] = None,
              out_ids: Optional[torch.Tensor] = None, out_logits: Optional[torch.Tensor] = None,
              layers: Optional[int] = None, run_head: bool = True) -> torch.Tensor:
-        """Embedding (when ids are given) -> layers -> head; returns hidden [T, H]."""
+        """Embedding (when ids are given) -> layers -> head; returns the fp32 residual stream [T, H]."""
         if hidden is None:
-            hidden = torch.empty(batch.num_tokens, self.cfg.hidden, dtype=torch.bfloat16, device="cuda")
+            hidden = torch.empty(batch.num_tokens, self.cfg.hidden, dtype=torch.float32, device="cuda")
             self.embed(ids, hidden)
         elif ids is not None:
             self.embed(ids, hidden)

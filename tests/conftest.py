@@ -16,6 +16,6 @@ def pytest_configure(config):
 @pytest.fixture(scope="session", autouse=True)
 def _built_libraries():
     """Build the native libraries in-tree (no-op when up to date)."""
-    from tensor_transformer_forward_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__._build_module().build()
     yield
