@@ -204,6 +204,24 @@ tp_status tp_decoder_layer_forward(tp_ctx* ctx, const void* layer_shards, const 
 tp_status tp_lm_head_argmax(tp_ctx* ctx, const void* head_shards, const tp_batch* batch, const void* hidden,
                             int32_t* out_ids, float* out_logits, int32_t* dev_status, void* stream);
 
+/* Same computation and results as tp_lm_head_argmax, for callers that cannot allocate device
+ * memory (and so cannot provide the workspace): code that must not call cudaMalloc at that
+ * point -- it can synchronise the device, or the process's device memory is owned by another
+ * allocator -- or a caller holding only the weights, its inputs and its outputs.  The pages have
+ * no counterpart; this is an interface convenience.
+ * Scratch lives in one fixed array compiled into the library (about 1.2 MiB, held on every GPU
+ * that loads the library until the process exits); no context workspace is needed and nothing
+ * is allocated.  Limits: num_seqs <= TP_STATIC_SCRATCH_MAX_SEQS and hidden <=
+ * TP_STATIC_SCRATCH_MAX_HIDDEN, else TP_ERR_INVALID_ARG before any launch.
+ * The first call on a device looks up the array's device address (with that device current);
+ * make that first call before any stream capture.  All calls share the array: calls that
+ * overlap on the GPU race and must not be issued; each call clears the part that must start
+ * at zero. */
+#define TP_STATIC_SCRATCH_MAX_SEQS 64
+#define TP_STATIC_SCRATCH_MAX_HIDDEN 8192
+tp_status tp_lm_head_argmax_static(tp_ctx* ctx, const void* head_shards, const tp_batch* batch, const void* hidden,
+                                   int32_t* out_ids, float* out_logits, int32_t* dev_status, void* stream);
+
 /* Synchronises the stream, reads the device status word and returns TP_OK,
  * TP_ERR_BAD_TOKEN or TP_ERR_TIMEOUT (the word is not cleared). */
 tp_status tp_read_status(const int32_t* dev_status, void* stream);

@@ -88,6 +88,7 @@ def _load() -> ctypes.CDLL:
         "tp_embed_vocab_parallel": ([P, P, P, I32, P, P, P], I32),
         "tp_decoder_layer_forward": ([P, P, ctypes.POINTER(TPBatch), P, P, I32, I32, P, P], I32),
         "tp_lm_head_argmax": ([P, P, ctypes.POINTER(TPBatch), P, P, P, P, P], I32),
+        "tp_lm_head_argmax_static": ([P, P, ctypes.POINTER(TPBatch), P, P, P, P, P], I32),
         "tp_read_status": ([P, P], I32),
         "tp_rank_sum_count": ([P, pI64], I32),
         "tp_workspace_part": ([P, I32, pSZ, pSZ], I32),
@@ -108,7 +109,7 @@ EXPORTED = ("tp_create", "tp_destroy", "tp_status_string", "tp_last_cuda_error",
             "tp_weights_bytes", "tp_weights_part", "tp_shard_weights", "tp_kv_cache_bytes", "tp_workspace_bytes",
             "tp_workspace_init", "tp_embed_vocab_parallel", "tp_decoder_layer_forward", "tp_lm_head_argmax",
             "tp_read_status", "tp_rank_sum_count", "tp_debug_wait_probe", "tp_workspace_part", "tp_launch_count",
-            "tp_profile_begin", "tp_profile_end")
+            "tp_profile_begin", "tp_profile_end", "tp_lm_head_argmax_static")
 KERNELS = ("embed", "rmsnorm", "gemm_qkv", "rope", "attn_prefill", "attn_decode", "gemm_o", "gemm_gate_up",
            "gemm_down", "final_norm", "gemm_lm_head", "argmax")
 
@@ -340,6 +341,18 @@ def tp_lm_head_argmax(ctx: Context, head_shards: torch.Tensor, batch: Batch, hid
     _check(_lib.tp_lm_head_argmax(ctx.handle, _dev(head_shards, "head_shards"), ctypes.byref(batch.c),
                                   _dev(hidden, "hidden", torch.float32), _dev(out_ids, "out_ids", torch.int32), lg,
                                   _dev(status, "status", torch.int32), _stream()), "tp_lm_head_argmax")
+
+
+def tp_lm_head_argmax_static(ctx: Context, head_shards: torch.Tensor, batch: Batch, hidden: torch.Tensor,
+                             out_ids: torch.Tensor, status: torch.Tensor,
+                             out_logits: Optional[torch.Tensor] = None) -> None:
+    """tp_lm_head_argmax without a workspace: for callers that cannot allocate
+    device memory; its scratch is a fixed array inside the library (see tpfwd.h)."""
+    lg = _dev(out_logits, "out_logits", torch.float32) if out_logits is not None else None
+    _check(_lib.tp_lm_head_argmax_static(ctx.handle, _dev(head_shards, "head_shards"), ctypes.byref(batch.c),
+                                         _dev(hidden, "hidden", torch.float32), _dev(out_ids, "out_ids", torch.int32),
+                                         lg, _dev(status, "status", torch.int32), _stream()),
+           "tp_lm_head_argmax_static")
 
 
 def tp_read_status(status: torch.Tensor) -> int:

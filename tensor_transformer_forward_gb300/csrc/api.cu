@@ -224,6 +224,21 @@ tp_status gemm(tp_ctx* x, int kind, const tpk::GemmProblem& pr, int32_t* dev_sta
 
 }  // namespace
 
+int tpk::ctx_head_view(tp_ctx* x, tpk::HeadView* out) {
+  if (!x || !out) return TP_ERR_INVALID_ARG;
+  const tp_status st = ensure_device(x);
+  if (st != TP_OK) return st;
+  out->H = x->H;
+  out->n = x->n;
+  out->vocab = x->c.vocab;
+  out->num_sms = x->num_sms;
+  out->v_l = x->v_l;
+  out->lm_head_off = x->lm_head.off;
+  out->final_norm_off = x->final_norm.off;
+  out->eps = x->c.rms_eps;
+  return TP_OK;
+}
+
 extern "C" {
 
 const char* tp_last_cuda_error(void) { return g_last_cuda_error; }

@@ -6,7 +6,18 @@
 #include <stddef.h>
 #include <stdint.h>
 
+struct tp_ctx;
+
 namespace tpk {
+
+// What the LM-head call needs to know about a context (filled by api.cu).
+struct HeadView {
+  int H, n, vocab, num_sms;
+  int64_t v_l;
+  size_t lm_head_off, final_norm_off;
+  float eps;
+};
+int ctx_head_view(tp_ctx* ctx, HeadView* out);  // returns a tp_status
 
 // ---------------- GEMM (tcgen05) ----------------
 enum GemmEpi : int { EPI_STORE = 0, EPI_SILU = 1, EPI_RESID = 2, EPI_ARGMAX = 3, EPI_QKV = 4 };
