@@ -154,8 +154,8 @@ tp_status tp_workspace_init(tp_ctx* ctx, void* ws, size_t ws_bytes, int32_t max_
 /* Intermediates of the last tp_decoder_layer_forward, inside the workspace (for tests and
  * debugging; valid until the next call): byte offset and size of
  *  TP_WS_NORMED  fp16 [T, H]                  RMSNorm output (post-attention norm after the call)
- *  TP_WS_QKV     fp16 [T, n, (nq_l+2nkv_l) hd] merged projection; its q heads hold post-RoPE q
- *                                              (k and v go straight to the cache)
+ *  TP_WS_QKV     [T, n, (nq_l+2nkv_l) hd]     merged projection; its q heads hold post-RoPE q
+ *                                              as bf16 (k and v go straight to the cache)
  *  TP_WS_ATTN    fp16 [T, n * nq_l * hd]      attention output (o_proj input)
  *  TP_WS_ACT     fp16 [T, n * I_p]            SiLU(gate) * up (down_proj input) */
 #define TP_WS_NORMED 0
@@ -180,7 +180,7 @@ typedef struct {
 /* A2: vocab-parallel embedding ([TP] VocabParallelEmbedding): per rank, ids inside its slice
  * are looked up and the others give 0; the rank outputs are summed (fixed rank order).
  * ids: device int32 [T]; hidden_out: device fp32 [T, H] (the residual stream is fp32; GEMM
- * and attention operands are fp16, the KV cache bf16).  Ids outside [0, V) give zero rows
+ * operands are fp16; attention runs on bf16 q and the bf16 KV cache).  Ids outside [0, V) give zero rows
  * and set TP_ERR_BAD_TOKEN in *dev_status (device int32, sticky, read by tp_read_status). */
 tp_status tp_embed_vocab_parallel(tp_ctx* ctx, const void* head_shards, const int32_t* ids, int32_t num_tokens,
                                   void* hidden_out, int32_t* dev_status, void* stream);

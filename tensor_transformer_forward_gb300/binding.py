@@ -247,13 +247,14 @@ class Context:
         self.workspace = ws
         return ws
 
-    def workspace_view(self, part: str, rows: int, cols: int) -> torch.Tensor:
-        """fp16 [rows, cols] view of an intermediate of the last layer call."""
+    def workspace_view(self, part: str, rows: int, cols: int, dtype=torch.float16) -> torch.Tensor:
+        """[rows, cols] view of an intermediate of the last layer call (fp16; the q
+        heads of the QKV buffer hold bf16)."""
         o, b = ctypes.c_size_t(), ctypes.c_size_t()
         _check(_lib.tp_workspace_part(self.handle, WS_PART[part], ctypes.byref(o), ctypes.byref(b)),
                "tp_workspace_part")
         assert rows * cols * 2 <= b.value
-        return self.workspace[o.value:o.value + rows * cols * 2].view(torch.float16).view(rows, cols)
+        return self.workspace[o.value:o.value + rows * cols * 2].view(dtype).view(rows, cols)
 
     def part_view(self, shards: torch.Tensor, part: str, shape: Sequence[int], dtype=torch.bfloat16) -> torch.Tensor:
         off, nbytes = self.weights_part(part)

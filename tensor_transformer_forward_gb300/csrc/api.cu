@@ -57,7 +57,7 @@ struct tp_ctx {
   char* ws = nullptr;
   size_t ws_bytes = 0;
   int ws_tokens = 0, ws_seqs = 0, ws_pos = 0;
-  Region r_rope, r_xn, r_qkv, r_attn, r_act, r_gpart, r_gcnt, r_apart, r_acnt, r_amax_v, r_amax_i, r_z, r_zidx;
+  Region r_rope, r_xn, r_qkv, r_qlo, r_attn, r_act, r_gpart, r_gcnt, r_apart, r_acnt, r_amax_v, r_amax_i, r_z, r_zidx;
   int lm_tiles_max = 0;
   int num_sms = 0;
   int64_t rank_sums = 0;
@@ -135,7 +135,7 @@ void lay_out(tp_ctx* x) {
 }
 
 struct WsPlan {
-  Region rope, xn, qkv, attn, act, gpart, gcnt, apart, acnt, amax_v, amax_i, z, zidx;
+  Region rope, xn, qkv, qlo, attn, act, gpart, gcnt, apart, acnt, amax_v, amax_i, z, zidx;
   size_t total = 0;
   int lm_tiles = 0;
 };
@@ -152,6 +152,7 @@ WsPlan plan_ws(const tp_ctx* x, int64_t T, int64_t B, int64_t P) {
   take(w.rope, static_cast<size_t>(P) * (x->hd / 2) * 8);
   take(w.xn, T * H * 2);
   take(w.qkv, T * n * x->w_rank * 2);
+  take(w.qlo, T * n * x->nq_l * x->hd * 2);
   take(w.attn, T * n * x->nq_l * x->hd * 2);
   take(w.act, T * n * x->i_p * 2);
   take(w.gpart, static_cast<size_t>(kMaxSms) * 128 * 128 * 4);
@@ -481,7 +482,7 @@ tp_status tp_workspace_init(tp_ctx* x, void* ws, size_t ws_bytes, int32_t max_to
   x->ws_tokens = max_tokens;
   x->ws_seqs = max_seqs;
   x->ws_pos = max_positions;
-  x->r_rope = w.rope; x->r_xn = w.xn; x->r_qkv = w.qkv; x->r_attn = w.attn; x->r_act = w.act;
+  x->r_rope = w.rope; x->r_xn = w.xn; x->r_qkv = w.qkv; x->r_qlo = w.qlo; x->r_attn = w.attn; x->r_act = w.act;
   x->r_gpart = w.gpart; x->r_gcnt = w.gcnt; x->r_apart = w.apart; x->r_acnt = w.acnt;
   x->r_amax_v = w.amax_v; x->r_amax_i = w.amax_i; x->r_z = w.z; x->r_zidx = w.zidx;
   x->lm_tiles_max = w.lm_tiles;
@@ -553,12 +554,13 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   g.qkv.rope = reinterpret_cast<const float2*>(x->ws + x->r_rope.off); g.qkv.max_pos = x->ws_pos;
   g.qkv.cu_q = b->cu_q; g.qkv.ctx_len = b->ctx_len; g.qkv.slot = b->slot; g.qkv.B = b->num_seqs;
   g.qkv.kv = kv; g.qkv.max_seqs = kv_max_seqs; g.qkv.cap = kv_cap;
+  g.qkv.num_prefill = b->num_prefill; g.qkv.q_lo = x->ws + x->r_qlo.off;
   st = gemm(x, TP_K_GEMM_QKV, g, dev_status, s);
   if (st != TP_OK) return st;
 
   // A6: per-rank attention
   tpk::AttnArgs aa{};
-  aa.qkv = qkv; aa.n = n; aa.nq_l = x->nq_l; aa.nkv_l = x->nkv_l; aa.hd = x->hd; aa.w_rank = x->w_rank;
+  aa.qkv = qkv; aa.q_lo = x->ws + x->r_qlo.off; aa.T = T; aa.n = n; aa.nq_l = x->nq_l; aa.nkv_l = x->nkv_l; aa.hd = x->hd; aa.w_rank = x->w_rank;
   aa.kv = kv; aa.max_seqs = kv_max_seqs; aa.cap = kv_cap;
   aa.cu_q = b->cu_q; aa.ctx_len = b->ctx_len; aa.slot = b->slot;
   aa.max_q_len = b->max_q_len; aa.max_kv_len = b->max_kv_len; aa.out = attn;

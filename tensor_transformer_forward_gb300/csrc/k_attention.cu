@@ -5,9 +5,11 @@
 // scores are scaled by 1/sqrt(hd); new token j of a sequence with ctx cached
 // tokens sees keys 0 .. ctx + j.  Softmax in fp32 (base-2, max-subtracted).
 //
-// Cache layout (per layer): [n][2 (K, V)][max_seqs][nkv_l][cap][hd] bf16.
-// q comes from the merged QKV buffer (fp16).  Output layout: [T][n * nq_l * hd]
-// fp16 (rank-major heads, the row-split o_proj operand).
+// Cache layout (per layer): [n][2 (K, V)][max_seqs][nkv_l][cap][hd] bf16.  q comes
+// from the merged QKV buffer: fp16 for decode tokens (fp32 math), bf16 high +
+// low parts for prefill tokens (bf16 tensor-core operands next to the bf16
+// cache).  Output layout: [T][n * nq_l * hd] fp16 (rank-major heads, the
+// row-split o_proj operand).
 #include <climits>
 
 #include "kernels.h"
@@ -232,260 +234,328 @@ cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s) {
 
 // ---------------------------------------------------------------------------
 // Prefill (several new tokens per sequence, causal with cache offset):
-// flash-attention style on the tensor cores with m16n8k16 fp16 MMA (fp32
-// accumulate).  One CTA = 64 queries of one (sequence, rank, q head), 4 warps
-// x 16 query rows; K/V blocks of 64 keys double-buffered in shared memory by
-// cp.async (rows beyond the sequence zero-filled), converted from the bf16
-// cache to fp16 in place (exact in fp16's normal range).
+// flash attention on the tcgen05 tensor cores.  One CTA = 128 queries of one
+// (sequence, rank, q head); 192 threads:
+//   warp 0      TMA: the Q tiles once (bf16 high and low parts), then K and V
+//               blocks of 128 keys from the rank's bf16 cache into a 2-stage
+//               shared-memory ring.
+//   warp 1      TMEM allocation + one MMA-issuing thread: S(j) = Q K(j)^T
+//               (as Q_hi K^T + Q_lo K^T, so q keeps ~16 significant bits) into
+//               one of two TMEM score buffers, then O += P(j) V(j) into the TMEM
+//               output accumulator (P from shared memory, V as an MN-major
+//               operand straight from the TMA tile).
+//   warps 2-5   softmax: one query row per thread (its TMEM lane) -- scale,
+//               causal mask, row max, exp2, row sum; P(j) written to shared
+//               memory in the swizzled K-major layout the MMA reads; the running
+//               output is rescaled only when the row max has grown by more than
+//               2^8 (otherwise P may exceed 1 by at most 2^8, exactly
+//               compensated by the row sum); final O / l written as fp16.
+// All waits are bounded (TP_WAIT_LIMIT_NS) and end in TP_DEVFLAG_TIMEOUT.
+// Cache positions never written must hold finite values (the runner zeroes the
+// cache once): keys past the sequence get P = 0, but 0 * NaN would not vanish.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 template <int HD>
-struct PrefillCfg {
-  static constexpr int BQ = 64, BK = 64;
-  static constexpr int LD = HD + 8;  // padded smem row (elements): conflict-free ldmatrix
-  static constexpr int TILE = BK * LD;
-  static constexpr int SMEM = (BQ * LD + 4 * TILE) * 2;
+struct FaCfg {
+  static constexpr int BQ = 128, BKV = 128;
+  static constexpr int NSUB = HD / 64;            // 64-column (128-byte) sub-tiles per row
+  static constexpr int SUB_BYTES = 128 * 128;     // one [128 rows][64] bf16 sub-tile
+  static constexpr int TILE_BYTES = NSUB * SUB_BYTES;
+  static constexpr int STAGES = 2;
+  static constexpr int Q_OFF = 0;                                  // [hi | lo]
+  static constexpr int KV_OFF = 2 * TILE_BYTES;                    // [stage][K | V]
+  static constexpr int P_OFF = KV_OFF + STAGES * 2 * TILE_BYTES;   // [2 sub-tiles of 64 keys]
+  static constexpr int BAR_OFF = P_OFF + 2 * SUB_BYTES;
+  static constexpr int SMEM = 1024 + BAR_OFF + 256;
+  static constexpr int S_COL = 0;      // two score buffers: columns [0,128) and [128,256)
+  static constexpr int O_COL = 256;    // output accumulator: columns [256, 256+HD)
 };
 
 template <int HD>
-__global__ void __launch_bounds__(128) attn_prefill_kernel(AttnArgs a) {
-  using C = PrefillCfg<HD>;
-  constexpr int BQ = C::BQ, BK = C::BK, LD = C::LD;
-  constexpr int KSTEPS = HD / 16;  // k-steps of the QK^T product
-  constexpr int NT_O = HD / 8;     // n-tiles of the output
-  extern __shared__ __align__(16) __half sm[];
-  __half* sQ = sm;
-  __half* sK = sm + BQ * LD;          // [2][BK][LD]
-  __half* sV = sK + 2 * C::TILE;      // [2][BK][LD]
+__global__ void __launch_bounds__(192, 1)
+    attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQlo,
+                           const __grid_constant__ CUtensorMap tmKV, const AttnArgs a) {
+  using C = FaCfg<HD>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  // barriers: 0 q_full | 1,2 kv_full | 3,4 kv_empty | 5,6 s_full | 7,8 s_empty | 9 p_full | 10 o_done | 11 drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+#define B_Q (bar0)
+#define B_KVF(s) (bar0 + 8u * (1 + (s)))
+#define B_KVE(s) (bar0 + 8u * (3 + (s)))
+#define B_SF(b) (bar0 + 8u * (5 + (b)))
+#define B_SE(b) (bar0 + 8u * (7 + (b)))
+#define B_PF (bar0 + 8u * 9)
+#define B_OD (bar0 + 8u * 10)
+#define B_DR (bar0 + 8u * 11)
 
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = a.seq_begin + blockIdx.z;
   const int qlen = a.cu_q[b + 1] - a.cu_q[b];
-  const int q0 = (gridDim.x - 1 - blockIdx.x) * BQ;  // heaviest blocks first
-  if (q0 >= qlen) return;
+  const int q0 = (gridDim.x - 1 - blockIdx.x) * C::BQ;  // heaviest blocks first
+  if (q0 >= qlen) return;                                // uniform: before any barrier or TMEM use
   const int hg = blockIdx.y;
   const int r = hg / a.nq_l, h = hg % a.nq_l;
-  const int G = a.nq_l / a.nkv_l;
-  const int g = h / G;
+  const int g = h / (a.nq_l / a.nkv_l);
   const int ctx = a.ctx_len[b];
   const int tbase = a.cu_q[b];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kend = ctx + min(q0 + C::BQ, qlen);          // keys this CTA needs: [0, kend)
+  const int nblk = (kend + C::BKV - 1) / C::BKV;
+  const int slot = a.slot[b];
+  const int krow0 = (((r * 2 + 0) * a.max_seqs + slot) * a.nkv_l + g) * a.cap;
+  const int vrow0 = (((r * 2 + 1) * a.max_seqs + slot) * a.nkv_l + g) * a.cap;
 
-  const size_t plane = static_cast<size_t>(a.max_seqs) * a.nkv_l * a.cap * HD;
-  const size_t head_off = (static_cast<size_t>(a.slot[b]) * a.nkv_l + g) * a.cap * HD;
-  const __nv_bfloat16* Kc = reinterpret_cast<const __nv_bfloat16*>(a.kv) + (2 * static_cast<size_t>(r)) * plane + head_off;
-  const __nv_bfloat16* Vc = reinterpret_cast<const __nv_bfloat16*>(a.kv) + (2 * static_cast<size_t>(r) + 1) * plane + head_off;
-
-  // Q tile
-  constexpr int CPR = HD / 8;  // 16-byte chunks per row
-  for (int c = threadIdx.x; c < BQ * CPR; c += 128) {
-    const int row = c / CPR, col = (c % CPR) * 8;
-    const int qi = q0 + row;
-    const __half* src = reinterpret_cast<const __half*>(a.qkv) +
-                        static_cast<size_t>(tbase + min(qi, qlen - 1)) * a.n * a.w_rank +
-                        static_cast<size_t>(r) * a.w_rank + h * HD + col;
-    cp_async16(smem_u32(sQ + row * LD + col), src, qi < qlen);
-  }
-  const int kend = ctx + min(q0 + BQ, qlen);  // keys needed by this CTA
-  const int nblocks = (kend + BK - 1) / BK;
-  auto load_kv = [&](int blk, int buf) {
-    for (int c = threadIdx.x; c < BK * CPR; c += 128) {
-      const int row = c / CPR, col = (c % CPR) * 8;
-      const int key = blk * BK + row;
-      const bool ok = key < kend;
-      const size_t off = static_cast<size_t>(ok ? key : 0) * HD + col;
-      cp_async16(smem_u32(sK + buf * C::TILE + row * LD + col), Kc + off, ok);
-      cp_async16(smem_u32(sV + buf * C::TILE + row * LD + col), Vc + off, ok);
+  if (threadIdx.x == 0) {
+    mbar_init(B_Q, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(B_KVF(s), 1);
+      mbar_init(B_KVE(s), 1);
     }
-  };
-  // the chunks this thread loaded, turned from bf16 into fp16 in place once they landed
-  auto convert_kv = [&](int buf) {
-    for (int c = threadIdx.x; c < BK * CPR; c += 128) {
-      const int row = c / CPR, col = (c % CPR) * 8;
-      uint4* pk = reinterpret_cast<uint4*>(sK + buf * C::TILE + row * LD + col);
-      uint4* pv = reinterpret_cast<uint4*>(sV + buf * C::TILE + row * LD + col);
-      uint4 k = *pk, v = *pv;
-      k.x = pack_f16x2(bf16lo(k.x), bf16hi(k.x)); k.y = pack_f16x2(bf16lo(k.y), bf16hi(k.y));
-      k.z = pack_f16x2(bf16lo(k.z), bf16hi(k.z)); k.w = pack_f16x2(bf16lo(k.w), bf16hi(k.w));
-      v.x = pack_f16x2(bf16lo(v.x), bf16hi(v.x)); v.y = pack_f16x2(bf16lo(v.y), bf16hi(v.y));
-      v.z = pack_f16x2(bf16lo(v.z), bf16hi(v.z)); v.w = pack_f16x2(bf16lo(v.w), bf16hi(v.w));
-      *pk = k;
-      *pv = v;
-    }
-  };
-  load_kv(0, 0);
-  cp_async_commit();
-
-  float o[NT_O][4];
-#pragma unroll
-  for (int i = 0; i < NT_O; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.0f, 0.0f};
-  uint32_t qa[KSTEPS][4];
-  const int qrow0 = q0 + warp * 16 + (lane >> 2);  // query index of c0/c1; +8 for c2/c3
-
-  for (int blk = 0; blk < nblocks; ++blk) {
-    const int buf = blk & 1;
-    if (blk + 1 < nblocks) load_kv(blk + 1, buf ^ 1);
-    cp_async_commit();
-    cp_async_wait<1>();
-    convert_kv(buf);
-    __syncthreads();
-    if (blk == 0) {
-#pragma unroll
-      for (int kk = 0; kk < KSTEPS; ++kk) {
-        const uint32_t addr = smem_u32(sQ + (warp * 16 + (lane & 15)) * LD + kk * 16 + (lane >> 4) * 8);
-        ldsm_x4(addr, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-      }
-    }
-    // S = Q K^T for 64 keys: 8 n-tiles of 8 keys
-    float s[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.0f;
-    const __half* kt = sK + buf * C::TILE;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int kk = 0; kk < KSTEPS; kk += 2) {
-        uint32_t b0, b1, b2, b3;
-        const uint32_t addr = smem_u32(kt + (j * 8 + (lane & 7)) * LD + kk * 16 + (lane >> 3) * 8);
-        ldsm_x4(addr, b0, b1, b2, b3);
-        mma16816(s[j], qa[kk], b0, b1);
-        mma16816(s[j], qa[kk + 1], b2, b3);
-      }
-    }
-    // scale, mask, online softmax (exp2 domain)
-    float bmax[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = blk * BK + j * 8 + (lane & 3) * 2 + (e & 1);
-        const int qi = qrow0 + (e >> 1) * 8;
-        const bool vis = (qi < qlen) && (key <= ctx + qi);
-        const float v = vis ? s[j][e] * a.scale_log2 : -INFINITY;
-        s[j][e] = v;
-        bmax[e >> 1] = fmaxf(bmax[e >> 1], v);
-      }
-    }
-    float corr[2], mbase[2];
-#pragma unroll
     for (int i = 0; i < 2; ++i) {
-      bmax[i] = fmaxf(bmax[i], __shfl_xor_sync(0xffffffffu, bmax[i], 1));
-      bmax[i] = fmaxf(bmax[i], __shfl_xor_sync(0xffffffffu, bmax[i], 2));
-      const float mn = fmaxf(mrow[i], bmax[i]);
-      mbase[i] = (mn == -INFINITY) ? 0.0f : mn;
-      corr[i] = exp2f(mrow[i] - mbase[i]);
-      mrow[i] = mn;
+      mbar_init(B_SF(i), 1);
+      mbar_init(B_SE(i), 4);
     }
-    float psum[2] = {0.0f, 0.0f};
-    uint32_t pa[4][4];  // P as A fragments: 4 k-steps of 16 keys
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float p0 = exp2f(s[j][0] - mbase[0]), p1 = exp2f(s[j][1] - mbase[0]);
-      const float p2 = exp2f(s[j][2] - mbase[1]), p3 = exp2f(s[j][3] - mbase[1]);
-      psum[0] += p0 + p1;
-      psum[1] += p2 + p3;
-      __half2 h01 = __floats2half2_rn(p0, p1), h23 = __floats2half2_rn(p2, p3);  // P in [0, 1]
-      pa[j >> 1][(j & 1) * 2 + 0] = *reinterpret_cast<uint32_t*>(&h01);
-      pa[j >> 1][(j & 1) * 2 + 1] = *reinterpret_cast<uint32_t*>(&h23);
+    mbar_init(B_PF, 4);
+    mbar_init(B_OD, 1);
+    mbar_init(B_DR, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmQlo);
+      tma_prefetch_desc(&tmKV);
+      const int qcol = r * a.w_rank + h * HD;
+      const int qlo_col = (r * a.nq_l + h) * HD;
+      mbar_arrive_expect_tx(B_Q, 2 * C::TILE_BYTES);
+      for (int s = 0; s < C::NSUB; ++s) {
+        tma_load_2d(smem_u32(smem + C::Q_OFF + s * C::SUB_BYTES), &tmQ, B_Q, qcol + s * 64, tbase + q0);
+        tma_load_2d(smem_u32(smem + C::Q_OFF + C::TILE_BYTES + s * C::SUB_BYTES), &tmQlo, B_Q, qlo_col + s * 64,
+                    tbase + q0);
+      }
+      int issued = 0;
+      for (int j = 0; j < nblk; ++j) {
+        const int st = j % STAGES;
+        if (!mbar_wait(B_KVE(st), ((j / STAGES) & 1) ^ 1u, abort_flag, a.status)) break;
+        uint8_t* kt = smem + C::KV_OFF + st * 2 * C::TILE_BYTES;
+        mbar_arrive_expect_tx(B_KVF(st), 2 * C::TILE_BYTES);
+        for (int s = 0; s < C::NSUB; ++s) {
+          tma_load_2d(smem_u32(kt + s * C::SUB_BYTES), &tmKV, B_KVF(st), s * 64, krow0 + j * C::BKV);
+          tma_load_2d(smem_u32(kt + C::TILE_BYTES + s * C::SUB_BYTES), &tmKV, B_KVF(st), s * 64,
+                      vrow0 + j * C::BKV);
+        }
+        issued = j + 1;
+      }
+      mbar_wait(B_Q, 0, nullptr, a.status);
+      for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j)
+        mbar_wait(B_KVF(j % STAGES), (j / STAGES) & 1, nullptr, a.status);
     }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, C::BKV);      // S = Q K^T: both K-major
+      const uint32_t id_o = idesc_bf16_f32(128, HD, true);    // O += P V: V MN-major
+      bool ok = mbar_wait(B_Q, 0, abort_flag, a.status);
+      tc_fence_after();
+      auto pv = [&](int j) -> bool {  // O += P(j) V(j)
+        if (!mbar_wait(B_PF, j & 1, abort_flag, a.status)) return false;
+        tc_fence_after();
+        const int st = j % STAGES;
+        const uint32_t vt = smem_u32(smem + C::KV_OFF + st * 2 * C::TILE_BYTES + C::TILE_BYTES);
+        const uint32_t pt = smem_u32(smem + C::P_OFF);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      psum[i] += __shfl_xor_sync(0xffffffffu, psum[i], 1);
-      psum[i] += __shfl_xor_sync(0xffffffffu, psum[i], 2);
-      lrow[i] = lrow[i] * corr[i] + psum[i];
+        for (int kk = 0; kk < C::BKV / 16; ++kk) {
+          const uint64_t ad = sdesc_k_sw128(pt + (kk >> 2) * C::SUB_BYTES) + 2ull * (kk & 3);
+          const uint64_t bd = sdesc_mn_sw128(vt + kk * 16 * 128, C::SUB_BYTES, 1024);
+          tc_mma_f16(tmem + C::O_COL, ad, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(B_OD);
+        tc_commit(B_KVE(st));
+        return true;
+      };
+      for (int j = 0; ok && j < nblk; ++j) {
+        const int st = j % STAGES, sb = j & 1;
+        if (!mbar_wait(B_KVF(st), (j / STAGES) & 1, abort_flag, a.status)) { ok = false; break; }
+        if (!mbar_wait(B_SE(sb), ((j >> 1) & 1) ^ 1u, abort_flag, a.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t qt = smem_u32(smem + C::Q_OFF);
+        const uint32_t kt = smem_u32(smem + C::KV_OFF + st * 2 * C::TILE_BYTES);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {  // S = Q_hi K^T + Q_lo K^T
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint64_t ad = sdesc_k_sw128(qt + part * C::TILE_BYTES + (kk >> 2) * C::SUB_BYTES) + 2ull * (kk & 3);
+            const uint64_t bd = sdesc_k_sw128(kt + (kk >> 2) * C::SUB_BYTES) + 2ull * (kk & 3);
+            tc_mma_f16(tmem + C::S_COL + sb * 128, ad, bd, id_s, (part > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        tc_commit(B_SF(sb));
+        if (j > 0 && !pv(j - 1)) { ok = false; break; }
+      }
+      if (ok) pv(nblk - 1);
+      tc_commit(B_DR);  // completes after every MMA above
+      mbar_wait(B_DR, 0, nullptr, a.status);
     }
+  } else {
+    // ---------------- softmax / output (warps 2..5) ----------------
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int qi = q0 + row;                    // query index within the sequence
+    const bool row_ok = qi < qlen;
+    const int last_key = ctx + qi;              // keys <= last_key are visible
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    uint8_t* prow = smem + C::P_OFF + row * 128;
+    float m_used = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < nblk; ++j) {
+      const int sb = j & 1;
+      if (!mbar_wait(B_SF(sb), (j >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+      tc_fence_after();
+      float sv[128];
 #pragma unroll
-    for (int i = 0; i < NT_O; ++i) {
-      o[i][0] *= corr[0];
-      o[i][1] *= corr[0];
-      o[i][2] *= corr[1];
-      o[i][3] *= corr[1];
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tc_ld32(lane_addr + C::S_COL + sb * 128 + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[c * 32 + i] = v[i];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B_SE(sb));
+      const int key0 = j * C::BKV;
+      const bool need_mask = (key0 + C::BKV - 1 > ctx + q0) || !row_ok;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        float x = sv[i] * a.scale_log2;
+        if (need_mask && (!row_ok || key0 + i > last_key)) x = -INFINITY;
+        sv[i] = x;
+        mx = fmaxf(mx, x);
+      }
+      // P buffer and O are free once the previous block's PV has completed
+      if (j > 0 && !mbar_wait(B_OD, (j - 1) & 1, abort_flag, a.status)) { ok = false; break; }
+      tc_fence_after();
+      if (mx > m_used + 8.0f) {
+        if (j > 0 && m_used != -INFINITY) {
+          const float corr = exp2f(m_used - mx);
+          l *= corr;
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            float v[32];
+            tc_ld32(lane_addr + C::O_COL + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= corr;
+            tc_st32(lane_addr + C::O_COL + c * 32, v);
+          }
+        }
+        m_used = mx;
+      }
+      const float mb = m_used == -INFINITY ? 0.0f : m_used;
+      float psum = 0.0f;
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {  // 16-byte chunks of 8 keys
+        float p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          p[i] = exp2f(sv[ch * 8 + i] - mb);
+          psum += p[i];
+        }
+        uint4 w;
+        w.x = pack_bf16x2(p[0], p[1]);
+        w.y = pack_bf16x2(p[2], p[3]);
+        w.z = pack_bf16x2(p[4], p[5]);
+        w.w = pack_bf16x2(p[6], p[7]);
+        const int sub = ch >> 3, c8 = ch & 7;
+        *reinterpret_cast<uint4*>(prow + sub * C::SUB_BYTES + ((c8 ^ (row & 7)) << 4)) = w;
+      }
+      l += psum;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B_PF);
     }
-    // O += P V
-    const __half* vt = sV + buf * C::TILE;
+    if (ok && mbar_wait(B_OD, (nblk - 1) & 1, abort_flag, a.status)) {
+      tc_fence_after();
+      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+      __half* orow = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(tbase + (row_ok ? qi : 0)) * a.n * a.nq_l * HD +
+                     (static_cast<size_t>(r) * a.nq_l + h) * HD;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t afr[4] = {pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3]};
+      for (int c = 0; c < HD / 32; ++c) {
+        float v[32];
+        tc_ld32(lane_addr + C::O_COL + c * 32, v);
+        if (row_ok) {
 #pragma unroll
-      for (int nt = 0; nt < NT_O; nt += 2) {
-        uint32_t b0, b1, b2, b3;
-        const uint32_t addr =
-            smem_u32(vt + (kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LD + nt * 8 + (lane >> 4) * 8);
-        ldsm_x4_t(addr, b0, b1, b2, b3);
-        mma16816(o[nt], afr, b0, b1);
-        mma16816(o[nt + 1], afr, b2, b3);
+          for (int k = 0; k < 4; ++k) {
+            uint4 w;
+            w.x = pack_f16x2(v[k * 8 + 0] * inv, v[k * 8 + 1] * inv);
+            w.y = pack_f16x2(v[k * 8 + 2] * inv, v[k * 8 + 3] * inv);
+            w.z = pack_f16x2(v[k * 8 + 4] * inv, v[k * 8 + 5] * inv);
+            w.w = pack_f16x2(v[k * 8 + 6] * inv, v[k * 8 + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + k * 8) = w;
+          }
+        }
       }
     }
-    __syncthreads();
   }
-  // normalise and store
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int qi = qrow0 + i * 8;
-    if (qi >= qlen) continue;
-    const float inv = 1.0f / lrow[i];
-    __half* orow = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(tbase + qi) * a.n * a.nq_l * HD +
-                   (static_cast<size_t>(r) * a.nq_l + h) * HD;
-#pragma unroll
-    for (int nt = 0; nt < NT_O; ++nt) {
-      const int d = nt * 8 + (lane & 3) * 2;
-      *reinterpret_cast<uint32_t*>(orow + d) = pack_f16x2(o[nt][i * 2] * inv, o[nt][i * 2 + 1] * inv);
-    }
+#undef B_Q
+#undef B_KVF
+#undef B_KVE
+#undef B_SF
+#undef B_SE
+#undef B_PF
+#undef B_OD
+#undef B_DR
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
   }
+}
+
+template <int HD>
+static cudaError_t launch_prefill_hd(const AttnArgs& a, cudaStream_t s) {
+  using C = FaCfg<HD>;
+  const int64_t w_cols = static_cast<int64_t>(a.n) * a.w_rank;
+  const int64_t kv_rows = static_cast<int64_t>(a.n) * 2 * a.max_seqs * a.nkv_l * a.cap;
+  if (kv_rows >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+  const int64_t q_cols = static_cast<int64_t>(a.n) * a.nq_l * HD;
+  CUtensorMap mq, mqlo, mkv;
+  if (!make_tmap_2d(&mq, a.qkv, a.T, w_cols, w_cols, 128, true)) return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&mqlo, a.q_lo, a.T, q_cols, q_cols, 128, true)) return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&mkv, a.kv, kv_rows, HD, HD, 128, true)) return cudaErrorInvalidValue;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_prefill_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid((a.max_q_len + C::BQ - 1) / C::BQ, a.n * a.nq_l, a.seq_end - a.seq_begin);
+  attn_prefill_tc_kernel<HD><<<grid, 192, C::SMEM, s>>>(mq, mqlo, mkv, a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_attention_prefill(const AttnArgs& a, cudaStream_t s) {
   const int seqs = a.seq_end - a.seq_begin;
   if (seqs <= 0 || a.max_q_len <= 0) return cudaSuccess;
-  dim3 grid((a.max_q_len + 63) / 64, a.n * a.nq_l, seqs);
-  if (a.hd == 128) {
-    constexpr int smem = PrefillCfg<128>::SMEM;
-    static bool attr = false;
-    if (!attr) {
-      cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
-    attn_prefill_kernel<128><<<grid, 128, smem, s>>>(a);
-  } else if (a.hd == 64) {
-    constexpr int smem = PrefillCfg<64>::SMEM;
-    static bool attr = false;
-    if (!attr) {
-      cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
-    attn_prefill_kernel<64><<<grid, 128, smem, s>>>(a);
-  } else {
-    return cudaErrorNotSupported;
-  }
-  return cudaGetLastError();
+  if (a.hd == 128) return launch_prefill_hd<128>(a, s);
+  if (a.hd == 64) return launch_prefill_hd<64>(a, s);
+  return cudaErrorNotSupported;
 }
 
 }  // namespace tpk

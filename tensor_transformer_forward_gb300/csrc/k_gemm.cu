@@ -177,7 +177,7 @@ __device__ __forceinline__ void argmax_scan(const GemmParams& p, int t, int f, c
 // Token row t -> its sequence, position and cache slot (binary search over cu_q).
 struct TokPos {
   int pos, seq_slot;
-  bool ok;
+  bool ok, prefill;
 };
 __device__ __forceinline__ TokPos token_position(const QkvEpi& q, int t) {
   int lo = 0, hi = q.B - 1;
@@ -190,6 +190,7 @@ __device__ __forceinline__ TokPos token_position(const QkvEpi& q, int t) {
   tp.pos = q.ctx_len[lo] + (t - q.cu_q[lo]);
   tp.seq_slot = q.slot[lo];
   tp.ok = tp.pos >= 0 && tp.pos < q.cap && tp.pos < q.max_pos;
+  tp.prefill = lo < q.num_prefill;
   return tp;
 }
 
@@ -221,7 +222,13 @@ __device__ __forceinline__ void qkv_head(const GemmParams& p, int t, const TokPo
   const float inv = rsqrtf(ss / static_cast<float>(HD) + q.eps);
   const __nv_bfloat16* nw = reinterpret_cast<const __nv_bfloat16*>(is_q ? q.q_norm : q.k_norm);
   const float2* cs = q.rope + static_cast<size_t>(tp.pos) * HALF;
-  __half* qdst = reinterpret_cast<__half*>(p.out) + static_cast<size_t>(t) * p.ldo + col0;       // q: fp16 operand
+  // q of a prefill token: bf16 high part in the QKV buffer and the bf16 low part
+  // q - bf16(q) in q_lo (the tensor-core attention multiplies both with the bf16
+  // keys); q of a decode token: fp16 in the QKV buffer (fp32 attention math).
+  __nv_bfloat16* qhi = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(t) * p.ldo + col0;
+  __half* q16 = reinterpret_cast<__half*>(qhi);
+  __nv_bfloat16* qlo = reinterpret_cast<__nv_bfloat16*>(q.q_lo) +
+                       static_cast<size_t>(t) * q.n * q.nq_l * HD + (static_cast<size_t>(r) * q.nq_l + sh) * HD;
   __nv_bfloat16* kdst = kv + (2 * static_cast<size_t>(r)) * plane +                                // k: bf16 cache
                         ((static_cast<size_t>(tp.seq_slot) * q.nkv_l + (sh - q.nq_l)) * q.cap + tp.pos) * HD;
 #pragma unroll
@@ -236,12 +243,23 @@ __device__ __forceinline__ void qkv_head(const GemmParams& p, int t, const TokPo
       y0[i] = u0 * c.x - u1 * c.y;
       y1[i] = u1 * c.x + u0 * c.y;
     }
-    if (is_q) {
-      store8(qdst + j * 8, y0);
-      store8(qdst + HALF + j * 8, y1);
-    } else {
+    if (!is_q) {
       store8(kdst + j * 8, y0);
       store8(kdst + HALF + j * 8, y1);
+    } else if (!tp.prefill) {
+      store8(q16 + j * 8, y0);
+      store8(q16 + HALF + j * 8, y1);
+    } else {
+      float l0[8], l1[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        l0[i] = y0[i] - bf2f(f2bf(y0[i]));
+        l1[i] = y1[i] - bf2f(f2bf(y1[i]));
+      }
+      store8(qhi + j * 8, y0);
+      store8(qhi + HALF + j * 8, y1);
+      store8(qlo + j * 8, l0);
+      store8(qlo + HALF + j * 8, l1);
     }
   }
 }
@@ -688,18 +706,22 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D fp16 row-major tensor [rows, cols] (row stride ld elements), box 64 x box_rows, 128 B swizzle.
-static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+// 2D 16-bit row-major tensor [rows, cols] (row stride ld elements), box 64 x box_rows, 128 B swizzle.
+bool make_tmap_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows, bool bf16) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
   cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  return make_tmap_2d(m, base, rows, cols, ld, box_rows, false);
 }
 
 static inline int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }

@@ -2,6 +2,7 @@
 // Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -37,6 +38,8 @@ struct QkvEpi {
   int B;
   void* kv;                  // cache [n][2][max_seqs][nkv_l][cap][hd]
   int max_seqs, cap;
+  int num_prefill;           // sequences [0, num_prefill): q as bf16 hi + lo parts; later ones: q as fp16
+  void* q_lo;                // bf16 [T, n * nq_l * hd]: q - bf16(q) of prefill tokens
 };
 
 // Y[t, f] = sum over rank segments r of X[t, r*x_k_seg : +K_seg] . W[r*w_row_seg + f, 0 : K_seg]
@@ -77,6 +80,9 @@ struct GemmPlan {
 };
 
 GemmPlan plan_gemm(const GemmProblem& pr, int num_sms);
+// TMA descriptor of a 2D 16-bit row-major tensor, box 64 columns x box_rows, 128-byte swizzle.
+bool make_tmap_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows,
+                  bool bf16);
 // workspace: partials (fp32) and per-tile counters (int, zeroed once, self-resetting)
 cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& plan, float* partials, int* counters,
                         int* status, cudaStream_t stream);
@@ -90,7 +96,9 @@ cudaError_t launch_rmsnorm(const void* x, int64_t rows, int H, const void* w, fl
 
 
 struct AttnArgs {
-  const void* qkv;           // [T, n * w_rank] (q post-RoPE)
+  const void* qkv;           // [T, n * w_rank] (q post-RoPE: bf16 high part for prefill tokens, fp16 for decode)
+  const void* q_lo;          // [T, n * nq_l * hd] bf16 low part of q (prefill tokens)
+  int T;                     // rows of qkv
   int n, nq_l, nkv_l, hd, w_rank;
   const void* kv;            // cache [n][2][max_seqs][nkv_l][cap][hd]
   int max_seqs, cap;

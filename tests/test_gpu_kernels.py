@@ -163,7 +163,7 @@ def test_layer_intermediates_match_oracle_trace(n):
     ctx = g.runner.ctx
     nq_l, nkv_l = s.num_q_heads // n, s.num_kv_heads // n
     wr = (nq_l + 2 * nkv_l) * hd
-    qkv = ctx.workspace_view("qkv", T, n * wr).float().cpu().view(T, n, wr)  # fp16 view
+    qkv = ctx.workspace_view("qkv", T, n * wr, torch.bfloat16).float().cpu().view(T, n, wr)  # q heads: bf16
     q_gpu = qkv[:, :, : nq_l * hd].reshape(T, n * nq_l, hd).transpose(0, 1)
     assert_close(q_gpu, trace["q"], "post-RoPE q", DIAG_TOL)
     attn = ctx.workspace_view("attn", T, s.num_q_heads * hd).float().cpu()
