@@ -235,17 +235,19 @@ cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s) {
 // ---------------------------------------------------------------------------
 // Prefill (several new tokens per sequence, causal with cache offset):
 // flash attention on the tcgen05 tensor cores.  One CTA = 128 queries of one
-// (sequence, rank, q head); 192 threads:
+// (sequence, rank, q head); 320 threads:
 //   warp 0      TMA: the Q tiles once (bf16 high and low parts), then K and V
-//               blocks of 128 keys from the rank's bf16 cache into a 2-stage
-//               shared-memory ring.
+//               blocks of 128 keys from the rank's bf16 cache into separate
+//               2-stage rings (one lane each): a K stage frees as soon as its S
+//               MMA is done, a V stage when its PV MMA is.
 //   warp 1      TMEM allocation + one MMA-issuing thread: S(j) = Q K(j)^T
 //               (as Q_hi K^T + Q_lo K^T, so q keeps ~16 significant bits) into
 //               one of two TMEM score buffers, then O += P(j) V(j) into the TMEM
 //               output accumulator (P from shared memory, V as an MN-major
 //               operand straight from the TMA tile).
-//   warps 2-5   softmax: one query row per thread (its TMEM lane) -- scale,
-//               causal mask, row max, exp2, row sum; P(j) written to shared
+//   warps 2-9   softmax: two threads per query row (its TMEM lane), one per
+//               64-key half -- scale, causal mask, row max, exp2, row sum;
+//               P(j) written to shared
 //               memory in the swizzled K-major layout the MMA reads; the running
 //               output is rescaled only when the row max has grown by more than
 //               2^8 (otherwise P may exceed 1 by at most 2^8, exactly
@@ -262,7 +264,7 @@ struct FaCfg {
   static constexpr int TILE_BYTES = NSUB * SUB_BYTES;
   static constexpr int STAGES = 2;
   static constexpr int Q_OFF = 0;                                  // [hi | lo]
-  static constexpr int KV_OFF = 2 * TILE_BYTES;                    // [stage][K | V]
+  static constexpr int KV_OFF = 2 * TILE_BYTES;                    // K ring [stage], then V ring [stage]
   static constexpr int P_OFF = KV_OFF + STAGES * 2 * TILE_BYTES;   // [2 sub-tiles of 64 keys]
   static constexpr int BAR_OFF = P_OFF + 2 * SUB_BYTES;
   static constexpr int SMEM = 1024 + BAR_OFF + 256;
@@ -271,7 +273,7 @@ struct FaCfg {
 };
 
 template <int HD>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQlo,
                            const __grid_constant__ CUtensorMap tmKV, const AttnArgs a) {
   using C = FaCfg<HD>;
@@ -279,13 +281,16 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  // barriers: 0 q_full | 1,2 kv_full | 3,4 kv_empty | 5,6 s_full | 7,8 s_empty | 9 p_full | 10 o_done | 11 drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  // barriers: 0 q_full | 1,2 k_full | 3,4 k_empty | 5,6 s_full | 7,8 s_empty | 9 p_full | 10 o_done | 11 drain
+  //           | 12,13 v_full | 14,15 v_empty
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
 #define B_Q (bar0)
-#define B_KVF(s) (bar0 + 8u * (1 + (s)))
-#define B_KVE(s) (bar0 + 8u * (3 + (s)))
+#define B_KF(s) (bar0 + 8u * (1 + (s)))
+#define B_KE(s) (bar0 + 8u * (3 + (s)))
+#define B_VF(s) (bar0 + 8u * (12 + (s)))
+#define B_VE(s) (bar0 + 8u * (14 + (s)))
 #define B_SF(b) (bar0 + 8u * (5 + (b)))
 #define B_SE(b) (bar0 + 8u * (7 + (b)))
 #define B_PF (bar0 + 8u * 9)
@@ -293,11 +298,16 @@ __global__ void __launch_bounds__(192, 1)
 #define B_DR (bar0 + 8u * 11)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = a.seq_begin + blockIdx.z;
+  // linear grid, heaviest work first: the q-block index (from the last) varies slowest
+  const int heads = a.n * a.nq_l;
+  const int nseq = a.seq_end - a.seq_begin;
+  const int qblocks = (a.max_q_len + C::BQ - 1) / C::BQ;
+  const int rest = blockIdx.x % (heads * nseq);
+  const int b = a.seq_begin + rest / heads;
+  const int hg = rest % heads;
   const int qlen = a.cu_q[b + 1] - a.cu_q[b];
-  const int q0 = (gridDim.x - 1 - blockIdx.x) * C::BQ;  // heaviest blocks first
+  const int q0 = (qblocks - 1 - static_cast<int>(blockIdx.x) / (heads * nseq)) * C::BQ;
   if (q0 >= qlen) return;                                // uniform: before any barrier or TMEM use
-  const int hg = blockIdx.y;
   const int r = hg / a.nq_l, h = hg % a.nq_l;
   const int g = h / (a.nq_l / a.nkv_l);
   const int ctx = a.ctx_len[b];
@@ -311,14 +321,16 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     mbar_init(B_Q, 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(B_KVF(s), 1);
-      mbar_init(B_KVE(s), 1);
+      mbar_init(B_KF(s), 1);
+      mbar_init(B_KE(s), 1);
+      mbar_init(B_VF(s), 1);
+      mbar_init(B_VE(s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(B_SF(i), 1);
-      mbar_init(B_SE(i), 4);
+      mbar_init(B_SE(i), 8);
     }
-    mbar_init(B_PF, 4);
+    mbar_init(B_PF, 8);
     mbar_init(B_OD, 1);
     mbar_init(B_DR, 1);
     *abort_flag = 0;
@@ -334,35 +346,39 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmQlo);
-      tma_prefetch_desc(&tmKV);
-      const int qcol = r * a.w_rank + h * HD;
-      const int qlo_col = (r * a.nq_l + h) * HD;
-      mbar_arrive_expect_tx(B_Q, 2 * C::TILE_BYTES);
-      for (int s = 0; s < C::NSUB; ++s) {
-        tma_load_2d(smem_u32(smem + C::Q_OFF + s * C::SUB_BYTES), &tmQ, B_Q, qcol + s * 64, tbase + q0);
-        tma_load_2d(smem_u32(smem + C::Q_OFF + C::TILE_BYTES + s * C::SUB_BYTES), &tmQlo, B_Q, qlo_col + s * 64,
-                    tbase + q0);
+    // ---------------- TMA producers: lane 0 streams Q then K, lane 1 streams V ----------------
+    if (lane < 2) {
+      const bool is_k = lane == 0;
+      if (is_k) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmQlo);
+        tma_prefetch_desc(&tmKV);
+        const int qcol = r * a.w_rank + h * HD;
+        const int qlo_col = (r * a.nq_l + h) * HD;
+        mbar_arrive_expect_tx(B_Q, 2 * C::TILE_BYTES);
+        for (int s = 0; s < C::NSUB; ++s) {
+          tma_load_2d(smem_u32(smem + C::Q_OFF + s * C::SUB_BYTES), &tmQ, B_Q, qcol + s * 64, tbase + q0);
+          tma_load_2d(smem_u32(smem + C::Q_OFF + C::TILE_BYTES + s * C::SUB_BYTES), &tmQlo, B_Q, qlo_col + s * 64,
+                      tbase + q0);
+        }
       }
+      const int row0 = is_k ? krow0 : vrow0;
+      uint8_t* ring = smem + C::KV_OFF + (is_k ? 0 : STAGES * C::TILE_BYTES);
       int issued = 0;
       for (int j = 0; j < nblk; ++j) {
         const int st = j % STAGES;
-        if (!mbar_wait(B_KVE(st), ((j / STAGES) & 1) ^ 1u, abort_flag, a.status)) break;
-        uint8_t* kt = smem + C::KV_OFF + st * 2 * C::TILE_BYTES;
-        mbar_arrive_expect_tx(B_KVF(st), 2 * C::TILE_BYTES);
-        for (int s = 0; s < C::NSUB; ++s) {
-          tma_load_2d(smem_u32(kt + s * C::SUB_BYTES), &tmKV, B_KVF(st), s * 64, krow0 + j * C::BKV);
-          tma_load_2d(smem_u32(kt + C::TILE_BYTES + s * C::SUB_BYTES), &tmKV, B_KVF(st), s * 64,
-                      vrow0 + j * C::BKV);
-        }
+        const uint32_t full = is_k ? B_KF(st) : B_VF(st);
+        const uint32_t empty = is_k ? B_KE(st) : B_VE(st);
+        if (!mbar_wait(empty, ((j / STAGES) & 1) ^ 1u, abort_flag, a.status)) break;
+        mbar_arrive_expect_tx(full, C::TILE_BYTES);
+        for (int s = 0; s < C::NSUB; ++s)
+          tma_load_2d(smem_u32(ring + st * C::TILE_BYTES + s * C::SUB_BYTES), &tmKV, full, s * 64,
+                      row0 + j * C::BKV);
         issued = j + 1;
       }
-      mbar_wait(B_Q, 0, nullptr, a.status);
+      if (is_k) mbar_wait(B_Q, 0, nullptr, a.status);
       for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j)
-        mbar_wait(B_KVF(j % STAGES), (j / STAGES) & 1, nullptr, a.status);
+        mbar_wait(is_k ? B_KF(j % STAGES) : B_VF(j % STAGES), (j / STAGES) & 1, nullptr, a.status);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -372,10 +388,11 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = mbar_wait(B_Q, 0, abort_flag, a.status);
       tc_fence_after();
       auto pv = [&](int j) -> bool {  // O += P(j) V(j)
-        if (!mbar_wait(B_PF, j & 1, abort_flag, a.status)) return false;
-        tc_fence_after();
         const int st = j % STAGES;
-        const uint32_t vt = smem_u32(smem + C::KV_OFF + st * 2 * C::TILE_BYTES + C::TILE_BYTES);
+        if (!mbar_wait(B_PF, j & 1, abort_flag, a.status)) return false;
+        if (!mbar_wait(B_VF(st), (j / STAGES) & 1, abort_flag, a.status)) return false;
+        tc_fence_after();
+        const uint32_t vt = smem_u32(smem + C::KV_OFF + (STAGES + st) * C::TILE_BYTES);
         const uint32_t pt = smem_u32(smem + C::P_OFF);
 #pragma unroll
         for (int kk = 0; kk < C::BKV / 16; ++kk) {
@@ -384,16 +401,16 @@ __global__ void __launch_bounds__(192, 1)
           tc_mma_f16(tmem + C::O_COL, ad, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(B_OD);
-        tc_commit(B_KVE(st));
+        tc_commit(B_VE(st));
         return true;
       };
       for (int j = 0; ok && j < nblk; ++j) {
         const int st = j % STAGES, sb = j & 1;
-        if (!mbar_wait(B_KVF(st), (j / STAGES) & 1, abort_flag, a.status)) { ok = false; break; }
+        if (!mbar_wait(B_KF(st), (j / STAGES) & 1, abort_flag, a.status)) { ok = false; break; }
         if (!mbar_wait(B_SE(sb), ((j >> 1) & 1) ^ 1u, abort_flag, a.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t qt = smem_u32(smem + C::Q_OFF);
-        const uint32_t kt = smem_u32(smem + C::KV_OFF + st * 2 * C::TILE_BYTES);
+        const uint32_t kt = smem_u32(smem + C::KV_OFF + st * C::TILE_BYTES);
 #pragma unroll
         for (int part = 0; part < 2; ++part) {  // S = Q_hi K^T + Q_lo K^T
 #pragma unroll
@@ -404,6 +421,7 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
         tc_commit(B_SF(sb));
+        tc_commit(B_KE(st));  // the K stage is free once S(j) is done
         if (j > 0 && !pv(j - 1)) { ok = false; break; }
       }
       if (ok) pv(nblk - 1);
@@ -411,92 +429,115 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait(B_DR, 0, nullptr, a.status);
     }
   } else {
-    // ---------------- softmax / output (warps 2..5) ----------------
+    // ---------------- softmax / output (warps 2..9) ----------------
+    // Two warps per query row: warps 2-5 take keys [0, 64) of each block and
+    // output dims [0, HD/2), warps 6-9 the other halves (both see the same TMEM
+    // lanes).  The halves exchange their row maxima through two spare TMEM
+    // columns and agree on every rescale decision.
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     const int qi = q0 + row;                    // query index within the sequence
     const bool row_ok = qi < qlen;
     const int last_key = ctx + qi;              // keys <= last_key are visible
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    uint8_t* prow = smem + C::P_OFF + row * 128;
+    uint8_t* prow = smem + C::P_OFF + half * C::SUB_BYTES + row * 128;
+    constexpr int OH = HD / 2;                  // output dims per half
     float m_used = -INFINITY, l = 0.0f;
     bool ok = true;
     for (int j = 0; j < nblk; ++j) {
       const int sb = j & 1;
-      if (!mbar_wait(B_SF(sb), (j >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+      if (!mbar_wait(B_SF(sb), (j >> 1) & 1, abort_flag, a.status)) ok = false;
+      if (!named_bar_and(1, 256, ok)) { ok = false; break; }
       tc_fence_after();
-      float sv[128];
+      float sv[64];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float v[32];
-        tc_ld32(lane_addr + C::S_COL + sb * 128 + c * 32, v);
+        tc_ld32(lane_addr + C::S_COL + sb * 128 + half * 64 + c * 32, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[c * 32 + i] = v[i];
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(B_SE(sb));
-      const int key0 = j * C::BKV;
-      const bool need_mask = (key0 + C::BKV - 1 > ctx + q0) || !row_ok;
+      const int key0 = j * C::BKV + half * 64;
+      const bool need_mask = (key0 + 63 > ctx + q0) || !row_ok;
       float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
+      for (int i = 0; i < 64; ++i) {
         float x = sv[i] * a.scale_log2;
         if (need_mask && (!row_ok || key0 + i > last_key)) x = -INFINITY;
         sv[i] = x;
         mx = fmaxf(mx, x);
       }
-      // P buffer and O are free once the previous block's PV has completed
-      if (j > 0 && !mbar_wait(B_OD, (j - 1) & 1, abort_flag, a.status)) { ok = false; break; }
+      // row max over both halves (TMEM columns 384 + 2 * (j & 1) + half)
+      tc_st1(lane_addr + 384 + 2 * (j & 1) + half, mx);
+      tc_fence_before();
+      named_bar_sync(1, 256);
       tc_fence_after();
-      if (mx > m_used + 8.0f) {
-        if (j > 0 && m_used != -INFINITY) {
-          const float corr = exp2f(m_used - mx);
-          l *= corr;
-#pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            float v[32];
-            tc_ld32(lane_addr + C::O_COL + c * 32, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= corr;
-            tc_st32(lane_addr + C::O_COL + c * 32, v);
-          }
-        }
-        m_used = mx;
-      }
-      const float mb = m_used == -INFINITY ? 0.0f : m_used;
+      mx = fmaxf(mx, tc_ld1(lane_addr + 384 + 2 * (j & 1) + (half ^ 1)));
+      const bool rescale = mx > m_used + 8.0f;
+      const float m_new = rescale ? mx : m_used;
+      const float mb = m_new == -INFINITY ? 0.0f : m_new;
       float psum = 0.0f;
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {  // 16-byte chunks of 8 keys
-        float p[8];
+      for (int i = 0; i < 64; ++i) {
+        sv[i] = exp2f(sv[i] - mb);
+        psum += sv[i];
+      }
+      // P buffer and O are free once the previous block's PV has completed.  A
+      // failed wait only marks the thread; every softmax thread leaves together at
+      // the next agreement point (named barriers have no time limit).
+      if (j > 0 && !mbar_wait(B_OD, (j - 1) & 1, abort_flag, a.status)) ok = false;
+      if (!ok) continue;
+      tc_fence_after();
+      if (rescale) {
+        if (j > 0 && m_used != -INFINITY) {
+          const float corr = exp2f(m_used - m_new);
+          l *= corr;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          p[i] = exp2f(sv[ch * 8 + i] - mb);
-          psum += p[i];
+          for (int c = 0; c < OH / 32; ++c) {
+            float v[32];
+            tc_ld32(lane_addr + C::O_COL + half * OH + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= corr;
+            tc_st32(lane_addr + C::O_COL + half * OH + c * 32, v);
+          }
         }
-        uint4 w;
-        w.x = pack_bf16x2(p[0], p[1]);
-        w.y = pack_bf16x2(p[2], p[3]);
-        w.z = pack_bf16x2(p[4], p[5]);
-        w.w = pack_bf16x2(p[6], p[7]);
-        const int sub = ch >> 3, c8 = ch & 7;
-        *reinterpret_cast<uint4*>(prow + sub * C::SUB_BYTES + ((c8 ^ (row & 7)) << 4)) = w;
+        m_used = m_new;
       }
       l += psum;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {  // 16-byte chunks of 8 keys
+        uint4 w;
+        w.x = pack_bf16x2(sv[ch * 8 + 0], sv[ch * 8 + 1]);
+        w.y = pack_bf16x2(sv[ch * 8 + 2], sv[ch * 8 + 3]);
+        w.z = pack_bf16x2(sv[ch * 8 + 4], sv[ch * 8 + 5]);
+        w.w = pack_bf16x2(sv[ch * 8 + 6], sv[ch * 8 + 7]);
+        *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = w;
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(B_PF);
     }
-    if (ok && mbar_wait(B_OD, (nblk - 1) & 1, abort_flag, a.status)) {
+    if (ok) ok = mbar_wait(B_OD, (nblk - 1) & 1, abort_flag, a.status);
+    if (named_bar_and(1, 256, ok)) {
       tc_fence_after();
+      // row sum over both halves (TMEM columns 388 + half)
+      tc_st1(lane_addr + 388 + half, l);
+      tc_fence_before();
+      named_bar_sync(1, 256);
+      tc_fence_after();
+      l += tc_ld1(lane_addr + 388 + (half ^ 1));
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
       __half* orow = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(tbase + (row_ok ? qi : 0)) * a.n * a.nq_l * HD +
-                     (static_cast<size_t>(r) * a.nq_l + h) * HD;
+                     (static_cast<size_t>(r) * a.nq_l + h) * HD + half * OH;
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 0; c < OH / 32; ++c) {
         float v[32];
-        tc_ld32(lane_addr + C::O_COL + c * 32, v);
+        tc_ld32(lane_addr + C::O_COL + half * OH + c * 32, v);
         if (row_ok) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -512,8 +553,10 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
 #undef B_Q
-#undef B_KVF
-#undef B_KVE
+#undef B_KF
+#undef B_KE
+#undef B_VF
+#undef B_VE
 #undef B_SF
 #undef B_SE
 #undef B_PF
@@ -545,8 +588,8 @@ static cudaError_t launch_prefill_hd(const AttnArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid((a.max_q_len + C::BQ - 1) / C::BQ, a.n * a.nq_l, a.seq_end - a.seq_begin);
-  attn_prefill_tc_kernel<HD><<<grid, 192, C::SMEM, s>>>(mq, mqlo, mkv, a);
+  const unsigned grid = static_cast<unsigned>((a.max_q_len + C::BQ - 1) / C::BQ) * a.n * a.nq_l * (a.seq_end - a.seq_begin);
+  attn_prefill_tc_kernel<HD><<<grid, 320, C::SMEM, s>>>(mq, mqlo, mkv, a);
   return cudaGetLastError();
 }
 

@@ -62,7 +62,8 @@ struct GemmCfg {
   static constexpr int A_BYTES = 128 * 128;  // 128 rows x 64 fp16
   static constexpr int B_BYTES = BN * 128;   // BN rows x 64 fp16
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);
+  // as many stages as fit in ~200 KB (narrow tiles stream weights: more bytes in flight)
+  static constexpr int STAGES = (204800 / STAGE_BYTES) > 12 ? 12 : (204800 / STAGE_BYTES);
   static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64 + 1536;
