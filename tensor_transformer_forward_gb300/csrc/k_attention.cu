@@ -19,17 +19,35 @@ namespace tpk {
 
 // ---------------------------------------------------------------------------
 // Decode (one new token per sequence): flash-decoding split over the keys.
-// One CTA = (sequence, rank, local kv head, key split), 4 warps; the G query
-// heads of the kv group share every K/V load.  Lanes split head_dim in 16-byte
-// pieces (hd/8 lanes per key), so one warp load covers 32/(hd/8) keys.
-// Splits combine through an fp32 workspace; the last CTA of a (seq, rank,
-// head) to finish (atomic counter, no waiting) merges them in split order.
+// One CTA = (sequence, rank, local kv head, key split).  Warp 4 streams the
+// split's K and V rows (contiguous in the cache) into a 4-stage shared-memory
+// ring with bulk copies; warps 0-3 compute from shared memory.  The G query
+// heads of the kv group share every K/V row.  Lanes split head_dim in 16-byte
+// pieces (hd/8 lanes per key); each half-warp-sized lane group takes one key,
+// a warp covers 32/(hd/8) keys per step, and the online-softmax correction is
+// applied once per 4 such steps.  Splits combine through an fp32 workspace;
+// the last CTA of a (seq, rank, head) to finish (atomic counter, no waiting)
+// merges them in split order.
 // ---------------------------------------------------------------------------
+template <int HD>
+struct DecCfg {
+  static constexpr int CK = HD == 128 ? 32 : 64;      // keys per ring stage (16 KB of K + V)
+  static constexpr int STAGES = 4;
+  static constexpr int ROW = HD * 2;                  // bytes per key row
+  static constexpr int STAGE_BYTES = 2 * CK * ROW;    // K then V
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 128;
+};
+
 template <int HD, int G>
-__global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
+  using C = DecCfg<HD>;
   constexpr int LPK = HD / 8;        // lanes per key
-  constexpr int KPI = 32 / LPK;      // keys per warp instruction
-  constexpr int U = 4;               // key groups in flight per lane
+  constexpr int KPI = 32 / LPK;      // keys per warp step
+  constexpr int U = 4;               // warp steps per softmax correction
+  extern __shared__ __align__(128) uint8_t dsm[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + C::STAGES * C::STAGE_BYTES);  // full[4], empty[4]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * C::STAGES);
+  const uint32_t bar0 = smem_u32(bars);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ks = lane / LPK, dc = lane % LPK;
   const int per_seq = a.n * a.nkv_l;
@@ -43,26 +61,24 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
   const int chunk = (L + a.splits - 1) / a.splits;
   const int k0 = split * chunk;
   const int k1 = min(L, k0 + chunk);
+  const int nchunks = k1 > k0 ? (k1 - k0 + C::CK - 1) / C::CK : 0;
 
   const size_t plane = static_cast<size_t>(a.max_seqs) * a.nkv_l * a.cap * HD;
   const size_t head_off = (static_cast<size_t>(a.slot[b]) * a.nkv_l + g) * a.cap * HD;
-  const uint4* Kc = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.kv) +
-                                                   (2 * static_cast<size_t>(r)) * plane + head_off);
-  const uint4* Vc = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.kv) +
-                                                   (2 * static_cast<size_t>(r) + 1) * plane + head_off);
+  const __nv_bfloat16* Kc = reinterpret_cast<const __nv_bfloat16*>(a.kv) + (2 * static_cast<size_t>(r)) * plane + head_off;
+  const __nv_bfloat16* Vc = reinterpret_cast<const __nv_bfloat16*>(a.kv) + (2 * static_cast<size_t>(r) + 1) * plane + head_off;
 
-  // this lane's 8 dims of each query head, pre-scaled into the exp2 domain
-  float q[G][8];
-  const __half* qrow = reinterpret_cast<const __half*>(a.qkv) + static_cast<size_t>(t) * a.n * a.w_rank +
-                       static_cast<size_t>(r) * a.w_rank;
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const uint4 u = *reinterpret_cast<const uint4*>(qrow + (g * G + h) * HD + dc * 8);
-    q[h][0] = f16lo(u.x); q[h][1] = f16hi(u.x); q[h][2] = f16lo(u.y); q[h][3] = f16hi(u.y);
-    q[h][4] = f16lo(u.z); q[h][5] = f16hi(u.z); q[h][6] = f16lo(u.w); q[h][7] = f16hi(u.w);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[h][i] *= a.scale_log2;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar0 + 8u * s, 1);
+      mbar_init(bar0 + 8u * (C::STAGES + s), 4);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
   }
+  __syncthreads();
+
+  // per-lane state for the warp's keys: G heads x (m, l, acc[8])
   float m[G], l[G], acc[G][8];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
@@ -72,49 +88,99 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
     for (int i = 0; i < 8; ++i) acc[h][i] = 0.0f;
   }
 
-  constexpr int STEP = 4 * KPI;  // keys covered by one pass of all warps
-  // the loop bound is warp-uniform (shuffles inside); each lane adds its key offset ks
-  for (int wb = k0 + warp * KPI; wb < k1; wb += STEP * U) {
-    const int base = wb + ks;
-    uint4 kv_k[U], kv_v[U];
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const int key = base + j * STEP;
-      if (key < k1) {
-        kv_k[j] = __ldcs(Kc + static_cast<size_t>(key) * LPK + dc);
-        kv_v[j] = __ldcs(Vc + static_cast<size_t>(key) * LPK + dc);
+  if (warp == 4) {
+    // ---------------- bulk-copy producer ----------------
+    if (lane == 0) {
+      int issued = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % C::STAGES;
+        if (!mbar_wait(bar0 + 8u * (C::STAGES + s), ((c / C::STAGES) & 1) ^ 1u, abort_flag, a.status)) break;
+        const int key = k0 + c * C::CK;
+        const uint32_t bytes = static_cast<uint32_t>(min(C::CK, k1 - key)) * C::ROW;
+        const uint32_t full = bar0 + 8u * s;
+        mbar_arrive_expect_tx(full, 2 * bytes);
+        uint8_t* st = dsm + s * C::STAGE_BYTES;
+        bulk_load(smem_u32(st), Kc + static_cast<size_t>(key) * HD, bytes, full);
+        bulk_load(smem_u32(st + C::CK * C::ROW), Vc + static_cast<size_t>(key) * HD, bytes, full);
+        issued = c + 1;
       }
+      for (int c = (issued > C::STAGES ? issued - C::STAGES : 0); c < issued; ++c)
+        mbar_wait(bar0 + 8u * (c % C::STAGES), (c / C::STAGES) & 1, nullptr, a.status);
     }
+  } else {
+    // ---------------- compute warps 0..3 ----------------
+    // this lane's 8 dims of each query head (fp16 q), pre-scaled into the exp2 domain
+    float q[G][8];
+    const __half* qrow = reinterpret_cast<const __half*>(a.qkv) + static_cast<size_t>(t) * a.n * a.w_rank +
+                         static_cast<size_t>(r) * a.w_rank;
 #pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const int key = base + j * STEP;
-      const bool valid = key < k1;  // uniform across the LPK lanes of this key
-      float kf[8], vf[8];
-      kf[0] = bf16lo(kv_k[j].x); kf[1] = bf16hi(kv_k[j].x); kf[2] = bf16lo(kv_k[j].y); kf[3] = bf16hi(kv_k[j].y);
-      kf[4] = bf16lo(kv_k[j].z); kf[5] = bf16hi(kv_k[j].z); kf[6] = bf16lo(kv_k[j].w); kf[7] = bf16hi(kv_k[j].w);
-      vf[0] = bf16lo(kv_v[j].x); vf[1] = bf16hi(kv_v[j].x); vf[2] = bf16lo(kv_v[j].y); vf[3] = bf16hi(kv_v[j].y);
-      vf[4] = bf16lo(kv_v[j].z); vf[5] = bf16hi(kv_v[j].z); vf[6] = bf16lo(kv_v[j].w); vf[7] = bf16hi(kv_v[j].w);
+    for (int h = 0; h < G; ++h) {
+      const uint4 u = *reinterpret_cast<const uint4*>(qrow + (g * G + h) * HD + dc * 8);
+      q[h][0] = f16lo(u.x); q[h][1] = f16hi(u.x); q[h][2] = f16lo(u.y); q[h][3] = f16hi(u.y);
+      q[h][4] = f16lo(u.z); q[h][5] = f16hi(u.z); q[h][6] = f16lo(u.w); q[h][7] = f16hi(u.w);
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float s = 0.0f;
+      for (int i = 0; i < 8; ++i) q[h][i] *= a.scale_log2;
+    }
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % C::STAGES;
+      if (!mbar_wait(bar0 + 8u * s, (c / C::STAGES) & 1, abort_flag, a.status)) break;
+      const uint8_t* st = dsm + s * C::STAGE_BYTES;
+      const int nk = min(C::CK, k1 - (k0 + c * C::CK));
+      // this warp's keys of the chunk: warp * (CK/4) .. + CK/4, KPI per step, U steps per correction
+      constexpr int KW = C::CK / 4;
+      static_assert(KW % (KPI * U) == 0, "a warp's share of a chunk is whole correction groups");
+      for (int base = warp * KW; base < warp * KW + KW; base += KPI * U) {
+        float sc[G][U];
+        uint4 vv[U];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) s += q[h][i] * kf[i];
+        for (int u = 0; u < U; ++u) {
+          const int kk = base + u * KPI + ks;
+          const bool valid = kk < nk;  // uniform across the LPK lanes of this key
+          const uint4 kr = *reinterpret_cast<const uint4*>(st + kk * C::ROW + dc * 16);
+          // rows past the chunk's end hold stale bytes: V is zeroed so 0 * NaN cannot occur
+          vv[u] = valid ? *reinterpret_cast<const uint4*>(st + C::CK * C::ROW + kk * C::ROW + dc * 16)
+                        : make_uint4(0u, 0u, 0u, 0u);
+          const float kf[8] = {bf16lo(kr.x), bf16hi(kr.x), bf16lo(kr.y), bf16hi(kr.y),
+                               bf16lo(kr.z), bf16hi(kr.z), bf16lo(kr.w), bf16hi(kr.w)};
 #pragma unroll
-        for (int o = LPK / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (valid) {
-          const float mn = fmaxf(m[h], s);
+          for (int h = 0; h < G; ++h) {
+            float d = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) d += q[h][i] * kf[i];
+#pragma unroll
+            for (int o = LPK / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+            sc[h][u] = valid ? d : -INFINITY;
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float mx = sc[h][0];
+#pragma unroll
+          for (int u = 1; u < U; ++u) mx = fmaxf(mx, sc[h][u]);
+          const float mn = fmaxf(m[h], mx);
+          if (mn == -INFINITY) continue;  // nothing valid yet
           const float corr = exp2f(m[h] - mn);
-          const float p = exp2f(s - mn);
-          l[h] = l[h] * corr + p;
+          l[h] *= corr;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[h][i] = acc[h][i] * corr + p * vf[i];
+          for (int i = 0; i < 8; ++i) acc[h][i] *= corr;
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const float pu = exp2f(sc[h][u] - mn);
+            l[h] += pu;
+            const float vf[8] = {bf16lo(vv[u].x), bf16hi(vv[u].x), bf16lo(vv[u].y), bf16hi(vv[u].y),
+                                 bf16lo(vv[u].z), bf16hi(vv[u].z), bf16lo(vv[u].w), bf16hi(vv[u].w)};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[h][i] += pu * vf[i];
+          }
           m[h] = mn;
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar0 + 8u * (C::STAGES + s));
     }
   }
 
-  // merge the KPI key groups of this warp (lanes with the same dims)
+  // merge the KPI key groups of each compute warp (lanes with the same dims)
 #pragma unroll
   for (int h = 0; h < G; ++h) {
 #pragma unroll
@@ -134,10 +200,11 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
       }
     }
   }
-  // merge the 4 warps through shared memory: [warp][h][HD + 2]
-  __shared__ float red[4][G][HD + 2];
+  // merge the 4 compute warps through shared memory (reusing the ring): [warp][h][HD + 2]
+  __syncthreads();
+  float (*red)[G][HD + 2] = reinterpret_cast<float (*)[G][HD + 2]>(dsm);
   __shared__ int last_flag;
-  if (ks == 0) {
+  if (warp < 4 && ks == 0) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
 #pragma unroll
@@ -149,7 +216,6 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
     }
   }
   __syncthreads();
-  // thread x handles (h, d) pairs; merged state of this split
   const int unit_heads = G * HD;
   float* part = a.part + (static_cast<size_t>(unit) * a.splits + split) * G * (HD + 2);
   for (int e = threadIdx.x; e < unit_heads; e += blockDim.x) {
@@ -169,7 +235,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
     if (a.splits == 1) {
       __half* o = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
                   (static_cast<size_t>(r) * a.nq_l + g * G + h) * HD + d;
-      *o = __float2half_rn(sat_f16(aa / ll));
+      *o = __float2half_rn(sat_f16(ll > 0.0f ? aa / ll : 0.0f));
     } else {
       part[h * (HD + 2) + d] = aa;
       if (d == 0) {
@@ -188,12 +254,12 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
   __syncthreads();
   if (!last_flag) return;
   __threadfence();
-  const float* base = a.part + static_cast<size_t>(unit) * a.splits * G * (HD + 2);
+  const float* pbase = a.part + static_cast<size_t>(unit) * a.splits * G * (HD + 2);
   for (int e = threadIdx.x; e < unit_heads; e += blockDim.x) {
     const int h = e / HD, d = e % HD;
     float mm = -INFINITY, ll = 0.0f, aa = 0.0f;
-    for (int s = 0; s < a.splits; ++s) {
-      const float* ps = base + (static_cast<size_t>(s) * G + h) * (HD + 2);
+    for (int sp = 0; sp < a.splits; ++sp) {
+      const float* ps = pbase + (static_cast<size_t>(sp) * G + h) * (HD + 2);
       const float m2 = __ldcg(ps + HD), l2 = __ldcg(ps + HD + 1), a2 = __ldcg(ps + d);
       const float mn = fmaxf(mm, m2);
       if (mn != -INFINITY) {
@@ -205,7 +271,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
     }
     __half* o = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
                 (static_cast<size_t>(r) * a.nq_l + g * G + h) * HD + d;
-    *o = __float2half_rn(sat_f16(aa / ll));
+    *o = __float2half_rn(sat_f16(ll > 0.0f ? aa / ll : 0.0f));
   }
   if (threadIdx.x == 0) a.counters[unit] = 0;
 }
@@ -219,13 +285,26 @@ int decode_splits(int max_kv_len, int num_units, int num_sms) {
   return s;
 }
 
+template <int HD, int G>
+static cudaError_t launch_decode_hd(const AttnArgs& a, dim3 grid, cudaStream_t s) {
+  auto kern = attn_decode_kernel<HD, G>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DecCfg<HD>::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  kern<<<grid, 160, DecCfg<HD>::SMEM, s>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s) {
   const int seqs = a.seq_end - a.seq_begin;
   if (seqs <= 0) return cudaSuccess;
   const int G = a.nq_l / a.nkv_l;
   dim3 grid(seqs * a.n * a.nkv_l, a.splits);
 #define TP_DEC(HD_, G_) \
-  if (a.hd == HD_ && G == G_) { attn_decode_kernel<HD_, G_><<<grid, 128, 0, s>>>(a); return cudaGetLastError(); }
+  if (a.hd == HD_ && G == G_) return launch_decode_hd<HD_, G_>(a, grid, s);
   TP_DEC(128, 1) TP_DEC(128, 2) TP_DEC(128, 4) TP_DEC(128, 8)
   TP_DEC(64, 1) TP_DEC(64, 2) TP_DEC(64, 4) TP_DEC(64, 8)
 #undef TP_DEC

@@ -450,26 +450,40 @@ __global__ void __launch_bounds__(192, 1)
           tc_ld32(lane_addr + static_cast<uint32_t>(b * BN + c0), v);
         }
         const int ncol = min(min(32, BN), p.T - (t0 + c0));  // valid token columns (warp-uniform)
+        if (p.logits && f_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < ncol) p.logits[static_cast<size_t>(t0 + c0 + i) * p.ld_logits + f] = v[i];
+        }
+        // Transpose-reduce across the warp: at each step a lane keeps half of its
+        // columns, trades the other half with its partner and keeps the better of
+        // each pair; after 5 steps lane l holds column l reduced over the warp's
+        // 32 rows (31 exchanges instead of 5 per column).
+        float bv[32];
+        int bi[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          if (i >= ncol) break;
-          float bv = f_ok ? v[i] : -INFINITY;
-          int bi = f_ok ? f : INT_MAX;
-          if (p.logits && f_ok) p.logits[static_cast<size_t>(t0 + c0 + i) * p.ld_logits + f] = v[i];
+          bv[i] = f_ok ? v[i] : -INFINITY;
+          bi[i] = f_ok ? f : INT_MAX;
+        }
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (amax_better(ov, oi, bv, bi)) {
-              bv = ov;
-              bi = oi;
-            }
-          }
-          if (lane == 0) {
-            red_v[q * 32 + i] = bv;
-            red_i[q * 32 + i] = bi;
+        for (int o = 16; o > 0; o >>= 1) {
+          const bool upper = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < o; ++i) {
+            const float send_v = upper ? bv[i] : bv[i + o];
+            const int send_i = upper ? bi[i] : bi[i + o];
+            const float keep_v = upper ? bv[i + o] : bv[i];
+            const int keep_i = upper ? bi[i + o] : bi[i];
+            const float rv = __shfl_xor_sync(0xffffffffu, send_v, o);
+            const int ri = __shfl_xor_sync(0xffffffffu, send_i, o);
+            const bool take = amax_better(rv, ri, keep_v, keep_i);
+            bv[i] = take ? rv : keep_v;
+            bi[i] = take ? ri : keep_i;
           }
         }
+        red_v[q * 32 + lane] = bv[0];
+        red_i[q * 32 + lane] = bi[0];
         named_bar_sync(1, 128);
         if (et < ncol) {
           const int t = t0 + c0 + et;
