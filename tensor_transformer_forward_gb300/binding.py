@@ -237,7 +237,9 @@ class Context:
         return torch.empty(self.weights_bytes(WEIGHTS_HEAD), dtype=torch.uint8, device="cuda")
 
     def alloc_kv_cache(self, max_seqs: int, capacity: int) -> torch.Tensor:
-        return torch.empty(self.kv_cache_bytes(max_seqs, capacity), dtype=torch.uint8, device="cuda")
+        # zeroed: attention tiles read whole 128-key blocks, so the unused tail of a
+        # slot must hold finite values (masked scores are 0, and 0 * NaN is NaN)
+        return torch.zeros(self.kv_cache_bytes(max_seqs, capacity), dtype=torch.uint8, device="cuda")
 
     def init_workspace(self, max_tokens: int, max_seqs: int, max_positions: int) -> torch.Tensor:
         nbytes = self.workspace_bytes(max_tokens, max_seqs, max_positions)

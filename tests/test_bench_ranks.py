@@ -1,0 +1,49 @@
+"""The bench's multi-process bookkeeping on CPU: two Gloo ranks, each with its
+own per-step time; both must see the slowest rank's time, and the whole-job
+throughput counts the tokens of every rank's replica."""
+
+import os
+import socket
+
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port() -> int:
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank(rank, world, port, out_q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    ms = [2.5, 4.0][rank]
+    got = bench.max_over_ranks(ms, world)
+    out_q.put((rank, got, bench.job_throughput(2048, world, got)))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_throughput_with_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    out_q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, out_q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(out_q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, ms, value in res:
+        assert ms == 4.0, f"rank {rank} saw {ms}"
+        assert abs(value - 2 * 2048 / 4.0e-3) < 1e-6
+
+
+def test_single_process_is_its_own_max():
+    import bench
+    assert bench.max_over_ranks(3.25, 1) == 3.25
+    assert bench.job_throughput(64, 1, 0.5) == 128000.0
