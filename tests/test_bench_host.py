@@ -1,6 +1,7 @@
-"""The bench's multi-process bookkeeping on CPU: two Gloo ranks, each with its
-own per-step time; both must see the slowest rank's time, and the whole-job
-throughput counts the tokens of every rank's replica."""
+"""Host-side bookkeeping of bench.py on CPU: the slowest-rank time and the
+whole-job throughput across two Gloo ranks, and the rule that a measured DRAM
+traffic figure is reported only while the kernel source it was taken on is
+unchanged."""
 
 import os
 import socket
@@ -47,3 +48,13 @@ def test_single_process_is_its_own_max():
     import bench
     assert bench.max_over_ranks(3.25, 1) == 3.25
     assert bench.job_throughput(64, 1, 0.5) == 128000.0
+
+
+def test_ncu_traffic_only_while_the_kernel_source_is_unchanged(monkeypatch):
+    import bench
+    key = ("qwen3_0.6b_layer_prefill2048", 2, "gemm_lm_head")
+    monkeypatch.setitem(bench.NCU_TRAFFIC, key, (1.0e6, "k_gemm.cu", bench.source_hash("k_gemm.cu")))
+    assert bench.ncu_traffic(*key) == 1.0e6
+    monkeypatch.setitem(bench.NCU_TRAFFIC, key, (1.0e6, "k_gemm.cu", "0" * 16))
+    assert bench.ncu_traffic(*key) is None
+    assert bench.ncu_traffic("no such workload", 2, "gemm_lm_head") is None
