@@ -209,7 +209,7 @@ tp_status tp_lm_head_argmax(tp_ctx* ctx, const void* head_shards, const tp_batch
  * point -- it can synchronise the device, or the process's device memory is owned by another
  * allocator -- or a caller holding only the weights, its inputs and its outputs.  The pages have
  * no counterpart; this is an interface convenience.
- * Scratch lives in one fixed array compiled into the library (about 1.2 MiB, held on every GPU
+ * Scratch lives in one fixed array compiled into the library (about 1 MiB, held on every GPU
  * that loads the library until the process exits); no context workspace is needed and nothing
  * is allocated.  Limits: num_seqs <= TP_STATIC_SCRATCH_MAX_SEQS and hidden <=
  * TP_STATIC_SCRATCH_MAX_HIDDEN, else TP_ERR_INVALID_ARG before any launch.

@@ -19,6 +19,7 @@ namespace {
 constexpr size_t kAlign = 1024;
 constexpr int kMaxSms = 256;            // bound used to size split-K partials
 constexpr int kGemmCounters = 4096;
+static_assert(kGemmCounters >= tpk::kGemmCounterInts, "GEMM counter region too small");
 constexpr int kMaxDecodeSplits = 64;
 
 thread_local char g_last_cuda_error[256] = "";
@@ -157,7 +158,7 @@ WsPlan plan_ws(const tp_ctx* x, int64_t T, int64_t B, int64_t P) {
   take(w.act, T * n * x->i_p * 2);
   take(w.gpart, static_cast<size_t>(kMaxSms) * 128 * 128 * 4);
   take(w.gcnt, kGemmCounters * 4);
-  const int64_t splits = std::min<int64_t>(kMaxDecodeSplits, std::max<int64_t>(1, (P + 511) / 512));
+  const int64_t splits = std::min<int64_t>(kMaxDecodeSplits, std::max<int64_t>(1, (P + 255) / 256));
   take(w.apart, static_cast<size_t>(B) * n * x->nq_l * (x->hd + 2) * splits * 4);
   take(w.acnt, static_cast<size_t>(B) * n * x->nkv_l * 4);
   w.lm_tiles = static_cast<int>(div_ceil64(n * x->v_l, 64));
@@ -216,7 +217,7 @@ struct Timed {
 tp_status gemm(tp_ctx* x, int kind, const tpk::GemmProblem& pr, int32_t* dev_status, cudaStream_t s) {
   tpk::GemmPlan pl = tpk::plan_gemm(pr, x->num_sms);
   if (pl.partial_floats * 4 > x->r_gpart.bytes) return TP_ERR_UNSUPPORTED;
-  if (pl.splits > 1 && pl.tiles_t * pl.tiles_f > kGemmCounters) return TP_ERR_UNSUPPORTED;
+  if (pl.splits > 1 && pl.tiles_t * pl.tiles_f > tpk::kArgmaxKeyOffset) return TP_ERR_UNSUPPORTED;
   Timed tm(x, kind, s);
   cudaError_t e = tpk::launch_gemm(pr, pl, at<float>(x->ws, x->r_gpart), at<int>(x->ws, x->r_gcnt), dev_status, s);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -577,11 +578,10 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   if (b->num_prefill < b->num_seqs) {
     aa.seq_begin = b->num_prefill; aa.seq_end = b->num_seqs;
     const int units = (b->num_seqs - b->num_prefill) * n * x->nkv_l;
-    aa.splits = tpk::decode_splits(b->max_kv_len, units, x->num_sms);
-    const int64_t need = static_cast<int64_t>(b->num_seqs - b->num_prefill) * n * x->nq_l * (x->hd + 2) * aa.splits * 4;
-    if (need > static_cast<int64_t>(x->r_apart.bytes)) {
-      aa.splits = 1;  // the workspace was planned for fewer positions
-    }
+    // split partials must fit the workspace region planned for them
+    const int64_t per_split = static_cast<int64_t>(b->num_seqs - b->num_prefill) * n * x->nq_l * (x->hd + 2) * 4;
+    const int max_splits = static_cast<int>(std::min<int64_t>(64, static_cast<int64_t>(x->r_apart.bytes) / per_split));
+    aa.splits = tpk::decode_splits(b->max_kv_len, units, x->num_sms, x->hd, x->nq_l / x->nkv_l, std::max(1, max_splits));
     Timed tm(x, TP_K_ATTN_DECODE, s);
     e = tpk::launch_attention_decode(aa, s);
     if (e != cudaSuccess) return cuda_fail(e);

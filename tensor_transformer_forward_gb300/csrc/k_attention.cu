@@ -58,13 +58,17 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
   const int split = blockIdx.y;
   const int t = a.cu_q[b];
   const int L = a.ctx_len[b] + 1;
+  const int slot = a.slot[b];
+  // a slot or length outside the cache reads nothing (zero output) and flags the batch
+  const bool bad = slot < 0 || slot >= a.max_seqs || L < 1 || L > a.cap;
+  if (bad && threadIdx.x == 0 && split == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
   const int chunk = (L + a.splits - 1) / a.splits;
   const int k0 = split * chunk;
-  const int k1 = min(L, k0 + chunk);
+  const int k1 = bad ? k0 : min(L, k0 + chunk);
   const int nchunks = k1 > k0 ? (k1 - k0 + C::CK - 1) / C::CK : 0;
 
   const size_t plane = static_cast<size_t>(a.max_seqs) * a.nkv_l * a.cap * HD;
-  const size_t head_off = (static_cast<size_t>(a.slot[b]) * a.nkv_l + g) * a.cap * HD;
+  const size_t head_off = (static_cast<size_t>(bad ? 0 : slot) * a.nkv_l + g) * a.cap * HD;
   const __nv_bfloat16* Kc = reinterpret_cast<const __nv_bfloat16*>(a.kv) + (2 * static_cast<size_t>(r)) * plane + head_off;
   const __nv_bfloat16* Vc = reinterpret_cast<const __nv_bfloat16*>(a.kv) + (2 * static_cast<size_t>(r) + 1) * plane + head_off;
 
@@ -276,25 +280,58 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
   if (threadIdx.x == 0) a.counters[unit] = 0;
 }
 
-int decode_splits(int max_kv_len, int num_units, int num_sms) {
-  int by_len = (max_kv_len + 511) / 512;
-  int by_fill = (4 * num_sms + num_units - 1) / (num_units > 0 ? num_units : 1);
-  int s = by_len < by_fill ? by_len : by_fill;
-  if (s < 1) s = 1;
-  if (s > 64) s = 64;
-  return s;
+template <int HD, int G>
+static cudaError_t prepare_decode(int* ctas_per_sm) {
+  static int occ = 0;
+  if (occ == 0) {
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DecCfg<HD>::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_decode_kernel<HD, G>, 160, DecCfg<HD>::SMEM);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) occ = 1;
+  }
+  *ctas_per_sm = occ;
+  return cudaSuccess;
+}
+
+// Key splits per (sequence, rank, kv head): the count that minimises
+//   waves(units * s / resident CTAs) * (keys per split + fixed cost)
+// so that the grid fills whole waves of resident CTAs; ties go to fewer splits.
+int decode_splits(int max_kv_len, int num_units, int num_sms, int hd, int G, int max_splits) {
+  int per_sm = 1;
+  cudaError_t e = cudaErrorNotSupported;
+#define TP_OCC(HD_, G_) \
+  if (hd == HD_ && G == G_) e = prepare_decode<HD_, G_>(&per_sm);
+  TP_OCC(128, 1) TP_OCC(128, 2) TP_OCC(128, 4) TP_OCC(128, 8)
+  TP_OCC(64, 1) TP_OCC(64, 2) TP_OCC(64, 4) TP_OCC(64, 8)
+#undef TP_OCC
+  if (e != cudaSuccess) per_sm = 1;
+  const long long resident = static_cast<long long>(num_sms) * per_sm;
+  const int units = num_units > 0 ? num_units : 1;
+  int limit = max_kv_len / 32;
+  if (limit > max_splits) limit = max_splits;
+  if (limit > 64) limit = 64;
+  if (limit < 1) limit = 1;
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= limit; ++s) {
+    const long long waves = (static_cast<long long>(units) * s + resident - 1) / resident;
+    const long long cost = waves * ((max_kv_len + s - 1) / s + 96);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
 }
 
 template <int HD, int G>
 static cudaError_t launch_decode_hd(const AttnArgs& a, dim3 grid, cudaStream_t s) {
-  auto kern = attn_decode_kernel<HD, G>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DecCfg<HD>::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  kern<<<grid, 160, DecCfg<HD>::SMEM, s>>>(a);
+  int per_sm = 0;
+  cudaError_t e = prepare_decode<HD, G>(&per_sm);  // sets the shared-memory attribute once
+  if (e != cudaSuccess) return e;
+  attn_decode_kernel<HD, G><<<grid, 160, DecCfg<HD>::SMEM, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -387,6 +424,13 @@ __global__ void __launch_bounds__(320, 1)
   const int qlen = a.cu_q[b + 1] - a.cu_q[b];
   const int q0 = (qblocks - 1 - static_cast<int>(blockIdx.x) / (heads * nseq)) * C::BQ;
   if (q0 >= qlen) return;                                // uniform: before any barrier or TMEM use
+  {
+    const int sl = a.slot[b], kmax = a.ctx_len[b] + qlen;
+    if (sl < 0 || sl >= a.max_seqs || a.ctx_len[b] < 0 || kmax > a.cap) {  // outside the cache: flag, skip
+      if (threadIdx.x == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
+      return;
+    }
+  }
   const int r = hg / a.nq_l, h = hg % a.nq_l;
   const int g = h / (a.nq_l / a.nkv_l);
   const int ctx = a.ctx_len[b];

@@ -52,7 +52,9 @@ struct GemmParams {
   float* logits;
   int ld_logits, vocab;
   int32_t* out_ids;
-  int* done_counter;
+  int* done_counter;   // CTAs finished (weight-streaming argmax)
+  int* sched_counter;  // tiles handed out beyond the first wave (weight-streaming argmax)
+  unsigned long long* amax_keys;  // [T] per-token argmax keys, zero between launches
   QkvEpi qkv;
   int* status;
 };
@@ -65,7 +67,8 @@ struct GemmCfg {
   // as many stages as fit in ~200 KB (narrow tiles stream weights: more bytes in flight)
   static constexpr int STAGES = (204800 / STAGE_BYTES) > 12 ? 12 : (204800 / STAGE_BYTES);
   static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
-  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int QUEUE = 4;  // tile queue depth (weight-streaming path)
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * QUEUE;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64 + 1536;
 };
 
@@ -93,6 +96,21 @@ __device__ __forceinline__ bool amax_better(float v, int i, float bv, int bi) {
   if (vn != bn) return vn;
   if (!vn && v != bv) return v > bv;
   return i < bi;
+}
+
+// The same order as one unsigned 64-bit key (larger = better): the value's bits
+// made monotone in the high word (NaN above everything, -0 taken as +0), the
+// complemented index in the low word (lower index wins a tie).  Every key is
+// above 0, the cleared state.
+__device__ __forceinline__ unsigned long long amax_key(float v, int i) {
+  uint32_t hi;
+  if (v != v) {
+    hi = 0xffffffffu;
+  } else {
+    const uint32_t b = __float_as_uint(v == 0.0f ? 0.0f : v);
+    hi = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  }
+  return (static_cast<unsigned long long>(hi) << 32) | static_cast<unsigned long long>(~static_cast<uint32_t>(i));
 }
 
 // 8 consecutive values as bf16 (the KV cache) or fp16 (GEMM / attention operands)
@@ -181,16 +199,29 @@ struct TokPos {
   bool ok, prefill;
 };
 __device__ __forceinline__ TokPos token_position(const QkvEpi& q, int t) {
-  int lo = 0, hi = q.B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (q.cu_q[mid] <= t) lo = mid;
-    else hi = mid - 1;
+  // decode sequences (one token each) follow the prefill ones: direct index;
+  // a prefill token searches the prefill sequences only
+  int lo;
+  const int t_dec = q.num_prefill < q.B ? q.cu_q[q.num_prefill] : INT_MAX;
+  if (t >= t_dec) {
+    lo = q.num_prefill + (t - t_dec);
+    if (lo >= q.B) {  // a "decode" sequence with more than one token: reject, stay in bounds
+      TokPos bad{0, 0, false, false};
+      return bad;
+    }
+  } else {
+    lo = 0;
+    int hi = q.num_prefill - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (q.cu_q[mid] <= t) lo = mid;
+      else hi = mid - 1;
+    }
   }
   TokPos tp;
   tp.pos = q.ctx_len[lo] + (t - q.cu_q[lo]);
   tp.seq_slot = q.slot[lo];
-  tp.ok = tp.pos >= 0 && tp.pos < q.cap && tp.pos < q.max_pos;
+  tp.ok = tp.pos >= 0 && tp.pos < q.cap && tp.pos < q.max_pos && tp.seq_slot >= 0 && tp.seq_slot < q.max_seqs;
   tp.prefill = lo < q.num_prefill;
   return tp;
 }
@@ -234,15 +265,26 @@ __device__ __forceinline__ void qkv_head(const GemmParams& p, int t, const TokPo
                         ((static_cast<size_t>(tp.seq_slot) * q.nkv_l + (sh - q.nq_l)) * q.cap + tp.pos) * HD;
 #pragma unroll
   for (int j = 0; j < HALF / 8; ++j) {
+    // 16-byte loads: 8 norm weights of each half, 8 (cos, sin) pairs
+    const uint4 w0 = *reinterpret_cast<const uint4*>(nw + j * 8);
+    const uint4 w1 = *reinterpret_cast<const uint4*>(nw + HALF + j * 8);
+    const float wa[8] = {bf16lo(w0.x), bf16hi(w0.x), bf16lo(w0.y), bf16hi(w0.y),
+                         bf16lo(w0.z), bf16hi(w0.z), bf16lo(w0.w), bf16hi(w0.w)};
+    const float wb[8] = {bf16lo(w1.x), bf16hi(w1.x), bf16lo(w1.y), bf16hi(w1.y),
+                         bf16lo(w1.z), bf16hi(w1.z), bf16lo(w1.w), bf16hi(w1.w)};
+    float4 c4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c4[i] = __ldg(reinterpret_cast<const float4*>(cs + j * 8) + i);
+    const float cx[8] = {c4[0].x, c4[0].z, c4[1].x, c4[1].z, c4[2].x, c4[2].z, c4[3].x, c4[3].z};
+    const float sy[8] = {c4[0].y, c4[0].w, c4[1].y, c4[1].w, c4[2].y, c4[2].w, c4[3].y, c4[3].w};
     float y0[8], y1[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int d = j * 8 + i;
-      const float u0 = h[d] * inv * bf2f(nw[d]);
-      const float u1 = h[d + HALF] * inv * bf2f(nw[d + HALF]);
-      const float2 c = cs[d];
-      y0[i] = u0 * c.x - u1 * c.y;
-      y1[i] = u1 * c.x + u0 * c.y;
+      const float u0 = h[d] * inv * wa[i];
+      const float u1 = h[d + HALF] * inv * wb[i];
+      y0[i] = u0 * cx[i] - u1 * sy[i];
+      y1[i] = u1 * cx[i] + u0 * sy[i];
     }
     if (!is_q) {
       store8(kdst + j * 8, y0);
@@ -312,6 +354,9 @@ __global__ void __launch_bounds__(192, 1)
 #define TFULL(b) (bar0 + 8u * (2 * STAGES + (b)))
 #define TEMPTY(b) (bar0 + 8u * (2 * STAGES + 2 + (b)))
 #define DRAIN (bar0 + 8u * (2 * STAGES + 4))
+#define QFULL(k) (bar0 + 8u * (2 * STAGES + 5 + (k)))
+#define QEMPTY(k) (bar0 + 8u * (2 * STAGES + 5 + C::QUEUE + (k)))
+  volatile int* queue = reinterpret_cast<volatile int*>(tmem_slot + 4);  // [QUEUE] tile ids
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -323,6 +368,10 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(TEMPTY(b), 4);
     }
     mbar_init(DRAIN, 1);
+    for (int k = 0; k < C::QUEUE; ++k) {
+      mbar_init(QFULL(k), 1);
+      mbar_init(QEMPTY(k), 5);  // the MMA thread and the 4 epilogue warps
+    }
     *abort_flag = 0;
     *last_flag = 0;
     fence_barrier_init();
@@ -353,7 +402,23 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      // Weight-streaming path: tiles are handed out dynamically (first wave by
+      // CTA index, then an atomic counter), so SMs that stream faster take more
+      // tiles; each tile id goes through a small queue to the MMA and epilogue
+      // warps, -1 ends it.  Otherwise a static round-robin over the tiles.
+      int qk = 0;
+      for (int u = blockIdx.x; ok && (SWAP || u < units);) {
+        if constexpr (SWAP) {
+          const int id = u < units ? u : -1;
+          if (!mbar_wait(QEMPTY(qk % C::QUEUE), ((qk / C::QUEUE) & 1) ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          queue[qk % C::QUEUE] = id;
+          mbar_arrive(QFULL(qk % C::QUEUE));
+          ++qk;
+          if (id < 0) break;
+        }
         const Unit un = unit_of(p, u);
         const int t0 = un.tt * TM_T, f0 = un.tf * TM_F;
         for (int g = un.g0; g < un.g1; ++g) {
@@ -371,6 +436,8 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_2d(wdst, &tmW, FULL(s), kb * 64, r * p.w_row_seg + f0);
           ++it;
         }
+        if constexpr (SWAP) u = static_cast<int>(gridDim.x) + atomicAdd(p.sched_counter, 1);
+        else u += gridDim.x;
       }
       // every load issued has landed before the CTA may exit
       for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
@@ -380,9 +447,16 @@ __global__ void __launch_bounds__(192, 1)
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t idesc = idesc_f16_f32(128, BN);
-      int it = 0, seg = 0;
+      int it = 0, seg = 0, qk = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      for (int u = blockIdx.x; ok && (SWAP || u < units); u += gridDim.x) {
+        if constexpr (SWAP) {
+          if (!mbar_wait(QFULL(qk % C::QUEUE), (qk / C::QUEUE) & 1, abort_flag, p.status)) break;
+          u = queue[qk % C::QUEUE];
+          mbar_arrive(QEMPTY(qk % C::QUEUE));
+          ++qk;
+          if (u < 0) break;
+        }
         const Unit un = unit_of(p, u);
         for (int g = un.g0; ok && g < un.g1;) {
           const int gend = min(un.g1, (g / p.kb_seg + 1) * p.kb_seg);
@@ -426,9 +500,16 @@ __global__ void __launch_bounds__(192, 1)
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const int et = threadIdx.x - 64;  // epilogue thread 0..127
-    int seg = 0;
+    int seg = 0, qk = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    for (;;) {
+      ok = mbar_wait(QFULL(qk % C::QUEUE), (qk / C::QUEUE) & 1, abort_flag, p.status);
+      if (!named_bar_and(1, 128, ok)) break;
+      const int u = queue[qk % C::QUEUE];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(QEMPTY(qk % C::QUEUE));
+      ++qk;
+      if (u < 0) break;  // uniform: every epilogue thread read the same id
       const Unit un = unit_of(p, u);
       const int f = un.tf * 128 + row;
       const int t0 = un.tt * BN;
@@ -508,12 +589,11 @@ __global__ void __launch_bounds__(192, 1)
       if (lane == 0) mbar_arrive(TEMPTY(b));
       ++seg;
     }
-    // CTA partials -> the last CTA to finish reduces them (no waiting)
+    // Each CTA folds its per-token best into one 64-bit key per token with
+    // atomicMax (key order = torch.argmax order); the last CTA to finish reads the
+    // keys back, writes the ids and clears the keys for the next launch.
     if (named_bar_and(1, 128, ok)) {
-      for (int t = et; t < p.T; t += 128) {
-        p.amax_val[static_cast<size_t>(blockIdx.x) * p.amax_ld + t] = best_v[t];
-        p.amax_idx[static_cast<size_t>(blockIdx.x) * p.amax_ld + t] = best_i[t];
-      }
+      for (int t = et; t < p.T; t += 128) atomicMax(p.amax_keys + t, amax_key(best_v[t], best_i[t]));
       __threadfence();
       named_bar_sync(1, 128);
       if (et == 0) *last_flag = (atomicAdd(p.done_counter, 1) == static_cast<int>(gridDim.x) - 1) ? 1 : 0;
@@ -521,19 +601,13 @@ __global__ void __launch_bounds__(192, 1)
       if (*last_flag) {
         __threadfence();
         for (int t = et; t < p.T; t += 128) {
-          float bv = -INFINITY;
-          int bi = INT_MAX;
-          for (int c = 0; c < static_cast<int>(gridDim.x); ++c) {
-            const float ov = __ldcg(p.amax_val + static_cast<size_t>(c) * p.amax_ld + t);
-            const int oi = __ldcg(p.amax_idx + static_cast<size_t>(c) * p.amax_ld + t);
-            if (amax_better(ov, oi, bv, bi)) {
-              bv = ov;
-              bi = oi;
-            }
-          }
-          p.out_ids[t] = bi;
+          const unsigned long long k = atomicExch(p.amax_keys + t, 0ull);
+          p.out_ids[t] = static_cast<int>(~static_cast<uint32_t>(k & 0xffffffffull));
         }
-        if (et == 0) *p.done_counter = 0;
+        if (et == 0) {  // every CTA has taken its last tile id: ready for the next launch
+          *p.done_counter = 0;
+          *p.sched_counter = 0;
+        }
       }
     }
   } else {
@@ -634,8 +708,10 @@ __global__ void __launch_bounds__(192, 1)
         if (p.splits > 1) {
           const int tile = un.tt * p.tiles_f + un.tf;
           float* part = p.partials + (static_cast<size_t>(tile) * p.splits + un.split) * (BN * 128);
+          if (row_ok) {  // rows past the last token are never read
 #pragma unroll
-          for (int c = 0; c < BN; ++c) part[c * 128 + row] = acc[c];
+            for (int c = 0; c < BN; ++c) part[c * 128 + row] = acc[c];
+          }
           __threadfence();
           named_bar_sync(1, 128);
           if (threadIdx.x == 64) {
@@ -647,12 +723,14 @@ __global__ void __launch_bounds__(192, 1)
           if (!last) continue;
           __threadfence();
           const float* base = p.partials + static_cast<size_t>(tile) * p.splits * (BN * 128);
+          if (row_ok) {
 #pragma unroll
-          for (int c = 0; c < BN; ++c) acc[c] = __ldcg(base + c * 128 + row);
-          for (int s = 1; s < p.splits; ++s) {
-            const float* ps = base + static_cast<size_t>(s) * (BN * 128);
+            for (int c = 0; c < BN; ++c) acc[c] = __ldcg(base + c * 128 + row);
+            for (int s = 1; s < p.splits; ++s) {
+              const float* ps = base + static_cast<size_t>(s) * (BN * 128);
 #pragma unroll
-            for (int c = 0; c < BN; ++c) acc[c] += __ldcg(ps + c * 128 + row);
+              for (int c = 0; c < BN; ++c) acc[c] += __ldcg(ps + c * 128 + row);
+            }
           }
           if (threadIdx.x == 64) p.counters[tile] = 0;
         }
@@ -698,6 +776,8 @@ __global__ void __launch_bounds__(192, 1)
 #undef TFULL
 #undef TEMPTY
 #undef DRAIN
+#undef QFULL
+#undef QEMPTY
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -842,6 +922,8 @@ cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partia
   gp.vocab = pr.vocab;
   gp.out_ids = pr.out_ids;
   gp.done_counter = counters;
+  gp.sched_counter = counters + 1;
+  gp.amax_keys = reinterpret_cast<unsigned long long*>(counters + kArgmaxKeyOffset);
   gp.qkv = pr.qkv;
   gp.status = status;
   const int g = pl.grid;

@@ -84,6 +84,12 @@ GemmPlan plan_gemm(const GemmProblem& pr, int num_sms);
 bool make_tmap_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows,
                   bool bf16);
 // workspace: partials (fp32) and per-tile counters (int, zeroed once, self-resetting)
+// counters (launch_gemm): split-K tile counters from index 0 (fewer than 256 tiles
+// are ever split); the weight-streaming argmax uses [0] and [1] and, from int
+// index kArgmaxKeyOffset, one 64-bit key per token (at most 64).  All zero
+// between launches; the kernels leave them zero.
+constexpr int kArgmaxKeyOffset = 2048;
+constexpr int kGemmCounterInts = kArgmaxKeyOffset + 2 * 64;
 cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& plan, float* partials, int* counters,
                         int* status, cudaStream_t stream);
 int gemm_num_tiles_f(const GemmProblem& pr, const GemmPlan& plan);
@@ -116,7 +122,7 @@ struct AttnArgs {
 };
 cudaError_t launch_attention_prefill(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s);
-int decode_splits(int max_kv_len, int num_units, int num_sms);
+int decode_splits(int max_kv_len, int num_units, int num_sms, int hd, int G, int max_splits);
 
 cudaError_t launch_final_norm_select(const void* hidden, int H, const int32_t* cu_q, int B, const void* w,
                                      float eps, void* out, int32_t* idx_scratch, cudaStream_t s);

@@ -1,19 +1,19 @@
 // LM head + greedy argmax for callers that cannot allocate device memory.
 //
 // tp_lm_head_argmax needs a caller-allocated workspace (from
-// tp_workspace_init) for its scratch: the normalised last-token rows, the
-// per-CTA argmax partials and an arrival counter.  Some callers cannot hand
-// one over: code that must not call cudaMalloc at that point (it can
-// synchronise the device, or the process's device memory belongs to another
-// allocator), or a caller that only holds the model weights and its inputs and
-// outputs.  tp_lm_head_argmax_static runs the same kernels with that scratch in
-// a fixed-size array compiled into this library instead.
+// tp_workspace_init) for its scratch: the normalised last-token rows, counters
+// (CTA arrivals, tiles handed out) and the per-token argmax keys.  Some callers
+// cannot hand one over: code that must not call cudaMalloc at that point (it
+// can synchronise the device, or the process's device memory belongs to
+// another allocator), or a caller that only holds the model weights and its
+// inputs and outputs.  tp_lm_head_argmax_static runs the same kernels with that
+// scratch in a fixed-size array compiled into this library instead.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds it until the process exits, and every call on a device shares
-// it (it keeps the previous call's contents).  The arrival counter is cleared
-// on the stream at the start of each call; the other scratch is overwritten
-// before it is read.  Two calls that overlap on the GPU (other streams) race on
+// it (it keeps the previous call's contents).  The counters and keys are
+// cleared on the stream at the start of each call; the other scratch is
+// overwritten before it is read.  Two calls that overlap on the GPU (other streams) race on
 // the array and must not be issued.
 #include <cuda_runtime.h>
 
@@ -27,19 +27,17 @@
 namespace {
 constexpr int kMaxSeqs = TP_STATIC_SCRATCH_MAX_SEQS;
 constexpr int kMaxHidden = TP_STATIC_SCRATCH_MAX_HIDDEN;
-constexpr int kMaxCtas = 256;  // one argmax partial per persistent CTA (never more CTAs than SMs)
 constexpr int kMaxDevices = 64;
 
 // byte layout of the scratch array
 constexpr size_t kZOff = 0;                                              // fp16 [kMaxSeqs][kMaxHidden]
 constexpr size_t kRowOff = kZOff + size_t(kMaxSeqs) * kMaxHidden * 2;    // int32 [kMaxSeqs]
-constexpr size_t kValOff = kRowOff + 256;                                // float [kMaxCtas][kMaxSeqs]
-constexpr size_t kIdxOff = kValOff + size_t(kMaxCtas) * kMaxSeqs * 4;    // int32 [kMaxCtas][kMaxSeqs]
-constexpr size_t kCntOff = kIdxOff + size_t(kMaxCtas) * kMaxSeqs * 4;    // int32 arrival counter
-constexpr size_t kScratchBytes = kCntOff + 256;
+constexpr size_t kCntOff = kRowOff + 256;                                // GEMM counters and argmax keys
+constexpr size_t kCntBytes = size_t(tpk::kGemmCounterInts) * 4;
+constexpr size_t kScratchBytes = kCntOff + kCntBytes;
 }  // namespace
 
-// The scratch (about 1.2 MiB).  Host code only ever sees a host-side stand-in
+// The scratch (about 1 MiB).  Host code only ever sees a host-side stand-in
 // for this name; kernels get its device address from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_lm_head_scratch[kScratchBytes];
 
@@ -77,7 +75,6 @@ extern "C" tp_status tp_lm_head_argmax_static(tp_ctx* ctx, const void* head_shar
   tp_status st = static_cast<tp_status>(tpk::ctx_head_view(ctx, &hv));
   if (st != TP_OK) return st;
   if (hv.H > kMaxHidden) return TP_ERR_INVALID_ARG;       // beyond the array's hidden-size limit
-  if (hv.num_sms > kMaxCtas) return TP_ERR_UNSUPPORTED;
   char* scratch = nullptr;
   st = scratch_address(&scratch);
   if (st != TP_OK) return st;
@@ -93,13 +90,13 @@ extern "C" tp_status tp_lm_head_argmax_static(tp_ctx* ctx, const void* head_shar
   g.w = w + hv.lm_head_off; g.w_rows = static_cast<int64_t>(hv.n) * hv.v_l; g.w_cols = hv.H; g.w_ld = hv.H;
   g.T = B; g.N = static_cast<int>(static_cast<int64_t>(hv.n) * hv.v_l); g.n_seg = 1; g.k_seg = hv.H;
   g.epi = tpk::EPI_ARGMAX; g.out = nullptr; g.ldo = 8; g.out_cols = 0;
-  g.amax_val = reinterpret_cast<float*>(scratch + kValOff);
-  g.amax_idx = reinterpret_cast<int*>(scratch + kIdxOff);
+  g.amax_val = nullptr;  // per-tile partials: only the many-token path uses them
+  g.amax_idx = nullptr;
   g.amax_ld = B; g.logits = out_logits; g.ld_logits = hv.vocab; g.vocab = hv.vocab; g.out_ids = out_ids;
   const tpk::GemmPlan pl = tpk::plan_gemm(g, hv.num_sms);
-  if (!pl.swap || pl.grid > kMaxCtas) return TP_ERR_UNSUPPORTED;
+  if (!pl.swap) return TP_ERR_UNSUPPORTED;
   int* counter = reinterpret_cast<int*>(scratch + kCntOff);
-  e = cudaMemsetAsync(counter, 0, sizeof(int), s);  // the last-arriving CTA counts from zero
+  e = cudaMemsetAsync(counter, 0, kCntBytes, s);  // counters and argmax keys start at zero
   if (e != cudaSuccess) return TP_ERR_CUDA;
   e = tpk::launch_gemm(g, pl, nullptr, counter, dev_status, s);
   return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;

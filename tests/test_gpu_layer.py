@@ -69,3 +69,32 @@ def test_untied_head_uneven_vocab():
     w = synth.Workload("untied_uneven", s, (3,), ((17, 0),), (5, 9), 1, True)
     g = GpuStep(w, 3, perturbed=True)
     check_step(g, [0, 1, 2])
+
+
+def test_slot_or_length_outside_the_cache_flags_bad_token():
+    """A batch whose device arrays point outside the cache (a slot >= max_seqs,
+    or a cached length beyond the capacity) is caught by the kernels' own bounds
+    checks: nothing outside the cache is read or written and the status word
+    reports TP_ERR_BAD_TOKEN."""
+    import torch
+    import synth.device as sd
+    from tensor_transformer_forward_gb300 import TP_ERR_BAD_TOKEN, TP_OK, tp_read_status
+    from tensor_transformer_forward_gb300.runner import TPRunner
+    from tests.gpu_harness import model_config
+    s = synth.TINY
+    r = TPRunner(model_config(s, 2), 1, max_seqs=2, capacity=64, max_tokens=16)
+    r.load_layer(0, sd.layer_weights(s, 0))
+    hidden = torch.randn(8, s.hidden, device="cuda")
+    cases = [r.make_batch([1, 1], [3, 4], [0, 2]),            # decode, slot 2 of 2
+             r.make_batch([5, 1], [0, 4], [3, 0]),            # prefill, slot 3 of 2
+             r.make_batch([1, 1], [3, 4], [0, 1])]            # decode, length tampered below
+    cases[2].ctx_len[1] = 100                                 # 101 keys in a 64-position cache
+    for batch in cases:
+        r.status.zero_()
+        h = hidden[: batch.num_tokens].clone()
+        r.layer(0, batch, h)
+        assert tp_read_status(r.status) == TP_ERR_BAD_TOKEN
+    r.status.zero_()
+    ok = r.make_batch([1, 1], [3, 4], [0, 1])
+    r.layer(0, ok, hidden[:2].clone())
+    assert tp_read_status(r.status) == TP_OK
