@@ -59,8 +59,16 @@ struct GemmParams {
   int* status;
 };
 
-template <int BN>
+template <int BN, int EPI = EPI_STORE, bool ACC = false, bool SWAP = false>
 struct GemmCfg {
+  // epilogue warps: 8 (two per TMEM lane quarter, splitting the columns) where the
+  // columns split into independent halves, else 4
+  static constexpr int EW =
+      (!SWAP && (EPI == EPI_STORE || EPI == EPI_RESID || (EPI == EPI_SILU && BN >= 256) ||
+                 (EPI == EPI_QKV && !ACC && BN >= 256)))
+          ? 8
+          : 4;
+  static constexpr int THREADS = 64 + 32 * EW;
   static constexpr int A_BYTES = 128 * 128;  // 128 rows x 64 fp16
   static constexpr int B_BYTES = BN * 128;   // BN rows x 64 fp16
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -87,7 +95,9 @@ __device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
   return un;
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+// fast divide: the result is rounded to fp16 (11 bits) next, far coarser than its ~2 ulp fp32 error;
+// for g very negative the divisor overflows to inf and the quotient is 0, the correct limit
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // (value, index) order of torch.argmax: larger value first, NaN above all,
 // then the lower index.
@@ -131,6 +141,24 @@ __device__ __forceinline__ void store8(__half* dst, const float* x) {
   *reinterpret_cast<uint4*>(dst) = w;
 }
 
+// 32-byte global accesses (one full sector per thread and instruction)
+__device__ __forceinline__ void st32B(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+__device__ __forceinline__ void ld32B(const void* p, float (&v)[8]) {
+  asm volatile("ld.global.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+               : "l"(p)
+               : "memory");
+}
+__device__ __forceinline__ void st32B(void* p, const float (&v)[8]) {
+  asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]),
+               "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+               : "memory");
+}
+
 // ---- epilogue stores for one token row, 32 consecutive tile columns ----
 // EPI_STORE writes fp16 (the next GEMM's operand); EPI_RESID adds the
 // rank-summed row into the fp32 residual stream in place.
@@ -138,16 +166,15 @@ template <int EPI>
 __device__ __forceinline__ void store_chunk(const GemmParams& p, int t, int f, const float* v) {
   if constexpr (EPI == EPI_RESID) {
     float* o = reinterpret_cast<float*>(p.out) + static_cast<size_t>(t) * p.ldo + f;
-    if (f + 32 <= p.out_cols) {
-      float4* o4 = reinterpret_cast<float4*>(o);
+    if (f + 32 <= p.out_cols && (reinterpret_cast<uintptr_t>(o) & 31) == 0) {
+      float r[4][8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float4 r = o4[j];
-        r.x += v[j * 4 + 0];
-        r.y += v[j * 4 + 1];
-        r.z += v[j * 4 + 2];
-        r.w += v[j * 4 + 3];
-        o4[j] = r;
+      for (int j = 0; j < 4; ++j) ld32B(o + j * 8, r[j]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r[j][i] += v[j * 8 + i];
+        st32B(o + j * 8, r[j]);
       }
     } else {
 #pragma unroll
@@ -156,7 +183,15 @@ __device__ __forceinline__ void store_chunk(const GemmParams& p, int t, int f, c
     }
   } else {
     __half* o = reinterpret_cast<__half*>(p.out) + static_cast<size_t>(t) * p.ldo + f;
-    if (f + 32 <= p.out_cols) {
+    if (f + 32 <= p.out_cols && (reinterpret_cast<uintptr_t>(o) & 31) == 0) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = pack_f16x2(v[j * 16 + 2 * i], v[j * 16 + 2 * i + 1]);
+        st32B(o + j * 16, w);
+      }
+    } else if (f + 32 <= p.out_cols) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) store8(o + j * 8, v + j * 8);
     } else {
@@ -310,9 +345,9 @@ __device__ __forceinline__ void qkv_head(const GemmParams& p, int t, const TokPo
 // Streams the heads of one accumulator tile (tokens on the M side) through qkv_head.
 template <int BN, int HD>
 __device__ __forceinline__ void qkv_stream(const GemmParams& p, uint32_t ta, int t, const TokPos& tp, int f0,
-                                           bool row_ok) {
+                                           bool row_ok, int c_begin, int c_end) {
 #pragma unroll 1
-  for (int hb = 0; hb < BN / HD; ++hb) {
+  for (int hb = c_begin / HD; hb < c_end / HD; ++hb) {
     const int col0 = f0 + hb * HD;
     if (col0 >= p.N) break;  // warp-uniform
     float h[HD];
@@ -328,10 +363,10 @@ __device__ __forceinline__ void qkv_stream(const GemmParams& p, uint32_t ta, int
 }
 
 template <int BN, int EPI, bool ACC, bool SWAP>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const GemmParams p) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, EPI, ACC, SWAP>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -365,7 +400,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(TFULL(b), 1);
-      mbar_init(TEMPTY(b), 4);
+      mbar_init(TEMPTY(b), C::EW);
     }
     mbar_init(DRAIN, 1);
     for (int k = 0; k < C::QUEUE; ++k) {
@@ -611,8 +646,15 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..5), tokens on the M side ----------------
+    // ---------------- epilogue (warps 2..), tokens on the M side ----------------
+    // A warp reads TMEM lanes 32*(warp % 4) .. +31 (one token row per thread);
+    // with 8 epilogue warps the two warps of a lane quarter take the two halves
+    // of the tile's columns (contiguous ranges that hold whole heads / whole
+    // gate-up blocks), so the epilogue keeps pace with the MMA.
+    constexpr int NSPLIT = C::EW / 4;
+    constexpr int BNH = BN / NSPLIT;  // accumulator columns per thread
     const int q = warp & 3;
+    const int cbase = ((warp - 2) >> 2) * BNH;
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
     int seg = 0;
@@ -625,7 +667,7 @@ __global__ void __launch_bounds__(192, 1)
       if constexpr (EPI == EPI_QKV) {
         if (row_ok) {
           tp = token_position(p.qkv, t);
-          if (!tp.ok) raise_flag(p.status, TP_DEVFLAG_BAD_TOKEN);
+          if (!tp.ok && cbase == 0) raise_flag(p.status, TP_DEVFLAG_BAD_TOKEN);
         }
       }
       if constexpr (!ACC) {
@@ -636,13 +678,14 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t ta = lane_addr + static_cast<uint32_t>(b * BN);
         if constexpr (EPI == EPI_QKV) {
           if (BN >= 128 && p.qkv.hd == 128) {
-            qkv_stream<BN, (BN >= 128 ? 128 : 64)>(p, ta, t, tp, f0, row_ok);
+            qkv_stream<BN, (BN >= 128 ? 128 : 64)>(p, ta, t, tp, f0, row_ok, cbase, cbase + BNH);
           } else {
-            qkv_stream<BN, 64>(p, ta, t, tp, f0, row_ok);
+            qkv_stream<BN, 64>(p, ta, t, tp, f0, row_ok, cbase, cbase + BNH);
           }
         } else if constexpr (EPI == EPI_SILU) {
+          // gate/up interleaved in 64-column blocks: 128 accumulator columns = 64 outputs
 #pragma unroll 1
-          for (int qb = 0; qb < BN / 128; ++qb) {
+          for (int qb = cbase / 128; qb < (cbase + BNH) / 128; ++qb) {
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
               float gv[32], uv[32];
@@ -666,7 +709,7 @@ __global__ void __launch_bounds__(192, 1)
           }
         } else {
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int c = cbase / 32; c < (cbase + BNH) / 32; ++c) {
             float v[32];
             tc_ld32(ta + c * 32, v);
             if (row_ok) store_chunk<EPI>(p, t, f0 + c * 32, v);
@@ -677,9 +720,9 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) mbar_arrive(TEMPTY(b));
         ++seg;
       } else {
-        float acc[BN];
+        float acc[BNH];  // this thread's columns cbase .. cbase + BNH
 #pragma unroll
-        for (int i = 0; i < BN; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < BNH; ++i) acc[i] = 0.0f;
         bool ok = true;
         for (int g = un.g0; g < un.g1;) {
           g = min(un.g1, (g / p.kb_seg + 1) * p.kb_seg);
@@ -690,9 +733,9 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t ta = lane_addr + static_cast<uint32_t>(b * BN);
+          const uint32_t ta = lane_addr + static_cast<uint32_t>(b * BN + cbase);
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int c = 0; c < BNH / 32; ++c) {
             float v[32];
             tc_ld32(ta + c * 32, v);
 #pragma unroll
@@ -704,38 +747,41 @@ __global__ void __launch_bounds__(192, 1)
           ++seg;
         }
         // every epilogue thread takes the same path from here (named barriers follow)
-        if (!named_bar_and(1, 128, ok)) break;
+        if (!named_bar_and(1, 32 * C::EW, ok)) break;
         if (p.splits > 1) {
           const int tile = un.tt * p.tiles_f + un.tf;
           float* part = p.partials + (static_cast<size_t>(tile) * p.splits + un.split) * (BN * 128);
           if (row_ok) {  // rows past the last token are never read
 #pragma unroll
-            for (int c = 0; c < BN; ++c) part[c * 128 + row] = acc[c];
+            for (int c = 0; c < BNH; ++c) part[(cbase + c) * 128 + row] = acc[c];
           }
           __threadfence();
-          named_bar_sync(1, 128);
+          named_bar_sync(1, 32 * C::EW);
           if (threadIdx.x == 64) {
             const int old = atomicAdd(p.counters + tile, 1);
             *last_flag = (old == p.splits - 1) ? 1 : 0;
           }
-          named_bar_sync(1, 128);
+          named_bar_sync(1, 32 * C::EW);
           const bool last = *last_flag != 0;
           if (!last) continue;
           __threadfence();
           const float* base = p.partials + static_cast<size_t>(tile) * p.splits * (BN * 128);
           if (row_ok) {
 #pragma unroll
-            for (int c = 0; c < BN; ++c) acc[c] = __ldcg(base + c * 128 + row);
+            for (int c = 0; c < BNH; ++c) acc[c] = __ldcg(base + (cbase + c) * 128 + row);
             for (int s = 1; s < p.splits; ++s) {
               const float* ps = base + static_cast<size_t>(s) * (BN * 128);
 #pragma unroll
-              for (int c = 0; c < BN; ++c) acc[c] += __ldcg(ps + c * 128 + row);
+              for (int c = 0; c < BNH; ++c) acc[c] += __ldcg(ps + (cbase + c) * 128 + row);
             }
           }
+          // the counter is cleared after every thread of this CTA has passed the
+          // second barrier above (it is read once per tile, by thread 64)
           if (threadIdx.x == 64) p.counters[tile] = 0;
         }
         if (row_ok) {
           if constexpr (EPI == EPI_QKV) {
+            static_assert(!ACC || C::EW == 4, "split-K QKV keeps whole heads in one thread");
             if (tp.ok) {
               if constexpr (BN >= 128) {
                 if (p.qkv.hd == 128) {
@@ -752,11 +798,13 @@ __global__ void __launch_bounds__(192, 1)
             }
           } else if constexpr (EPI == EPI_SILU) {
 #pragma unroll
-            for (int qb = 0; qb < BN / 128; ++qb)
+            for (int qb = 0; qb < BNH / 128; ++qb)
 #pragma unroll
               for (int h = 0; h < 2; ++h)
-                store_silu(p, t, f0 / 2 + qb * 64 + h * 32, acc + qb * 128 + h * 32, acc + qb * 128 + 64 + h * 32);
+                store_silu(p, t, f0 / 2 + (cbase / 128 + qb) * 64 + h * 32, acc + qb * 128 + h * 32,
+                           acc + qb * 128 + 64 + h * 32);
           } else if constexpr (EPI == EPI_ARGMAX) {
+            static_assert(C::EW == 4, "argmax keeps a whole tile row in one thread");
             float best = -INFINITY;
             int bi = -1;
 #pragma unroll
@@ -765,7 +813,7 @@ __global__ void __launch_bounds__(192, 1)
             p.amax_idx[static_cast<size_t>(un.tf) * p.amax_ld + t] = bi < 0 ? INT_MAX : bi;
           } else {
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) store_chunk<EPI>(p, t, f0 + c * 32, acc + c * 32);
+            for (int c = 0; c < BNH / 32; ++c) store_chunk<EPI>(p, t, f0 + cbase + c * 32, acc + c * 32);
           }
         }
       }
@@ -880,14 +928,15 @@ template <int BN, int EPI, bool ACC, bool SWAP>
 static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, const GemmParams& gp, int grid,
                                   cudaStream_t s) {
   auto kern = gemm_tc_kernel<BN, EPI, ACC, SWAP>;
-  constexpr int smem = GemmCfg<BN>::SMEM;
+  using Cfg = GemmCfg<BN, EPI, ACC, SWAP>;
+  constexpr int smem = Cfg::SMEM;
   static bool attr_done = false;  // per instantiation
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  kern<<<grid, 192, smem, s>>>(mx, mw, gp);
+  kern<<<grid, Cfg::THREADS, smem, s>>>(mx, mw, gp);
   return cudaGetLastError();
 }
 
