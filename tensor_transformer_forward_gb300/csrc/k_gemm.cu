@@ -77,7 +77,12 @@ struct GemmCfg {
   static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int QUEUE = 4;  // tile queue depth (weight-streaming path)
   static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * QUEUE;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64 + 1536;
+  // outputs leave through TMA stores (fp16) / TMA reduce-adds (fp32 residual) from one
+  // 32-row x 128-byte staging box per epilogue warp
+  static constexpr bool TMA_OUT = !SWAP && (EPI == EPI_STORE || EPI == EPI_SILU || EPI == EPI_RESID);
+  static constexpr int OUT_BYTES = TMA_OUT ? EW * 4096 : 0;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + OUT_BYTES + NUM_BARS * 8 + 64 + 1536;
+  static_assert(SMEM <= 232448, "shared memory per block");
 };
 
 struct Unit {
@@ -141,73 +146,42 @@ __device__ __forceinline__ void store8(__half* dst, const float* x) {
   *reinterpret_cast<uint4*>(dst) = w;
 }
 
-// 32-byte global accesses (one full sector per thread and instruction)
-__device__ __forceinline__ void st32B(void* p, const uint32_t (&w)[8]) {
-  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-               : "memory");
+// ---- TMA-store staging: one thread = one row of a 32-row x 128-byte box, written
+// with the 128-byte swizzle the tensor map declares (16-byte chunk c of row r at
+// chunk c ^ (r & 7)), so the 8 rows of a bank group never collide.
+__device__ __forceinline__ void stage_f32x32(uint8_t* box, int r, const float* v) {
+  uint8_t* rowp = box + r * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<float4*>(rowp + ((c ^ (r & 7)) << 4)) = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
 }
-__device__ __forceinline__ void ld32B(const void* p, float (&v)[8]) {
-  asm volatile("ld.global.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
-               : "l"(p)
-               : "memory");
-}
-__device__ __forceinline__ void st32B(void* p, const float (&v)[8]) {
-  asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]),
-               "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
-               : "memory");
-}
-
-// ---- epilogue stores for one token row, 32 consecutive tile columns ----
-// EPI_STORE writes fp16 (the next GEMM's operand); EPI_RESID adds the
-// rank-summed row into the fp32 residual stream in place.
-template <int EPI>
-__device__ __forceinline__ void store_chunk(const GemmParams& p, int t, int f, const float* v) {
-  if constexpr (EPI == EPI_RESID) {
-    float* o = reinterpret_cast<float*>(p.out) + static_cast<size_t>(t) * p.ldo + f;
-    if (f + 32 <= p.out_cols && (reinterpret_cast<uintptr_t>(o) & 31) == 0) {
-      float r[4][8];
+__device__ __forceinline__ void stage_f16x64(uint8_t* box, int r, const float* v) {
+  uint8_t* rowp = box + r * 128;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) ld32B(o + j * 8, r[j]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) r[j][i] += v[j * 8 + i];
-        st32B(o + j * 8, r[j]);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (f + i < p.out_cols) o[i] += v[i];
-    }
-  } else {
-    __half* o = reinterpret_cast<__half*>(p.out) + static_cast<size_t>(t) * p.ldo + f;
-    if (f + 32 <= p.out_cols && (reinterpret_cast<uintptr_t>(o) & 31) == 0) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        uint32_t w[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) w[i] = pack_f16x2(v[j * 16 + 2 * i], v[j * 16 + 2 * i + 1]);
-        st32B(o + j * 16, w);
-      }
-    } else if (f + 32 <= p.out_cols) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) store8(o + j * 8, v + j * 8);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (f + i < p.out_cols) o[i] = __float2half_rn(sat_f16(v[i]));
-    }
+  for (int c = 0; c < 8; ++c) {
+    uint4 w;
+    w.x = pack_f16x2(v[8 * c + 0], v[8 * c + 1]);
+    w.y = pack_f16x2(v[8 * c + 2], v[8 * c + 3]);
+    w.z = pack_f16x2(v[8 * c + 4], v[8 * c + 5]);
+    w.w = pack_f16x2(v[8 * c + 6], v[8 * c + 7]);
+    *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) = w;
   }
 }
-
-// SiLU(gate) * up for 32 output features starting at fo.
-__device__ __forceinline__ void store_silu(const GemmParams& p, int t, int fo, const float* g, const float* u) {
-  float v[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = silu_f(g[i]) * u[i];
-  store_chunk<EPI_STORE>(p, t, fo, v);
+// Whole warp: wait until the box's previous store has read it.
+__device__ __forceinline__ void box_acquire(int lane) {
+  if (lane == 0) bulk_wait_read();
+  __syncwarp();
+}
+// Whole warp, after every lane staged its row: hand the box to the TMA unit.
+__device__ __forceinline__ void box_release(const CUtensorMap* map, uint8_t* box, int x, int y, bool reduce_add,
+                                            int lane) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (reduce_add) tma_reduce_add_2d(map, smem_u32(box), x, y);
+    else tma_store_2d(map, smem_u32(box), x, y);
+    bulk_commit();
+  }
 }
 
 __device__ __forceinline__ void argmax_scan(const GemmParams& p, int t, int f, const float* v, float& best,
@@ -365,14 +339,15 @@ __device__ __forceinline__ void qkv_stream(const GemmParams& p, uint32_t ta, int
 template <int BN, int EPI, bool ACC, bool SWAP>
 __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   using C = GemmCfg<BN, EPI, ACC, SWAP>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * C::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint8_t* sOut = smem + STAGES * C::STAGE_BYTES;  // [EW][4096] output staging boxes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + C::OUT_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
@@ -657,10 +632,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
     const int cbase = ((warp - 2) >> 2) * BNH;
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    uint8_t* box = sOut + (warp - 2) * 4096;  // this warp's output staging box (TMA_OUT)
     int seg = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit un = unit_of(p, u);
       const int t = un.tt * 128 + row;
+      const int tbox = un.tt * 128 + q * 32;  // first row of this warp's boxes
       const int f0 = un.tf * BN;
       const bool row_ok = t < p.T;
       TokPos tp{0, 0, false};
@@ -686,13 +663,18 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
           // gate/up interleaved in 64-column blocks: 128 accumulator columns = 64 outputs
 #pragma unroll 1
           for (int qb = cbase / 128; qb < (cbase + BNH) / 128; ++qb) {
-#pragma unroll 1
+            float o[64];
+#pragma unroll
             for (int h = 0; h < 2; ++h) {
               float gv[32], uv[32];
               tc_ld32(ta + qb * 128 + h * 32, gv);
               tc_ld32(ta + qb * 128 + 64 + h * 32, uv);
-              if (row_ok) store_silu(p, t, f0 / 2 + qb * 64 + h * 32, gv, uv);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[h * 32 + i] = silu_f(gv[i]) * uv[i];
             }
+            box_acquire(lane);
+            stage_f16x64(box, lane, o);
+            box_release(&tmO, box, f0 / 2 + qb * 64, tbox, false, lane);
           }
         } else if constexpr (EPI == EPI_ARGMAX) {
           float best = -INFINITY;
@@ -707,12 +689,25 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
             p.amax_val[static_cast<size_t>(un.tf) * p.amax_ld + t] = best;
             p.amax_idx[static_cast<size_t>(un.tf) * p.amax_ld + t] = bi < 0 ? INT_MAX : bi;
           }
-        } else {
+        } else if constexpr (EPI == EPI_RESID) {
+          // residual += this tile: TMA reduce-add of fp32 boxes (one add per element in L2)
 #pragma unroll 1
           for (int c = cbase / 32; c < (cbase + BNH) / 32; ++c) {
             float v[32];
             tc_ld32(ta + c * 32, v);
-            if (row_ok) store_chunk<EPI>(p, t, f0 + c * 32, v);
+            box_acquire(lane);
+            stage_f32x32(box, lane, v);
+            box_release(&tmO, box, f0 + c * 32, tbox, true, lane);
+          }
+        } else {
+#pragma unroll 1
+          for (int c = cbase / 64; c < (cbase + BNH) / 64; ++c) {
+            float v[64];
+            tc_ld32(ta + c * 64, *reinterpret_cast<float(*)[32]>(v));
+            tc_ld32(ta + c * 64 + 32, *reinterpret_cast<float(*)[32]>(v + 32));
+            box_acquire(lane);
+            stage_f16x64(box, lane, v);
+            box_release(&tmO, box, f0 + c * 64, tbox, false, lane);
           }
         }
         tc_fence_before();
@@ -779,7 +774,35 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
           // second barrier above (it is read once per tile, by thread 64)
           if (threadIdx.x == 64) p.counters[tile] = 0;
         }
-        if (row_ok) {
+        if constexpr (C::TMA_OUT) {  // whole warp (rows past the last token are clipped by the TMA unit)
+          if constexpr (EPI == EPI_SILU) {
+#pragma unroll
+            for (int qb = 0; qb < BNH / 128; ++qb) {
+              float o[64];
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[h * 32 + i] = silu_f(acc[qb * 128 + h * 32 + i]) * acc[qb * 128 + 64 + h * 32 + i];
+              box_acquire(lane);
+              stage_f16x64(box, lane, o);
+              box_release(&tmO, box, f0 / 2 + (cbase / 128 + qb) * 64, tbox, false, lane);
+            }
+          } else if constexpr (EPI == EPI_RESID) {
+#pragma unroll
+            for (int c = 0; c < BNH / 32; ++c) {
+              box_acquire(lane);
+              stage_f32x32(box, lane, acc + c * 32);
+              box_release(&tmO, box, f0 + cbase + c * 32, tbox, true, lane);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < BNH / 64; ++c) {
+              box_acquire(lane);
+              stage_f16x64(box, lane, acc + c * 64);
+              box_release(&tmO, box, f0 + cbase + c * 64, tbox, false, lane);
+            }
+          }
+        } else if (row_ok) {
           if constexpr (EPI == EPI_QKV) {
             static_assert(!ACC || C::EW == 4, "split-K QKV keeps whole heads in one thread");
             if (tp.ok) {
@@ -796,13 +819,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
                   if (f0 + hb * 64 < p.N) qkv_head<64>(p, t, tp, f0 + hb * 64, acc + hb * 64);
               }
             }
-          } else if constexpr (EPI == EPI_SILU) {
-#pragma unroll
-            for (int qb = 0; qb < BNH / 128; ++qb)
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-                store_silu(p, t, f0 / 2 + (cbase / 128 + qb) * 64 + h * 32, acc + qb * 128 + h * 32,
-                           acc + qb * 128 + 64 + h * 32);
           } else if constexpr (EPI == EPI_ARGMAX) {
             static_assert(C::EW == 4, "argmax keeps a whole tile row in one thread");
             float best = -INFINITY;
@@ -811,12 +827,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
             for (int c = 0; c < BN / 32; ++c) argmax_scan(p, t, f0 + c * 32, acc + c * 32, best, bi);
             p.amax_val[static_cast<size_t>(un.tf) * p.amax_ld + t] = best;
             p.amax_idx[static_cast<size_t>(un.tf) * p.amax_ld + t] = bi < 0 ? INT_MAX : bi;
-          } else {
-#pragma unroll
-            for (int c = 0; c < BNH / 32; ++c) store_chunk<EPI>(p, t, f0 + cbase + c * 32, acc + c * 32);
           }
         }
       }
+    }
+    if constexpr (C::TMA_OUT) {  // every store has landed before the CTA (and its staging) goes away
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
     }
   }
 #undef FULL
@@ -865,6 +882,22 @@ bool make_tmap_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, 
 
 static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
   return make_tmap_2d(m, base, rows, cols, ld, box_rows, false);
+}
+
+// Output tensor [rows, cols] (row stride ld elements) written by the epilogue's
+// TMA stores: boxes of 128 bytes x 32 rows, 128-byte swizzle.
+static bool make_map_out(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld,
+                         CUtensorMapDataType type, int elem_bytes) {
+  auto fn = encode_fn();
+  if (!fn || !base || rows <= 0 || cols <= 0) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (ld * elem_bytes) % 16) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * elem_bytes)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem_bytes), 32u};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
 }
 
 static inline int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
@@ -925,8 +958,8 @@ GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
 int gemm_num_tiles_f(const GemmProblem& pr, const GemmPlan& plan) { return plan.tiles_f; }
 
 template <int BN, int EPI, bool ACC, bool SWAP>
-static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, const GemmParams& gp, int grid,
-                                  cudaStream_t s) {
+static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, const GemmProblem& pr,
+                                  const GemmParams& gp, int grid, cudaStream_t s) {
   auto kern = gemm_tc_kernel<BN, EPI, ACC, SWAP>;
   using Cfg = GemmCfg<BN, EPI, ACC, SWAP>;
   constexpr int smem = Cfg::SMEM;
@@ -936,7 +969,14 @@ static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, 
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  kern<<<grid, Cfg::THREADS, smem, s>>>(mx, mw, gp);
+  CUtensorMap mo = mx;  // unused unless the outputs leave through TMA
+  if constexpr (Cfg::TMA_OUT) {
+    const bool ok = EPI == EPI_RESID
+                        ? make_map_out(&mo, pr.out, pr.T, pr.out_cols, pr.ldo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4)
+                        : make_map_out(&mo, pr.out, pr.T, pr.out_cols, pr.ldo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2);
+    if (!ok) return cudaErrorInvalidValue;
+  }
+  kern<<<grid, Cfg::THREADS, smem, s>>>(mx, mw, mo, gp);
   return cudaGetLastError();
 }
 
@@ -978,7 +1018,7 @@ cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partia
   const int g = pl.grid;
 #define TP_V(BN_, EPI_, ACC_, SW_)                                                           \
   if (pl.BN == BN_ && pr.epi == EPI_ && pl.acc == ACC_ && pl.swap == SW_)                     \
-    return launch_variant<BN_, EPI_, ACC_, SW_>(mx, mw, gp, g, stream);
+    return launch_variant<BN_, EPI_, ACC_, SW_>(mx, mw, pr, gp, g, stream);
   TP_V(256, EPI_STORE, false, false)
   TP_V(128, EPI_STORE, false, false)
   TP_V(64, EPI_STORE, false, false)
