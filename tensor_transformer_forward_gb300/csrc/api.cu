@@ -150,7 +150,7 @@ WsPlan plan_ws(const tp_ctx* x, int64_t T, int64_t B, int64_t P) {
     off = align_up(off + std::max<size_t>(bytes, 16));
   };
   const size_t H = x->H, n = x->n;
-  take(w.rope, static_cast<size_t>(P) * (x->hd / 2) * 8);
+  take(w.rope, static_cast<size_t>((P + 31) / 32 * 32) * (x->hd / 2) * 8);
   take(w.xn, T * H * 2);
   take(w.qkv, T * n * x->w_rank * 2);
   take(w.qlo, T * n * x->nq_l * x->hd * 2);
@@ -489,15 +489,20 @@ tp_status tp_workspace_init(tp_ctx* x, void* ws, size_t ws_bytes, int32_t max_to
   x->lm_tiles_max = w.lm_tiles;
   TP_CUDA(cudaMemsetAsync(x->ws + w.gcnt.off, 0, w.gcnt.bytes, s));
   TP_CUDA(cudaMemsetAsync(x->ws + w.acnt.off, 0, w.acnt.bytes, s));
-  // RoPE table: angle(p, d) = p * theta^(-2d/hd), rotate-half pairs (d, d + hd/2); fp64, stored fp32
+  // RoPE table: angle(p, d) = p * theta^(-2d/hd), rotate-half pairs (d, d + hd/2); fp64, stored
+  // fp32 as (cos, sin).  Blocked by 32 positions so that the 32 consecutive positions a warp
+  // reads side by side are adjacent: float4 (cos_d, sin_d, cos_d+1, sin_d+1) of position p at
+  // index ((p / 32) * (hd / 4) + d / 2) * 32 + p % 32.
   const int half = x->hd / 2;
-  std::vector<float> tab(static_cast<size_t>(max_positions) * half * 2);
+  const int P32 = (max_positions + 31) / 32 * 32;
+  std::vector<float> tab(static_cast<size_t>(P32) * half * 2, 0.0f);
   for (int d = 0; d < half; ++d) {
     const double inv_freq = std::pow(static_cast<double>(x->c.rope_theta), -2.0 * d / x->hd);
     for (int p = 0; p < max_positions; ++p) {
       const double ang = static_cast<double>(p) * inv_freq;
-      tab[(static_cast<size_t>(p) * half + d) * 2] = static_cast<float>(std::cos(ang));
-      tab[(static_cast<size_t>(p) * half + d) * 2 + 1] = static_cast<float>(std::sin(ang));
+      const size_t f4 = (static_cast<size_t>(p / 32) * (half / 2) + d / 2) * 32 + p % 32;
+      tab[f4 * 4 + (d % 2) * 2] = static_cast<float>(std::cos(ang));
+      tab[f4 * 4 + (d % 2) * 2 + 1] = static_cast<float>(std::sin(ang));
     }
   }
   TP_CUDA(cudaMemcpyAsync(x->ws + w.rope.off, tab.data(), tab.size() * 4, cudaMemcpyHostToDevice, s));

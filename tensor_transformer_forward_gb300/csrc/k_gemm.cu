@@ -262,7 +262,9 @@ __device__ __forceinline__ void qkv_head(const GemmParams& p, int t, const TokPo
   for (int i = 0; i < HD; ++i) ss += h[i] * h[i];
   const float inv = rsqrtf(ss / static_cast<float>(HD) + q.eps);
   const __nv_bfloat16* nw = reinterpret_cast<const __nv_bfloat16*>(is_q ? q.q_norm : q.k_norm);
-  const float2* cs = q.rope + static_cast<size_t>(tp.pos) * HALF;
+  // (cos, sin) pairs of d and d+1 for this position: one float4 every 32 (positions side by side)
+  const float4* cs4 = reinterpret_cast<const float4*>(q.rope) + static_cast<size_t>(tp.pos >> 5) * (HALF / 2) * 32 +
+                      (tp.pos & 31);
   // q of a prefill token: bf16 high part in the QKV buffer and the bf16 low part
   // q - bf16(q) in q_lo (the tensor-core attention multiplies both with the bf16
   // keys); q of a decode token: fp16 in the QKV buffer (fp32 attention math).
@@ -283,7 +285,7 @@ __device__ __forceinline__ void qkv_head(const GemmParams& p, int t, const TokPo
                          bf16lo(w1.z), bf16hi(w1.z), bf16lo(w1.w), bf16hi(w1.w)};
     float4 c4[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) c4[i] = __ldg(reinterpret_cast<const float4*>(cs + j * 8) + i);
+    for (int i = 0; i < 4; ++i) c4[i] = __ldg(cs4 + (j * 4 + i) * 32);
     const float cx[8] = {c4[0].x, c4[0].z, c4[1].x, c4[1].z, c4[2].x, c4[2].z, c4[3].x, c4[3].z};
     const float sy[8] = {c4[0].y, c4[0].w, c4[1].y, c4[1].w, c4[2].y, c4[2].w, c4[3].y, c4[3].w};
     float y0[8], y1[8];

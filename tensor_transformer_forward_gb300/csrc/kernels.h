@@ -30,7 +30,7 @@ struct QkvEpi {
   const void* q_norm;        // [hd] bf16
   const void* k_norm;
   float eps;
-  const float2* rope;        // [max_pos, hd/2] (cos, sin)
+  const float2* rope;        // (cos, sin) per (position, d < hd/2), blocked by 32 positions (see api.cu)
   int max_pos;
   const int32_t* cu_q;       // [B+1]
   const int32_t* ctx_len;    // [B]
