@@ -58,7 +58,7 @@ struct tp_ctx {
   char* ws = nullptr;
   size_t ws_bytes = 0;
   int ws_tokens = 0, ws_seqs = 0, ws_pos = 0;
-  Region r_rope, r_xn, r_qkv, r_qlo, r_attn, r_act, r_gpart, r_gcnt, r_apart, r_acnt, r_amax_v, r_amax_i, r_z, r_zidx;
+  Region r_rope, r_xn, r_qkv, r_qlo, r_attn, r_act, r_gpart, r_gcnt, r_apart, r_acnt, r_amax_v, r_amax_i, r_z;
   int lm_tiles_max = 0;
   int num_sms = 0;
   int64_t rank_sums = 0;
@@ -136,7 +136,7 @@ void lay_out(tp_ctx* x) {
 }
 
 struct WsPlan {
-  Region rope, xn, qkv, qlo, attn, act, gpart, gcnt, apart, acnt, amax_v, amax_i, z, zidx;
+  Region rope, xn, qkv, qlo, attn, act, gpart, gcnt, apart, acnt, amax_v, amax_i, z;
   size_t total = 0;
   int lm_tiles = 0;
 };
@@ -165,7 +165,6 @@ WsPlan plan_ws(const tp_ctx* x, int64_t T, int64_t B, int64_t P) {
   take(w.amax_v, static_cast<size_t>(w.lm_tiles) * B * 4);
   take(w.amax_i, static_cast<size_t>(w.lm_tiles) * B * 4);
   take(w.z, B * H * 2);
-  take(w.zidx, B * 4);
   w.total = off;
   return w;
 }
@@ -485,7 +484,7 @@ tp_status tp_workspace_init(tp_ctx* x, void* ws, size_t ws_bytes, int32_t max_to
   x->ws_pos = max_positions;
   x->r_rope = w.rope; x->r_xn = w.xn; x->r_qkv = w.qkv; x->r_qlo = w.qlo; x->r_attn = w.attn; x->r_act = w.act;
   x->r_gpart = w.gpart; x->r_gcnt = w.gcnt; x->r_apart = w.apart; x->r_acnt = w.acnt;
-  x->r_amax_v = w.amax_v; x->r_amax_i = w.amax_i; x->r_z = w.z; x->r_zidx = w.zidx;
+  x->r_amax_v = w.amax_v; x->r_amax_i = w.amax_i; x->r_z = w.z;
   x->lm_tiles_max = w.lm_tiles;
   TP_CUDA(cudaMemsetAsync(x->ws + w.gcnt.off, 0, w.gcnt.bytes, s));
   TP_CUDA(cudaMemsetAsync(x->ws + w.acnt.off, 0, w.acnt.bytes, s));
@@ -544,7 +543,7 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   // A3: input RMSNorm
   {
     Timed tm(x, TP_K_RMSNORM, s);
-    e = tpk::launch_rmsnorm(hidden, T, H, w + x->in_norm.off, x->c.rms_eps, xn, nullptr, s);
+    e = tpk::launch_rmsnorm(hidden, T, H, w + x->in_norm.off, x->c.rms_eps, xn, s);
   }
   if (e != cudaSuccess) return cuda_fail(e);
 
@@ -605,7 +604,7 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   // A8: post-attention RMSNorm
   {
     Timed tm(x, TP_K_RMSNORM, s);
-    e = tpk::launch_rmsnorm(hidden, T, H, w + x->post_norm.off, x->c.rms_eps, xn, nullptr, s);
+    e = tpk::launch_rmsnorm(hidden, T, H, w + x->post_norm.off, x->c.rms_eps, xn, s);
   }
   if (e != cudaSuccess) return cuda_fail(e);
 
@@ -643,9 +642,8 @@ tp_status tp_lm_head_argmax(tp_ctx* x, const void* head_shards, const tp_batch* 
   void* z = x->ws + x->r_z.off;
   cudaError_t e;
   {
-    Timed tm(x, TP_K_FINAL_NORM, s, 2);
-    e = tpk::launch_final_norm_select(hidden, H, b->cu_q, B, w + x->final_norm.off, x->c.rms_eps, z,
-                                      reinterpret_cast<int32_t*>(x->ws + x->r_zidx.off), s);
+    Timed tm(x, TP_K_FINAL_NORM, s);
+    e = tpk::launch_final_norm_select(hidden, H, b->cu_q, B, w + x->final_norm.off, x->c.rms_eps, z, s);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   tpk::GemmProblem g{};

@@ -26,6 +26,13 @@ __device__ __forceinline__ void raise_flag(int* status, int flag) {
   if (status) atomicOr(status, flag);
 }
 
+// Programmatic dependent launch: every kernel of the path is launched so that it
+// may start while the previous kernel in the stream finishes.  A kernel calls
+// griddep_wait() before it reads anything an earlier kernel wrote and before
+// its first global write; griddep_launch() lets the next kernel be scheduled.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
 __device__ __forceinline__ __nv_bfloat16 f2bf(float v) { return __float2bfloat16_rn(v); }
 

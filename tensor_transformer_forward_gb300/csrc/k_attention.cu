@@ -61,7 +61,6 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
   const int slot = a.slot[b];
   // a slot or length outside the cache reads nothing (zero output) and flags the batch
   const bool bad = slot < 0 || slot >= a.max_seqs || L < 1 || L > a.cap;
-  if (bad && threadIdx.x == 0 && split == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
   const int chunk = (L + a.splits - 1) / a.splits;
   const int k0 = split * chunk;
   const int k1 = bad ? k0 : min(L, k0 + chunk);
@@ -81,6 +80,10 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
     fence_barrier_init();
   }
   __syncthreads();
+  // the batch arrays are the host's; q and the cache come from earlier kernels
+  griddep_wait();
+  griddep_launch();
+  if (bad && threadIdx.x == 0 && split == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
 
   // per-lane state for the warp's keys: G heads x (m, l, acc[8])
   float m[G], l[G], acc[G][8];
@@ -331,8 +334,7 @@ static cudaError_t launch_decode_hd(const AttnArgs& a, dim3 grid, cudaStream_t s
   int per_sm = 0;
   cudaError_t e = prepare_decode<HD, G>(&per_sm);  // sets the shared-memory attribute once
   if (e != cudaSuccess) return e;
-  attn_decode_kernel<HD, G><<<grid, 160, DecCfg<HD>::SMEM, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(attn_decode_kernel<HD, G>, grid, dim3(160), DecCfg<HD>::SMEM, s, a);
 }
 
 cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s) {
@@ -427,6 +429,7 @@ __global__ void __launch_bounds__(320, 1)
   {
     const int sl = a.slot[b], kmax = a.ctx_len[b] + qlen;
     if (sl < 0 || sl >= a.max_seqs || a.ctx_len[b] < 0 || kmax > a.cap) {  // outside the cache: flag, skip
+      griddep_wait();
       if (threadIdx.x == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
       return;
     }
@@ -467,6 +470,8 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // q and the cache come from the QKV GEMM
+  griddep_launch();
 
   if (warp == 0) {
     // ---------------- TMA producers: lane 0 streams Q then K, lane 1 streams V ----------------
@@ -712,8 +717,7 @@ static cudaError_t launch_prefill_hd(const AttnArgs& a, cudaStream_t s) {
     attr = true;
   }
   const unsigned grid = static_cast<unsigned>((a.max_q_len + C::BQ - 1) / C::BQ) * a.n * a.nq_l * (a.seq_end - a.seq_begin);
-  attn_prefill_tc_kernel<HD><<<grid, 320, C::SMEM, s>>>(mq, mqlo, mkv, a);
-  return cudaGetLastError();
+  return launch_pdl(attn_prefill_tc_kernel<HD>, dim3(grid), dim3(320), C::SMEM, s, mq, mqlo, mkv, a);
 }
 
 cudaError_t launch_attention_prefill(const AttnArgs& a, cudaStream_t s) {

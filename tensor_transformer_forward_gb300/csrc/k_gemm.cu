@@ -405,6 +405,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int units = p.tiles_t * p.tiles_f * p.splits;
+  // the set-up above overlaps the previous kernel; inputs, counters and outputs come after
+  griddep_wait();
+  griddep_launch();
   // tile extents on the token and feature sides
   constexpr int TM_T = SWAP ? BN : 128;  // tokens per tile
   constexpr int TM_F = SWAP ? 128 : BN;  // features per tile
@@ -978,8 +981,7 @@ static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, 
                         : make_map_out(&mo, pr.out, pr.T, pr.out_cols, pr.ldo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2);
     if (!ok) return cudaErrorInvalidValue;
   }
-  kern<<<grid, Cfg::THREADS, smem, s>>>(mx, mw, mo, gp);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(Cfg::THREADS), smem, s, mx, mw, mo, gp);
 }
 
 cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partials, int* counters, int* status,

@@ -23,6 +23,8 @@ namespace tpk {
 __global__ void embed_vocab_parallel_kernel(const int32_t* __restrict__ ids, const uint4* __restrict__ table,
                                             int n, int64_t v_local, int64_t vocab, int H,
                                             float4* __restrict__ out, int* status) {
+  griddep_wait();  // the ids may come from the previous step's argmax
+  griddep_launch();
   const int t = blockIdx.x;
   const int id = ids[t];
   if (threadIdx.x == 0 && (id < 0 || id >= vocab)) raise_flag(status, TP_DEVFLAG_BAD_TOKEN);
@@ -51,9 +53,9 @@ cudaError_t launch_embed(const int32_t* ids, int T, const void* embed_stacked, i
                          int64_t vocab, int H, void* out, int* status, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int threads = H / 8 < 128 ? 32 * ((H / 8 + 31) / 32) : 128;
-  embed_vocab_parallel_kernel<<<T, threads, 0, s>>>(ids, reinterpret_cast<const uint4*>(embed_stacked), n, v_local,
-                                                    vocab, H, reinterpret_cast<float4*>(out), status);
-  return cudaGetLastError();
+  return launch_pdl(embed_vocab_parallel_kernel, dim3(T), dim3(threads), 0, s, ids,
+                    reinterpret_cast<const uint4*>(embed_stacked), n, v_local, vocab, H, reinterpret_cast<float4*>(out),
+                    status);
 }
 
 // ---------------------------------------------------------------------------
@@ -63,12 +65,14 @@ cudaError_t launch_embed(const int32_t* ids, int T, const void* embed_stacked, i
 // ---------------------------------------------------------------------------
 template <int VPL>  // 8-element groups per lane kept in registers
 __global__ void rmsnorm_kernel(const float4* __restrict__ x, int64_t rows, int H, const uint4* __restrict__ w,
-                               float eps, uint4* __restrict__ out, const int32_t* __restrict__ row_index) {
+                               float eps, uint4* __restrict__ out, const int32_t* __restrict__ cu_last) {
+  griddep_wait();
+  griddep_launch();
   const int warps = blockDim.x / 32;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * warps + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  const int64_t src = row_index ? row_index[row] : row;
+  const int64_t src = cu_last ? cu_last[row + 1] - 1 : row;
   const int chunks = H / 8;
   const float4* xr = x + src * (H / 4);
   float v[VPL][8];
@@ -105,12 +109,14 @@ __global__ void rmsnorm_kernel(const float4* __restrict__ x, int64_t rows, int H
 
 // Wide rows (H > 2048): one warp per row, two passes (the second re-reads the row from L1/L2).
 __global__ void rmsnorm_wide_kernel(const float4* __restrict__ x, int64_t rows, int H, const uint4* __restrict__ w,
-                                    float eps, uint4* __restrict__ out, const int32_t* __restrict__ row_index) {
+                                    float eps, uint4* __restrict__ out, const int32_t* __restrict__ cu_last) {
+  griddep_wait();
+  griddep_launch();
   const int warps = blockDim.x / 32;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * warps + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  const int64_t src = row_index ? row_index[row] : row;
+  const int64_t src = cu_last ? cu_last[row + 1] - 1 : row;
   const int chunks = H / 8;
   const float4* xr = x + src * (H / 4);
   float ss = 0.0f;
@@ -132,36 +138,30 @@ __global__ void rmsnorm_wide_kernel(const float4* __restrict__ x, int64_t rows, 
   }
 }
 
-cudaError_t launch_rmsnorm(const void* x, int64_t rows, int H, const void* w, float eps, void* out,
-                           const int32_t* row_index, cudaStream_t s) {
+static cudaError_t rmsnorm_rows(const void* x, int64_t rows, int H, const void* w, float eps, void* out,
+                                const int32_t* cu_last, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const int vpl = (H / 8 + 31) / 32;
   const int warps = 4;
-  const unsigned grid = static_cast<unsigned>((rows + warps - 1) / warps);
+  const dim3 grid(static_cast<unsigned>((rows + warps - 1) / warps)), block(32 * warps);
   auto X = reinterpret_cast<const float4*>(x);
   auto W = reinterpret_cast<const uint4*>(w);
   auto O = reinterpret_cast<uint4*>(out);
-  if (vpl <= 1) rmsnorm_kernel<1><<<grid, 32 * warps, 0, s>>>(X, rows, H, W, eps, O, row_index);
-  else if (vpl <= 2) rmsnorm_kernel<2><<<grid, 32 * warps, 0, s>>>(X, rows, H, W, eps, O, row_index);
-  else if (vpl <= 4) rmsnorm_kernel<4><<<grid, 32 * warps, 0, s>>>(X, rows, H, W, eps, O, row_index);
-  else if (vpl <= 8) rmsnorm_kernel<8><<<grid, 32 * warps, 0, s>>>(X, rows, H, W, eps, O, row_index);
-  else rmsnorm_wide_kernel<<<grid, 32 * warps, 0, s>>>(X, rows, H, W, eps, O, row_index);
-  return cudaGetLastError();
+  if (vpl <= 1) return launch_pdl(rmsnorm_kernel<1>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
+  if (vpl <= 2) return launch_pdl(rmsnorm_kernel<2>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
+  if (vpl <= 4) return launch_pdl(rmsnorm_kernel<4>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
+  if (vpl <= 8) return launch_pdl(rmsnorm_kernel<8>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
+  return launch_pdl(rmsnorm_wide_kernel, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
 }
 
-// Last token of each sequence (cu_q[b+1]-1), then RMSNorm with the final norm weight.
-__global__ void last_token_index_kernel(const int32_t* cu_q, int B, int32_t* idx) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b < B) idx[b] = cu_q[b + 1] - 1;
+cudaError_t launch_rmsnorm(const void* x, int64_t rows, int H, const void* w, float eps, void* out, cudaStream_t s) {
+  return rmsnorm_rows(x, rows, H, w, eps, out, nullptr, s);
 }
 
+// Final RMSNorm of each sequence's last token (row cu_q[b+1] - 1 of the residual stream).
 cudaError_t launch_final_norm_select(const void* hidden, int H, const int32_t* cu_q, int B, const void* w,
-                                     float eps, void* out, int32_t* idx, cudaStream_t s) {
-  if (B <= 0) return cudaSuccess;
-  last_token_index_kernel<<<(B + 127) / 128, 128, 0, s>>>(cu_q, B, idx);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return launch_rmsnorm(hidden, B, H, w, eps, out, idx, s);
+                                     float eps, void* out, cudaStream_t s) {
+  return rmsnorm_rows(hidden, B, H, w, eps, out, cu_q, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -203,6 +203,8 @@ __device__ __forceinline__ bool amax_better(float v, int i, float bv, int bi) {
 
 __global__ void argmax_reduce_kernel(const float* __restrict__ val, const int* __restrict__ idx, int tiles, int ld,
                                      int B, int32_t* __restrict__ out) {
+  griddep_wait();
+  griddep_launch();
   const int b = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (b >= B) return;
@@ -231,8 +233,7 @@ __global__ void argmax_reduce_kernel(const float* __restrict__ val, const int* _
 cudaError_t launch_argmax_reduce(const float* val, const int* idx, int tiles, int ld, int B, int32_t* out,
                                  cudaStream_t s) {
   if (B <= 0) return cudaSuccess;
-  argmax_reduce_kernel<<<(B + 3) / 4, 128, 0, s>>>(val, idx, tiles, ld, B, out);
-  return cudaGetLastError();
+  return launch_pdl(argmax_reduce_kernel, dim3((B + 3) / 4), dim3(128), 0, s, val, idx, tiles, ld, B, out);
 }
 
 // ---------------------------------------------------------------------------

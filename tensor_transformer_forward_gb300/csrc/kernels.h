@@ -20,6 +20,24 @@ struct HeadView {
 };
 int ctx_head_view(tp_ctx* ctx, HeadView* out);  // returns a tp_status
 
+// Launch with programmatic stream serialization: the kernel may begin (up to its
+// griddep_wait()) while the previous kernel on the stream is still running.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---------------- GEMM (tcgen05) ----------------
 enum GemmEpi : int { EPI_STORE = 0, EPI_SILU = 1, EPI_RESID = 2, EPI_ARGMAX = 3, EPI_QKV = 4 };
 
@@ -97,8 +115,7 @@ int gemm_num_tiles_f(const GemmProblem& pr, const GemmPlan& plan);
 // ---------------- small kernels ----------------
 cudaError_t launch_embed(const int32_t* ids, int T, const void* embed_stacked, int n, int64_t v_local,
                          int64_t vocab, int H, void* out, int* status, cudaStream_t s);
-cudaError_t launch_rmsnorm(const void* x, int64_t rows, int H, const void* w, float eps, void* out,
-                           const int32_t* row_index, cudaStream_t s);
+cudaError_t launch_rmsnorm(const void* x, int64_t rows, int H, const void* w, float eps, void* out, cudaStream_t s);
 
 
 struct AttnArgs {
@@ -125,7 +142,7 @@ cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s);
 int decode_splits(int max_kv_len, int num_units, int num_sms, int hd, int G, int max_splits);
 
 cudaError_t launch_final_norm_select(const void* hidden, int H, const int32_t* cu_q, int B, const void* w,
-                                     float eps, void* out, int32_t* idx_scratch, cudaStream_t s);
+                                     float eps, void* out, cudaStream_t s);
 cudaError_t launch_argmax_reduce(const float* val, const int* idx, int tiles, int ld, int B, int32_t* out,
                                  cudaStream_t s);
 cudaError_t launch_wait_probe(const int* flag, int* status, long long limit_ns, cudaStream_t s);

@@ -31,8 +31,7 @@ constexpr int kMaxDevices = 64;
 
 // byte layout of the scratch array
 constexpr size_t kZOff = 0;                                              // fp16 [kMaxSeqs][kMaxHidden]
-constexpr size_t kRowOff = kZOff + size_t(kMaxSeqs) * kMaxHidden * 2;    // int32 [kMaxSeqs]
-constexpr size_t kCntOff = kRowOff + 256;                                // GEMM counters and argmax keys
+constexpr size_t kCntOff = kZOff + size_t(kMaxSeqs) * kMaxHidden * 2;    // GEMM counters and argmax keys
 constexpr size_t kCntBytes = size_t(tpk::kGemmCounterInts) * 4;
 constexpr size_t kScratchBytes = kCntOff + kCntBytes;
 }  // namespace
@@ -82,8 +81,7 @@ extern "C" tp_status tp_lm_head_argmax_static(tp_ctx* ctx, const void* head_shar
   const char* w = static_cast<const char*>(head_shards);
   const int B = b->num_seqs;
   void* z = scratch + kZOff;
-  cudaError_t e = tpk::launch_final_norm_select(hidden, hv.H, b->cu_q, B, w + hv.final_norm_off, hv.eps, z,
-                                                reinterpret_cast<int32_t*>(scratch + kRowOff), s);
+  cudaError_t e = tpk::launch_final_norm_select(hidden, hv.H, b->cu_q, B, w + hv.final_norm_off, hv.eps, z, s);
   if (e != cudaSuccess) return TP_ERR_CUDA;
   tpk::GemmProblem g{};
   g.x = z; g.x_rows = B; g.x_cols = hv.H; g.x_ld = hv.H;
