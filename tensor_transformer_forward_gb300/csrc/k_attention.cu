@@ -17,6 +17,33 @@
 
 namespace tpk {
 
+// 2^x for the softmax numerators (hardware approximation, results below 2^-126
+// flush to zero: such terms are far below the bf16 rounding of P)
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// paired fp32 arithmetic (two lanes of one 64-bit register)
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // ---------------------------------------------------------------------------
 // Decode (one new token per sequence): flash-decoding split over the keys.
 // One CTA = (sequence, rank, local kv head, key split).  Warp 4 streams the
@@ -361,15 +388,20 @@ cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s) {
 //   warp 1      TMEM allocation + one MMA-issuing thread: S(j) = Q K(j)^T
 //               (as Q_hi K^T + Q_lo K^T, so q keeps ~16 significant bits) into
 //               one of two TMEM score buffers, then O += P(j) V(j) into the TMEM
-//               output accumulator (P from shared memory, V as an MN-major
-//               operand straight from the TMA tile).
+//               output accumulator (P read from tensor memory, V as an MN-major
+//               operand straight from the TMA tile).  S(j+1) is issued before
+//               O += P(j) V(j), so the scores of the next block are computed
+//               while the softmax of this one runs.
 //   warps 2-9   softmax: two threads per query row (its TMEM lane), one per
 //               64-key half -- scale, causal mask, row max, exp2, row sum;
-//               P(j) written to shared
-//               memory in the swizzled K-major layout the MMA reads; the running
-//               output is rescaled only when the row max has grown by more than
-//               2^8 (otherwise P may exceed 1 by at most 2^8, exactly
-//               compensated by the row sum); final O / l written as fp16.
+//               P(j) (bf16) written back over its own scores in TMEM, so the
+//               two score buffers double as two P buffers; the running output
+//               is rescaled only when the row max has grown by more than 2^8
+//               (otherwise P may exceed 1 by at most 2^8, exactly compensated by
+//               the row sum); final O / l written as fp16.
+// Ordering: tcgen05 operations of the MMA thread complete in issue order, so
+// S(j+2) (issued after O += P(j) V(j)) never overwrites P(j) before it is read,
+// and the completion of S(j) implies that of O += P(j-2) V(j-2).
 // All waits are bounded (TP_WAIT_LIMIT_NS) and end in TP_DEVFLAG_TIMEOUT.
 // Cache positions never written must hold finite values (the runner zeroes the
 // cache once): keys past the sequence get P = 0, but 0 * NaN would not vanish.
@@ -383,10 +415,10 @@ struct FaCfg {
   static constexpr int STAGES = 2;
   static constexpr int Q_OFF = 0;                                  // [hi | lo]
   static constexpr int KV_OFF = 2 * TILE_BYTES;                    // K ring [stage], then V ring [stage]
-  static constexpr int P_OFF = KV_OFF + STAGES * 2 * TILE_BYTES;   // [2 sub-tiles of 64 keys]
-  static constexpr int BAR_OFF = P_OFF + 2 * SUB_BYTES;
+  static constexpr int BAR_OFF = KV_OFF + STAGES * 2 * TILE_BYTES;
   static constexpr int SMEM = 1024 + BAR_OFF + 256;
-  static constexpr int S_COL = 0;      // two score buffers: columns [0,128) and [128,256)
+  static constexpr int S_COL = 0;      // two score buffers: columns [0,128) and [128,256); P(j) (bf16
+                                       // pairs) overwrites the first 64 columns of its score buffer
   static constexpr int O_COL = 256;    // output accumulator: columns [256, 256+HD)
 };
 
@@ -410,8 +442,7 @@ __global__ void __launch_bounds__(320, 1)
 #define B_VF(s) (bar0 + 8u * (12 + (s)))
 #define B_VE(s) (bar0 + 8u * (14 + (s)))
 #define B_SF(b) (bar0 + 8u * (5 + (b)))
-#define B_SE(b) (bar0 + 8u * (7 + (b)))
-#define B_PF (bar0 + 8u * 9)
+#define B_PF(b) (bar0 + 8u * (7 + (b)))
 #define B_OD (bar0 + 8u * 10)
 #define B_DR (bar0 + 8u * 11)
 
@@ -454,9 +485,8 @@ __global__ void __launch_bounds__(320, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(B_SF(i), 1);
-      mbar_init(B_SE(i), 8);
+      mbar_init(B_PF(i), 8);
     }
-    mbar_init(B_PF, 8);
     mbar_init(B_OD, 1);
     mbar_init(B_DR, 1);
     *abort_flag = 0;
@@ -515,18 +545,17 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t id_o = idesc_bf16_f32(128, HD, true);    // O += P V: V MN-major
       bool ok = mbar_wait(B_Q, 0, abort_flag, a.status);
       tc_fence_after();
-      auto pv = [&](int j) -> bool {  // O += P(j) V(j)
-        const int st = j % STAGES;
-        if (!mbar_wait(B_PF, j & 1, abort_flag, a.status)) return false;
+      auto pv = [&](int j) -> bool {  // O += P(j) V(j), P(j) from TMEM (score buffer j & 1)
+        const int st = j % STAGES, sb = j & 1;
+        if (!mbar_wait(B_PF(sb), (j >> 1) & 1, abort_flag, a.status)) return false;
         if (!mbar_wait(B_VF(st), (j / STAGES) & 1, abort_flag, a.status)) return false;
         tc_fence_after();
         const uint32_t vt = smem_u32(smem + C::KV_OFF + (STAGES + st) * C::TILE_BYTES);
-        const uint32_t pt = smem_u32(smem + C::P_OFF);
+        const uint32_t pa = tmem + C::S_COL + sb * 128;
 #pragma unroll
         for (int kk = 0; kk < C::BKV / 16; ++kk) {
-          const uint64_t ad = sdesc_k_sw128(pt + (kk >> 2) * C::SUB_BYTES) + 2ull * (kk & 3);
           const uint64_t bd = sdesc_mn_sw128(vt + kk * 16 * 128, C::SUB_BYTES, 1024);
-          tc_mma_f16(tmem + C::O_COL, ad, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16_ts(tmem + C::O_COL, pa + kk * 8, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(B_OD);
         tc_commit(B_VE(st));
@@ -534,8 +563,8 @@ __global__ void __launch_bounds__(320, 1)
       };
       for (int j = 0; ok && j < nblk; ++j) {
         const int st = j % STAGES, sb = j & 1;
+        // score buffer sb last held P(j-2), whose PV MMA was issued before this point
         if (!mbar_wait(B_KF(st), (j / STAGES) & 1, abort_flag, a.status)) { ok = false; break; }
-        if (!mbar_wait(B_SE(sb), ((j >> 1) & 1) ^ 1u, abort_flag, a.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t qt = smem_u32(smem + C::Q_OFF);
         const uint32_t kt = smem_u32(smem + C::KV_OFF + st * C::TILE_BYTES);
@@ -569,7 +598,6 @@ __global__ void __launch_bounds__(320, 1)
     const bool row_ok = qi < qlen;
     const int last_key = ctx + qi;              // keys <= last_key are visible
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    uint8_t* prow = smem + C::P_OFF + half * C::SUB_BYTES + row * 128;
     constexpr int OH = HD / 2;                  // output dims per half
     float m_used = -INFINITY, l = 0.0f;
     bool ok = true;
@@ -586,20 +614,19 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[c * 32 + i] = v[i];
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(B_SE(sb));
       const int key0 = j * C::BKV + half * 64;
-      const bool need_mask = (key0 + 63 > ctx + q0) || !row_ok;
-      float mx = -INFINITY;
+      const bool need_mask = (key0 + 63 > ctx + q0) || !row_ok;  // diagonal blocks and padding rows only
+      if (need_mask) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        float x = sv[i] * a.scale_log2;
-        if (need_mask && (!row_ok || key0 + i > last_key)) x = -INFINITY;
-        sv[i] = x;
-        mx = fmaxf(mx, x);
+        for (int i = 0; i < 64; ++i)
+          if (!row_ok || key0 + i > last_key) sv[i] = -INFINITY;
       }
-      // row max over both halves (TMEM columns 384 + 2 * (j & 1) + half)
+      float mx = sv[0];
+#pragma unroll
+      for (int i = 1; i < 64; ++i) mx = fmaxf(mx, sv[i]);
+      mx *= a.scale_log2;  // the scale is positive: max of the scaled scores
+      // row max over both halves (TMEM columns 384 + 2 * (j & 1) + half); past this
+      // barrier both halves have read their scores, so P may overwrite them
       tc_st1(lane_addr + 384 + 2 * (j & 1) + half, mx);
       tc_fence_before();
       named_bar_sync(1, 256);
@@ -608,20 +635,35 @@ __global__ void __launch_bounds__(320, 1)
       const bool rescale = mx > m_used + 8.0f;
       const float m_new = rescale ? mx : m_used;
       const float mb = m_new == -INFINITY ? 0.0f : m_new;
-      float psum = 0.0f;
+      // p = 2^(s * scale - m): one paired FMA, two ex2, one paired add per two keys;
+      // P(j) as bf16 pairs (keys 2c, 2c+1 in column c)
+      uint32_t pw[32];
+      float psum;
+      {
+        const uint64_t sc2 = f32x2(a.scale_log2, a.scale_log2), nb2 = f32x2(-mb, -mb);
+        uint64_t acc2 = f32x2(0.0f, 0.0f);
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        sv[i] = exp2f(sv[i] - mb);
-        psum += sv[i];
+        for (int c = 0; c < 32; ++c) {
+          float x0, x1;
+          unpack_f32x2(fma_f32x2(f32x2(sv[2 * c], sv[2 * c + 1]), sc2, nb2), x0, x1);
+          const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+          acc2 = add_f32x2(acc2, f32x2(p0, p1));
+          pw[c] = pack_bf16x2(p0, p1);
+        }
+        float s0, s1;
+        unpack_f32x2(acc2, s0, s1);
+        psum = s0 + s1;
       }
-      // P buffer and O are free once the previous block's PV has completed.  A
-      // failed wait only marks the thread; every softmax thread leaves together at
-      // the next agreement point (named barriers have no time limit).
-      if (j > 0 && !mbar_wait(B_OD, (j - 1) & 1, abort_flag, a.status)) ok = false;
+      // A rescale of O waits for the previous block's PV MMA (S(j) done implies
+      // PV(j-2) done, so the output barrier is at phase j-1 or j here).  A failed
+      // wait only marks the thread; every softmax thread leaves together at the
+      // next agreement point (named barriers have no time limit).
+      const bool touch_o = rescale && j > 0 && m_used != -INFINITY;
+      if (touch_o && !mbar_wait(B_OD, (j - 1) & 1, abort_flag, a.status)) ok = false;
       if (!ok) continue;
-      tc_fence_after();
       if (rescale) {
-        if (j > 0 && m_used != -INFINITY) {
+        if (touch_o) {
+          tc_fence_after();
           const float corr = exp2f(m_used - m_new);
           l *= corr;
 #pragma unroll
@@ -636,21 +678,13 @@ __global__ void __launch_bounds__(320, 1)
         m_used = m_new;
       }
       l += psum;
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {  // 16-byte chunks of 8 keys
-        uint4 w;
-        w.x = pack_bf16x2(sv[ch * 8 + 0], sv[ch * 8 + 1]);
-        w.y = pack_bf16x2(sv[ch * 8 + 2], sv[ch * 8 + 3]);
-        w.z = pack_bf16x2(sv[ch * 8 + 4], sv[ch * 8 + 5]);
-        w.w = pack_bf16x2(sv[ch * 8 + 6], sv[ch * 8 + 7]);
-        *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = w;
-      }
-      fence_proxy_async_smem();
+      tc_st32u(lane_addr + C::S_COL + sb * 128 + half * 32, pw);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(B_PF);
+      if (lane == 0) mbar_arrive(B_PF(sb));
     }
-    if (ok) ok = mbar_wait(B_OD, (nblk - 1) & 1, abort_flag, a.status);
+    // the MMA thread commits the drain barrier after the last PV
+    if (ok) ok = mbar_wait(B_DR, 0, abort_flag, a.status);
     if (named_bar_and(1, 256, ok)) {
       tc_fence_after();
       // row sum over both halves (TMEM columns 388 + half)
@@ -686,7 +720,6 @@ __global__ void __launch_bounds__(320, 1)
 #undef B_VF
 #undef B_VE
 #undef B_SF
-#undef B_SE
 #undef B_PF
 #undef B_OD
 #undef B_DR
