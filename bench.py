@@ -76,9 +76,9 @@ def workload_config(w: synth.Workload, n: int) -> dict:
 # source at capture time and is reported only while the source is unchanged.
 # The summaries of those captures are under profiles/.
 NCU_TRAFFIC = {
-    ("qwen3_0.6b_layer_prefill2048", 2, "gemm_lm_head"): (311.230464e6 + 3.654144e6, "k_gemm.cu", "6811fe163e8e14fb"),
-    ("qwen3_0.6b_layer_decode64x4096", 2, "attn_decode"): (1075.294208e6 + 4.061952e6, "k_attention.cu",
-                                                            "aef07859faa39a23"),
+    ("qwen3_0.6b_layer_prefill2048", 2, "gemm_lm_head"): (311.240192e6 + 3.263232e6, "k_gemm.cu", "6f65af780262acdb"),
+    ("qwen3_0.6b_layer_decode64x4096", 2, "attn_decode"): (1078.347e6 + 5.781504e6, "k_attention.cu",
+                                                            "0b9845b2495a61a7"),
 }
 KERNEL_HEADERS = ("kernels.h", "sm100.cuh", "common.cuh")
 
