@@ -24,6 +24,11 @@ __device__ __forceinline__ float ex2_ftz(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 // paired fp32 arithmetic (two lanes of one 64-bit register)
 __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
   uint64_t r;
@@ -621,9 +626,16 @@ __global__ void __launch_bounds__(320, 1)
         for (int i = 0; i < 64; ++i)
           if (!row_ok || key0 + i > last_key) sv[i] = -INFINITY;
       }
-      float mx = sv[0];
+      // row max in four independent three-input chains (short dependency chains)
+      float mc[4];
 #pragma unroll
-      for (int i = 1; i < 64; ++i) mx = fmaxf(mx, sv[i]);
+      for (int c = 0; c < 4; ++c) {
+        mc[c] = sv[16 * c];
+#pragma unroll
+        for (int i = 1; i < 15; i += 2) mc[c] = max3f(mc[c], sv[16 * c + i], sv[16 * c + i + 1]);
+        mc[c] = fmaxf(mc[c], sv[16 * c + 15]);
+      }
+      float mx = max3f(mc[0], mc[1], fmaxf(mc[2], mc[3]));
       mx *= a.scale_log2;  // the scale is positive: max of the scaled scores
       // row max over both halves (TMEM columns 384 + 2 * (j & 1) + half); past this
       // barrier both halves have read their scores, so P may overwrite them
@@ -641,18 +653,21 @@ __global__ void __launch_bounds__(320, 1)
       float psum;
       {
         const uint64_t sc2 = f32x2(a.scale_log2, a.scale_log2), nb2 = f32x2(-mb, -mb);
-        uint64_t acc2 = f32x2(0.0f, 0.0f);
+        uint64_t acc2[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc2[k] = f32x2(0.0f, 0.0f);
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           float x0, x1;
           unpack_f32x2(fma_f32x2(f32x2(sv[2 * c], sv[2 * c + 1]), sc2, nb2), x0, x1);
           const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
-          acc2 = add_f32x2(acc2, f32x2(p0, p1));
+          acc2[c & 3] = add_f32x2(acc2[c & 3], f32x2(p0, p1));
           pw[c] = pack_bf16x2(p0, p1);
         }
-        float s0, s1;
-        unpack_f32x2(acc2, s0, s1);
-        psum = s0 + s1;
+        float s0, s1, s2, s3;
+        unpack_f32x2(add_f32x2(acc2[0], acc2[1]), s0, s1);
+        unpack_f32x2(add_f32x2(acc2[2], acc2[3]), s2, s3);
+        psum = (s0 + s1) + (s2 + s3);
       }
       // A rescale of O waits for the previous block's PV MMA (S(j) done implies
       // PV(j-2) done, so the output barrier is at phase j-1 or j here).  A failed
