@@ -73,15 +73,23 @@ struct GemmCfg {
   static constexpr int B_BYTES = BN * 128;   // BN rows x 64 fp16
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // as many stages as fit in ~200 KB (narrow tiles stream weights: more bytes in flight)
-  static constexpr int STAGES = (204800 / STAGE_BYTES) > 12 ? 12 : (204800 / STAGE_BYTES);
+  static constexpr int STAGES = ((204800 - ((SWAP && EPI != EPI_ARGMAX) ? BN * 512 : 0)) / STAGE_BYTES) > 12
+                                     ? 12
+                                     : ((204800 - ((SWAP && EPI != EPI_ARGMAX) ? BN * 512 : 0)) / STAGE_BYTES);
   static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
-  static constexpr int QUEUE = 4;  // tile queue depth (weight-streaming path)
+  static constexpr int QUEUE = 4;  // tile queue depth (weight-streaming argmax)
+  // weight-streaming argmax: tiles from a dynamic queue; other swapped (few-token)
+  // GEMMs: static round-robin over tiles x K splits
+  static constexpr bool DYN = SWAP && EPI == EPI_ARGMAX;
+  // swapped epilogues other than the argmax stage the summed tile token-major in
+  // fp32 ([BN tokens][128 features]) and write whole token rows from there
+  static constexpr int TROW_BYTES = (SWAP && EPI != EPI_ARGMAX) ? BN * 128 * 4 : 0;
   static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * QUEUE;
   // outputs leave through TMA stores (fp16) / TMA reduce-adds (fp32 residual) from one
   // 32-row x 128-byte staging box per epilogue warp
   static constexpr bool TMA_OUT = !SWAP && (EPI == EPI_STORE || EPI == EPI_SILU || EPI == EPI_RESID);
   static constexpr int OUT_BYTES = TMA_OUT ? EW * 4096 : 0;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + OUT_BYTES + NUM_BARS * 8 + 64 + 1536;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + OUT_BYTES + TROW_BYTES + NUM_BARS * 8 + 64 + 1536;
   static_assert(SMEM <= 232448, "shared memory per block");
 };
 
@@ -338,6 +346,279 @@ __device__ __forceinline__ void qkv_stream(const GemmParams& p, uint32_t ta, int
   }
 }
 
+// ---- few-token GEMMs with the weights on the MMA's M side ----
+// The accumulator tile is 128 features (TMEM lanes) x BN tokens (columns).  Each
+// epilogue thread owns one feature row: it adds the rank segments of its unit in
+// rank order, the K splits are added in split order (last CTA to arrive), and
+// the sum is staged token-major in shared memory.  Each warp then writes whole
+// token rows: lane l holds features 4l .. 4l+3 of the tile.
+
+// q/k RMSNorm + rotate-half RoPE for one token row of one head spread over a
+// group of G lanes (G = HD / 4; lane i of the group holds dims 4i .. 4i+3), then
+// the q / k / v row written out.  ("Tensor parallelism from scratch", tp.py
+// TPAttention.forward: q_norm / k_norm, apply_rope, cache.update.)
+template <int HD>
+__device__ __forceinline__ void qkv_row_group(const GemmParams& p, int t, const TokPos& tp, int col0, int gl,
+                                              float4 v) {
+  const QkvEpi& q = p.qkv;
+  constexpr int G = HD / 4;  // lanes per head
+  constexpr int HALF = HD / 2;
+  const int r = col0 / q.w_rank;
+  const int sh = (col0 - r * q.w_rank) / HD;
+  const int d0 = 4 * gl;  // first dim of this lane
+  const size_t plane = static_cast<size_t>(q.max_seqs) * q.nkv_l * q.cap * HD;
+  __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(q.kv);
+  float y[4] = {v.x, v.y, v.z, v.w};
+  const bool is_v = sh >= q.nq_l + q.nkv_l, is_q = sh < q.nq_l;
+  {  // every lane runs the shuffles (the two heads of a 64-dim pair may be of different kinds)
+    float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = rsqrtf(ss / static_cast<float>(HD) + q.eps);
+    const __nv_bfloat16* nw = reinterpret_cast<const __nv_bfloat16*>(is_q ? q.q_norm : q.k_norm);
+    const uint2 wv = *reinterpret_cast<const uint2*>(nw + d0);
+    const float w4[4] = {bf16lo(wv.x), bf16hi(wv.x), bf16lo(wv.y), bf16hi(wv.y)};
+    float u[4], o4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) u[i] = y[i] * inv * w4[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o4[i] = __shfl_xor_sync(0xffffffffu, u[i], G / 2);  // the dim HALF away
+    const bool lower = d0 < HALF;
+    const int dr = lower ? d0 : d0 - HALF;  // rotation index of dims dr .. dr+3
+    const float4* cs4 = reinterpret_cast<const float4*>(q.rope) +
+                        (static_cast<size_t>(tp.pos >> 5) * (HALF / 2) + dr / 2) * 32 + (tp.pos & 31);
+    const float4 c01 = __ldg(cs4), c23 = __ldg(cs4 + 32);
+    const float cx[4] = {c01.x, c01.z, c23.x, c23.z};
+    const float sy[4] = {c01.y, c01.w, c23.y, c23.w};
+    if (!is_v) {  // v is cached raw
+#pragma unroll
+      for (int i = 0; i < 4; ++i) y[i] = lower ? u[i] * cx[i] - o4[i] * sy[i] : u[i] * cx[i] + o4[i] * sy[i];
+    }
+  }
+  if (col0 >= p.N) return;  // a 64-dim head past the last feature (its weights were zero fill)
+  if (is_q) {
+    if (tp.prefill) {  // bf16 high part to the QKV buffer, bf16 low part to q_lo
+      __nv_bfloat16* qhi = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(t) * p.ldo + col0 + d0;
+      __nv_bfloat16* qlo = reinterpret_cast<__nv_bfloat16*>(q.q_lo) + static_cast<size_t>(t) * q.n * q.nq_l * HD +
+                           (static_cast<size_t>(r) * q.nq_l + sh) * HD + d0;
+      float lo[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) lo[i] = y[i] - bf2f(f2bf(y[i]));
+      *reinterpret_cast<uint2*>(qhi) = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+      *reinterpret_cast<uint2*>(qlo) = make_uint2(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]));
+    } else {  // fp16 (decode attention runs in fp32)
+      __half* q16 = reinterpret_cast<__half*>(p.out) + static_cast<size_t>(t) * p.ldo + col0 + d0;
+      *reinterpret_cast<uint2*>(q16) = make_uint2(pack_f16x2(y[0], y[1]), pack_f16x2(y[2], y[3]));
+    }
+    return;
+  }
+  const int g = is_v ? sh - q.nq_l - q.nkv_l : sh - q.nq_l;
+  __nv_bfloat16* dst = kv + (2 * static_cast<size_t>(r) + (is_v ? 1 : 0)) * plane +
+                       ((static_cast<size_t>(tp.seq_slot) * q.nkv_l + g) * q.cap + tp.pos) * HD + d0;
+  *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+}
+
+// One token row t of a swapped tile (features f0 .. f0+127; this lane: f0 + 4 lane ..).
+template <int EPI>
+__device__ __forceinline__ void swap_row(const GemmParams& p, int t, int f0, int lane, float4 v) {
+  if constexpr (EPI == EPI_RESID) {  // residual += row (fp32, in place)
+    const int f = f0 + 4 * lane;
+    float* o = reinterpret_cast<float*>(p.out) + static_cast<size_t>(t) * p.ldo + f;
+    if (f + 4 <= p.out_cols) {
+      float4 x = *reinterpret_cast<float4*>(o);
+      x.x += v.x; x.y += v.y; x.z += v.z; x.w += v.w;
+      *reinterpret_cast<float4*>(o) = x;
+    } else {
+      const float vv[4] = {v.x, v.y, v.z, v.w};
+      for (int i = 0; i < 4; ++i)
+        if (f + i < p.out_cols) o[i] += vv[i];
+    }
+  } else if constexpr (EPI == EPI_STORE) {
+    const int f = f0 + 4 * lane;
+    __half* o = reinterpret_cast<__half*>(p.out) + static_cast<size_t>(t) * p.ldo + f;
+    if (f + 4 <= p.out_cols) {
+      *reinterpret_cast<uint2*>(o) = make_uint2(pack_f16x2(v.x, v.y), pack_f16x2(v.z, v.w));
+    } else {
+      const float vv[4] = {v.x, v.y, v.z, v.w};
+      for (int i = 0; i < 4; ++i)
+        if (f + i < p.out_cols) o[i] = __float2half_rn(sat_f16(vv[i]));
+    }
+  } else if constexpr (EPI == EPI_SILU) {
+    // tile rows 0..63 are gate rows, 64..127 the matching up rows: lane l < 16 pairs
+    // with lane l + 16 and writes 4 of the 64 outputs
+    float4 u;
+    u.x = __shfl_xor_sync(0xffffffffu, v.x, 16);
+    u.y = __shfl_xor_sync(0xffffffffu, v.y, 16);
+    u.z = __shfl_xor_sync(0xffffffffu, v.z, 16);
+    u.w = __shfl_xor_sync(0xffffffffu, v.w, 16);
+    if (lane < 16) {
+      const int fo = f0 / 2 + 4 * lane;
+      __half* o = reinterpret_cast<__half*>(p.out) + static_cast<size_t>(t) * p.ldo + fo;
+      const float a0 = silu_f(v.x) * u.x, a1 = silu_f(v.y) * u.y, a2 = silu_f(v.z) * u.z, a3 = silu_f(v.w) * u.w;
+      if (fo + 4 <= p.out_cols) {
+        *reinterpret_cast<uint2*>(o) = make_uint2(pack_f16x2(a0, a1), pack_f16x2(a2, a3));
+      } else {
+        const float aa[4] = {a0, a1, a2, a3};
+        for (int i = 0; i < 4; ++i)
+          if (fo + i < p.out_cols) o[i] = __float2half_rn(sat_f16(aa[i]));
+      }
+    }
+  }
+}
+
+// The q/k/v heads of one token row of a swapped QKV tile (warp-uniform token).
+__device__ __forceinline__ void swap_qkv_row(const GemmParams& p, int t, const TokPos& tp, int f0, int lane,
+                                             float4 v) {
+  if (f0 >= p.N) return;
+  if (p.qkv.hd == 128) {
+    qkv_row_group<128>(p, t, tp, f0, lane, v);
+  } else {  // two 64-dim heads per tile: lanes 0..15 and 16..31
+    qkv_row_group<64>(p, t, tp, f0 + (lane >> 4) * 64, lane & 15, v);
+  }
+}
+
+template <int BN, int EPI>
+__device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem, int warp, int lane, int units,
+                                              volatile int* abort_flag, volatile int* last_flag, float* sRow,
+                                              int* sPos, uint32_t bar0, int stages) {
+  const int q = warp & 3;         // TMEM lane quarter
+  const int wq = warp - 2;        // 0..3 for the token rows
+  const int row = q * 32 + lane;  // feature row of the tile
+  const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+  const uint32_t tfull0 = bar0 + 8u * (2 * stages), tempty0 = bar0 + 8u * (2 * stages + 2);
+  if constexpr (EPI == EPI_QKV) {
+    // every unit covers the same tokens (one token tile): their positions once, in
+    // parallel (sPos: [BN] position, [BN] cache slot, [BN] flags 1 = valid, 2 = prefill)
+    const int et = threadIdx.x - 64;
+    if (et < BN) {
+      int pos = 0, slot = 0, fl = 0;
+      if (et < p.T) {
+        const TokPos tp = token_position(p.qkv, et);
+        if (!tp.ok) raise_flag(p.status, TP_DEVFLAG_BAD_TOKEN);
+        pos = tp.pos;
+        slot = tp.seq_slot;
+        fl = (tp.ok ? 1 : 0) | (tp.prefill ? 2 : 0);
+      }
+      sPos[et] = pos;
+      sPos[BN + et] = slot;
+      sPos[2 * BN + et] = fl;
+    }
+    named_bar_sync(1, 128);
+  }
+  int seg = 0;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const Unit un = unit_of(p, u);
+    const int f0 = un.tf * 128;
+    float acc[BN];
+#pragma unroll
+    for (int i = 0; i < BN; ++i) acc[i] = 0.0f;
+    bool ok = true;
+    for (int g = un.g0; g < un.g1;) {  // one accumulator use per rank segment, in rank order
+      g = min(un.g1, (g / p.kb_seg + 1) * p.kb_seg);
+      const int b = seg & 1;
+      const uint32_t use = (seg >> 1) & 1;
+      if (!mbar_wait(tfull0 + 8u * b, use, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t ta = lane_addr + static_cast<uint32_t>(b * BN);
+      if constexpr (BN == 16) {
+        float v[16];
+        tc_ld16(ta, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] += v[i];
+      } else {
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tc_ld32(ta + c * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[c * 32 + i] += v[i];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8u * b);
+      ++seg;
+    }
+    // every epilogue thread takes the same path from here (named barriers follow)
+    if (!named_bar_and(1, 128, ok)) break;
+    if (p.splits > 1) {
+      const int tile = un.tt * p.tiles_f + un.tf;
+      float* part = p.partials + (static_cast<size_t>(tile) * p.splits + un.split) * (BN * 128);
+#pragma unroll
+      for (int t = 0; t < BN; ++t) part[t * 128 + row] = acc[t];
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (threadIdx.x == 64) {
+        const int old = atomicAdd(p.counters + tile, 1);
+        *last_flag = (old == p.splits - 1) ? 1 : 0;
+      }
+      named_bar_sync(1, 128);
+      if (*last_flag == 0) continue;
+      __threadfence();
+      const float* base = p.partials + static_cast<size_t>(tile) * p.splits * (BN * 128);
+#pragma unroll
+      for (int t = 0; t < BN; ++t) acc[t] = __ldcg(base + t * 128 + row);
+      for (int sp = 1; sp < p.splits; ++sp) {
+        const float* ps = base + static_cast<size_t>(sp) * (BN * 128);
+#pragma unroll
+        for (int t = 0; t < BN; ++t) acc[t] += __ldcg(ps + t * 128 + row);
+      }
+      if (threadIdx.x == 64) p.counters[tile] = 0;
+    }
+#pragma unroll
+    for (int t = 0; t < BN; ++t) sRow[t * 128 + row] = acc[t];
+    named_bar_sync(1, 128);
+    const int nt = min(BN, p.T - un.tt * BN);
+    if constexpr (EPI == EPI_RESID) {
+      // residual rows: all of this warp's loads first, then the adds and stores
+      constexpr int TPW = BN / 4;
+      const int f = f0 + 4 * lane;
+      if (f + 4 <= p.out_cols) {
+        float4 x[TPW];
+#pragma unroll
+        for (int k = 0; k < TPW; ++k) {
+          const int t = wq + 4 * k;
+          if (t < nt) x[k] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.out) +
+                                                              static_cast<size_t>(un.tt * BN + t) * p.ldo + f);
+        }
+#pragma unroll
+        for (int k = 0; k < TPW; ++k) {
+          const int t = wq + 4 * k;
+          if (t < nt) {
+            const float4 v = *reinterpret_cast<const float4*>(sRow + t * 128 + 4 * lane);
+            float4 y = x[k];
+            y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + static_cast<size_t>(un.tt * BN + t) * p.ldo +
+                                       f) = y;
+          }
+        }
+      } else {
+        for (int t = wq; t < nt; t += 4)
+          swap_row<EPI>(p, un.tt * BN + t, f0, lane, *reinterpret_cast<const float4*>(sRow + t * 128 + 4 * lane));
+      }
+    } else {
+      for (int t = wq; t < nt; t += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(sRow + t * 128 + 4 * lane);
+        if constexpr (EPI == EPI_QKV) {
+          const int fl = sPos[2 * BN + t];
+          TokPos tp;
+          tp.pos = sPos[t];
+          tp.seq_slot = sPos[BN + t];
+          tp.ok = (fl & 1) != 0;
+          tp.prefill = (fl & 2) != 0;
+          if (tp.ok) swap_qkv_row(p, un.tt * BN + t, tp, f0, lane, v);
+        } else {
+          swap_row<EPI>(p, un.tt * BN + t, f0, lane, v);
+        }
+      }
+    }
+    named_bar_sync(1, 128);  // the staging rows are reused by the next unit
+  }
+}
+
 template <int BN, int EPI, bool ACC, bool SWAP>
 __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -349,7 +630,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * C::A_BYTES;
   uint8_t* sOut = smem + STAGES * C::STAGE_BYTES;  // [EW][4096] output staging boxes
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + C::OUT_BYTES);
+  float* sRow = reinterpret_cast<float*>(sOut + C::OUT_BYTES);  // [BN][128] token rows (swapped epilogues)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + C::OUT_BYTES + C::TROW_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
@@ -422,8 +704,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
       // tiles; each tile id goes through a small queue to the MMA and epilogue
       // warps, -1 ends it.  Otherwise a static round-robin over the tiles.
       int qk = 0;
-      for (int u = blockIdx.x; ok && (SWAP || u < units);) {
-        if constexpr (SWAP) {
+      for (int u = blockIdx.x; ok && (C::DYN || u < units);) {
+        if constexpr (C::DYN) {
           const int id = u < units ? u : -1;
           if (!mbar_wait(QEMPTY(qk % C::QUEUE), ((qk / C::QUEUE) & 1) ^ 1u, abort_flag, p.status)) {
             ok = false;
@@ -451,7 +733,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
           tma_load_2d(wdst, &tmW, FULL(s), kb * 64, r * p.w_row_seg + f0);
           ++it;
         }
-        if constexpr (SWAP) u = static_cast<int>(gridDim.x) + atomicAdd(p.sched_counter, 1);
+        if constexpr (C::DYN) u = static_cast<int>(gridDim.x) + atomicAdd(p.sched_counter, 1);
         else u += gridDim.x;
       }
       // every load issued has landed before the CTA may exit
@@ -464,8 +746,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
       const uint32_t idesc = idesc_f16_f32(128, BN);
       int it = 0, seg = 0, qk = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && (SWAP || u < units); u += gridDim.x) {
-        if constexpr (SWAP) {
+      for (int u = blockIdx.x; ok && (C::DYN || u < units); u += gridDim.x) {
+        if constexpr (C::DYN) {
           if (!mbar_wait(QFULL(qk % C::QUEUE), (qk / C::QUEUE) & 1, abort_flag, p.status)) break;
           u = queue[qk % C::QUEUE];
           mbar_arrive(QEMPTY(qk % C::QUEUE));
@@ -508,6 +790,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
       tc_commit(DRAIN);
       mbar_wait(DRAIN, 0, nullptr, p.status);
     }
+  } else if constexpr (SWAP && EPI != EPI_ARGMAX) {
+    // ---------------- epilogue, weights on the M side, few tokens ----------------
+    // token positions: the argmax scratch area is free here (3 x 64 ints)
+    swap_epilogue<BN, EPI>(p, tmem, warp, lane, units, abort_flag, last_flag, sRow, reinterpret_cast<int*>(red_v),
+                           bar0, STAGES);
   } else if constexpr (SWAP) {
     // ---------------- epilogue, weights on the M side: argmax over features ----------------
     static_assert(EPI == EPI_ARGMAX && !ACC, "weight-streaming path implements the argmax epilogue");
@@ -923,6 +1210,28 @@ GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
     pl.partial_floats = 0;
     return pl;
   }
+  const double weight_bytes = static_cast<double>(pr.N) * total_kb * 64 * 2;
+  if (pr.T <= 64 && pr.epi != EPI_ARGMAX && weight_bytes >= 24e6) {
+    // few tokens (decode) against a large weight: weights on the M side (128-feature
+    // tiles), tokens as N, K split so that tiles x splits fill the GPU.  (For small
+    // weights the launch is latency-bound and token tiles with more K splits win.)
+    pl.swap = true;
+    pl.BN = pr.T <= 32 ? 32 : 64;
+    pl.tiles_t = 1;
+    pl.tiles_f = cdiv(pr.N, 128);
+    // at least 8 K blocks per split (the last CTA of a tile adds every split's
+    // partial serially) and at most 8 splits
+    int splits = num_sms / pl.tiles_f;
+    if (splits > total_kb / 8) splits = total_kb / 8;
+    if (splits > 8) splits = 8;
+    if (splits < 1) splits = 1;
+    pl.splits = splits;
+    pl.acc = true;
+    const int units = pl.tiles_f * splits;
+    pl.grid = units < num_sms ? units : num_sms;
+    pl.partial_floats = splits > 1 ? static_cast<size_t>(pl.tiles_f) * splits * pl.BN * 128 : 0;
+    return pl;
+  }
   pl.tiles_t = cdiv(pr.T, 128);
   // tile width: wide tiles while there are enough of them to fill the GPU
   int BN;
@@ -1041,6 +1350,14 @@ cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partia
   TP_V(64, EPI_RESID, false, false)
   TP_V(128, EPI_RESID, true, false)
   TP_V(64, EPI_RESID, true, false)
+  TP_V(32, EPI_STORE, true, true)
+  TP_V(64, EPI_STORE, true, true)
+  TP_V(32, EPI_QKV, true, true)
+  TP_V(64, EPI_QKV, true, true)
+  TP_V(32, EPI_SILU, true, true)
+  TP_V(64, EPI_SILU, true, true)
+  TP_V(32, EPI_RESID, true, true)
+  TP_V(64, EPI_RESID, true, true)
   TP_V(64, EPI_ARGMAX, false, false)
   TP_V(16, EPI_ARGMAX, false, true)
   TP_V(32, EPI_ARGMAX, false, true)

@@ -98,3 +98,14 @@ def test_slot_or_length_outside_the_cache_flags_bad_token():
     ok = r.make_batch([1, 1], [3, 4], [0, 1])
     r.layer(0, ok, hidden[:2].clone())
     assert tp_read_status(r.status) == TP_OK
+
+
+def test_decode_large_weights_64dim_heads_few_tokens():
+    """Few tokens against large weights take the weights-on-M tiles (128 features x
+    the tokens): 64-dim heads (two per tile), a prefill sequence among decode
+    sequences, K split over CTAs, tp 2."""
+    s = synth.ModelShape(hidden=4096, num_q_heads=32, num_kv_heads=8, head_dim=64, intermediate=11008, vocab=2048,
+                         num_layers=1, tie_word_embeddings=False)
+    w = synth.Workload("large_w_decode", s, (2,), ((9, 0),), (3, 70, 200, 0), 1, False)
+    g = GpuStep(w, 2, perturbed=True)
+    check_step(g, list(range(5)))
