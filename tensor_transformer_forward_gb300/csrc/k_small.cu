@@ -52,7 +52,8 @@ __global__ void embed_vocab_parallel_kernel(const int32_t* __restrict__ ids, con
 cudaError_t launch_embed(const int32_t* ids, int T, const void* embed_stacked, int n, int64_t v_local,
                          int64_t vocab, int H, void* out, int* status, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  const int threads = H / 8 < 128 ? 32 * ((H / 8 + 31) / 32) : 128;
+  // enough threads that a row takes one or two chunks per thread (the loads overlap)
+  const int threads = H / 8 < 512 ? 32 * ((H / 8 + 31) / 32) : 512;
   return launch_pdl(embed_vocab_parallel_kernel, dim3(T), dim3(threads), 0, s, ids,
                     reinterpret_cast<const uint4*>(embed_stacked), n, v_local, vocab, H, reinterpret_cast<float4*>(out),
                     status);
@@ -138,9 +139,70 @@ __global__ void rmsnorm_wide_kernel(const float4* __restrict__ x, int64_t rows, 
   }
 }
 
+// Few long rows (decode): one 256-thread block per row, every 8-element chunk of
+// the row loaded at once (CPT chunks per thread), one block-wide sum of squares.
+template <int CPT>
+__global__ void __launch_bounds__(256) rmsnorm_row_block_kernel(const float4* __restrict__ x, int64_t rows, int H,
+                                                                 const uint4* __restrict__ w, float eps,
+                                                                 uint4* __restrict__ out,
+                                                                 const int32_t* __restrict__ cu_last) {
+  griddep_wait();
+  griddep_launch();
+  __shared__ float red[8];
+  const int64_t row = blockIdx.x;
+  const int64_t src = cu_last ? cu_last[row + 1] - 1 : row;
+  const int chunks = H / 8;
+  const float4* xr = x + src * (H / 4);
+  float v[CPT][8];
+  float ss = 0.0f;
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const int c = threadIdx.x + 256 * j;
+    if (c < chunks) {
+      const float4 a = xr[2 * c], b = xr[2 * c + 1];
+      v[j][0] = a.x; v[j][1] = a.y; v[j][2] = a.z; v[j][3] = a.w;
+      v[j][4] = b.x; v[j][5] = b.y; v[j][6] = b.z; v[j][7] = b.w;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss += v[j][i] * v[j][i];
+    }
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) tot += red[i];
+  const float inv = rsqrtf(tot / static_cast<float>(H) + eps);
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const int c = threadIdx.x + 256 * j;
+    if (c < chunks) {
+      const uint4 wu = w[c];
+      const float wf[8] = {bf16lo(wu.x), bf16hi(wu.x), bf16lo(wu.y), bf16hi(wu.y),
+                           bf16lo(wu.z), bf16hi(wu.z), bf16lo(wu.w), bf16hi(wu.w)};
+      uint4 o;
+      o.x = pack_f16x2(v[j][0] * inv * wf[0], v[j][1] * inv * wf[1]);
+      o.y = pack_f16x2(v[j][2] * inv * wf[2], v[j][3] * inv * wf[3]);
+      o.z = pack_f16x2(v[j][4] * inv * wf[4], v[j][5] * inv * wf[5]);
+      o.w = pack_f16x2(v[j][6] * inv * wf[6], v[j][7] * inv * wf[7]);
+      out[row * chunks + c] = o;
+    }
+  }
+}
+
 static cudaError_t rmsnorm_rows(const void* x, int64_t rows, int H, const void* w, float eps, void* out,
                                 const int32_t* cu_last, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
+  const int chunks = H / 8;
+  if (rows <= 256 && chunks > 128 && chunks <= 4 * 256) {  // few long rows: a block per row
+    auto X = reinterpret_cast<const float4*>(x);
+    auto W = reinterpret_cast<const uint4*>(w);
+    auto O = reinterpret_cast<uint4*>(out);
+    const dim3 grid(static_cast<unsigned>(rows)), block(256);
+    if (chunks <= 256) return launch_pdl(rmsnorm_row_block_kernel<1>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
+    if (chunks <= 512) return launch_pdl(rmsnorm_row_block_kernel<2>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
+    return launch_pdl(rmsnorm_row_block_kernel<4>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
+  }
   const int vpl = (H / 8 + 31) / 32;
   const int warps = 4;
   const dim3 grid(static_cast<unsigned>((rows + warps - 1) / warps)), block(32 * warps);
