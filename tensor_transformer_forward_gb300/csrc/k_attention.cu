@@ -330,6 +330,10 @@ static cudaError_t prepare_decode(int* ctas_per_sm) {
   return cudaSuccess;
 }
 
+template <int HD, int G>
+static cudaError_t launch_decode_tc_hd(const AttnArgs& a, dim3 grid, cudaStream_t s);
+static cudaError_t decode_tc_ctas_per_sm(int G, int* per_sm);
+
 // Key splits per (sequence, rank, kv head): the count that minimises
 //   waves(units * s / resident CTAs) * (keys per split + fixed cost)
 // so that the grid fills whole waves of resident CTAs; ties go to fewer splits.
@@ -341,6 +345,13 @@ int decode_splits(int max_kv_len, int num_units, int num_sms, int hd, int G, int
   TP_OCC(128, 1) TP_OCC(128, 2) TP_OCC(128, 4) TP_OCC(128, 8)
   TP_OCC(64, 1) TP_OCC(64, 2) TP_OCC(64, 4) TP_OCC(64, 8)
 #undef TP_OCC
+  // 128-dim heads run on the tensor-core kernel: 128-key tiles, its own occupancy
+  int gran = 1, fixed = 96;
+  if (hd == 128) {
+    e = decode_tc_ctas_per_sm(G, &per_sm);
+    gran = 128;
+    fixed = 256;
+  }
   if (e != cudaSuccess) per_sm = 1;
   const long long resident = static_cast<long long>(num_sms) * per_sm;
   const int units = num_units > 0 ? num_units : 1;
@@ -352,7 +363,8 @@ int decode_splits(int max_kv_len, int num_units, int num_sms, int hd, int G, int
   long long best_cost = -1;
   for (int s = 1; s <= limit; ++s) {
     const long long waves = (static_cast<long long>(units) * s + resident - 1) / resident;
-    const long long cost = waves * ((max_kv_len + s - 1) / s + 96);
+    const long long per_split = ((max_kv_len + s - 1) / s + gran - 1) / gran * gran;
+    const long long cost = waves * (per_split + fixed);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = s;
@@ -374,12 +386,411 @@ cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s) {
   if (seqs <= 0) return cudaSuccess;
   const int G = a.nq_l / a.nkv_l;
   dim3 grid(seqs * a.n * a.nkv_l, a.splits);
+#define TP_DEC_TC(HD_, G_) \
+  if (a.hd == HD_ && G == G_) return launch_decode_tc_hd<HD_, G_>(a, grid, s);
 #define TP_DEC(HD_, G_) \
   if (a.hd == HD_ && G == G_) return launch_decode_hd<HD_, G_>(a, grid, s);
-  TP_DEC(128, 1) TP_DEC(128, 2) TP_DEC(128, 4) TP_DEC(128, 8)
+  TP_DEC_TC(128, 1) TP_DEC_TC(128, 2) TP_DEC_TC(128, 4) TP_DEC_TC(128, 8)
   TP_DEC(64, 1) TP_DEC(64, 2) TP_DEC(64, 4) TP_DEC(64, 8)
 #undef TP_DEC
+#undef TP_DEC_TC
   return cudaErrorNotSupported;
+}
+
+// ---------------------------------------------------------------------------
+// Decode on the tensor cores.  One CTA = (sequence, rank, local kv head, key
+// split), 192 threads: warp 0 streams 128-key K and V tiles of the split with TMA
+// (one stage each; two CTAs per SM overlap each other's loads), warp 1 allocates
+// TMEM and issues the MMAs, warps 2-5 run the softmax with one thread per key.
+//   S^T = K Q^T   M = 128 keys, N = 16, K = head_dim: the B operand holds the
+//                 G query heads of the kv group as bf16 high parts (rows 0..G-1)
+//                 and bf16 low parts (rows G..2G-1), so S = S_hi + S_lo carries q
+//                 to ~16 significant bits against the bf16 cache
+//   O^T += V^T P^T   M = head_dim (V read MN-major from its TMA tile), N = 16,
+//                 K = 128 keys; P^T ([head][key]) written by the softmax as bf16
+//                 high parts (rows 0..G-1) and low parts (rows G..2G-1), summed
+//                 at the end, so P also keeps ~16 significant bits
+// S^T and P^T are double-buffered; the output is rescaled only when a head's
+// running max grows by more than 2^8.  Splits combine as in the kernel above.
+// ---------------------------------------------------------------------------
+template <int HD>
+struct DtcCfg {
+  static constexpr int BK = 128;                   // keys per tile
+  static constexpr int NSUB = HD / 64;             // 64-dim sub-tiles
+  static constexpr int SUB_BYTES = BK * 128;       // [128 keys][64 dims] bf16
+  static constexpr int KT_BYTES = NSUB * SUB_BYTES;
+  static constexpr int QSUB = 16 * 128;            // [16 rows][64 dims] bf16
+  static constexpr int QT_BYTES = NSUB * QSUB;
+  static constexpr int PT_BYTES = 2 * QSUB;        // [16 heads][128 keys] bf16 (two 64-key sub-tiles)
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + KT_BYTES;
+  static constexpr int Q_OFF = V_OFF + KT_BYTES;
+  static constexpr int P_OFF = Q_OFF + QT_BYTES;   // two P^T buffers
+  static constexpr int RED_OFF = P_OFF + 2 * PT_BYTES;  // max then sum: [2][4 warps][8 heads] fp32 each
+  static constexpr int BAR_OFF = RED_OFF + 512;
+  static constexpr int SMEM = 1024 + BAR_OFF + 128;
+  static constexpr int S_COL = 0, O_COL = 32, TMEM_COLS = 64;
+};
+
+template <int HD, int G>
+__global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
+                                                             const AttnArgs a) {
+  using C = DtcCfg<HD>;
+  static_assert(2 * G <= 16, "hi and lo rows of the kv group fit N = 16");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  // barriers: 0 q_ready | 1 k_full | 2 k_empty | 3 v_full | 4 v_empty | 5,6 s_full | 7,8 p_full | 9 o_done | 10 drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
+  const uint32_t bar0 = smem_u32(bars);
+#define D_QR (bar0)
+#define D_KF (bar0 + 8u * 1)
+#define D_KE (bar0 + 8u * 2)
+#define D_VF (bar0 + 8u * 3)
+#define D_VE (bar0 + 8u * 4)
+#define D_SF(b) (bar0 + 8u * (5 + (b)))
+#define D_PF(b) (bar0 + 8u * (7 + (b)))
+#define D_OD (bar0 + 8u * 9)
+#define D_DR (bar0 + 8u * 10)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per_seq = a.n * a.nkv_l;
+  const int unit = blockIdx.x;
+  const int b = a.seq_begin + unit / per_seq;
+  const int r = (unit % per_seq) / a.nkv_l;
+  const int g = unit % a.nkv_l;
+  const int split = blockIdx.y;
+  const int t = a.cu_q[b];
+  const int L = a.ctx_len[b] + 1;
+  const int slot = a.slot[b];
+  const bool bad = slot < 0 || slot >= a.max_seqs || L < 1 || L > a.cap;
+  const int chunk = (L + a.splits - 1) / a.splits;
+  const int k0 = split * chunk;
+  const int k1 = bad ? k0 : min(L, k0 + chunk);
+  const int ntiles = k1 > k0 ? (k1 - k0 + C::BK - 1) / C::BK : 0;
+  const int krow0 = (((r * 2 + 0) * a.max_seqs + (bad ? 0 : slot)) * a.nkv_l + g) * a.cap + k0;
+  const int vrow0 = (((r * 2 + 1) * a.max_seqs + (bad ? 0 : slot)) * a.nkv_l + g) * a.cap + k0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(D_QR, 128);
+    mbar_init(D_KF, 1);
+    mbar_init(D_KE, 1);
+    mbar_init(D_VF, 1);
+    mbar_init(D_VE, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(D_SF(i), 1);
+      mbar_init(D_PF(i), 4);
+    }
+    mbar_init(D_OD, 1);
+    mbar_init(D_DR, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // q and the cache come from the QKV GEMM
+  griddep_launch();
+  if (bad && threadIdx.x == 0 && split == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
+
+  float m[G], l[G];  // running max (exp2 domain) and sum per head: the same in every softmax thread
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.0f;
+  }
+
+  if (warp == 0) {
+    // ---------------- TMA: lane 0 streams K tiles, lane 1 V tiles ----------------
+    if (lane < 2) {
+      const bool is_k = lane == 0;
+      if (is_k) tma_prefetch_desc(&tmKV);
+      const uint32_t full = is_k ? D_KF : D_VF, empty = is_k ? D_KE : D_VE;
+      uint8_t* dst = smem + (is_k ? C::K_OFF : C::V_OFF);
+      const int row0 = is_k ? krow0 : vrow0;
+      int issued = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        if (!mbar_wait(empty, (j & 1) ^ 1u, abort_flag, a.status)) break;
+        mbar_arrive_expect_tx(full, C::KT_BYTES);
+        for (int sub = 0; sub < C::NSUB; ++sub)
+          tma_load_2d(smem_u32(dst + sub * C::SUB_BYTES), &tmKV, full, sub * 64, row0 + j * C::BK);
+        issued = j + 1;
+      }
+      if (issued > 0) mbar_wait(full, (issued - 1) & 1, nullptr, a.status);  // the last tile has landed
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, 16);                 // K (K-major) x Q^T (K-major)
+      const uint32_t id_o = idesc_bf16_f32(128, 16, false, true);    // V^T (MN-major) x P^T (K-major)
+      bool ok = mbar_wait(D_QR, 0, abort_flag, a.status);
+      tc_fence_after();
+      const uint32_t qt = smem_u32(smem + C::Q_OFF), kt = smem_u32(smem + C::K_OFF), vt = smem_u32(smem + C::V_OFF);
+      auto pv = [&](int j) -> bool {  // O^T += V(j)^T P(j)^T
+        const int pb = j & 1;
+        if (!mbar_wait(D_PF(pb), (j >> 1) & 1, abort_flag, a.status)) return false;
+        if (!mbar_wait(D_VF, j & 1, abort_flag, a.status)) return false;
+        tc_fence_after();
+        const uint32_t pt = smem_u32(smem + C::P_OFF + pb * C::PT_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < C::BK / 16; ++kk) {
+          const uint64_t ad = sdesc_mn_sw128(vt + kk * 16 * 128, C::SUB_BYTES, 1024);
+          const uint64_t bd = sdesc_k_sw128(pt + (kk >> 2) * C::QSUB) + 2ull * (kk & 3);
+          tc_mma_f16(tmem + C::O_COL, ad, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(D_OD);
+        tc_commit(D_VE);
+        return true;
+      };
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int sb = j & 1;
+        // score buffer sb last held S(j-2), read by the softmax before P(j-2) was ready
+        if (!mbar_wait(D_KF, j & 1, abort_flag, a.status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t ad = sdesc_k_sw128(kt + (kk >> 2) * C::SUB_BYTES) + 2ull * (kk & 3);
+          const uint64_t bd = sdesc_k_sw128(qt + (kk >> 2) * C::QSUB) + 2ull * (kk & 3);
+          tc_mma_f16(tmem + C::S_COL + sb * 16, ad, bd, id_s, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(D_SF(sb));
+        tc_commit(D_KE);  // the K tile is free once S(j) is done
+        if (j > 0 && !pv(j - 1)) { ok = false; break; }
+      }
+      if (ok && ntiles > 0) pv(ntiles - 1);
+      tc_commit(D_DR);  // completes after every MMA above
+      mbar_wait(D_DR, 0, nullptr, a.status);
+    }
+  } else {
+    // ---------------- softmax, one thread per key of the tile (warps 2..5) ----------------
+    const int q = warp & 3;           // TMEM lane quarter
+    const int row = q * 32 + lane;    // key of the tile / output dim
+    const int wq = warp - 2;          // 0..3 for the cross-warp reductions
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    // Q^T: rows 0..G-1 = bf16(q_h), rows G..2G-1 = bf16(q_h - bf16(q_h)), the rest 0;
+    // 16-byte chunks in the 128-byte-swizzled K-major layout of the MMA's B operand
+    {
+      const __half* qrow = reinterpret_cast<const __half*>(a.qkv) + static_cast<size_t>(t) * a.n * a.w_rank +
+                           static_cast<size_t>(r) * a.w_rank + static_cast<size_t>(g) * G * HD;
+      for (int i = row; i < 16 * (HD / 8); i += 128) {
+        const int rr = i / (HD / 8), c = i % (HD / 8);  // row, 8-dim chunk
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (rr < 2 * G) {
+          const int h = rr < G ? rr : rr - G;
+          const uint4 u = *reinterpret_cast<const uint4*>(qrow + h * HD + c * 8);
+          const float x[8] = {f16lo(u.x), f16hi(u.x), f16lo(u.y), f16hi(u.y),
+                              f16lo(u.z), f16hi(u.z), f16lo(u.w), f16hi(u.w)};
+          float y[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) y[k] = rr < G ? x[k] : x[k] - bf2f(f2bf(x[k]));
+          w.x = pack_bf16x2(y[0], y[1]); w.y = pack_bf16x2(y[2], y[3]);
+          w.z = pack_bf16x2(y[4], y[5]); w.w = pack_bf16x2(y[6], y[7]);
+        }
+        *reinterpret_cast<uint4*>(smem + C::Q_OFF + (c >> 3) * C::QSUB + rr * 128 + (((c & 7) ^ (rr & 7)) << 4)) = w;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(D_QR);
+    }
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int sb = j & 1;
+      if (!mbar_wait(D_SF(sb), (j >> 1) & 1, abort_flag, a.status)) ok = false;
+      tc_fence_after();
+      float sv[16];
+      tc_ld16(lane_addr + C::S_COL + sb * 16, sv);
+      const bool valid = k0 + j * C::BK + row < k1;
+      float sc[G], mw[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        sc[h] = valid ? (sv[h] + sv[G + h]) * a.scale_log2 : -INFINITY;
+        mw[h] = warp_max(sc[h]);
+      }
+      float* rmax = red + (j & 1) * 32;  // [4 warps][8 heads], alternating buffers
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) rmax[wq * 8 + h] = mw[h];
+      }
+      // the barrier also agrees on failed waits (named barriers have no time limit)
+      if (!named_bar_and(1, 128, ok)) { ok = false; break; }
+      float mt[G], corr[G];
+      bool rescale = false;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        mt[h] = fmaxf(fmaxf(rmax[h], rmax[8 + h]), fmaxf(rmax[16 + h], rmax[24 + h]));
+        corr[h] = 1.0f;
+        if (mt[h] > m[h] + 8.0f) {  // uniform across the block
+          corr[h] = m[h] == -INFINITY ? 0.0f : exp2f(m[h] - mt[h]);
+          m[h] = mt[h];
+          rescale = true;
+        }
+      }
+      float p[G], pw[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        p[h] = exp2f(sc[h] - (m[h] == -INFINITY ? 0.0f : m[h]));
+        pw[h] = warp_sum(p[h]);
+      }
+      float* rsum = red + 64 + (j & 1) * 32;  // the same for the sums
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) rsum[wq * 8 + h] = pw[h];
+      }
+      // P^T(j): key `row` of head h at row h, column row of the [16][128] tile
+      uint8_t* pt = smem + C::P_OFF + (j & 1) * C::PT_BYTES + (row >> 6) * C::QSUB;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {  // bf16 high part in row h, bf16 low part in row G + h
+        const __nv_bfloat16 hi = f2bf(p[h]);
+        const __nv_bfloat16 lo = f2bf(p[h] - bf2f(hi));
+        const int rl = G + h;
+        *reinterpret_cast<__nv_bfloat16*>(pt + h * 128 + ((((row & 63) >> 3) ^ (h & 7)) << 4) + (row & 7) * 2) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(pt + rl * 128 + ((((row & 63) >> 3) ^ (rl & 7)) << 4) + (row & 7) * 2) = lo;
+      }
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int h = 0; h < G; ++h) l[h] = l[h] * corr[h] + (rsum[h] + rsum[8 + h] + rsum[16 + h] + rsum[24 + h]);
+      if (rescale && j > 0) {
+        // O^T columns of the rescaled heads, once O += P(j-1) V(j-1) has completed
+        // (S(j) done implies PV(j-2) done: the barrier is at phase j-1 or j)
+        if (!mbar_wait(D_OD, (j - 1) & 1, abort_flag, a.status)) ok = false;
+        if (ok) {
+          tc_fence_after();
+          float ov[16];
+          tc_ld16(lane_addr + C::O_COL, ov);
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            ov[h] *= corr[h];
+            ov[G + h] *= corr[h];
+          }
+          tc_st16(lane_addr + C::O_COL, ov);
+        }
+      }
+      if (!ok) continue;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(D_PF(sb));
+    }
+    if (ok) ok = mbar_wait(D_DR, 0, abort_flag, a.status);
+    if (named_bar_and(1, 128, ok)) {
+      tc_fence_after();
+      float ov[16];
+      tc_ld16(lane_addr + C::O_COL, ov);  // O^T row `row` = output dim row of every head
+      if (ntiles == 0) {  // an empty split never wrote the accumulator
+#pragma unroll
+        for (int h = 0; h < 16; ++h) ov[h] = 0.0f;
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) ov[h] += ov[G + h];  // P V = P_hi V + P_lo V
+      const int d = row;
+      if (d < HD) {
+        if (a.splits == 1) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            __half* o = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
+                        (static_cast<size_t>(r) * a.nq_l + g * G + h) * HD + d;
+            *o = __float2half_rn(sat_f16(l[h] > 0.0f ? ov[h] / l[h] : 0.0f));
+          }
+        } else {
+          float* part = a.part + (static_cast<size_t>(unit) * a.splits + split) * G * (HD + 2);
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            part[h * (HD + 2) + d] = ov[h];
+            if (d == 0) {
+              part[h * (HD + 2) + HD] = m[h];
+              part[h * (HD + 2) + HD + 1] = l[h];
+            }
+          }
+        }
+      }
+    }
+  }
+#undef D_QR
+#undef D_KF
+#undef D_KE
+#undef D_VF
+#undef D_VE
+#undef D_SF
+#undef D_PF
+#undef D_OD
+#undef D_DR
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (a.splits == 1) return;
+  // the last CTA of this (sequence, rank, head) to finish merges the splits in order
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) *last_flag = (atomicAdd(a.counters + unit, 1) == a.splits - 1) ? 1 : 0;
+  __syncthreads();
+  if (!*last_flag) return;
+  __threadfence();
+  const float* pbase = a.part + static_cast<size_t>(unit) * a.splits * G * (HD + 2);
+  for (int e = threadIdx.x; e < G * HD; e += blockDim.x) {
+    const int h = e / HD, d = e % HD;
+    float mm = -INFINITY, ll = 0.0f, aa = 0.0f;
+    for (int sp = 0; sp < a.splits; ++sp) {
+      const float* ps = pbase + (static_cast<size_t>(sp) * G + h) * (HD + 2);
+      const float m2 = __ldcg(ps + HD), l2 = __ldcg(ps + HD + 1), a2 = __ldcg(ps + d);
+      const float mn = fmaxf(mm, m2);
+      if (mn != -INFINITY) {
+        const float c1 = exp2f(mm - mn), c2 = exp2f(m2 - mn);
+        ll = ll * c1 + l2 * c2;
+        aa = aa * c1 + a2 * c2;
+        mm = mn;
+      }
+    }
+    __half* o = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
+                (static_cast<size_t>(r) * a.nq_l + g * G + h) * HD + d;
+    *o = __float2half_rn(sat_f16(ll > 0.0f ? aa / ll : 0.0f));
+  }
+  if (threadIdx.x == 0) a.counters[unit] = 0;
+}
+
+template <int HD, int G>
+static cudaError_t prepare_decode_tc(int* ctas_per_sm) {
+  static int occ = 0;
+  if (occ == 0) {
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_tc_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DtcCfg<HD>::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_decode_tc_kernel<HD, G>, 192, DtcCfg<HD>::SMEM);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) occ = 1;
+  }
+  *ctas_per_sm = occ;
+  return cudaSuccess;
+}
+
+static cudaError_t decode_tc_ctas_per_sm(int G, int* per_sm) {
+  if (G == 1) return prepare_decode_tc<128, 1>(per_sm);
+  if (G == 2) return prepare_decode_tc<128, 2>(per_sm);
+  if (G == 4) return prepare_decode_tc<128, 4>(per_sm);
+  if (G == 8) return prepare_decode_tc<128, 8>(per_sm);
+  return cudaErrorNotSupported;
+}
+
+template <int HD, int G>
+static cudaError_t launch_decode_tc_hd(const AttnArgs& a, dim3 grid, cudaStream_t s) {
+  using C = DtcCfg<HD>;
+  int per_sm = 0;
+  cudaError_t e0 = prepare_decode_tc<HD, G>(&per_sm);  // sets the shared-memory attribute once
+  if (e0 != cudaSuccess) return e0;
+  const int64_t kv_rows = static_cast<int64_t>(a.n) * 2 * a.max_seqs * a.nkv_l * a.cap;
+  if (kv_rows >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+  CUtensorMap mkv;
+  if (!make_tmap_2d(&mkv, a.kv, kv_rows, HD, HD, 128, true)) return cudaErrorInvalidValue;
+  return launch_pdl(attn_decode_tc_kernel<HD, G>, grid, dim3(192), C::SMEM, s, mkv, a);
 }
 
 // ---------------------------------------------------------------------------
