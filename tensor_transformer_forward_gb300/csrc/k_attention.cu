@@ -434,6 +434,7 @@ struct DtcCfg {
 
 template <int HD, int G>
 __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
+                                                             const __grid_constant__ CUtensorMap tmKV16,
                                                              const AttnArgs a) {
   using C = DtcCfg<HD>;
   static_assert(2 * G <= 16, "hi and lo rows of the kv group fit N = 16");
@@ -519,9 +520,12 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
       int issued = 0;
       for (int j = 0; j < ntiles; ++j) {
         if (!mbar_wait(empty, (j & 1) ^ 1u, abort_flag, a.status)) break;
-        mbar_arrive_expect_tx(full, C::KT_BYTES);
+        // a last tile of at most 16 keys loads 16 rows (the typical ctx + 1 tail)
+        const bool short_tail = j == ntiles - 1 && k1 - (k0 + j * C::BK) <= 16;
+        mbar_arrive_expect_tx(full, short_tail ? C::KT_BYTES / 8 : C::KT_BYTES);
         for (int sub = 0; sub < C::NSUB; ++sub)
-          tma_load_2d(smem_u32(dst + sub * C::SUB_BYTES), &tmKV, full, sub * 64, row0 + j * C::BK);
+          tma_load_2d(smem_u32(dst + sub * C::SUB_BYTES), short_tail ? &tmKV16 : &tmKV, full, sub * 64,
+                      row0 + j * C::BK);
         issued = j + 1;
       }
       if (issued > 0) mbar_wait(full, (issued - 1) & 1, nullptr, a.status);  // the last tile has landed
@@ -595,6 +599,16 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
           w.z = pack_bf16x2(y[4], y[5]); w.w = pack_bf16x2(y[6], y[7]);
         }
         *reinterpret_cast<uint4*>(smem + C::Q_OFF + (c >> 3) * C::QSUB + rr * 128 + (((c & 7) ^ (rr & 7)) << 4)) = w;
+      }
+      // A split of one short tile leaves V rows 16..127 unwritten: zero them (their
+      // P is 0, and 0 * NaN would not vanish).  Longer splits keep the previous
+      // tile's rows there, which are finite cache values.
+      if (ntiles == 1 && k1 - k0 <= 16) {
+        for (int i = row; i < C::NSUB * 112 * 8; i += 128) {
+          const int sub = i / (112 * 8), rem = i % (112 * 8);
+          *reinterpret_cast<uint4*>(smem + C::V_OFF + sub * C::SUB_BYTES + (16 + rem / 8) * 128 + (rem % 8) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
       }
       fence_proxy_async_smem();
       mbar_arrive(D_QR);
@@ -788,9 +802,10 @@ static cudaError_t launch_decode_tc_hd(const AttnArgs& a, dim3 grid, cudaStream_
   if (e0 != cudaSuccess) return e0;
   const int64_t kv_rows = static_cast<int64_t>(a.n) * 2 * a.max_seqs * a.nkv_l * a.cap;
   if (kv_rows >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
-  CUtensorMap mkv;
+  CUtensorMap mkv, mkv16;
   if (!make_tmap_2d(&mkv, a.kv, kv_rows, HD, HD, 128, true)) return cudaErrorInvalidValue;
-  return launch_pdl(attn_decode_tc_kernel<HD, G>, grid, dim3(192), C::SMEM, s, mkv, a);
+  if (!make_tmap_2d(&mkv16, a.kv, kv_rows, HD, HD, 16, true)) return cudaErrorInvalidValue;
+  return launch_pdl(attn_decode_tc_kernel<HD, G>, grid, dim3(192), C::SMEM, s, mkv, mkv16, a);
 }
 
 // ---------------------------------------------------------------------------
