@@ -76,9 +76,11 @@ def workload_config(w: synth.Workload, n: int) -> dict:
 # source at capture time and is reported only while the source is unchanged.
 # The summaries of those captures are under profiles/.
 NCU_TRAFFIC = {
-    ("qwen3_0.6b_layer_prefill2048", 2, "gemm_lm_head"): (311.240192e6 + 3.263232e6, "k_gemm.cu", "6f65af780262acdb"),
-    ("qwen3_0.6b_layer_decode64x4096", 2, "attn_decode"): (1078.347e6 + 5.781504e6, "k_attention.cu",
-                                                            "0b9845b2495a61a7"),
+    ("qwen3_0.6b_layer_prefill2048", 2, "gemm_lm_head"): (311243264 + 3043072, "k_gemm.cu", "6ef65cd8b9c4a1c0"),
+    ("qwen3_0.6b_layer_decode64x4096", 2, "attn_decode"): (1077.722e6 + 4.766976e6, "k_attention.cu",
+                                                            "ecda642c874595de"),
+    ("qwen3_32b_layer_tp16_decode32x2048", 16, "gemm_lm_head"): (1558542592 + 3048192, "k_gemm.cu",
+                                                                  "6ef65cd8b9c4a1c0"),
 }
 KERNEL_HEADERS = ("kernels.h", "sm100.cuh", "common.cuh")
 
