@@ -152,7 +152,9 @@ tp_status tp_workspace_init(tp_ctx* ctx, void* ws, size_t ws_bytes, int32_t max_
                             int32_t max_positions, void* stream);
 
 /* Intermediates of the last tp_decoder_layer_forward, inside the workspace (for tests and
- * debugging; valid until the next call): byte offset and size of
+ * debugging; valid until the next call, and only while tp_keep_intermediates(ctx, 1) is set:
+ * by default the calls drop each intermediate from L2 without writing it back once its last
+ * reader has run, so that dead data costs no HBM write traffic): byte offset and size of
  *  TP_WS_NORMED  fp16 [T, H]                  RMSNorm output (post-attention norm after the call)
  *  TP_WS_QKV     [T, n, (nq_l+2nkv_l) hd]     merged projection; its q heads hold post-RoPE q
  *                                              as bf16 (k and v go straight to the cache)
@@ -163,6 +165,9 @@ tp_status tp_workspace_init(tp_ctx* ctx, void* ws, size_t ws_bytes, int32_t max_
 #define TP_WS_ATTN 2
 #define TP_WS_ACT 3
 tp_status tp_workspace_part(const tp_ctx* ctx, int32_t part, size_t* offset, size_t* bytes);
+/* keep != 0: leave the intermediates above readable after each call (no L2 discards).
+ * The pages have no counterpart; this is a debugging switch. */
+tp_status tp_keep_intermediates(tp_ctx* ctx, int32_t keep);
 
 /* A step's batch.  Sequences [0, num_prefill) may have several new tokens; sequences
  * [num_prefill, num_seqs) have exactly one.  Tokens are packed per sequence in order. */

@@ -92,6 +92,7 @@ def _load() -> ctypes.CDLL:
         "tp_read_status": ([P, P], I32),
         "tp_rank_sum_count": ([P, pI64], I32),
         "tp_workspace_part": ([P, I32, pSZ, pSZ], I32),
+        "tp_keep_intermediates": ([P, I32], I32),
         "tp_launch_count": ([P, pI64], I32),
         "tp_profile_begin": ([P, ctypes.c_uint32, I32], I32),
         "tp_profile_end": ([P, ctypes.POINTER(F32), pI32], I32),
@@ -109,7 +110,7 @@ EXPORTED = ("tp_create", "tp_destroy", "tp_status_string", "tp_last_cuda_error",
             "tp_weights_bytes", "tp_weights_part", "tp_shard_weights", "tp_kv_cache_bytes", "tp_workspace_bytes",
             "tp_workspace_init", "tp_embed_vocab_parallel", "tp_decoder_layer_forward", "tp_lm_head_argmax",
             "tp_read_status", "tp_rank_sum_count", "tp_debug_wait_probe", "tp_workspace_part", "tp_launch_count",
-            "tp_profile_begin", "tp_profile_end", "tp_lm_head_argmax_static")
+            "tp_profile_begin", "tp_profile_end", "tp_lm_head_argmax_static", "tp_keep_intermediates")
 KERNELS = ("embed", "rmsnorm", "gemm_qkv", "rope", "attn_prefill", "attn_decode", "gemm_o", "gemm_gate_up",
            "gemm_down", "final_norm", "gemm_lm_head", "argmax")
 
@@ -249,9 +250,13 @@ class Context:
         self.workspace = ws
         return ws
 
+    def keep_intermediates(self, keep: bool = True) -> None:
+        """Leave the layer's intermediates readable after each call (debugging)."""
+        _check(_lib.tp_keep_intermediates(self.handle, 1 if keep else 0), "tp_keep_intermediates")
+
     def workspace_view(self, part: str, rows: int, cols: int, dtype=torch.float16) -> torch.Tensor:
         """[rows, cols] view of an intermediate of the last layer call (fp16; the q
-        heads of the QKV buffer hold bf16)."""
+        heads of the QKV buffer hold bf16); needs keep_intermediates()."""
         o, b = ctypes.c_size_t(), ctypes.c_size_t()
         _check(_lib.tp_workspace_part(self.handle, WS_PART[part], ctypes.byref(o), ctypes.byref(b)),
                "tp_workspace_part")

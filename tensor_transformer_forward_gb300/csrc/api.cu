@@ -59,6 +59,7 @@ struct tp_ctx {
   size_t ws_bytes = 0;
   int ws_tokens = 0, ws_seqs = 0, ws_pos = 0;
   Region r_rope, r_xn, r_qkv, r_qlo, r_attn, r_act, r_gpart, r_gcnt, r_apart, r_acnt, r_amax_v, r_amax_i, r_z;
+  bool keep_intermediates = false;  // leave dead intermediates in L2 (to read them after a call)
   int lm_tiles_max = 0;
   int num_sms = 0;
   int64_t rank_sums = 0;
@@ -212,6 +213,14 @@ struct Timed {
     if (slot >= 0) cudaEventRecord(x->prof_ev[2 * slot + 1], s);
   }
 };
+
+// Whole 128-byte lines of [p, p + bytes) for a GEMM's L2 discard list (p is
+// 256-byte aligned: workspace regions are).
+void set_discard(const tp_ctx* x, tpk::GemmProblem& g, int k, const void* p, size_t bytes) {
+  if (x->keep_intermediates) return;
+  g.discard[k] = p;
+  g.discard_lines[k] = static_cast<int64_t>(bytes / 128);
+}
 
 tp_status gemm(tp_ctx* x, int kind, const tpk::GemmProblem& pr, int32_t* dev_status, cudaStream_t s) {
   tpk::GemmPlan pl = tpk::plan_gemm(pr, x->num_sms);
@@ -560,6 +569,8 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   g.qkv.cu_q = b->cu_q; g.qkv.ctx_len = b->ctx_len; g.qkv.slot = b->slot; g.qkv.B = b->num_seqs;
   g.qkv.kv = kv; g.qkv.max_seqs = kv_max_seqs; g.qkv.cap = kv_cap;
   g.qkv.num_prefill = b->num_prefill; g.qkv.q_lo = x->ws + x->r_qlo.off;
+  // dead by now: the SiLU*up rows of the previous layer (read by its down_proj)
+  set_discard(x, g, 0, act, static_cast<size_t>(T) * n * x->i_p * 2);
   st = gemm(x, TP_K_GEMM_QKV, g, dev_status, s);
   if (st != TP_OK) return st;
 
@@ -597,6 +608,9 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   g.w = w + x->o.off; g.w_rows = static_cast<int64_t>(n) * H; g.w_cols = x->k_r; g.w_ld = x->k_r;
   g.T = T; g.N = H; g.n_seg = n; g.k_seg = x->k_r; g.x_k_seg = x->k_r; g.w_row_seg = H;
   g.epi = tpk::EPI_RESID; g.out = hidden; g.ldo = H; g.out_cols = H;
+  // dead by now: q (high part / decode q) and its low part, read by the attention
+  set_discard(x, g, 0, qkv, static_cast<size_t>(T) * n * x->w_rank * 2);
+  set_discard(x, g, 1, x->ws + x->r_qlo.off, static_cast<size_t>(T) * n * x->nq_l * x->hd * 2);
   st = gemm(x, TP_K_GEMM_O, g, dev_status, s);
   if (st != TP_OK) return st;
   x->rank_sums += 1;
@@ -614,6 +628,8 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   g.w = w + x->gate_up.off; g.w_rows = static_cast<int64_t>(n) * 2 * x->i_p; g.w_cols = H; g.w_ld = H;
   g.T = T; g.N = n * 2 * x->i_p; g.n_seg = 1; g.k_seg = H;
   g.epi = tpk::EPI_SILU; g.out = act; g.ldo = n * x->i_p; g.out_cols = n * x->i_p;
+  // dead by now: the attention output, read by o_proj
+  set_discard(x, g, 0, attn, static_cast<size_t>(T) * n * x->nq_l * x->hd * 2);
   st = gemm(x, TP_K_GEMM_GATE_UP, g, dev_status, s);
   if (st != TP_OK) return st;
 
@@ -623,6 +639,8 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   g.w = w + x->down.off; g.w_rows = static_cast<int64_t>(n) * H; g.w_cols = x->i_p; g.w_ld = x->i_p;
   g.T = T; g.N = H; g.n_seg = n; g.k_seg = x->i_p; g.x_k_seg = x->i_p; g.w_row_seg = H;
   g.epi = tpk::EPI_RESID; g.out = hidden; g.ldo = H; g.out_cols = H;
+  // dead by now: the post-attention RMSNorm rows, read by gate_up
+  set_discard(x, g, 0, xn, static_cast<size_t>(T) * H * 2);
   st = gemm(x, TP_K_GEMM_DOWN, g, dev_status, s);
   if (st != TP_OK) return st;
   x->rank_sums += 1;
@@ -654,6 +672,8 @@ tp_status tp_lm_head_argmax(tp_ctx* x, const void* head_shards, const tp_batch* 
   g.amax_val = reinterpret_cast<float*>(x->ws + x->r_amax_v.off);
   g.amax_idx = reinterpret_cast<int*>(x->ws + x->r_amax_i.off);
   g.amax_ld = B; g.logits = out_logits; g.ld_logits = x->c.vocab; g.vocab = x->c.vocab; g.out_ids = out_ids;
+  // dead by now: the last layer's SiLU*up rows (the weights stream next, through L2)
+  set_discard(x, g, 0, x->ws + x->r_act.off, static_cast<size_t>(b->num_tokens) * x->n * x->i_p * 2);
   tpk::GemmPlan pl = tpk::plan_gemm(g, x->num_sms);
   if (pl.tiles_f > x->lm_tiles_max || pl.splits != 1 || (pl.swap && pl.grid > x->lm_tiles_max)) return TP_ERR_UNSUPPORTED;
   {
@@ -668,6 +688,12 @@ tp_status tp_lm_head_argmax(tp_ctx* x, const void* head_shards, const tp_batch* 
     e = tpk::launch_argmax_reduce(g.amax_val, g.amax_idx, pl.tiles_f, B, B, out_ids, s);
   }
   if (e != cudaSuccess) return cuda_fail(e);
+  return TP_OK;
+}
+
+tp_status tp_keep_intermediates(tp_ctx* x, int32_t keep) {
+  if (!x) return TP_ERR_INVALID_ARG;
+  x->keep_intermediates = keep != 0;
   return TP_OK;
 }
 

@@ -57,6 +57,8 @@ struct GemmParams {
   unsigned long long* amax_keys;  // [T] per-token argmax keys, zero between launches
   QkvEpi qkv;
   int* status;
+  const void* discard[2];
+  int64_t discard_lines[2];
 };
 
 template <int BN, int EPI = EPI_STORE, bool ACC = false, bool SWAP = false>
@@ -690,6 +692,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
   // the set-up above overlaps the previous kernel; inputs, counters and outputs come after
   griddep_wait();
   griddep_launch();
+  if (threadIdx.x >= 64) {  // dead intermediates out of L2, no write-back
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * (blockDim.x - 64);
+    const int64_t me = static_cast<int64_t>(blockIdx.x) * (blockDim.x - 64) + (threadIdx.x - 64);
+    for (int k = 0; k < 2; ++k)
+      for (int64_t i = me; i < p.discard_lines[k]; i += nthr) l2_discard(static_cast<const char*>(p.discard[k]) + i * 128);
+  }
   // tile extents on the token and feature sides
   constexpr int TM_T = SWAP ? BN : 128;  // tokens per tile
   constexpr int TM_F = SWAP ? 128 : BN;  // features per tile
@@ -1327,6 +1335,10 @@ cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partia
   gp.sched_counter = counters + 1;
   gp.amax_keys = reinterpret_cast<unsigned long long*>(counters + kArgmaxKeyOffset);
   gp.qkv = pr.qkv;
+  for (int k = 0; k < 2; ++k) {
+    gp.discard[k] = pr.discard[k];
+    gp.discard_lines[k] = pr.discard[k] ? pr.discard_lines[k] : 0;
+  }
   gp.status = status;
   const int g = pl.grid;
 #define TP_V(BN_, EPI_, ACC_, SW_)                                                           \

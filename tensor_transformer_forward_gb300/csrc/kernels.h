@@ -86,6 +86,10 @@ struct GemmProblem {
   int vocab;        // features >= vocab are masked out of the argmax
   int32_t* out_ids; // argmax result per token (weight-streaming path: reduced in the kernel)
   QkvEpi qkv;       // EPI_QKV only
+  // dead workspace ranges (their last reader has completed) dropped from L2 without
+  // write-back by the epilogue warps at the start (128-byte aligned, whole lines)
+  const void* discard[2];
+  int64_t discard_lines[2];
 };
 
 struct GemmPlan {

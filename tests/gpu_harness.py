@@ -66,7 +66,8 @@ class GpuStep:
     """Runs one step of a workload on the GPU and keeps what the tests compare."""
 
     def __init__(self, w: synth.Workload, n: int, layers: Optional[int] = None, perturbed: bool = False,
-                 head: bool = True, logits: bool = True, capacity: Optional[int] = None):
+                 head: bool = True, logits: bool = True, capacity: Optional[int] = None,
+                 keep_intermediates: bool = False):
         from tensor_transformer_forward_gb300.runner import TPRunner
         self.w, self.n, self.perturbed = w, n, perturbed
         s = w.shape
@@ -76,6 +77,8 @@ class GpuStep:
         self.capacity = capacity or ((max_kv + 63) // 64 * 64)
         self.runner = TPRunner(model_config(s, n), self.L, w.num_seqs, self.capacity, w.num_tokens)
         r = self.runner
+        if keep_intermediates:
+            r.ctx.keep_intermediates()
         for li in range(self.L):
             full = sd.layer_weights(s, li, perturbed)
             r.load_layer(li, full)

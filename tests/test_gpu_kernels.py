@@ -152,7 +152,7 @@ def test_layer_intermediates_match_oracle_trace(n):
     128-row tiles and a ragged tail): merged QKV with post-RoPE q, attention
     output, post-attention norm, SiLU*up, then the layer outputs."""
     w = synth.Workload("prefill300", synth.QWEN3_06B, (n,), ((300, 0),), (), 1, False)
-    g = GpuStep(w, n, head=False, perturbed=True)
+    g = GpuStep(w, n, head=False, perturbed=True, keep_intermediates=True)
     s = w.shape
     T, H, hd = 300, s.hidden, s.head_dim
     shape = oi.shape_of(s)
