@@ -76,11 +76,11 @@ def workload_config(w: synth.Workload, n: int) -> dict:
 # source at capture time and is reported only while the source is unchanged.
 # The summaries of those captures are under profiles/.
 NCU_TRAFFIC = {
-    ("qwen3_0.6b_layer_prefill2048", 2, "gemm_lm_head"): (311243264 + 3043072, "k_gemm.cu", "6ef65cd8b9c4a1c0"),
-    ("qwen3_0.6b_layer_decode64x4096", 2, "attn_decode"): (1077.722e6 + 4.766976e6, "k_attention.cu",
-                                                            "ecda642c874595de"),
-    ("qwen3_32b_layer_tp16_decode32x2048", 16, "gemm_lm_head"): (1558542592 + 3048192, "k_gemm.cu",
-                                                                  "6ef65cd8b9c4a1c0"),
+    ("qwen3_0.6b_layer_prefill2048", 2, "gemm_lm_head"): (311230976 + 3280640, "k_gemm.cu", "f2d6ed64937da547"),
+    ("qwen3_0.6b_layer_decode64x4096", 2, "attn_decode"): (1077717248 + 4120320, "k_attention.cu",
+                                                            "a130fce51b14d28e"),
+    ("qwen3_32b_layer_tp16_decode32x2048", 16, "gemm_lm_head"): (1558420992 + 2980864, "k_gemm.cu",
+                                                                  "f2d6ed64937da547"),
 }
 KERNEL_HEADERS = ("kernels.h", "sm100.cuh", "common.cuh")
 
