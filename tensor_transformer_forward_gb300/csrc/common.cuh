@@ -26,6 +26,11 @@ __device__ __forceinline__ void raise_flag(int* status, int flag) {
   if (status) atomicOr(status, flag);
 }
 
+// True on every lane when v is true on every lane of the (converged) warp.  A
+// bounded wait can give up on one lane and succeed on another; warp-collective
+// instructions after it (tcgen05.ld/st, __syncwarp) need one decision per warp.
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
+
 // Programmatic dependent launch: every kernel of the path is launched so that it
 // may start while the previous kernel in the stream finishes.  A kernel calls
 // griddep_wait() before it reads anything an earlier kernel wrote and before

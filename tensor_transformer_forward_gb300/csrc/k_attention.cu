@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1;
-      if (!mbar_wait(D_SF(sb), (j >> 1) & 1, abort_flag, a.status)) ok = false;
+      if (!warp_all(mbar_wait(D_SF(sb), (j >> 1) & 1, abort_flag, a.status))) ok = false;
       tc_fence_after();
       float sv[16];
       tc_ld16(lane_addr + C::S_COL + sb * 16, sv);
@@ -673,7 +673,7 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
       if (rescale && j > 0) {
         // O^T columns of the rescaled heads, once O += P(j-1) V(j-1) has completed
         // (S(j) done implies PV(j-2) done: the barrier is at phase j-1 or j)
-        if (!mbar_wait(D_OD, (j - 1) & 1, abort_flag, a.status)) ok = false;
+        if (!warp_all(mbar_wait(D_OD, (j - 1) & 1, abort_flag, a.status))) ok = false;
         if (ok) {
           tc_fence_after();
           float ov[16];
@@ -1099,25 +1099,28 @@ __global__ void __launch_bounds__(320, 1)
       // PV(j-2) done, so the output barrier is at phase j-1 or j here).  A failed
       // wait only marks the thread; every softmax thread leaves together at the
       // next agreement point (named barriers have no time limit).
+      // The rescale is decided per row (lane) but the O update is warp-collective
+      // (tcgen05.ld/st): when any row of the warp needs it, every lane waits for
+      // the output barrier and loads and stores its O row, the others with a
+      // factor of 1.
       const bool touch_o = rescale && j > 0 && m_used != -INFINITY;
-      if (touch_o && !mbar_wait(B_OD, (j - 1) & 1, abort_flag, a.status)) ok = false;
-      if (!ok) continue;
-      if (rescale) {
-        if (touch_o) {
-          tc_fence_after();
-          const float corr = exp2f(m_used - m_new);
-          l *= corr;
+      const bool warp_touch = __any_sync(0xffffffffu, touch_o);
+      if (warp_touch && !warp_all(mbar_wait(B_OD, (j - 1) & 1, abort_flag, a.status))) ok = false;
+      if (!ok) continue;  // warp-uniform here
+      if (warp_touch) {
+        tc_fence_after();
+        const float corr = exp2f(touch_o ? m_used - m_new : 0.0f);  // no branch before the collectives
+        l *= corr;
 #pragma unroll
-          for (int c = 0; c < OH / 32; ++c) {
-            float v[32];
-            tc_ld32(lane_addr + C::O_COL + half * OH + c * 32, v);
+        for (int c = 0; c < OH / 32; ++c) {
+          float v[32];
+          tc_ld32(lane_addr + C::O_COL + half * OH + c * 32, v);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= corr;
-            tc_st32(lane_addr + C::O_COL + half * OH + c * 32, v);
-          }
+          for (int i = 0; i < 32; ++i) v[i] *= corr;
+          tc_st32(lane_addr + C::O_COL + half * OH + c * 32, v);
         }
-        m_used = m_new;
       }
+      if (rescale) m_used = m_new;
       l += psum;
       tc_st32u(lane_addr + C::S_COL + sb * 128 + half * 32, pw);
       tc_fence_before();

@@ -75,9 +75,14 @@ struct GemmCfg {
   static constexpr int B_BYTES = BN * 128;   // BN rows x 64 fp16
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // as many stages as fit in ~200 KB (narrow tiles stream weights: more bytes in flight)
-  static constexpr int STAGES = ((204800 - ((SWAP && EPI != EPI_ARGMAX) ? BN * 512 : 0)) / STAGE_BYTES) > 12
-                                     ? 12
-                                     : ((204800 - ((SWAP && EPI != EPI_ARGMAX) ? BN * 512 : 0)) / STAGE_BYTES);
+  // QKV with two warps per lane quarter (see QKV_PAIR below) keeps 3 stages: its
+  // row staging takes the room of the fourth
+  static constexpr bool QKV_PAIR = EPI == EPI_QKV && !SWAP && !ACC && EW == 8;
+  static constexpr int STAGES =
+      QKV_PAIR ? 3
+      : ((204800 - ((SWAP && EPI != EPI_ARGMAX) ? BN * 512 : 0)) / STAGE_BYTES) > 12
+          ? 12
+          : ((204800 - ((SWAP && EPI != EPI_ARGMAX) ? BN * 512 : 0)) / STAGE_BYTES);
   static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int QUEUE = 4;  // tile queue depth (weight-streaming argmax)
   // weight-streaming argmax: tiles from a dynamic queue; other swapped (few-token)
@@ -91,7 +96,12 @@ struct GemmCfg {
   // 32-row x 128-byte staging box per epilogue warp
   static constexpr bool TMA_OUT = !SWAP && (EPI == EPI_STORE || EPI == EPI_SILU || EPI == EPI_RESID);
   static constexpr int OUT_BYTES = TMA_OUT ? EW * 4096 : 0;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + OUT_BYTES + TROW_BYTES + NUM_BARS * 8 + 64 + 1536;
+  // QKV with two warps per lane quarter: q/k norm weights [2][128] fp32, the
+  // per-row partial sums of squares [2 parities][2 warps][BN/64 heads at most][128]
+  // and each warp's row staging [2 outputs][32 rows][128 bytes at most]
+  static constexpr int QKV_BYTES = QKV_PAIR ? 128 + 256 * 4 + 2 * 2 * (BN / 64) * 128 * 4 + EW * 2 * 32 * 128 : 0;
+  static constexpr int SMEM =
+      1024 + STAGES * STAGE_BYTES + OUT_BYTES + TROW_BYTES + NUM_BARS * 8 + 64 + 1536 + QKV_BYTES;
   static_assert(SMEM <= 232448, "shared memory per block");
 };
 
@@ -328,6 +338,202 @@ __device__ __forceinline__ void qkv_head(const GemmParams& p, int t, const TokPo
   }
 }
 
+// Each thread of the warp reads 8 consecutive fp32 columns of its TMEM lane.
+__device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// QKV tile epilogue with two warps per TMEM lane quarter (tokens on the M side).
+// Warp w of the pair takes rotation pairs [w*QP, (w+1)*QP) of every head in the
+// tile, i.e. dims d and d + hd/2 of those pairs; a q/k head's sum of squares is
+// completed across the pair through shared memory (ss, double-buffered by tile
+// parity).  The (cos, sin) values of the thread's token and pairs are loaded
+// before the accumulator is ready, so their latency hides behind the MMA, and
+// they serve every q/k head of the tile; the q/k norm weights sit in shared
+// memory (nw: [2][128] fp32, q then k).  Same arithmetic as qkv_head.
+// Each thread stages its row's results (two hd-byte segments per output: its
+// pairs' first and second halves) in the warp's swizzled staging rows (stg:
+// [2 outputs][32 rows][hd bytes]); the warp then writes them out as whole
+// 64-byte row segments (a few rows per instruction instead of 32 scattered
+// 16-byte pieces), each row to its own destination.
+// Returns false (on both warps of the pair) when the accumulator wait failed.
+template <int BN, int HD>
+__device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, uint32_t tfull, uint32_t use,
+                                              volatile int* abort_flag, uint32_t ta, int t, const TokPos& tp,
+                                              int f0, bool row_ok, int w, int q, int row, int par, const float* nw,
+                                              float* ss, uint8_t* stg) {
+  constexpr int HALF = HD / 2, QP = HALF / 2, NR = QP / 2, HPT = BN / HD;
+  constexpr int RB = HD;        // staged bytes per row and output: 2 segments x QP bf16
+  constexpr int CPR = RB / 16;  // 16-byte chunks per staged row
+  constexpr int RPI = 32 / CPR; // rows per write-out instruction
+  const int lane = threadIdx.x & 31;
+  const QkvEpi& e = p.qkv;
+  int kind[HPT];  // per head of the tile: 0 q, 1 k, 2 v, -1 past the last column (warp-uniform)
+  bool any_rot = false;
+#pragma unroll
+  for (int hb = 0; hb < HPT; ++hb) {
+    const int col0 = f0 + hb * HD;
+    if (col0 >= p.N) {
+      kind[hb] = -1;
+    } else {
+      const int sh = (col0 - (col0 / e.w_rank) * e.w_rank) / HD;
+      kind[hb] = sh < e.nq_l ? 0 : (sh < e.nq_l + e.nkv_l ? 1 : 2);
+      any_rot |= kind[hb] < 2;
+    }
+  }
+  const bool live = row_ok && tp.ok;
+  float4 rc[NR];
+  if (any_rot && live) {
+    const float4* cs4 = reinterpret_cast<const float4*>(e.rope) + static_cast<size_t>(tp.pos >> 5) * (HALF / 2) * 32 +
+                        (tp.pos & 31) + w * NR * 32;
+#pragma unroll
+    for (int i = 0; i < NR; ++i) rc[i] = __ldg(cs4 + i * 32);
+  } else {
+#pragma unroll
+    for (int i = 0; i < NR; ++i) rc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const bool ok = mbar_wait(tfull, use, abort_flag, p.status);
+  if (!named_bar_and(2 + q, 64, ok)) return false;
+  tc_fence_after();
+  float inv[HPT];
+#pragma unroll
+  for (int hb = 0; hb < HPT; ++hb) inv[hb] = 0.0f;
+  if (any_rot) {
+    float* mine = ss + (par * 2 + w) * (HPT * 128);
+    const float* other = ss + (par * 2 + (1 - w)) * (HPT * 128);
+#pragma unroll
+    for (int hb = 0; hb < HPT; ++hb) {
+      if (kind[hb] < 0 || kind[hb] == 2) continue;
+      float s = 0.0f;
+#pragma unroll
+      for (int c = 0; c < QP / 8; ++c) {
+        float a[8], b[8];
+        tc_ld8(ta + hb * HD + w * QP + c * 8, a);
+        tc_ld8(ta + hb * HD + HALF + w * QP + c * 8, b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s += a[i] * a[i] + b[i] * b[i];
+      }
+      mine[hb * 128 + row] = s;
+      inv[hb] = s;
+    }
+    named_bar_sync(2 + q, 64);
+#pragma unroll
+    for (int hb = 0; hb < HPT; ++hb)
+      if (kind[hb] == 0 || kind[hb] == 1)
+        inv[hb] = rsqrtf((inv[hb] + other[hb * 128 + row]) / static_cast<float>(HD) + e.eps);
+  }
+  const size_t plane = static_cast<size_t>(e.max_seqs) * e.nkv_l * e.cap * HD;
+  __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(e.kv);
+  uint8_t* my_row = stg + lane * RB;
+  uint8_t* my_row_lo = stg + 32 * RB + lane * RB;
+#pragma unroll
+  for (int hb = 0; hb < HPT; ++hb) {
+    if (kind[hb] < 0) continue;
+    const int col0 = f0 + hb * HD;
+    const int r = col0 / e.w_rank;
+    const int sh = (col0 - r * e.w_rank) / HD;
+    // destinations of this head's row (as in qkv_head): k / v rows of the rank's
+    // cache, or q (high part / fp16) in the QKV buffer and its low part
+    __nv_bfloat16* dst;
+    __nv_bfloat16* qlo = nullptr;
+    if (kind[hb] == 0) {
+      dst = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(t) * p.ldo + col0;
+      qlo = reinterpret_cast<__nv_bfloat16*>(e.q_lo) + static_cast<size_t>(t) * e.n * e.nq_l * HD +
+            (static_cast<size_t>(r) * e.nq_l + sh) * HD;
+    } else {
+      const int g = kind[hb] == 1 ? sh - e.nq_l : sh - e.nq_l - e.nkv_l;
+      dst = kv + (2 * static_cast<size_t>(r) + (kind[hb] == 2 ? 1 : 0)) * plane +
+            ((static_cast<size_t>(tp.seq_slot) * e.nkv_l + g) * e.cap + tp.pos) * HD;
+    }
+    const bool lo_out = kind[hb] == 0 && tp.prefill;  // per row
+    const float* w8 = nw + (kind[hb] == 1 ? 128 : 0);
+#pragma unroll
+    for (int c = 0; c < QP / 8; ++c) {
+      const int d0 = w * QP + c * 8;
+      float a[8], b[8];
+      __syncwarp();  // tcgen05.ld is warp-collective; rows of a mixed tile branch below
+      tc_ld8(ta + hb * HD + d0, a);
+      tc_ld8(ta + hb * HD + HALF + d0, b);
+      // staged chunk positions of this pair chunk: segment 0 (dims d0..) and 1 (HALF + d0..)
+      const int k0 = (c ^ (lane % CPR)) * 16, k1 = ((CPR / 2 + c) ^ (lane % CPR)) * 16;
+      uint4 h0, h1;
+      if (kind[hb] == 2) {  // v: raw
+        h0 = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                        pack_bf16x2(a[6], a[7]));
+        h1 = make_uint4(pack_bf16x2(b[0], b[1]), pack_bf16x2(b[2], b[3]), pack_bf16x2(b[4], b[5]),
+                        pack_bf16x2(b[6], b[7]));
+      } else {
+        float y0[8], y1[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 cc = rc[(c * 8 + i) >> 1];
+          const float cs = (i & 1) ? cc.z : cc.x;
+          const float sn = (i & 1) ? cc.w : cc.y;
+          const float u0 = a[i] * inv[hb] * w8[d0 + i];
+          const float u1 = b[i] * inv[hb] * w8[HALF + d0 + i];
+          y0[i] = u0 * cs - u1 * sn;
+          y1[i] = u1 * cs + u0 * sn;
+        }
+        if (kind[hb] == 0 && !tp.prefill) {  // decode q: fp16
+          h0 = make_uint4(pack_f16x2(y0[0], y0[1]), pack_f16x2(y0[2], y0[3]), pack_f16x2(y0[4], y0[5]),
+                          pack_f16x2(y0[6], y0[7]));
+          h1 = make_uint4(pack_f16x2(y1[0], y1[1]), pack_f16x2(y1[2], y1[3]), pack_f16x2(y1[4], y1[5]),
+                          pack_f16x2(y1[6], y1[7]));
+        } else {  // k, prefill q high part: bf16
+          h0 = make_uint4(pack_bf16x2(y0[0], y0[1]), pack_bf16x2(y0[2], y0[3]), pack_bf16x2(y0[4], y0[5]),
+                          pack_bf16x2(y0[6], y0[7]));
+          h1 = make_uint4(pack_bf16x2(y1[0], y1[1]), pack_bf16x2(y1[2], y1[3]), pack_bf16x2(y1[4], y1[5]),
+                          pack_bf16x2(y1[6], y1[7]));
+          if (lo_out) {  // q - bf16(q)
+            float l0[8], l1[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              l0[i] = y0[i] - bf2f(f2bf(y0[i]));
+              l1[i] = y1[i] - bf2f(f2bf(y1[i]));
+            }
+            *reinterpret_cast<uint4*>(my_row_lo + k0) =
+                make_uint4(pack_bf16x2(l0[0], l0[1]), pack_bf16x2(l0[2], l0[3]), pack_bf16x2(l0[4], l0[5]),
+                           pack_bf16x2(l0[6], l0[7]));
+            *reinterpret_cast<uint4*>(my_row_lo + k1) =
+                make_uint4(pack_bf16x2(l1[0], l1[1]), pack_bf16x2(l1[2], l1[3]), pack_bf16x2(l1[4], l1[5]),
+                           pack_bf16x2(l1[6], l1[7]));
+          }
+        }
+      }
+      *reinterpret_cast<uint4*>(my_row + k0) = h0;
+      *reinterpret_cast<uint4*>(my_row + k1) = h1;
+    }
+    __syncwarp();
+    // write-out: lane -> (row rr, chunk k) of the staged rows; row rr's destination
+    // comes from its owner lane
+    const unsigned long long my_dst = live ? reinterpret_cast<unsigned long long>(dst) : 0ull;
+    const unsigned long long my_lo = (live && lo_out) ? reinterpret_cast<unsigned long long>(qlo) : 0ull;
+    const bool any_lo = __any_sync(0xffffffffu, my_lo != 0ull);
+#pragma unroll
+    for (int i = 0; i < CPR; ++i) {
+      const int rr = i * RPI + lane / CPR, k = lane % CPR;
+      const int off = (k / (CPR / 2)) * HALF + w * QP + (k % (CPR / 2)) * 8;  // elements within the head row
+      const int sk = (k ^ (rr % CPR)) * 16;
+      const unsigned long long d = __shfl_sync(0xffffffffu, my_dst, rr);
+      if (d) *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(d) + off) =
+          *reinterpret_cast<const uint4*>(stg + rr * RB + sk);
+      if (any_lo) {
+        const unsigned long long dl = __shfl_sync(0xffffffffu, my_lo, rr);
+        if (dl) *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dl) + off) =
+            *reinterpret_cast<const uint4*>(stg + 32 * RB + rr * RB + sk);
+      }
+    }
+    __syncwarp();  // the staging rows are rewritten by the next head
+  }
+  return true;
+}
+
 // Streams the heads of one accumulator tile (tokens on the M side) through qkv_head.
 template <int BN, int HD>
 __device__ __forceinline__ void qkv_stream(const GemmParams& p, uint32_t ta, int t, const TokPos& tp, int f0,
@@ -519,7 +725,7 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
       g = min(un.g1, (g / p.kb_seg + 1) * p.kb_seg);
       const int b = seg & 1;
       const uint32_t use = (seg >> 1) & 1;
-      if (!mbar_wait(tfull0 + 8u * b, use, abort_flag, p.status)) {
+      if (!warp_all(mbar_wait(tfull0 + 8u * b, use, abort_flag, p.status))) {
         ok = false;
         break;
       }
@@ -642,6 +848,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
   int* red_i = reinterpret_cast<int*>(red_v + 128);          // [4][32]
   float* best_v = reinterpret_cast<float*>(red_i + 128);     // [64]
   int* best_i = reinterpret_cast<int*>(best_v + 64);         // [64]
+  // QKV_PAIR: [2][128] q/k norm weights, 128-byte aligned (the staging rows below take 16-byte accesses)
+  float* sNw = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(best_i + 64) + 127) & ~uintptr_t(127));
+  float* sSS = sNw + 256;                                    // QKV_PAIR: partial sums of squares
+  uint8_t* sStg = reinterpret_cast<uint8_t*>(sSS + 2 * 2 * (BN / 64) * 128);  // QKV_PAIR: [EW][2][32][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bar0 = smem_u32(bars);
@@ -933,6 +1143,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
     uint8_t* box = sOut + (warp - 2) * 4096;  // this warp's output staging box (TMA_OUT)
+    if constexpr (C::QKV_PAIR) {
+      const int e = threadIdx.x - 64;
+      if (e < p.qkv.hd) {
+        sNw[e] = bf2f(reinterpret_cast<const __nv_bfloat16*>(p.qkv.q_norm)[e]);
+        sNw[128 + e] = bf2f(reinterpret_cast<const __nv_bfloat16*>(p.qkv.k_norm)[e]);
+      }
+      named_bar_sync(1, 32 * C::EW);
+    }
     int seg = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit un = unit_of(p, u);
@@ -947,10 +1165,26 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
           if (!tp.ok && cbase == 0) raise_flag(p.status, TP_DEVFLAG_BAD_TOKEN);
         }
       }
-      if constexpr (!ACC) {
+      if constexpr (C::QKV_PAIR) {
         const int b = seg & 1;
         const uint32_t use = (seg >> 1) & 1;
-        if (!mbar_wait(TFULL(b), use, abort_flag, p.status)) break;
+        const uint32_t ta = lane_addr + static_cast<uint32_t>(b * BN);
+        const int w = (warp - 2) >> 2;
+        uint8_t* stg = sStg + (warp - 2) * (2 * 32 * 128);
+        const bool ok = p.qkv.hd == 128
+                            ? qkv_pair_tile<BN, 128>(p, TFULL(b), use, abort_flag, ta, t, tp, f0, row_ok, w, q, row,
+                                                     seg & 1, sNw, sSS, stg)
+                            : qkv_pair_tile<BN, 64>(p, TFULL(b), use, abort_flag, ta, t, tp, f0, row_ok, w, q, row,
+                                                    seg & 1, sNw, sSS, stg);
+        if (!ok) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(TEMPTY(b));
+        ++seg;
+      } else if constexpr (!ACC) {
+        const int b = seg & 1;
+        const uint32_t use = (seg >> 1) & 1;
+        if (!warp_all(mbar_wait(TFULL(b), use, abort_flag, p.status))) break;
         tc_fence_after();
         const uint32_t ta = lane_addr + static_cast<uint32_t>(b * BN);
         if constexpr (EPI == EPI_QKV) {
@@ -1023,7 +1257,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
           g = min(un.g1, (g / p.kb_seg + 1) * p.kb_seg);
           const int b = seg & 1;
           const uint32_t use = (seg >> 1) & 1;
-          if (!mbar_wait(TFULL(b), use, abort_flag, p.status)) {
+          if (!warp_all(mbar_wait(TFULL(b), use, abort_flag, p.status))) {
             ok = false;
             break;
           }

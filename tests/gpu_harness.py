@@ -67,7 +67,7 @@ class GpuStep:
 
     def __init__(self, w: synth.Workload, n: int, layers: Optional[int] = None, perturbed: bool = False,
                  head: bool = True, logits: bool = True, capacity: Optional[int] = None,
-                 keep_intermediates: bool = False):
+                 keep_intermediates: bool = False, q_norm_scale: float = 1.0):
         from tensor_transformer_forward_gb300.runner import TPRunner
         self.w, self.n, self.perturbed = w, n, perturbed
         s = w.shape
@@ -81,6 +81,8 @@ class GpuStep:
             r.ctx.keep_intermediates()
         for li in range(self.L):
             full = sd.layer_weights(s, li, perturbed)
+            if q_norm_scale != 1.0:  # a power of two keeps the bf16 weights exact
+                full["q_norm"].mul_(q_norm_scale)
             r.load_layer(li, full)
             del full
         if head or w.input_from_ids:

@@ -10,7 +10,7 @@ import synth
 import synth.device as sd
 from oracle import forward as of
 from oracle import inputs as oi
-from tests.gpu_harness import GpuStep, assert_close, assert_close_bf16_stored, model_config, oracle_layer
+from tests.gpu_harness import GpuStep, assert_close, assert_close_bf16_stored, model_config, oracle_layer, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -178,3 +178,76 @@ def test_layer_intermediates_match_oracle_trace(n):
     assert_close_bf16_stored(Kg, K, "cached K")
     assert_close_bf16_stored(Vg, V, "cached V")
     assert g.runner.ctx.rank_sum_count() == 2
+
+
+def _lazy_rescale_mixed_warps(q: torch.Tensor, K: torch.Tensor, group: int, bq: int = 128, bkv: int = 128,
+                              threshold: float = 8.0) -> int:
+    """Counts (head, 32-row warp, key block) triples in which the flash-attention
+    softmax's lazy rescale of O (the row max, in log2 units, grew by more than
+    ``threshold`` since the last rescale) is taken by some rows of the warp and
+    not by others.  q: [heads, T, hd] post-RoPE, K: [kv heads, T, hd]; causal."""
+    heads, T, hd = q.shape
+    s = torch.einsum("htd,hsd->hts", q, K.repeat_interleave(group, dim=0)) * (np.log2(np.e) / np.sqrt(hd))
+    s = s.masked_fill(torch.ones(T, T, dtype=torch.bool).triu(1), float("-inf"))
+    nb = (T + bkv - 1) // bkv
+    s = torch.nn.functional.pad(s, (0, nb * bkv - T), value=float("-inf"))
+    bmax = s.view(heads, T, nb, bkv).amax(dim=-1)  # [heads, T, nb]
+    m_used = torch.full((heads, T), float("-inf"), dtype=s.dtype)
+    rows_nblk = torch.arange(T) // bq + 1
+    mixed = 0
+    for j in range(nb):
+        live = rows_nblk > j
+        mx = bmax[:, :, j]
+        rescale = (mx > m_used + threshold) & live
+        touch = rescale & (m_used != float("-inf")) & (j > 0)
+        m_used = torch.where(rescale, mx, m_used)
+        w = touch[:, : T // 32 * 32].reshape(heads, -1, 32)
+        mixed += int((w.any(-1) & ~w.all(-1)).sum())
+    return mixed
+
+
+def test_prefill_attention_rescales_taken_by_part_of_a_warp():
+    """q-norm weights x 8 (exact in bf16) make the row maxima of the scores grow
+    by more than 2^8 at different key blocks for different rows of one warp, so
+    the lazy O rescale of the flash-attention softmax is taken by part of a warp
+    (the O update is warp-collective); 1024 prefill tokens, 8 key blocks."""
+    import dataclasses
+    n, T = 2, 1024
+    w = synth.Workload("prefill1024", synth.QWEN3_06B, (n,), ((T, 0),), (), 1, False)
+    g = GpuStep(w, n, head=False, perturbed=True, keep_intermediates=True, q_norm_scale=8.0)
+    s = w.shape
+    shape = oi.shape_of(s)
+    lw = oracle_layer(s, 0, True)
+    lw = dataclasses.replace(lw, q_norm=lw.q_norm * 8.0)
+    x = of.from_bf16_bits(synth.hidden_bits(T, s.hidden))
+    trace = {}
+    empty = torch.zeros(s.num_kv_heads, 0, s.head_dim, dtype=torch.float64)
+    y, K, V = of.decoder_layer(x, lw, shape, empty, empty, trace)
+    group = s.num_q_heads // s.num_kv_heads
+    mixed = _lazy_rescale_mixed_warps(trace["q"], K, group)
+    assert mixed > 100, f"the workload should split rescale decisions inside warps (got {mixed})"
+    # Scores 8x larger make the softmax sharp, and the bf16 rounding of the cached
+    # K and V (the cache format) then moves the output by itself: the oracle's own
+    # attention over bf16-rounded K, V is ~8e-2 x RMS away.  The bound is that
+    # cache error plus the usual 3e-2 for the rest of the path.
+    e_cache = rel_err(_oracle_attention(trace["q"], _bf16(K), _bf16(V), group), trace["attn"])
+    attn = g.runner.ctx.workspace_view("attn", T, s.num_q_heads * s.head_dim).float().cpu()
+    assert_close(attn, trace["attn"], "attention output", e_cache + 3e-2)
+    Kg, Vg = g.new_kv(0, 0)
+    assert_close_bf16_stored(Kg, K, "cached K")
+    assert_close_bf16_stored(Vg, V, "cached V")
+
+
+def _bf16(t: torch.Tensor) -> torch.Tensor:
+    return t.to(torch.bfloat16).to(torch.float64)
+
+
+def _oracle_attention(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, group: int) -> torch.Tensor:
+    """Causal softmax attention in fp64 (no blocking): q [heads, T, hd], K/V
+    [kv heads, T, hd] -> [T, heads * hd]."""
+    heads, T, hd = q.shape
+    Kr, Vr = K.repeat_interleave(group, 0), V.repeat_interleave(group, 0)
+    S = torch.einsum("htd,hsd->hts", q, Kr) / np.sqrt(hd)
+    S = S.masked_fill(torch.ones(T, T, dtype=torch.bool).triu(1), float("-inf"))
+    P = torch.softmax(S, dim=-1)
+    return torch.einsum("hts,hsd->htd", P, Vr).transpose(0, 1).reshape(T, heads * hd)
