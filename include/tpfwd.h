@@ -227,6 +227,21 @@ tp_status tp_lm_head_argmax(tp_ctx* ctx, const void* head_shards, const tp_batch
 tp_status tp_lm_head_argmax_static(tp_ctx* ctx, const void* head_shards, const tp_batch* batch, const void* hidden,
                                    int32_t* out_ids, float* out_logits, int32_t* dev_status, void* stream);
 
+/* Greedy generation between two forwards ([TP] tp.py main: the argmax of the last logits is
+ * appended and fed back as the next one-token input).  batch: a decode batch (num_prefill
+ * == 0, one token per sequence) whose forward (tp_decoder_layer_forward for every layer, then
+ * tp_lm_head_argmax) has just run; its device ctx_len[b] grows by one (the token that
+ * forward wrote to the cache; the array is written although tp_batch declares it const).
+ * ids: device int32 [num_seqs], that forward's argmax ids; they are copied to row *step of
+ * history (device int32 [max_rows][num_seqs]) and *step (device int32) grows by one.  All
+ * state is on the device, so a CUDA graph of one decode forward plus this call can be
+ * replayed unchanged step after step; the ids buffer can be the next forward's embedding
+ * input.  A row outside [0, max_rows) is not written and sets TP_ERR_BAD_TOKEN in
+ * *dev_status; a position beyond the cache is flagged by the next forward.
+ * TP_ERR_INVALID_ARG for a null pointer, max_rows <= 0 or a batch with prefill sequences. */
+tp_status tp_decode_advance(tp_ctx* ctx, const tp_batch* batch, const int32_t* ids, int32_t* history,
+                            int32_t max_rows, int32_t* step, int32_t* dev_status, void* stream);
+
 /* Synchronises the stream, reads the device status word and returns TP_OK,
  * TP_ERR_BAD_TOKEN or TP_ERR_TIMEOUT (the word is not cleared). */
 tp_status tp_read_status(const int32_t* dev_status, void* stream);
@@ -249,7 +264,8 @@ tp_status tp_rank_sum_count(const tp_ctx* ctx, int64_t* count);
 #define TP_K_FINAL_NORM 9
 #define TP_K_GEMM_LM_HEAD 10
 #define TP_K_ARGMAX 11
-#define TP_K_COUNT 12
+#define TP_K_DECODE_ADVANCE 12
+#define TP_K_COUNT 13
 
 /* Kernels this context has launched so far (every kernel counts once). */
 tp_status tp_launch_count(const tp_ctx* ctx, int64_t* count);

@@ -510,6 +510,28 @@ def run_sequence(seq: SeqInput, layers: Sequence[LayerWeights], hw: Optional[Hea
     return out
 
 
+def greedy_generate(prompt: torch.Tensor, layers: Sequence[LayerWeights], hw: HeadWeights, shape: Shape,
+                    steps: int, n: int = 0, comm: Optional[Comm] = None) -> Tuple[List[int], List[float], torch.Tensor]:
+    """Greedy generation as in "Tensor parallelism from scratch", tp.py main: one
+    forward over the prompt with an empty cache, then ``steps`` times: take the
+    argmax (first index on ties) of the last position's logits, append it, and run
+    a one-token forward that extends the cache.  Returns the chosen ids, the top-2
+    margin of the logits each was chosen from, and the logits of the last forward.
+    n >= 1 runs every forward through the TP emulation (the page compares the two)."""
+    empty = [torch.zeros(shape.num_kv_heads, 0, shape.head_dim, dtype=DTYPE) for _ in layers]
+    out = run_sequence(SeqInput(hidden=None, ids=prompt, k_cache=list(empty), v_cache=list(empty)), layers, hw,
+                       shape, n=n, comm=comm)
+    tokens: List[int] = []
+    margins: List[float] = []
+    for _ in range(steps):
+        top2 = torch.topk(out.logits, 2).values
+        tokens.append(out.next_id)
+        margins.append(float(top2[0] - top2[1]))
+        out = run_sequence(SeqInput(hidden=None, ids=torch.tensor([out.next_id]), k_cache=out.k_cache,
+                                    v_cache=out.v_cache), layers, hw, shape, n=n, comm=comm)
+    return tokens, margins, out.logits
+
+
 def _merge_kv(per_rank: Sequence[torch.Tensor], shape: Shape, n: int) -> torch.Tensor:
     """Global-head cache from rank caches (the first rank holding a head supplies it)."""
     got: Dict[int, torch.Tensor] = {}

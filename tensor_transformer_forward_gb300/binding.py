@@ -93,6 +93,7 @@ def _load() -> ctypes.CDLL:
         "tp_rank_sum_count": ([P, pI64], I32),
         "tp_workspace_part": ([P, I32, pSZ, pSZ], I32),
         "tp_keep_intermediates": ([P, I32], I32),
+        "tp_decode_advance": ([P, P, P, P, I32, P, P, P], I32),
         "tp_launch_count": ([P, pI64], I32),
         "tp_profile_begin": ([P, ctypes.c_uint32, I32], I32),
         "tp_profile_end": ([P, ctypes.POINTER(F32), pI32], I32),
@@ -110,9 +111,10 @@ EXPORTED = ("tp_create", "tp_destroy", "tp_status_string", "tp_last_cuda_error",
             "tp_weights_bytes", "tp_weights_part", "tp_shard_weights", "tp_kv_cache_bytes", "tp_workspace_bytes",
             "tp_workspace_init", "tp_embed_vocab_parallel", "tp_decoder_layer_forward", "tp_lm_head_argmax",
             "tp_read_status", "tp_rank_sum_count", "tp_debug_wait_probe", "tp_workspace_part", "tp_launch_count",
-            "tp_profile_begin", "tp_profile_end", "tp_lm_head_argmax_static", "tp_keep_intermediates")
+            "tp_profile_begin", "tp_profile_end", "tp_lm_head_argmax_static", "tp_keep_intermediates",
+            "tp_decode_advance")
 KERNELS = ("embed", "rmsnorm", "gemm_qkv", "rope", "attn_prefill", "attn_decode", "gemm_o", "gemm_gate_up",
-           "gemm_down", "final_norm", "gemm_lm_head", "argmax")
+           "gemm_down", "final_norm", "gemm_lm_head", "argmax", "decode_advance")
 
 
 def lib() -> ctypes.CDLL:
@@ -276,7 +278,8 @@ class Context:
 class Batch:
     """Device arrays of one step plus the host summary the launches need."""
 
-    def __init__(self, q_lens: Sequence[int], ctx_lens: Sequence[int], slots: Sequence[int], num_prefill: int):
+    def __init__(self, q_lens: Sequence[int], ctx_lens: Sequence[int], slots: Sequence[int], num_prefill: int,
+                 max_kv_len: Optional[int] = None):
         cu = [0]
         for q in q_lens:
             cu.append(cu[-1] + int(q))
@@ -286,8 +289,14 @@ class Batch:
         self.ctx_len = torch.tensor(list(ctx_lens), dtype=torch.int32, device="cuda")
         self.slot = torch.tensor(list(slots), dtype=torch.int32, device="cuda")
         pre = list(q_lens[:num_prefill])
-        self.c = TPBatch(len(q_lens), num_prefill, cu[-1], max(pre) if pre else 0,
-                         max(int(c) + int(q) for c, q in zip(ctx_lens, q_lens)),
+        # max_kv_len plans the launches; a batch whose device ctx_len grows between
+        # forwards (greedy decoding, one graph for every step) plans for its last one
+        kv = max(int(c) + int(q) for c, q in zip(ctx_lens, q_lens))
+        if max_kv_len is not None:
+            if max_kv_len < kv:
+                raise ValueError("max_kv_len below the batch's current kv length")
+            kv = int(max_kv_len)
+        self.c = TPBatch(len(q_lens), num_prefill, cu[-1], max(pre) if pre else 0, kv,
                          self.cu_q.data_ptr(), self.ctx_len.data_ptr(), self.slot.data_ptr())
 
     @property
@@ -361,6 +370,16 @@ def tp_lm_head_argmax_static(ctx: Context, head_shards: torch.Tensor, batch: Bat
                                          _dev(hidden, "hidden", torch.float32), _dev(out_ids, "out_ids", torch.int32),
                                          lg, _dev(status, "status", torch.int32), _stream()),
            "tp_lm_head_argmax_static")
+
+
+def tp_decode_advance(ctx: Context, batch: Batch, ids: torch.Tensor, history: torch.Tensor, step: torch.Tensor,
+                      status: torch.Tensor) -> None:
+    """Greedy decoding bookkeeping after a decode forward: ctx_len += 1 on the
+    device, the forward's ids to row ``step`` of ``history`` [rows, B], step += 1."""
+    _check(_lib.tp_decode_advance(ctx.handle, ctypes.byref(batch.c), _dev(ids, "ids", torch.int32),
+                                  _dev(history, "history", torch.int32), int(history.shape[0]),
+                                  _dev(step, "step", torch.int32), _dev(status, "status", torch.int32), _stream()),
+           "tp_decode_advance")
 
 
 def tp_read_status(status: torch.Tensor) -> int:

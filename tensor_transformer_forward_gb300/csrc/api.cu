@@ -691,6 +691,25 @@ tp_status tp_lm_head_argmax(tp_ctx* x, const void* head_shards, const tp_batch* 
   return TP_OK;
 }
 
+tp_status tp_decode_advance(tp_ctx* x, const tp_batch* b, const int32_t* ids, int32_t* history, int32_t max_rows,
+                            int32_t* step, int32_t* dev_status, void* stream) {
+  if (!x || !ids || !history || !step || !dev_status || max_rows <= 0) return TP_ERR_INVALID_ARG;
+  tp_status st = check_batch(x, b);
+  if (st != TP_OK) return st;
+  if (b->num_prefill != 0 || b->num_tokens != b->num_seqs) return TP_ERR_INVALID_ARG;  // decode batches only
+  st = ensure_device(x);
+  if (st != TP_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  {
+    Timed tm(x, TP_K_DECODE_ADVANCE, s);
+    e = tpk::launch_decode_advance(const_cast<int32_t*>(b->ctx_len), b->num_seqs, ids, history, max_rows, step,
+                                   dev_status, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  return TP_OK;
+}
+
 tp_status tp_keep_intermediates(tp_ctx* x, int32_t keep) {
   if (!x) return TP_ERR_INVALID_ARG;
   x->keep_intermediates = keep != 0;

@@ -299,6 +299,39 @@ cudaError_t launch_argmax_reduce(const float* val, const int* idx, int tiles, in
 }
 
 // ---------------------------------------------------------------------------
+// Greedy decoding between two forwards ("Tensor parallelism from scratch", tp.py
+// main: the argmax of the last logits is appended and fed back as the next
+// single-token input): each sequence's cached length grows by the token the
+// forward just wrote, and the forward's argmax ids go to row *step of the
+// history.  One block; the step counter lives on the device so that a captured
+// graph of the decode forward + this kernel can be replayed unchanged.
+// ---------------------------------------------------------------------------
+__global__ void decode_advance_kernel(int32_t* ctx_len, int B, const int32_t* ids, int32_t* history, int max_rows,
+                                      int32_t* step, int32_t* status) {
+  griddep_wait();
+  griddep_launch();
+  __shared__ int row;
+  if (threadIdx.x == 0) row = *step;
+  __syncthreads();
+  const bool in = row >= 0 && row < max_rows;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    ctx_len[b] += 1;
+    if (in) history[static_cast<size_t>(row) * B + b] = ids[b];
+  }
+  if (threadIdx.x == 0) {
+    if (!in) raise_flag(status, TP_DEVFLAG_BAD_TOKEN);
+    *step = row + 1;
+  }
+}
+
+cudaError_t launch_decode_advance(int32_t* ctx_len, int B, const int32_t* ids, int32_t* history, int max_rows,
+                                  int32_t* step, int32_t* status, cudaStream_t s) {
+  if (B <= 0) return cudaSuccess;
+  return launch_pdl(decode_advance_kernel, dim3(1), dim3(B < 1024 ? ((B + 31) / 32) * 32 : 1024), 0, s, ctx_len, B,
+                    ids, history, max_rows, step, status);
+}
+
+// ---------------------------------------------------------------------------
 // Bounded-wait probe: waits on an mbarrier that nothing completes (and on a
 // global flag the caller never sets), with the same bounded wait the GEMM
 // uses; must return with TP_DEVFLAG_TIMEOUT set instead of hanging.

@@ -150,6 +150,8 @@ cudaError_t launch_final_norm_select(const void* hidden, int H, const int32_t* c
 cudaError_t launch_argmax_reduce(const float* val, const int* idx, int tiles, int ld, int B, int32_t* out,
                                  cudaStream_t s);
 cudaError_t launch_wait_probe(const int* flag, int* status, long long limit_ns, cudaStream_t s);
+cudaError_t launch_decode_advance(int32_t* ctx_len, int B, const int32_t* ids, int32_t* history, int max_rows,
+                                  int32_t* step, int32_t* status, cudaStream_t s);
 cudaError_t launch_bf16_to_f16(void* w, size_t elems, cudaStream_t s);
 
 }  // namespace tpk

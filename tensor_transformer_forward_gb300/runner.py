@@ -8,13 +8,13 @@ or a few C-ABI calls on the current stream.
 
 from __future__ import annotations
 
-from typing import Dict, List, Optional, Sequence
+from typing import Dict, List, Optional, Sequence, Tuple
 
 import torch
 
 from .binding import (WEIGHTS_HEAD, WEIGHTS_LAYER, Batch, Context, ModelConfig, TP_OK, TPError,
-                      tp_decoder_layer_forward, tp_embed_vocab_parallel, tp_lm_head_argmax, tp_read_status,
-                      tp_shard_weights)
+                      tp_decode_advance, tp_decoder_layer_forward, tp_embed_vocab_parallel, tp_lm_head_argmax,
+                      tp_read_status, tp_shard_weights)
 
 
 class TPRunner:
@@ -93,6 +93,57 @@ class TPRunner:
         if run_head:
             self.head(batch, hidden, out_ids, out_logits)
         return hidden
+
+    # ---- greedy generation ----
+    def generate(self, prompts: Sequence[Sequence[int]], steps: int, graph: bool = True,
+                 slots: Optional[Sequence[int]] = None) -> Tuple[List[List[int]], torch.Tensor]:
+        """Greedy generation as the pages' tp.py main does it: one prefill forward
+        over the prompts, then ``steps`` one-token forwards, each fed the argmax of
+        the previous one; returns the ``steps`` chosen ids per sequence and the fp32
+        logits [B, V] of the last forward.  The decode forward (embedding, layers,
+        head, then tp_decode_advance) is captured once in a CUDA graph and replayed
+        (graph=False launches it eagerly every step; both give the same ids)."""
+        B = len(prompts)
+        lens = [len(p) for p in prompts]
+        if B == 0 or min(lens) < 1 or steps < 1:
+            raise ValueError("generate needs at least one non-empty prompt and one step")
+        if max(lens) + steps > self.capacity:
+            raise ValueError("prompt + steps exceed the KV cache capacity")
+        slots = list(range(B)) if slots is None else list(slots)
+        H, V = self.cfg.hidden, self.cfg.vocab
+        dev = "cuda"
+        cur = torch.empty(B, dtype=torch.int32, device=dev)  # argmax ids out, next embedding input in
+        history = torch.full((steps + 1, B), -1, dtype=torch.int32, device=dev)
+        logits = torch.empty(B, V, dtype=torch.float32, device=dev)
+        step_ctr = torch.ones(1, dtype=torch.int32, device=dev)  # row 0 holds the prefill's ids
+        # prefill forward
+        ids = torch.tensor([t for p in prompts for t in p], dtype=torch.int32, device=dev)
+        pb = self.make_batch(lens, [0] * B, slots, num_prefill=B)
+        hidden_p = torch.empty(sum(lens), H, dtype=torch.float32, device=dev)
+        self.step(pb, ids=ids, hidden=hidden_p, out_ids=cur)
+        history[0].copy_(cur)
+        # decode forwards: positions lens[b], lens[b] + 1, ...; launches planned for the last
+        db = Batch([1] * B, lens, slots, 0, max_kv_len=max(lens) + steps)
+        hidden_d = torch.empty(B, H, dtype=torch.float32, device=dev)
+
+        def decode() -> None:
+            self.step(db, ids=cur, hidden=hidden_d, out_ids=cur, out_logits=logits)
+            tp_decode_advance(self.ctx, db, cur, history, step_ctr, self.status)
+
+        decode()  # eager: also makes every kernel variant ready before a capture
+        if graph and steps > 1:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                decode()
+            for _ in range(steps - 1):
+                g.replay()
+        else:
+            for _ in range(steps - 1):
+                decode()
+        torch.cuda.synchronize()
+        self.check_status()
+        got = history[:steps].t().cpu().tolist()
+        return got, logits
 
     def check_status(self) -> None:
         st = tp_read_status(self.status)

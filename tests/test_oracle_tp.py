@@ -184,3 +184,26 @@ def test_column_then_row_needs_no_exchange_between():
         cols = of.shard_index("o", SMALL, n, r)[1]
         parts.append(attn[:, cols] @ rl.o.T)
     assert torch.allclose(of.Comm().all_reduce(parts), attn @ w.o.T, atol=1e-12)
+
+
+def test_greedy_generation_cache_equals_recompute_and_tp_equals_unsharded():
+    """The generation loop against two things it does not compute itself: every
+    step's token and the last logits equal a cache-free forward over prompt +
+    tokens so far (positions, RoPE offsets and cache appends of the loop), and the
+    TP emulation generates the same tokens as the unsharded model (the page's own
+    check of its 20 greedy tokens)."""
+    layers, hw = _weights(SMALL, 20, layers=2)
+    prompt = torch.randint(0, SMALL.vocab, (7,), generator=torch.Generator().manual_seed(21))
+    tokens, margins, last = of.greedy_generate(prompt, layers, hw, SMALL, steps=6)
+    assert len(tokens) == 6 and all(m >= 0 for m in margins)
+    empty = [torch.zeros(SMALL.num_kv_heads, 0, SMALL.head_dim, dtype=D) for _ in layers]
+    seq = prompt.clone()
+    for k in range(6):
+        full = of.run_sequence(of.SeqInput(None, seq, list(empty), list(empty)), layers, hw, SMALL)
+        assert full.next_id == tokens[k]
+        seq = torch.cat([seq, torch.tensor([tokens[k]])])
+    full = of.run_sequence(of.SeqInput(None, seq, list(empty), list(empty)), layers, hw, SMALL)
+    assert torch.allclose(last, full.logits, rtol=1e-10, atol=1e-10)
+    tp_tokens, _, tp_last = of.greedy_generate(prompt, layers, hw, SMALL, steps=6, n=2)
+    assert tp_tokens == tokens
+    assert torch.allclose(tp_last, last, rtol=1e-10, atol=1e-10)
