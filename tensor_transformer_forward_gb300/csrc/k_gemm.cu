@@ -1494,7 +1494,11 @@ GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
   pl.tiles_f = cdiv(pr.N, BN);
   const int tiles = pl.tiles_t * pl.tiles_f;
   int splits = 1;
-  if (pr.epi != EPI_ARGMAX && tiles < num_sms) {
+  // K splits fill the GPU when tiles are few, but each split costs a partial
+  // written and re-read; a few-token GEMM with at least 32 feature tiles (QKV,
+  // gate_up at decode) streams its weights faster unsplit (measured, 0.6B decode)
+  const bool few_tokens_wide = pr.T <= 64 && tiles >= 32 && pr.n_seg == 1;
+  if (pr.epi != EPI_ARGMAX && tiles < num_sms && !few_tokens_wide) {
     splits = num_sms / tiles;
     if (splits > total_kb / 2) splits = total_kb / 2;
     if (splits < 1) splits = 1;
