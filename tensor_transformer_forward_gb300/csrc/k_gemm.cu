@@ -1503,6 +1503,9 @@ GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
     if (splits > total_kb / 2) splits = total_kb / 2;
     if (splits < 1) splits = 1;
   }
+  // few-token row-parallel GEMMs (o_proj, down at decode): at most 4 K splits (a
+  // sweep of 2 / 4 / 6 / 9 on the 0.6B layer found 4 best: fewer partials to add)
+  if (pr.T <= 64 && pr.n_seg > 1 && splits > 4) splits = 4;
   pl.splits = splits;
   pl.acc = (pr.n_seg > 1) || (splits > 1);
   if (pl.acc && BN > 128) {  // running sums need BN <= 128
