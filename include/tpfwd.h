@@ -103,7 +103,10 @@ tp_status tp_shard_index_map(const tp_ctx* ctx, int32_t kind, int32_t rank, int6
  * The projection parts (QKV, O, GATE_UP, DOWN) and the LM head are tensor-core operands and
  * are stored fp16 (converted from the bf16 inputs: exact for magnitudes in [2^-14, 65504],
  * smaller ones rounded to fp16's subnormal grid, larger ones saturated); embedding rows and
- * norm weights stay bf16.
+ * norm weights stay bf16.  QKV and GATE_UP hold their columns multiplied by the RMSNorm
+ * weight that precedes them (input norm, post-attention norm): W[r][c] * w[c], the exact
+ * bf16 x bf16 product rounded once to fp16.  The norms themselves are deferred: the layer
+ * scales each output row by rsqrt(mean(x^2) + eps) of its input row.
  */
 #define TP_WEIGHTS_LAYER 0
 #define TP_WEIGHTS_HEAD 1
@@ -155,7 +158,9 @@ tp_status tp_workspace_init(tp_ctx* ctx, void* ws, size_t ws_bytes, int32_t max_
  * debugging; valid until the next call, and only while tp_keep_intermediates(ctx, 1) is set:
  * by default the calls drop each intermediate from L2 without writing it back once its last
  * reader has run, so that dead data costs no HBM write traffic): byte offset and size of
- *  TP_WS_NORMED  fp16 [T, H]                  RMSNorm output (post-attention norm after the call)
+ *  TP_WS_NORMED  fp16 [T, H]                  the residual rows the post-attention norm reads (after
+ *                                              the call; the norm is deferred into gate_up, whose
+ *                                              epilogue scales row t by rsqrt(mean(x_t^2) + eps))
  *  TP_WS_QKV     [T, n, (nq_l+2nkv_l) hd]     merged projection; its q heads hold post-RoPE q
  *                                              as bf16 (k and v go straight to the cache)
  *  TP_WS_ATTN    fp16 [T, n * nq_l * hd]      attention output (o_proj input)

@@ -58,7 +58,7 @@ struct tp_ctx {
   char* ws = nullptr;
   size_t ws_bytes = 0;
   int ws_tokens = 0, ws_seqs = 0, ws_pos = 0;
-  Region r_rope, r_xn, r_qkv, r_qlo, r_attn, r_act, r_gpart, r_gcnt, r_apart, r_acnt, r_amax_v, r_amax_i, r_z;
+  Region r_rope, r_xn, r_qkv, r_qlo, r_attn, r_act, r_gpart, r_gcnt, r_apart, r_acnt, r_amax_v, r_amax_i, r_z, r_ss;
   bool keep_intermediates = false;  // leave dead intermediates in L2 (to read them after a call)
   int lm_tiles_max = 0;
   int num_sms = 0;
@@ -137,7 +137,7 @@ void lay_out(tp_ctx* x) {
 }
 
 struct WsPlan {
-  Region rope, xn, qkv, qlo, attn, act, gpart, gcnt, apart, acnt, amax_v, amax_i, z;
+  Region rope, xn, qkv, qlo, attn, act, gpart, gcnt, apart, acnt, amax_v, amax_i, z, ss;
   size_t total = 0;
   int lm_tiles = 0;
 };
@@ -166,6 +166,7 @@ WsPlan plan_ws(const tp_ctx* x, int64_t T, int64_t B, int64_t P) {
   take(w.amax_v, static_cast<size_t>(w.lm_tiles) * B * 4);
   take(w.amax_i, static_cast<size_t>(w.lm_tiles) * B * 4);
   take(w.z, B * H * 2);
+  take(w.ss, T * (H / 32) * 4);  // deferred RMSNorm: sums of squares of 32-column groups
   w.total = off;
   return w;
 }
@@ -438,8 +439,18 @@ tp_status tp_shard_weights(tp_ctx* x, const tp_layer_full* L, const tp_head_full
     TP_CUDA(cudaMemcpyAsync(d + x->post_norm.off, L->post_norm, row, cudaMemcpyDeviceToDevice, s));
     TP_CUDA(cudaMemcpyAsync(d + x->q_norm.off, L->q_norm, hd * 2, cudaMemcpyDeviceToDevice, s));
     TP_CUDA(cudaMemcpyAsync(d + x->k_norm.off, L->k_norm, hd * 2, cudaMemcpyDeviceToDevice, s));
-    // the projection shards are tensor-core operands: stored fp16
-    for (const Region* r : {&x->qkv, &x->o, &x->gate_up, &x->down}) {
+    // the projection shards are tensor-core operands: stored fp16; the RMSNorm
+    // weights that precede QKV and gate_up are folded into their columns
+    // (x_n W^T = (x inv) (W diag(w))^T, the row scale inv applied in the epilogue)
+    {
+      cudaError_t e = tpk::launch_fold_norm_f16(d + x->qkv.off, static_cast<size_t>(n) * x->w_rank, x->H,
+                                                d + x->in_norm.off, s);
+      if (e == cudaSuccess)
+        e = tpk::launch_fold_norm_f16(d + x->gate_up.off, static_cast<size_t>(n) * 2 * x->i_p, x->H,
+                                      d + x->post_norm.off, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    for (const Region* r : {&x->o, &x->down}) {
       cudaError_t e = tpk::launch_bf16_to_f16(d + r->off, r->bytes / 2, s);
       if (e != cudaSuccess) return cuda_fail(e);
     }
@@ -493,7 +504,7 @@ tp_status tp_workspace_init(tp_ctx* x, void* ws, size_t ws_bytes, int32_t max_to
   x->ws_pos = max_positions;
   x->r_rope = w.rope; x->r_xn = w.xn; x->r_qkv = w.qkv; x->r_qlo = w.qlo; x->r_attn = w.attn; x->r_act = w.act;
   x->r_gpart = w.gpart; x->r_gcnt = w.gcnt; x->r_apart = w.apart; x->r_acnt = w.acnt;
-  x->r_amax_v = w.amax_v; x->r_amax_i = w.amax_i; x->r_z = w.z;
+  x->r_amax_v = w.amax_v; x->r_amax_i = w.amax_i; x->r_z = w.z; x->r_ss = w.ss;
   x->lm_tiles_max = w.lm_tiles;
   TP_CUDA(cudaMemsetAsync(x->ws + w.gcnt.off, 0, w.gcnt.bytes, s));
   TP_CUDA(cudaMemsetAsync(x->ws + w.acnt.off, 0, w.acnt.bytes, s));
@@ -549,10 +560,14 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   void* act = x->ws + x->r_act.off;
   cudaError_t e;
 
-  // A3: input RMSNorm
+  float* ss = reinterpret_cast<float*>(x->ws + x->r_ss.off);
+
+  // A3: input RMSNorm, deferred: the fp16 residual rows and their sums of squares
+  // here; w_in is folded into the QKV weights and each row's rsqrt(mean + eps)
+  // scales its accumulators in the QKV epilogue
   {
     Timed tm(x, TP_K_RMSNORM, s);
-    e = tpk::launch_rmsnorm(hidden, T, H, w + x->in_norm.off, x->c.rms_eps, xn, s);
+    e = tpk::launch_row_stats(hidden, T, H, xn, ss, s);
   }
   if (e != cudaSuccess) return cuda_fail(e);
 
@@ -569,6 +584,7 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   g.qkv.cu_q = b->cu_q; g.qkv.ctx_len = b->ctx_len; g.qkv.slot = b->slot; g.qkv.B = b->num_seqs;
   g.qkv.kv = kv; g.qkv.max_seqs = kv_max_seqs; g.qkv.cap = kv_cap;
   g.qkv.num_prefill = b->num_prefill; g.qkv.q_lo = x->ws + x->r_qlo.off;
+  g.row_ss = ss; g.row_groups = H / 32; g.row_eps = x->c.rms_eps;
   // dead by now: the SiLU*up rows of the previous layer (read by its down_proj)
   set_discard(x, g, 0, act, static_cast<size_t>(T) * n * x->i_p * 2);
   st = gemm(x, TP_K_GEMM_QKV, g, dev_status, s);
@@ -615,10 +631,10 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   if (st != TP_OK) return st;
   x->rank_sums += 1;
 
-  // A8: post-attention RMSNorm
+  // A8: post-attention RMSNorm, deferred as A3 (w_post folded into gate_up)
   {
     Timed tm(x, TP_K_RMSNORM, s);
-    e = tpk::launch_rmsnorm(hidden, T, H, w + x->post_norm.off, x->c.rms_eps, xn, s);
+    e = tpk::launch_row_stats(hidden, T, H, xn, ss, s);
   }
   if (e != cudaSuccess) return cuda_fail(e);
 
@@ -628,6 +644,7 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   g.w = w + x->gate_up.off; g.w_rows = static_cast<int64_t>(n) * 2 * x->i_p; g.w_cols = H; g.w_ld = H;
   g.T = T; g.N = n * 2 * x->i_p; g.n_seg = 1; g.k_seg = H;
   g.epi = tpk::EPI_SILU; g.out = act; g.ldo = n * x->i_p; g.out_cols = n * x->i_p;
+  g.row_ss = ss; g.row_groups = H / 32; g.row_eps = x->c.rms_eps;
   // dead by now: the attention output, read by o_proj
   set_discard(x, g, 0, attn, static_cast<size_t>(T) * n * x->nq_l * x->hd * 2);
   st = gemm(x, TP_K_GEMM_GATE_UP, g, dev_status, s);

@@ -59,6 +59,9 @@ struct GemmParams {
   int* status;
   const void* discard[2];
   int64_t discard_lines[2];
+  const float* row_ss;  // deferred RMSNorm: per-row 32-column sums of squares, or null
+  int row_groups;
+  float row_inv_k, row_eps;
 };
 
 template <int BN, int EPI = EPI_STORE, bool ACC = false, bool SWAP = false>
@@ -118,6 +121,26 @@ __device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
   un.g0 = static_cast<int>((static_cast<long long>(un.split) * p.total_kb) / p.splits);
   un.g1 = static_cast<int>((static_cast<long long>(un.split + 1) * p.total_kb) / p.splits);
   return un;
+}
+
+// Deferred RMSNorm of input row t: rsqrt(mean of squares + eps) from the
+// row's 32-column sums of squares ("Tensor parallelism from scratch", the
+// RMSNorm before each projection; its weight is folded into W), 1 without them.
+__device__ __forceinline__ float row_scale(const GemmParams& p, int t) {
+  if (p.row_ss == nullptr) return 1.0f;
+  const float* g = p.row_ss + static_cast<size_t>(t) * p.row_groups;
+  float s0 = 0.0f, s1 = 0.0f;
+  int i = 0;
+  if ((p.row_groups & 3) == 0) {
+    for (; i < p.row_groups; i += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(g + i);
+      s0 += v.x + v.y;
+      s1 += v.z + v.w;
+    }
+  } else {
+    for (; i < p.row_groups; ++i) s0 += g[i];
+  }
+  return rsqrtf((s0 + s1) * p.row_inv_k + p.row_eps);
 }
 
 // fast divide: the result is rounded to fp16 (11 bits) next, far coarser than its ~2 ulp fp32 error;
@@ -367,7 +390,7 @@ template <int BN, int HD>
 __device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, uint32_t tfull, uint32_t use,
                                               volatile int* abort_flag, uint32_t ta, int t, const TokPos& tp,
                                               int f0, bool row_ok, int w, int q, int row, int par, const float* nw,
-                                              float* ss, uint8_t* stg) {
+                                              float* ss, uint8_t* stg, float rinv) {
   constexpr int HALF = HD / 2, QP = HALF / 2, NR = QP / 2, HPT = BN / HD;
   constexpr int RB = HD;        // staged bytes per row and output: 2 segments x QP bf16
   constexpr int CPR = RB / 16;  // 16-byte chunks per staged row
@@ -426,7 +449,7 @@ __device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, uint32_t tful
 #pragma unroll
     for (int hb = 0; hb < HPT; ++hb)
       if (kind[hb] == 0 || kind[hb] == 1)
-        inv[hb] = rsqrtf((inv[hb] + other[hb * 128 + row]) / static_cast<float>(HD) + e.eps);
+        inv[hb] = rsqrtf((inv[hb] + other[hb * 128 + row]) * (rinv * rinv) / static_cast<float>(HD) + e.eps);
   }
   const size_t plane = static_cast<size_t>(e.max_seqs) * e.nkv_l * e.cap * HD;
   __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(e.kv);
@@ -460,6 +483,11 @@ __device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, uint32_t tful
       __syncwarp();  // tcgen05.ld is warp-collective; rows of a mixed tile branch below
       tc_ld8(ta + hb * HD + d0, a);
       tc_ld8(ta + hb * HD + HALF + d0, b);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {  // deferred RMSNorm of the input row
+        a[i] *= rinv;
+        b[i] *= rinv;
+      }
       // staged chunk positions of this pair chunk: segment 0 (dims d0..) and 1 (HALF + d0..)
       const int k0 = (c ^ (lane % CPR)) * 16, k1 = ((CPR / 2 + c) ^ (lane % CPR)) * 16;
       uint4 h0, h1;
@@ -537,7 +565,7 @@ __device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, uint32_t tful
 // Streams the heads of one accumulator tile (tokens on the M side) through qkv_head.
 template <int BN, int HD>
 __device__ __forceinline__ void qkv_stream(const GemmParams& p, uint32_t ta, int t, const TokPos& tp, int f0,
-                                           bool row_ok, int c_begin, int c_end) {
+                                           bool row_ok, int c_begin, int c_end, float rinv) {
 #pragma unroll 1
   for (int hb = c_begin / HD; hb < c_end / HD; ++hb) {
     const int col0 = f0 + hb * HD;
@@ -548,7 +576,7 @@ __device__ __forceinline__ void qkv_stream(const GemmParams& p, uint32_t ta, int
       float v[32];
       tc_ld32(ta + hb * HD + c * 32, v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) h[c * 32 + i] = v[i];
+      for (int i = 0; i < 32; ++i) h[c * 32 + i] = v[i] * rinv;
     }
     if (row_ok && tp.ok) qkv_head<HD>(p, t, tp, col0, h);
   }
@@ -694,6 +722,14 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
   const int row = q * 32 + lane;  // feature row of the tile
   const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
   const uint32_t tfull0 = bar0 + 8u * (2 * stages), tempty0 = bar0 + 8u * (2 * stages + 2);
+  // every unit covers the same tokens (one token tile): their deferred-RMSNorm
+  // row scales once (sInv: [BN], after the [3][BN] position table)
+  float* sInv = reinterpret_cast<float*>(sPos + 192);
+  if constexpr (EPI == EPI_QKV || EPI == EPI_SILU) {
+    const int et = threadIdx.x - 64;
+    if (et < BN) sInv[et] = et < p.T ? row_scale(p, et) : 0.0f;
+    if constexpr (EPI == EPI_SILU) named_bar_sync(1, 128);
+  }
   if constexpr (EPI == EPI_QKV) {
     // every unit covers the same tokens (one token tile): their positions once, in
     // parallel (sPos: [BN] position, [BN] cache slot, [BN] flags 1 = valid, 2 = prefill)
@@ -809,7 +845,14 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
       }
     } else {
       for (int t = wq; t < nt; t += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(sRow + t * 128 + 4 * lane);
+        float4 v = *reinterpret_cast<const float4*>(sRow + t * 128 + 4 * lane);
+        if constexpr (EPI == EPI_QKV || EPI == EPI_SILU) {
+          const float ri = sInv[t];
+          v.x *= ri;
+          v.y *= ri;
+          v.z *= ri;
+          v.w *= ri;
+        }
         if constexpr (EPI == EPI_QKV) {
           const int fl = sPos[2 * BN + t];
           TokPos tp;
@@ -1158,6 +1201,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
       const int tbox = un.tt * 128 + q * 32;  // first row of this warp's boxes
       const int f0 = un.tf * BN;
       const bool row_ok = t < p.T;
+      float rinv = 1.0f;  // deferred RMSNorm of the input row (QKV, gate_up)
+      if constexpr (EPI == EPI_QKV || EPI == EPI_SILU) rinv = row_ok ? row_scale(p, t) : 0.0f;
       TokPos tp{0, 0, false};
       if constexpr (EPI == EPI_QKV) {
         if (row_ok) {
@@ -1173,9 +1218,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
         uint8_t* stg = sStg + (warp - 2) * (2 * 32 * 128);
         const bool ok = p.qkv.hd == 128
                             ? qkv_pair_tile<BN, 128>(p, TFULL(b), use, abort_flag, ta, t, tp, f0, row_ok, w, q, row,
-                                                     seg & 1, sNw, sSS, stg)
+                                                     seg & 1, sNw, sSS, stg, rinv)
                             : qkv_pair_tile<BN, 64>(p, TFULL(b), use, abort_flag, ta, t, tp, f0, row_ok, w, q, row,
-                                                    seg & 1, sNw, sSS, stg);
+                                                    seg & 1, sNw, sSS, stg, rinv);
         if (!ok) break;
         tc_fence_before();
         __syncwarp();
@@ -1189,9 +1234,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
         const uint32_t ta = lane_addr + static_cast<uint32_t>(b * BN);
         if constexpr (EPI == EPI_QKV) {
           if (BN >= 128 && p.qkv.hd == 128) {
-            qkv_stream<BN, (BN >= 128 ? 128 : 64)>(p, ta, t, tp, f0, row_ok, cbase, cbase + BNH);
+            qkv_stream<BN, (BN >= 128 ? 128 : 64)>(p, ta, t, tp, f0, row_ok, cbase, cbase + BNH, rinv);
           } else {
-            qkv_stream<BN, 64>(p, ta, t, tp, f0, row_ok, cbase, cbase + BNH);
+            qkv_stream<BN, 64>(p, ta, t, tp, f0, row_ok, cbase, cbase + BNH, rinv);
           }
         } else if constexpr (EPI == EPI_SILU) {
           // gate/up interleaved in 64-column blocks: 128 accumulator columns = 64 outputs
@@ -1204,7 +1249,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
               tc_ld32(ta + qb * 128 + h * 32, gv);
               tc_ld32(ta + qb * 128 + 64 + h * 32, uv);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[h * 32 + i] = silu_f(gv[i]) * uv[i];
+              for (int i = 0; i < 32; ++i) o[h * 32 + i] = silu_f(gv[i] * rinv) * (uv[i] * rinv);
             }
             box_acquire(lane);
             stage_f16x64(box, lane, o);
@@ -1307,6 +1352,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
           // the counter is cleared after every thread of this CTA has passed the
           // second barrier above (it is read once per tile, by thread 64)
           if (threadIdx.x == 64) p.counters[tile] = 0;
+        }
+        if constexpr (EPI == EPI_QKV || EPI == EPI_SILU) {
+#pragma unroll
+          for (int c = 0; c < BNH; ++c) acc[c] *= rinv;
         }
         if constexpr (C::TMA_OUT) {  // whole warp (rows past the last token are clipped by the TMA unit)
           if constexpr (EPI == EPI_SILU) {
@@ -1580,6 +1629,12 @@ cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partia
     gp.discard[k] = pr.discard[k];
     gp.discard_lines[k] = pr.discard[k] ? pr.discard_lines[k] : 0;
   }
+  gp.row_ss = pr.row_ss;
+  gp.row_groups = pr.row_groups;
+  gp.row_inv_k = pr.row_ss ? 1.0f / static_cast<float>(pr.k_seg) : 0.0f;
+  gp.row_eps = pr.row_eps;
+  if (pr.row_ss && (pr.n_seg != 1 || pr.row_groups * 32 != pr.k_seg || (pr.epi != EPI_QKV && pr.epi != EPI_SILU)))
+    return cudaErrorInvalidValue;
   gp.status = status;
   const int g = pl.grid;
 #define TP_V(BN_, EPI_, ACC_, SW_)                                                           \

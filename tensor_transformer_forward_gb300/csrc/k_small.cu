@@ -216,6 +216,48 @@ static cudaError_t rmsnorm_rows(const void* x, int64_t rows, int H, const void* 
   return launch_pdl(rmsnorm_wide_kernel, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
 }
 
+// Row statistics for a deferred RMSNorm (the norm itself happens in the next
+// GEMM's epilogue, its weight folded into that GEMM's weights): fp16 copy of
+// each fp32 residual row and the sum of squares of each 32-column group.  One
+// warp per row; lane l takes 8-column chunks l, l + 32, ...; the 4 lanes of a
+// 32-column group add their sums with two shuffles.
+__global__ void row_stats_kernel(const float4* __restrict__ x, int64_t rows, int H, uint4* __restrict__ xh,
+                                 float* __restrict__ ss) {
+  griddep_wait();
+  griddep_launch();
+  const int warps = blockDim.x / 32;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * warps + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;  // warp-uniform
+  const int chunks = H / 8, groups = H / 32;
+  const float4* xr = x + row * (H / 4);
+  for (int c0 = 0; c0 < chunks; c0 += 32) {  // same trip count on every lane
+    const int c = c0 + lane;
+    float s = 0.0f;
+    if (c < chunks) {
+      const float4 a = xr[2 * c], b = xr[2 * c + 1];
+      s = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
+      uint4 o;
+      o.x = pack_f16x2(a.x, a.y);
+      o.y = pack_f16x2(a.z, a.w);
+      o.z = pack_f16x2(b.x, b.y);
+      o.w = pack_f16x2(b.z, b.w);
+      xh[row * chunks + c] = o;
+    }
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    if ((lane & 3) == 0 && c < chunks) ss[row * groups + c / 4] = s;
+  }
+}
+
+cudaError_t launch_row_stats(const void* x, int64_t rows, int H, void* xh, float* ss, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (H % 32) return cudaErrorInvalidValue;
+  const int warps = 4;
+  return launch_pdl(row_stats_kernel, dim3(static_cast<unsigned>((rows + warps - 1) / warps)), dim3(32 * warps), 0,
+                    s, reinterpret_cast<const float4*>(x), rows, H, reinterpret_cast<uint4*>(xh), ss);
+}
+
 cudaError_t launch_rmsnorm(const void* x, int64_t rows, int H, const void* w, float eps, void* out, cudaStream_t s) {
   return rmsnorm_rows(x, rows, H, w, eps, out, nullptr, s);
 }
@@ -238,6 +280,30 @@ __global__ void bf16_to_f16_kernel(uint32_t* __restrict__ w, size_t n_pairs) {
     const uint32_t v = w[i];
     w[i] = pack_f16x2(bf16lo(v), bf16hi(v));
   }
+}
+
+// W[r][c] * norm[c] -> fp16, in place ([rows][cols] bf16 in, fp16 out): an
+// RMSNorm weight folded into the projection that reads the normed rows
+// (xn W^T = (x * inv) (W * diag(w))^T).  The bf16 x bf16 product is exact in
+// fp32, so the only rounding is the one to fp16.
+__global__ void fold_norm_f16_kernel(uint32_t* __restrict__ w, size_t n_pairs, int cols,
+                                     const __nv_bfloat16* __restrict__ norm) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n_pairs;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint32_t v = w[i];
+    const int c = static_cast<int>((2 * i) % static_cast<size_t>(cols));  // cols is even
+    w[i] = pack_f16x2(bf16lo(v) * bf2f(norm[c]), bf16hi(v) * bf2f(norm[c + 1]));
+  }
+}
+
+cudaError_t launch_fold_norm_f16(void* w, size_t rows, int cols, const void* norm, cudaStream_t s) {
+  const size_t pairs = rows * static_cast<size_t>(cols) / 2;
+  if (pairs == 0) return cudaSuccess;
+  if (cols % 2) return cudaErrorInvalidValue;
+  const size_t blocks = (pairs + 255) / 256;
+  fold_norm_f16_kernel<<<static_cast<unsigned>(blocks < 65536 ? blocks : 65536), 256, 0, s>>>(
+      reinterpret_cast<uint32_t*>(w), pairs, cols, reinterpret_cast<const __nv_bfloat16*>(norm));
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bf16_to_f16(void* w, size_t elems, cudaStream_t s) {

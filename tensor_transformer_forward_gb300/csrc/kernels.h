@@ -90,6 +90,12 @@ struct GemmProblem {
   // write-back by the epilogue warps at the start (128-byte aligned, whole lines)
   const void* discard[2];
   int64_t discard_lines[2];
+  // deferred RMSNorm of the input rows (QKV, gate_up): X holds the raw residual
+  // rows (fp16), the norm weight is folded into W, and the epilogue scales row t
+  // by rsqrt(sum(row_ss[t][0 .. row_groups)) / K + eps); null: no scaling
+  const float* row_ss;  // [T][row_groups] sums of squares of 32-column groups
+  int row_groups;
+  float row_eps;
 };
 
 struct GemmPlan {
@@ -120,6 +126,9 @@ int gemm_num_tiles_f(const GemmProblem& pr, const GemmPlan& plan);
 cudaError_t launch_embed(const int32_t* ids, int T, const void* embed_stacked, int n, int64_t v_local,
                          int64_t vocab, int H, void* out, int* status, cudaStream_t s);
 cudaError_t launch_rmsnorm(const void* x, int64_t rows, int H, const void* w, float eps, void* out, cudaStream_t s);
+// Row statistics for a deferred RMSNorm: fp16 copy of x [rows][H] and the sums of
+// squares of each 32-column group, ss [rows][H / 32].
+cudaError_t launch_row_stats(const void* x, int64_t rows, int H, void* xh, float* ss, cudaStream_t s);
 
 
 struct AttnArgs {
@@ -153,5 +162,6 @@ cudaError_t launch_wait_probe(const int* flag, int* status, long long limit_ns, 
 cudaError_t launch_decode_advance(int32_t* ctx_len, int B, const int32_t* ids, int32_t* history, int max_rows,
                                   int32_t* step, int32_t* status, cudaStream_t s);
 cudaError_t launch_bf16_to_f16(void* w, size_t elems, cudaStream_t s);
+cudaError_t launch_fold_norm_f16(void* w, size_t rows, int cols, const void* norm, cudaStream_t s);
 
 }  // namespace tpk
