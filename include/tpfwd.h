@@ -158,9 +158,10 @@ tp_status tp_workspace_init(tp_ctx* ctx, void* ws, size_t ws_bytes, int32_t max_
  * debugging; valid until the next call, and only while tp_keep_intermediates(ctx, 1) is set:
  * by default the calls drop each intermediate from L2 without writing it back once its last
  * reader has run, so that dead data costs no HBM write traffic): byte offset and size of
- *  TP_WS_NORMED  fp16 [T, H]                  the residual rows the post-attention norm reads (after
- *                                              the call; the norm is deferred into gate_up, whose
- *                                              epilogue scales row t by rsqrt(mean(x_t^2) + eps))
+ *  TP_WS_NORMED  fp16 [T, H]                  the layer's output rows (the residual stream in fp16),
+ *                                              which the next layer's deferred input norm reads (the
+ *                                              norms are deferred into the next projection's epilogue,
+ *                                              which scales row t by rsqrt(mean(x_t^2) + eps))
  *  TP_WS_QKV     [T, n, (nq_l+2nkv_l) hd]     merged projection; its q heads hold post-RoPE q
  *                                              as bf16 (k and v go straight to the cache)
  *  TP_WS_ATTN    fp16 [T, n * nq_l * hd]      attention output (o_proj input)
@@ -170,6 +171,14 @@ tp_status tp_workspace_init(tp_ctx* ctx, void* ws, size_t ws_bytes, int32_t max_
 #define TP_WS_ATTN 2
 #define TP_WS_ACT 3
 tp_status tp_workspace_part(const tp_ctx* ctx, int32_t part, size_t* offset, size_t* bytes);
+/* The deferred RMSNorms read an fp16 copy of the residual rows and their 32-column sums of
+ * squares, which tp_embed_vocab_parallel and each tp_decoder_layer_forward leave in the
+ * workspace for the hidden buffer they wrote; the next layer call on the same buffer and
+ * token count reuses them, any other buffer gets them recomputed.  A caller that writes
+ * hidden itself between two such calls tells the context with this (the pages have no
+ * counterpart: the norms there are separate passes). */
+tp_status tp_hidden_written(tp_ctx* ctx);
+
 /* keep != 0: leave the intermediates above readable after each call (no L2 discards).
  * The pages have no counterpart; this is a debugging switch. */
 tp_status tp_keep_intermediates(tp_ctx* ctx, int32_t keep);

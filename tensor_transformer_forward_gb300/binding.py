@@ -94,6 +94,7 @@ def _load() -> ctypes.CDLL:
         "tp_workspace_part": ([P, I32, pSZ, pSZ], I32),
         "tp_keep_intermediates": ([P, I32], I32),
         "tp_decode_advance": ([P, P, P, P, I32, P, P, P], I32),
+        "tp_hidden_written": ([P], I32),
         "tp_launch_count": ([P, pI64], I32),
         "tp_profile_begin": ([P, ctypes.c_uint32, I32], I32),
         "tp_profile_end": ([P, ctypes.POINTER(F32), pI32], I32),
@@ -112,7 +113,7 @@ EXPORTED = ("tp_create", "tp_destroy", "tp_status_string", "tp_last_cuda_error",
             "tp_workspace_init", "tp_embed_vocab_parallel", "tp_decoder_layer_forward", "tp_lm_head_argmax",
             "tp_read_status", "tp_rank_sum_count", "tp_debug_wait_probe", "tp_workspace_part", "tp_launch_count",
             "tp_profile_begin", "tp_profile_end", "tp_lm_head_argmax_static", "tp_keep_intermediates",
-            "tp_decode_advance")
+            "tp_decode_advance", "tp_hidden_written")
 KERNELS = ("embed", "rmsnorm", "gemm_qkv", "rope", "attn_prefill", "attn_decode", "gemm_o", "gemm_gate_up",
            "gemm_down", "final_norm", "gemm_lm_head", "argmax", "decode_advance")
 
@@ -251,6 +252,11 @@ class Context:
                                       max_positions, _stream()), "tp_workspace_init")
         self.workspace = ws
         return ws
+
+    def hidden_written(self) -> None:
+        """The caller wrote the residual stream itself: the next layer call recomputes
+        the deferred norm's inputs (see tp_hidden_written)."""
+        _check(_lib.tp_hidden_written(self.handle), "tp_hidden_written")
 
     def keep_intermediates(self, keep: bool = True) -> None:
         """Leave the layer's intermediates readable after each call (debugging)."""

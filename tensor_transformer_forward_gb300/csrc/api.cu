@@ -60,6 +60,10 @@ struct tp_ctx {
   int ws_tokens = 0, ws_seqs = 0, ws_pos = 0;
   Region r_rope, r_xn, r_qkv, r_qlo, r_attn, r_act, r_gpart, r_gcnt, r_apart, r_acnt, r_amax_v, r_amax_i, r_z, r_ss;
   bool keep_intermediates = false;  // leave dead intermediates in L2 (to read them after a call)
+  // the workspace's fp16 residual rows and row sums of squares (the deferred
+  // RMSNorm's inputs) belong to this hidden buffer with this many rows, or to none
+  const void* stats_for = nullptr;
+  int stats_T = -1;
   int lm_tiles_max = 0;
   int num_sms = 0;
   int64_t rank_sums = 0;
@@ -533,12 +537,21 @@ tp_status tp_embed_vocab_parallel(tp_ctx* x, const void* head_shards, const int3
                                   void* hidden_out, int32_t* dev_status, void* stream) {
   if (!x || !head_shards || !ids || !hidden_out || !dev_status || T <= 0) return TP_ERR_INVALID_ARG;
   cudaError_t e;
+  // with a workspace large enough, also the first layer's deferred-norm inputs
+  const bool stats = x->ws != nullptr && T <= x->ws_tokens;
+  x->stats_for = nullptr;
   {
     Timed tm(x, TP_K_EMBED, static_cast<cudaStream_t>(stream));
     e = tpk::launch_embed(ids, T, static_cast<const char*>(head_shards) + x->embed.off, x->n, x->v_l, x->c.vocab,
-                          x->H, hidden_out, dev_status, static_cast<cudaStream_t>(stream));
+                          x->H, hidden_out, stats ? x->ws + x->r_xn.off : nullptr,
+                          stats ? reinterpret_cast<float*>(x->ws + x->r_ss.off) : nullptr, dev_status,
+                          static_cast<cudaStream_t>(stream));
   }
   if (e != cudaSuccess) return cuda_fail(e);
+  if (stats) {
+    x->stats_for = hidden_out;
+    x->stats_T = T;
+  }
   x->rank_sums += 1;
   return TP_OK;
 }
@@ -562,14 +575,18 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
 
   float* ss = reinterpret_cast<float*>(x->ws + x->r_ss.off);
 
-  // A3: input RMSNorm, deferred: the fp16 residual rows and their sums of squares
-  // here; w_in is folded into the QKV weights and each row's rsqrt(mean + eps)
-  // scales its accumulators in the QKV epilogue
-  {
+  // A3: input RMSNorm, deferred: w_in is folded into the QKV weights and each row's
+  // rsqrt(mean + eps) scales its accumulators in the QKV epilogue.  Its inputs (the
+  // fp16 residual rows and their 32-column sums of squares) are left in the
+  // workspace by the embedding or the previous layer's down_proj epilogue; computed
+  // here only when hidden came from elsewhere.
+  const bool have_stats = x->stats_for == hidden && x->stats_T == T;
+  x->stats_for = nullptr;  // until this call completes
+  if (!have_stats) {
     Timed tm(x, TP_K_RMSNORM, s);
     e = tpk::launch_row_stats(hidden, T, H, xn, ss, s);
+    if (e != cudaSuccess) return cuda_fail(e);
   }
-  if (e != cudaSuccess) return cuda_fail(e);
 
   // A4 + A5: merged QKV of all ranks (column split: no exchange), with q/k RMSNorm,
   // RoPE and the K/V cache write fused into the epilogue (fp32, no intermediate rounding)
@@ -624,6 +641,8 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   g.w = w + x->o.off; g.w_rows = static_cast<int64_t>(n) * H; g.w_cols = x->k_r; g.w_ld = x->k_r;
   g.T = T; g.N = H; g.n_seg = n; g.k_seg = x->k_r; g.x_k_seg = x->k_r; g.w_row_seg = H;
   g.epi = tpk::EPI_RESID; g.out = hidden; g.ldo = H; g.out_cols = H;
+  // A8 (post-attention RMSNorm, deferred into gate_up): its inputs from this epilogue
+  g.row_out16 = xn; g.row_ss_out = ss;
   // dead by now: q (high part / decode q) and its low part, read by the attention
   set_discard(x, g, 0, qkv, static_cast<size_t>(T) * n * x->w_rank * 2);
   set_discard(x, g, 1, x->ws + x->r_qlo.off, static_cast<size_t>(T) * n * x->nq_l * x->hd * 2);
@@ -631,12 +650,8 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   if (st != TP_OK) return st;
   x->rank_sums += 1;
 
-  // A8: post-attention RMSNorm, deferred as A3 (w_post folded into gate_up)
-  {
-    Timed tm(x, TP_K_RMSNORM, s);
-    e = tpk::launch_row_stats(hidden, T, H, xn, ss, s);
-  }
-  if (e != cudaSuccess) return cuda_fail(e);
+  // A8: post-attention RMSNorm, deferred as A3 (w_post folded into gate_up; its
+  // inputs came from the o_proj epilogue)
 
   // A9: merged gate/up of all ranks (column split) with SiLU(gate) * up
   g = tpk::GemmProblem{};
@@ -656,11 +671,13 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   g.w = w + x->down.off; g.w_rows = static_cast<int64_t>(n) * H; g.w_cols = x->i_p; g.w_ld = x->i_p;
   g.T = T; g.N = H; g.n_seg = n; g.k_seg = x->i_p; g.x_k_seg = x->i_p; g.w_row_seg = H;
   g.epi = tpk::EPI_RESID; g.out = hidden; g.ldo = H; g.out_cols = H;
-  // dead by now: the post-attention RMSNorm rows, read by gate_up
-  set_discard(x, g, 0, xn, static_cast<size_t>(T) * H * 2);
+  // the next layer's deferred input norm: its inputs from this epilogue
+  g.row_out16 = xn; g.row_ss_out = ss;
   st = gemm(x, TP_K_GEMM_DOWN, g, dev_status, s);
   if (st != TP_OK) return st;
   x->rank_sums += 1;
+  x->stats_for = hidden;
+  x->stats_T = T;
   return TP_OK;
 }
 
@@ -690,7 +707,13 @@ tp_status tp_lm_head_argmax(tp_ctx* x, const void* head_shards, const tp_batch* 
   g.amax_idx = reinterpret_cast<int*>(x->ws + x->r_amax_i.off);
   g.amax_ld = B; g.logits = out_logits; g.ld_logits = x->c.vocab; g.vocab = x->c.vocab; g.out_ids = out_ids;
   // dead by now: the last layer's SiLU*up rows (the weights stream next, through L2)
+  // and the fp16 rows its down_proj left for a next layer (a later layer call on
+  // this hidden recomputes them)
   set_discard(x, g, 0, x->ws + x->r_act.off, static_cast<size_t>(b->num_tokens) * x->n * x->i_p * 2);
+  if (!x->keep_intermediates) {
+    set_discard(x, g, 1, x->ws + x->r_xn.off, static_cast<size_t>(b->num_tokens) * H * 2);
+    x->stats_for = nullptr;
+  }
   tpk::GemmPlan pl = tpk::plan_gemm(g, x->num_sms);
   if (pl.tiles_f > x->lm_tiles_max || pl.splits != 1 || (pl.swap && pl.grid > x->lm_tiles_max)) return TP_ERR_UNSUPPORTED;
   {
@@ -724,6 +747,12 @@ tp_status tp_decode_advance(tp_ctx* x, const tp_batch* b, const int32_t* ids, in
                                    dev_status, s);
   }
   if (e != cudaSuccess) return cuda_fail(e);
+  return TP_OK;
+}
+
+tp_status tp_hidden_written(tp_ctx* x) {
+  if (!x) return TP_ERR_INVALID_ARG;
+  x->stats_for = nullptr;
   return TP_OK;
 }
 

@@ -62,6 +62,11 @@ struct GemmParams {
   const float* row_ss;  // deferred RMSNorm: per-row 32-column sums of squares, or null
   int row_groups;
   float row_inv_k, row_eps;
+  // residual epilogues: also leave the next norm's inputs (fp16 rows through tmO2,
+  // 32-column sums of squares), reading the old residual instead of a reduce-add
+  float* row_ss_out;
+  int row_ss_out_groups;
+  __half* row_out16;  // the fp16 rows (weights-on-M path writes them directly; ld = out_cols)
 };
 
 template <int BN, int EPI = EPI_STORE, bool ACC = false, bool SWAP = false>
@@ -81,11 +86,15 @@ struct GemmCfg {
   // QKV with two warps per lane quarter (see QKV_PAIR below) keeps 3 stages: its
   // row staging takes the room of the fourth
   static constexpr bool QKV_PAIR = EPI == EPI_QKV && !SWAP && !ACC && EW == 8;
+  // token-tile residual epilogues also stage fp16 rows (one 32 x 32 box of 2 KB per
+  // epilogue warp next to its fp32 box)
+  static constexpr bool RESID_ROWS = !SWAP && EPI == EPI_RESID;
+  static constexpr int ROW16_BYTES = RESID_ROWS ? EW * 2048 : 0;
   static constexpr int STAGES =
       QKV_PAIR ? 3
-      : ((204800 - ((SWAP && EPI != EPI_ARGMAX) ? BN * 512 : 0)) / STAGE_BYTES) > 12
+      : ((204800 - ROW16_BYTES - ((SWAP && EPI != EPI_ARGMAX) ? BN * 512 : 0)) / STAGE_BYTES) > 12
           ? 12
-          : ((204800 - ((SWAP && EPI != EPI_ARGMAX) ? BN * 512 : 0)) / STAGE_BYTES);
+          : ((204800 - ROW16_BYTES - ((SWAP && EPI != EPI_ARGMAX) ? BN * 512 : 0)) / STAGE_BYTES);
   static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int QUEUE = 4;  // tile queue depth (weight-streaming argmax)
   // weight-streaming argmax: tiles from a dynamic queue; other swapped (few-token)
@@ -98,7 +107,7 @@ struct GemmCfg {
   // outputs leave through TMA stores (fp16) / TMA reduce-adds (fp32 residual) from one
   // 32-row x 128-byte staging box per epilogue warp
   static constexpr bool TMA_OUT = !SWAP && (EPI == EPI_STORE || EPI == EPI_SILU || EPI == EPI_RESID);
-  static constexpr int OUT_BYTES = TMA_OUT ? EW * 4096 : 0;
+  static constexpr int OUT_BYTES = (TMA_OUT ? EW * 4096 : 0) + ROW16_BYTES;
   // QKV with two warps per lane quarter: q/k norm weights [2][128] fp32, the
   // per-row partial sums of squares [2 parities][2 warps][BN/64 heads at most][128]
   // and each warp's row staging [2 outputs][32 rows][128 bytes at most]
@@ -210,6 +219,14 @@ __device__ __forceinline__ void stage_f16x64(uint8_t* box, int r, const float* v
     *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) = w;
   }
 }
+// One row of a 32-row x 64-byte fp16 box (tensor map without swizzle).
+__device__ __forceinline__ void stage_f16x32(uint8_t* box, int r, const float* v) {
+  uint4* rowp = reinterpret_cast<uint4*>(box + r * 64);
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    rowp[c] = make_uint4(pack_f16x2(v[8 * c], v[8 * c + 1]), pack_f16x2(v[8 * c + 2], v[8 * c + 3]),
+                         pack_f16x2(v[8 * c + 4], v[8 * c + 5]), pack_f16x2(v[8 * c + 6], v[8 * c + 7]));
+}
 // Whole warp: wait until the box's previous store has read it.
 __device__ __forceinline__ void box_acquire(int lane) {
   if (lane == 0) bulk_wait_read();
@@ -223,6 +240,42 @@ __device__ __forceinline__ void box_release(const CUtensorMap* map, uint8_t* box
   if (lane == 0) {
     if (reduce_add) tma_reduce_add_2d(map, smem_u32(box), x, y);
     else tma_store_2d(map, smem_u32(box), x, y);
+    bulk_commit();
+  }
+}
+
+// Residual epilogue with the next norm's inputs: v (32 columns of this row's
+// rank-summed tile, starting at column col) += the old residual; the new
+// residual leaves through the fp32 box (plain TMA store), its fp16 copy through
+// the fp16 box, and the group's sum of squares goes to row_ss_out.  Whole warp.
+template <typename Cfg>
+__device__ __forceinline__ void resid_rows32(const GemmParams& p, const CUtensorMap* tmO, const CUtensorMap* tmO2,
+                                             uint8_t* box, uint8_t* box16, int t, bool row_ok, int col, int tbox,
+                                             int lane, float* v) {
+  float s = 0.0f;
+  if (row_ok && col < p.out_cols) {  // out_cols % 32 == 0: a group is wholly inside or outside
+    const float4* x = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.out) +
+                                                      static_cast<size_t>(t) * p.ldo + col);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 o = x[i];
+      v[4 * i] += o.x;
+      v[4 * i + 1] += o.y;
+      v[4 * i + 2] += o.z;
+      v[4 * i + 3] += o.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) s += v[i] * v[i];
+    p.row_ss_out[static_cast<size_t>(t) * p.row_ss_out_groups + col / 32] = s;
+  }
+  box_acquire(lane);  // both boxes of this warp were handed to the TMA unit together
+  stage_f32x32(box, lane, v);
+  stage_f16x32(box16, lane, v);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmO, smem_u32(box), col, tbox);
+    tma_store_2d(tmO2, smem_u32(box16), col, tbox);
     bulk_commit();
   }
 }
@@ -818,9 +871,12 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
     const int nt = min(BN, p.T - un.tt * BN);
     if constexpr (EPI == EPI_RESID) {
       // residual rows: all of this warp's loads first, then the adds and stores
+      // (with row_ss_out: also the fp16 row and the 32-column sums of squares the
+      // next norm reads; lanes 8g .. 8g+7 hold the 32 features of group g)
       constexpr int TPW = BN / 4;
       const int f = f0 + 4 * lane;
-      if (f + 4 <= p.out_cols) {
+      const bool stats = p.row_ss_out != nullptr;
+      if (f0 + 128 <= p.out_cols) {  // uniform: the whole feature tile is inside
         float4 x[TPW];
 #pragma unroll
         for (int k = 0; k < TPW; ++k) {
@@ -831,17 +887,47 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
 #pragma unroll
         for (int k = 0; k < TPW; ++k) {
           const int t = wq + 4 * k;
-          if (t < nt) {
+          if (t < nt) {  // uniform over the warp
             const float4 v = *reinterpret_cast<const float4*>(sRow + t * 128 + 4 * lane);
             float4 y = x[k];
             y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
-            *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + static_cast<size_t>(un.tt * BN + t) * p.ldo +
-                                       f) = y;
+            const size_t tok = static_cast<size_t>(un.tt * BN + t);
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + tok * p.ldo + f) = y;
+            if (stats) {
+              *reinterpret_cast<uint2*>(p.row_out16 + tok * p.out_cols + f) =
+                  make_uint2(pack_f16x2(y.x, y.y), pack_f16x2(y.z, y.w));
+              float s = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+              s += __shfl_xor_sync(0xffffffffu, s, 1);
+              s += __shfl_xor_sync(0xffffffffu, s, 2);
+              s += __shfl_xor_sync(0xffffffffu, s, 4);
+              if ((lane & 7) == 0) p.row_ss_out[tok * p.row_ss_out_groups + f / 32] = s;
+            }
           }
         }
-      } else {
-        for (int t = wq; t < nt; t += 4)
-          swap_row<EPI>(p, un.tt * BN + t, f0, lane, *reinterpret_cast<const float4*>(sRow + t * 128 + 4 * lane));
+      } else {  // the last, partial feature tile
+        for (int t = wq; t < nt; t += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(sRow + t * 128 + 4 * lane);
+          const float vv[4] = {v.x, v.y, v.z, v.w};
+          const size_t tok = static_cast<size_t>(un.tt * BN + t);
+          float* o = reinterpret_cast<float*>(p.out) + tok * p.ldo;
+          float s = 0.0f;
+          for (int i = 0; i < 4; ++i) {
+            if (f + i < p.out_cols) {
+              const float y = o[f + i] + vv[i];
+              o[f + i] = y;
+              if (stats) {
+                p.row_out16[tok * p.out_cols + f + i] = __float2half_rn(sat_f16(y));
+                s += y * y;
+              }
+            }
+          }
+          if (stats) {  // uniform
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            s += __shfl_xor_sync(0xffffffffu, s, 4);
+            if ((lane & 7) == 0 && f < p.out_cols) p.row_ss_out[tok * p.row_ss_out_groups + f / 32] = s;
+          }
+        }
       }
     } else {
       for (int t = wq; t < nt; t += 4) {
@@ -873,14 +959,15 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
 template <int BN, int EPI, bool ACC, bool SWAP>
 __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                   const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2,
+                   const GemmParams p) {
   using C = GemmCfg<BN, EPI, ACC, SWAP>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * C::A_BYTES;
-  uint8_t* sOut = smem + STAGES * C::STAGE_BYTES;  // [EW][4096] output staging boxes
+  uint8_t* sOut = smem + STAGES * C::STAGE_BYTES;  // [EW][4096] output staging boxes, then [EW][2048] fp16 boxes
   float* sRow = reinterpret_cast<float*>(sOut + C::OUT_BYTES);  // [BN][128] token rows (swapped epilogues)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + C::OUT_BYTES + C::TROW_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
@@ -1186,6 +1273,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
     uint8_t* box = sOut + (warp - 2) * 4096;  // this warp's output staging box (TMA_OUT)
+    uint8_t* box16 = sOut + C::EW * 4096 + (warp - 2) * 2048;  // its fp16 row box (RESID_ROWS)
     if constexpr (C::QKV_PAIR) {
       const int e = threadIdx.x - 64;
       if (e < p.qkv.hd) {
@@ -1274,9 +1362,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
           for (int c = cbase / 32; c < (cbase + BNH) / 32; ++c) {
             float v[32];
             tc_ld32(ta + c * 32, v);
-            box_acquire(lane);
-            stage_f32x32(box, lane, v);
-            box_release(&tmO, box, f0 + c * 32, tbox, true, lane);
+            if (p.row_ss_out != nullptr) {  // uniform: read-add-store and the next norm's inputs
+              resid_rows32<C>(p, &tmO, &tmO2, box, box16, t, row_ok, f0 + c * 32, tbox, lane, v);
+            } else {
+              box_acquire(lane);
+              stage_f32x32(box, lane, v);
+              box_release(&tmO, box, f0 + c * 32, tbox, true, lane);
+            }
           }
         } else {
 #pragma unroll 1
@@ -1373,9 +1465,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
           } else if constexpr (EPI == EPI_RESID) {
 #pragma unroll
             for (int c = 0; c < BNH / 32; ++c) {
-              box_acquire(lane);
-              stage_f32x32(box, lane, acc + c * 32);
-              box_release(&tmO, box, f0 + cbase + c * 32, tbox, true, lane);
+              if (p.row_ss_out != nullptr) {  // uniform: read-add-store and the next norm's inputs
+                resid_rows32<C>(p, &tmO, &tmO2, box, box16, t, row_ok, f0 + cbase + c * 32, tbox, lane, acc + c * 32);
+              } else {
+                box_acquire(lane);
+                stage_f32x32(box, lane, acc + c * 32);
+                box_release(&tmO, box, f0 + cbase + c * 32, tbox, true, lane);
+              }
             }
           } else {
 #pragma unroll
@@ -1483,6 +1579,20 @@ static bool make_map_out(CUtensorMap* m, const void* base, int64_t rows, int64_t
          CUDA_SUCCESS;
 }
 
+// fp16 [rows][cols] row-major, box 32 columns (64 bytes) x 32 rows, no swizzle.
+static bool make_map_rows16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+  auto fn = encode_fn();
+  if (!fn || !base || rows <= 0 || cols <= 0) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (cols * 2) % 16) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+  cuuint32_t box[2] = {32u, 32u};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static inline int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
 GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
@@ -1582,13 +1692,17 @@ static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, 
     attr_done = true;
   }
   CUtensorMap mo = mx;  // unused unless the outputs leave through TMA
+  CUtensorMap mo2 = mx;  // fp16 residual rows of the residual epilogues (row_ss_out set)
   if constexpr (Cfg::TMA_OUT) {
     const bool ok = EPI == EPI_RESID
                         ? make_map_out(&mo, pr.out, pr.T, pr.out_cols, pr.ldo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4)
                         : make_map_out(&mo, pr.out, pr.T, pr.out_cols, pr.ldo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2);
     if (!ok) return cudaErrorInvalidValue;
   }
-  return launch_pdl(kern, dim3(grid), dim3(Cfg::THREADS), smem, s, mx, mw, mo, gp);
+  if constexpr (Cfg::RESID_ROWS) {
+    if (gp.row_ss_out && !make_map_rows16(&mo2, pr.row_out16, pr.T, pr.out_cols)) return cudaErrorInvalidValue;
+  }
+  return launch_pdl(kern, dim3(grid), dim3(Cfg::THREADS), smem, s, mx, mw, mo, mo2, gp);
 }
 
 cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partials, int* counters, int* status,
@@ -1629,6 +1743,10 @@ cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partia
     gp.discard[k] = pr.discard[k];
     gp.discard_lines[k] = pr.discard[k] ? pr.discard_lines[k] : 0;
   }
+  gp.row_ss_out = pr.row_ss_out;
+  gp.row_ss_out_groups = pr.out_cols / 32;
+  gp.row_out16 = static_cast<__half*>(pr.row_out16);
+  if (pr.row_ss_out && (pr.epi != EPI_RESID || !pr.row_out16 || pr.out_cols % 32 || pr.ldo % 4)) return cudaErrorInvalidValue;
   gp.row_ss = pr.row_ss;
   gp.row_groups = pr.row_groups;
   gp.row_inv_k = pr.row_ss ? 1.0f / static_cast<float>(pr.k_seg) : 0.0f;

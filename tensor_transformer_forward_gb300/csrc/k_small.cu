@@ -18,22 +18,28 @@ namespace tpk {
 // rank by rank in fixed order (exactly one term is non-zero, so the sum is
 // the table row, bit for bit).  Ids outside [0, V) give a zero row and raise
 // TP_DEVFLAG_BAD_TOKEN.
-// One CTA per token; each thread owns 8 consecutive hidden elements.
+// One CTA per token; each thread owns 8 consecutive hidden elements.  Also the
+// first layer's deferred-RMSNorm inputs: the row in fp16 (xh) and the sums of
+// squares of its 32-column groups (ss), or neither when xh is null.
 // ---------------------------------------------------------------------------
 __global__ void embed_vocab_parallel_kernel(const int32_t* __restrict__ ids, const uint4* __restrict__ table,
                                             int n, int64_t v_local, int64_t vocab, int H,
-                                            float4* __restrict__ out, int* status) {
+                                            float4* __restrict__ out, uint4* __restrict__ xh,
+                                            float* __restrict__ ss, int* status) {
   griddep_wait();  // the ids may come from the previous step's argmax
   griddep_launch();
   const int t = blockIdx.x;
   const int id = ids[t];
   if (threadIdx.x == 0 && (id < 0 || id >= vocab)) raise_flag(status, TP_DEVFLAG_BAD_TOKEN);
   const int chunks = H / 8;
-  for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+  const int trips = (chunks + blockDim.x - 1) / blockDim.x;  // the same on every lane (group shuffles)
+  for (int k = 0; k < trips; ++k) {
+    const int c = threadIdx.x + k * blockDim.x;
+    const bool live = c < chunks;
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int r = 0; r < n; ++r) {
+    for (int r = 0; r < n && live; ++r) {
       const int64_t start = r * v_local;
       const int64_t end = min(start + v_local, vocab);
       if (id >= start && id < end) {  // this rank's slice holds the id
@@ -44,19 +50,38 @@ __global__ void embed_vocab_parallel_kernel(const int32_t* __restrict__ ids, con
         acc[6] += bf16lo(w.w); acc[7] += bf16hi(w.w);
       }
     }
-    out[(static_cast<int64_t>(t) * chunks + c) * 2] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    out[(static_cast<int64_t>(t) * chunks + c) * 2 + 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (live) {
+      out[(static_cast<int64_t>(t) * chunks + c) * 2] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      out[(static_cast<int64_t>(t) * chunks + c) * 2 + 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    if (xh != nullptr) {  // uniform
+      float s = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s += acc[i] * acc[i];
+      s += __shfl_xor_sync(0xffffffffu, s, 1);  // the 4 chunks of a 32-column group
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      if (live) {
+        uint4 o;
+        o.x = pack_f16x2(acc[0], acc[1]);
+        o.y = pack_f16x2(acc[2], acc[3]);
+        o.z = pack_f16x2(acc[4], acc[5]);
+        o.w = pack_f16x2(acc[6], acc[7]);
+        xh[static_cast<int64_t>(t) * chunks + c] = o;
+        if ((c & 3) == 0) ss[static_cast<int64_t>(t) * (H / 32) + c / 4] = s;
+      }
+    }
   }
 }
 
 cudaError_t launch_embed(const int32_t* ids, int T, const void* embed_stacked, int n, int64_t v_local,
-                         int64_t vocab, int H, void* out, int* status, cudaStream_t s) {
+                         int64_t vocab, int H, void* out, void* xh, float* ss, int* status, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
+  if (H % 32) return cudaErrorInvalidValue;
   // enough threads that a row takes one or two chunks per thread (the loads overlap)
   const int threads = H / 8 < 512 ? 32 * ((H / 8 + 31) / 32) : 512;
   return launch_pdl(embed_vocab_parallel_kernel, dim3(T), dim3(threads), 0, s, ids,
                     reinterpret_cast<const uint4*>(embed_stacked), n, v_local, vocab, H, reinterpret_cast<float4*>(out),
-                    status);
+                    reinterpret_cast<uint4*>(xh), ss, status);
 }
 
 // ---------------------------------------------------------------------------

@@ -96,6 +96,11 @@ struct GemmProblem {
   const float* row_ss;  // [T][row_groups] sums of squares of 32-column groups
   int row_groups;
   float row_eps;
+  // residual epilogue (EPI_RESID) that also leaves the next deferred norm's inputs:
+  // the new residual rows in fp16 (row_out16, [T][out_cols]) and their 32-column
+  // sums of squares (row_ss_out, [T][out_cols / 32]); null: plain reduce-add
+  void* row_out16;
+  float* row_ss_out;
 };
 
 struct GemmPlan {
@@ -124,7 +129,7 @@ int gemm_num_tiles_f(const GemmProblem& pr, const GemmPlan& plan);
 
 // ---------------- small kernels ----------------
 cudaError_t launch_embed(const int32_t* ids, int T, const void* embed_stacked, int n, int64_t v_local,
-                         int64_t vocab, int H, void* out, int* status, cudaStream_t s);
+                         int64_t vocab, int H, void* out, void* xh, float* ss, int* status, cudaStream_t s);
 cudaError_t launch_rmsnorm(const void* x, int64_t rows, int H, const void* w, float eps, void* out, cudaStream_t s);
 // Row statistics for a deferred RMSNorm: fp16 copy of x [rows][H] and the sums of
 // squares of each 32-column group, ss [rows][H / 32].

@@ -88,6 +88,8 @@ class TPRunner:
             self.embed(ids, hidden)
         elif ids is not None:
             self.embed(ids, hidden)
+        else:
+            self.ctx.hidden_written()  # rows from the caller: the first layer derives its norm inputs
         for li in range(self.num_layers if layers is None else layers):
             self.layer(li, batch, hidden)
         if run_head:
