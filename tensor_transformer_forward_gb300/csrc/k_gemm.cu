@@ -89,7 +89,10 @@ struct GemmCfg {
   // token-tile residual epilogues also stage fp16 rows (one 32 x 32 box of 2 KB per
   // epilogue warp next to its fp32 box)
   static constexpr bool RESID_ROWS = !SWAP && EPI == EPI_RESID;
-  static constexpr int ROW16_BYTES = RESID_ROWS ? EW * 2048 : 0;
+  // ... and prefetch the old residual of their first NXB 32-column chunks into
+  // extra fp32 boxes while the MMA runs (one box per chunk)
+  static constexpr int NXB = RESID_ROWS ? ((BN / (EW / 4)) / 32 < 2 ? (BN / (EW / 4)) / 32 : 2) : 1;
+  static constexpr int ROW16_BYTES = RESID_ROWS ? EW * (2048 + (NXB - 1) * 4096) : 0;
   static constexpr int STAGES =
       QKV_PAIR ? 3
       : ((204800 - ROW16_BYTES - ((SWAP && EPI != EPI_ARGMAX) ? BN * 512 : 0)) / STAGE_BYTES) > 12
@@ -244,21 +247,43 @@ __device__ __forceinline__ void box_release(const CUtensorMap* map, uint8_t* box
   }
 }
 
+// Per-thread asynchronous copies (cp.async, 16 bytes each) and their waits.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// The old residual of this row's 32 columns from col, copied asynchronously into
+// row `lane` of an fp32 staging box (in the swizzled layout stage_f32x32 writes).
+__device__ __forceinline__ void prefetch_rows32(const GemmParams& p, uint8_t* xbox, int t, bool row_ok, int col,
+                                                int lane) {
+  if (row_ok && col < p.out_cols) {
+    const float* src = reinterpret_cast<const float*>(p.out) + static_cast<size_t>(t) * p.ldo + col;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) cp_async16(smem_u32(xbox + lane * 128 + ((c ^ (lane & 7)) << 4)), src + 4 * c);
+  }
+  cp_async_commit();
+}
+
 // Residual epilogue with the next norm's inputs: v (32 columns of this row's
 // rank-summed tile, starting at column col) += the old residual; the new
 // residual leaves through the fp32 box (plain TMA store), its fp16 copy through
 // the fp16 box, and the group's sum of squares goes to row_ss_out.  Whole warp.
+// With prefetched (box already holds the old residual, copied by prefetch_rows32
+// and waited for) the old values come from the box, else from global memory.
 template <typename Cfg>
 __device__ __forceinline__ void resid_rows32(const GemmParams& p, const CUtensorMap* tmO, const CUtensorMap* tmO2,
                                              uint8_t* box, uint8_t* box16, int t, bool row_ok, int col, int tbox,
-                                             int lane, float* v) {
+                                             int lane, float* v, bool prefetched) {
   float s = 0.0f;
   if (row_ok && col < p.out_cols) {  // out_cols % 32 == 0: a group is wholly inside or outside
     const float4* x = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.out) +
                                                       static_cast<size_t>(t) * p.ldo + col);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float4 o = x[i];
+      const float4 o = prefetched ? *reinterpret_cast<const float4*>(box + lane * 128 + ((i ^ (lane & 7)) << 4))
+                                  : x[i];
       v[4 * i] += o.x;
       v[4 * i + 1] += o.y;
       v[4 * i + 2] += o.z;
@@ -268,7 +293,7 @@ __device__ __forceinline__ void resid_rows32(const GemmParams& p, const CUtensor
     for (int i = 0; i < 32; ++i) s += v[i] * v[i];
     p.row_ss_out[static_cast<size_t>(t) * p.row_ss_out_groups + col / 32] = s;
   }
-  box_acquire(lane);  // both boxes of this warp were handed to the TMA unit together
+  box_acquire(lane);  // the fp16 box (and a reused fp32 box) of the previous chunk has been read
   stage_f32x32(box, lane, v);
   stage_f16x32(box16, lane, v);
   fence_proxy_async_smem();
@@ -1272,8 +1297,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
     const int cbase = ((warp - 2) >> 2) * BNH;
     const int row = q * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    uint8_t* box = sOut + (warp - 2) * 4096;  // this warp's output staging box (TMA_OUT)
-    uint8_t* box16 = sOut + C::EW * 4096 + (warp - 2) * 2048;  // its fp16 row box (RESID_ROWS)
+    // this warp's output staging box (TMA_OUT); with RESID_ROWS its NXB fp32 boxes
+    // (the first is `box`) and then its fp16 row box
+    uint8_t* box = sOut + (warp - 2) * (C::RESID_ROWS ? C::NXB * 4096 + 2048 : 4096);
+    uint8_t* box16 = box + C::NXB * 4096;
     if constexpr (C::QKV_PAIR) {
       const int e = threadIdx.x - 64;
       if (e < p.qkv.hd) {
@@ -1291,6 +1318,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
       const bool row_ok = t < p.T;
       float rinv = 1.0f;  // deferred RMSNorm of the input row (QKV, gate_up)
       if constexpr (EPI == EPI_QKV || EPI == EPI_SILU) rinv = row_ok ? row_scale(p, t) : 0.0f;
+      if constexpr (C::RESID_ROWS) {  // old residual of the first chunks, copied while the MMA runs
+        if (p.row_ss_out != nullptr) {
+          cp_async_wait_all();  // copies of a unit this CTA did not finish (a non-last split)
+          box_acquire(lane);    // the boxes' previous stores have read them
+#pragma unroll
+          for (int k = 0; k < C::NXB; ++k) prefetch_rows32(p, box + k * 4096, t, row_ok, f0 + cbase + 32 * k, lane);
+        }
+      }
       TokPos tp{0, 0, false};
       if constexpr (EPI == EPI_QKV) {
         if (row_ok) {
@@ -1363,7 +1398,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
             float v[32];
             tc_ld32(ta + c * 32, v);
             if (p.row_ss_out != nullptr) {  // uniform: read-add-store and the next norm's inputs
-              resid_rows32<C>(p, &tmO, &tmO2, box, box16, t, row_ok, f0 + c * 32, tbox, lane, v);
+              const int k = c - cbase / 32;
+              if (k == 0) cp_async_wait_all();
+              resid_rows32<C>(p, &tmO, &tmO2, k < C::NXB ? box + k * 4096 : box, box16, t, row_ok, f0 + c * 32,
+                              tbox, lane, v, k < C::NXB);
             } else {
               box_acquire(lane);
               stage_f32x32(box, lane, v);
@@ -1466,7 +1504,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
 #pragma unroll
             for (int c = 0; c < BNH / 32; ++c) {
               if (p.row_ss_out != nullptr) {  // uniform: read-add-store and the next norm's inputs
-                resid_rows32<C>(p, &tmO, &tmO2, box, box16, t, row_ok, f0 + cbase + c * 32, tbox, lane, acc + c * 32);
+                if (c == 0) cp_async_wait_all();
+                resid_rows32<C>(p, &tmO, &tmO2, c < C::NXB ? box + c * 4096 : box, box16, t, row_ok,
+                                f0 + cbase + c * 32, tbox, lane, acc + c * 32, c < C::NXB);
               } else {
                 box_acquire(lane);
                 stage_f32x32(box, lane, acc + c * 32);
@@ -1510,6 +1550,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
         }
       }
     }
+    if constexpr (C::RESID_ROWS) cp_async_wait_all();  // no copy into the staging outlives the CTA
     if constexpr (C::TMA_OUT) {  // every store has landed before the CTA (and its staging) goes away
       if (lane == 0) bulk_wait_all();
       __syncwarp();
