@@ -473,7 +473,10 @@ tp_status tp_shard_weights(tp_ctx* x, const tp_layer_full* L, const tp_head_full
   }
   TP_CUDA(cudaMemcpyAsync(d + x->final_norm.off, Hd->final_norm, row, cudaMemcpyDeviceToDevice, s));
   {
-    cudaError_t e = tpk::launch_bf16_to_f16(d + x->lm_head.off, x->lm_head.bytes / 2, s);
+    // the LM head's fp16 copy carries the final RMSNorm weight in its columns (the
+    // norm's row scale is applied to the logits, or dropped for the argmax alone)
+    cudaError_t e = tpk::launch_fold_norm_f16(d + x->lm_head.off, static_cast<size_t>(n) * x->v_l, x->H,
+                                              d + x->final_norm.off, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return TP_OK;
@@ -693,13 +696,23 @@ tp_status tp_lm_head_argmax(tp_ctx* x, const void* head_shards, const tp_batch* 
   const int B = b->num_seqs, H = x->H;
   void* z = x->ws + x->r_z.off;
   cudaError_t e;
-  {
+  // A11.  The final norm's weight is folded into the LM head copy, and its row scale
+  // rsqrt(mean(x^2) + eps) > 0 does not move the argmax: when only the ids are asked
+  // for and the last tokens' fp16 rows (left by the last down_proj) are contiguous
+  // (one sequence, or one token per sequence), the head reads them directly;
+  // otherwise the select kernel gathers and normalizes the rows (ones for weight).
+  const bool contiguous = B == 1 || (b->num_prefill == 0 && b->num_tokens == B);
+  const bool direct = out_logits == nullptr && contiguous && x->stats_for == hidden && x->stats_T == b->num_tokens;
+  const void* zin = z;
+  if (direct) {
+    zin = x->ws + x->r_xn.off + static_cast<size_t>(B == 1 ? b->num_tokens - 1 : 0) * H * 2;
+  } else {
     Timed tm(x, TP_K_FINAL_NORM, s);
-    e = tpk::launch_final_norm_select(hidden, H, b->cu_q, B, w + x->final_norm.off, x->c.rms_eps, z, s);
+    e = tpk::launch_final_norm_select(hidden, H, b->cu_q, B, nullptr, x->c.rms_eps, z, s);
+    if (e != cudaSuccess) return cuda_fail(e);
   }
-  if (e != cudaSuccess) return cuda_fail(e);
   tpk::GemmProblem g{};
-  g.x = z; g.x_rows = B; g.x_cols = H; g.x_ld = H;
+  g.x = zin; g.x_rows = B; g.x_cols = H; g.x_ld = H;
   g.w = w + x->lm_head.off; g.w_rows = static_cast<int64_t>(x->n) * x->v_l; g.w_cols = H; g.w_ld = H;
   g.T = B; g.N = static_cast<int>(static_cast<int64_t>(x->n) * x->v_l); g.n_seg = 1; g.k_seg = H;
   g.epi = tpk::EPI_ARGMAX; g.out = nullptr; g.ldo = 8; g.out_cols = 0;
@@ -707,10 +720,10 @@ tp_status tp_lm_head_argmax(tp_ctx* x, const void* head_shards, const tp_batch* 
   g.amax_idx = reinterpret_cast<int*>(x->ws + x->r_amax_i.off);
   g.amax_ld = B; g.logits = out_logits; g.ld_logits = x->c.vocab; g.vocab = x->c.vocab; g.out_ids = out_ids;
   // dead by now: the last layer's SiLU*up rows (the weights stream next, through L2)
-  // and the fp16 rows its down_proj left for a next layer (a later layer call on
-  // this hidden recomputes them)
+  // and, when the head does not read them, the fp16 rows its down_proj left for a
+  // next layer (a later layer call on this hidden then recomputes them)
   set_discard(x, g, 0, x->ws + x->r_act.off, static_cast<size_t>(b->num_tokens) * x->n * x->i_p * 2);
-  if (!x->keep_intermediates) {
+  if (!direct && !x->keep_intermediates) {
     set_discard(x, g, 1, x->ws + x->r_xn.off, static_cast<size_t>(b->num_tokens) * H * 2);
     x->stats_for = nullptr;
   }

@@ -84,9 +84,13 @@ cudaError_t launch_embed(const int32_t* ids, int T, const void* embed_stacked, i
                     reinterpret_cast<uint4*>(xh), ss, status);
 }
 
+// two bf16 ones: the norm weight of a norm whose weight is folded into the next GEMM
+constexpr uint32_t kOnes2 = 0x3F803F80u;
+
 // ---------------------------------------------------------------------------
 // RMSNorm over the hidden dimension of the fp32 residual stream, fp32 math:
-// y = x * rsqrt(mean(x^2) + eps) * w, written as fp16 (the next GEMM's operand).
+// y = x * rsqrt(mean(x^2) + eps) * w, written as fp16 (the next GEMM's operand);
+// w null: ones (the weight is folded into that GEMM's weights).
 // One warp per row; row_index (optional) picks the source row of each output row.
 // ---------------------------------------------------------------------------
 template <int VPL>  // 8-element groups per lane kept in registers
@@ -120,7 +124,7 @@ __global__ void rmsnorm_kernel(const float4* __restrict__ x, int64_t rows, int H
   for (int j = 0; j < VPL; ++j) {
     const int c = lane + 32 * j;
     if (c < chunks) {
-      const uint4 wu = w[c];
+      const uint4 wu = w ? w[c] : make_uint4(kOnes2, kOnes2, kOnes2, kOnes2);
       const float wf[8] = {bf16lo(wu.x), bf16hi(wu.x), bf16lo(wu.y), bf16hi(wu.y),
                            bf16lo(wu.z), bf16hi(wu.z), bf16lo(wu.w), bf16hi(wu.w)};
       uint4 o;
@@ -154,7 +158,7 @@ __global__ void rmsnorm_wide_kernel(const float4* __restrict__ x, int64_t rows, 
   const float inv = rsqrtf(ss / static_cast<float>(H) + eps);
   for (int c = lane; c < chunks; c += 32) {
     const float4 a = xr[2 * c], b = xr[2 * c + 1];
-    const uint4 wu = w[c];
+    const uint4 wu = w ? w[c] : make_uint4(kOnes2, kOnes2, kOnes2, kOnes2);
     uint4 o;
     o.x = pack_f16x2(a.x * inv * bf16lo(wu.x), a.y * inv * bf16hi(wu.x));
     o.y = pack_f16x2(a.z * inv * bf16lo(wu.y), a.w * inv * bf16hi(wu.y));
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(256) rmsnorm_row_block_kernel(const float4* __
   for (int j = 0; j < CPT; ++j) {
     const int c = threadIdx.x + 256 * j;
     if (c < chunks) {
-      const uint4 wu = w[c];
+      const uint4 wu = w ? w[c] : make_uint4(kOnes2, kOnes2, kOnes2, kOnes2);
       const float wf[8] = {bf16lo(wu.x), bf16hi(wu.x), bf16lo(wu.y), bf16hi(wu.y),
                            bf16lo(wu.z), bf16hi(wu.z), bf16lo(wu.w), bf16hi(wu.w)};
       uint4 o;

@@ -81,7 +81,8 @@ extern "C" tp_status tp_lm_head_argmax_static(tp_ctx* ctx, const void* head_shar
   const char* w = static_cast<const char*>(head_shards);
   const int B = b->num_seqs;
   void* z = scratch + kZOff;
-  cudaError_t e = tpk::launch_final_norm_select(hidden, hv.H, b->cu_q, B, w + hv.final_norm_off, hv.eps, z, s);
+  // the final norm's weight is folded into the LM head copy: normalize with ones
+  cudaError_t e = tpk::launch_final_norm_select(hidden, hv.H, b->cu_q, B, nullptr, hv.eps, z, s);
   if (e != cudaSuccess) return TP_ERR_CUDA;
   tpk::GemmProblem g{};
   g.x = z; g.x_rows = B; g.x_cols = hv.H; g.x_ld = hv.H;

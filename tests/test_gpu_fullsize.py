@@ -44,3 +44,14 @@ def test_qwen3_06b_model_mixed_step(n):
     g = GpuStep(w, n)
     check_step(g, [0, 4, 131])
     assert g.runner.ctx.rank_sum_count() == 2 * 28 + 1
+
+
+@pytest.mark.parametrize("workload,seqs", [("qwen3_0.6b_layer_prefill2048", [0]),
+                                           ("qwen3_0.6b_layer_decode64x4096", [0, 31, 63])])
+def test_greedy_ids_from_the_last_fp16_rows(workload, seqs):
+    """Without logits the LM head reads the last tokens' fp16 rows that the down_proj
+    epilogue left (one sequence, or one token per sequence): the final norm's weight
+    is folded into the head and its positive row scale cannot move the argmax."""
+    w = synth.WORKLOADS[workload]
+    g = GpuStep(w, 2, logits=False)
+    check_step(g, seqs)

@@ -95,7 +95,8 @@ def test_shard_weights_bit_exact(s, n):
     for r in range(n):
         a, b = of.vocab_range(s.vocab, n, r)
         assert torch.equal(emb[r, : b - a], hw.embed[a:b]) and torch.count_nonzero(emb[r, b - a:]) == 0
-        assert torch.equal(lm[r, : b - a], hw.lm_head[a:b].to(torch.float16))
+        # the LM head copy carries the final norm weight in its columns
+        assert torch.equal(lm[r, : b - a], (hw.lm_head[a:b] * hw.final_norm[None, :]).to(torch.float16))
 
 
 @pytest.mark.parametrize("n", [1, 2, 3, 4])
