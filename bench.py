@@ -76,12 +76,12 @@ def workload_config(w: synth.Workload, n: int) -> dict:
 # source at capture time and is reported only while the source is unchanged.
 # The summaries of those captures are under profiles/.
 NCU_TRAFFIC = {
-    ("qwen3_0.6b_layer_prefill2048", 2, "gemm_lm_head"): (311220480 + 3005696, "k_gemm.cu",
-                                                          "bf197ba55cb98a45"),
-    ("qwen3_0.6b_layer_decode64x4096", 2, "attn_decode"): (1077744128 + 4192768, "k_attention.cu",
-                                                            "0ddc8b37fcc5984a"),
-    ("qwen3_32b_layer_tp16_decode32x2048", 16, "gemm_lm_head"): (1558474496 + 3022080, "k_gemm.cu",
-                                                                  "bf197ba55cb98a45"),
+    ("qwen3_0.6b_layer_prefill2048", 2, "gemm_lm_head"): (311220992 + 3300096, "k_gemm.cu",
+                                                          "f1118f2c9374b043"),
+    ("qwen3_0.6b_layer_decode64x4096", 2, "attn_decode"): (1077700096 + 4140032, "k_attention.cu",
+                                                            "805c1fd9119b17d0"),
+    ("qwen3_32b_layer_tp16_decode32x2048", 16, "gemm_lm_head"): (1558444288 + 2683136, "k_gemm.cu",
+                                                                  "f1118f2c9374b043"),
 }
 KERNEL_HEADERS = ("kernels.h", "sm100.cuh", "common.cuh")
 
