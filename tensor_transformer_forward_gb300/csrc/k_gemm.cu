@@ -457,23 +457,26 @@ __device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8]) {
 // parity).  The (cos, sin) values of the thread's token and pairs are loaded
 // before the accumulator is ready, so their latency hides behind the MMA, and
 // they serve every q/k head of the tile; the q/k norm weights sit in shared
-// memory (nw: [2][128] fp32, q then k).  Same arithmetic as qkv_head.
-// Each thread stages its row's results (two hd-byte segments per output: its
-// pairs' first and second halves) in the warp's swizzled staging rows (stg:
-// [2 outputs][32 rows][hd bytes]); the warp then writes them out as whole
-// 64-byte row segments (a few rows per instruction instead of 32 scattered
-// 16-byte pieces), each row to its own destination.
+// memory (nw: [2][128] fp32, q then k).  Same arithmetic as qkv_head, after the
+// deferred input norm's row scale rinv.
+// Each thread stages its row's results in the warp's staging (stg: [2 outputs:
+// high / k / v, q low][2 segments: the pairs' first and second halves][32 rows]
+// [QP bf16]).  q rows leave through TMA stores of those 32-row boxes (tmQ: the
+// QKV buffer, tmQlo: the q low part); k and v rows go to each token's cache
+// position, written by the warp as whole row segments (several rows per
+// instruction instead of 32 scattered 16-byte pieces).
 // Returns false (on both warps of the pair) when the accumulator wait failed.
 template <int BN, int HD>
-__device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, uint32_t tfull, uint32_t use,
-                                              volatile int* abort_flag, uint32_t ta, int t, const TokPos& tp,
-                                              int f0, bool row_ok, int w, int q, int row, int par, const float* nw,
-                                              float* ss, uint8_t* stg, float rinv) {
+__device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmQlo,
+                                              uint32_t tfull, uint32_t use, volatile int* abort_flag, uint32_t ta,
+                                              int t, const TokPos& tp, int f0, bool row_ok, int w, int q, int row,
+                                              int par, const float* nw, float* ss, uint8_t* stg, float rinv) {
   constexpr int HALF = HD / 2, QP = HALF / 2, NR = QP / 2, HPT = BN / HD;
-  constexpr int RB = HD;        // staged bytes per row and output: 2 segments x QP bf16
-  constexpr int CPR = RB / 16;  // 16-byte chunks per staged row
-  constexpr int RPI = 32 / CPR; // rows per write-out instruction
+  constexpr int SEGB = QP * 2;        // bytes of one row segment (QP bf16)
+  constexpr int NC = SEGB / 16;       // 16-byte chunks per row segment
+  constexpr int OUTB = 2 * 32 * SEGB; // bytes per output
   const int lane = threadIdx.x & 31;
+  const int tbox = t - lane;          // first row of this warp's 32 rows
   const QkvEpi& e = p.qkv;
   int kind[HPT];  // per head of the tile: 0 q, 1 k, 2 v, -1 past the last column (warp-uniform)
   bool any_rot = false;
@@ -513,12 +516,12 @@ __device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, uint32_t tful
       if (kind[hb] < 0 || kind[hb] == 2) continue;
       float s = 0.0f;
 #pragma unroll
-      for (int c = 0; c < QP / 8; ++c) {
-        float a[8], b[8];
-        tc_ld8(ta + hb * HD + w * QP + c * 8, a);
-        tc_ld8(ta + hb * HD + HALF + w * QP + c * 8, b);
+      for (int c = 0; c < QP / 16; ++c) {
+        float a[16], b[16];
+        tc_ld16(ta + hb * HD + w * QP + c * 16, a);
+        tc_ld16(ta + hb * HD + HALF + w * QP + c * 16, b);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) s += a[i] * a[i] + b[i] * b[i];
+        for (int i = 0; i < 16; ++i) s += a[i] * a[i] + b[i] * b[i];
       }
       mine[hb * 128 + row] = s;
       inv[hb] = s;
@@ -531,71 +534,62 @@ __device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, uint32_t tful
   }
   const size_t plane = static_cast<size_t>(e.max_seqs) * e.nkv_l * e.cap * HD;
   __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(e.kv);
-  uint8_t* my_row = stg + lane * RB;
-  uint8_t* my_row_lo = stg + 32 * RB + lane * RB;
 #pragma unroll
   for (int hb = 0; hb < HPT; ++hb) {
     if (kind[hb] < 0) continue;
     const int col0 = f0 + hb * HD;
     const int r = col0 / e.w_rank;
     const int sh = (col0 - r * e.w_rank) / HD;
-    // destinations of this head's row (as in qkv_head): k / v rows of the rank's
-    // cache, or q (high part / fp16) in the QKV buffer and its low part
-    __nv_bfloat16* dst;
-    __nv_bfloat16* qlo = nullptr;
-    if (kind[hb] == 0) {
-      dst = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(t) * p.ldo + col0;
-      qlo = reinterpret_cast<__nv_bfloat16*>(e.q_lo) + static_cast<size_t>(t) * e.n * e.nq_l * HD +
-            (static_cast<size_t>(r) * e.nq_l + sh) * HD;
-    } else {
-      const int g = kind[hb] == 1 ? sh - e.nq_l : sh - e.nq_l - e.nkv_l;
-      dst = kv + (2 * static_cast<size_t>(r) + (kind[hb] == 2 ? 1 : 0)) * plane +
-            ((static_cast<size_t>(tp.seq_slot) * e.nkv_l + g) * e.cap + tp.pos) * HD;
-    }
     const bool lo_out = kind[hb] == 0 && tp.prefill;  // per row
     const float* w8 = nw + (kind[hb] == 1 ? 128 : 0);
+    // the staging's previous TMA stores have read it
+    if (lane == 0) bulk_wait_read();
+    __syncwarp();
 #pragma unroll
-    for (int c = 0; c < QP / 8; ++c) {
-      const int d0 = w * QP + c * 8;
-      float a[8], b[8];
-      __syncwarp();  // tcgen05.ld is warp-collective; rows of a mixed tile branch below
-      tc_ld8(ta + hb * HD + d0, a);
-      tc_ld8(ta + hb * HD + HALF + d0, b);
+    for (int c2 = 0; c2 < QP / 16; ++c2) {
+      float a[16], b[16];
+      tc_ld16(ta + hb * HD + w * QP + c2 * 16, a);
+      tc_ld16(ta + hb * HD + HALF + w * QP + c2 * 16, b);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {  // deferred RMSNorm of the input row
-        a[i] *= rinv;
-        b[i] *= rinv;
-      }
-      // staged chunk positions of this pair chunk: segment 0 (dims d0..) and 1 (HALF + d0..)
-      const int k0 = (c ^ (lane % CPR)) * 16, k1 = ((CPR / 2 + c) ^ (lane % CPR)) * 16;
-      uint4 h0, h1;
-      if (kind[hb] == 2) {  // v: raw
-        h0 = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
-                        pack_bf16x2(a[6], a[7]));
-        h1 = make_uint4(pack_bf16x2(b[0], b[1]), pack_bf16x2(b[2], b[3]), pack_bf16x2(b[4], b[5]),
-                        pack_bf16x2(b[6], b[7]));
-      } else {
+      for (int hc = 0; hc < 2; ++hc) {  // 8 pairs per staged chunk
+        const int c = c2 * 2 + hc;       // chunk within the row segment
+        const int d0 = w * QP + c * 8;
+        float x0[8], x1[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {  // deferred RMSNorm of the input row
+          x0[i] = a[hc * 8 + i] * rinv;
+          x1[i] = b[hc * 8 + i] * rinv;
+        }
+        uint8_t* s0 = stg + lane * SEGB + c * 16;                 // output 0, segment 0
+        uint8_t* s1 = stg + 32 * SEGB + lane * SEGB + c * 16;     // output 0, segment 1
+        if (kind[hb] == 2) {  // v: raw
+          *reinterpret_cast<uint4*>(s0) = make_uint4(pack_bf16x2(x0[0], x0[1]), pack_bf16x2(x0[2], x0[3]),
+                                                     pack_bf16x2(x0[4], x0[5]), pack_bf16x2(x0[6], x0[7]));
+          *reinterpret_cast<uint4*>(s1) = make_uint4(pack_bf16x2(x1[0], x1[1]), pack_bf16x2(x1[2], x1[3]),
+                                                     pack_bf16x2(x1[4], x1[5]), pack_bf16x2(x1[6], x1[7]));
+          continue;
+        }
         float y0[8], y1[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float4 cc = rc[(c * 8 + i) >> 1];
           const float cs = (i & 1) ? cc.z : cc.x;
           const float sn = (i & 1) ? cc.w : cc.y;
-          const float u0 = a[i] * inv[hb] * w8[d0 + i];
-          const float u1 = b[i] * inv[hb] * w8[HALF + d0 + i];
+          const float u0 = x0[i] * inv[hb] * w8[d0 + i];
+          const float u1 = x1[i] * inv[hb] * w8[HALF + d0 + i];
           y0[i] = u0 * cs - u1 * sn;
           y1[i] = u1 * cs + u0 * sn;
         }
         if (kind[hb] == 0 && !tp.prefill) {  // decode q: fp16
-          h0 = make_uint4(pack_f16x2(y0[0], y0[1]), pack_f16x2(y0[2], y0[3]), pack_f16x2(y0[4], y0[5]),
-                          pack_f16x2(y0[6], y0[7]));
-          h1 = make_uint4(pack_f16x2(y1[0], y1[1]), pack_f16x2(y1[2], y1[3]), pack_f16x2(y1[4], y1[5]),
-                          pack_f16x2(y1[6], y1[7]));
+          *reinterpret_cast<uint4*>(s0) = make_uint4(pack_f16x2(y0[0], y0[1]), pack_f16x2(y0[2], y0[3]),
+                                                     pack_f16x2(y0[4], y0[5]), pack_f16x2(y0[6], y0[7]));
+          *reinterpret_cast<uint4*>(s1) = make_uint4(pack_f16x2(y1[0], y1[1]), pack_f16x2(y1[2], y1[3]),
+                                                     pack_f16x2(y1[4], y1[5]), pack_f16x2(y1[6], y1[7]));
         } else {  // k, prefill q high part: bf16
-          h0 = make_uint4(pack_bf16x2(y0[0], y0[1]), pack_bf16x2(y0[2], y0[3]), pack_bf16x2(y0[4], y0[5]),
-                          pack_bf16x2(y0[6], y0[7]));
-          h1 = make_uint4(pack_bf16x2(y1[0], y1[1]), pack_bf16x2(y1[2], y1[3]), pack_bf16x2(y1[4], y1[5]),
-                          pack_bf16x2(y1[6], y1[7]));
+          *reinterpret_cast<uint4*>(s0) = make_uint4(pack_bf16x2(y0[0], y0[1]), pack_bf16x2(y0[2], y0[3]),
+                                                     pack_bf16x2(y0[4], y0[5]), pack_bf16x2(y0[6], y0[7]));
+          *reinterpret_cast<uint4*>(s1) = make_uint4(pack_bf16x2(y1[0], y1[1]), pack_bf16x2(y1[2], y1[3]),
+                                                     pack_bf16x2(y1[4], y1[5]), pack_bf16x2(y1[6], y1[7]));
           if (lo_out) {  // q - bf16(q)
             float l0[8], l1[8];
 #pragma unroll
@@ -603,37 +597,49 @@ __device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, uint32_t tful
               l0[i] = y0[i] - bf2f(f2bf(y0[i]));
               l1[i] = y1[i] - bf2f(f2bf(y1[i]));
             }
-            *reinterpret_cast<uint4*>(my_row_lo + k0) =
+            *reinterpret_cast<uint4*>(s0 + OUTB) =
                 make_uint4(pack_bf16x2(l0[0], l0[1]), pack_bf16x2(l0[2], l0[3]), pack_bf16x2(l0[4], l0[5]),
                            pack_bf16x2(l0[6], l0[7]));
-            *reinterpret_cast<uint4*>(my_row_lo + k1) =
+            *reinterpret_cast<uint4*>(s1 + OUTB) =
                 make_uint4(pack_bf16x2(l1[0], l1[1]), pack_bf16x2(l1[2], l1[3]), pack_bf16x2(l1[4], l1[5]),
                            pack_bf16x2(l1[6], l1[7]));
           }
         }
       }
-      *reinterpret_cast<uint4*>(my_row + k0) = h0;
-      *reinterpret_cast<uint4*>(my_row + k1) = h1;
+    }
+    if (kind[hb] == 0) {
+      // q: 32-row boxes to the QKV buffer (and the low part), rows past the last
+      // token clipped by the tensor maps
+      const bool any_lo = __any_sync(0xffffffffu, live && lo_out);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int lo_col = (r * e.nq_l + sh) * HD;
+#pragma unroll
+        for (int sg = 0; sg < 2; ++sg) {
+          tma_store_2d(tmQ, smem_u32(stg + sg * 32 * SEGB), col0 + sg * HALF + w * QP, tbox);
+          if (any_lo) tma_store_2d(tmQlo, smem_u32(stg + OUTB + sg * 32 * SEGB), lo_col + sg * HALF + w * QP, tbox);
+        }
+        bulk_commit();
+      }
+      continue;
     }
     __syncwarp();
-    // write-out: lane -> (row rr, chunk k) of the staged rows; row rr's destination
-    // comes from its owner lane
-    const unsigned long long my_dst = live ? reinterpret_cast<unsigned long long>(dst) : 0ull;
-    const unsigned long long my_lo = (live && lo_out) ? reinterpret_cast<unsigned long long>(qlo) : 0ull;
-    const bool any_lo = __any_sync(0xffffffffu, my_lo != 0ull);
+    // k / v: lane -> (row rr, segment sg, chunk k) of the staged rows; row rr's
+    // cache row comes from its owner lane
+    const int g = kind[hb] == 1 ? sh - e.nq_l : sh - e.nq_l - e.nkv_l;
+    const unsigned long long my_dst =
+        live ? reinterpret_cast<unsigned long long>(
+                   kv + (2 * static_cast<size_t>(r) + (kind[hb] == 2 ? 1 : 0)) * plane +
+                   ((static_cast<size_t>(tp.seq_slot) * e.nkv_l + g) * e.cap + tp.pos) * HD)
+             : 0ull;
 #pragma unroll
-    for (int i = 0; i < CPR; ++i) {
-      const int rr = i * RPI + lane / CPR, k = lane % CPR;
-      const int off = (k / (CPR / 2)) * HALF + w * QP + (k % (CPR / 2)) * 8;  // elements within the head row
-      const int sk = (k ^ (rr % CPR)) * 16;
-      const unsigned long long d = __shfl_sync(0xffffffffu, my_dst, rr);
-      if (d) *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(d) + off) =
-          *reinterpret_cast<const uint4*>(stg + rr * RB + sk);
-      if (any_lo) {
-        const unsigned long long dl = __shfl_sync(0xffffffffu, my_lo, rr);
-        if (dl) *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dl) + off) =
-            *reinterpret_cast<const uint4*>(stg + 32 * RB + rr * RB + sk);
-      }
+    for (int i = 0; i < 2 * NC; ++i) {
+      const int idx = i * 32 + lane;
+      const int rr = idx / (2 * NC), rem = idx % (2 * NC), sg = rem / NC, k = rem % NC;
+      const unsigned long long dd = __shfl_sync(0xffffffffu, my_dst, rr);
+      if (dd) *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dd) + sg * HALF + w * QP + k * 8) =
+          *reinterpret_cast<const uint4*>(stg + sg * 32 * SEGB + rr * SEGB + k * 16);
     }
     __syncwarp();  // the staging rows are rewritten by the next head
   }
@@ -1340,10 +1346,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
         const int w = (warp - 2) >> 2;
         uint8_t* stg = sStg + (warp - 2) * (2 * 32 * 128);
         const bool ok = p.qkv.hd == 128
-                            ? qkv_pair_tile<BN, 128>(p, TFULL(b), use, abort_flag, ta, t, tp, f0, row_ok, w, q, row,
-                                                     seg & 1, sNw, sSS, stg, rinv)
-                            : qkv_pair_tile<BN, 64>(p, TFULL(b), use, abort_flag, ta, t, tp, f0, row_ok, w, q, row,
-                                                    seg & 1, sNw, sSS, stg, rinv);
+                            ? qkv_pair_tile<BN, 128>(p, &tmO, &tmO2, TFULL(b), use, abort_flag, ta, t, tp, f0, row_ok,
+                                                     w, q, row, seg & 1, sNw, sSS, stg, rinv)
+                            : qkv_pair_tile<BN, 64>(p, &tmO, &tmO2, TFULL(b), use, abort_flag, ta, t, tp, f0, row_ok,
+                                                    w, q, row, seg & 1, sNw, sSS, stg, rinv);
         if (!ok) break;
         tc_fence_before();
         __syncwarp();
@@ -1551,7 +1557,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
       }
     }
     if constexpr (C::RESID_ROWS) cp_async_wait_all();  // no copy into the staging outlives the CTA
-    if constexpr (C::TMA_OUT) {  // every store has landed before the CTA (and its staging) goes away
+    if constexpr (C::TMA_OUT || C::QKV_PAIR) {  // every store has landed before the CTA (and its staging) goes away
       if (lane == 0) bulk_wait_all();
       __syncwarp();
     }
@@ -1620,15 +1626,16 @@ static bool make_map_out(CUtensorMap* m, const void* base, int64_t rows, int64_t
          CUDA_SUCCESS;
 }
 
-// fp16 [rows][cols] row-major, box 32 columns (64 bytes) x 32 rows, no swizzle.
-static bool make_map_rows16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+// 16-bit [rows][cols] row-major, box box_cols columns x 32 rows, no swizzle.
+static bool make_map_rows16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_cols = 32) {
   auto fn = encode_fn();
   if (!fn || !base || rows <= 0 || cols <= 0) return false;
   if ((reinterpret_cast<uintptr_t>(base) & 15) || (cols * 2) % 16) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
-  cuuint32_t box[2] = {32u, 32u};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), 32u};
   cuuint32_t estr[2] = {1u, 1u};
+  if ((box_cols * 2) % 16) return false;
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -1742,6 +1749,12 @@ static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, 
   }
   if constexpr (Cfg::RESID_ROWS) {
     if (gp.row_ss_out && !make_map_rows16(&mo2, pr.row_out16, pr.T, pr.out_cols)) return cudaErrorInvalidValue;
+  }
+  if constexpr (Cfg::QKV_PAIR) {  // q rows (high / fp16 part, low part) leave through TMA
+    const int qp = pr.qkv.hd / 4;
+    if (pr.ldo != pr.out_cols || !pr.qkv.q_lo || !make_map_rows16(&mo, pr.out, pr.T, pr.ldo, qp) ||
+        !make_map_rows16(&mo2, pr.qkv.q_lo, pr.T, static_cast<int64_t>(pr.qkv.n) * pr.qkv.nq_l * pr.qkv.hd, qp))
+      return cudaErrorInvalidValue;
   }
   return launch_pdl(kern, dim3(grid), dim3(Cfg::THREADS), smem, s, mx, mw, mo, mo2, gp);
 }
