@@ -462,13 +462,14 @@ __device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8]) {
 // Each thread stages its row's results in the warp's staging (stg: [2 outputs:
 // high / k / v, q low][2 segments: the pairs' first and second halves][32 rows]
 // [QP bf16]).  q rows leave through TMA stores of those 32-row boxes (tmQ: the
-// QKV buffer, tmQlo: the q low part); k and v rows go to each token's cache
-// position, written by the warp as whole row segments (several rows per
-// instruction instead of 32 scattered 16-byte pieces).
+// QKV buffer, tmQlo: the q low part); so do k and v rows when the warp's 32
+// tokens are one sequence at consecutive positions (32 consecutive rows of the
+// cache seen as [rows][hd], tmKV); otherwise each row goes to its token's cache
+// position, written by the warp as whole row segments.
 // Returns false (on both warps of the pair) when the accumulator wait failed.
 template <int BN, int HD>
 __device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmQlo,
-                                              uint32_t tfull, uint32_t use, volatile int* abort_flag, uint32_t ta,
+                                              const CUtensorMap* tmKV, uint32_t tfull, uint32_t use, volatile int* abort_flag, uint32_t ta,
                                               int t, const TokPos& tp, int f0, bool row_ok, int w, int q, int row,
                                               int par, const float* nw, float* ss, uint8_t* stg, float rinv) {
   constexpr int HALF = HD / 2, QP = HALF / 2, NR = QP / 2, HPT = BN / HD;
@@ -624,10 +625,28 @@ __device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, const CUtenso
       }
       continue;
     }
+    const int g = kind[hb] == 1 ? sh - e.nq_l : sh - e.nq_l - e.nkv_l;
+    {
+      // k / v of one sequence at consecutive positions: 32 consecutive cache rows
+      const int slot0 = __shfl_sync(0xffffffffu, tp.seq_slot, 0);
+      const int pos0 = __shfl_sync(0xffffffffu, tp.pos, 0);
+      if (__all_sync(0xffffffffu, live && tp.seq_slot == slot0 && tp.pos == pos0 + lane)) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int crow = static_cast<int>(
+              (((static_cast<int64_t>(r) * 2 + (kind[hb] == 2 ? 1 : 0)) * e.max_seqs + slot0) * e.nkv_l + g) * e.cap +
+              pos0);
+#pragma unroll
+          for (int sg = 0; sg < 2; ++sg) tma_store_2d(tmKV, smem_u32(stg + sg * 32 * SEGB), sg * HALF + w * QP, crow);
+          bulk_commit();
+        }
+        continue;
+      }
+    }
     __syncwarp();
     // k / v: lane -> (row rr, segment sg, chunk k) of the staged rows; row rr's
     // cache row comes from its owner lane
-    const int g = kind[hb] == 1 ? sh - e.nq_l : sh - e.nq_l - e.nkv_l;
     const unsigned long long my_dst =
         live ? reinterpret_cast<unsigned long long>(
                    kv + (2 * static_cast<size_t>(r) + (kind[hb] == 2 ? 1 : 0)) * plane +
@@ -991,7 +1010,7 @@ template <int BN, int EPI, bool ACC, bool SWAP>
 __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmKV, const GemmParams p) {
   using C = GemmCfg<BN, EPI, ACC, SWAP>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -1346,10 +1365,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
         const int w = (warp - 2) >> 2;
         uint8_t* stg = sStg + (warp - 2) * (2 * 32 * 128);
         const bool ok = p.qkv.hd == 128
-                            ? qkv_pair_tile<BN, 128>(p, &tmO, &tmO2, TFULL(b), use, abort_flag, ta, t, tp, f0, row_ok,
-                                                     w, q, row, seg & 1, sNw, sSS, stg, rinv)
-                            : qkv_pair_tile<BN, 64>(p, &tmO, &tmO2, TFULL(b), use, abort_flag, ta, t, tp, f0, row_ok,
-                                                    w, q, row, seg & 1, sNw, sSS, stg, rinv);
+                            ? qkv_pair_tile<BN, 128>(p, &tmO, &tmO2, &tmKV, TFULL(b), use, abort_flag, ta, t, tp, f0,
+                                                     row_ok, w, q, row, seg & 1, sNw, sSS, stg, rinv)
+                            : qkv_pair_tile<BN, 64>(p, &tmO, &tmO2, &tmKV, TFULL(b), use, abort_flag, ta, t, tp, f0,
+                                                    row_ok, w, q, row, seg & 1, sNw, sSS, stg, rinv);
         if (!ok) break;
         tc_fence_before();
         __syncwarp();
@@ -1741,6 +1760,7 @@ static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, 
   }
   CUtensorMap mo = mx;  // unused unless the outputs leave through TMA
   CUtensorMap mo2 = mx;  // fp16 residual rows of the residual epilogues (row_ss_out set)
+  CUtensorMap mkv = mx;  // the KV cache as [rows][hd] (paired QKV epilogue)
   if constexpr (Cfg::TMA_OUT) {
     const bool ok = EPI == EPI_RESID
                         ? make_map_out(&mo, pr.out, pr.T, pr.out_cols, pr.ldo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4)
@@ -1752,11 +1772,15 @@ static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, 
   }
   if constexpr (Cfg::QKV_PAIR) {  // q rows (high / fp16 part, low part) leave through TMA
     const int qp = pr.qkv.hd / 4;
-    if (pr.ldo != pr.out_cols || !pr.qkv.q_lo || !make_map_rows16(&mo, pr.out, pr.T, pr.ldo, qp) ||
-        !make_map_rows16(&mo2, pr.qkv.q_lo, pr.T, static_cast<int64_t>(pr.qkv.n) * pr.qkv.nq_l * pr.qkv.hd, qp))
+    const int64_t kv_rows =
+        static_cast<int64_t>(pr.qkv.n) * 2 * pr.qkv.max_seqs * pr.qkv.nkv_l * static_cast<int64_t>(pr.qkv.cap);
+    if (pr.ldo != pr.out_cols || !pr.qkv.q_lo || kv_rows >= (int64_t(1) << 31) ||
+        !make_map_rows16(&mo, pr.out, pr.T, pr.ldo, qp) ||
+        !make_map_rows16(&mo2, pr.qkv.q_lo, pr.T, static_cast<int64_t>(pr.qkv.n) * pr.qkv.nq_l * pr.qkv.hd, qp) ||
+        !make_map_rows16(&mkv, pr.qkv.kv, kv_rows, pr.qkv.hd, qp))
       return cudaErrorInvalidValue;
   }
-  return launch_pdl(kern, dim3(grid), dim3(Cfg::THREADS), smem, s, mx, mw, mo, mo2, gp);
+  return launch_pdl(kern, dim3(grid), dim3(Cfg::THREADS), smem, s, mx, mw, mo, mo2, mkv, gp);
 }
 
 cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partials, int* counters, int* status,
