@@ -109,3 +109,16 @@ def test_decode_large_weights_64dim_heads_few_tokens():
     w = synth.Workload("large_w_decode", s, (2,), ((9, 0),), (3, 70, 200, 0), 1, False)
     g = GpuStep(w, 2, perturbed=True)
     check_step(g, list(range(5)))
+
+
+@pytest.mark.parametrize("prefill,decode", [(((130, 0),), (3, 70)), (((9, 0),), (3, 70, 200))])
+def test_hidden_not_a_multiple_of_128(prefill, decode):
+    """hidden 4160 = 32.5 x 128: the residual epilogues' last feature tile lies half
+    outside the rows (token tiles for the 132-token step, weights-on-M rows for the
+    12-token one), the embedding's last chunk round is partial, and the deferred
+    norms add 130 column groups per row."""
+    s = synth.ModelShape(hidden=4160, num_q_heads=32, num_kv_heads=8, head_dim=64, intermediate=11008, vocab=2048,
+                         num_layers=1, tie_word_embeddings=False)
+    w = synth.Workload("ragged_hidden", s, (2,), prefill, decode, 1, True)
+    g = GpuStep(w, 2, perturbed=True)
+    check_step(g, list(range(w.num_seqs)))
