@@ -15,6 +15,10 @@ Readings taken where the pages are silent (each listed in the design doc):
     keys may see keys 0 .. j + (S - T).
   * Uneven splits are errors (no silent short chunks); vocab slices use
     div_ceil and the last slice may be shorter, but none may be empty.
+  * Sequence parallelism splits the tokens into contiguous rank chunks as even
+    as possible, the first T mod n ranks taking one token more (a rank may get
+    none); the final norm runs on the chunks and an all-gather of the normed
+    rows feeds the vocab-parallel head, as before any column-split layer.
   * No bias anywhere.
 """
 
@@ -248,6 +252,14 @@ def even_chunk(size: int, n: int, r: int) -> Tuple[int, int]:
     return r * c, (r + 1) * c
 
 
+def token_chunk(T: int, n: int, r: int) -> Tuple[int, int]:
+    """[start, end) of rank r's tokens under sequence parallelism: contiguous,
+    as even as possible, the first T mod n ranks one token more."""
+    base, extra = divmod(T, n)
+    start = r * base + min(r, extra)
+    return start, start + base + (1 if r < extra else 0)
+
+
 def kv_heads_of_rank(shape: Shape, n: int, r: int) -> List[int]:
     """Global kv heads held by rank r: an even chunk, or, when there are fewer kv
     heads than ranks, the single head r * nkv // n (replicated on several ranks)."""
@@ -341,11 +353,33 @@ def shard_layer(w: LayerWeights, shape: Shape, n: int, r: int) -> RankLayer:
 # ---------------------------------------------------------------------------
 
 class Comm:
-    """Stands in for the collectives: a rank-ordered sum and a gather, counted."""
+    """Stands in for the collectives: a rank-ordered sum and a gather, counted;
+    for sequence parallelism also the sum scattered by token chunk and the
+    gather of token chunks."""
 
     def __init__(self) -> None:
         self.num_all_reduce = 0
         self.num_all_gather = 0
+        self.num_reduce_scatter = 0
+        self.num_all_gather_rows = 0
+
+    def reduce_scatter(self, partials: Sequence[torch.Tensor]) -> List[torch.Tensor]:
+        """Rank r receives the rank-ordered sum of rows token_chunk(T, n, r)."""
+        self.num_reduce_scatter += 1
+        n, T = len(partials), partials[0].shape[0]
+        out = []
+        for r in range(n):
+            a, b = token_chunk(T, n, r)
+            acc = partials[0][a:b].clone()
+            for p in partials[1:]:
+                acc = acc + p[a:b]
+            out.append(acc)
+        return out
+
+    def all_gather_rows(self, chunks: Sequence[torch.Tensor]) -> torch.Tensor:
+        """Every rank receives the token chunks of all ranks, in rank order."""
+        self.num_all_gather_rows += 1
+        return torch.cat(list(chunks), dim=0)
 
     def all_reduce(self, partials: Sequence[torch.Tensor]) -> torch.Tensor:
         self.num_all_reduce += 1
@@ -431,6 +465,79 @@ def tp_lm_head(x_last: torch.Tensor, hw: HeadWeights, shape: Shape, n: int, comm
     return comm.all_gather(parts)[..., : shape.vocab]
 
 
+# ---------------------------------------------------------------------------
+# Sequence parallelism ("Tensor parallelism from scratch", section "Exercises",
+# exercise 1): each all-reduce after a row-split GEMM becomes a reduce-scatter
+# to the ranks' token chunks; the residual add and the RMSNorm run on a rank's
+# own tokens only; an all-gather of the normed chunks precedes each
+# column-split GEMM.  The collectives move the same data as the all-reduce
+# they replace; the per-token work of each rank drops to its 1/n of the tokens.
+# ---------------------------------------------------------------------------
+
+def sp_embed(ids: torch.Tensor, hw: HeadWeights, shape: Shape, n: int, comm: Comm) -> List[torch.Tensor]:
+    """Vocab-parallel embedding whose rank sum is scattered by token chunk."""
+    partials = []
+    for r in range(n):
+        start, end = vocab_range(shape.vocab, n, r)
+        e_r = shard_tensor("embed", hw.embed, shape, n, r)
+        outside = (ids < start) | (ids >= end)
+        local = (ids - start).masked_fill(outside, 0)
+        partials.append(e_r[local].masked_fill(outside[..., None], 0.0))
+    return comm.reduce_scatter(partials)
+
+
+def sp_decoder_layer(x_chunks: Sequence[torch.Tensor], ranks: Sequence[RankLayer], shape: Shape,
+                     k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor], comm: Comm
+                     ) -> Tuple[List[torch.Tensor], List[torch.Tensor], List[torch.Tensor]]:
+    """One layer under tensor + sequence parallelism for one sequence.  Rank r
+    holds x_chunks[r], the residual rows of its token chunk; the column GEMMs
+    and attention see all tokens (gathered), the row GEMMs' partials are
+    summed into the chunks."""
+    eps, hd = shape.rms_eps, shape.head_dim
+    h = comm.all_gather_rows([rms_norm(x_chunks[r], ranks[r].in_norm, eps) for r in range(len(ranks))])
+    T = h.shape[0]
+    attn_partials, new_k, new_v = [], [], []
+    for r, rl in enumerate(ranks):
+        ctx = k_caches[r].shape[1]
+        pos = torch.arange(ctx, ctx + T)
+        qkv = h @ rl.qkv.T
+        nq_w, nkv_w = rl.nq_l * hd, rl.nkv_l * hd
+        q = qkv[:, :nq_w].reshape(T, rl.nq_l, hd).transpose(0, 1)
+        k = qkv[:, nq_w:nq_w + nkv_w].reshape(T, rl.nkv_l, hd).transpose(0, 1)
+        v = qkv[:, nq_w + nkv_w:].reshape(T, rl.nkv_l, hd).transpose(0, 1)
+        q = apply_rope(rms_norm(q, rl.q_norm, eps), pos, shape.rope_theta)
+        k = apply_rope(rms_norm(k, rl.k_norm, eps), pos, shape.rope_theta)
+        K = torch.cat([k_caches[r], k], dim=1)
+        V = torch.cat([v_caches[r], v], dim=1)
+        o = causal_gqa_attention(q, K, V)
+        attn_partials.append(o.transpose(0, 1).reshape(T, nq_w) @ rl.o.T)
+        new_k.append(K)
+        new_v.append(V)
+    x_chunks = [x + s for x, s in zip(x_chunks, comm.reduce_scatter(attn_partials))]
+    h2 = comm.all_gather_rows([rms_norm(x_chunks[r], ranks[r].post_norm, eps) for r in range(len(ranks))])
+    mlp_partials = []
+    for rl in ranks:
+        gu = h2 @ rl.gate_up.T
+        a = silu(gu[:, : rl.i_l]) * gu[:, rl.i_l:]
+        mlp_partials.append(a @ rl.down.T)
+    x_chunks = [x + s for x, s in zip(x_chunks, comm.reduce_scatter(mlp_partials))]
+    return x_chunks, new_k, new_v
+
+
+def sp_lm_head(x_chunks: Sequence[torch.Tensor], hw: HeadWeights, shape: Shape, n: int, comm: Comm) -> torch.Tensor:
+    """Final norm on each rank's chunk, all-gather of the normed rows, then the
+    vocab-parallel logits of the last position (tp_lm_head's slices and gather)."""
+    z = comm.all_gather_rows([rms_norm(x, hw.final_norm, shape.rms_eps) for x in x_chunks])[-1]
+    parts = []
+    per = div_ceil(shape.vocab, n)
+    for r in range(n):
+        local = z @ shard_tensor("lm_head", hw.lm_head, shape, n, r).T
+        if local.shape[-1] < per:
+            local = torch.cat([local, torch.zeros(per - local.shape[-1], dtype=local.dtype)], dim=-1)
+        parts.append(local)
+    return comm.all_gather(parts)[: shape.vocab]
+
+
 def split_kv_by_rank(K: torch.Tensor, shape: Shape, n: int) -> List[torch.Tensor]:
     """Rank-local view of a global-head cache [nkv, S, hd]: rank r keeps its heads."""
     return [K[kv_heads_of_rank(shape, n, r)].clone() for r in range(n)]
@@ -507,6 +614,41 @@ def run_sequence(seq: SeqInput, layers: Sequence[LayerWeights], hw: Optional[Hea
         logits = tp_lm_head(x[-1], hw, shape, n, comm) if tp else lm_head(x[-1], hw, shape)
         out.logits = logits
         out.next_id = int(argmax_first(logits))
+    return out
+
+
+@dataclasses.dataclass
+class SpSeqOutput:
+    hidden_chunks: List[torch.Tensor]       # rank r: [token_chunk(T, n, r) rows, H] after the last layer
+    k_cache: List[torch.Tensor]             # extended caches, global heads
+    v_cache: List[torch.Tensor]
+    logits: Optional[torch.Tensor] = None   # [V] for the last position
+    next_id: Optional[int] = None
+
+
+def run_sequence_sp(seq: SeqInput, layers: Sequence[LayerWeights], hw: Optional[HeadWeights], shape: Shape,
+                    n: int, comm: Optional[Comm] = None, head: bool = True) -> SpSeqOutput:
+    """run_sequence under tensor + sequence parallelism: the residual stream
+    lives as token chunks (hidden rows given as input are split the same way)."""
+    validate_tp(shape, n)
+    comm = comm if comm is not None else Comm()
+    if seq.ids is not None:
+        x = sp_embed(seq.ids, hw, shape, n, comm)
+    else:
+        T = seq.hidden.shape[0]
+        x = [seq.hidden[slice(*token_chunk(T, n, r))] for r in range(n)]
+    ks, vs = [], []
+    for li, w in enumerate(layers):
+        ranks = [shard_layer(w, shape, n, r) for r in range(n)]
+        kc = split_kv_by_rank(seq.k_cache[li], shape, n)
+        vc = split_kv_by_rank(seq.v_cache[li], shape, n)
+        x, nk, nv = sp_decoder_layer(x, ranks, shape, kc, vc, comm)
+        ks.append(_merge_kv(nk, shape, n))
+        vs.append(_merge_kv(nv, shape, n))
+    out = SpSeqOutput(hidden_chunks=x, k_cache=ks, v_cache=vs)
+    if hw is not None and head:
+        out.logits = sp_lm_head(x, hw, shape, n, comm)
+        out.next_id = int(argmax_first(out.logits))
     return out
 
 

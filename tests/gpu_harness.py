@@ -145,6 +145,15 @@ def oracle_run(w: synth.Workload, seqs: Sequence[int], layers: int, perturbed: b
     return outs, ins
 
 
+def oracle_run_sp(w: synth.Workload, seq: int, layers: int, n: int, perturbed: bool = False, head: bool = True):
+    """One sequence through the oracle's tensor + sequence parallel form."""
+    s = w.shape
+    lw = [oracle_layer(s, li, perturbed) for li in range(layers)]
+    hw = oracle_head(s, perturbed) if (head or w.input_from_ids) else None
+    ins = oi.workload_seq_inputs(w, [seq], range(layers))
+    return of.run_sequence_sp(ins[0], lw, hw, oi.shape_of(s), n, head=head)
+
+
 def check_step(g: GpuStep, seqs: Sequence[int], head: bool = True, layers: Optional[int] = None) -> Dict[str, float]:
     """Compare the chosen sequences of a GPU step against the oracle."""
     L = g.L if layers is None else layers

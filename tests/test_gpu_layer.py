@@ -7,7 +7,8 @@ greedy ids equal where the reference top-2 margin exceeds 0.05."""
 import pytest
 
 import synth
-from tests.gpu_harness import GpuStep, check_step
+from oracle import forward as of
+from tests.gpu_harness import MARGIN, GpuStep, assert_close, check_step, oracle_run_sp
 
 pytestmark = pytest.mark.gpu
 
@@ -122,3 +123,24 @@ def test_hidden_not_a_multiple_of_128(prefill, decode):
     w = synth.Workload("ragged_hidden", s, (2,), prefill, decode, 1, True)
     g = GpuStep(w, 2, perturbed=True)
     check_step(g, list(range(w.num_seqs)))
+
+
+@pytest.mark.parametrize("n", [2, 4])
+def test_sequence_parallel_token_chunks(n):
+    """Sequence parallelism ("Tensor parallelism from scratch", Exercises, 1): one
+    prefill sequence of 301 tokens from ids, two layers and the head.  On one GPU
+    the reduce-scatter's token chunks are contiguous row ranges of the rank-summed
+    [T, H] residual that the row GEMM epilogues write, and the all-gather before a
+    column GEMM is the identity on that layout: rows token_chunk(T, n, r) of the
+    device's residual are rank r's chunk of the oracle's sequence-parallel form."""
+    T = 301
+    w = synth.Workload("sp_prefill", S06, (n,), ((T, 0),), (), 2, True)
+    g = GpuStep(w, n)
+    sp = oracle_run_sp(w, 0, 2, n)
+    for r in range(n):
+        a, b = of.token_chunk(T, n, r)
+        assert_close(g.hidden[a:b].float().cpu(), sp.hidden_chunks[r], f"token chunk of rank {r}")
+    assert_close(g.logits[0].cpu(), sp.logits, "logits")
+    top2 = sp.logits.topk(2).values
+    if float(top2[0] - top2[1]) > MARGIN:
+        assert int(g.out_ids[0]) == sp.next_id
