@@ -198,7 +198,10 @@ typedef struct {
 
 /* A2: vocab-parallel embedding ([TP] VocabParallelEmbedding): per rank, ids inside its slice
  * are looked up and the others give 0; the rank outputs are summed (fixed rank order).
- * ids: device int32 [T]; hidden_out: device fp32 [T, H] (the residual stream is fp32; GEMM
+ * ids: int32 [T] in device memory or in page-locked host memory (cudaHostAlloc / registered),
+ * which the kernel then reads over the host link itself (no separate copy; the buffer must
+ * stay unchanged until the kernel has run); other host memory is rejected with
+ * TP_ERR_INVALID_ARG.  hidden_out: device fp32 [T, H] (the residual stream is fp32; GEMM
  * operands are fp16; attention runs on bf16 q and the bf16 KV cache).  Ids outside [0, V) give zero rows
  * and set TP_ERR_BAD_TOKEN in *dev_status (device int32, sticky, read by tp_read_status). */
 tp_status tp_embed_vocab_parallel(tp_ctx* ctx, const void* head_shards, const int32_t* ids, int32_t num_tokens,
@@ -218,8 +221,10 @@ tp_status tp_decoder_layer_forward(tp_ctx* ctx, const void* layer_shards, const 
 /* A11-A13: final RMSNorm of each sequence's last token, vocab-parallel logits (all ranks'
  * slices, padded columns masked) with a fused (max, first index) epilogue, and the argmax
  * reduction that replaces the all-gather ([TP] TPTransformer.forward; [CH9] ParallelLMHead).
- * hidden: device fp32 [T, H].  out_ids: device int32 [num_seqs]; out_logits: device fp32
- * [num_seqs, V] or NULL. */
+ * hidden: device fp32 [T, H].  out_ids: int32 [num_seqs], in device memory or in page-locked
+ * host memory, which the kernel then writes over the host link itself (complete when the
+ * stream reaches this call's end); other host memory is rejected with TP_ERR_INVALID_ARG.
+ * out_logits: device fp32 [num_seqs, V] or NULL. */
 tp_status tp_lm_head_argmax(tp_ctx* ctx, const void* head_shards, const tp_batch* batch, const void* hidden,
                             int32_t* out_ids, float* out_logits, int32_t* dev_status, void* stream);
 

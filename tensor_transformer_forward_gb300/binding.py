@@ -142,6 +142,20 @@ def _dev(t: torch.Tensor, name: str, dtype: Optional[torch.dtype] = None) -> cty
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _dev_or_pinned(t: torch.Tensor, name: str, dtype: Optional[torch.dtype] = None) -> ctypes.c_void_p:
+    """A CUDA tensor, or a page-locked CPU tensor that the kernel reads or writes over
+    the host link itself."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda:
+        if not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or a page-locked (pinned) CPU tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if dtype is not None and t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+        return ctypes.c_void_p(t.data_ptr())
+    return _dev(t, name, dtype)
+
+
 @dataclasses.dataclass(frozen=True)
 class ModelConfig:
     hidden: int
@@ -344,8 +358,9 @@ def tp_shard_weights(ctx: Context, dst: torch.Tensor, layer: Optional[Dict[str, 
 
 def tp_embed_vocab_parallel(ctx: Context, head_shards: torch.Tensor, ids: torch.Tensor, hidden_out: torch.Tensor,
                             status: torch.Tensor) -> None:
-    _check(_lib.tp_embed_vocab_parallel(ctx.handle, _dev(head_shards, "head_shards"), _dev(ids, "ids", torch.int32),
-                                        ids.numel(), _dev(hidden_out, "hidden_out", torch.float32),
+    _check(_lib.tp_embed_vocab_parallel(ctx.handle, _dev(head_shards, "head_shards"),
+                                        _dev_or_pinned(ids, "ids", torch.int32), ids.numel(),
+                                        _dev(hidden_out, "hidden_out", torch.float32),
                                         _dev(status, "status", torch.int32), _stream()), "tp_embed_vocab_parallel")
 
 
@@ -362,7 +377,8 @@ def tp_lm_head_argmax(ctx: Context, head_shards: torch.Tensor, batch: Batch, hid
                       out_ids: torch.Tensor, status: torch.Tensor, out_logits: Optional[torch.Tensor] = None) -> None:
     lg = _dev(out_logits, "out_logits", torch.float32) if out_logits is not None else None
     _check(_lib.tp_lm_head_argmax(ctx.handle, _dev(head_shards, "head_shards"), ctypes.byref(batch.c),
-                                  _dev(hidden, "hidden", torch.float32), _dev(out_ids, "out_ids", torch.int32), lg,
+                                  _dev(hidden, "hidden", torch.float32),
+                                  _dev_or_pinned(out_ids, "out_ids", torch.int32), lg,
                                   _dev(status, "status", torch.int32), _stream()), "tp_lm_head_argmax")
 
 

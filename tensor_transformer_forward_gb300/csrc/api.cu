@@ -191,6 +191,20 @@ T* at(const void* base, const Region& r) {
   return reinterpret_cast<T*>(const_cast<char*>(reinterpret_cast<const char*>(base)) + r.off);
 }
 
+// The address a kernel uses for p: device (or managed) memory as it is, page-locked
+// host memory through its device mapping; null for memory the GPU cannot address.
+template <typename T>
+T* gpu_view(T* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return p;
+  if (a.type == cudaMemoryTypeHost) return static_cast<T*>(a.devicePointer);
+  return nullptr;
+}
+
 tp_status check_batch(const tp_ctx* x, const tp_batch* b) {
   if (!b || !b->cu_q || !b->ctx_len || !b->slot) return TP_ERR_INVALID_ARG;
   if (b->num_seqs <= 0 || b->num_seqs > x->ws_seqs) return TP_ERR_INVALID_ARG;
@@ -539,6 +553,8 @@ tp_status tp_workspace_init(tp_ctx* x, void* ws, size_t ws_bytes, int32_t max_to
 tp_status tp_embed_vocab_parallel(tp_ctx* x, const void* head_shards, const int32_t* ids, int32_t T,
                                   void* hidden_out, int32_t* dev_status, void* stream) {
   if (!x || !head_shards || !ids || !hidden_out || !dev_status || T <= 0) return TP_ERR_INVALID_ARG;
+  ids = gpu_view(ids);  // page-locked host ids are read by the kernel over the host link
+  if (!ids) return TP_ERR_INVALID_ARG;
   cudaError_t e;
   // with a workspace large enough, also the first layer's deferred-norm inputs
   const bool stats = x->ws != nullptr && T <= x->ws_tokens;
@@ -687,6 +703,8 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
 tp_status tp_lm_head_argmax(tp_ctx* x, const void* head_shards, const tp_batch* b, const void* hidden,
                             int32_t* out_ids, float* out_logits, int32_t* dev_status, void* stream) {
   if (!x || !head_shards || !hidden || !out_ids || !dev_status || !x->ws) return TP_ERR_INVALID_ARG;
+  out_ids = gpu_view(out_ids);  // page-locked host ids are written by the kernel over the host link
+  if (!out_ids) return TP_ERR_INVALID_ARG;
   tp_status st = check_batch(x, b);
   if (st != TP_OK) return st;
   st = ensure_device(x);

@@ -29,7 +29,10 @@ __global__ void embed_vocab_parallel_kernel(const int32_t* __restrict__ ids, con
   griddep_wait();  // the ids may come from the previous step's argmax
   griddep_launch();
   const int t = blockIdx.x;
-  const int id = ids[t];
+  // one read per warp (the ids may live in host memory, read over the host link)
+  int id = 0;
+  if ((threadIdx.x & 31) == 0) id = ids[t];
+  id = __shfl_sync(0xffffffffu, id, 0);
   if (threadIdx.x == 0 && (id < 0 || id >= vocab)) raise_flag(status, TP_DEVFLAG_BAD_TOKEN);
   const int chunks = H / 8;
   const int trips = (chunks + blockDim.x - 1) / blockDim.x;  // the same on every lane (group shuffles)
