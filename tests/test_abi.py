@@ -104,3 +104,14 @@ def test_layout_sizes():
     t = Context(_cfg(synth.QWEN3_06B, 2))
     assert t.weights_part("lm_head")[0] != t.weights_part("embed")[0]       # fp16 operand copy even when tied
     assert t.rank_sum_count() == 0
+
+
+def test_binding_refuses_pageable_host_buffers():
+    """ids / out_ids may be CUDA tensors or page-locked CPU tensors (read and written
+    by the kernels over the host link); other CPU memory is refused before any call."""
+    import torch
+    from tensor_transformer_forward_gb300 import binding
+    with pytest.raises(ValueError, match="page-locked"):
+        binding._dev_or_pinned(torch.zeros(4, dtype=torch.int32), "ids", torch.int32)
+    with pytest.raises(ValueError):
+        binding._dev(torch.zeros(4, dtype=torch.int32), "ids", torch.int32)
