@@ -115,3 +115,27 @@ def test_binding_refuses_pageable_host_buffers():
         binding._dev_or_pinned(torch.zeros(4, dtype=torch.int32), "ids", torch.int32)
     with pytest.raises(ValueError):
         binding._dev(torch.zeros(4, dtype=torch.int32), "ids", torch.int32)
+
+
+def test_entry_points_refuse_empty_or_missing_inputs_before_device_work():
+    """Degenerate calls (no tokens, no sequences, no workspace, null buffers) come back
+    as TP_ERR_INVALID_ARG from host-side checks, with nothing launched."""
+    import ctypes
+    from tensor_transformer_forward_gb300 import Context, binding
+    L = binding._lib
+    ctx = Context(_cfg(synth.TINY, 2))
+    h = ctx.handle
+    fake = ctypes.c_void_p(4096)  # never dereferenced: every call below fails its checks first
+    inval = binding.TP_ERR_INVALID_ARG
+    assert L.tp_embed_vocab_parallel(h, fake, fake, 0, fake, fake, None) == inval          # no tokens
+    assert L.tp_embed_vocab_parallel(h, fake, None, 4, fake, fake, None) == inval          # no ids
+    b = binding.TPBatch()
+    b.num_seqs, b.num_tokens = 0, 0
+    assert L.tp_decoder_layer_forward(h, fake, ctypes.byref(b), fake, fake, 1, 64, fake, None) == inval  # no workspace
+    assert L.tp_lm_head_argmax(h, fake, ctypes.byref(b), fake, fake, None, fake, None) == inval
+    assert L.tp_decoder_layer_forward(None, fake, ctypes.byref(b), fake, fake, 1, 64, fake, None) == inval
+    nb = ctypes.c_size_t()
+    assert L.tp_kv_cache_bytes(h, 0, 64, ctypes.byref(nb)) == inval                         # no sequences
+    assert L.tp_kv_cache_bytes(h, 1, 0, ctypes.byref(nb)) == inval                          # no positions
+    assert L.tp_hidden_written(None) == inval
+    assert ctx.launch_count() == 0
