@@ -334,9 +334,18 @@ template <int HD, int G>
 static cudaError_t launch_decode_tc_hd(const AttnArgs& a, dim3 grid, cudaStream_t s);
 static cudaError_t decode_tc_ctas_per_sm(int G, int* per_sm);
 
-// Key splits per (sequence, rank, kv head): the count that minimises
-//   waves(units * s / resident CTAs) * (keys per split + fixed cost)
-// so that the grid fills whole waves of resident CTAs; ties go to fewer splits.
+// Key splits per (sequence, rank, kv head).  CUDA-core kernel (64-dim heads): the
+// count that minimises waves(units * s / resident CTAs) * (keys per split + fixed
+// cost), so that the grid fills whole waves.  Tensor-core kernel (128-dim heads),
+// which streams K and V at the HBM rate: a wave of c CTAs takes as long as
+// max(c, nsat) CTAs' shares of the bytes, nsat being the CTAs that keep HBM
+// saturated, and each CTA adds about 1.25 key tiles of fixed work (set-up, the split
+// merge); minimised over s is
+//   sum over waves of (key tiles per split + 1.25) * max(CTAs in the wave, nsat).
+// nsat = 0.36 x the resident CTAs (one per SM here, by the occupancy query) and the
+// 1.25 tiles fit split sweeps of 64 sequences x 4097 keys (tp 2) and 32 x 2049
+// (tp 16), 512 units each: 1 split was best in both, 161 / 91 us against 177 / 109 us
+// with 2 and more with 3, 4 or 6.  Ties go to fewer splits.
 int decode_splits(int max_kv_len, int num_units, int num_sms, int hd, int G, int max_splits) {
   int per_sm = 1;
   cudaError_t e = cudaErrorNotSupported;
@@ -345,13 +354,9 @@ int decode_splits(int max_kv_len, int num_units, int num_sms, int hd, int G, int
   TP_OCC(128, 1) TP_OCC(128, 2) TP_OCC(128, 4) TP_OCC(128, 8)
   TP_OCC(64, 1) TP_OCC(64, 2) TP_OCC(64, 4) TP_OCC(64, 8)
 #undef TP_OCC
-  // 128-dim heads run on the tensor-core kernel: 128-key tiles, its own occupancy
-  int gran = 1, fixed = 96;
-  if (hd == 128) {
-    e = decode_tc_ctas_per_sm(G, &per_sm);
-    gran = 128;
-    fixed = 256;
-  }
+  // 128-dim heads run on the tensor-core kernel, with its own occupancy
+  if (hd == 128) e = decode_tc_ctas_per_sm(G, &per_sm);
+  const int gran = 1, fixed = 96;
   if (e != cudaSuccess) per_sm = 1;
   const long long resident = static_cast<long long>(num_sms) * per_sm;
   const int units = num_units > 0 ? num_units : 1;
@@ -361,6 +366,25 @@ int decode_splits(int max_kv_len, int num_units, int num_sms, int hd, int G, int
   if (limit < 1) limit = 1;
   int best = 1;
   long long best_cost = -1;
+  if (hd == 128) {
+    const long long tiles = (static_cast<long long>(max_kv_len) + 127) / 128;
+    if (limit > tiles) limit = static_cast<int>(tiles);  // every split holds a key tile
+    if (limit < 1) limit = 1;
+    long long nsat = resident * 36 / 100;
+    if (nsat < 1) nsat = 1;
+    for (int s = 1; s <= limit; ++s) {
+      const long long t = ((max_kv_len + s - 1) / s + 127) / 128;  // key tiles per split
+      const long long ctas = static_cast<long long>(units) * s;
+      const long long full = ctas / resident, rem = ctas % resident;
+      const long long weight = full * (resident > nsat ? resident : nsat) + (rem > 0 ? (rem > nsat ? rem : nsat) : 0);
+      const long long cost = (4 * t + 5) * weight;  // (tiles + 1.25) * weight, x4
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best = s;
+      }
+    }
+    return best;
+  }
   for (int s = 1; s <= limit; ++s) {
     const long long waves = (static_cast<long long>(units) * s + resident - 1) / resident;
     const long long per_split = ((max_kv_len + s - 1) / s + gran - 1) / gran * gran;
@@ -777,6 +801,11 @@ static cudaError_t prepare_decode_tc(int* ctas_per_sm) {
   if (occ == 0) {
     cudaError_t e = cudaFuncSetAttribute(attn_decode_tc_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DtcCfg<HD>::SMEM);
+    if (e != cudaSuccess) return e;
+    // all of the unified L1 / shared storage as shared memory: the occupancy below
+    // (and the split plan built on it) is then the one the launches get
+    e = cudaFuncSetAttribute(attn_decode_tc_kernel<HD, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_decode_tc_kernel<HD, G>, 192, DtcCfg<HD>::SMEM);
     if (e != cudaSuccess) return e;
