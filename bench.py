@@ -78,8 +78,8 @@ def workload_config(w: synth.Workload, n: int) -> dict:
 NCU_TRAFFIC = {
     ("qwen3_0.6b_layer_prefill2048", 2, "gemm_lm_head"): (311221504 + 2994944, "k_gemm.cu",
                                                           "60871d5f8a01c0f8"),
-    ("qwen3_0.6b_layer_decode64x4096", 2, "attn_decode"): (1077715712 + 3816960, "k_attention.cu",
-                                                            "805c1fd9119b17d0"),
+    ("qwen3_0.6b_layer_decode64x4096", 2, "attn_decode"): (1078256384 + 3111168, "k_attention.cu",
+                                                            "8f850ff8ed60af93"),
     ("qwen3_32b_layer_tp16_decode32x2048", 16, "gemm_lm_head"): (1558532864 + 3108608, "k_gemm.cu",
                                                                   "60871d5f8a01c0f8"),
 }
