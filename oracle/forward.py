@@ -5,7 +5,7 @@ TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  Everything computes in
 upcast exactly.  No blocking, fusion or reordering beyond what each definition
 states; library calls are limited to matmul and elementwise math.
 
-Readings taken where the pages are silent (each listed in the design doc):
+Readings taken where the pages are silent:
   * RMSNorm is x / sqrt(mean(x^2) + eps) * w (the pages import it, never show it).
   * RoPE is the rotate-half form: for d < hd/2, angle = p * theta^(-2d/hd),
     (a, b) = (u[d], u[d + hd/2]) -> (a cos - b sin, b cos + a sin).
