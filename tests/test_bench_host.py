@@ -58,3 +58,25 @@ def test_ncu_traffic_only_while_the_kernel_source_is_unchanged(monkeypatch):
     monkeypatch.setitem(bench.NCU_TRAFFIC, key, (1.0e6, "k_gemm.cu", "0" * 16))
     assert bench.ncu_traffic(*key) is None
     assert bench.ncu_traffic("no such workload", 2, "gemm_lm_head") is None
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one JSON
+    line with the keys the driver reads, on the tiny workload, without a GPU."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny_prefill8",
+                          "--steps", "1", "--warmup", "3"], cwd=root, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 3
+    assert d["config"]["workload"] == "tiny_prefill8"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
