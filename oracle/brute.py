@@ -13,7 +13,8 @@ from [TP] "Tensor parallelism from scratch", tp.py.
 from __future__ import annotations
 
 import math
-from typing import List, Sequence, Tuple
+import struct
+from typing import Callable, List, Optional, Sequence, Tuple
 
 Vec = List[float]
 Mat = List[List[float]]  # row-major [out][in]
@@ -50,12 +51,23 @@ def rope(u: Vec, p: int, theta: float) -> Vec:
     return out
 
 
+def bf16_value(x: float) -> float:
+    """x rounded to fp32 (struct's round to nearest), then to bf16: the upper 16 bits
+    with round to nearest, ties to even, on the bit pattern; finite inputs."""
+    u = struct.unpack("<I", struct.pack("<f", x))[0]
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFFFFFF
+    return struct.unpack("<f", struct.pack("<I", u & 0xFFFF0000))[0]
+
+
 def layer(x_rows: Sequence[Vec], w: dict, nq: int, nkv: int, hd: int, eps: float, theta: float,
-          k_cache: Sequence[Sequence[Vec]], v_cache: Sequence[Sequence[Vec]]
+          k_cache: Sequence[Sequence[Vec]], v_cache: Sequence[Sequence[Vec]],
+          store: Optional[Callable[[float], float]] = None
           ) -> Tuple[List[Vec], List[List[Vec]], List[List[Vec]]]:
     """x_rows: T new tokens (rows of length H).  k_cache[g][p] / v_cache[g][p]:
     cached rows of kv head g at position p.  w: dict of nested lists
-    (q, k, v, o, gate, up, down, in_norm, post_norm, q_norm, k_norm)."""
+    (q, k, v, o, gate, up, down, in_norm, post_norm, q_norm, k_norm).
+    store: what the cache keeps of each new K / V element (None: the value)."""
+    keep = store if store is not None else (lambda a: a)
     T = len(x_rows)
     ctx = len(k_cache[0]) if nkv else 0
     K = [list(k_cache[g]) for g in range(nkv)]
@@ -74,8 +86,8 @@ def layer(x_rows: Sequence[Vec], w: dict, nq: int, nkv: int, hd: int, eps: float
         qs.append(qh)
         for g in range(nkv):
             kv = rmsnorm(k[g * hd:(g + 1) * hd], w["k_norm"], eps)
-            K[g].append(rope(kv, pos, theta))
-            V[g].append(v[g * hd:(g + 1) * hd])
+            K[g].append([keep(a) for a in rope(kv, pos, theta)])
+            V[g].append([keep(a) for a in v[g * hd:(g + 1) * hd]])
     group = nq // nkv
     out_rows = []
     for t in range(T):

@@ -15,6 +15,11 @@ Readings taken where the pages are silent:
     keys may see keys 0 .. j + (S - T).
   * Uneven splits are errors (no silent short chunks); vocab slices use
     div_ceil and the last slice may be shorter, but none may be empty.
+  * The KV cache holds values in its own element type (``kv_dtype``): None keeps
+    the computing precision (the pages' fp32 demo), torch.bfloat16 is the bf16
+    cache the workloads name.  New K/V are rounded when appended (via fp32, round
+    to nearest even at each step) and attention reads what the cache holds, as
+    it does in tp.py (the cache is updated, then attention reads the cache).
   * Sequence parallelism splits the tokens into contiguous rank chunks as even
     as possible, the first T mod n ranks taking one token more (a rank may get
     none); the final norm runs on the chunks and an all-gather of the normed
@@ -117,6 +122,15 @@ def apply_rope(u: torch.Tensor, positions: torch.Tensor, theta: float) -> torch.
     return torch.cat([a * cos - b * sin, b * cos + a * sin], dim=-1)
 
 
+def cache_store(x: torch.Tensor, kv_dtype: Optional[torch.dtype]) -> torch.Tensor:
+    """The values a KV cache of element type ``kv_dtype`` holds for ``x``: x itself
+    when kv_dtype is None, else x rounded to fp32 and then to kv_dtype (round to
+    nearest, ties to even) and read back exactly."""
+    if kv_dtype is None:
+        return x
+    return x.to(torch.float32).to(kv_dtype).to(x.dtype)
+
+
 def silu(z: torch.Tensor) -> torch.Tensor:
     """silu(z) = z * sigmoid(z) = z / (1 + exp(-z))."""
     return z / (1.0 + torch.exp(-z))
@@ -164,13 +178,14 @@ def argmax_first(logits: torch.Tensor) -> torch.Tensor:
 # ---------------------------------------------------------------------------
 
 def decoder_layer(x: torch.Tensor, w: LayerWeights, shape: Shape,
-                  k_cache: torch.Tensor, v_cache: torch.Tensor, trace: Optional[dict] = None
-                  ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+                  k_cache: torch.Tensor, v_cache: torch.Tensor, trace: Optional[dict] = None,
+                  kv_dtype: Optional[torch.dtype] = None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """One decoder layer for one sequence, unsharded.
 
     x [T, H] are the sequence's T new tokens at positions ctx .. ctx+T-1 where
     ctx = k_cache.shape[1]; k_cache/v_cache [nkv, ctx, hd].  Returns the new
-    hidden [T, H] and the caches extended by T positions.
+    hidden [T, H] and the caches extended by T positions (the new K and V as a
+    cache of element type kv_dtype holds them; ``trace`` gets them unrounded).
     ([TP] TPTransformer.forward loop body: x = x + attn(ln1(x)); x = x + mlp(ln2(x)).)
     """
     T = x.shape[0]
@@ -185,8 +200,8 @@ def decoder_layer(x: torch.Tensor, w: LayerWeights, shape: Shape,
     k = rms_norm(k, w.k_norm, shape.rms_eps)
     q = apply_rope(q, pos, shape.rope_theta)
     k = apply_rope(k, pos, shape.rope_theta)
-    K = torch.cat([k_cache, k], dim=1)
-    V = torch.cat([v_cache, v], dim=1)
+    K = torch.cat([k_cache, cache_store(k, kv_dtype)], dim=1)
+    V = torch.cat([v_cache, cache_store(v, kv_dtype)], dim=1)
     o = causal_gqa_attention(q, K, V)
     x = x + o.transpose(0, 1).reshape(T, nq * hd) @ w.o.T
     h2 = rms_norm(x, w.post_norm, shape.rms_eps)
@@ -408,7 +423,8 @@ def tp_embed(ids: torch.Tensor, hw: HeadWeights, shape: Shape, n: int, comm: Com
 
 
 def tp_decoder_layer(x: torch.Tensor, ranks: Sequence[RankLayer], shape: Shape,
-                     k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor], comm: Comm
+                     k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor], comm: Comm,
+                     kv_dtype: Optional[torch.dtype] = None
                      ) -> Tuple[torch.Tensor, List[torch.Tensor], List[torch.Tensor]]:
     """One layer under tensor parallelism for one sequence.
 
@@ -431,8 +447,8 @@ def tp_decoder_layer(x: torch.Tensor, ranks: Sequence[RankLayer], shape: Shape,
         v = qkv[:, nq_w + nkv_w:].reshape(T, rl.nkv_l, hd).transpose(0, 1)
         q = apply_rope(rms_norm(q, rl.q_norm, eps), pos, shape.rope_theta)
         k = apply_rope(rms_norm(k, rl.k_norm, eps), pos, shape.rope_theta)
-        K = torch.cat([k_caches[r], k], dim=1)
-        V = torch.cat([v_caches[r], v], dim=1)
+        K = torch.cat([k_caches[r], cache_store(k, kv_dtype)], dim=1)
+        V = torch.cat([v_caches[r], cache_store(v, kv_dtype)], dim=1)
         o = causal_gqa_attention(q, K, V)
         attn_partials.append(o.transpose(0, 1).reshape(T, nq_w) @ rl.o.T)
         new_k.append(K)
@@ -487,7 +503,8 @@ def sp_embed(ids: torch.Tensor, hw: HeadWeights, shape: Shape, n: int, comm: Com
 
 
 def sp_decoder_layer(x_chunks: Sequence[torch.Tensor], ranks: Sequence[RankLayer], shape: Shape,
-                     k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor], comm: Comm
+                     k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor], comm: Comm,
+                     kv_dtype: Optional[torch.dtype] = None
                      ) -> Tuple[List[torch.Tensor], List[torch.Tensor], List[torch.Tensor]]:
     """One layer under tensor + sequence parallelism for one sequence.  Rank r
     holds x_chunks[r], the residual rows of its token chunk; the column GEMMs
@@ -507,8 +524,8 @@ def sp_decoder_layer(x_chunks: Sequence[torch.Tensor], ranks: Sequence[RankLayer
         v = qkv[:, nq_w + nkv_w:].reshape(T, rl.nkv_l, hd).transpose(0, 1)
         q = apply_rope(rms_norm(q, rl.q_norm, eps), pos, shape.rope_theta)
         k = apply_rope(rms_norm(k, rl.k_norm, eps), pos, shape.rope_theta)
-        K = torch.cat([k_caches[r], k], dim=1)
-        V = torch.cat([v_caches[r], v], dim=1)
+        K = torch.cat([k_caches[r], cache_store(k, kv_dtype)], dim=1)
+        V = torch.cat([v_caches[r], cache_store(v, kv_dtype)], dim=1)
         o = causal_gqa_attention(q, K, V)
         attn_partials.append(o.transpose(0, 1).reshape(T, nq_w) @ rl.o.T)
         new_k.append(K)
@@ -579,16 +596,20 @@ class SeqInput:
 @dataclasses.dataclass
 class SeqOutput:
     hidden: torch.Tensor                    # [T, H] after the last layer run
-    k_cache: List[torch.Tensor]             # extended caches, global heads
+    k_cache: List[torch.Tensor]             # extended caches, global heads (as the cache holds them)
     v_cache: List[torch.Tensor]
     logits: Optional[torch.Tensor] = None   # [V] for the last position
     next_id: Optional[int] = None
+    k_new: Optional[List[torch.Tensor]] = None  # per layer, the new positions' K / V [nkv, T, hd] before
+    v_new: Optional[List[torch.Tensor]] = None  # the cache stored them (unsharded runs)
 
 
 def run_sequence(seq: SeqInput, layers: Sequence[LayerWeights], hw: Optional[HeadWeights],
-                 shape: Shape, n: int = 0, comm: Optional[Comm] = None, head: bool = True) -> SeqOutput:
+                 shape: Shape, n: int = 0, comm: Optional[Comm] = None, head: bool = True,
+                 kv_dtype: Optional[torch.dtype] = None) -> SeqOutput:
     """Embedding (if ids) -> layers -> (if hw and head) final norm, logits of the
-    last position, argmax.  n == 0 runs unsharded; n >= 1 runs the TP emulation."""
+    last position, argmax.  n == 0 runs unsharded; n >= 1 runs the TP emulation.
+    kv_dtype: element type of the KV cache (None: the computing precision)."""
     tp = n >= 1
     if tp:
         validate_tp(shape, n)
@@ -596,20 +617,23 @@ def run_sequence(seq: SeqInput, layers: Sequence[LayerWeights], hw: Optional[Hea
     x = seq.hidden
     if seq.ids is not None:
         x = tp_embed(seq.ids, hw, shape, n, comm) if tp else embed(seq.ids, hw)
-    ks, vs = [], []
+    ks, vs, k_new, v_new = [], [], [], []
     for li, w in enumerate(layers):
         if tp:
             ranks = [shard_layer(w, shape, n, r) for r in range(n)]
             kc = split_kv_by_rank(seq.k_cache[li], shape, n)
             vc = split_kv_by_rank(seq.v_cache[li], shape, n)
-            x, nk, nv = tp_decoder_layer(x, ranks, shape, kc, vc, comm)
+            x, nk, nv = tp_decoder_layer(x, ranks, shape, kc, vc, comm, kv_dtype)
             ks.append(_merge_kv(nk, shape, n))
             vs.append(_merge_kv(nv, shape, n))
         else:
-            x, K, V = decoder_layer(x, w, shape, seq.k_cache[li], seq.v_cache[li])
+            tr: dict = {}
+            x, K, V = decoder_layer(x, w, shape, seq.k_cache[li], seq.v_cache[li], tr, kv_dtype)
             ks.append(K)
             vs.append(V)
-    out = SeqOutput(hidden=x, k_cache=ks, v_cache=vs)
+            k_new.append(tr["k"])
+            v_new.append(tr["v"])
+    out = SeqOutput(hidden=x, k_cache=ks, v_cache=vs, k_new=None if tp else k_new, v_new=None if tp else v_new)
     if hw is not None and head:
         logits = tp_lm_head(x[-1], hw, shape, n, comm) if tp else lm_head(x[-1], hw, shape)
         out.logits = logits
@@ -627,7 +651,8 @@ class SpSeqOutput:
 
 
 def run_sequence_sp(seq: SeqInput, layers: Sequence[LayerWeights], hw: Optional[HeadWeights], shape: Shape,
-                    n: int, comm: Optional[Comm] = None, head: bool = True) -> SpSeqOutput:
+                    n: int, comm: Optional[Comm] = None, head: bool = True,
+                    kv_dtype: Optional[torch.dtype] = None) -> SpSeqOutput:
     """run_sequence under tensor + sequence parallelism: the residual stream
     lives as token chunks (hidden rows given as input are split the same way)."""
     validate_tp(shape, n)
@@ -642,7 +667,7 @@ def run_sequence_sp(seq: SeqInput, layers: Sequence[LayerWeights], hw: Optional[
         ranks = [shard_layer(w, shape, n, r) for r in range(n)]
         kc = split_kv_by_rank(seq.k_cache[li], shape, n)
         vc = split_kv_by_rank(seq.v_cache[li], shape, n)
-        x, nk, nv = sp_decoder_layer(x, ranks, shape, kc, vc, comm)
+        x, nk, nv = sp_decoder_layer(x, ranks, shape, kc, vc, comm, kv_dtype)
         ks.append(_merge_kv(nk, shape, n))
         vs.append(_merge_kv(nv, shape, n))
     out = SpSeqOutput(hidden_chunks=x, k_cache=ks, v_cache=vs)
@@ -653,7 +678,8 @@ def run_sequence_sp(seq: SeqInput, layers: Sequence[LayerWeights], hw: Optional[
 
 
 def greedy_generate(prompt: torch.Tensor, layers: Sequence[LayerWeights], hw: HeadWeights, shape: Shape,
-                    steps: int, n: int = 0, comm: Optional[Comm] = None) -> Tuple[List[int], List[float], torch.Tensor]:
+                    steps: int, n: int = 0, comm: Optional[Comm] = None,
+                    kv_dtype: Optional[torch.dtype] = None) -> Tuple[List[int], List[float], torch.Tensor]:
     """Greedy generation as in "Tensor parallelism from scratch", tp.py main: one
     forward over the prompt with an empty cache, then ``steps`` times: take the
     argmax (first index on ties) of the last position's logits, append it, and run
@@ -662,7 +688,7 @@ def greedy_generate(prompt: torch.Tensor, layers: Sequence[LayerWeights], hw: He
     n >= 1 runs every forward through the TP emulation (the page compares the two)."""
     empty = [torch.zeros(shape.num_kv_heads, 0, shape.head_dim, dtype=DTYPE) for _ in layers]
     out = run_sequence(SeqInput(hidden=None, ids=prompt, k_cache=list(empty), v_cache=list(empty)), layers, hw,
-                       shape, n=n, comm=comm)
+                       shape, n=n, comm=comm, kv_dtype=kv_dtype)
     tokens: List[int] = []
     margins: List[float] = []
     for _ in range(steps):
@@ -670,7 +696,7 @@ def greedy_generate(prompt: torch.Tensor, layers: Sequence[LayerWeights], hw: He
         tokens.append(out.next_id)
         margins.append(float(top2[0] - top2[1]))
         out = run_sequence(SeqInput(hidden=None, ids=torch.tensor([out.next_id]), k_cache=out.k_cache,
-                                    v_cache=out.v_cache), layers, hw, shape, n=n, comm=comm)
+                                    v_cache=out.v_cache), layers, hw, shape, n=n, comm=comm, kv_dtype=kv_dtype)
     return tokens, margins, out.logits
 
 

@@ -32,9 +32,13 @@ def layer_weights(s: synth.ModelShape, layer: int, perturbed_norms: bool = False
                         q_norm=g(synth.W_Q_NORM), k_norm=g(synth.W_K_NORM))
 
 
-def head_weights(s: synth.ModelShape, perturbed_norms: bool = False, dtype=DTYPE) -> HeadWeights:
-    emb = from_bf16_bits(synth.global_weight_bits(s, synth.W_EMBED), dtype)
-    lm = emb if s.tie_word_embeddings else from_bf16_bits(synth.global_weight_bits(s, synth.W_LM_HEAD), dtype)
+def head_weights(s: synth.ModelShape, perturbed_norms: bool = False, dtype=DTYPE,
+                 need_embed: bool = True) -> HeadWeights:
+    """The embedding, LM head and final norm.  need_embed=False leaves out an
+    untied embedding table (for steps that start from hidden states)."""
+    tied = s.tie_word_embeddings
+    emb = from_bf16_bits(synth.global_weight_bits(s, synth.W_EMBED), dtype) if (tied or need_embed) else None
+    lm = emb if tied else from_bf16_bits(synth.global_weight_bits(s, synth.W_LM_HEAD), dtype)
     fn = from_bf16_bits(synth.global_weight_bits(s, synth.W_FINAL_NORM, perturbed_norms), dtype)
     return HeadWeights(embed=emb, lm_head=lm, final_norm=fn)
 

@@ -143,6 +143,45 @@ def test_decoder_layer_matches_brute_force_loops():
     assert torch.allclose(V, torch.tensor(bV, dtype=D), atol=0)
 
 
+def test_cache_store_rounds_like_independent_bf16_conversions():
+    """cache_store(x, bfloat16) is x rounded to fp32, then to bf16 with round to
+    nearest, ties to even: checked against the input generator's bit-level rounding
+    (numpy) and the brute-force scalar one, on random values and on exact ties
+    (an odd last bf16 bit rounds up, an even one down)."""
+    g = torch.Generator().manual_seed(11)
+    x = torch.cat([torch.randn(10000, dtype=D, generator=g) * 3,
+                   torch.tensor([1 + 2**-8, 1 + 3 * 2**-8, -(2 + 2**-7), 0.5 + 2**-10], dtype=D)])
+    got = of.cache_store(x, torch.bfloat16)
+    ref = synth.bf16_bits_to_f32(synth._f32_to_bf16_bits(x.numpy().astype(np.float32)))
+    assert np.array_equal(got.numpy(), ref.astype(np.float64))
+    assert [brute.bf16_value(float(v)) for v in x] == got.tolist()
+    assert got[-4:].tolist() == [1.0, 1 + 4 * 2**-8, -2.0, 0.5]
+    assert torch.equal(of.cache_store(x, None), x)
+
+
+def test_bf16_cache_layer_matches_brute_force_loops():
+    """With a bf16 cache the new K / V are stored rounded and attention reads the
+    stored values: the layer equals the scalar loops that round what they append,
+    the returned cache holds the rounded values, the trace the unrounded ones, and
+    the output differs from that of a cache in full precision."""
+    w = _tiny_weights(TINY, 5)
+    g = torch.Generator().manual_seed(6)
+    x = torch.randn(3, 32, dtype=D, generator=g)
+    kc = of.cache_store(torch.randn(2, 4, 8, dtype=D, generator=g), torch.bfloat16)
+    vc = of.cache_store(torch.randn(2, 4, 8, dtype=D, generator=g), torch.bfloat16)
+    tr = {}
+    y, K, V = of.decoder_layer(x, w, TINY, kc, vc, tr, torch.bfloat16)
+    by, bK, bV = brute.layer(x.tolist(), _as_lists(w), 4, 2, 8, TINY.rms_eps, TINY.rope_theta,
+                             kc.tolist(), vc.tolist(), store=brute.bf16_value)
+    assert torch.allclose(y, torch.tensor(by, dtype=D), rtol=1e-12, atol=1e-12)
+    assert torch.equal(K, torch.tensor(bK, dtype=D)) and torch.equal(V, torch.tensor(bV, dtype=D))
+    assert torch.equal(K[:, 4:], of.cache_store(tr["k"], torch.bfloat16))
+    assert torch.equal(V[:, 4:], of.cache_store(tr["v"], torch.bfloat16))
+    assert not torch.equal(K[:, 4:], tr["k"])
+    y_full, _, _ = of.decoder_layer(x, w, TINY, kc, vc)
+    assert float((y - y_full).abs().max()) > 1e-6
+
+
 def test_head_matches_brute_force():
     g = torch.Generator().manual_seed(7)
     hw = of.HeadWeights(embed=torch.randn(50, 32, dtype=D, generator=g), lm_head=None,

@@ -2,40 +2,63 @@
 shard rules of "Tensor parallelism from scratch" allow (kv-head replication, uneven
 vocab slices, tied or untied heads), random tp sizes, token counts and cached
 lengths, the all-reduce TP emulation and the sequence-parallel form both equal the
-unsharded forward, which is itself pinned against brute force."""
+unsharded forward, which is itself pinned against brute force.
+
+The cases come from a seeded generator of their own (always run), and, where the
+``hypothesis`` package is installed, also from its search."""
+
+import random
 
 import pytest
 import torch
 
 from oracle import forward as of
 
-hypothesis = pytest.importorskip("hypothesis")
-st = hypothesis.strategies
+try:
+    import hypothesis
+    st = hypothesis.strategies
+except ImportError:  # the seeded cases below still run
+    hypothesis = None
 
 D = torch.float64
 
 
-@st.composite
-def cases(draw):
-    nkv = draw(st.sampled_from([1, 2, 4]))
-    group = draw(st.sampled_from([1, 2, 4]))
+def _case(pick, assume):
+    """One case from a chooser pick(kind, options) and a rejection hook assume(cond)."""
+    nkv = pick("choice", [1, 2, 4])
+    group = pick("choice", [1, 2, 4])
     nq = nkv * group
-    n = draw(st.sampled_from([d for d in (1, 2, 4, 8) if nq % d == 0]))
-    hd = draw(st.sampled_from([8, 12, 16]))
-    hidden = draw(st.sampled_from([16, 32, 48]))
-    inter = n * draw(st.integers(1, 6)) * 4
-    vocab = draw(st.integers(2 * n + 1, 97))
-    tied = draw(st.booleans())
+    n = pick("choice", [d for d in (1, 2, 4, 8) if nq % d == 0])
+    hd = pick("choice", [8, 12, 16])
+    hidden = pick("choice", [16, 32, 48])
+    inter = n * pick("int", (1, 6)) * 4
+    vocab = pick("int", (2 * n + 1, 97))
+    tied = pick("choice", [False, True])
     shape = of.Shape(hidden=hidden, num_q_heads=nq, num_kv_heads=nkv, head_dim=hd, intermediate=inter,
                      vocab=vocab, num_layers=2, tie_word_embeddings=tied)
     try:
         of.validate_tp(shape, n)
     except of.ShardError:
-        hypothesis.assume(False)
-    T = draw(st.integers(1, 9))
-    ctx = draw(st.integers(0, 6))
-    seed = draw(st.integers(0, 2**31 - 1))
+        assume(False)
+        return None
+    T = pick("int", (1, 9))
+    ctx = pick("int", (0, 6))
+    seed = pick("int", (0, 2**31 - 1))
     return shape, n, T, ctx, seed
+
+
+def _seeded_cases(count: int, seed: int = 20251202):
+    rng = random.Random(seed)
+
+    def pick(kind, opts):
+        return rng.choice(opts) if kind == "choice" else rng.randint(*opts)
+
+    out = []
+    while len(out) < count:
+        c = _case(pick, lambda ok: None)
+        if c is not None:
+            out.append(c)
+    return out
 
 
 def _inputs(shape, T, ctx, seed):
@@ -59,9 +82,7 @@ def _close(a, b):
     return a.shape == b.shape and float((a - b).abs().max()) <= 1e-11 * scale
 
 
-@hypothesis.settings(max_examples=40, deadline=None, derandomize=True)
-@hypothesis.given(cases())
-def test_sharded_forms_equal_the_unsharded_forward(case):
+def _check(case):
     shape, n, T, ctx, seed = case
     layers, hw, seq = _inputs(shape, T, ctx, seed)
     ref = of.run_sequence(seq, layers, hw, shape, n=0)
@@ -76,3 +97,32 @@ def test_sharded_forms_equal_the_unsharded_forward(case):
     assert tp.next_id == ref.next_id == sp.next_id
     for a, b in zip(tp.k_cache + tp.v_cache + sp.k_cache + sp.v_cache, 2 * (ref.k_cache + ref.v_cache)):
         assert _close(a, b)
+
+
+SEEDED = _seeded_cases(40)
+
+
+@pytest.mark.parametrize("case", SEEDED, ids=[f"n{c[1]}-nq{c[0].num_q_heads}-nkv{c[0].num_kv_heads}-T{c[2]}-ctx{c[3]}"
+                                              for c in SEEDED])
+def test_sharded_forms_equal_the_unsharded_forward_seeded(case):
+    _check(case)
+
+
+def test_seeded_cases_cover_replication_uneven_vocab_and_both_head_kinds():
+    assert any(c[0].num_kv_heads < c[1] for c in SEEDED)           # kv heads replicated
+    assert any(c[0].vocab % c[1] for c in SEEDED)                   # uneven vocab slices
+    assert {c[0].tie_word_embeddings for c in SEEDED} == {False, True}
+    assert {c[1] for c in SEEDED} >= {1, 2, 4}
+
+
+if hypothesis is not None:
+    @st.composite
+    def cases(draw):
+        def pick(kind, opts):
+            return draw(st.sampled_from(opts)) if kind == "choice" else draw(st.integers(*opts))
+        return _case(pick, hypothesis.assume)
+
+    @hypothesis.settings(max_examples=40, deadline=None, derandomize=True)
+    @hypothesis.given(cases())
+    def test_sharded_forms_equal_the_unsharded_forward(case):
+        _check(case)
