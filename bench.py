@@ -4,9 +4,12 @@
 A step is one pass of the whole hot path over one batch: vocab-parallel
 embedding of the step's token ids, the decoder layer(s) (every rank shard of
 the tensor-parallel layer, rank-sums in the row-parallel GEMM epilogues), the
-final norm, the vocab-parallel LM head and the argmax.  Default workload: one
-Qwen3-0.6B-shaped layer, prefill 1 x 2048 tokens, tp_size 2 emulated on one
-GPU.  Prints one JSON line.
+final norm, the vocab-parallel LM head and the argmax.  Default workload: the
+full 28-layer Qwen3-0.6B-shaped model on a mixed batch (4 prefill sequences of
+512 tokens + 128 decode sequences at 2048 cached tokens), tp_size 2 emulated on
+one GPU.  Prints one JSON line; its "workloads" key holds the same measurement
+(step time, tokens/s, each kernel's roofline fraction) for the other
+configurations, taken in the same run.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--tp N]
@@ -36,7 +39,16 @@ import torch.distributed as dist  # noqa: E402
 
 import synth  # noqa: E402
 
-DEFAULT_WORKLOAD = "qwen3_0.6b_layer_prefill2048"
+DEFAULT_WORKLOAD = "qwen3_0.6b_model_mixed"
+DEFAULT_TP = 2
+# measured in the same run as the main line, one after another (each frees its
+# buffers before the next is built)
+# (workload, tp_size, page size of a paged KV cache or 0 for the contiguous one)
+SUB_RECORDS = (("qwen3_0.6b_layer_prefill2048", 1, 0), ("qwen3_0.6b_layer_prefill2048", 2, 0),
+               ("qwen3_0.6b_layer_decode64x4096", 1, 0), ("qwen3_0.6b_layer_decode64x4096", 2, 0),
+               ("qwen3_0.6b_layer_decode64x4096", 4, 0), ("qwen3_0.6b_layer_decode64x4096", 2, 128),
+               ("qwen3_32b_layer_tp16_decode32x2048", 16, 0), ("qwen3_32b_layer_tp16_prefill1024", 16, 0),
+               ("qwen3_0.6b_model_mixed", 1, 0), ("qwen3_0.6b_model_mixed", 4, 0))
 METRIC = "tokens/sec per layer-forward (prefill & decode) on 1 GB300; % HBM BW / % TC peak"
 L2_FLUSH_BYTES = 256 << 20
 # tensor-core operands fp16 (weights converted from bf16 at shard time) and bf16
@@ -105,33 +117,61 @@ def ncu_traffic(workload: str, n: int, kernel: str):
 
 
 def kernel_work(kind: str, w: synth.Workload, n: int):
+    """(flops, bytes) of one launch of a kernel kind: the algorithmic work of all
+    emulated ranks (weights fp16, residual stream fp32, fp16 operand rows with their
+    32-column sums of squares, bf16 KV cache)."""
     s = w.shape
     T, H, hd, I, V = w.num_tokens, s.hidden, s.head_dim, s.intermediate, s.vocab
     nq_l = s.num_q_heads // n
     nkv_l = s.num_kv_heads // n if s.num_kv_heads >= n else 1
     B = w.num_seqs
+    nqkv = n * (nq_l + 2 * nkv_l) * hd   # merged QKV outputs of all ranks (replicated kv heads counted)
+    nqo = s.num_q_heads * hd
+    rows_in = T * H * 2 + T * (H // 32) * 4            # fp16 operand rows + their sums of squares
+    resid = T * H * (4 + 4 + 2) + T * (H // 32) * 4    # residual read + write, next fp16 rows + sums
     if kind == "gemm_qkv":
-        return "tensor", 2.0 * T * H * n * (nq_l + 2 * nkv_l) * hd
+        return 2.0 * T * H * nqkv, float(nqkv * H * 2 + rows_in + T * nqkv * 2)
     if kind == "gemm_o":
-        return "tensor", 2.0 * T * H * s.num_q_heads * hd
+        return 2.0 * T * nqo * H, float(H * nqo * 2 + T * nqo * 2 + resid)
     if kind == "gemm_gate_up":
-        return "tensor", 2.0 * T * H * 2 * I
+        return 2.0 * T * H * 2 * I, float(2 * I * H * 2 + rows_in + T * I * 2)
     if kind == "gemm_down":
-        return "tensor", 2.0 * T * I * H
+        return 2.0 * T * I * H, float(H * I * 2 + T * I * 2 + resid)
     if kind == "attn_prefill":
-        f = 0.0
+        f, by = 0.0, 0.0
         for q, c in w.prefill:
             f += 4.0 * hd * s.num_q_heads * (q * c + q * (q + 1) / 2)
-        return "tensor", f
+            by += q * nqo * (2 + 2 + 2) + (c + q) * n * nkv_l * hd * 2 * 2   # q hi/lo + out; K and V
+        return f, by
     if kind == "attn_decode":
-        return "hbm", float(sum(c + 1 for c in w.decode)) * n * nkv_l * hd * 2 * 2
+        keys = float(sum(c + 1 for c in w.decode))
+        return 4.0 * hd * s.num_q_heads * keys, keys * n * nkv_l * hd * 2 * 2
     if kind == "gemm_lm_head":
-        return "hbm", float(V) * H * 2 + B * H * 2
-    if kind in ("embed", "rmsnorm"):
-        return "hbm", float(T) * H * 2 * 2
-    if kind == "rope":
-        return "hbm", float(T) * n * (nq_l + 2 * nkv_l) * hd * 2 * 2
-    return "hbm", 0.0
+        return 2.0 * B * V * H, float(V) * H * 2 + B * H * 2
+    if kind == "embed":  # bf16 table row in; fp32 residual row and its fp16 copy out
+        return 0.0, float(T) * H * (2 + 4 + 2)
+    if kind == "rmsnorm":  # fp32 residual row in; fp16 row and sums out
+        return 0.0, float(T) * H * (4 + 2)
+    if kind == "final_norm":
+        return 0.0, float(B) * H * (4 + 2)
+    return 0.0, 0.0
+
+
+def kernel_roofline(kind: str, w: synth.Workload, n: int, ms_per_launch: float, pk: dict) -> dict:
+    """The kernel's bound (the larger of its tensor-core time at the sustained bf16 peak
+    and its HBM time at the measured copy bandwidth), the rate it achieved against
+    that bound and the fraction of the peak."""
+    flops, by = kernel_work(kind, w, n)
+    t_tc = flops / (pk["bf16_tflops_sustained"] * 1e12)
+    t_hbm = by / (pk["hbm_gbs"] * 1e9)
+    sec = ms_per_launch / 1e3
+    if t_tc >= t_hbm and flops > 0:
+        ach = flops / sec / 1e12
+        return {"bound": "tensor", "achieved": round(ach, 2), "unit": "TFLOP/s",
+                "frac": round(ach / pk["bf16_tflops_sustained"], 4), "roofline_us": round(t_tc * 1e6, 2)}
+    ach = by / sec / 1e9 if sec > 0 else 0.0
+    return {"bound": "hbm", "achieved": round(ach, 2), "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
+            "roofline_us": round(t_hbm * 1e6, 2)}
 
 
 # ---------------------------------------------------------------------------
@@ -312,7 +352,7 @@ def job_throughput(tokens_per_step: int, world: int, ms_per_step: float) -> floa
     return world * tokens_per_step / (ms_per_step / 1e3)
 
 
-def build_runner(w: synth.Workload, n: int):
+def build_runner(w: synth.Workload, n: int, page_size: int = 0):
     import synth.device as sd
     from tensor_transformer_forward_gb300 import ModelConfig
     from tensor_transformer_forward_gb300.runner import TPRunner
@@ -321,7 +361,7 @@ def build_runner(w: synth.Workload, n: int):
                       s.rms_eps, s.rope_theta, n, s.tie_word_embeddings)
     q, c = w.q_lens, w.ctx_lens
     cap = (max(a + b for a, b in zip(q, c)) + 63) // 64 * 64
-    r = TPRunner(cfg, w.layers_run, w.num_seqs, cap, w.num_tokens)
+    r = TPRunner(cfg, w.layers_run, w.num_seqs, cap, w.num_tokens, page_size=page_size)
     for li in range(w.layers_run):
         full = sd.layer_weights(s, li)
         r.load_layer(li, full)
@@ -329,36 +369,126 @@ def build_runner(w: synth.Workload, n: int):
     r.load_head(sd.head_weights(s))
     hmap = r.kv_head_map()
     fill = max(c)
+    contig = None
     for li in range(w.layers_run):
         if fill > 0:
-            sd.fill_kv_cache(r.kv[li], n, w.num_seqs, r.nkv_l, cap, s.head_dim, hmap, s.num_kv_heads, li,
-                             w.num_seqs, fill)
+            if page_size:  # generated in the contiguous layout, then copied into the pages
+                if contig is None:
+                    contig = torch.zeros(r.ctx.kv_cache_bytes(w.num_seqs, cap), dtype=torch.uint8, device="cuda")
+                sd.fill_kv_cache(contig, n, w.num_seqs, r.nkv_l, cap, s.head_dim, hmap, s.num_kv_heads, li,
+                                 w.num_seqs, fill)
+                r.load_kv_contiguous(li, contig)
+            else:
+                sd.fill_kv_cache(r.kv[li], n, w.num_seqs, r.nkv_l, cap, s.head_dim, hmap, s.num_kv_heads, li,
+                                 w.num_seqs, fill)
+    del contig
     batch = r.make_batch(q, c, list(range(w.num_seqs)), num_prefill=len(w.prefill))
     ids = sd.token_ids(w.num_tokens, s.vocab)
     return r, batch, ids
 
 
+class L2Flush:
+    """Between timed steps: write a buffer larger than L2, then read another one, so
+    that the dirty lines of the write are evicted (their write-back lands here,
+    outside the timed step) and L2 holds only data the step never uses."""
+
+    def __init__(self):
+        self.dst = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.src = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+
+    def __call__(self):
+        self.dst.zero_()
+        self.src.sum()
+
+
+def kernel_table(prof: dict, steps: int, w: synth.Workload, n: int, pk: dict) -> dict:
+    """Per kernel kind: device time per step and per launch and its roofline."""
+    out = {}
+    for k, (ms, cnt) in sorted(prof.items(), key=lambda kv: -kv[1][0]):
+        per_launch = ms / max(cnt, 1)
+        rec = {"us_per_step": round(ms / steps * 1e3, 2), "launches_per_step": round(cnt / steps, 2),
+               "us_per_launch": round(per_launch * 1e3, 2)}
+        rec.update(kernel_roofline(k, w, n, per_launch, pk))
+        out[k] = rec
+    return out
+
+
+def step_roofline_us(w: synth.Workload, n: int, launches: dict, pk: dict) -> float:
+    """Sum over the step's kernels of max(flops / tensor peak, bytes / HBM bandwidth)."""
+    t = 0.0
+    for k, per_step in launches.items():
+        flops, by = kernel_work(k, w, n)
+        t += per_step * max(flops / (pk["bf16_tflops_sustained"] * 1e12), by / (pk["hbm_gbs"] * 1e9))
+    return t * 1e6
+
+
+def sub_record(name: str, n: int, pk: dict, flush, page_size: int = 0) -> dict:
+    """One configuration measured the way the main line is: L2 flushed between
+    steps, CUDA events around each step (no per-kernel events), then a second pass
+    with events around every launch for the per-kernel table."""
+    w = synth.WORKLOADS[name]
+    r, batch, ids = build_runner(w, n, page_size)
+    T, B = w.num_tokens, w.num_seqs
+    hidden = torch.empty(T, w.shape.hidden, dtype=torch.float32, device="cuda")
+    out_ids = torch.empty(B, dtype=torch.int32, device="cuda")
+
+    def step():
+        r.step(batch, ids=ids, hidden=hidden, out_ids=out_ids)
+
+    step()
+    torch.cuda.synchronize()
+    r.check_status()
+    t0 = time.perf_counter()
+    for _ in range(3):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    est = (time.perf_counter() - t0) / 3
+    steps = max(10, min(200, int(0.15 / max(est, 1e-6))))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        flush()
+        a.record()
+        step()
+        b.record()
+    torch.cuda.synchronize()
+    times = sorted(a.elapsed_time(b) for a, b in ev)
+    ms = sum(times) / steps
+    psteps = min(steps, 20)
+    r.ctx.profile_begin(list(__import__("tensor_transformer_forward_gb300").binding.KERNELS))
+    for _ in range(psteps):
+        flush()
+        step()
+    prof = r.ctx.profile_end()
+    r.check_status()
+    table = kernel_table(prof, psteps, w, n, pk)
+    roof = step_roofline_us(w, n, {k: v["launches_per_step"] for k, v in table.items()}, pk)
+    rec = {"workload": name, "tp_size": n, "kv_cache": f"paged, {page_size}-position pages" if page_size else "contiguous",
+           "tokens_per_step": T, "steps": steps, "ms_per_step": round(ms, 5),
+           "tokens_per_s": round(T / (ms / 1e3), 1),
+           "step_ms_p10_p50_p90": [round(times[len(times) // 10], 5), round(times[len(times) // 2], 5),
+                                   round(times[9 * len(times) // 10], 5)],
+           "step_roofline_us": round(roof, 2), "step_roofline_frac": round(roof / (ms * 1e3), 4),
+           "dominant": next(iter(table)), "kernels": table}
+    del r, batch, ids, hidden, out_ids
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_ours(args, w: synth.Workload, n: int, rank: int, world: int) -> dict:
     dev = torch.cuda.current_device()
+    pk = peaks()
+    flush_l2 = L2Flush()
     r, batch, ids = build_runner(w, n)
     ctx = r.ctx
     T, H, B = w.num_tokens, w.shape.hidden, w.num_seqs
     hidden = torch.empty(T, H, dtype=torch.float32, device="cuda")
     out_ids = torch.empty(B, dtype=torch.int32, device="cuda")
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    flush_src = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
-
-    def flush_l2():
-        # write a buffer larger than L2, then read another one: the read evicts the
-        # dirty lines of the write, so their write-back lands here, outside the
-        # timed step, and L2 is left holding only data the step never uses
-        flush.zero_()
-        flush_src.sum()
 
     def step():
         r.step(batch, ids=ids, hidden=hidden, out_ids=out_ids)
 
-    # untimed: which kernel dominates the step
+    # untimed: which kernel dominates the step, and every kernel's share
     step()
     torch.cuda.synchronize()
     r.check_status()
@@ -368,7 +498,7 @@ def run_ours(args, w: synth.Workload, n: int, rank: int, world: int) -> dict:
         step()
     prof = ctx.profile_end()
     dominant = max(prof, key=lambda k: prof[k][0])
-    breakdown = {k: round(v[0] / 5 * 1e3, 2) for k, v in sorted(prof.items(), key=lambda kv: -kv[1][0])}
+    table = kernel_table(prof, 5, w, n, pk)
 
     for _ in range(args.warmup):
         flush_l2()
@@ -397,35 +527,28 @@ def run_ours(args, w: synth.Workload, n: int, rank: int, world: int) -> dict:
     # second timed pass over the same steps, with events around each launch of the
     # dominant kernel: events between two kernels split their programmatic-launch
     # overlap, so the step times above are taken without them
-    ctx.profile_begin([dominant], max_launches=max(64, 8 * args.steps))
+    ctx.profile_begin([dominant], max_launches=max(64, 64 * args.steps))
     for i in range(args.steps):
         flush_l2()
         step()
     torch.cuda.synchronize()
     dom = ctx.profile_end()
-    clk = clocks.stop()
     r.check_status()
     step_ms = sorted(s.elapsed_time(e) for s, e in zip(starts, ends))
     ms = sum(step_ms) / args.steps
     ms_max = max_over_ranks(ms, world)
 
     # roofline of the dominant kernel, timed live in the timed region
-    pk = peaks()
-    bound, work = kernel_work(dominant, w, n)
     dms, dcount = dom.get(dominant, (0.0, 0))
-    avg_s = dms / max(dcount, 1) / 1e3
-    if bound == "tensor":
-        achieved = work / avg_s / 1e12
-        peak = pk["bf16_tflops_sustained"]
-        unit = "TFLOP/s"
-    else:
-        achieved = work / avg_s / 1e9
-        peak = pk["hbm_gbs"]
-        unit = "GB/s"
-    roofline = {"bound": "tensor" if bound == "tensor" else "hbm", "kernel": dominant,
-                "achieved": round(achieved, 2), "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
-                "traffic": ncu_traffic(w.name, n, dominant), "peak_source": f"{pk['source']} ({'sustained bf16' if bound == 'tensor' else 'copy'})",
-                "algorithmic_per_launch": work, "avg_launch_ms": round(avg_s * 1e3, 4), "launches_timed": dcount,
+    avg_ms = dms / max(dcount, 1)
+    dr = kernel_roofline(dominant, w, n, avg_ms, pk)
+    flops, by = kernel_work(dominant, w, n)
+    roofline = {"bound": dr["bound"], "kernel": dominant, "achieved": dr["achieved"],
+                "peak": pk["bf16_tflops_sustained"] if dr["bound"] == "tensor" else pk["hbm_gbs"], "unit": dr["unit"],
+                "frac": dr["frac"], "traffic": ncu_traffic(w.name, n, dominant),
+                "peak_source": f"{pk['source']} ({'sustained bf16' if dr['bound'] == 'tensor' else 'copy'})",
+                "algorithmic_per_launch": flops if dr["bound"] == "tensor" else by,
+                "avg_launch_ms": round(avg_ms, 4), "launches_timed": dcount,
                 "launch_timing": "CUDA events around each launch, in a second timed pass of the same steps"}
 
     # end to end through the public API, every step: the step's ids from page-locked
@@ -443,41 +566,61 @@ def run_ours(args, w: synth.Workload, n: int, rank: int, world: int) -> dict:
         r.step(batch, ids=ids_host, hidden=hidden, out_ids=out_host)
         e_e[i].record()
     torch.cuda.synchronize()
+    wall_all = time.perf_counter() - wall0
+    clk = clocks.stop()
+    clk["window"] = (f"the timed steps, the dominant kernel's timed pass and the e2e pass "
+                     f"({2 * args.steps + e2e_steps} steps, {wall_all:.2f} s)")
     r.check_status()
     if not torch.equal(out_host, out_ids.cpu()):
         raise RuntimeError("the ids written to host memory differ from the device run's")
     e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / e2e_steps
+    roof_us = step_roofline_us(w, n, {k: v["launches_per_step"] for k, v in table.items()}, pk)
+    del r, batch, ids, hidden, out_ids
+    torch.cuda.empty_cache()
 
+    config = workload_config(w, n)
+    if w.layers_run > 1:
+        config["tokens_x_layers_per_s"] = round(T * w.layers_run / (ms_max / 1e3), 1)
     line = {"metric": METRIC, "value": job_throughput(T, world, ms_max), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
             "data": "synthetic (seeded counter generator; random-init weights of the named shape)",
-            "config": workload_config(w, n), "roofline": roofline,
-            "e2e": {"value": job_throughput(T, world, max_over_ranks(e2e_ms, world)), "unit": "tokens/s", "h2d_bytes_per_step": T * 4,
-                    "d2h_bytes_per_step": B * 4,
+            "config": config, "roofline": roofline,
+            "e2e": {"value": job_throughput(T, world, max_over_ranks(e2e_ms, world)), "unit": "tokens/s",
+                    "h2d_bytes_per_step": T * 4, "d2h_bytes_per_step": B * 4,
                     "transfer": "ids read from / next ids written to page-locked host memory by the kernels"},
             "gpu_launches": launches, "clocks": clk,
-            "kernel_us_per_step": breakdown, "wall_s_timed_region": round(wall, 3),
+            "step_roofline_us": round(roof_us, 2), "step_roofline_frac": round(roof_us / (ms_max * 1e3), 4),
+            "kernels": table, "wall_s_timed_region": round(wall, 3),
             "step_ms_p10_p50_p90": [round(step_ms[len(step_ms) // 10], 4), round(step_ms[len(step_ms) // 2], 4),
                                     round(step_ms[9 * len(step_ms) // 10], 4)]}
+    if not args.no_sub and world == 1:
+        line["workloads"] = [sub_record(name, tp, pk, flush_l2, ps) for name, tp, ps in SUB_RECORDS
+                             if not (name == w.name and tp == n and ps == 0)]
     return line
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--tp", type=int, default=None)
     ap.add_argument("--quick", action="store_true",
                     help="only warm-up + timed steps (no kernel breakdown, e2e or CPU baseline): for profilers")
+    ap.add_argument("--no-sub", action="store_true", help="skip the other configurations' records")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = synth.WORKLOADS[args.workload]
-    n = args.tp if args.tp is not None else max(w.tp_sizes)
+    if args.tp is not None:
+        n = args.tp
+    elif w.name == DEFAULT_WORKLOAD:
+        n = DEFAULT_TP
+    else:
+        n = max(w.tp_sizes)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

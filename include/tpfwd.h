@@ -47,6 +47,9 @@ typedef int32_t tp_status;
 #define TP_ERR_CUDA 7                 /* a CUDA runtime call or launch failed */
 #define TP_ERR_BAD_TOKEN 8            /* device: a token id outside [0, V) or a position outside the cache */
 #define TP_ERR_TIMEOUT 9              /* device: a bounded wait inside a kernel gave up */
+#define TP_ERR_SATURATED 10           /* device: a value converted to an fp16 operand (a weight, a residual
+                                         row, an attention output, SiLU*up, a decode q) was outside the fp16
+                                         range and was clamped to +-65504; the results are not trustworthy */
 
 typedef struct {
   int32_t hidden, num_q_heads, num_kv_heads, head_dim, intermediate, vocab, num_layers;
@@ -136,13 +139,22 @@ typedef struct {
 
 /* A1: shard then merge ([SHD] weight.py:34-52; [CH9] 3.3).  Exactly one of layer / head is
  * non-NULL; dst (device, tp_weights_bytes of that kind) receives every rank's shards in the
- * layout above.  Reads src only; asynchronous on stream. */
+ * layout above.  Reads src only; asynchronous on stream.  dev_status (device int32, sticky,
+ * may be NULL) receives TP_ERR_SATURATED's flag when a weight (times its folded norm weight)
+ * is outside the fp16 range of the tensor-core copies. */
 tp_status tp_shard_weights(tp_ctx* ctx, const tp_layer_full* layer, const tp_head_full* head, void* dst,
-                           void* stream);
+                           int32_t* dev_status, void* stream);
 
 /* ---------------- KV cache and workspace ----------------
- * KV cache of one layer: [n][2 (K, V)][max_seqs][nkv_l][capacity][hd] bf16; rank r keeps its
- * own kv heads (replicated heads stored once per holding rank, [TP] "KV heads ..."). */
+ * KV cache of one layer: [n][2 (K, V)][blocks][nkv_l][block_len][hd] bf16; rank r keeps its
+ * own kv heads (replicated heads stored once per holding rank, [TP] "KV heads ...").
+ * Contiguous cache: a block is a sequence slot of `capacity` positions (blocks = max_seqs,
+ * block_len = capacity), chosen per sequence by tp_batch.slot.
+ * Paged cache (zero-to-sglang "Chapter 9", section 3.3: the engine sets up the KV cache and
+ * its page table): a block is a page of page_size positions (blocks = the number of pages);
+ * tp_batch.page_table maps (sequence, position / page_size) to a page, so a sequence's
+ * pages need be neither contiguous nor in order, and sequences may share none.
+ * tp_kv_cache_bytes(ctx, blocks, block_len) sizes either. */
 tp_status tp_kv_cache_bytes(const tp_ctx* ctx, int32_t max_seqs, int32_t capacity, size_t* bytes);
 
 /* Workspace for steps of at most max_tokens tokens and max_seqs sequences and positions
@@ -193,7 +205,18 @@ typedef struct {
   int32_t max_kv_len;  /* max over sequences of ctx_len + q_len */
   const int32_t* cu_q;    /* device [num_seqs + 1]: first packed token of each sequence */
   const int32_t* ctx_len; /* device [num_seqs]: cached tokens = position of the first new token */
-  const int32_t* slot;    /* device [num_seqs]: cache slot (< max_seqs of the cache) */
+  const int32_t* slot;    /* device [num_seqs]: cache slot (< max_seqs of the cache); contiguous cache only */
+  /* Paged cache (page_table != NULL; slot is then ignored and may be NULL):
+   * page_table: device int32 [num_seqs][max_pages_per_seq]; entry [b][i] is the page that
+   *   holds positions [i * page_size, (i + 1) * page_size) of sequence b (the entries a
+   *   step reads or writes must be pages of the cache, else the device flags TP_ERR_BAD_TOKEN
+   *   and that part of the step is skipped);
+   * page_size: positions per page, a positive multiple of 128 (every 128-key tile of the
+   *   attention kernels then lies in one page);
+   * max_pages_per_seq: the table's row length; max_kv_len <= max_pages_per_seq * page_size. */
+  const int32_t* page_table;
+  int32_t page_size;
+  int32_t max_pages_per_seq;
 } tp_batch;
 
 /* A2: vocab-parallel embedding ([TP] VocabParallelEmbedding): per rank, ids inside its slice
@@ -212,7 +235,9 @@ tp_status tp_embed_vocab_parallel(tp_ctx* ctx, const void* head_shards, const in
  * per-rank GQA attention -> o_proj (row) + rank-sum + residual -> RMSNorm -> gate/up (column) with
  * SiLU*up -> down (row) + rank-sum + residual.  hidden: device fp32 [T, H] residual stream,
  * updated in place.
- * kv_cache: this layer's cache (tp_kv_cache_bytes(kv_max_seqs, kv_capacity)); positions
+ * kv_cache: this layer's cache (tp_kv_cache_bytes(kv_max_seqs, kv_capacity)): for a contiguous
+ * cache kv_max_seqs slots of kv_capacity positions, for a paged one (batch->page_table set)
+ * kv_max_seqs pages of kv_capacity = batch->page_size positions; positions
  * [ctx_len, ctx_len + q_len) of each sequence are written.  Exactly two rank-sums. */
 tp_status tp_decoder_layer_forward(tp_ctx* ctx, const void* layer_shards, const tp_batch* batch, void* hidden,
                                    void* kv_cache, int32_t kv_max_seqs, int32_t kv_capacity, int32_t* dev_status,
@@ -224,7 +249,7 @@ tp_status tp_decoder_layer_forward(tp_ctx* ctx, const void* layer_shards, const 
  * hidden: device fp32 [T, H].  out_ids: int32 [num_seqs], in device memory or in page-locked
  * host memory, which the kernel then writes over the host link itself (complete when the
  * stream reaches this call's end); other host memory is rejected with TP_ERR_INVALID_ARG.
- * out_logits: device fp32 [num_seqs, V] or NULL. */
+ * out_logits: fp32 [num_seqs, V] or NULL, under the same memory rule as out_ids. */
 tp_status tp_lm_head_argmax(tp_ctx* ctx, const void* head_shards, const tp_batch* batch, const void* hidden,
                             int32_t* out_ids, float* out_logits, int32_t* dev_status, void* stream);
 
@@ -261,8 +286,12 @@ tp_status tp_lm_head_argmax_static(tp_ctx* ctx, const void* head_shards, const t
 tp_status tp_decode_advance(tp_ctx* ctx, const tp_batch* batch, const int32_t* ids, int32_t* history,
                             int32_t max_rows, int32_t* step, int32_t* dev_status, void* stream);
 
-/* Synchronises the stream, reads the device status word and returns TP_OK,
- * TP_ERR_BAD_TOKEN or TP_ERR_TIMEOUT (the word is not cleared). */
+/* Synchronises the stream, reads the device status word and returns TP_OK, TP_ERR_TIMEOUT,
+ * TP_ERR_BAD_TOKEN or TP_ERR_SATURATED (in that order of precedence; the word is not cleared).
+ * Every device call ORs its flags into the caller's word: an fp16 conversion that clamps sets
+ * the saturation flag, so a clamp is never silent.  After TP_ERR_TIMEOUT the context's
+ * workspace counters are still consistent (every kernel counts itself in on its way out), but
+ * that step's outputs are not valid. */
 tp_status tp_read_status(const int32_t* dev_status, void* stream);
 
 /* Rank-sums (emulated all-reduces) issued through this context so far: one per embedding,

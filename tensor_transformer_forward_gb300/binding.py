@@ -27,6 +27,7 @@ TP_ERR_UNSUPPORTED = 6
 TP_ERR_CUDA = 7
 TP_ERR_BAD_TOKEN = 8
 TP_ERR_TIMEOUT = 9
+TP_ERR_SATURATED = 10
 
 PARAM = dict(q=0, k=1, v=2, o=3, gate=4, up=5, down=6, embed=7, lm_head=8, norm=9)
 PART = dict(qkv=0, o=1, gate_up=2, down=3, in_norm=4, post_norm=5, q_norm=6, k_norm=7,
@@ -54,7 +55,8 @@ class TPConfig(ctypes.Structure):
 class TPBatch(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("num_prefill", ctypes.c_int32), ("num_tokens", ctypes.c_int32),
                 ("max_q_len", ctypes.c_int32), ("max_kv_len", ctypes.c_int32),
-                ("cu_q", ctypes.c_void_p), ("ctx_len", ctypes.c_void_p), ("slot", ctypes.c_void_p)]
+                ("cu_q", ctypes.c_void_p), ("ctx_len", ctypes.c_void_p), ("slot", ctypes.c_void_p),
+                ("page_table", ctypes.c_void_p), ("page_size", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32)]
 
 
 class TPLayerFull(ctypes.Structure):
@@ -81,7 +83,7 @@ def _load() -> ctypes.CDLL:
         "tp_shard_index_map": ([P, I32, I32, P, pI64, pI32], I32),
         "tp_weights_bytes": ([P, I32, pSZ], I32),
         "tp_weights_part": ([P, I32, pSZ, pSZ], I32),
-        "tp_shard_weights": ([P, ctypes.POINTER(TPLayerFull), ctypes.POINTER(TPHeadFull), P, P], I32),
+        "tp_shard_weights": ([P, ctypes.POINTER(TPLayerFull), ctypes.POINTER(TPHeadFull), P, P, P], I32),
         "tp_kv_cache_bytes": ([P, I32, I32, pSZ], I32),
         "tp_workspace_bytes": ([P, I32, I32, I32, pSZ], I32),
         "tp_workspace_init": ([P, P, SZ, I32, I32, I32, P], I32),
@@ -296,18 +298,35 @@ class Context:
 
 
 class Batch:
-    """Device arrays of one step plus the host summary the launches need."""
+    """Device arrays of one step plus the host summary the launches need.
 
-    def __init__(self, q_lens: Sequence[int], ctx_lens: Sequence[int], slots: Sequence[int], num_prefill: int,
-                 max_kv_len: Optional[int] = None):
+    A contiguous cache takes ``slots`` (the cache slot of each sequence).  A paged
+    cache takes ``page_table`` ([num_seqs][max_pages_per_seq] page ids, a list of
+    lists or an int32 tensor) and ``page_size`` (a multiple of 128); ``slots`` is
+    then unused (it may be None)."""
+
+    def __init__(self, q_lens: Sequence[int], ctx_lens: Sequence[int], slots: Optional[Sequence[int]],
+                 num_prefill: int, max_kv_len: Optional[int] = None, page_table=None, page_size: int = 0):
         cu = [0]
         for q in q_lens:
             cu.append(cu[-1] + int(q))
-        self.q_lens, self.ctx_lens, self.slots = list(q_lens), list(ctx_lens), list(slots)
+        self.q_lens, self.ctx_lens = list(q_lens), list(ctx_lens)
+        self.slots = None if slots is None else list(slots)
         self.num_prefill = num_prefill
         self.cu_q = torch.tensor(cu, dtype=torch.int32, device="cuda")
         self.ctx_len = torch.tensor(list(ctx_lens), dtype=torch.int32, device="cuda")
-        self.slot = torch.tensor(list(slots), dtype=torch.int32, device="cuda")
+        self.slot = None if slots is None else torch.tensor(list(slots), dtype=torch.int32, device="cuda")
+        self.page_table = None
+        pages = 0
+        if page_table is not None:
+            pt = page_table if isinstance(page_table, torch.Tensor) else torch.tensor(page_table, dtype=torch.int32)
+            if pt.dim() != 2 or pt.shape[0] != len(q_lens) or page_size <= 0:
+                raise ValueError("page_table must be [num_seqs][max_pages_per_seq] with a page_size > 0")
+            self.page_table = pt.to(device="cuda", dtype=torch.int32).contiguous()
+            pages = int(pt.shape[1])
+        elif slots is None:
+            raise ValueError("a batch needs slots (contiguous cache) or a page_table (paged cache)")
+        self.page_size = int(page_size) if page_table is not None else 0
         pre = list(q_lens[:num_prefill])
         # max_kv_len plans the launches; a batch whose device ctx_len grows between
         # forwards (greedy decoding, one graph for every step) plans for its last one
@@ -317,7 +336,10 @@ class Batch:
                 raise ValueError("max_kv_len below the batch's current kv length")
             kv = int(max_kv_len)
         self.c = TPBatch(len(q_lens), num_prefill, cu[-1], max(pre) if pre else 0, kv,
-                         self.cu_q.data_ptr(), self.ctx_len.data_ptr(), self.slot.data_ptr())
+                         self.cu_q.data_ptr(), self.ctx_len.data_ptr(),
+                         self.slot.data_ptr() if self.slot is not None else None,
+                         self.page_table.data_ptr() if self.page_table is not None else None,
+                         self.page_size, pages)
 
     @property
     def num_tokens(self) -> int:
@@ -333,8 +355,10 @@ class Batch:
 # ---------------------------------------------------------------------------
 
 def tp_shard_weights(ctx: Context, dst: torch.Tensor, layer: Optional[Dict[str, torch.Tensor]] = None,
-                     head: Optional[Dict[str, torch.Tensor]] = None) -> None:
-    """A1: shard then merge full bf16 tensors (dict by name) into ``dst``."""
+                     head: Optional[Dict[str, torch.Tensor]] = None, status: Optional[torch.Tensor] = None) -> None:
+    """A1: shard then merge full bf16 tensors (dict by name) into ``dst``; ``status``
+    (device int32, optional) receives the saturation flag when a weight is outside
+    the fp16 range of the tensor-core copies."""
     lp = hp = None
     keep: List[torch.Tensor] = []
     if layer is not None:
@@ -353,7 +377,8 @@ def tp_shard_weights(ctx: Context, dst: torch.Tensor, layer: Optional[Dict[str, 
             keep.append(t)
             setattr(f2, k, _dev(t, k, torch.bfloat16).value)
         hp = ctypes.byref(f2)
-    _check(_lib.tp_shard_weights(ctx.handle, lp, hp, _dev(dst, "dst"), _stream()), "tp_shard_weights")
+    st = _dev(status, "status", torch.int32) if status is not None else None
+    _check(_lib.tp_shard_weights(ctx.handle, lp, hp, _dev(dst, "dst"), st, _stream()), "tp_shard_weights")
 
 
 def tp_embed_vocab_parallel(ctx: Context, head_shards: torch.Tensor, ids: torch.Tensor, hidden_out: torch.Tensor,
@@ -375,7 +400,7 @@ def tp_decoder_layer_forward(ctx: Context, layer_shards: torch.Tensor, batch: Ba
 
 def tp_lm_head_argmax(ctx: Context, head_shards: torch.Tensor, batch: Batch, hidden: torch.Tensor,
                       out_ids: torch.Tensor, status: torch.Tensor, out_logits: Optional[torch.Tensor] = None) -> None:
-    lg = _dev(out_logits, "out_logits", torch.float32) if out_logits is not None else None
+    lg = _dev_or_pinned(out_logits, "out_logits", torch.float32) if out_logits is not None else None
     _check(_lib.tp_lm_head_argmax(ctx.handle, _dev(head_shards, "head_shards"), ctypes.byref(batch.c),
                                   _dev(hidden, "hidden", torch.float32),
                                   _dev_or_pinned(out_ids, "out_ids", torch.int32), lg,
@@ -387,9 +412,10 @@ def tp_lm_head_argmax_static(ctx: Context, head_shards: torch.Tensor, batch: Bat
                              out_logits: Optional[torch.Tensor] = None) -> None:
     """tp_lm_head_argmax without a workspace: for callers that cannot allocate
     device memory; its scratch is a fixed array inside the library (see tpfwd.h)."""
-    lg = _dev(out_logits, "out_logits", torch.float32) if out_logits is not None else None
+    lg = _dev_or_pinned(out_logits, "out_logits", torch.float32) if out_logits is not None else None
     _check(_lib.tp_lm_head_argmax_static(ctx.handle, _dev(head_shards, "head_shards"), ctypes.byref(batch.c),
-                                         _dev(hidden, "hidden", torch.float32), _dev(out_ids, "out_ids", torch.int32),
+                                         _dev(hidden, "hidden", torch.float32),
+                                         _dev_or_pinned(out_ids, "out_ids", torch.int32),
                                          lg, _dev(status, "status", torch.int32), _stream()),
            "tp_lm_head_argmax_static")
 
@@ -406,7 +432,7 @@ def tp_decode_advance(ctx: Context, batch: Batch, ids: torch.Tensor, history: to
 
 def tp_read_status(status: torch.Tensor) -> int:
     """Synchronises the current stream and returns the device status (TP_OK,
-    TP_ERR_BAD_TOKEN or TP_ERR_TIMEOUT)."""
+    TP_ERR_BAD_TOKEN, TP_ERR_TIMEOUT or TP_ERR_SATURATED)."""
     return _lib.tp_read_status(_dev(status, "status", torch.int32), _stream())
 
 

@@ -191,22 +191,13 @@ T* at(const void* base, const Region& r) {
   return reinterpret_cast<T*>(const_cast<char*>(reinterpret_cast<const char*>(base)) + r.off);
 }
 
-// The address a kernel uses for p: device (or managed) memory as it is, page-locked
-// host memory through its device mapping; null for memory the GPU cannot address.
-template <typename T>
-T* gpu_view(T* p) {
-  cudaPointerAttributes a{};
-  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return nullptr;
-  }
-  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return p;
-  if (a.type == cudaMemoryTypeHost) return static_cast<T*>(a.devicePointer);
-  return nullptr;
-}
-
 tp_status check_batch(const tp_ctx* x, const tp_batch* b) {
-  if (!b || !b->cu_q || !b->ctx_len || !b->slot) return TP_ERR_INVALID_ARG;
+  if (!b || !b->cu_q || !b->ctx_len || (!b->slot && !b->page_table)) return TP_ERR_INVALID_ARG;
+  if (b->page_table) {  // paged cache: pages hold whole 128-key tiles
+    if (b->page_size <= 0 || b->page_size % tpk::kKeyAlign || b->max_pages_per_seq <= 0) return TP_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(b->max_kv_len) > static_cast<int64_t>(b->max_pages_per_seq) * b->page_size)
+      return TP_ERR_INVALID_ARG;
+  }
   if (b->num_seqs <= 0 || b->num_seqs > x->ws_seqs) return TP_ERR_INVALID_ARG;
   if (b->num_prefill < 0 || b->num_prefill > b->num_seqs) return TP_ERR_INVALID_ARG;
   if (b->num_tokens < b->num_seqs || b->num_tokens > x->ws_tokens) return TP_ERR_INVALID_ARG;
@@ -253,6 +244,8 @@ tp_status gemm(tp_ctx* x, int kind, const tpk::GemmProblem& pr, int32_t* dev_sta
 
 }  // namespace
 
+int tpk::ctx_hidden_size(const tp_ctx* x) { return x ? x->H : 0; }
+
 int tpk::ctx_head_view(tp_ctx* x, tpk::HeadView* out) {
   if (!x || !out) return TP_ERR_INVALID_ARG;
   const tp_status st = ensure_device(x);
@@ -284,6 +277,7 @@ const char* tp_status_string(tp_status s) {
     case TP_ERR_CUDA: return "CUDA error";
     case TP_ERR_BAD_TOKEN: return "token id or position out of range";
     case TP_ERR_TIMEOUT: return "bounded wait timed out in a kernel";
+    case TP_ERR_SATURATED: return "an fp16 operand exceeded the fp16 range and was clamped";
     default: return "unknown status";
   }
 }
@@ -401,7 +395,8 @@ tp_status tp_weights_part(const tp_ctx* x, int32_t part, size_t* offset, size_t*
   return TP_OK;
 }
 
-tp_status tp_shard_weights(tp_ctx* x, const tp_layer_full* L, const tp_head_full* Hd, void* dst, void* stream) {
+tp_status tp_shard_weights(tp_ctx* x, const tp_layer_full* L, const tp_head_full* Hd, void* dst, int32_t* dev_status,
+                           void* stream) {
   if (!x || !dst || (L == nullptr) == (Hd == nullptr)) return TP_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* d = static_cast<char*>(dst);
@@ -462,14 +457,14 @@ tp_status tp_shard_weights(tp_ctx* x, const tp_layer_full* L, const tp_head_full
     // (x_n W^T = (x inv) (W diag(w))^T, the row scale inv applied in the epilogue)
     {
       cudaError_t e = tpk::launch_fold_norm_f16(d + x->qkv.off, static_cast<size_t>(n) * x->w_rank, x->H,
-                                                d + x->in_norm.off, s);
+                                                d + x->in_norm.off, dev_status, s);
       if (e == cudaSuccess)
         e = tpk::launch_fold_norm_f16(d + x->gate_up.off, static_cast<size_t>(n) * 2 * x->i_p, x->H,
-                                      d + x->post_norm.off, s);
+                                      d + x->post_norm.off, dev_status, s);
       if (e != cudaSuccess) return cuda_fail(e);
     }
     for (const Region* r : {&x->o, &x->down}) {
-      cudaError_t e = tpk::launch_bf16_to_f16(d + r->off, r->bytes / 2, s);
+      cudaError_t e = tpk::launch_bf16_to_f16(d + r->off, r->bytes / 2, dev_status, s);
       if (e != cudaSuccess) return cuda_fail(e);
     }
     return TP_OK;
@@ -490,7 +485,7 @@ tp_status tp_shard_weights(tp_ctx* x, const tp_layer_full* L, const tp_head_full
     // the LM head's fp16 copy carries the final RMSNorm weight in its columns (the
     // norm's row scale is applied to the logits, or dropped for the argmax alone)
     cudaError_t e = tpk::launch_fold_norm_f16(d + x->lm_head.off, static_cast<size_t>(n) * x->v_l, x->H,
-                                              d + x->final_norm.off, s);
+                                              d + x->final_norm.off, dev_status, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return TP_OK;
@@ -553,7 +548,7 @@ tp_status tp_workspace_init(tp_ctx* x, void* ws, size_t ws_bytes, int32_t max_to
 tp_status tp_embed_vocab_parallel(tp_ctx* x, const void* head_shards, const int32_t* ids, int32_t T,
                                   void* hidden_out, int32_t* dev_status, void* stream) {
   if (!x || !head_shards || !ids || !hidden_out || !dev_status || T <= 0) return TP_ERR_INVALID_ARG;
-  ids = gpu_view(ids);  // page-locked host ids are read by the kernel over the host link
+  ids = tpk::gpu_view(ids);  // page-locked host ids are read by the kernel over the host link
   if (!ids) return TP_ERR_INVALID_ARG;
   cudaError_t e;
   // with a workspace large enough, also the first layer's deferred-norm inputs
@@ -580,7 +575,16 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   if (!x || !shards || !hidden || !kv || !dev_status || !x->ws) return TP_ERR_INVALID_ARG;
   tp_status st = check_batch(x, b);
   if (st != TP_OK) return st;
-  if (kv_max_seqs <= 0 || kv_cap < b->max_kv_len) return TP_ERR_INVALID_ARG;
+  if (kv_max_seqs <= 0 || kv_cap <= 0) return TP_ERR_INVALID_ARG;
+  if (b->page_table ? kv_cap != b->page_size : kv_cap < b->max_kv_len) return TP_ERR_INVALID_ARG;
+  // the cache's blocks: slots of a contiguous cache, or pages
+  tpk::KvMap kvm;
+  if (b->page_table) {
+    kvm.table = b->page_table; kvm.stride = b->max_pages_per_seq; kvm.block_len = b->page_size;
+  } else {
+    kvm.table = b->slot; kvm.stride = 1; kvm.block_len = kv_cap;
+  }
+  kvm.blocks = kv_max_seqs;
   st = ensure_device(x);
   if (st != TP_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -603,7 +607,7 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   x->stats_for = nullptr;  // until this call completes
   if (!have_stats) {
     Timed tm(x, TP_K_RMSNORM, s);
-    e = tpk::launch_row_stats(hidden, T, H, xn, ss, s);
+    e = tpk::launch_row_stats(hidden, T, H, xn, ss, dev_status, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
 
@@ -617,8 +621,8 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   g.qkv.n = n; g.qkv.nq_l = x->nq_l; g.qkv.nkv_l = x->nkv_l; g.qkv.hd = x->hd; g.qkv.w_rank = x->w_rank;
   g.qkv.q_norm = w + x->q_norm.off; g.qkv.k_norm = w + x->k_norm.off; g.qkv.eps = x->c.rms_eps;
   g.qkv.rope = reinterpret_cast<const float2*>(x->ws + x->r_rope.off); g.qkv.max_pos = x->ws_pos;
-  g.qkv.cu_q = b->cu_q; g.qkv.ctx_len = b->ctx_len; g.qkv.slot = b->slot; g.qkv.B = b->num_seqs;
-  g.qkv.kv = kv; g.qkv.max_seqs = kv_max_seqs; g.qkv.cap = kv_cap;
+  g.qkv.cu_q = b->cu_q; g.qkv.ctx_len = b->ctx_len; g.qkv.B = b->num_seqs;
+  g.qkv.kv = kv; g.qkv.kvm = kvm;
   g.qkv.num_prefill = b->num_prefill; g.qkv.q_lo = x->ws + x->r_qlo.off;
   g.row_ss = ss; g.row_groups = H / 32; g.row_eps = x->c.rms_eps;
   // dead by now: the SiLU*up rows of the previous layer (read by its down_proj)
@@ -629,8 +633,8 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   // A6: per-rank attention
   tpk::AttnArgs aa{};
   aa.qkv = qkv; aa.q_lo = x->ws + x->r_qlo.off; aa.T = T; aa.n = n; aa.nq_l = x->nq_l; aa.nkv_l = x->nkv_l; aa.hd = x->hd; aa.w_rank = x->w_rank;
-  aa.kv = kv; aa.max_seqs = kv_max_seqs; aa.cap = kv_cap;
-  aa.cu_q = b->cu_q; aa.ctx_len = b->ctx_len; aa.slot = b->slot;
+  aa.kv = kv; aa.kvm = kvm;
+  aa.cu_q = b->cu_q; aa.ctx_len = b->ctx_len;
   aa.max_q_len = b->max_q_len; aa.max_kv_len = b->max_kv_len; aa.out = attn;
   aa.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(x->hd)));
   aa.part = reinterpret_cast<float*>(x->ws + x->r_apart.off);
@@ -703,8 +707,12 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
 tp_status tp_lm_head_argmax(tp_ctx* x, const void* head_shards, const tp_batch* b, const void* hidden,
                             int32_t* out_ids, float* out_logits, int32_t* dev_status, void* stream) {
   if (!x || !head_shards || !hidden || !out_ids || !dev_status || !x->ws) return TP_ERR_INVALID_ARG;
-  out_ids = gpu_view(out_ids);  // page-locked host ids are written by the kernel over the host link
+  out_ids = tpk::gpu_view(out_ids);  // page-locked host ids are written by the kernel over the host link
   if (!out_ids) return TP_ERR_INVALID_ARG;
+  if (out_logits) {  // the same rule for the logits
+    out_logits = tpk::gpu_view(out_logits);
+    if (!out_logits) return TP_ERR_INVALID_ARG;
+  }
   tp_status st = check_batch(x, b);
   if (st != TP_OK) return st;
   st = ensure_device(x);
@@ -726,7 +734,7 @@ tp_status tp_lm_head_argmax(tp_ctx* x, const void* head_shards, const tp_batch* 
     zin = x->ws + x->r_xn.off + static_cast<size_t>(B == 1 ? b->num_tokens - 1 : 0) * H * 2;
   } else {
     Timed tm(x, TP_K_FINAL_NORM, s);
-    e = tpk::launch_final_norm_select(hidden, H, b->cu_q, B, nullptr, x->c.rms_eps, z, s);
+    e = tpk::launch_final_norm_select(hidden, H, b->cu_q, B, nullptr, x->c.rms_eps, z, dev_status, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   tpk::GemmProblem g{};
@@ -800,6 +808,7 @@ tp_status tp_read_status(const int32_t* dev_status, void* stream) {
   TP_CUDA(cudaMemcpy(&v, dev_status, 4, cudaMemcpyDeviceToHost));
   if (v & TP_DEVFLAG_TIMEOUT) return TP_ERR_TIMEOUT;
   if (v & TP_DEVFLAG_BAD_TOKEN) return TP_ERR_BAD_TOKEN;
+  if (v & TP_DEVFLAG_SATURATED) return TP_ERR_SATURATED;
   return TP_OK;
 }
 

@@ -9,6 +9,7 @@
 // Bits OR-ed into the caller's device status word (read back by tp_read_status).
 #define TP_DEVFLAG_BAD_TOKEN 1
 #define TP_DEVFLAG_TIMEOUT 2
+#define TP_DEVFLAG_SATURATED 4  // an fp16 operand was clamped to +-65504
 
 // Every spin-wait in these kernels gives up after this long, sets
 // TP_DEVFLAG_TIMEOUT and lets the kernel return.
@@ -56,13 +57,25 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 #define TP_F16_MAX 65504.0f
 
-// fp16 operands (GEMM/attention inputs): saturate to the finite fp16 range.
-__device__ __forceinline__ float sat_f16(float x) { return fabsf(x) > TP_F16_MAX ? copysignf(TP_F16_MAX, x) : x; }
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  lo = sat_f16(lo);  // NaN passes through
-  hi = sat_f16(hi);
+// fp16 operands (GEMM / attention inputs): saturate to the finite fp16 range.  Each
+// conversion ORs into `sat` (a per-thread accumulator) whether it clamped; the
+// thread reports it with report_sat, which sets TP_DEVFLAG_SATURATED in the
+// status word, so a clamp is never silent.  NaN passes through unflagged.
+__device__ __forceinline__ float sat_f16(float x, uint32_t& sat) {
+  const bool over = fabsf(x) > TP_F16_MAX;
+  sat |= over ? 1u : 0u;
+  return over ? copysignf(TP_F16_MAX, x) : x;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi, uint32_t& sat) {
+  lo = sat_f16(lo, sat);
+  hi = sat_f16(hi, sat);
   __half2 p = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
+}
+__device__ __forceinline__ __half to_f16(float x, uint32_t& sat) { return __float2half_rn(sat_f16(x, sat)); }
+// Per thread, no warp collective (callers may have diverged); the branch is rarely taken.
+__device__ __forceinline__ void report_sat(int* status, uint32_t sat) {
+  if (sat) raise_flag(status, TP_DEVFLAG_SATURATED);
 }
 __device__ __forceinline__ float f16lo(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu))); }
 __device__ __forceinline__ float f16hi(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))); }

@@ -5,7 +5,9 @@
 // scores are scaled by 1/sqrt(hd); new token j of a sequence with ctx cached
 // tokens sees keys 0 .. ctx + j.  Softmax in fp32 (base-2, max-subtracted).
 //
-// Cache layout (per layer): [n][2 (K, V)][max_seqs][nkv_l][cap][hd] bf16.  q comes
+// Cache layout (per layer): [n][2 (K, V)][blocks][nkv_l][block_len][hd] bf16, a
+// block being a sequence slot of a contiguous cache or a page of a paged one (the
+// batch's block table maps (sequence, position / block_len) to a block).  q comes
 // from the merged QKV buffer: fp16 for decode tokens (fp32 math), bf16 high +
 // low parts for prefill tokens (bf16 tensor-core operands next to the bf16
 // cache).  Output layout: [T][n * nq_l * hd] fp16 (rank-major heads, the
@@ -90,18 +92,10 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
   const int split = blockIdx.y;
   const int t = a.cu_q[b];
   const int L = a.ctx_len[b] + 1;
-  const int slot = a.slot[b];
-  // a slot or length outside the cache reads nothing (zero output) and flags the batch
-  const bool bad = slot < 0 || slot >= a.max_seqs || L < 1 || L > a.cap;
-  const int chunk = (L + a.splits - 1) / a.splits;
+  // splits start on kKeyAlign-key boundaries (pages hold whole chunks)
+  const int chunk = ((L + a.splits - 1) / a.splits + kKeyAlign - 1) / kKeyAlign * kKeyAlign;
   const int k0 = split * chunk;
-  const int k1 = bad ? k0 : min(L, k0 + chunk);
-  const int nchunks = k1 > k0 ? (k1 - k0 + C::CK - 1) / C::CK : 0;
-
-  const size_t plane = static_cast<size_t>(a.max_seqs) * a.nkv_l * a.cap * HD;
-  const size_t head_off = (static_cast<size_t>(bad ? 0 : slot) * a.nkv_l + g) * a.cap * HD;
-  const __nv_bfloat16* Kc = reinterpret_cast<const __nv_bfloat16*>(a.kv) + (2 * static_cast<size_t>(r)) * plane + head_off;
-  const __nv_bfloat16* Vc = reinterpret_cast<const __nv_bfloat16*>(a.kv) + (2 * static_cast<size_t>(r) + 1) * plane + head_off;
+  const int k1n = min(L, k0 + chunk);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -111,11 +105,16 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
     *abort_flag = 0;
     fence_barrier_init();
   }
-  __syncthreads();
+  // a split whose keys lie (partly) outside the cache reads nothing (zero output)
+  // and flags the batch
+  const bool bad = __syncthreads_or(L < 1 || kv_blocks_bad(a.kvm, b, k0, k1n, threadIdx.x, blockDim.x));
+  const int k1 = bad ? k0 : k1n;
+  const int nchunks = k1 > k0 ? (k1 - k0 + C::CK - 1) / C::CK : 0;
+  const __nv_bfloat16* kvb = reinterpret_cast<const __nv_bfloat16*>(a.kv);
   // the batch arrays are the host's; q and the cache come from earlier kernels
   griddep_wait();
   griddep_launch();
-  if (bad && threadIdx.x == 0 && split == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
+  if (bad && threadIdx.x == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
 
   // per-lane state for the warp's keys: G heads x (m, l, acc[8])
   float m[G], l[G], acc[G][8];
@@ -131,16 +130,21 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
     // ---------------- bulk-copy producer ----------------
     if (lane == 0) {
       int issued = 0;
+      // block of the next chunk, looked up one chunk ahead (its load overlaps the wait)
+      int blk_next = nchunks > 0 ? kv_block_checked(a.kvm, b, k0) : 0;
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % C::STAGES;
-        if (!mbar_wait(bar0 + 8u * (C::STAGES + s), ((c / C::STAGES) & 1) ^ 1u, abort_flag, a.status)) break;
         const int key = k0 + c * C::CK;
+        const int blk = blk_next;
+        if (c + 1 < nchunks) blk_next = kv_block_checked(a.kvm, b, key + C::CK);
+        if (!mbar_wait(bar0 + 8u * (C::STAGES + s), ((c / C::STAGES) & 1) ^ 1u, abort_flag, a.status)) break;
         const uint32_t bytes = static_cast<uint32_t>(min(C::CK, k1 - key)) * C::ROW;
         const uint32_t full = bar0 + 8u * s;
         mbar_arrive_expect_tx(full, 2 * bytes);
         uint8_t* st = dsm + s * C::STAGE_BYTES;
-        bulk_load(smem_u32(st), Kc + static_cast<size_t>(key) * HD, bytes, full);
-        bulk_load(smem_u32(st + C::CK * C::ROW), Vc + static_cast<size_t>(key) * HD, bytes, full);
+        const int brow = key % a.kvm.block_len;
+        bulk_load(smem_u32(st), kvb + kv_row(a.kvm, a.nkv_l, r, 0, blk, g, brow) * HD, bytes, full);
+        bulk_load(smem_u32(st + C::CK * C::ROW), kvb + kv_row(a.kvm, a.nkv_l, r, 1, blk, g, brow) * HD, bytes, full);
         issued = c + 1;
       }
       for (int c = (issued > C::STAGES ? issued - C::STAGES : 0); c < issued; ++c)
@@ -274,7 +278,9 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
     if (a.splits == 1) {
       __half* o = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
                   (static_cast<size_t>(r) * a.nq_l + g * G + h) * HD + d;
-      *o = __float2half_rn(sat_f16(ll > 0.0f ? aa / ll : 0.0f));
+      uint32_t sat = 0;
+      *o = to_f16(ll > 0.0f ? aa / ll : 0.0f, sat);
+      report_sat(a.status, sat);
     } else {
       part[h * (HD + 2) + d] = aa;
       if (d == 0) {
@@ -310,21 +316,25 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
     }
     __half* o = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
                 (static_cast<size_t>(r) * a.nq_l + g * G + h) * HD + d;
-    *o = __float2half_rn(sat_f16(ll > 0.0f ? aa / ll : 0.0f));
+    uint32_t sat = 0;
+    *o = to_f16(ll > 0.0f ? aa / ll : 0.0f, sat);
+    report_sat(a.status, sat);
   }
   if (threadIdx.x == 0) a.counters[unit] = 0;
 }
 
 template <int HD, int G>
 static cudaError_t prepare_decode(int* ctas_per_sm) {
-  static int occ = 0;
-  if (occ == 0) {
+  static PerDevice pd;  // the attribute and the occupancy, once per device
+  int dev = -1, occ = 0;
+  if (!per_device_ready(pd, &dev, &occ)) {
     cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DecCfg<HD>::SMEM);
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_decode_kernel<HD, G>, 160, DecCfg<HD>::SMEM);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
+    per_device_mark(pd, dev, occ);
   }
   *ctas_per_sm = occ;
   return cudaSuccess;
@@ -489,14 +499,12 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
   const int split = blockIdx.y;
   const int t = a.cu_q[b];
   const int L = a.ctx_len[b] + 1;
-  const int slot = a.slot[b];
-  const bool bad = slot < 0 || slot >= a.max_seqs || L < 1 || L > a.cap;
-  const int chunk = (L + a.splits - 1) / a.splits;
+  // splits start on kKeyAlign-key boundaries (a page holds whole key tiles)
+  const int chunk = ((L + a.splits - 1) / a.splits + kKeyAlign - 1) / kKeyAlign * kKeyAlign;
   const int k0 = split * chunk;
-  const int k1 = bad ? k0 : min(L, k0 + chunk);
-  const int ntiles = k1 > k0 ? (k1 - k0 + C::BK - 1) / C::BK : 0;
-  const int krow0 = (((r * 2 + 0) * a.max_seqs + (bad ? 0 : slot)) * a.nkv_l + g) * a.cap + k0;
-  const int vrow0 = (((r * 2 + 1) * a.max_seqs + (bad ? 0 : slot)) * a.nkv_l + g) * a.cap + k0;
+  const int k1n = min(L, k0 + chunk);
+  // a split whose keys lie (partly) outside the cache reads nothing and flags the batch
+  const bool bad_mine = L < 1 || kv_blocks_bad(a.kvm, b, k0, k1n, threadIdx.x, blockDim.x);
 
   if (threadIdx.x == 0) {
     mbar_init(D_QR, 128);
@@ -519,12 +527,14 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  const bool bad = __syncthreads_or(bad_mine);
   tc_fence_after();
+  const int k1 = bad ? k0 : k1n;
+  const int ntiles = k1 > k0 ? (k1 - k0 + C::BK - 1) / C::BK : 0;
   const uint32_t tmem = *tmem_slot;
   griddep_wait();  // q and the cache come from the QKV GEMM
   griddep_launch();
-  if (bad && threadIdx.x == 0 && split == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
+  if (bad && threadIdx.x == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
 
   float m[G], l[G];  // running max (exp2 domain) and sum per head: the same in every softmax thread
 #pragma unroll
@@ -540,16 +550,20 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
       if (is_k) tma_prefetch_desc(&tmKV);
       const uint32_t full = is_k ? D_KF : D_VF, empty = is_k ? D_KE : D_VE;
       uint8_t* dst = smem + (is_k ? C::K_OFF : C::V_OFF);
-      const int row0 = is_k ? krow0 : vrow0;
       int issued = 0;
+      // block of the next tile, looked up one tile ahead (its load overlaps the wait)
+      int blk_next = ntiles > 0 ? kv_block_checked(a.kvm, b, k0) : 0;
       for (int j = 0; j < ntiles; ++j) {
+        const int key = k0 + j * C::BK;
+        const int blk = blk_next;
+        if (j + 1 < ntiles) blk_next = kv_block_checked(a.kvm, b, key + C::BK);
         if (!mbar_wait(empty, (j & 1) ^ 1u, abort_flag, a.status)) break;
         // a last tile of at most 16 keys loads 16 rows (the typical ctx + 1 tail)
-        const bool short_tail = j == ntiles - 1 && k1 - (k0 + j * C::BK) <= 16;
+        const bool short_tail = j == ntiles - 1 && k1 - key <= 16;
         mbar_arrive_expect_tx(full, short_tail ? C::KT_BYTES / 8 : C::KT_BYTES);
+        const int row = static_cast<int>(kv_row(a.kvm, a.nkv_l, r, is_k ? 0 : 1, blk, g, key % a.kvm.block_len));
         for (int sub = 0; sub < C::NSUB; ++sub)
-          tma_load_2d(smem_u32(dst + sub * C::SUB_BYTES), short_tail ? &tmKV16 : &tmKV, full, sub * 64,
-                      row0 + j * C::BK);
+          tma_load_2d(smem_u32(dst + sub * C::SUB_BYTES), short_tail ? &tmKV16 : &tmKV, full, sub * 64, row);
         issued = j + 1;
       }
       if (issued > 0) mbar_wait(full, (issued - 1) & 1, nullptr, a.status);  // the last tile has landed
@@ -734,7 +748,9 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
           for (int h = 0; h < G; ++h) {
             __half* o = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
                         (static_cast<size_t>(r) * a.nq_l + g * G + h) * HD + d;
-            *o = __float2half_rn(sat_f16(l[h] > 0.0f ? ov[h] / l[h] : 0.0f));
+            uint32_t sat = 0;
+            *o = to_f16(l[h] > 0.0f ? ov[h] / l[h] : 0.0f, sat);
+            report_sat(a.status, sat);
           }
         } else {
           float* part = a.part + (static_cast<size_t>(unit) * a.splits + split) * G * (HD + 2);
@@ -790,15 +806,18 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
     }
     __half* o = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
                 (static_cast<size_t>(r) * a.nq_l + g * G + h) * HD + d;
-    *o = __float2half_rn(sat_f16(ll > 0.0f ? aa / ll : 0.0f));
+    uint32_t sat = 0;
+    *o = to_f16(ll > 0.0f ? aa / ll : 0.0f, sat);
+    report_sat(a.status, sat);
   }
   if (threadIdx.x == 0) a.counters[unit] = 0;
 }
 
 template <int HD, int G>
 static cudaError_t prepare_decode_tc(int* ctas_per_sm) {
-  static int occ = 0;
-  if (occ == 0) {
+  static PerDevice pd;  // the attributes and the occupancy, once per device
+  int dev = -1, occ = 0;
+  if (!per_device_ready(pd, &dev, &occ)) {
     cudaError_t e = cudaFuncSetAttribute(attn_decode_tc_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DtcCfg<HD>::SMEM);
     if (e != cudaSuccess) return e;
@@ -810,6 +829,7 @@ static cudaError_t prepare_decode_tc(int* ctas_per_sm) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_decode_tc_kernel<HD, G>, 192, DtcCfg<HD>::SMEM);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
+    per_device_mark(pd, dev, occ);
   }
   *ctas_per_sm = occ;
   return cudaSuccess;
@@ -829,7 +849,7 @@ static cudaError_t launch_decode_tc_hd(const AttnArgs& a, dim3 grid, cudaStream_
   int per_sm = 0;
   cudaError_t e0 = prepare_decode_tc<HD, G>(&per_sm);  // sets the shared-memory attribute once
   if (e0 != cudaSuccess) return e0;
-  const int64_t kv_rows = static_cast<int64_t>(a.n) * 2 * a.max_seqs * a.nkv_l * a.cap;
+  const int64_t kv_rows = static_cast<int64_t>(a.n) * 2 * a.kvm.blocks * a.nkv_l * a.kvm.block_len;
   if (kv_rows >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
   CUtensorMap mkv, mkv16;
   if (!make_tmap_2d(&mkv, a.kv, kv_rows, HD, HD, 128, true)) return cudaErrorInvalidValue;
@@ -918,8 +938,10 @@ __global__ void __launch_bounds__(320, 1)
   const int q0 = (qblocks - 1 - static_cast<int>(blockIdx.x) / (heads * nseq)) * C::BQ;
   if (q0 >= qlen) return;                                // uniform: before any barrier or TMEM use
   {
-    const int sl = a.slot[b], kmax = a.ctx_len[b] + qlen;
-    if (sl < 0 || sl >= a.max_seqs || a.ctx_len[b] < 0 || kmax > a.cap) {  // outside the cache: flag, skip
+    // every cache block of the sequence's keys [0, ctx + qlen) must be inside the
+    // cache (block table entries checked by the CTA's threads together); else flag, skip
+    const int c0 = a.ctx_len[b];
+    if (__syncthreads_or(c0 < 0 || kv_blocks_bad(a.kvm, b, 0, c0 + qlen, threadIdx.x, blockDim.x))) {
       griddep_wait();
       if (threadIdx.x == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
       return;
@@ -931,9 +953,6 @@ __global__ void __launch_bounds__(320, 1)
   const int tbase = a.cu_q[b];
   const int kend = ctx + min(q0 + C::BQ, qlen);          // keys this CTA needs: [0, kend)
   const int nblk = (kend + C::BKV - 1) / C::BKV;
-  const int slot = a.slot[b];
-  const int krow0 = (((r * 2 + 0) * a.max_seqs + slot) * a.nkv_l + g) * a.cap;
-  const int vrow0 = (((r * 2 + 1) * a.max_seqs + slot) * a.nkv_l + g) * a.cap;
 
   if (threadIdx.x == 0) {
     mbar_init(B_Q, 1);
@@ -980,18 +999,21 @@ __global__ void __launch_bounds__(320, 1)
                       tbase + q0);
         }
       }
-      const int row0 = is_k ? krow0 : vrow0;
       uint8_t* ring = smem + C::KV_OFF + (is_k ? 0 : STAGES * C::TILE_BYTES);
       int issued = 0;
+      // block of the next key block, looked up one block ahead (its load overlaps the wait)
+      int blk_next = nblk > 0 ? kv_block_checked(a.kvm, b, 0) : 0;
       for (int j = 0; j < nblk; ++j) {
         const int st = j % STAGES;
         const uint32_t full = is_k ? B_KF(st) : B_VF(st);
         const uint32_t empty = is_k ? B_KE(st) : B_VE(st);
+        const int blk = blk_next;
+        if (j + 1 < nblk) blk_next = kv_block_checked(a.kvm, b, (j + 1) * C::BKV);
         if (!mbar_wait(empty, ((j / STAGES) & 1) ^ 1u, abort_flag, a.status)) break;
         mbar_arrive_expect_tx(full, C::TILE_BYTES);
+        const int row = static_cast<int>(kv_row(a.kvm, a.nkv_l, r, is_k ? 0 : 1, blk, g, (j * C::BKV) % a.kvm.block_len));
         for (int s = 0; s < C::NSUB; ++s)
-          tma_load_2d(smem_u32(ring + st * C::TILE_BYTES + s * C::SUB_BYTES), &tmKV, full, s * 64,
-                      row0 + j * C::BKV);
+          tma_load_2d(smem_u32(ring + st * C::TILE_BYTES + s * C::SUB_BYTES), &tmKV, full, s * 64, row);
         issued = j + 1;
       }
       if (is_k) mbar_wait(B_Q, 0, nullptr, a.status);
@@ -1170,6 +1192,7 @@ __global__ void __launch_bounds__(320, 1)
       __half* orow = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(tbase + (row_ok ? qi : 0)) * a.n * a.nq_l * HD +
                      (static_cast<size_t>(r) * a.nq_l + h) * HD + half * OH;
 #pragma unroll
+      uint32_t sat = 0;
       for (int c = 0; c < OH / 32; ++c) {
         float v[32];
         tc_ld32(lane_addr + C::O_COL + half * OH + c * 32, v);
@@ -1177,14 +1200,15 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             uint4 w;
-            w.x = pack_f16x2(v[k * 8 + 0] * inv, v[k * 8 + 1] * inv);
-            w.y = pack_f16x2(v[k * 8 + 2] * inv, v[k * 8 + 3] * inv);
-            w.z = pack_f16x2(v[k * 8 + 4] * inv, v[k * 8 + 5] * inv);
-            w.w = pack_f16x2(v[k * 8 + 6] * inv, v[k * 8 + 7] * inv);
+            w.x = pack_f16x2(v[k * 8 + 0] * inv, v[k * 8 + 1] * inv, sat);
+            w.y = pack_f16x2(v[k * 8 + 2] * inv, v[k * 8 + 3] * inv, sat);
+            w.z = pack_f16x2(v[k * 8 + 4] * inv, v[k * 8 + 5] * inv, sat);
+            w.w = pack_f16x2(v[k * 8 + 6] * inv, v[k * 8 + 7] * inv, sat);
             *reinterpret_cast<uint4*>(orow + c * 32 + k * 8) = w;
           }
         }
       }
+      report_sat(a.status, sat);
     }
   }
 #undef B_Q
@@ -1208,19 +1232,17 @@ template <int HD>
 static cudaError_t launch_prefill_hd(const AttnArgs& a, cudaStream_t s) {
   using C = FaCfg<HD>;
   const int64_t w_cols = static_cast<int64_t>(a.n) * a.w_rank;
-  const int64_t kv_rows = static_cast<int64_t>(a.n) * 2 * a.max_seqs * a.nkv_l * a.cap;
+  const int64_t kv_rows = static_cast<int64_t>(a.n) * 2 * a.kvm.blocks * a.nkv_l * a.kvm.block_len;
   if (kv_rows >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
   const int64_t q_cols = static_cast<int64_t>(a.n) * a.nq_l * HD;
   CUtensorMap mq, mqlo, mkv;
   if (!make_tmap_2d(&mq, a.qkv, a.T, w_cols, w_cols, 128, true)) return cudaErrorInvalidValue;
   if (!make_tmap_2d(&mqlo, a.q_lo, a.T, q_cols, q_cols, 128, true)) return cudaErrorInvalidValue;
   if (!make_tmap_2d(&mkv, a.kv, kv_rows, HD, HD, 128, true)) return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(attn_prefill_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  static PerDevice attr;  // per device
+  {
+    const cudaError_t e = smem_attr_per_device(attr, attn_prefill_tc_kernel<HD>, C::SMEM);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const unsigned grid = static_cast<unsigned>((a.max_q_len + C::BQ - 1) / C::BQ) * a.n * a.nq_l * (a.seq_end - a.seq_begin);
   return launch_pdl(attn_prefill_tc_kernel<HD>, dim3(grid), dim3(320), C::SMEM, s, mq, mqlo, mkv, a);

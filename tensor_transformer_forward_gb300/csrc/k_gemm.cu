@@ -13,14 +13,17 @@
 // accumulator (fp32) and the partials are added in fixed rank order in the
 // epilogue -- the all-reduce of the pages, done on one GPU.
 //
-// Structure: persistent, warp-specialised, 192 threads per CTA.
+// Structure: persistent, warp-specialised, 64 + 32 * EW threads per CTA
+// (EW = 4 or 8 epilogue warps, GemmCfg::EW).
 //   warp 0      TMA producer: X and W tiles (64-wide K blocks, 128-byte
 //               swizzle) into a STAGES-deep shared-memory ring.
 //   warp 1      TMEM allocator + MMA issuer (one thread): tcgen05.mma
 //               M=128 x N=BN x K=16, two TMEM accumulators so the epilogue of
 //               one segment overlaps the main loop of the next.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
-//               row of the MMA's M side per thread), then the fused epilogue.
+//   warps 2..   epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
+//               row of the MMA's M side per thread), then the fused epilogue;
+//               with 8 warps (320 threads) the two warps of a TMEM lane
+//               quarter take the two halves of the tile's columns.
 // Orientation: tokens on the M side (tiles of 128 tokens x BN features), or,
 // for a handful of tokens against a long weight (the LM head), weights on the
 // M side (tiles of 128 features x BN tokens) so no shared-memory traffic is
@@ -135,6 +138,18 @@ __device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
   return un;
 }
 
+// After a wait gave up (TP_DEVFLAG_TIMEOUT is set, the results are not valid):
+// counts unit u and every later unit of this CTA in on their split-K tile
+// counters, so that each counter still returns to zero (the last to arrive
+// clears it) and the next launch starts clean.  One thread.
+__device__ __forceinline__ void drain_split_counters(const GemmParams& p, int u, int units) {
+  if (p.splits <= 1) return;
+  for (; u < units; u += gridDim.x) {
+    const int tile = u / p.splits;
+    if (atomicAdd(p.counters + tile, 1) == p.splits - 1) p.counters[tile] = 0;
+  }
+}
+
 // Deferred RMSNorm of input row t: rsqrt(mean of squares + eps) from the
 // row's 32-column sums of squares ("Tensor parallelism from scratch", the
 // RMSNorm before each projection; its weight is folded into W), 1 without them.
@@ -192,12 +207,12 @@ __device__ __forceinline__ void store8(__nv_bfloat16* dst, const float* x) {
   w.w = pack_bf16x2(x[6], x[7]);
   *reinterpret_cast<uint4*>(dst) = w;
 }
-__device__ __forceinline__ void store8(__half* dst, const float* x) {
+__device__ __forceinline__ void store8(__half* dst, const float* x, uint32_t& sat) {
   uint4 w;
-  w.x = pack_f16x2(x[0], x[1]);
-  w.y = pack_f16x2(x[2], x[3]);
-  w.z = pack_f16x2(x[4], x[5]);
-  w.w = pack_f16x2(x[6], x[7]);
+  w.x = pack_f16x2(x[0], x[1], sat);
+  w.y = pack_f16x2(x[2], x[3], sat);
+  w.z = pack_f16x2(x[4], x[5], sat);
+  w.w = pack_f16x2(x[6], x[7], sat);
   *reinterpret_cast<uint4*>(dst) = w;
 }
 
@@ -210,25 +225,25 @@ __device__ __forceinline__ void stage_f32x32(uint8_t* box, int r, const float* v
   for (int c = 0; c < 8; ++c)
     *reinterpret_cast<float4*>(rowp + ((c ^ (r & 7)) << 4)) = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
 }
-__device__ __forceinline__ void stage_f16x64(uint8_t* box, int r, const float* v) {
+__device__ __forceinline__ void stage_f16x64(uint8_t* box, int r, const float* v, uint32_t& sat) {
   uint8_t* rowp = box + r * 128;
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     uint4 w;
-    w.x = pack_f16x2(v[8 * c + 0], v[8 * c + 1]);
-    w.y = pack_f16x2(v[8 * c + 2], v[8 * c + 3]);
-    w.z = pack_f16x2(v[8 * c + 4], v[8 * c + 5]);
-    w.w = pack_f16x2(v[8 * c + 6], v[8 * c + 7]);
+    w.x = pack_f16x2(v[8 * c + 0], v[8 * c + 1], sat);
+    w.y = pack_f16x2(v[8 * c + 2], v[8 * c + 3], sat);
+    w.z = pack_f16x2(v[8 * c + 4], v[8 * c + 5], sat);
+    w.w = pack_f16x2(v[8 * c + 6], v[8 * c + 7], sat);
     *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) = w;
   }
 }
 // One row of a 32-row x 64-byte fp16 box (tensor map without swizzle).
-__device__ __forceinline__ void stage_f16x32(uint8_t* box, int r, const float* v) {
+__device__ __forceinline__ void stage_f16x32(uint8_t* box, int r, const float* v, uint32_t& sat) {
   uint4* rowp = reinterpret_cast<uint4*>(box + r * 64);
 #pragma unroll
   for (int c = 0; c < 4; ++c)
-    rowp[c] = make_uint4(pack_f16x2(v[8 * c], v[8 * c + 1]), pack_f16x2(v[8 * c + 2], v[8 * c + 3]),
-                         pack_f16x2(v[8 * c + 4], v[8 * c + 5]), pack_f16x2(v[8 * c + 6], v[8 * c + 7]));
+    rowp[c] = make_uint4(pack_f16x2(v[8 * c], v[8 * c + 1], sat), pack_f16x2(v[8 * c + 2], v[8 * c + 3], sat),
+                         pack_f16x2(v[8 * c + 4], v[8 * c + 5], sat), pack_f16x2(v[8 * c + 6], v[8 * c + 7], sat));
 }
 // Whole warp: wait until the box's previous store has read it.
 __device__ __forceinline__ void box_acquire(int lane) {
@@ -275,7 +290,7 @@ __device__ __forceinline__ void prefetch_rows32(const GemmParams& p, uint8_t* xb
 template <typename Cfg>
 __device__ __forceinline__ void resid_rows32(const GemmParams& p, const CUtensorMap* tmO, const CUtensorMap* tmO2,
                                              uint8_t* box, uint8_t* box16, int t, bool row_ok, int col, int tbox,
-                                             int lane, float* v, bool prefetched) {
+                                             int lane, float* v, bool prefetched, uint32_t& sat) {
   float s = 0.0f;
   if (row_ok && col < p.out_cols) {  // out_cols % 32 == 0: a group is wholly inside or outside
     const float4* x = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.out) +
@@ -295,7 +310,7 @@ __device__ __forceinline__ void resid_rows32(const GemmParams& p, const CUtensor
   }
   box_acquire(lane);  // the fp16 box (and a reused fp32 box) of the previous chunk has been read
   stage_f32x32(box, lane, v);
-  stage_f16x32(box16, lane, v);
+  stage_f16x32(box16, lane, v, sat);
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
@@ -323,9 +338,10 @@ __device__ __forceinline__ void argmax_scan(const GemmParams& p, int t, int f, c
   }
 }
 
-// Token row t -> its sequence, position and cache slot (binary search over cu_q).
+// Token row t -> its position and where its K / V go in the cache: block (slot
+// or page) and row in the block (binary search over cu_q for prefill tokens).
 struct TokPos {
-  int pos, seq_slot;
+  int pos, blk, brow;
   bool ok, prefill;
 };
 __device__ __forceinline__ TokPos token_position(const QkvEpi& q, int t) {
@@ -336,7 +352,7 @@ __device__ __forceinline__ TokPos token_position(const QkvEpi& q, int t) {
   if (t >= t_dec) {
     lo = q.num_prefill + (t - t_dec);
     if (lo >= q.B) {  // a "decode" sequence with more than one token: reject, stay in bounds
-      TokPos bad{0, 0, false, false};
+      TokPos bad{0, 0, 0, false, false};
       return bad;
     }
   } else {
@@ -350,8 +366,10 @@ __device__ __forceinline__ TokPos token_position(const QkvEpi& q, int t) {
   }
   TokPos tp;
   tp.pos = q.ctx_len[lo] + (t - q.cu_q[lo]);
-  tp.seq_slot = q.slot[lo];
-  tp.ok = tp.pos >= 0 && tp.pos < q.cap && tp.pos < q.max_pos && tp.seq_slot >= 0 && tp.seq_slot < q.max_seqs;
+  const int blk = tp.pos < q.max_pos ? kv_block(q.kvm, lo, tp.pos) : -1;
+  tp.ok = blk >= 0;
+  tp.blk = tp.ok ? blk : 0;
+  tp.brow = tp.ok ? tp.pos % q.kvm.block_len : 0;
   tp.prefill = lo < q.num_prefill;
   return tp;
 }
@@ -362,17 +380,16 @@ __device__ __forceinline__ TokPos token_position(const QkvEpi& q, int t) {
 // (post-RoPE K, raw V).  ("Tensor parallelism from scratch", tp.py
 // TPAttention.forward: q_norm / k_norm, apply_rope, cache.update.)
 template <int HD>
-__device__ __forceinline__ void qkv_head(const GemmParams& p, int t, const TokPos& tp, int col0, const float* h) {
+__device__ __forceinline__ void qkv_head(const GemmParams& p, int t, const TokPos& tp, int col0, const float* h,
+                                         uint32_t& sat) {
   const QkvEpi& q = p.qkv;
   constexpr int HALF = HD / 2;
   const int r = col0 / q.w_rank;
   const int sh = (col0 - r * q.w_rank) / HD;
-  const size_t plane = static_cast<size_t>(q.max_seqs) * q.nkv_l * q.cap * HD;
   __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(q.kv);
   if (sh >= q.nq_l + q.nkv_l) {  // v: raw into the cache
     const int g = sh - q.nq_l - q.nkv_l;
-    __nv_bfloat16* dst = kv + (2 * static_cast<size_t>(r) + 1) * plane +
-                         ((static_cast<size_t>(tp.seq_slot) * q.nkv_l + g) * q.cap + tp.pos) * HD;
+    __nv_bfloat16* dst = kv + kv_row(q.kvm, q.nkv_l, r, 1, tp.blk, g, tp.brow) * HD;
 #pragma unroll
     for (int j = 0; j < HD / 8; ++j) store8(dst + j * 8, h + j * 8);
     return;
@@ -393,8 +410,7 @@ __device__ __forceinline__ void qkv_head(const GemmParams& p, int t, const TokPo
   __half* q16 = reinterpret_cast<__half*>(qhi);
   __nv_bfloat16* qlo = reinterpret_cast<__nv_bfloat16*>(q.q_lo) +
                        static_cast<size_t>(t) * q.n * q.nq_l * HD + (static_cast<size_t>(r) * q.nq_l + sh) * HD;
-  __nv_bfloat16* kdst = kv + (2 * static_cast<size_t>(r)) * plane +                                // k: bf16 cache
-                        ((static_cast<size_t>(tp.seq_slot) * q.nkv_l + (sh - q.nq_l)) * q.cap + tp.pos) * HD;
+  __nv_bfloat16* kdst = kv + kv_row(q.kvm, q.nkv_l, r, 0, tp.blk, sh - q.nq_l, tp.brow) * HD;  // k: bf16 cache
 #pragma unroll
   for (int j = 0; j < HALF / 8; ++j) {
     // 16-byte loads: 8 norm weights of each half, 8 (cos, sin) pairs
@@ -422,8 +438,8 @@ __device__ __forceinline__ void qkv_head(const GemmParams& p, int t, const TokPo
       store8(kdst + j * 8, y0);
       store8(kdst + HALF + j * 8, y1);
     } else if (!tp.prefill) {
-      store8(q16 + j * 8, y0);
-      store8(q16 + HALF + j * 8, y1);
+      store8(q16 + j * 8, y0, sat);
+      store8(q16 + HALF + j * 8, y1, sat);
     } else {
       float l0[8], l1[8];
 #pragma unroll
@@ -471,7 +487,8 @@ template <int BN, int HD>
 __device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmQlo,
                                               const CUtensorMap* tmKV, uint32_t tfull, uint32_t use, volatile int* abort_flag, uint32_t ta,
                                               int t, const TokPos& tp, int f0, bool row_ok, int w, int q, int row,
-                                              int par, const float* nw, float* ss, uint8_t* stg, float rinv) {
+                                              int par, const float* nw, float* ss, uint8_t* stg, float rinv,
+                                              uint32_t& sat) {
   constexpr int HALF = HD / 2, QP = HALF / 2, NR = QP / 2, HPT = BN / HD;
   constexpr int SEGB = QP * 2;        // bytes of one row segment (QP bf16)
   constexpr int NC = SEGB / 16;       // 16-byte chunks per row segment
@@ -533,7 +550,6 @@ __device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, const CUtenso
       if (kind[hb] == 0 || kind[hb] == 1)
         inv[hb] = rsqrtf((inv[hb] + other[hb * 128 + row]) * (rinv * rinv) / static_cast<float>(HD) + e.eps);
   }
-  const size_t plane = static_cast<size_t>(e.max_seqs) * e.nkv_l * e.cap * HD;
   __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(e.kv);
 #pragma unroll
   for (int hb = 0; hb < HPT; ++hb) {
@@ -582,10 +598,10 @@ __device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, const CUtenso
           y1[i] = u1 * cs + u0 * sn;
         }
         if (kind[hb] == 0 && !tp.prefill) {  // decode q: fp16
-          *reinterpret_cast<uint4*>(s0) = make_uint4(pack_f16x2(y0[0], y0[1]), pack_f16x2(y0[2], y0[3]),
-                                                     pack_f16x2(y0[4], y0[5]), pack_f16x2(y0[6], y0[7]));
-          *reinterpret_cast<uint4*>(s1) = make_uint4(pack_f16x2(y1[0], y1[1]), pack_f16x2(y1[2], y1[3]),
-                                                     pack_f16x2(y1[4], y1[5]), pack_f16x2(y1[6], y1[7]));
+          *reinterpret_cast<uint4*>(s0) = make_uint4(pack_f16x2(y0[0], y0[1], sat), pack_f16x2(y0[2], y0[3], sat),
+                                                     pack_f16x2(y0[4], y0[5], sat), pack_f16x2(y0[6], y0[7], sat));
+          *reinterpret_cast<uint4*>(s1) = make_uint4(pack_f16x2(y1[0], y1[1], sat), pack_f16x2(y1[2], y1[3], sat),
+                                                     pack_f16x2(y1[4], y1[5], sat), pack_f16x2(y1[6], y1[7], sat));
         } else {  // k, prefill q high part: bf16
           *reinterpret_cast<uint4*>(s0) = make_uint4(pack_bf16x2(y0[0], y0[1]), pack_bf16x2(y0[2], y0[3]),
                                                      pack_bf16x2(y0[4], y0[5]), pack_bf16x2(y0[6], y0[7]));
@@ -627,16 +643,15 @@ __device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, const CUtenso
     }
     const int g = kind[hb] == 1 ? sh - e.nq_l : sh - e.nq_l - e.nkv_l;
     {
-      // k / v of one sequence at consecutive positions: 32 consecutive cache rows
-      const int slot0 = __shfl_sync(0xffffffffu, tp.seq_slot, 0);
-      const int pos0 = __shfl_sync(0xffffffffu, tp.pos, 0);
-      if (__all_sync(0xffffffffu, live && tp.seq_slot == slot0 && tp.pos == pos0 + lane)) {
+      // k / v of 32 tokens at consecutive rows of one cache block (one sequence at
+      // consecutive positions, not crossing a page): 32 consecutive cache rows
+      const int blk0 = __shfl_sync(0xffffffffu, tp.blk, 0);
+      const int brow0 = __shfl_sync(0xffffffffu, tp.brow, 0);
+      if (__all_sync(0xffffffffu, live && tp.blk == blk0 && tp.brow == brow0 + lane)) {
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          const int crow = static_cast<int>(
-              (((static_cast<int64_t>(r) * 2 + (kind[hb] == 2 ? 1 : 0)) * e.max_seqs + slot0) * e.nkv_l + g) * e.cap +
-              pos0);
+          const int crow = static_cast<int>(kv_row(e.kvm, e.nkv_l, r, kind[hb] == 2 ? 1 : 0, blk0, g, brow0));
 #pragma unroll
           for (int sg = 0; sg < 2; ++sg) tma_store_2d(tmKV, smem_u32(stg + sg * 32 * SEGB), sg * HALF + w * QP, crow);
           bulk_commit();
@@ -649,8 +664,7 @@ __device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, const CUtenso
     // cache row comes from its owner lane
     const unsigned long long my_dst =
         live ? reinterpret_cast<unsigned long long>(
-                   kv + (2 * static_cast<size_t>(r) + (kind[hb] == 2 ? 1 : 0)) * plane +
-                   ((static_cast<size_t>(tp.seq_slot) * e.nkv_l + g) * e.cap + tp.pos) * HD)
+                   kv + kv_row(e.kvm, e.nkv_l, r, kind[hb] == 2 ? 1 : 0, tp.blk, g, tp.brow) * HD)
              : 0ull;
 #pragma unroll
     for (int i = 0; i < 2 * NC; ++i) {
@@ -668,7 +682,7 @@ __device__ __forceinline__ bool qkv_pair_tile(const GemmParams& p, const CUtenso
 // Streams the heads of one accumulator tile (tokens on the M side) through qkv_head.
 template <int BN, int HD>
 __device__ __forceinline__ void qkv_stream(const GemmParams& p, uint32_t ta, int t, const TokPos& tp, int f0,
-                                           bool row_ok, int c_begin, int c_end, float rinv) {
+                                           bool row_ok, int c_begin, int c_end, float rinv, uint32_t& sat) {
 #pragma unroll 1
   for (int hb = c_begin / HD; hb < c_end / HD; ++hb) {
     const int col0 = f0 + hb * HD;
@@ -681,7 +695,7 @@ __device__ __forceinline__ void qkv_stream(const GemmParams& p, uint32_t ta, int
 #pragma unroll
       for (int i = 0; i < 32; ++i) h[c * 32 + i] = v[i] * rinv;
     }
-    if (row_ok && tp.ok) qkv_head<HD>(p, t, tp, col0, h);
+    if (row_ok && tp.ok) qkv_head<HD>(p, t, tp, col0, h, sat);
   }
 }
 
@@ -698,14 +712,13 @@ __device__ __forceinline__ void qkv_stream(const GemmParams& p, uint32_t ta, int
 // TPAttention.forward: q_norm / k_norm, apply_rope, cache.update.)
 template <int HD>
 __device__ __forceinline__ void qkv_row_group(const GemmParams& p, int t, const TokPos& tp, int col0, int gl,
-                                              float4 v) {
+                                              float4 v, uint32_t& sat) {
   const QkvEpi& q = p.qkv;
   constexpr int G = HD / 4;  // lanes per head
   constexpr int HALF = HD / 2;
   const int r = col0 / q.w_rank;
   const int sh = (col0 - r * q.w_rank) / HD;
   const int d0 = 4 * gl;  // first dim of this lane
-  const size_t plane = static_cast<size_t>(q.max_seqs) * q.nkv_l * q.cap * HD;
   __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(q.kv);
   float y[4] = {v.x, v.y, v.z, v.w};
   const bool is_v = sh >= q.nq_l + q.nkv_l, is_q = sh < q.nq_l;
@@ -747,19 +760,18 @@ __device__ __forceinline__ void qkv_row_group(const GemmParams& p, int t, const 
       *reinterpret_cast<uint2*>(qlo) = make_uint2(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]));
     } else {  // fp16 (decode attention runs in fp32)
       __half* q16 = reinterpret_cast<__half*>(p.out) + static_cast<size_t>(t) * p.ldo + col0 + d0;
-      *reinterpret_cast<uint2*>(q16) = make_uint2(pack_f16x2(y[0], y[1]), pack_f16x2(y[2], y[3]));
+      *reinterpret_cast<uint2*>(q16) = make_uint2(pack_f16x2(y[0], y[1], sat), pack_f16x2(y[2], y[3], sat));
     }
     return;
   }
   const int g = is_v ? sh - q.nq_l - q.nkv_l : sh - q.nq_l;
-  __nv_bfloat16* dst = kv + (2 * static_cast<size_t>(r) + (is_v ? 1 : 0)) * plane +
-                       ((static_cast<size_t>(tp.seq_slot) * q.nkv_l + g) * q.cap + tp.pos) * HD + d0;
+  __nv_bfloat16* dst = kv + kv_row(q.kvm, q.nkv_l, r, is_v ? 1 : 0, tp.blk, g, tp.brow) * HD + d0;
   *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
 }
 
 // One token row t of a swapped tile (features f0 .. f0+127; this lane: f0 + 4 lane ..).
 template <int EPI>
-__device__ __forceinline__ void swap_row(const GemmParams& p, int t, int f0, int lane, float4 v) {
+__device__ __forceinline__ void swap_row(const GemmParams& p, int t, int f0, int lane, float4 v, uint32_t& sat) {
   if constexpr (EPI == EPI_RESID) {  // residual += row (fp32, in place)
     const int f = f0 + 4 * lane;
     float* o = reinterpret_cast<float*>(p.out) + static_cast<size_t>(t) * p.ldo + f;
@@ -776,11 +788,11 @@ __device__ __forceinline__ void swap_row(const GemmParams& p, int t, int f0, int
     const int f = f0 + 4 * lane;
     __half* o = reinterpret_cast<__half*>(p.out) + static_cast<size_t>(t) * p.ldo + f;
     if (f + 4 <= p.out_cols) {
-      *reinterpret_cast<uint2*>(o) = make_uint2(pack_f16x2(v.x, v.y), pack_f16x2(v.z, v.w));
+      *reinterpret_cast<uint2*>(o) = make_uint2(pack_f16x2(v.x, v.y, sat), pack_f16x2(v.z, v.w, sat));
     } else {
       const float vv[4] = {v.x, v.y, v.z, v.w};
       for (int i = 0; i < 4; ++i)
-        if (f + i < p.out_cols) o[i] = __float2half_rn(sat_f16(vv[i]));
+        if (f + i < p.out_cols) o[i] = to_f16(vv[i], sat);
     }
   } else if constexpr (EPI == EPI_SILU) {
     // tile rows 0..63 are gate rows, 64..127 the matching up rows: lane l < 16 pairs
@@ -795,11 +807,11 @@ __device__ __forceinline__ void swap_row(const GemmParams& p, int t, int f0, int
       __half* o = reinterpret_cast<__half*>(p.out) + static_cast<size_t>(t) * p.ldo + fo;
       const float a0 = silu_f(v.x) * u.x, a1 = silu_f(v.y) * u.y, a2 = silu_f(v.z) * u.z, a3 = silu_f(v.w) * u.w;
       if (fo + 4 <= p.out_cols) {
-        *reinterpret_cast<uint2*>(o) = make_uint2(pack_f16x2(a0, a1), pack_f16x2(a2, a3));
+        *reinterpret_cast<uint2*>(o) = make_uint2(pack_f16x2(a0, a1, sat), pack_f16x2(a2, a3, sat));
       } else {
         const float aa[4] = {a0, a1, a2, a3};
         for (int i = 0; i < 4; ++i)
-          if (fo + i < p.out_cols) o[i] = __float2half_rn(sat_f16(aa[i]));
+          if (fo + i < p.out_cols) o[i] = to_f16(aa[i], sat);
       }
     }
   }
@@ -807,12 +819,12 @@ __device__ __forceinline__ void swap_row(const GemmParams& p, int t, int f0, int
 
 // The q/k/v heads of one token row of a swapped QKV tile (warp-uniform token).
 __device__ __forceinline__ void swap_qkv_row(const GemmParams& p, int t, const TokPos& tp, int f0, int lane,
-                                             float4 v) {
+                                             float4 v, uint32_t& sat) {
   if (f0 >= p.N) return;
   if (p.qkv.hd == 128) {
-    qkv_row_group<128>(p, t, tp, f0, lane, v);
+    qkv_row_group<128>(p, t, tp, f0, lane, v, sat);
   } else {  // two 64-dim heads per tile: lanes 0..15 and 16..31
-    qkv_row_group<64>(p, t, tp, f0 + (lane >> 4) * 64, lane & 15, v);
+    qkv_row_group<64>(p, t, tp, f0 + (lane >> 4) * 64, lane & 15, v, sat);
   }
 }
 
@@ -825,9 +837,10 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
   const int row = q * 32 + lane;  // feature row of the tile
   const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
   const uint32_t tfull0 = bar0 + 8u * (2 * stages), tempty0 = bar0 + 8u * (2 * stages + 2);
+  uint32_t sat = 0;  // an fp16 output clamped to the fp16 range (reported at the end)
   // every unit covers the same tokens (one token tile): their deferred-RMSNorm
-  // row scales once (sInv: [BN], after the [3][BN] position table)
-  float* sInv = reinterpret_cast<float*>(sPos + 192);
+  // row scales once (sInv: [BN], after the [4][BN] position table)
+  float* sInv = reinterpret_cast<float*>(sPos + 256);
   if constexpr (EPI == EPI_QKV || EPI == EPI_SILU) {
     const int et = threadIdx.x - 64;
     if (et < BN) sInv[et] = et < p.T ? row_scale(p, et) : 0.0f;
@@ -835,20 +848,19 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
   }
   if constexpr (EPI == EPI_QKV) {
     // every unit covers the same tokens (one token tile): their positions once, in
-    // parallel (sPos: [BN] position, [BN] cache slot, [BN] flags 1 = valid, 2 = prefill)
+    // parallel (sPos: [BN] position, [BN] cache block, [BN] row in the block, [BN]
+    // flags 1 = valid, 2 = prefill)
     const int et = threadIdx.x - 64;
     if (et < BN) {
-      int pos = 0, slot = 0, fl = 0;
+      TokPos tp{0, 0, 0, false, false};
       if (et < p.T) {
-        const TokPos tp = token_position(p.qkv, et);
+        tp = token_position(p.qkv, et);
         if (!tp.ok) raise_flag(p.status, TP_DEVFLAG_BAD_TOKEN);
-        pos = tp.pos;
-        slot = tp.seq_slot;
-        fl = (tp.ok ? 1 : 0) | (tp.prefill ? 2 : 0);
       }
-      sPos[et] = pos;
-      sPos[BN + et] = slot;
-      sPos[2 * BN + et] = fl;
+      sPos[et] = tp.pos;
+      sPos[BN + et] = tp.blk;
+      sPos[2 * BN + et] = tp.brow;
+      sPos[3 * BN + et] = (tp.ok ? 1 : 0) | (tp.prefill ? 2 : 0);
     }
     named_bar_sync(1, 128);
   }
@@ -890,7 +902,10 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
       ++seg;
     }
     // every epilogue thread takes the same path from here (named barriers follow)
-    if (!named_bar_and(1, 128, ok)) break;
+    if (!named_bar_and(1, 128, ok)) {
+      if (threadIdx.x == 64) drain_split_counters(p, u, units);
+      break;
+    }
     if (p.splits > 1) {
       const int tile = un.tt * p.tiles_f + un.tf;
       float* part = p.partials + (static_cast<size_t>(tile) * p.splits + un.split) * (BN * 128);
@@ -945,7 +960,7 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
             *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + tok * p.ldo + f) = y;
             if (stats) {
               *reinterpret_cast<uint2*>(p.row_out16 + tok * p.out_cols + f) =
-                  make_uint2(pack_f16x2(y.x, y.y), pack_f16x2(y.z, y.w));
+                  make_uint2(pack_f16x2(y.x, y.y, sat), pack_f16x2(y.z, y.w, sat));
               float s = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
               s += __shfl_xor_sync(0xffffffffu, s, 1);
               s += __shfl_xor_sync(0xffffffffu, s, 2);
@@ -966,7 +981,7 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
               const float y = o[f + i] + vv[i];
               o[f + i] = y;
               if (stats) {
-                p.row_out16[tok * p.out_cols + f + i] = __float2half_rn(sat_f16(y));
+                p.row_out16[tok * p.out_cols + f + i] = to_f16(y, sat);
                 s += y * y;
               }
             }
@@ -990,20 +1005,22 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
           v.w *= ri;
         }
         if constexpr (EPI == EPI_QKV) {
-          const int fl = sPos[2 * BN + t];
+          const int fl = sPos[3 * BN + t];
           TokPos tp;
           tp.pos = sPos[t];
-          tp.seq_slot = sPos[BN + t];
+          tp.blk = sPos[BN + t];
+          tp.brow = sPos[2 * BN + t];
           tp.ok = (fl & 1) != 0;
           tp.prefill = (fl & 2) != 0;
-          if (tp.ok) swap_qkv_row(p, un.tt * BN + t, tp, f0, lane, v);
+          if (tp.ok) swap_qkv_row(p, un.tt * BN + t, tp, f0, lane, v, sat);
         } else {
-          swap_row<EPI>(p, un.tt * BN + t, f0, lane, v);
+          swap_row<EPI>(p, un.tt * BN + t, f0, lane, v, sat);
         }
       }
     }
     named_bar_sync(1, 128);  // the staging rows are reused by the next unit
   }
+  report_sat(p.status, sat);
 }
 
 template <int BN, int EPI, bool ACC, bool SWAP>
@@ -1291,9 +1308,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
     }
     // Each CTA folds its per-token best into one 64-bit key per token with
     // atomicMax (key order = torch.argmax order); the last CTA to finish reads the
-    // keys back, writes the ids and clears the keys for the next launch.
-    if (named_bar_and(1, 128, ok)) {
-      for (int t = et; t < p.T; t += 128) atomicMax(p.amax_keys + t, amax_key(best_v[t], best_i[t]));
+    // keys back, writes the ids and clears the keys for the next launch.  A CTA
+    // whose wait gave up (TP_DEVFLAG_TIMEOUT is set, the ids are not valid) adds
+    // no key but still counts itself in, so the counters and keys always return
+    // to zero for the next launch.
+    {
+      const bool all_ok = named_bar_and(1, 128, ok);
+      if (all_ok)
+        for (int t = et; t < p.T; t += 128) atomicMax(p.amax_keys + t, amax_key(best_v[t], best_i[t]));
       __threadfence();
       named_bar_sync(1, 128);
       if (et == 0) *last_flag = (atomicAdd(p.done_counter, 1) == static_cast<int>(gridDim.x) - 1) ? 1 : 0;
@@ -1326,6 +1348,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
     // (the first is `box`) and then its fp16 row box
     uint8_t* box = sOut + (warp - 2) * (C::RESID_ROWS ? C::NXB * 4096 + 2048 : 4096);
     uint8_t* box16 = box + C::NXB * 4096;
+    uint32_t sat = 0;  // an fp16 output clamped to the fp16 range (reported at the end)
     if constexpr (C::QKV_PAIR) {
       const int e = threadIdx.x - 64;
       if (e < p.qkv.hd) {
@@ -1351,7 +1374,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
           for (int k = 0; k < C::NXB; ++k) prefetch_rows32(p, box + k * 4096, t, row_ok, f0 + cbase + 32 * k, lane);
         }
       }
-      TokPos tp{0, 0, false};
+      TokPos tp{0, 0, 0, false, false};
       if constexpr (EPI == EPI_QKV) {
         if (row_ok) {
           tp = token_position(p.qkv, t);
@@ -1366,9 +1389,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
         uint8_t* stg = sStg + (warp - 2) * (2 * 32 * 128);
         const bool ok = p.qkv.hd == 128
                             ? qkv_pair_tile<BN, 128>(p, &tmO, &tmO2, &tmKV, TFULL(b), use, abort_flag, ta, t, tp, f0,
-                                                     row_ok, w, q, row, seg & 1, sNw, sSS, stg, rinv)
+                                                     row_ok, w, q, row, seg & 1, sNw, sSS, stg, rinv, sat)
                             : qkv_pair_tile<BN, 64>(p, &tmO, &tmO2, &tmKV, TFULL(b), use, abort_flag, ta, t, tp, f0,
-                                                    row_ok, w, q, row, seg & 1, sNw, sSS, stg, rinv);
+                                                    row_ok, w, q, row, seg & 1, sNw, sSS, stg, rinv, sat);
         if (!ok) break;
         tc_fence_before();
         __syncwarp();
@@ -1382,9 +1405,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
         const uint32_t ta = lane_addr + static_cast<uint32_t>(b * BN);
         if constexpr (EPI == EPI_QKV) {
           if (BN >= 128 && p.qkv.hd == 128) {
-            qkv_stream<BN, (BN >= 128 ? 128 : 64)>(p, ta, t, tp, f0, row_ok, cbase, cbase + BNH, rinv);
+            qkv_stream<BN, (BN >= 128 ? 128 : 64)>(p, ta, t, tp, f0, row_ok, cbase, cbase + BNH, rinv, sat);
           } else {
-            qkv_stream<BN, 64>(p, ta, t, tp, f0, row_ok, cbase, cbase + BNH, rinv);
+            qkv_stream<BN, 64>(p, ta, t, tp, f0, row_ok, cbase, cbase + BNH, rinv, sat);
           }
         } else if constexpr (EPI == EPI_SILU) {
           // gate/up interleaved in 64-column blocks: 128 accumulator columns = 64 outputs
@@ -1400,7 +1423,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
               for (int i = 0; i < 32; ++i) o[h * 32 + i] = silu_f(gv[i] * rinv) * (uv[i] * rinv);
             }
             box_acquire(lane);
-            stage_f16x64(box, lane, o);
+            stage_f16x64(box, lane, o, sat);
             box_release(&tmO, box, f0 / 2 + qb * 64, tbox, false, lane);
           }
         } else if constexpr (EPI == EPI_ARGMAX) {
@@ -1426,7 +1449,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
               const int k = c - cbase / 32;
               if (k == 0) cp_async_wait_all();
               resid_rows32<C>(p, &tmO, &tmO2, k < C::NXB ? box + k * 4096 : box, box16, t, row_ok, f0 + c * 32,
-                              tbox, lane, v, k < C::NXB);
+                              tbox, lane, v, k < C::NXB, sat);
             } else {
               box_acquire(lane);
               stage_f32x32(box, lane, v);
@@ -1440,7 +1463,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
             tc_ld32(ta + c * 64, *reinterpret_cast<float(*)[32]>(v));
             tc_ld32(ta + c * 64 + 32, *reinterpret_cast<float(*)[32]>(v + 32));
             box_acquire(lane);
-            stage_f16x64(box, lane, v);
+            stage_f16x64(box, lane, v, sat);
             box_release(&tmO, box, f0 + c * 64, tbox, false, lane);
           }
         }
@@ -1476,7 +1499,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
           ++seg;
         }
         // every epilogue thread takes the same path from here (named barriers follow)
-        if (!named_bar_and(1, 32 * C::EW, ok)) break;
+        if (!named_bar_and(1, 32 * C::EW, ok)) {
+          if (threadIdx.x == 64) drain_split_counters(p, u, units);
+          break;
+        }
         if (p.splits > 1) {
           const int tile = un.tt * p.tiles_f + un.tf;
           float* part = p.partials + (static_cast<size_t>(tile) * p.splits + un.split) * (BN * 128);
@@ -1522,7 +1548,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[h * 32 + i] = silu_f(acc[qb * 128 + h * 32 + i]) * acc[qb * 128 + 64 + h * 32 + i];
               box_acquire(lane);
-              stage_f16x64(box, lane, o);
+              stage_f16x64(box, lane, o, sat);
               box_release(&tmO, box, f0 / 2 + (cbase / 128 + qb) * 64, tbox, false, lane);
             }
           } else if constexpr (EPI == EPI_RESID) {
@@ -1531,7 +1557,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
               if (p.row_ss_out != nullptr) {  // uniform: read-add-store and the next norm's inputs
                 if (c == 0) cp_async_wait_all();
                 resid_rows32<C>(p, &tmO, &tmO2, c < C::NXB ? box + c * 4096 : box, box16, t, row_ok,
-                                f0 + cbase + c * 32, tbox, lane, acc + c * 32, c < C::NXB);
+                                f0 + cbase + c * 32, tbox, lane, acc + c * 32, c < C::NXB, sat);
               } else {
                 box_acquire(lane);
                 stage_f32x32(box, lane, acc + c * 32);
@@ -1542,7 +1568,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
 #pragma unroll
             for (int c = 0; c < BNH / 64; ++c) {
               box_acquire(lane);
-              stage_f16x64(box, lane, acc + c * 64);
+              stage_f16x64(box, lane, acc + c * 64, sat);
               box_release(&tmO, box, f0 + cbase + c * 64, tbox, false, lane);
             }
           }
@@ -1554,13 +1580,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
                 if (p.qkv.hd == 128) {
 #pragma unroll
                   for (int hb = 0; hb < BN / 128; ++hb)
-                    if (f0 + hb * 128 < p.N) qkv_head<128>(p, t, tp, f0 + hb * 128, acc + hb * 128);
+                    if (f0 + hb * 128 < p.N) qkv_head<128>(p, t, tp, f0 + hb * 128, acc + hb * 128, sat);
                 }
               }
               if (p.qkv.hd == 64) {
 #pragma unroll
                 for (int hb = 0; hb < BN / 64; ++hb)
-                  if (f0 + hb * 64 < p.N) qkv_head<64>(p, t, tp, f0 + hb * 64, acc + hb * 64);
+                  if (f0 + hb * 64 < p.N) qkv_head<64>(p, t, tp, f0 + hb * 64, acc + hb * 64, sat);
               }
             }
           } else if constexpr (EPI == EPI_ARGMAX) {
@@ -1575,6 +1601,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
         }
       }
     }
+    report_sat(p.status, sat);
     if constexpr (C::RESID_ROWS) cp_async_wait_all();  // no copy into the staging outlives the CTA
     if constexpr (C::TMA_OUT || C::QKV_PAIR) {  // every store has landed before the CTA (and its staging) goes away
       if (lane == 0) bulk_wait_all();
@@ -1755,11 +1782,10 @@ static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, 
   auto kern = gemm_tc_kernel<BN, EPI, ACC, SWAP>;
   using Cfg = GemmCfg<BN, EPI, ACC, SWAP>;
   constexpr int smem = Cfg::SMEM;
-  static bool attr_done = false;  // per instantiation
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static PerDevice attr;  // per instantiation and device
+  {
+    const cudaError_t e = smem_attr_per_device(attr, kern, smem);
     if (e != cudaSuccess) return e;
-    attr_done = true;
   }
   CUtensorMap mo = mx;  // unused unless the outputs leave through TMA
   CUtensorMap mo2 = mx;  // fp16 residual rows of the residual epilogues (row_ss_out set)
@@ -1776,7 +1802,7 @@ static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, 
   if constexpr (Cfg::QKV_PAIR) {  // q rows (high / fp16 part, low part) leave through TMA
     const int qp = pr.qkv.hd / 4;
     const int64_t kv_rows =
-        static_cast<int64_t>(pr.qkv.n) * 2 * pr.qkv.max_seqs * pr.qkv.nkv_l * static_cast<int64_t>(pr.qkv.cap);
+        static_cast<int64_t>(pr.qkv.n) * 2 * pr.qkv.kvm.blocks * pr.qkv.nkv_l * static_cast<int64_t>(pr.qkv.kvm.block_len);
     if (pr.ldo != pr.out_cols || !pr.qkv.q_lo || kv_rows >= (int64_t(1) << 31) ||
         !make_map_rows16(&mo, pr.out, pr.T, pr.ldo, qp) ||
         !make_map_rows16(&mo2, pr.qkv.q_lo, pr.T, static_cast<int64_t>(pr.qkv.n) * pr.qkv.nq_l * pr.qkv.hd, qp) ||

@@ -36,6 +36,7 @@ __global__ void embed_vocab_parallel_kernel(const int32_t* __restrict__ ids, con
   if (threadIdx.x == 0 && (id < 0 || id >= vocab)) raise_flag(status, TP_DEVFLAG_BAD_TOKEN);
   const int chunks = H / 8;
   const int trips = (chunks + blockDim.x - 1) / blockDim.x;  // the same on every lane (group shuffles)
+  uint32_t sat = 0;  // an fp16 row element clamped to the fp16 range
   for (int k = 0; k < trips; ++k) {
     const int c = threadIdx.x + k * blockDim.x;
     const bool live = c < chunks;
@@ -65,15 +66,16 @@ __global__ void embed_vocab_parallel_kernel(const int32_t* __restrict__ ids, con
       s += __shfl_xor_sync(0xffffffffu, s, 2);
       if (live) {
         uint4 o;
-        o.x = pack_f16x2(acc[0], acc[1]);
-        o.y = pack_f16x2(acc[2], acc[3]);
-        o.z = pack_f16x2(acc[4], acc[5]);
-        o.w = pack_f16x2(acc[6], acc[7]);
+        o.x = pack_f16x2(acc[0], acc[1], sat);
+        o.y = pack_f16x2(acc[2], acc[3], sat);
+        o.z = pack_f16x2(acc[4], acc[5], sat);
+        o.w = pack_f16x2(acc[6], acc[7], sat);
         xh[static_cast<int64_t>(t) * chunks + c] = o;
         if ((c & 3) == 0) ss[static_cast<int64_t>(t) * (H / 32) + c / 4] = s;
       }
     }
   }
+  report_sat(status, sat);
 }
 
 cudaError_t launch_embed(const int32_t* ids, int T, const void* embed_stacked, int n, int64_t v_local,
@@ -98,7 +100,7 @@ constexpr uint32_t kOnes2 = 0x3F803F80u;
 // ---------------------------------------------------------------------------
 template <int VPL>  // 8-element groups per lane kept in registers
 __global__ void rmsnorm_kernel(const float4* __restrict__ x, int64_t rows, int H, const uint4* __restrict__ w,
-                               float eps, uint4* __restrict__ out, const int32_t* __restrict__ cu_last) {
+                               float eps, uint4* __restrict__ out, const int32_t* __restrict__ cu_last, int* status) {
   griddep_wait();
   griddep_launch();
   const int warps = blockDim.x / 32;
@@ -123,6 +125,7 @@ __global__ void rmsnorm_kernel(const float4* __restrict__ x, int64_t rows, int H
   }
   ss = warp_sum(ss);
   const float inv = rsqrtf(ss / static_cast<float>(H) + eps);
+  uint32_t sat = 0;
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
     const int c = lane + 32 * j;
@@ -131,18 +134,20 @@ __global__ void rmsnorm_kernel(const float4* __restrict__ x, int64_t rows, int H
       const float wf[8] = {bf16lo(wu.x), bf16hi(wu.x), bf16lo(wu.y), bf16hi(wu.y),
                            bf16lo(wu.z), bf16hi(wu.z), bf16lo(wu.w), bf16hi(wu.w)};
       uint4 o;
-      o.x = pack_f16x2(v[j][0] * inv * wf[0], v[j][1] * inv * wf[1]);
-      o.y = pack_f16x2(v[j][2] * inv * wf[2], v[j][3] * inv * wf[3]);
-      o.z = pack_f16x2(v[j][4] * inv * wf[4], v[j][5] * inv * wf[5]);
-      o.w = pack_f16x2(v[j][6] * inv * wf[6], v[j][7] * inv * wf[7]);
+      o.x = pack_f16x2(v[j][0] * inv * wf[0], v[j][1] * inv * wf[1], sat);
+      o.y = pack_f16x2(v[j][2] * inv * wf[2], v[j][3] * inv * wf[3], sat);
+      o.z = pack_f16x2(v[j][4] * inv * wf[4], v[j][5] * inv * wf[5], sat);
+      o.w = pack_f16x2(v[j][6] * inv * wf[6], v[j][7] * inv * wf[7], sat);
       out[row * chunks + c] = o;
     }
   }
+  report_sat(status, sat);
 }
 
 // Wide rows (H > 2048): one warp per row, two passes (the second re-reads the row from L1/L2).
 __global__ void rmsnorm_wide_kernel(const float4* __restrict__ x, int64_t rows, int H, const uint4* __restrict__ w,
-                                    float eps, uint4* __restrict__ out, const int32_t* __restrict__ cu_last) {
+                                    float eps, uint4* __restrict__ out, const int32_t* __restrict__ cu_last,
+                                    int* status) {
   griddep_wait();
   griddep_launch();
   const int warps = blockDim.x / 32;
@@ -159,16 +164,18 @@ __global__ void rmsnorm_wide_kernel(const float4* __restrict__ x, int64_t rows, 
   }
   ss = warp_sum(ss);
   const float inv = rsqrtf(ss / static_cast<float>(H) + eps);
+  uint32_t sat = 0;
   for (int c = lane; c < chunks; c += 32) {
     const float4 a = xr[2 * c], b = xr[2 * c + 1];
     const uint4 wu = w ? w[c] : make_uint4(kOnes2, kOnes2, kOnes2, kOnes2);
     uint4 o;
-    o.x = pack_f16x2(a.x * inv * bf16lo(wu.x), a.y * inv * bf16hi(wu.x));
-    o.y = pack_f16x2(a.z * inv * bf16lo(wu.y), a.w * inv * bf16hi(wu.y));
-    o.z = pack_f16x2(b.x * inv * bf16lo(wu.z), b.y * inv * bf16hi(wu.z));
-    o.w = pack_f16x2(b.z * inv * bf16lo(wu.w), b.w * inv * bf16hi(wu.w));
+    o.x = pack_f16x2(a.x * inv * bf16lo(wu.x), a.y * inv * bf16hi(wu.x), sat);
+    o.y = pack_f16x2(a.z * inv * bf16lo(wu.y), a.w * inv * bf16hi(wu.y), sat);
+    o.z = pack_f16x2(b.x * inv * bf16lo(wu.z), b.y * inv * bf16hi(wu.z), sat);
+    o.w = pack_f16x2(b.z * inv * bf16lo(wu.w), b.w * inv * bf16hi(wu.w), sat);
     out[row * chunks + c] = o;
   }
+  report_sat(status, sat);
 }
 
 // Few long rows (decode): one 256-thread block per row, every 8-element chunk of
@@ -177,7 +184,7 @@ template <int CPT>
 __global__ void __launch_bounds__(256) rmsnorm_row_block_kernel(const float4* __restrict__ x, int64_t rows, int H,
                                                                  const uint4* __restrict__ w, float eps,
                                                                  uint4* __restrict__ out,
-                                                                 const int32_t* __restrict__ cu_last) {
+                                                                 const int32_t* __restrict__ cu_last, int* status) {
   griddep_wait();
   griddep_launch();
   __shared__ float red[8];
@@ -205,6 +212,7 @@ __global__ void __launch_bounds__(256) rmsnorm_row_block_kernel(const float4* __
 #pragma unroll
   for (int i = 0; i < 8; ++i) tot += red[i];
   const float inv = rsqrtf(tot / static_cast<float>(H) + eps);
+  uint32_t sat = 0;
 #pragma unroll
   for (int j = 0; j < CPT; ++j) {
     const int c = threadIdx.x + 256 * j;
@@ -213,17 +221,18 @@ __global__ void __launch_bounds__(256) rmsnorm_row_block_kernel(const float4* __
       const float wf[8] = {bf16lo(wu.x), bf16hi(wu.x), bf16lo(wu.y), bf16hi(wu.y),
                            bf16lo(wu.z), bf16hi(wu.z), bf16lo(wu.w), bf16hi(wu.w)};
       uint4 o;
-      o.x = pack_f16x2(v[j][0] * inv * wf[0], v[j][1] * inv * wf[1]);
-      o.y = pack_f16x2(v[j][2] * inv * wf[2], v[j][3] * inv * wf[3]);
-      o.z = pack_f16x2(v[j][4] * inv * wf[4], v[j][5] * inv * wf[5]);
-      o.w = pack_f16x2(v[j][6] * inv * wf[6], v[j][7] * inv * wf[7]);
+      o.x = pack_f16x2(v[j][0] * inv * wf[0], v[j][1] * inv * wf[1], sat);
+      o.y = pack_f16x2(v[j][2] * inv * wf[2], v[j][3] * inv * wf[3], sat);
+      o.z = pack_f16x2(v[j][4] * inv * wf[4], v[j][5] * inv * wf[5], sat);
+      o.w = pack_f16x2(v[j][6] * inv * wf[6], v[j][7] * inv * wf[7], sat);
       out[row * chunks + c] = o;
     }
   }
+  report_sat(status, sat);
 }
 
 static cudaError_t rmsnorm_rows(const void* x, int64_t rows, int H, const void* w, float eps, void* out,
-                                const int32_t* cu_last, cudaStream_t s) {
+                                const int32_t* cu_last, int* status, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const int chunks = H / 8;
   if (rows <= 256 && chunks > 128 && chunks <= 4 * 256) {  // few long rows: a block per row
@@ -231,9 +240,9 @@ static cudaError_t rmsnorm_rows(const void* x, int64_t rows, int H, const void* 
     auto W = reinterpret_cast<const uint4*>(w);
     auto O = reinterpret_cast<uint4*>(out);
     const dim3 grid(static_cast<unsigned>(rows)), block(256);
-    if (chunks <= 256) return launch_pdl(rmsnorm_row_block_kernel<1>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
-    if (chunks <= 512) return launch_pdl(rmsnorm_row_block_kernel<2>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
-    return launch_pdl(rmsnorm_row_block_kernel<4>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
+    if (chunks <= 256) return launch_pdl(rmsnorm_row_block_kernel<1>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last, status);
+    if (chunks <= 512) return launch_pdl(rmsnorm_row_block_kernel<2>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last, status);
+    return launch_pdl(rmsnorm_row_block_kernel<4>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last, status);
   }
   const int vpl = (H / 8 + 31) / 32;
   const int warps = 4;
@@ -241,11 +250,11 @@ static cudaError_t rmsnorm_rows(const void* x, int64_t rows, int H, const void* 
   auto X = reinterpret_cast<const float4*>(x);
   auto W = reinterpret_cast<const uint4*>(w);
   auto O = reinterpret_cast<uint4*>(out);
-  if (vpl <= 1) return launch_pdl(rmsnorm_kernel<1>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
-  if (vpl <= 2) return launch_pdl(rmsnorm_kernel<2>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
-  if (vpl <= 4) return launch_pdl(rmsnorm_kernel<4>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
-  if (vpl <= 8) return launch_pdl(rmsnorm_kernel<8>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
-  return launch_pdl(rmsnorm_wide_kernel, grid, block, 0, s, X, rows, H, W, eps, O, cu_last);
+  if (vpl <= 1) return launch_pdl(rmsnorm_kernel<1>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last, status);
+  if (vpl <= 2) return launch_pdl(rmsnorm_kernel<2>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last, status);
+  if (vpl <= 4) return launch_pdl(rmsnorm_kernel<4>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last, status);
+  if (vpl <= 8) return launch_pdl(rmsnorm_kernel<8>, grid, block, 0, s, X, rows, H, W, eps, O, cu_last, status);
+  return launch_pdl(rmsnorm_wide_kernel, grid, block, 0, s, X, rows, H, W, eps, O, cu_last, status);
 }
 
 // Row statistics for a deferred RMSNorm (the norm itself happens in the next
@@ -254,7 +263,7 @@ static cudaError_t rmsnorm_rows(const void* x, int64_t rows, int H, const void* 
 // warp per row; lane l takes 8-column chunks l, l + 32, ...; the 4 lanes of a
 // 32-column group add their sums with two shuffles.
 __global__ void row_stats_kernel(const float4* __restrict__ x, int64_t rows, int H, uint4* __restrict__ xh,
-                                 float* __restrict__ ss) {
+                                 float* __restrict__ ss, int* status) {
   griddep_wait();
   griddep_launch();
   const int warps = blockDim.x / 32;
@@ -263,6 +272,7 @@ __global__ void row_stats_kernel(const float4* __restrict__ x, int64_t rows, int
   if (row >= rows) return;  // warp-uniform
   const int chunks = H / 8, groups = H / 32;
   const float4* xr = x + row * (H / 4);
+  uint32_t sat = 0;
   for (int c0 = 0; c0 < chunks; c0 += 32) {  // same trip count on every lane
     const int c = c0 + lane;
     float s = 0.0f;
@@ -270,34 +280,37 @@ __global__ void row_stats_kernel(const float4* __restrict__ x, int64_t rows, int
       const float4 a = xr[2 * c], b = xr[2 * c + 1];
       s = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
       uint4 o;
-      o.x = pack_f16x2(a.x, a.y);
-      o.y = pack_f16x2(a.z, a.w);
-      o.z = pack_f16x2(b.x, b.y);
-      o.w = pack_f16x2(b.z, b.w);
+      o.x = pack_f16x2(a.x, a.y, sat);
+      o.y = pack_f16x2(a.z, a.w, sat);
+      o.z = pack_f16x2(b.x, b.y, sat);
+      o.w = pack_f16x2(b.z, b.w, sat);
       xh[row * chunks + c] = o;
     }
     s += __shfl_xor_sync(0xffffffffu, s, 1);
     s += __shfl_xor_sync(0xffffffffu, s, 2);
     if ((lane & 3) == 0 && c < chunks) ss[row * groups + c / 4] = s;
   }
+  report_sat(status, sat);
 }
 
-cudaError_t launch_row_stats(const void* x, int64_t rows, int H, void* xh, float* ss, cudaStream_t s) {
+cudaError_t launch_row_stats(const void* x, int64_t rows, int H, void* xh, float* ss, int* status,
+                             cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   if (H % 32) return cudaErrorInvalidValue;
   const int warps = 4;
   return launch_pdl(row_stats_kernel, dim3(static_cast<unsigned>((rows + warps - 1) / warps)), dim3(32 * warps), 0,
-                    s, reinterpret_cast<const float4*>(x), rows, H, reinterpret_cast<uint4*>(xh), ss);
+                    s, reinterpret_cast<const float4*>(x), rows, H, reinterpret_cast<uint4*>(xh), ss, status);
 }
 
-cudaError_t launch_rmsnorm(const void* x, int64_t rows, int H, const void* w, float eps, void* out, cudaStream_t s) {
-  return rmsnorm_rows(x, rows, H, w, eps, out, nullptr, s);
+cudaError_t launch_rmsnorm(const void* x, int64_t rows, int H, const void* w, float eps, void* out, int* status,
+                           cudaStream_t s) {
+  return rmsnorm_rows(x, rows, H, w, eps, out, nullptr, status, s);
 }
 
 // Final RMSNorm of each sequence's last token (row cu_q[b+1] - 1 of the residual stream).
 cudaError_t launch_final_norm_select(const void* hidden, int H, const int32_t* cu_q, int B, const void* w,
-                                     float eps, void* out, cudaStream_t s) {
-  return rmsnorm_rows(hidden, B, H, w, eps, out, cu_q, s);
+                                     float eps, void* out, int* status, cudaStream_t s) {
+  return rmsnorm_rows(hidden, B, H, w, eps, out, cu_q, status, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -306,12 +319,14 @@ cudaError_t launch_final_norm_select(const void* hidden, int H, const int32_t* c
 // round to fp16's subnormal grid (absolute error <= 2^-25), larger ones
 // saturate.
 // ---------------------------------------------------------------------------
-__global__ void bf16_to_f16_kernel(uint32_t* __restrict__ w, size_t n_pairs) {
+__global__ void bf16_to_f16_kernel(uint32_t* __restrict__ w, size_t n_pairs, int* status) {
+  uint32_t sat = 0;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n_pairs;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const uint32_t v = w[i];
-    w[i] = pack_f16x2(bf16lo(v), bf16hi(v));
+    w[i] = pack_f16x2(bf16lo(v), bf16hi(v), sat);
   }
+  report_sat(status, sat);
 }
 
 // W[r][c] * norm[c] -> fp16, in place ([rows][cols] bf16 in, fp16 out): an
@@ -319,31 +334,33 @@ __global__ void bf16_to_f16_kernel(uint32_t* __restrict__ w, size_t n_pairs) {
 // (xn W^T = (x * inv) (W * diag(w))^T).  The bf16 x bf16 product is exact in
 // fp32, so the only rounding is the one to fp16.
 __global__ void fold_norm_f16_kernel(uint32_t* __restrict__ w, size_t n_pairs, int cols,
-                                     const __nv_bfloat16* __restrict__ norm) {
+                                     const __nv_bfloat16* __restrict__ norm, int* status) {
+  uint32_t sat = 0;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n_pairs;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const uint32_t v = w[i];
     const int c = static_cast<int>((2 * i) % static_cast<size_t>(cols));  // cols is even
-    w[i] = pack_f16x2(bf16lo(v) * bf2f(norm[c]), bf16hi(v) * bf2f(norm[c + 1]));
+    w[i] = pack_f16x2(bf16lo(v) * bf2f(norm[c]), bf16hi(v) * bf2f(norm[c + 1]), sat);
   }
+  report_sat(status, sat);
 }
 
-cudaError_t launch_fold_norm_f16(void* w, size_t rows, int cols, const void* norm, cudaStream_t s) {
+cudaError_t launch_fold_norm_f16(void* w, size_t rows, int cols, const void* norm, int* status, cudaStream_t s) {
   const size_t pairs = rows * static_cast<size_t>(cols) / 2;
   if (pairs == 0) return cudaSuccess;
   if (cols % 2) return cudaErrorInvalidValue;
   const size_t blocks = (pairs + 255) / 256;
   fold_norm_f16_kernel<<<static_cast<unsigned>(blocks < 65536 ? blocks : 65536), 256, 0, s>>>(
-      reinterpret_cast<uint32_t*>(w), pairs, cols, reinterpret_cast<const __nv_bfloat16*>(norm));
+      reinterpret_cast<uint32_t*>(w), pairs, cols, reinterpret_cast<const __nv_bfloat16*>(norm), status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bf16_to_f16(void* w, size_t elems, cudaStream_t s) {
+cudaError_t launch_bf16_to_f16(void* w, size_t elems, int* status, cudaStream_t s) {
   if (elems == 0) return cudaSuccess;
   const size_t pairs = elems / 2;
   const size_t blocks = (pairs + 255) / 256;
   bf16_to_f16_kernel<<<static_cast<unsigned>(blocks < 65536 ? blocks : 65536), 256, 0, s>>>(
-      reinterpret_cast<uint32_t*>(w), pairs);
+      reinterpret_cast<uint32_t*>(w), pairs, status);
   return cudaGetLastError();
 }
 

@@ -7,9 +7,56 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 struct tp_ctx;
 
 namespace tpk {
+
+// One-time per-device set-up of a kernel (cudaFuncSetAttribute applies to the
+// current device only): bit d of `done` is set once device d is prepared, and
+// `value[d]` keeps a per-device result (an occupancy).  Devices >= 64 are
+// prepared on every call.  Two threads may both prepare a device; the calls are
+// idempotent.
+struct PerDevice {
+  std::atomic<uint64_t> done{0};
+  int value[64] = {};
+};
+inline bool per_device_ready(PerDevice& pd, int* dev, int* value) {
+  if (cudaGetDevice(dev) != cudaSuccess) *dev = -1;
+  if (*dev < 0 || *dev >= 64) return false;
+  if (!(pd.done.load(std::memory_order_acquire) >> *dev & 1u)) return false;
+  if (value) *value = pd.value[*dev];
+  return true;
+}
+inline void per_device_mark(PerDevice& pd, int dev, int value) {
+  if (dev < 0 || dev >= 64) return;
+  pd.value[dev] = value;
+  pd.done.fetch_or(uint64_t(1) << dev, std::memory_order_release);
+}
+// The kernel's dynamic shared-memory limit raised to smem bytes on the current device.
+template <typename K>
+inline cudaError_t smem_attr_per_device(PerDevice& pd, K kern, int smem) {
+  int dev = -1;
+  if (per_device_ready(pd, &dev, nullptr)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) per_device_mark(pd, dev, 1);
+  return e;
+}
+
+// The address a kernel uses for p: device (or managed) memory as it is, page-locked
+// host memory through its device mapping; null for memory the GPU cannot address.
+template <typename T>
+T* gpu_view(T* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return p;
+  if (a.type == cudaMemoryTypeHost) return static_cast<T*>(a.devicePointer);
+  return nullptr;
+}
 
 // What the LM-head call needs to know about a context (filled by api.cu).
 struct HeadView {
@@ -19,6 +66,7 @@ struct HeadView {
   float eps;
 };
 int ctx_head_view(tp_ctx* ctx, HeadView* out);  // returns a tp_status
+int ctx_hidden_size(const tp_ctx* ctx);          // H, without touching the device (0 for null)
 
 // Launch with programmatic stream serialization: the kernel may begin (up to its
 // griddep_wait()) while the previous kernel on the stream is still running.
@@ -38,6 +86,50 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// ---------------- KV cache addressing ----------------
+// A layer's cache is [n][2 (K, V)][blocks][nkv_l][block_len][hd] bf16.  Position p
+// of sequence b lives in block table[b * stride + p / block_len], at row
+// p % block_len.  A contiguous cache is the case of one block per sequence slot
+// (table = the batch's slot array, stride 1, block_len = the capacity); a paged
+// cache has pages of block_len positions and a page table of stride entries per
+// sequence.
+struct KvMap {
+  const int32_t* table;
+  int stride;     // table entries per sequence
+  int block_len;  // positions per block
+  int blocks;     // blocks in the cache
+};
+// The block holding position p of sequence b, or -1 when p or the table entry is
+// outside the cache.
+__device__ __forceinline__ int kv_block(const KvMap& m, int b, int p) {
+  if (p < 0) return -1;
+  const int i = p / m.block_len;
+  if (i >= m.stride) return -1;
+  const int blk = m.table[static_cast<int64_t>(b) * m.stride + i];
+  return (blk >= 0 && blk < m.blocks) ? blk : -1;
+}
+// The block of position p of sequence b once the range it is in has been checked.
+__device__ __forceinline__ int kv_block_checked(const KvMap& m, int b, int p) {
+  return m.table[static_cast<int64_t>(b) * m.stride + p / m.block_len];
+}
+// This thread's share of the check that every block holding keys [k0, k1) of
+// sequence b (k0 >= 0) is inside the cache: threads tid, tid + nthr, ... take one
+// block each; the CTA combines the answers (__syncthreads_or).
+__device__ __forceinline__ bool kv_blocks_bad(const KvMap& m, int b, int k0, int k1, int tid, int nthr) {
+  if (k1 <= k0) return false;
+  const int ib0 = k0 / m.block_len, ib1 = (k1 - 1) / m.block_len;
+  bool bad = false;
+  for (int ib = ib0 + tid; ib <= ib1; ib += nthr) bad |= kv_block(m, b, ib * m.block_len) < 0;
+  return bad;
+}
+// Key splits of the decode kernels start on multiples of this many keys, so that a
+// page of a paged cache (a multiple of it) holds whole key tiles of a split.
+constexpr int kKeyAlign = 128;
+// Row (of hd elements) of (rank r, K or V, block, local kv head g, row in block).
+__device__ __forceinline__ int64_t kv_row(const KvMap& m, int nkv_l, int r, int kv, int blk, int g, int row) {
+  return ((((static_cast<int64_t>(r) * 2 + kv) * m.blocks + blk) * nkv_l + g) * m.block_len) + row;
+}
+
 // ---------------- GEMM (tcgen05) ----------------
 enum GemmEpi : int { EPI_STORE = 0, EPI_SILU = 1, EPI_RESID = 2, EPI_ARGMAX = 3, EPI_QKV = 4 };
 
@@ -52,10 +144,9 @@ struct QkvEpi {
   int max_pos;
   const int32_t* cu_q;       // [B+1]
   const int32_t* ctx_len;    // [B]
-  const int32_t* slot;       // [B]
   int B;
-  void* kv;                  // cache [n][2][max_seqs][nkv_l][cap][hd]
-  int max_seqs, cap;
+  void* kv;                  // cache [n][2][blocks][nkv_l][block_len][hd]
+  KvMap kvm;
   int num_prefill;           // sequences [0, num_prefill): q as bf16 hi + lo parts; later ones: q as fp16
   void* q_lo;                // bf16 [T, n * nq_l * hd]: q - bf16(q) of prefill tokens
 };
@@ -130,10 +221,12 @@ int gemm_num_tiles_f(const GemmProblem& pr, const GemmPlan& plan);
 // ---------------- small kernels ----------------
 cudaError_t launch_embed(const int32_t* ids, int T, const void* embed_stacked, int n, int64_t v_local,
                          int64_t vocab, int H, void* out, void* xh, float* ss, int* status, cudaStream_t s);
-cudaError_t launch_rmsnorm(const void* x, int64_t rows, int H, const void* w, float eps, void* out, cudaStream_t s);
+cudaError_t launch_rmsnorm(const void* x, int64_t rows, int H, const void* w, float eps, void* out, int* status,
+                           cudaStream_t s);
 // Row statistics for a deferred RMSNorm: fp16 copy of x [rows][H] and the sums of
 // squares of each 32-column group, ss [rows][H / 32].
-cudaError_t launch_row_stats(const void* x, int64_t rows, int H, void* xh, float* ss, cudaStream_t s);
+cudaError_t launch_row_stats(const void* x, int64_t rows, int H, void* xh, float* ss, int* status,
+                             cudaStream_t s);
 
 
 struct AttnArgs {
@@ -141,11 +234,10 @@ struct AttnArgs {
   const void* q_lo;          // [T, n * nq_l * hd] bf16 low part of q (prefill tokens)
   int T;                     // rows of qkv
   int n, nq_l, nkv_l, hd, w_rank;
-  const void* kv;            // cache [n][2][max_seqs][nkv_l][cap][hd]
-  int max_seqs, cap;
+  const void* kv;            // cache [n][2][blocks][nkv_l][block_len][hd]
+  KvMap kvm;
   const int32_t* cu_q;
   const int32_t* ctx_len;
-  const int32_t* slot;
   int seq_begin, seq_end;    // sequences handled by this launch
   int max_q_len, max_kv_len;
   void* out;                 // [T, n * nq_l * hd]
@@ -160,13 +252,15 @@ cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s);
 int decode_splits(int max_kv_len, int num_units, int num_sms, int hd, int G, int max_splits);
 
 cudaError_t launch_final_norm_select(const void* hidden, int H, const int32_t* cu_q, int B, const void* w,
-                                     float eps, void* out, cudaStream_t s);
+                                     float eps, void* out, int* status, cudaStream_t s);
 cudaError_t launch_argmax_reduce(const float* val, const int* idx, int tiles, int ld, int B, int32_t* out,
                                  cudaStream_t s);
 cudaError_t launch_wait_probe(const int* flag, int* status, long long limit_ns, cudaStream_t s);
 cudaError_t launch_decode_advance(int32_t* ctx_len, int B, const int32_t* ids, int32_t* history, int max_rows,
                                   int32_t* step, int32_t* status, cudaStream_t s);
-cudaError_t launch_bf16_to_f16(void* w, size_t elems, cudaStream_t s);
-cudaError_t launch_fold_norm_f16(void* w, size_t rows, int cols, const void* norm, cudaStream_t s);
+// Weight conversions at shard time; status (device int32, may be null) receives
+// TP_DEVFLAG_SATURATED when a weight is outside the fp16 range.
+cudaError_t launch_bf16_to_f16(void* w, size_t elems, int* status, cudaStream_t s);
+cudaError_t launch_fold_norm_f16(void* w, size_t rows, int cols, const void* norm, int* status, cudaStream_t s);
 
 }  // namespace tpk

@@ -69,11 +69,20 @@ extern "C" tp_status tp_lm_head_argmax_static(tp_ctx* ctx, const void* head_shar
                                               int32_t* dev_status, void* stream) {
   if (!ctx || !head_shards || !b || !hidden || !out_ids || !dev_status) return TP_ERR_INVALID_ARG;
   if (!b->cu_q || b->num_seqs <= 0 || b->num_tokens < b->num_seqs) return TP_ERR_INVALID_ARG;
-  if (b->num_seqs > kMaxSeqs) return TP_ERR_INVALID_ARG;  // beyond the array's sequence limit
+  // the array's limits, checked before any CUDA call
+  if (b->num_seqs > kMaxSeqs) return TP_ERR_INVALID_ARG;
+  if (tpk::ctx_hidden_size(ctx) > kMaxHidden) return TP_ERR_INVALID_ARG;
+  // outputs: device memory, or page-locked host memory through its device mapping,
+  // as tp_lm_head_argmax accepts them; anything else is refused before a launch
+  out_ids = tpk::gpu_view(out_ids);
+  if (!out_ids) return TP_ERR_INVALID_ARG;
+  if (out_logits) {
+    out_logits = tpk::gpu_view(out_logits);
+    if (!out_logits) return TP_ERR_INVALID_ARG;
+  }
   tpk::HeadView hv{};
   tp_status st = static_cast<tp_status>(tpk::ctx_head_view(ctx, &hv));
   if (st != TP_OK) return st;
-  if (hv.H > kMaxHidden) return TP_ERR_INVALID_ARG;       // beyond the array's hidden-size limit
   char* scratch = nullptr;
   st = scratch_address(&scratch);
   if (st != TP_OK) return st;
@@ -82,7 +91,7 @@ extern "C" tp_status tp_lm_head_argmax_static(tp_ctx* ctx, const void* head_shar
   const int B = b->num_seqs;
   void* z = scratch + kZOff;
   // the final norm's weight is folded into the LM head copy: normalize with ones
-  cudaError_t e = tpk::launch_final_norm_select(hidden, hv.H, b->cu_q, B, nullptr, hv.eps, z, s);
+  cudaError_t e = tpk::launch_final_norm_select(hidden, hv.H, b->cu_q, B, nullptr, hv.eps, z, dev_status, s);
   if (e != cudaSuccess) return TP_ERR_CUDA;
   tpk::GemmProblem g{};
   g.x = z; g.x_rows = B; g.x_cols = hv.H; g.x_ld = hv.H;

@@ -18,16 +18,35 @@ from .binding import (WEIGHTS_HEAD, WEIGHTS_LAYER, Batch, Context, ModelConfig, 
 
 
 class TPRunner:
-    def __init__(self, cfg: ModelConfig, num_layers: int, max_seqs: int, capacity: int, max_tokens: int):
+    """page_size == 0: one contiguous cache slot of ``capacity`` positions per
+    sequence.  page_size > 0 (a multiple of 128): a paged cache of
+    max_seqs * ceil(capacity / page_size) pages (+ ``spare_pages``), each sequence
+    slot owning the pages of one row of a page table drawn as a seeded random
+    permutation, so that no sequence's pages are contiguous or in order."""
+
+    def __init__(self, cfg: ModelConfig, num_layers: int, max_seqs: int, capacity: int, max_tokens: int,
+                 page_size: int = 0, spare_pages: int = 0, page_seed: int = 0):
         self.cfg = cfg
         self.ctx = Context(cfg)
         self.num_layers = num_layers
         self.max_seqs = max_seqs
         self.capacity = capacity
         self.max_tokens = max_tokens
+        self.page_size = page_size
         self.layer_shards: List[Optional[torch.Tensor]] = [None] * num_layers
         self.head_shards: Optional[torch.Tensor] = None
-        self.kv: List[torch.Tensor] = [self.ctx.alloc_kv_cache(max_seqs, capacity) for _ in range(num_layers)]
+        if page_size > 0:
+            self.pages_per_seq = -(-capacity // page_size)
+            self.num_pages = max_seqs * self.pages_per_seq + spare_pages
+            g = torch.Generator().manual_seed(page_seed)
+            perm = torch.randperm(self.num_pages, generator=g)[: max_seqs * self.pages_per_seq]
+            self.page_table = perm.view(max_seqs, self.pages_per_seq).to(torch.int32)  # host copy
+            self.kv_blocks, self.kv_block_len = self.num_pages, page_size
+        else:
+            self.page_table = None
+            self.kv_blocks, self.kv_block_len = max_seqs, capacity
+        self.kv: List[torch.Tensor] = [self.ctx.alloc_kv_cache(self.kv_blocks, self.kv_block_len)
+                                       for _ in range(num_layers)]
         self.workspace = self.ctx.init_workspace(max_tokens, max(max_seqs, 1), capacity)
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
         n = cfg.tp_size
@@ -36,12 +55,12 @@ class TPRunner:
     # ---- weights ----
     def load_layer(self, layer: int, full: Dict[str, torch.Tensor]) -> None:
         dst = self.ctx.alloc_layer_shards()
-        tp_shard_weights(self.ctx, dst, layer=full)
+        tp_shard_weights(self.ctx, dst, layer=full, status=self.status)
         self.layer_shards[layer] = dst
 
     def load_head(self, full: Dict[str, torch.Tensor]) -> None:
         dst = self.ctx.alloc_head_shards()
-        tp_shard_weights(self.ctx, dst, head=full)
+        tp_shard_weights(self.ctx, dst, head=full, status=self.status)
         self.head_shards = dst
 
     def kv_head_map(self) -> List[int]:
@@ -54,26 +73,62 @@ class TPRunner:
         return out
 
     def kv_view(self, layer: int) -> torch.Tensor:
-        """[n, 2, max_seqs, nkv_l, capacity, hd] bf16 view of a layer cache."""
+        """[n, 2, blocks, nkv_l, block_len, hd] bf16 view of a layer cache (blocks =
+        slots of `capacity` positions, or pages of `page_size`)."""
         c = self.cfg
-        return self.kv[layer].view(torch.bfloat16).view(c.tp_size, 2, self.max_seqs, self.nkv_l, self.capacity,
-                                                        c.head_dim)
+        return self.kv[layer].view(torch.bfloat16).view(c.tp_size, 2, self.kv_blocks, self.nkv_l,
+                                                        self.kv_block_len, c.head_dim)
+
+    def kv_positions(self, layer: int, slot: int, p0: int, p1: int) -> torch.Tensor:
+        """Positions [p0, p1) of sequence slot `slot`: [n, 2, nkv_l, p1 - p0, hd] (either layout)."""
+        v = self.kv_view(layer)
+        if self.page_table is None:
+            return v[:, :, slot, :, p0:p1]
+        ps = self.page_size
+        parts = []
+        p = p0
+        while p < p1:
+            e = min(p1, (p // ps + 1) * ps)
+            parts.append(v[:, :, int(self.page_table[slot, p // ps]), :, p % ps:p % ps + (e - p)])
+            p = e
+        return torch.cat(parts, dim=3)
+
+    def load_kv_contiguous(self, layer: int, contig: torch.Tensor) -> None:
+        """Copies a cache given in the contiguous layout [n][2][max_seqs][nkv_l][capacity][hd]
+        (bf16 elements) into this runner's layout (setup, not a step)."""
+        c = self.cfg
+        src = contig.view(torch.bfloat16).view(c.tp_size, 2, self.max_seqs, self.nkv_l, self.capacity, c.head_dim)
+        if self.page_table is None:
+            self.kv_view(layer).copy_(src)
+            return
+        ps, P = self.page_size, self.pages_per_seq
+        pad = P * ps - self.capacity
+        if pad:
+            src = torch.nn.functional.pad(src, (0, 0, 0, pad))
+        blocks = src.reshape(c.tp_size, 2, self.max_seqs, self.nkv_l, P, ps, c.head_dim).permute(0, 1, 2, 4, 3, 5, 6)
+        blocks = blocks.reshape(c.tp_size, 2, self.max_seqs * P, self.nkv_l, ps, c.head_dim)
+        dst = self.kv_view(layer)
+        dst[:, :, self.page_table.flatten().long().to(dst.device)] = blocks
 
     # ---- one step ----
     def make_batch(self, q_lens: Sequence[int], ctx_lens: Sequence[int], slots: Optional[Sequence[int]] = None,
-                   num_prefill: Optional[int] = None) -> Batch:
+                   num_prefill: Optional[int] = None, max_kv_len: Optional[int] = None) -> Batch:
         if slots is None:
             slots = list(range(len(q_lens)))
         if num_prefill is None:
             num_prefill = sum(1 for q in q_lens if q > 1)
-        return Batch(q_lens, ctx_lens, slots, num_prefill)
+        if self.page_table is not None:  # each sequence takes its slot's row of the page table
+            rows = self.page_table[torch.as_tensor(list(slots), dtype=torch.long)]
+            return Batch(q_lens, ctx_lens, slots, num_prefill, max_kv_len=max_kv_len, page_table=rows,
+                         page_size=self.page_size)
+        return Batch(q_lens, ctx_lens, slots, num_prefill, max_kv_len=max_kv_len)
 
     def embed(self, ids: torch.Tensor, hidden_out: torch.Tensor) -> None:
         tp_embed_vocab_parallel(self.ctx, self.head_shards, ids, hidden_out, self.status)
 
     def layer(self, layer: int, batch: Batch, hidden: torch.Tensor) -> None:
-        tp_decoder_layer_forward(self.ctx, self.layer_shards[layer], batch, hidden, self.kv[layer], self.max_seqs,
-                                 self.capacity, self.status)
+        tp_decoder_layer_forward(self.ctx, self.layer_shards[layer], batch, hidden, self.kv[layer], self.kv_blocks,
+                                 self.kv_block_len, self.status)
 
     def head(self, batch: Batch, hidden: torch.Tensor, out_ids: torch.Tensor,
              out_logits: Optional[torch.Tensor] = None) -> None:
@@ -125,7 +180,7 @@ class TPRunner:
         self.step(pb, ids=ids, hidden=hidden_p, out_ids=cur)
         history[0].copy_(cur)
         # decode forwards: positions lens[b], lens[b] + 1, ...; launches planned for the last
-        db = Batch([1] * B, lens, slots, 0, max_kv_len=max(lens) + steps)
+        db = self.make_batch([1] * B, lens, slots, num_prefill=0, max_kv_len=max(lens) + steps)
         hidden_d = torch.empty(B, H, dtype=torch.float32, device=dev)
 
         def decode() -> None:

@@ -17,6 +17,9 @@ from oracle import inputs as oi
 
 TOL = 2e-2  # max |err| <= TOL * RMS(reference), per tensor
 MARGIN = 0.05  # greedy ids compared where the reference top-2 margin exceeds this
+# the workloads' KV cache is bf16: the oracle's cache stores bf16 too (its arithmetic
+# stays fp64), and attention reads what the cache holds
+KV_DTYPE = torch.bfloat16
 
 
 def model_config(s: synth.ModelShape, n: int):
@@ -38,28 +41,14 @@ def assert_close(got, ref, what: str, tol: float = TOL) -> float:
     return e
 
 
-def assert_close_bf16_stored(got, ref, what: str, tol: float = TOL) -> float:
-    """For outputs the method stores as bf16 (the KV cache): the bound applies on
-    top of the format's own rounding, half a bf16 ulp of each reference value
-    (bf16 keeps 8 significant bits, so the half-ulp of x is 2^(floor(log2|x|) - 8))."""
-    got = got.to(torch.float64).cpu()
-    ref = ref.to(torch.float64).cpu()
-    mag = ref.abs().clamp_min(1e-30)
-    half_ulp = torch.exp2(torch.floor(torch.log2(mag)) - 8)
-    excess = ((got - ref).abs() - half_ulp).clamp_min(0.0)
-    e = float(excess.max()) / max(float(ref.pow(2).mean().sqrt()), 1e-30)
-    assert e <= tol, f"{what}: max(|err| - half bf16 ulp)/RMS(ref) = {e:.3e} > {tol}"
-    return e
-
-
 @functools.lru_cache(maxsize=64)
 def oracle_layer(s: synth.ModelShape, layer: int, perturbed: bool) -> of.LayerWeights:
     return oi.layer_weights(s, layer, perturbed_norms=perturbed)
 
 
 @functools.lru_cache(maxsize=4)
-def oracle_head(s: synth.ModelShape, perturbed: bool) -> of.HeadWeights:
-    return oi.head_weights(s, perturbed_norms=perturbed)
+def oracle_head(s: synth.ModelShape, perturbed: bool, need_embed: bool = True) -> of.HeadWeights:
+    return oi.head_weights(s, perturbed_norms=perturbed, need_embed=need_embed)
 
 
 class GpuStep:
@@ -67,7 +56,7 @@ class GpuStep:
 
     def __init__(self, w: synth.Workload, n: int, layers: Optional[int] = None, perturbed: bool = False,
                  head: bool = True, logits: bool = True, capacity: Optional[int] = None,
-                 keep_intermediates: bool = False, q_norm_scale: float = 1.0):
+                 keep_intermediates: bool = False, q_norm_scale: float = 1.0, page_size: int = 0):
         from tensor_transformer_forward_gb300.runner import TPRunner
         self.w, self.n, self.perturbed = w, n, perturbed
         s = w.shape
@@ -75,7 +64,8 @@ class GpuStep:
         q, c = w.q_lens, w.ctx_lens
         max_kv = max(a + b for a, b in zip(q, c))
         self.capacity = capacity or ((max_kv + 63) // 64 * 64)
-        self.runner = TPRunner(model_config(s, n), self.L, w.num_seqs, self.capacity, w.num_tokens)
+        self.runner = TPRunner(model_config(s, n), self.L, w.num_seqs, self.capacity, w.num_tokens,
+                               page_size=page_size, spare_pages=3 if page_size else 0)
         r = self.runner
         if keep_intermediates:
             r.ctx.keep_intermediates()
@@ -89,11 +79,22 @@ class GpuStep:
             r.load_head(sd.head_weights(s, perturbed))
         fill = max(c) if c else 0
         hmap = r.kv_head_map()
+        contig = None
         for li in range(self.L):
             r.kv[li].zero_()
             if fill > 0:
-                sd.fill_kv_cache(r.kv[li], n, w.num_seqs, r.nkv_l, self.capacity, s.head_dim, hmap, s.num_kv_heads,
-                                 li, w.num_seqs, fill)
+                if page_size:  # filled in the contiguous layout, then copied into the pages
+                    if contig is None:
+                        contig = torch.zeros(r.ctx.kv_cache_bytes(w.num_seqs, self.capacity), dtype=torch.uint8,
+                                             device="cuda")
+                    contig.zero_()
+                    sd.fill_kv_cache(contig, n, w.num_seqs, r.nkv_l, self.capacity, s.head_dim, hmap,
+                                     s.num_kv_heads, li, w.num_seqs, fill)
+                    r.load_kv_contiguous(li, contig)
+                else:
+                    sd.fill_kv_cache(r.kv[li], n, w.num_seqs, r.nkv_l, self.capacity, s.head_dim, hmap,
+                                     s.num_kv_heads, li, w.num_seqs, fill)
+        del contig
         self.batch = r.make_batch(q, c, list(range(w.num_seqs)), num_prefill=len(w.prefill))
         T = w.num_tokens
         self.ids = sd.token_ids(T, s.vocab) if w.input_from_ids else None
@@ -115,17 +116,17 @@ class GpuStep:
         """The positions this step wrote, gathered to global kv heads [nkv, q_len, hd]
         (the first rank holding a head supplies it); also checks replicas agree."""
         s = self.w.shape
-        view = self.runner.kv_view(layer)
         c0 = self.w.ctx_lens[b]
         t0, t1 = self.seq_rows(b)
         q = t1 - t0
         got: Dict[int, Tuple[torch.Tensor, torch.Tensor]] = {}
         nkv_l = self.runner.nkv_l
+        pos = self.runner.kv_positions(layer, b, c0, c0 + q)  # [n, 2, nkv_l, q, hd]
         for r in range(self.n):
             for j in range(nkv_l):
                 g = self.head_map[r * nkv_l + j]
-                k = view[r, 0, b, j, c0:c0 + q].float().cpu()
-                v = view[r, 1, b, j, c0:c0 + q].float().cpu()
+                k = pos[r, 0, j].float().cpu()
+                v = pos[r, 1, j].float().cpu()
                 if g in got:
                     assert torch.equal(got[g][0], k) and torch.equal(got[g][1], v), "replicated kv heads differ"
                 else:
@@ -139,9 +140,9 @@ def oracle_run(w: synth.Workload, seqs: Sequence[int], layers: int, perturbed: b
     s = w.shape
     shape = oi.shape_of(s)
     lw = [oracle_layer(s, li, perturbed) for li in range(layers)]
-    hw = oracle_head(s, perturbed) if (head or w.input_from_ids) else None
+    hw = oracle_head(s, perturbed, w.input_from_ids) if (head or w.input_from_ids) else None
     ins = oi.workload_seq_inputs(w, seqs, range(layers))
-    outs = [of.run_sequence(seq, lw, hw, shape, n=0, head=head) for seq in ins]
+    outs = [of.run_sequence(seq, lw, hw, shape, n=0, head=head, kv_dtype=KV_DTYPE) for seq in ins]
     return outs, ins
 
 
@@ -151,7 +152,7 @@ def oracle_run_sp(w: synth.Workload, seq: int, layers: int, n: int, perturbed: b
     lw = [oracle_layer(s, li, perturbed) for li in range(layers)]
     hw = oracle_head(s, perturbed) if (head or w.input_from_ids) else None
     ins = oi.workload_seq_inputs(w, [seq], range(layers))
-    return of.run_sequence_sp(ins[0], lw, hw, oi.shape_of(s), n, head=head)
+    return of.run_sequence_sp(ins[0], lw, hw, oi.shape_of(s), n, head=head, kv_dtype=KV_DTYPE)
 
 
 def check_step(g: GpuStep, seqs: Sequence[int], head: bool = True, layers: Optional[int] = None) -> Dict[str, float]:
@@ -162,10 +163,11 @@ def check_step(g: GpuStep, seqs: Sequence[int], head: bool = True, layers: Optio
     for b, o, i in zip(seqs, outs, ins):
         t0, t1 = g.seq_rows(b)
         errs[f"hidden[{b}]"] = assert_close(g.hidden[t0:t1].float().cpu(), o.hidden, f"hidden of seq {b}")
-        c0 = g.w.ctx_lens[b]
+        # the new positions' K / V, stored bf16 on the GPU, against the oracle's values
+        # before its cache stored them: the bar includes the bf16 rounding
         K, V = g.new_kv(L - 1, b)
-        errs[f"k[{b}]"] = assert_close_bf16_stored(K, o.k_cache[L - 1][:, c0:], f"new K of seq {b}")
-        errs[f"v[{b}]"] = assert_close_bf16_stored(V, o.v_cache[L - 1][:, c0:], f"new V of seq {b}")
+        errs[f"k[{b}]"] = assert_close(K, o.k_new[L - 1], f"new K of seq {b}")
+        errs[f"v[{b}]"] = assert_close(V, o.v_new[L - 1], f"new V of seq {b}")
         if head:
             if g.logits is not None:
                 errs[f"logits[{b}]"] = assert_close(g.logits[b].cpu(), o.logits, f"logits of seq {b}")
@@ -176,4 +178,5 @@ def check_step(g: GpuStep, seqs: Sequence[int], head: bool = True, layers: Optio
                 # several ids are correct: the GPU's pick must be a maximiser of its own logits
                 lg = g.logits[b].cpu()
                 assert float(lg[int(g.out_ids[b])]) == float(lg.max())
+    print(f"\n{g.w.name} tp {g.n}: " + ", ".join(f"{k} {v:.2e}" for k, v in errs.items()))
     return errs

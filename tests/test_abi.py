@@ -139,3 +139,25 @@ def test_entry_points_refuse_empty_or_missing_inputs_before_device_work():
     assert L.tp_kv_cache_bytes(h, 1, 0, ctypes.byref(nb)) == inval                          # no positions
     assert L.tp_hidden_written(None) == inval
     assert ctx.launch_count() == 0
+
+
+def test_static_scratch_entry_point_refuses_sizes_beyond_its_array_before_device_work():
+    """tp_lm_head_argmax_static has a fixed scratch array: more than 64 sequences or a
+    hidden size above 8192 comes back as TP_ERR_INVALID_ARG from the host-side checks,
+    before any CUDA call (this runs without a GPU)."""
+    import ctypes
+    from tensor_transformer_forward_gb300 import Context, binding
+    L = binding._lib
+    fake = ctypes.c_void_p(4096)  # never dereferenced: the size checks come first
+    inval = binding.TP_ERR_INVALID_ARG
+    big = synth.ModelShape(hidden=8256, num_q_heads=16, num_kv_heads=8, head_dim=128, intermediate=256,
+                           vocab=1024, num_layers=1)
+    ctx = Context(_cfg(big, 1))
+    b = binding.TPBatch()
+    b.num_seqs, b.num_prefill, b.num_tokens, b.max_q_len, b.max_kv_len = 1, 0, 1, 1, 1
+    b.cu_q = b.ctx_len = b.slot = 4096
+    assert L.tp_lm_head_argmax_static(ctx.handle, fake, ctypes.byref(b), fake, fake, None, fake, None) == inval
+    small = Context(_cfg(synth.TINY, 2))
+    b.num_seqs, b.num_tokens = 65, 65
+    assert L.tp_lm_head_argmax_static(small.handle, fake, ctypes.byref(b), fake, fake, None, fake, None) == inval
+    assert ctx.launch_count() == 0 and small.launch_count() == 0

@@ -80,3 +80,31 @@ def test_reference_arm_prints_the_contract_line():
     assert d["config"]["workload"] == "tiny_prefill8"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_algorithmic_work_matches_the_closed_forms():
+    """The per-launch work bench.py divides by the measured time: GEMM and attention
+    flops of the 0.6B prefill layer and the KV bytes of the 0.6B decode layer, as
+    computed by hand from the shapes (2 T H N per projection, causal 4 hd nq T(T+1)/2,
+    K and V rows of every cached key)."""
+    import bench
+    import synth
+    pre = synth.WORKLOADS["qwen3_0.6b_layer_prefill2048"]
+    T, H = 2048, 1024
+    gemm = sum(bench.kernel_work(k, pre, 2)[0] for k in ("gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down"))
+    assert gemm == 2 * T * H * (4096 + 2048 + 6144) + 2 * T * 3072 * H      # 64.42 GFLOP
+    assert bench.kernel_work("attn_prefill", pre, 2)[0] == 4 * 128 * 16 * T * (T + 1) / 2
+    dec = synth.WORKLOADS["qwen3_0.6b_layer_decode64x4096"]
+    for n in (1, 2, 4):
+        assert bench.kernel_work("attn_decode", dec, n)[1] == 64 * 4097 * 8 * 128 * 2 * 2  # 1074.0 MB
+    # 32B at tp 16: kv heads replicated on two ranks, so 16 cached heads per key
+    d32 = synth.WORKLOADS["qwen3_32b_layer_tp16_decode32x2048"]
+    assert bench.kernel_work("attn_decode", d32, 16)[1] == 32 * 2049 * 16 * 128 * 2 * 2
+    assert bench.kernel_work("gemm_lm_head", d32, 16)[1] == 151936 * 5120 * 2 + 32 * 5120 * 2
+    pk = {"bf16_tflops_sustained": 1772.4, "hbm_gbs": 6682.2}
+    r = bench.kernel_roofline("attn_decode", dec, 2, 1.0, pk)     # 1.074 GB in 1 ms
+    assert r["bound"] == "hbm" and abs(r["achieved"] - 1074.0) < 0.1
+    r = bench.kernel_roofline("gemm_gate_up", pre, 2, 1.0, pk)    # 25.77 GFLOP in 1 ms
+    assert r["bound"] == "tensor" and abs(r["achieved"] - 25.77) < 0.01
+    # a decode GEMM streams its weights: HBM-bound
+    assert bench.kernel_roofline("gemm_gate_up", dec, 2, 1.0, pk)["bound"] == "hbm"

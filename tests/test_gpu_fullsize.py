@@ -25,19 +25,21 @@ def test_qwen3_06b_layer_decode_64x4096_with_head(n):
     check_step(g, [0, 31, 63])
 
 
-def test_qwen3_32b_layer_tp16_decode_32x2048():
+def test_qwen3_32b_layer_tp16_decode_32x2048_with_untied_head():
+    """32B layer at tp 16 (each kv head replicated on two ranks) and the untied
+    151936 x 5120 vocab-parallel LM head (16 slices of 9496 rows)."""
     w = synth.WORKLOADS["qwen3_32b_layer_tp16_decode32x2048"]
-    g = GpuStep(w, 16, head=False)
-    check_step(g, [0, 17], head=False)
+    g = GpuStep(w, 16)
+    check_step(g, [0, 17, 31])
 
 
-def test_qwen3_32b_layer_tp16_prefill_1024():
+def test_qwen3_32b_layer_tp16_prefill_1024_with_untied_head():
     w = synth.WORKLOADS["qwen3_32b_layer_tp16_prefill1024"]
-    g = GpuStep(w, 16, head=False)
-    check_step(g, [0], head=False)
+    g = GpuStep(w, 16)
+    check_step(g, [0])
 
 
-@pytest.mark.parametrize("n", [2])
+@pytest.mark.parametrize("n", [1, 2, 4])
 def test_qwen3_06b_model_mixed_step(n):
     """28 layers, 4 x 512 prefill + 128 decode at ctx 2048, from ids, greedy ids."""
     w = synth.WORKLOADS["qwen3_0.6b_model_mixed"]

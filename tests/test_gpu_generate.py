@@ -10,7 +10,7 @@ import synth
 import synth.device as sd
 from oracle import forward as of
 from oracle import inputs as oi
-from tests.gpu_harness import MARGIN, assert_close, model_config
+from tests.gpu_harness import KV_DTYPE, MARGIN, assert_close, model_config
 
 pytestmark = pytest.mark.gpu
 
@@ -55,7 +55,7 @@ def test_greedy_generation_graph_matches_eager_and_oracle(n):
     lw = [oi.layer_weights(s, li, perturbed_norms=True) for li in range(LAYERS)]
     hw = oi.head_weights(s, perturbed_norms=True)
     for b, p in enumerate(prompts):
-        tokens, margins, last = of.greedy_generate(torch.tensor(p), lw, hw, shape, STEPS)
+        tokens, margins, last = of.greedy_generate(torch.tensor(p), lw, hw, shape, STEPS, kv_dtype=KV_DTYPE)
         parted = False
         for k in range(STEPS):
             if ids_graph[b][k] != tokens[k]:

@@ -144,3 +144,38 @@ def test_sequence_parallel_token_chunks(n):
     top2 = sp.logits.topk(2).values
     if float(top2[0] - top2[1]) > MARGIN:
         assert int(g.out_ids[0]) == sp.next_id
+
+
+@pytest.mark.parametrize("prefill", [True, False])
+def test_fp16_saturation_is_reported(prefill):
+    """GEMM operands are fp16 and clamp at +-65504: residual rows scaled by 2^17
+    (a host-side input, no fault) must set TP_ERR_SATURATED in the status word,
+    and so must a weight outside the fp16 range at shard time; the same inputs at
+    their normal scale leave the word clear."""
+    import torch
+    import synth.device as sd
+    from tensor_transformer_forward_gb300 import TP_ERR_SATURATED, TP_OK, tp_read_status, tp_shard_weights
+    from tensor_transformer_forward_gb300.runner import TPRunner
+    from tests.gpu_harness import model_config
+    s = synth.QWEN3_06B
+    r = TPRunner(model_config(s, 2), 1, max_seqs=4, capacity=128, max_tokens=64)
+    full = sd.layer_weights(s, 0)
+    r.load_layer(0, full)
+    q = [48, 1, 1, 1] if prefill else [1, 1, 1, 1]
+    batch = r.make_batch(q, [0, 5, 9, 17], [0, 1, 2, 3], num_prefill=1 if prefill else 0)
+    h = torch.empty(batch.num_tokens, s.hidden, dtype=torch.bfloat16, device="cuda")
+    sd.fill_normal(h, synth.SEED_ACTIVATIONS, 7, 1.0)
+    r.status.zero_()
+    r.step(batch, hidden=h.float(), run_head=False)
+    assert tp_read_status(r.status) == TP_OK
+    r.step(batch, hidden=h.float() * 2.0 ** 17, run_head=False)
+    assert tp_read_status(r.status) == TP_ERR_SATURATED
+    # a weight beyond the fp16 range: flagged when the shards are made
+    big = {k: v.clone() for k, v in full.items()}
+    big["down"][3, 5] = 1.0e5
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tp_shard_weights(r.ctx, r.ctx.alloc_layer_shards(), layer=big, status=st)
+    assert tp_read_status(st) == TP_ERR_SATURATED
+    st.zero_()
+    tp_shard_weights(r.ctx, r.ctx.alloc_layer_shards(), layer=full, status=st)
+    assert tp_read_status(st) == TP_OK
