@@ -118,8 +118,14 @@ struct GemmCfg {
   // per-row partial sums of squares [2 parities][2 warps][BN/64 heads at most][128]
   // and each warp's row staging [2 outputs][32 rows][128 bytes at most]
   static constexpr int QKV_BYTES = QKV_PAIR ? 128 + 256 * 4 + 2 * 2 * (BN / 64) * 128 * 4 + EW * 2 * 32 * 128 : 0;
+  // small area after the barriers: TMEM address and flags (64 B), the argmax
+  // epilogue's per-warp partials (2 x 512 B) and per-token running best (2 x BEST
+  // entries: up to 256 tokens on the weight-streaming argmax path, else 64; the
+  // other swapped epilogues use the same area for their token table)
+  static constexpr int BEST = (SWAP && EPI == EPI_ARGMAX) ? 256 : 64;
+  static constexpr int SMALL_BYTES = 64 + 1024 + 8 * BEST;
   static constexpr int SMEM =
-      1024 + STAGES * STAGE_BYTES + OUT_BYTES + TROW_BYTES + NUM_BARS * 8 + 64 + 1536 + QKV_BYTES;
+      1024 + STAGES * STAGE_BYTES + OUT_BYTES + TROW_BYTES + NUM_BARS * 8 + SMALL_BYTES + 128 + QKV_BYTES;
   static_assert(SMEM <= 232448, "shared memory per block");
 };
 
@@ -1043,10 +1049,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
   // weight-streaming argmax: per-column partials of the 4 epilogue warps and the CTA's running best
   float* red_v = reinterpret_cast<float*>(tmem_slot + 16);  // [4][32]
   int* red_i = reinterpret_cast<int*>(red_v + 128);          // [4][32]
-  float* best_v = reinterpret_cast<float*>(red_i + 128);     // [64]
-  int* best_i = reinterpret_cast<int*>(best_v + 64);         // [64]
+  float* best_v = reinterpret_cast<float*>(red_i + 128);     // [BEST]
+  int* best_i = reinterpret_cast<int*>(best_v + C::BEST);    // [BEST]
   // QKV_PAIR: [2][128] q/k norm weights, 128-byte aligned (the staging rows below take 16-byte accesses)
-  float* sNw = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(best_i + 64) + 127) & ~uintptr_t(127));
+  float* sNw = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(best_i + C::BEST) + 127) & ~uintptr_t(127));
   float* sSS = sNw + 256;                                    // QKV_PAIR: partial sums of squares
   uint8_t* sStg = reinterpret_cast<uint8_t*>(sSS + 2 * 2 * (BN / 64) * 128);  // QKV_PAIR: [EW][2][32][128]
 
@@ -1079,9 +1085,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
     *last_flag = 0;
     fence_barrier_init();
   }
-  if (SWAP && threadIdx.x >= 64 && threadIdx.x < 128) {
-    best_v[threadIdx.x - 64] = -INFINITY;
-    best_i[threadIdx.x - 64] = INT_MAX;
+  if (SWAP && EPI == EPI_ARGMAX && threadIdx.x >= 64) {
+    for (int i = threadIdx.x - 64; i < BN; i += blockDim.x - 64) {
+      best_v[i] = -INFINITY;
+      best_i[i] = INT_MAX;
+    }
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmX);
@@ -1692,10 +1700,11 @@ static inline int cdiv(long long a, long long b) { return static_cast<int>((a + 
 GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
   GemmPlan pl{};
   const int total_kb = pr.n_seg * (pr.k_seg / 64);
-  if (pr.epi == EPI_ARGMAX && pr.T <= 64) {
-    // few tokens against the whole vocab: weights on the M side, tokens as N
+  if (pr.epi == EPI_ARGMAX && pr.T <= 256) {
+    // up to 256 tokens against the whole vocab: weights on the M side, tokens as N,
+    // so the weights stream from HBM once
     pl.swap = true;
-    pl.BN = pr.T <= 16 ? 16 : (pr.T <= 32 ? 32 : 64);
+    pl.BN = pr.T <= 16 ? 16 : (pr.T <= 32 ? 32 : (pr.T <= 64 ? 64 : (pr.T <= 128 ? 128 : 256)));
     pl.tiles_t = 1;
     pl.tiles_f = cdiv(pr.N, 128);
     pl.splits = 1;
@@ -1895,6 +1904,8 @@ cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partia
   TP_V(16, EPI_ARGMAX, false, true)
   TP_V(32, EPI_ARGMAX, false, true)
   TP_V(64, EPI_ARGMAX, false, true)
+  TP_V(128, EPI_ARGMAX, false, true)
+  TP_V(256, EPI_ARGMAX, false, true)
 #undef TP_V
   return cudaErrorNotSupported;
 }

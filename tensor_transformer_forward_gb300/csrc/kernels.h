@@ -210,10 +210,11 @@ bool make_tmap_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, 
 // workspace: partials (fp32) and per-tile counters (int, zeroed once, self-resetting)
 // counters (launch_gemm): split-K tile counters from index 0 (fewer than 256 tiles
 // are ever split); the weight-streaming argmax uses [0] and [1] and, from int
-// index kArgmaxKeyOffset, one 64-bit key per token (at most 64).  All zero
-// between launches; the kernels leave them zero.
+// index kArgmaxKeyOffset, one 64-bit key per token (at most kArgmaxMaxTokens).
+// All zero between launches; the kernels leave them zero.
 constexpr int kArgmaxKeyOffset = 2048;
-constexpr int kGemmCounterInts = kArgmaxKeyOffset + 2 * 64;
+constexpr int kArgmaxMaxTokens = 256;
+constexpr int kGemmCounterInts = kArgmaxKeyOffset + 2 * kArgmaxMaxTokens;
 cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& plan, float* partials, int* counters,
                         int* status, cudaStream_t stream);
 int gemm_num_tiles_f(const GemmProblem& pr, const GemmPlan& plan);
