@@ -1191,8 +1191,8 @@ __global__ void __launch_bounds__(320, 1)
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
       __half* orow = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(tbase + (row_ok ? qi : 0)) * a.n * a.nq_l * HD +
                      (static_cast<size_t>(r) * a.nq_l + h) * HD + half * OH;
-#pragma unroll
       uint32_t sat = 0;
+#pragma unroll
       for (int c = 0; c < OH / 32; ++c) {
         float v[32];
         tc_ld32(lane_addr + C::O_COL + half * OH + c * 32, v);

@@ -72,7 +72,12 @@ struct GemmParams {
   __half* row_out16;  // the fp16 rows (weights-on-M path writes them directly; ld = out_cols)
 };
 
-template <int BN, int EPI = EPI_STORE, bool ACC = false, bool SWAP = false>
+// PAIR: a cluster of two CTAs computes 256-token x BN tiles with one
+// tcgen05.mma.cta_group::2 (M = 256): each CTA loads its own 128 token rows and
+// half of the BN weight rows (BN / 2), so a K block moves 32 KB (BN = 256) into
+// and out of each SM's shared memory instead of 48 KB; each CTA's epilogue
+// handles its 128 rows from its own TMEM.
+template <int BN, int EPI = EPI_STORE, bool ACC = false, bool SWAP = false, bool PAIR = false>
 struct GemmCfg {
   // epilogue warps: 8 (two per TMEM lane quarter, splitting the columns) where the
   // columns split into independent halves, else 4
@@ -83,7 +88,8 @@ struct GemmCfg {
           : 4;
   static constexpr int THREADS = 64 + 32 * EW;
   static constexpr int A_BYTES = 128 * 128;  // 128 rows x 64 fp16
-  static constexpr int B_BYTES = BN * 128;   // BN rows x 64 fp16
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * 128;  // this CTA's weight rows x 64 fp16
+  static constexpr int TM_T = SWAP ? BN : (PAIR ? 256 : 128);  // tokens per tile (both CTAs of a pair)
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // as many stages as fit in ~200 KB (narrow tiles stream weights: more bytes in flight)
   // QKV with two warps per lane quarter (see QKV_PAIR below) keeps 3 stages: its
@@ -97,7 +103,7 @@ struct GemmCfg {
   static constexpr int NXB = RESID_ROWS ? ((BN / (EW / 4)) / 32 < 2 ? (BN / (EW / 4)) / 32 : 2) : 1;
   static constexpr int ROW16_BYTES = RESID_ROWS ? EW * (2048 + (NXB - 1) * 4096) : 0;
   static constexpr int STAGES =
-      QKV_PAIR ? 3
+      QKV_PAIR ? (PAIR ? 4 : 3)
       : ((204800 - ROW16_BYTES - ((SWAP && EPI != EPI_ARGMAX) ? BN * 512 : 0)) / STAGE_BYTES) > 12
           ? 12
           : ((204800 - ROW16_BYTES - ((SWAP && EPI != EPI_ARGMAX) ? BN * 512 : 0)) / STAGE_BYTES);
@@ -123,7 +129,9 @@ struct GemmCfg {
   // entries: up to 256 tokens on the weight-streaming argmax path, else 64; the
   // other swapped epilogues use the same area for their token table)
   static constexpr int BEST = (SWAP && EPI == EPI_ARGMAX) ? 256 : 64;
-  static constexpr int SMALL_BYTES = 64 + 1024 + 8 * BEST;
+  // the weight-streaming argmax keeps 64-bit keys instead: [4 warps][BN] column
+  // maxima of a tile and [BN] per-token running maxima
+  static constexpr int SMALL_BYTES = 64 + ((SWAP && EPI == EPI_ARGMAX) ? 40 * BN : 1024 + 8 * BEST);
   static constexpr int SMEM =
       1024 + STAGES * STAGE_BYTES + OUT_BYTES + TROW_BYTES + NUM_BARS * 8 + SMALL_BYTES + 128 + QKV_BYTES;
   static_assert(SMEM <= 232448, "shared memory per block");
@@ -180,16 +188,8 @@ __device__ __forceinline__ float row_scale(const GemmParams& p, int t) {
 // for g very negative the divisor overflows to inf and the quotient is 0, the correct limit
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-// (value, index) order of torch.argmax: larger value first, NaN above all,
-// then the lower index.
-__device__ __forceinline__ bool amax_better(float v, int i, float bv, int bi) {
-  const bool vn = v != v, bn = bv != bv;
-  if (vn != bn) return vn;
-  if (!vn && v != bv) return v > bv;
-  return i < bi;
-}
-
-// The same order as one unsigned 64-bit key (larger = better): the value's bits
+// (value, index) order of torch.argmax (larger value first, NaN above all, then
+// the lower index) as one unsigned 64-bit key (larger = better): the value's bits
 // made monotone in the high word (NaN above everything, -0 taken as +0), the
 // complemented index in the low word (lower index wins a tie).  Every key is
 // above 0, the cleared state.
@@ -1029,13 +1029,19 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
   report_sat(p.status, sat);
 }
 
-template <int BN, int EPI, bool ACC, bool SWAP>
-__global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
+template <int BN, int EPI, bool ACC, bool SWAP, bool PAIR>
+__global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2,
                    const __grid_constant__ CUtensorMap tmKV, const GemmParams p) {
-  using C = GemmCfg<BN, EPI, ACC, SWAP>;
+  using C = GemmCfg<BN, EPI, ACC, SWAP, PAIR>;
   constexpr int STAGES = C::STAGES;
+  static_assert(!PAIR || (!SWAP && EPI != EPI_ARGMAX), "CTA pairs: token tiles only");
+  // rank in the CTA pair (0 issues the MMAs for both); 0 without pairs
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+  // a pair takes every unit its cluster index selects (both CTAs the same units)
+  const int u0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -1046,13 +1052,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
-  // weight-streaming argmax: per-column partials of the 4 epilogue warps and the CTA's running best
-  float* red_v = reinterpret_cast<float*>(tmem_slot + 16);  // [4][32]
-  int* red_i = reinterpret_cast<int*>(red_v + 128);          // [4][32]
-  float* best_v = reinterpret_cast<float*>(red_i + 128);     // [BEST]
-  int* best_i = reinterpret_cast<int*>(best_v + C::BEST);    // [BEST]
+  // small area: the swapped epilogues' token table (red_v, reused as sPos / sInv),
+  // or the weight-streaming argmax's 64-bit keys: [4 warps][BN] per-tile column
+  // maxima (wkey) and [BN] per-token running maxima (bestk)
+  uint8_t* small = reinterpret_cast<uint8_t*>(tmem_slot + 16);
+  float* red_v = reinterpret_cast<float*>(small);
+  unsigned long long* wkey = reinterpret_cast<unsigned long long*>(small);
+  unsigned long long* bestk = wkey + 4 * BN;
   // QKV_PAIR: [2][128] q/k norm weights, 128-byte aligned (the staging rows below take 16-byte accesses)
-  float* sNw = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(best_i + C::BEST) + 127) & ~uintptr_t(127));
+  float* sNw = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(small + (C::SMALL_BYTES - 64)) + 127) &
+                                        ~uintptr_t(127));
   float* sSS = sNw + 256;                                    // QKV_PAIR: partial sums of squares
   uint8_t* sStg = reinterpret_cast<uint8_t*>(sSS + 2 * 2 * (BN / 64) * 128);  // QKV_PAIR: [EW][2][32][128]
 
@@ -1066,6 +1075,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
 #define QFULL(k) (bar0 + 8u * (2 * STAGES + 5 + (k)))
 #define QEMPTY(k) (bar0 + 8u * (2 * STAGES + 5 + C::QUEUE + (k)))
   volatile int* queue = reinterpret_cast<volatile int*>(tmem_slot + 4);  // [QUEUE] tile ids
+  // an epilogue warp hands an accumulator back to the MMA issuer (a pair's leader)
+  auto tempty_arrive = [&](uint32_t bar) {
+    if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(bar, 0));
+    else mbar_arrive(bar);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -1074,7 +1088,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(TFULL(b), 1);
-      mbar_init(TEMPTY(b), C::EW);
+      mbar_init(TEMPTY(b), PAIR ? 2 * C::EW : C::EW);  // a pair's leader counts both CTAs' epilogue warps
     }
     mbar_init(DRAIN, 1);
     for (int k = 0; k < C::QUEUE; ++k) {
@@ -1085,22 +1099,25 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
     *last_flag = 0;
     fence_barrier_init();
   }
-  if (SWAP && EPI == EPI_ARGMAX && threadIdx.x >= 64) {
-    for (int i = threadIdx.x - 64; i < BN; i += blockDim.x - 64) {
-      best_v[i] = -INFINITY;
-      best_i[i] = INT_MAX;
-    }
-  }
+  if (SWAP && EPI == EPI_ARGMAX && threadIdx.x >= 64)
+    for (int i = threadIdx.x - 64; i < BN; i += blockDim.x - 64) bestk[i] = 0ull;  // below every key
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmW);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // a pair's barriers are initialised in both CTAs before either signals the other's
+  if constexpr (PAIR) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int units = p.tiles_t * p.tiles_f * p.splits;
@@ -1114,7 +1131,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
       for (int64_t i = me; i < p.discard_lines[k]; i += nthr) l2_discard(static_cast<const char*>(p.discard[k]) + i * 128);
   }
   // tile extents on the token and feature sides
-  constexpr int TM_T = SWAP ? BN : 128;  // tokens per tile
+  constexpr int TM_T = C::TM_T;         // tokens per tile
   constexpr int TM_F = SWAP ? 128 : BN;  // features per tile
 
   if (warp == 0) {
@@ -1127,7 +1144,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
       // tiles; each tile id goes through a small queue to the MMA and epilogue
       // warps, -1 ends it.  Otherwise a static round-robin over the tiles.
       int qk = 0;
-      for (int u = blockIdx.x; ok && (C::DYN || u < units);) {
+      for (int u = u0; ok && (C::DYN || u < units);) {
         if constexpr (C::DYN) {
           const int id = u < units ? u : -1;
           if (!mbar_wait(QEMPTY(qk % C::QUEUE), ((qk / C::QUEUE) & 1) ^ 1u, abort_flag, p.status)) {
@@ -1140,7 +1157,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
           if (id < 0) break;
         }
         const Unit un = unit_of(p, u);
-        const int t0 = un.tt * TM_T, f0 = un.tf * TM_F;
+        // this CTA's token rows and (pairs) its half of the tile's weight rows
+        const int t0 = un.tt * TM_T + static_cast<int>(crank) * 128;
+        const int f0 = un.tf * TM_F + static_cast<int>(crank) * (BN / 2);
         for (int g = un.g0; g < un.g1; ++g) {
           const int r = g / p.kb_seg, kb = g - r * p.kb_seg;
           const int s = it % STAGES;
@@ -1149,27 +1168,38 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(FULL(s), C::STAGE_BYTES);
           const uint32_t xdst = smem_u32(SWAP ? sB + s * C::B_BYTES : sA + s * C::A_BYTES);
           const uint32_t wdst = smem_u32(SWAP ? sA + s * C::A_BYTES : sB + s * C::B_BYTES);
-          tma_load_2d(xdst, &tmX, FULL(s), r * p.x_k_seg + kb * 64, t0);
-          tma_load_2d(wdst, &tmW, FULL(s), kb * 64, r * p.w_row_seg + f0);
+          if constexpr (PAIR) {
+            // both CTAs' loads complete on the leader's full barrier, which expects both
+            const uint32_t cbar = mapa_shared(FULL(s), 0);
+            if (crank == 0) mbar_arrive_expect_tx(FULL(s), 2 * C::STAGE_BYTES);
+            tma_load_2d_pair(xdst, &tmX, cbar, r * p.x_k_seg + kb * 64, t0);
+            tma_load_2d_pair(wdst, &tmW, cbar, kb * 64, r * p.w_row_seg + f0);
+          } else {
+            mbar_arrive_expect_tx(FULL(s), C::STAGE_BYTES);
+            tma_load_2d(xdst, &tmX, FULL(s), r * p.x_k_seg + kb * 64, t0);
+            tma_load_2d(wdst, &tmW, FULL(s), kb * 64, r * p.w_row_seg + f0);
+          }
           ++it;
         }
         if constexpr (C::DYN) u = static_cast<int>(gridDim.x) + atomicAdd(p.sched_counter, 1);
-        else u += gridDim.x;
+        else u += ustep;
       }
-      // every load issued has landed before the CTA may exit
-      for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-        mbar_wait(FULL(j % STAGES), (j / STAGES) & 1, nullptr, p.status);
+      // every load issued has landed before the CTA may exit (a pair's loads land on
+      // the leader's barriers: the leader waits for both CTAs', and the peer stays
+      // until the final cluster barrier, which the leader reaches after this)
+      if (crank == 0)
+        for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+          mbar_wait(FULL(j % STAGES), (j / STAGES) & 1, nullptr, p.status);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(128, BN);
+    // ---------------- MMA issuer (a pair's leader issues for both CTAs) ----------------
+    if (lane == 0 && crank == 0) {
+      const uint32_t idesc = idesc_f16_f32(PAIR ? 256 : 128, BN);
       int it = 0, seg = 0, qk = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && (C::DYN || u < units); u += gridDim.x) {
+      for (int u = u0; ok && (C::DYN || u < units); u += ustep) {
         if constexpr (C::DYN) {
           if (!mbar_wait(QFULL(qk % C::QUEUE), (qk / C::QUEUE) & 1, abort_flag, p.status)) break;
           u = queue[qk % C::QUEUE];
@@ -1201,16 +1231,22 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
             const uint64_t bd = sdesc_k_sw128(smem_u32(sB + s * C::B_BYTES));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              tc_mma_f16(d, ad + 2ull * kk, bd + 2ull * kk, idesc, (g > gs || kk > 0) ? 1u : 0u);
-            tc_commit(EMPTY(s));
+            {
+              if constexpr (PAIR) tc_mma_f16_pair(d, ad + 2ull * kk, bd + 2ull * kk, idesc, (g > gs || kk > 0) ? 1u : 0u);
+              else tc_mma_f16(d, ad + 2ull * kk, bd + 2ull * kk, idesc, (g > gs || kk > 0) ? 1u : 0u);
+            }
+            if constexpr (PAIR) tc_commit_pair_mc(EMPTY(s));  // frees the stage in both CTAs
+            else tc_commit(EMPTY(s));
             ++it;
           }
           if (!ok) break;
-          tc_commit(TFULL(b));
+          if constexpr (PAIR) tc_commit_pair_mc(TFULL(b));  // both CTAs' epilogues
+          else tc_commit(TFULL(b));
           ++seg;
         }
       }
-      tc_commit(DRAIN);
+      if constexpr (PAIR) tc_commit_pair_local(DRAIN);
+      else tc_commit(DRAIN);
       mbar_wait(DRAIN, 0, nullptr, p.status);
     }
   } else if constexpr (SWAP && EPI != EPI_ARGMAX) {
@@ -1244,6 +1280,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
       ok = mbar_wait(TFULL(b), use, abort_flag, p.status);
       if (!named_bar_and(1, 128, ok)) break;
       tc_fence_after();
+      // Each warp reduces every token column of the tile over its 32 vocab rows:
+      // redux.sync max of the order-preserving 32-bit image of the logit (amax_key's
+      // high word), then the lowest lane holding it (the lowest vocab index); lane l
+      // keeps column c0 + l.  No barrier inside the tile: the 4 warps meet once, in
+      // shared memory, after the accumulator has been handed back.
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         float v[32];
@@ -1261,58 +1302,35 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
           for (int i = 0; i < 32; ++i)
             if (i < ncol) p.logits[static_cast<size_t>(t0 + c0 + i) * p.ld_logits + f] = v[i];
         }
-        // Transpose-reduce across the warp: at each step a lane keeps half of its
-        // columns, trades the other half with its partner and keeps the better of
-        // each pair; after 5 steps lane l holds column l reduced over the warp's
-        // 32 rows (31 exchanges instead of 5 per column).
-        float bv[32];
-        int bi[32];
+        uint32_t mkey = 0u, mlane = 0u;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          bv[i] = f_ok ? v[i] : -INFINITY;
-          bi[i] = f_ok ? f : INT_MAX;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const bool upper = (lane & o) != 0;
-#pragma unroll
-          for (int i = 0; i < o; ++i) {
-            const float send_v = upper ? bv[i] : bv[i + o];
-            const int send_i = upper ? bi[i] : bi[i + o];
-            const float keep_v = upper ? bv[i + o] : bv[i];
-            const int keep_i = upper ? bi[i + o] : bi[i];
-            const float rv = __shfl_xor_sync(0xffffffffu, send_v, o);
-            const int ri = __shfl_xor_sync(0xffffffffu, send_i, o);
-            const bool take = amax_better(rv, ri, keep_v, keep_i);
-            bv[i] = take ? rv : keep_v;
-            bi[i] = take ? ri : keep_i;
+        for (int i = 0; i < (BN < 32 ? BN : 32); ++i) {
+          const uint32_t k = f_ok ? static_cast<uint32_t>(amax_key(v[i], 0) >> 32) : 0u;  // 0: no row
+          const uint32_t m = __reduce_max_sync(0xffffffffu, k);
+          const uint32_t bal = __ballot_sync(0xffffffffu, k == m);
+          if (lane == i) {
+            mkey = m;
+            mlane = static_cast<uint32_t>(__ffs(bal) - 1);
           }
         }
-        red_v[q * 32 + lane] = bv[0];
-        red_i[q * 32 + lane] = bi[0];
-        named_bar_sync(1, 128);
-        if (et < ncol) {
-          const int t = t0 + c0 + et;
-          float bv = best_v[t];
-          int bi = best_i[t];
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const float ov = red_v[w * 32 + et];
-            const int oi = red_i[w * 32 + et];
-            if (amax_better(ov, oi, bv, bi)) {
-              bv = ov;
-              bi = oi;
-            }
-          }
-          best_v[t] = bv;
-          best_i[t] = bi;
+        if (c0 + lane < BN) {
+          const uint32_t fw = static_cast<uint32_t>(un.tf * 128 + q * 32) + mlane;
+          wkey[q * BN + c0 + lane] =
+              mkey == 0u ? 0ull : ((static_cast<unsigned long long>(mkey) << 32) | static_cast<unsigned long long>(~fw));
         }
-        named_bar_sync(1, 128);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(TEMPTY(b));
       ++seg;
+      named_bar_sync(1, 128);
+      for (int c = et; c < BN && t0 + c < p.T; c += 128) {
+        unsigned long long k = bestk[c];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) k = max(k, wkey[w * BN + c]);
+        bestk[c] = k;
+      }
+      named_bar_sync(1, 128);  // wkey is rewritten by the next tile
     }
     // Each CTA folds its per-token best into one 64-bit key per token with
     // atomicMax (key order = torch.argmax order); the last CTA to finish reads the
@@ -1323,7 +1341,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
     {
       const bool all_ok = named_bar_and(1, 128, ok);
       if (all_ok)
-        for (int t = et; t < p.T; t += 128) atomicMax(p.amax_keys + t, amax_key(best_v[t], best_i[t]));
+        for (int t = et; t < p.T; t += 128)
+          if (bestk[t] != 0ull) atomicMax(p.amax_keys + t, bestk[t]);
       __threadfence();
       named_bar_sync(1, 128);
       if (et == 0) *last_flag = (atomicAdd(p.done_counter, 1) == static_cast<int>(gridDim.x) - 1) ? 1 : 0;
@@ -1366,10 +1385,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
       named_bar_sync(1, 32 * C::EW);
     }
     int seg = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    for (int u = u0; u < units; u += ustep) {
       const Unit un = unit_of(p, u);
-      const int t = un.tt * 128 + row;
-      const int tbox = un.tt * 128 + q * 32;  // first row of this warp's boxes
+      const int t = un.tt * C::TM_T + static_cast<int>(crank) * 128 + row;
+      const int tbox = un.tt * C::TM_T + static_cast<int>(crank) * 128 + q * 32;  // first row of this warp's boxes
       const int f0 = un.tf * BN;
       const bool row_ok = t < p.T;
       float rinv = 1.0f;  // deferred RMSNorm of the input row (QKV, gate_up)
@@ -1403,7 +1422,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
         if (!ok) break;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(TEMPTY(b));
+        if (lane == 0) tempty_arrive(TEMPTY(b));
         ++seg;
       } else if constexpr (!ACC) {
         const int b = seg & 1;
@@ -1477,7 +1496,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(TEMPTY(b));
+        if (lane == 0) tempty_arrive(TEMPTY(b));
         ++seg;
       } else {
         float acc[BNH];  // this thread's columns cbase .. cbase + BNH
@@ -1503,7 +1522,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(TEMPTY(b));
+          if (lane == 0) tempty_arrive(TEMPTY(b));
           ++seg;
         }
         // every epilogue thread takes the same path from here (named barriers follow)
@@ -1625,9 +1644,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP>::THREADS, 1)
 #undef QEMPTY
   tc_fence_before();
   __syncthreads();
+  // a pair: the leader's MMAs into this CTA's TMEM and shared memory, and the
+  // peer's arrivals on the leader's barriers, are all done before either leaves
+  if constexpr (PAIR) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    else tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -1696,6 +1719,10 @@ static bool make_map_rows16(CUtensorMap* m, const void* base, int64_t rows, int6
 }
 
 static inline int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// tile width of a CTA pair (TMEM: two accumulators of BN columns per CTA): 256,
+// or 128 for the rank-sum epilogue (its running sums in registers hold BN at 128)
+constexpr int kPairMaxBN = 256;
 
 GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
   GemmPlan pl{};
@@ -1777,6 +1804,23 @@ GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
     pl.BN = 128;
     pl.tiles_f = cdiv(pr.N, 128);
   }
+  // CTA pairs (256-token tiles, cta_group::2): unsplit token tiles with enough
+  // pair tiles to keep at least half of the SM pairs busy
+  if (pl.splits == 1 && (pr.epi == EPI_STORE || pr.epi == EPI_SILU || pr.epi == EPI_QKV || pr.epi == EPI_RESID) &&
+      pr.T >= 256) {
+    const int bn = (pl.acc || pr.epi == EPI_RESID) ? 128 : kPairMaxBN;  // the pair variants instantiated
+    const int tt2 = cdiv(pr.T, 256), tf2 = cdiv(pr.N, bn);
+    if (tt2 * tf2 >= num_sms / 4) {
+      pl.pair = true;
+      pl.BN = bn;
+      pl.tiles_t = tt2;
+      pl.tiles_f = tf2;
+      const int pairs = tt2 * tf2 < num_sms / 2 ? tt2 * tf2 : num_sms / 2;
+      pl.grid = 2 * pairs;
+      pl.partial_floats = 0;
+      return pl;
+    }
+  }
   const int units = pl.tiles_t * pl.tiles_f * pl.splits;
   pl.grid = units < num_sms ? units : num_sms;
   pl.partial_floats = pl.splits > 1 ? static_cast<size_t>(pl.tiles_t) * pl.tiles_f * pl.splits * pl.BN * 128 : 0;
@@ -1785,11 +1829,11 @@ GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
 
 int gemm_num_tiles_f(const GemmProblem& pr, const GemmPlan& plan) { return plan.tiles_f; }
 
-template <int BN, int EPI, bool ACC, bool SWAP>
+template <int BN, int EPI, bool ACC, bool SWAP, bool PAIR = false>
 static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, const GemmProblem& pr,
                                   const GemmParams& gp, int grid, cudaStream_t s) {
-  auto kern = gemm_tc_kernel<BN, EPI, ACC, SWAP>;
-  using Cfg = GemmCfg<BN, EPI, ACC, SWAP>;
+  auto kern = gemm_tc_kernel<BN, EPI, ACC, SWAP, PAIR>;
+  using Cfg = GemmCfg<BN, EPI, ACC, SWAP, PAIR>;
   constexpr int smem = Cfg::SMEM;
   static PerDevice attr;  // per instantiation and device
   {
@@ -1818,6 +1862,7 @@ static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, 
         !make_map_rows16(&mkv, pr.qkv.kv, kv_rows, pr.qkv.hd, qp))
       return cudaErrorInvalidValue;
   }
+  if constexpr (PAIR) return launch_pdl_pair(kern, dim3(grid), dim3(Cfg::THREADS), smem, s, mx, mw, mo, mo2, mkv, gp);
   return launch_pdl(kern, dim3(grid), dim3(Cfg::THREADS), smem, s, mx, mw, mo, mo2, mkv, gp);
 }
 
@@ -1827,7 +1872,8 @@ cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partia
   if (pr.k_seg % 64 || pr.ldo % 8) return cudaErrorInvalidValue;
   CUtensorMap mx, mw;
   if (!make_map(&mx, pr.x, pr.x_rows, pr.x_cols, pr.x_ld, pl.swap ? pl.BN : 128)) return cudaErrorInvalidValue;
-  if (!make_map(&mw, pr.w, pr.w_rows, pr.w_cols, pr.w_ld, pl.swap ? 128 : pl.BN)) return cudaErrorInvalidValue;
+  if (!make_map(&mw, pr.w, pr.w_rows, pr.w_cols, pr.w_ld, pl.swap ? 128 : (pl.pair ? pl.BN / 2 : pl.BN)))
+    return cudaErrorInvalidValue;
   GemmParams gp{};
   gp.T = pr.T;
   gp.N = pr.N;
@@ -1872,8 +1918,16 @@ cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partia
   gp.status = status;
   const int g = pl.grid;
 #define TP_V(BN_, EPI_, ACC_, SW_)                                                           \
-  if (pl.BN == BN_ && pr.epi == EPI_ && pl.acc == ACC_ && pl.swap == SW_)                     \
+  if (pl.BN == BN_ && pr.epi == EPI_ && pl.acc == ACC_ && pl.swap == SW_ && !pl.pair)         \
     return launch_variant<BN_, EPI_, ACC_, SW_>(mx, mw, pr, gp, g, stream);
+#define TP_VP(BN_, EPI_, ACC_)                                                               \
+  if (pl.BN == BN_ && pr.epi == EPI_ && pl.acc == ACC_ && !pl.swap && pl.pair)               \
+    return launch_variant<BN_, EPI_, ACC_, false, true>(mx, mw, pr, gp, g, stream);
+  TP_VP(256, EPI_STORE, false)
+  TP_VP(256, EPI_SILU, false)
+  TP_VP(256, EPI_QKV, false)
+  TP_VP(128, EPI_RESID, false)
+  TP_VP(128, EPI_RESID, true)
   TP_V(256, EPI_STORE, false, false)
   TP_V(128, EPI_STORE, false, false)
   TP_V(64, EPI_STORE, false, false)
@@ -1907,6 +1961,7 @@ cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partia
   TP_V(128, EPI_ARGMAX, false, true)
   TP_V(256, EPI_ARGMAX, false, true)
 #undef TP_V
+#undef TP_VP
   return cudaErrorNotSupported;
 }
 

@@ -86,6 +86,28 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// The same, as clusters of two CTAs (a CTA pair sharing tcgen05 cta_group::2 MMAs);
+// grid.x must be even.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl_pair(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                   Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---------------- KV cache addressing ----------------
 // A layer's cache is [n][2 (K, V)][blocks][nkv_l][block_len][hd] bf16.  Position p
 // of sequence b lives in block table[b * stride + p / block_len], at row
@@ -197,6 +219,7 @@ struct GemmProblem {
 struct GemmPlan {
   int BN;
   bool swap;        // weights on the MMA's M side (few tokens): tiles of 128 features x BN tokens
+  bool pair;        // CTA pairs (clusters of 2): tiles of 256 tokens x BN features, cta_group::2 MMAs
   bool acc;         // running sum in registers (multi-segment or split-K)
   int tiles_t, tiles_f, splits;
   int grid;
