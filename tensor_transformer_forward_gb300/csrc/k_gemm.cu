@@ -131,7 +131,8 @@ struct GemmCfg {
   static constexpr int BEST = (SWAP && EPI == EPI_ARGMAX) ? 256 : 64;
   // the weight-streaming argmax keeps 64-bit keys instead: [4 warps][BN] column
   // maxima of a tile and [BN] per-token running maxima
-  static constexpr int SMALL_BYTES = 64 + ((SWAP && EPI == EPI_ARGMAX) ? 40 * BN : 1024 + 8 * BEST);
+  // and, per epilogue warp, a 32 x 33 word buffer that transposes a 32 x 32 block of keys
+  static constexpr int SMALL_BYTES = 64 + ((SWAP && EPI == EPI_ARGMAX) ? 40 * BN + 4 * 32 * 33 * 4 : 1024 + 8 * BEST);
   static constexpr int SMEM =
       1024 + STAGES * STAGE_BYTES + OUT_BYTES + TROW_BYTES + NUM_BARS * 8 + SMALL_BYTES + 128 + QKV_BYTES;
   static_assert(SMEM <= 232448, "shared memory per block");
@@ -1059,6 +1060,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
   float* red_v = reinterpret_cast<float*>(small);
   unsigned long long* wkey = reinterpret_cast<unsigned long long*>(small);
   unsigned long long* bestk = wkey + 4 * BN;
+  uint32_t* transp = reinterpret_cast<uint32_t*>(bestk + BN);  // [4 warps][32][33]
   // QKV_PAIR: [2][128] q/k norm weights, 128-byte aligned (the staging rows below take 16-byte accesses)
   float* sNw = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(small + (C::SMALL_BYTES - 64)) + 127) &
                                         ~uintptr_t(127));
@@ -1280,11 +1282,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
       ok = mbar_wait(TFULL(b), use, abort_flag, p.status);
       if (!named_bar_and(1, 128, ok)) break;
       tc_fence_after();
-      // Each warp reduces every token column of the tile over its 32 vocab rows:
-      // redux.sync max of the order-preserving 32-bit image of the logit (amax_key's
-      // high word), then the lowest lane holding it (the lowest vocab index); lane l
-      // keeps column c0 + l.  No barrier inside the tile: the 4 warps meet once, in
-      // shared memory, after the accumulator has been handed back.
+      // Each warp reduces every token column of the tile over its 32 vocab rows.
+      // A 32 x 32 block (rows = lanes, columns = tokens) of order-preserving keys
+      // (amax_key's high word) goes through a padded shared-memory buffer, so that
+      // lane l then scans column c0 + l down the 32 rows (strictly greater keeps
+      // the lowest row, the lowest vocab index, on ties).  No barrier inside the
+      // tile: the 4 warps meet once, after the accumulator has been handed back.
+      uint32_t* tb = transp + q * (32 * 33);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         float v[32];
@@ -1302,17 +1306,20 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
           for (int i = 0; i < 32; ++i)
             if (i < ncol) p.logits[static_cast<size_t>(t0 + c0 + i) * p.ld_logits + f] = v[i];
         }
+#pragma unroll
+        for (int i = 0; i < (BN < 32 ? BN : 32); ++i)  // 0: no row (every key of a row is above 0)
+          tb[i * 33 + lane] = f_ok ? static_cast<uint32_t>(amax_key(v[i], 0) >> 32) : 0u;
+        __syncwarp();
         uint32_t mkey = 0u, mlane = 0u;
 #pragma unroll
-        for (int i = 0; i < (BN < 32 ? BN : 32); ++i) {
-          const uint32_t k = f_ok ? static_cast<uint32_t>(amax_key(v[i], 0) >> 32) : 0u;  // 0: no row
-          const uint32_t m = __reduce_max_sync(0xffffffffu, k);
-          const uint32_t bal = __ballot_sync(0xffffffffu, k == m);
-          if (lane == i) {
-            mkey = m;
-            mlane = static_cast<uint32_t>(__ffs(bal) - 1);
+        for (int r = 0; r < 32; ++r) {
+          const uint32_t k = tb[lane * 33 + r];
+          if (k > mkey) {
+            mkey = k;
+            mlane = static_cast<uint32_t>(r);
           }
         }
+        __syncwarp();  // the buffer is rewritten by the next block
         if (c0 + lane < BN) {
           const uint32_t fw = static_cast<uint32_t>(un.tf * 128 + q * 32) + mlane;
           wkey[q * BN + c0 + lane] =
