@@ -79,6 +79,7 @@ struct GemmParams {
 // handles its 128 rows from its own TMEM.
 template <int BN, int EPI = EPI_STORE, bool ACC = false, bool SWAP = false, bool PAIR = false>
 struct GemmCfg {
+  static constexpr int CL = PAIR ? 2 : 1;  // CTAs per cluster
   // epilogue warps: 8 (two per TMEM lane quarter, splitting the columns) where the
   // columns split into independent halves, else 4
   static constexpr int EW =
@@ -115,7 +116,7 @@ struct GemmCfg {
   // swapped epilogues other than the argmax stage the summed tile token-major in
   // fp32 ([BN tokens][128 features]) and write whole token rows from there
   static constexpr int TROW_BYTES = (SWAP && EPI != EPI_ARGMAX) ? BN * 128 * 4 : 0;
-  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * QUEUE;
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * QUEUE + 1;
   // outputs leave through TMA stores (fp16) / TMA reduce-adds (fp32 residual) from one
   // 32-row x 128-byte staging box per epilogue warp
   static constexpr bool TMA_OUT = !SWAP && (EPI == EPI_STORE || EPI == EPI_SILU || EPI == EPI_RESID);
@@ -1041,8 +1042,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
   // rank in the CTA pair (0 issues the MMAs for both); 0 without pairs
   const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
   // a pair takes every unit its cluster index selects (both CTAs the same units)
-  const int u0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int u0 = static_cast<int>(blockIdx.x) / C::CL;
+  const int ustep = static_cast<int>(gridDim.x) / C::CL;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -1076,6 +1077,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
 #define DRAIN (bar0 + 8u * (2 * STAGES + 4))
 #define QFULL(k) (bar0 + 8u * (2 * STAGES + 5 + (k)))
 #define QEMPTY(k) (bar0 + 8u * (2 * STAGES + 5 + C::QUEUE + (k)))
+#define PRO (bar0 + 8u * (2 * STAGES + 5 + 2 * C::QUEUE))
   volatile int* queue = reinterpret_cast<volatile int*>(tmem_slot + 4);  // [QUEUE] tile ids
   // an epilogue warp hands an accumulator back to the MMA issuer (a pair's leader)
   auto tempty_arrive = [&](uint32_t bar) {
@@ -1097,6 +1099,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
       mbar_init(QFULL(k), 1);
       mbar_init(QEMPTY(k), 5);  // the MMA thread and the 4 epilogue warps
     }
+    mbar_init(PRO, 1);
     *abort_flag = 0;
     *last_flag = 0;
     fence_barrier_init();
@@ -1123,14 +1126,21 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int units = p.tiles_t * p.tiles_f * p.splits;
-  // the set-up above overlaps the previous kernel; inputs, counters and outputs come after
-  griddep_wait();
-  griddep_launch();
+  // The set-up above overlaps the previous kernel; inputs, counters and outputs
+  // come after it.  The producer waits on its own, after issuing its first weight
+  // tiles (constant data), so their latency hides behind the previous kernel.
+  if (warp != 0) {
+    griddep_wait();
+    griddep_launch();
+  }
   if (threadIdx.x >= 64) {  // dead intermediates out of L2, no write-back
-    const int64_t nthr = static_cast<int64_t>(gridDim.x) * (blockDim.x - 64);
-    const int64_t me = static_cast<int64_t>(blockIdx.x) * (blockDim.x - 64) + (threadIdx.x - 64);
-    for (int k = 0; k < 2; ++k)
-      for (int64_t i = me; i < p.discard_lines[k]; i += nthr) l2_discard(static_cast<const char*>(p.discard[k]) + i * 128);
+    // after the producer's first loads are out (the discards would queue ahead of them)
+    if (mbar_wait(PRO, 0, abort_flag, p.status)) {
+      const int64_t nthr = static_cast<int64_t>(gridDim.x) * (blockDim.x - 64);
+      const int64_t me = static_cast<int64_t>(blockIdx.x) * (blockDim.x - 64) + (threadIdx.x - 64);
+      for (int k = 0; k < 2; ++k)
+        for (int64_t i = me; i < p.discard_lines[k]; i += nthr) l2_discard(static_cast<const char*>(p.discard[k]) + i * 128);
+    }
   }
   // tile extents on the token and feature sides
   constexpr int TM_T = C::TM_T;         // tokens per tile
@@ -1146,6 +1156,47 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
       // tiles; each tile id goes through a small queue to the MMA and epilogue
       // warps, -1 ends it.  Otherwise a static round-robin over the tiles.
       int qk = 0;
+      // one K block of unit un into stage s: the X part, the W part or both
+      auto load = [&](const Unit& un, int g, int s, bool x_part, bool w_part) {
+        const int r = g / p.kb_seg, kb = g - r * p.kb_seg;
+        // this CTA's token rows and (pairs) its half of the tile's weight rows
+        const int t0 = un.tt * TM_T + static_cast<int>(crank) * 128;
+        const int f0 = un.tf * TM_F + static_cast<int>(crank) * (BN / 2);
+        const uint32_t xdst = smem_u32(SWAP ? sB + s * C::B_BYTES : sA + s * C::A_BYTES);
+        const uint32_t wdst = smem_u32(SWAP ? sA + s * C::A_BYTES : sB + s * C::B_BYTES);
+        if constexpr (PAIR) {
+          // both CTAs' loads complete on the leader's full barrier, which expects both
+          const uint32_t cbar = mapa_shared(FULL(s), 0);
+          if (x_part) tma_load_2d_pair(xdst, &tmX, cbar, r * p.x_k_seg + kb * 64, t0);
+          if (w_part) tma_load_2d_pair(wdst, &tmW, cbar, kb * 64, r * p.w_row_seg + f0);
+        } else {
+          if (x_part) tma_load_2d(xdst, &tmX, FULL(s), r * p.x_k_seg + kb * 64, t0);
+          if (w_part) tma_load_2d(wdst, &tmW, FULL(s), kb * 64, r * p.w_row_seg + f0);
+        }
+      };
+      auto expect = [&](int s) {
+        if constexpr (PAIR) {
+          if (crank == 0) mbar_arrive_expect_tx(FULL(s), 2 * C::STAGE_BYTES);
+        } else {
+          mbar_arrive_expect_tx(FULL(s), C::STAGE_BYTES);
+        }
+      };
+      // The first unit's first stages (all free): weight tiles before the previous
+      // kernel has finished, the X tiles once its outputs are visible.
+      int npre = 0;
+      Unit un0{};
+      if (u0 < units) {
+        un0 = unit_of(p, u0);
+        npre = min(STAGES, un0.g1 - un0.g0);
+        for (int i = 0; i < npre; ++i) {
+          expect(i);
+          load(un0, un0.g0 + i, i, false, true);
+        }
+      }
+      griddep_wait();
+      griddep_launch();
+      for (int i = 0; i < npre; ++i) load(un0, un0.g0 + i, i, true, false);
+      mbar_arrive(PRO);
       for (int u = u0; ok && (C::DYN || u < units);) {
         if constexpr (C::DYN) {
           const int id = u < units ? u : -1;
@@ -1159,29 +1210,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
           if (id < 0) break;
         }
         const Unit un = unit_of(p, u);
-        // this CTA's token rows and (pairs) its half of the tile's weight rows
-        const int t0 = un.tt * TM_T + static_cast<int>(crank) * 128;
-        const int f0 = un.tf * TM_F + static_cast<int>(crank) * (BN / 2);
         for (int g = un.g0; g < un.g1; ++g) {
-          const int r = g / p.kb_seg, kb = g - r * p.kb_seg;
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(EMPTY(s), ph ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t xdst = smem_u32(SWAP ? sB + s * C::B_BYTES : sA + s * C::A_BYTES);
-          const uint32_t wdst = smem_u32(SWAP ? sA + s * C::A_BYTES : sB + s * C::B_BYTES);
-          if constexpr (PAIR) {
-            // both CTAs' loads complete on the leader's full barrier, which expects both
-            const uint32_t cbar = mapa_shared(FULL(s), 0);
-            if (crank == 0) mbar_arrive_expect_tx(FULL(s), 2 * C::STAGE_BYTES);
-            tma_load_2d_pair(xdst, &tmX, cbar, r * p.x_k_seg + kb * 64, t0);
-            tma_load_2d_pair(wdst, &tmW, cbar, kb * 64, r * p.w_row_seg + f0);
-          } else {
-            mbar_arrive_expect_tx(FULL(s), C::STAGE_BYTES);
-            tma_load_2d(xdst, &tmX, FULL(s), r * p.x_k_seg + kb * 64, t0);
-            tma_load_2d(wdst, &tmW, FULL(s), kb * 64, r * p.w_row_seg + f0);
+          if (it >= npre) {  // the first npre K blocks (of unit u0) were issued above
+            const int s = it % STAGES;
+            const uint32_t ph = (it / STAGES) & 1;
+            if (!mbar_wait(EMPTY(s), ph ^ 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            expect(s);
+            load(un, g, s, true, true);
           }
           ++it;
         }
@@ -1649,6 +1687,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
 #undef DRAIN
 #undef QFULL
 #undef QEMPTY
+#undef PRO
   tc_fence_before();
   __syncthreads();
   // a pair: the leader's MMAs into this CTA's TMEM and shared memory, and the
@@ -1869,7 +1908,8 @@ static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, 
         !make_map_rows16(&mkv, pr.qkv.kv, kv_rows, pr.qkv.hd, qp))
       return cudaErrorInvalidValue;
   }
-  if constexpr (PAIR) return launch_pdl_pair(kern, dim3(grid), dim3(Cfg::THREADS), smem, s, mx, mw, mo, mo2, mkv, gp);
+  if constexpr (PAIR)
+    return launch_pdl_cluster(kern, 2, dim3(grid), dim3(Cfg::THREADS), smem, s, mx, mw, mo, mo2, mkv, gp);
   return launch_pdl(kern, dim3(grid), dim3(Cfg::THREADS), smem, s, mx, mw, mo, mo2, mkv, gp);
 }
 

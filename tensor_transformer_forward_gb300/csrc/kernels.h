@@ -86,11 +86,11 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
-// The same, as clusters of two CTAs (a CTA pair sharing tcgen05 cta_group::2 MMAs);
-// grid.x must be even.
+// The same, as clusters of `cluster` CTAs along x (2: a CTA pair sharing tcgen05
+// cta_group::2 MMAs); grid.x must be a multiple of the cluster size.
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl_pair(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                                   Args&&... args) {
+inline cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), int cluster, dim3 grid, dim3 block, size_t smem,
+                                      cudaStream_t s, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -100,7 +100,7 @@ inline cudaError_t launch_pdl_pair(void (*kern)(KArgs...), dim3 grid, dim3 block
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;

@@ -357,12 +357,13 @@ __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// Arrives once on the mbarrier at this shared offset in both CTAs of the pair when
-// every tcgen05 operation the thread issued so far has completed.
-__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar) {
+// Arrives once on the mbarrier at this shared offset in every CTA of `mask` (the
+// cluster ranks' bits; 3 = both CTAs of the first pair) when every tcgen05
+// operation the thread issued so far has completed.
+__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask = 3) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(static_cast<uint16_t>(3))
+      "h"(mask)
       : "memory");
 }
 // The same, on this CTA's mbarrier only.
