@@ -641,7 +641,7 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   aa.counters = reinterpret_cast<int*>(x->ws + x->r_acnt.off);
   aa.status = dev_status;
   if (b->num_prefill > 0) {
-    aa.seq_begin = 0; aa.seq_end = b->num_prefill; aa.splits = 1;
+    aa.seq_begin = 0; aa.seq_end = b->num_prefill; aa.splits = 1; aa.tail_units = 0; aa.tail_splits = 1;
     Timed tm(x, TP_K_ATTN_PREFILL, s);
     e = tpk::launch_attention_prefill(aa, s);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -652,7 +652,9 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
     // split partials must fit the workspace region planned for them
     const int64_t per_split = static_cast<int64_t>(b->num_seqs - b->num_prefill) * n * x->nq_l * (x->hd + 2) * 4;
     const int max_splits = static_cast<int>(std::min<int64_t>(64, static_cast<int64_t>(x->r_apart.bytes) / per_split));
-    aa.splits = tpk::decode_splits(b->max_kv_len, units, x->num_sms, x->hd, x->nq_l / x->nkv_l, std::max(1, max_splits));
+    const tpk::DecodeSplit ds =
+        tpk::decode_split_plan(b->max_kv_len, units, x->num_sms, x->hd, x->nq_l / x->nkv_l, std::max(1, max_splits));
+    aa.splits = ds.splits; aa.tail_units = ds.tail_units; aa.tail_splits = ds.tail_splits;
     Timed tm(x, TP_K_ATTN_DECODE, s);
     e = tpk::launch_attention_decode(aa, s);
     if (e != cudaSuccess) return cuda_fail(e);

@@ -51,6 +51,33 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   return r;
 }
 
+// CTA i of a decode launch (1D grid): its (sequence, rank, kv head) unit, its key
+// split and the unit's split count.  Units [0, U - tail_units) have `splits`
+// splits, the rest tail_splits; a unit's CTAs are consecutive.
+struct DecCta {
+  int unit, split, nsplit;
+};
+__device__ __forceinline__ DecCta dec_cta(const AttnArgs& a, int i) {
+  const int units = (a.seq_end - a.seq_begin) * a.n * a.nkv_l;
+  const int u1 = units - a.tail_units;
+  DecCta c;
+  if (i < u1 * a.splits) {
+    c.unit = i / a.splits;
+    c.split = i % a.splits;
+    c.nsplit = a.splits;
+  } else {
+    const int j = i - u1 * a.splits;
+    c.unit = u1 + j / a.tail_splits;
+    c.split = j % a.tail_splits;
+    c.nsplit = a.tail_splits;
+  }
+  return c;
+}
+// partials per unit in the split workspace (the larger of the two split counts)
+__device__ __forceinline__ int dec_part_stride(const AttnArgs& a) {
+  return a.tail_units > 0 && a.tail_splits > a.splits ? a.tail_splits : a.splits;
+}
+
 // ---------------------------------------------------------------------------
 // Decode (one new token per sequence): flash-decoding split over the keys.
 // One CTA = (sequence, rank, local kv head, key split).  Warp 4 streams the
@@ -85,15 +112,15 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ks = lane / LPK, dc = lane % LPK;
   const int per_seq = a.n * a.nkv_l;
-  const int unit = blockIdx.x;
+  const DecCta cta = dec_cta(a, blockIdx.x);
+  const int unit = cta.unit, split = cta.split, nsplit = cta.nsplit, pstride = dec_part_stride(a);
   const int b = a.seq_begin + unit / per_seq;
   const int r = (unit % per_seq) / a.nkv_l;
   const int g = unit % a.nkv_l;
-  const int split = blockIdx.y;
   const int t = a.cu_q[b];
   const int L = a.ctx_len[b] + 1;
   // splits start on kKeyAlign-key boundaries (pages hold whole chunks)
-  const int chunk = ((L + a.splits - 1) / a.splits + kKeyAlign - 1) / kKeyAlign * kKeyAlign;
+  const int chunk = ((L + nsplit - 1) / nsplit + kKeyAlign - 1) / kKeyAlign * kKeyAlign;
   const int k0 = split * chunk;
   const int k1n = min(L, k0 + chunk);
 
@@ -260,7 +287,7 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
   }
   __syncthreads();
   const int unit_heads = G * HD;
-  float* part = a.part + (static_cast<size_t>(unit) * a.splits + split) * G * (HD + 2);
+  float* part = a.part + (static_cast<size_t>(unit) * pstride + split) * G * (HD + 2);
   for (int e = threadIdx.x; e < unit_heads; e += blockDim.x) {
     const int h = e / HD, d = e % HD;
     float mm = -INFINITY, ll = 0.0f, aa = 0.0f;
@@ -275,7 +302,7 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
         mm = mn;
       }
     }
-    if (a.splits == 1) {
+    if (nsplit == 1) {
       __half* o = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
                   (static_cast<size_t>(r) * a.nq_l + g * G + h) * HD + d;
       uint32_t sat = 0;
@@ -289,21 +316,21 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
       }
     }
   }
-  if (a.splits == 1) return;
+  if (nsplit == 1) return;
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     const int old = atomicAdd(a.counters + unit, 1);
-    last_flag = (old == a.splits - 1);
+    last_flag = (old == nsplit - 1);
   }
   __syncthreads();
   if (!last_flag) return;
   __threadfence();
-  const float* pbase = a.part + static_cast<size_t>(unit) * a.splits * G * (HD + 2);
+  const float* pbase = a.part + static_cast<size_t>(unit) * pstride * G * (HD + 2);
   for (int e = threadIdx.x; e < unit_heads; e += blockDim.x) {
     const int h = e / HD, d = e % HD;
     float mm = -INFINITY, ll = 0.0f, aa = 0.0f;
-    for (int sp = 0; sp < a.splits; ++sp) {
+    for (int sp = 0; sp < nsplit; ++sp) {
       const float* ps = pbase + (static_cast<size_t>(sp) * G + h) * (HD + 2);
       const float m2 = __ldcg(ps + HD), l2 = __ldcg(ps + HD + 1), a2 = __ldcg(ps + d);
       const float mn = fmaxf(mm, m2);
@@ -356,7 +383,7 @@ static cudaError_t decode_tc_ctas_per_sm(int G, int* per_sm);
 // 1.25 tiles fit split sweeps of 64 sequences x 4097 keys (tp 2) and 32 x 2049
 // (tp 16), 512 units each: 1 split was best in both, 161 / 91 us against 177 / 109 us
 // with 2 and more with 3, 4 or 6.  Ties go to fewer splits.
-int decode_splits(int max_kv_len, int num_units, int num_sms, int hd, int G, int max_splits) {
+static int decode_splits(int max_kv_len, int num_units, int num_sms, int hd, int G, int max_splits) {
   int per_sm = 1;
   cudaError_t e = cudaErrorNotSupported;
 #define TP_OCC(HD_, G_) \
@@ -419,7 +446,10 @@ cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s) {
   const int seqs = a.seq_end - a.seq_begin;
   if (seqs <= 0) return cudaSuccess;
   const int G = a.nq_l / a.nkv_l;
-  dim3 grid(seqs * a.n * a.nkv_l, a.splits);
+  const int units = seqs * a.n * a.nkv_l;
+  if (a.splits < 1 || a.tail_units < 0 || a.tail_units > units || (a.tail_units > 0 && a.tail_splits < 1))
+    return cudaErrorInvalidValue;
+  dim3 grid((units - a.tail_units) * a.splits + a.tail_units * (a.tail_units > 0 ? a.tail_splits : 0));
 #define TP_DEC_TC(HD_, G_) \
   if (a.hd == HD_ && G == G_) return launch_decode_tc_hd<HD_, G_>(a, grid, s);
 #define TP_DEC(HD_, G_) \
@@ -492,15 +522,15 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
 #define D_DR (bar0 + 8u * 10)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int per_seq = a.n * a.nkv_l;
-  const int unit = blockIdx.x;
+  const DecCta cta = dec_cta(a, blockIdx.x);
+  const int unit = cta.unit, split = cta.split, nsplit = cta.nsplit, pstride = dec_part_stride(a);
   const int b = a.seq_begin + unit / per_seq;
   const int r = (unit % per_seq) / a.nkv_l;
   const int g = unit % a.nkv_l;
-  const int split = blockIdx.y;
   const int t = a.cu_q[b];
   const int L = a.ctx_len[b] + 1;
   // splits start on kKeyAlign-key boundaries (a page holds whole key tiles)
-  const int chunk = ((L + a.splits - 1) / a.splits + kKeyAlign - 1) / kKeyAlign * kKeyAlign;
+  const int chunk = ((L + nsplit - 1) / nsplit + kKeyAlign - 1) / kKeyAlign * kKeyAlign;
   const int k0 = split * chunk;
   const int k1n = min(L, k0 + chunk);
   // a split whose keys lie (partly) outside the cache reads nothing and flags the batch
@@ -743,7 +773,7 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
       for (int h = 0; h < G; ++h) ov[h] += ov[G + h];  // P V = P_hi V + P_lo V
       const int d = row;
       if (d < HD) {
-        if (a.splits == 1) {
+        if (nsplit == 1) {
 #pragma unroll
           for (int h = 0; h < G; ++h) {
             __half* o = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
@@ -753,7 +783,7 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
             report_sat(a.status, sat);
           }
         } else {
-          float* part = a.part + (static_cast<size_t>(unit) * a.splits + split) * G * (HD + 2);
+          float* part = a.part + (static_cast<size_t>(unit) * pstride + split) * G * (HD + 2);
 #pragma unroll
           for (int h = 0; h < G; ++h) {
             part[h * (HD + 2) + d] = ov[h];
@@ -781,19 +811,19 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
-  if (a.splits == 1) return;
+  if (nsplit == 1) return;
   // the last CTA of this (sequence, rank, head) to finish merges the splits in order
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) *last_flag = (atomicAdd(a.counters + unit, 1) == a.splits - 1) ? 1 : 0;
+  if (threadIdx.x == 0) *last_flag = (atomicAdd(a.counters + unit, 1) == nsplit - 1) ? 1 : 0;
   __syncthreads();
   if (!*last_flag) return;
   __threadfence();
-  const float* pbase = a.part + static_cast<size_t>(unit) * a.splits * G * (HD + 2);
+  const float* pbase = a.part + static_cast<size_t>(unit) * pstride * G * (HD + 2);
   for (int e = threadIdx.x; e < G * HD; e += blockDim.x) {
     const int h = e / HD, d = e % HD;
     float mm = -INFINITY, ll = 0.0f, aa = 0.0f;
-    for (int sp = 0; sp < a.splits; ++sp) {
+    for (int sp = 0; sp < nsplit; ++sp) {
       const float* ps = pbase + (static_cast<size_t>(sp) * G + h) * (HD + 2);
       const float m2 = __ldcg(ps + HD), l2 = __ldcg(ps + HD + 1), a2 = __ldcg(ps + d);
       const float mn = fmaxf(mm, m2);
@@ -855,6 +885,39 @@ static cudaError_t launch_decode_tc_hd(const AttnArgs& a, dim3 grid, cudaStream_
   if (!make_tmap_2d(&mkv, a.kv, kv_rows, HD, HD, 128, true)) return cudaErrorInvalidValue;
   if (!make_tmap_2d(&mkv16, a.kv, kv_rows, HD, HD, 16, true)) return cudaErrorInvalidValue;
   return launch_pdl(attn_decode_tc_kernel<HD, G>, grid, dim3(192), C::SMEM, s, mkv, mkv16, a);
+}
+
+// The split count of decode_splits for every unit, and a thinner last wave split further:
+// with one split per unit, when the units of the last partial wave fill at most
+// half of the resident CTAs, each of them takes f = resident / units-in-the-wave
+// splits (at most 4, each at least two key tiles) so that the wave keeps enough
+// loads in flight to hold the HBM rate (measured on 128 sequences x 2049 keys,
+// tp 2: 1024 units on 304 resident CTAs leave 112 for the last wave).
+DecodeSplit decode_split_plan(int max_kv_len, int num_units, int num_sms, int hd, int G, int max_splits) {
+  DecodeSplit d{decode_splits(max_kv_len, num_units, num_sms, hd, G, max_splits), 0, 1};
+  if (hd != 128 || d.splits != 1 || num_units <= 0) return d;
+  // resident CTAs per SM from the shared memory they take (the occupancy query
+  // reports one for this kernel, while two run side by side on every SM)
+  int dev = 0, smem_sm = 0, smem_rsv = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+    return d;
+  int per_sm = smem_sm / (DtcCfg<128>::SMEM + smem_rsv);
+  if (per_sm > 2048 / 192) per_sm = 2048 / 192;  // threads
+  if (per_sm < 1) return d;
+  const int resident = num_sms * per_sm;
+  const int rem = num_units % resident;
+  if (rem == 0 || num_units < resident || 2 * rem > resident) return d;
+  int f = resident / rem;
+  const int tiles = (max_kv_len + 127) / 128;
+  if (f > tiles / 2) f = tiles / 2;
+  if (f > 4) f = 4;
+  if (f > max_splits) f = max_splits;
+  if (f < 2) return d;
+  d.tail_units = rem;
+  d.tail_splits = f;
+  return d;
 }
 
 // ---------------------------------------------------------------------------

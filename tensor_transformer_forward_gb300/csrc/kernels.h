@@ -268,12 +268,20 @@ struct AttnArgs {
   float scale_log2;          // log2(e) / sqrt(hd)
   float* part;               // split-KV partials (decode)
   int* counters;
-  int splits;
+  int splits;                // key splits per (sequence, rank, kv head) unit
+  int tail_units;            // decode: the last tail_units units take tail_splits splits instead
+  int tail_splits;
   int* status;
 };
 cudaError_t launch_attention_prefill(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s);
-int decode_splits(int max_kv_len, int num_units, int num_sms, int hd, int G, int max_splits);
+// Decode split plan: every unit's keys in `splits` parts, except the last
+// tail_units units, in tail_splits parts (a last wave too thin to keep HBM busy,
+// split further); tail_units 0 when no such wave.
+struct DecodeSplit {
+  int splits, tail_units, tail_splits;
+};
+DecodeSplit decode_split_plan(int max_kv_len, int num_units, int num_sms, int hd, int G, int max_splits);
 
 cudaError_t launch_final_norm_select(const void* hidden, int H, const int32_t* cu_q, int B, const void* w,
                                      float eps, void* out, int* status, cudaStream_t s);

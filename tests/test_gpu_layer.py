@@ -35,6 +35,17 @@ def test_decode_varied_context_lengths(n):
     check_step(g, list(range(len(ctxs))))
 
 
+def test_decode_thin_last_wave_split_further():
+    """40 decode sequences at tp 2 (320 (sequence, rank, kv head) units): on a GPU
+    holding 304 resident decode CTAs the last 16 units form a thin last wave and
+    take 4 key splits each.  Those units belong to the last two sequences: one with
+    a single key (three empty splits) and one with 2200; the others ragged."""
+    ctxs = tuple((i * 613) % 2300 for i in range(38)) + (0, 2200)
+    w = synth.Workload("decode_tail", S06, (2,), (), ctxs, 1, False)
+    g = GpuStep(w, 2)
+    check_step(g, [0, 1, 17, 37, 38, 39])
+
+
 @pytest.mark.parametrize("n", [1, 2])
 def test_prefill_with_cache_offset_and_ragged_lengths(n):
     """Prefill sequences with cached context (mask tril(S - T)) and lengths that
