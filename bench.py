@@ -23,6 +23,7 @@ rank 0 prints.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -88,6 +89,9 @@ def workload_config(w: synth.Workload, n: int) -> dict:
 # source at capture time and is reported only while the source is unchanged.
 # The summaries of those captures are under profiles/.
 NCU_TRAFFIC = {
+    # one layer of the mixed step (bench.py --quick --layers 1): the same decode
+    # attention launch as each of the 28 layers' (128 sequences x 2049 keys, tp 2)
+    ("qwen3_0.6b_model_mixed", 2, "attn_decode"): (1082728192 + 5173248, "k_attention.cu", "c6fda36bbfdb82d5"),
     ("qwen3_0.6b_layer_prefill2048", 2, "gemm_lm_head"): (311221504 + 2994944, "k_gemm.cu",
                                                           "60871d5f8a01c0f8"),
     ("qwen3_0.6b_layer_decode64x4096", 2, "attn_decode"): (1078256384 + 3111168, "k_attention.cu",
@@ -611,10 +615,17 @@ def main():
     ap.add_argument("--quick", action="store_true",
                     help="only warm-up + timed steps (no kernel breakdown, e2e or CPU baseline): for profilers")
     ap.add_argument("--no-sub", action="store_true", help="skip the other configurations' records")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="with --quick: run only the first LAYERS layers of the workload (each layer's launches "
+                         "unchanged, less memory held): for profilers")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = synth.WORKLOADS[args.workload]
+    if args.layers is not None:
+        if not args.quick or not 1 <= args.layers <= w.layers_run:
+            ap.error("--layers needs --quick and 1 <= LAYERS <= the workload's layers")
+        w = dataclasses.replace(w, layers_run=args.layers)
     if args.tp is not None:
         n = args.tp
     elif w.name == DEFAULT_WORKLOAD:
