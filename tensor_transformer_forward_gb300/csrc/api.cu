@@ -655,6 +655,7 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
     const tpk::DecodeSplit ds =
         tpk::decode_split_plan(b->max_kv_len, units, x->num_sms, x->hd, x->nq_l / x->nkv_l, std::max(1, max_splits));
     aa.splits = ds.splits; aa.tail_units = ds.tail_units; aa.tail_splits = ds.tail_splits;
+    aa.overlap_prev = b->num_prefill > 0 ? 1 : 0;  // launched right after the prefill attention above
     Timed tm(x, TP_K_ATTN_DECODE, s);
     e = tpk::launch_attention_decode(aa, s);
     if (e != cudaSuccess) return cuda_fail(e);

@@ -139,7 +139,9 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
   const int nchunks = k1 > k0 ? (k1 - k0 + C::CK - 1) / C::CK : 0;
   const __nv_bfloat16* kvb = reinterpret_cast<const __nv_bfloat16*>(a.kv);
   // the batch arrays are the host's; q and the cache come from earlier kernels
-  griddep_wait();
+  // (after a prefill attention launch, which reads and writes nothing of this
+  // launch's, the wait on it moves to the end: see AttnArgs::overlap_prev)
+  if (!a.overlap_prev) griddep_wait();
   griddep_launch();
   if (bad && threadIdx.x == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
 
@@ -316,6 +318,7 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
       }
     }
   }
+  if (a.overlap_prev) griddep_wait();
   if (nsplit == 1) return;
   __threadfence();
   __syncthreads();
@@ -562,7 +565,9 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
   const int k1 = bad ? k0 : k1n;
   const int ntiles = k1 > k0 ? (k1 - k0 + C::BK - 1) / C::BK : 0;
   const uint32_t tmem = *tmem_slot;
-  griddep_wait();  // q and the cache come from the QKV GEMM
+  // q and the cache come from the QKV GEMM (after a prefill attention launch, which
+  // reads and writes nothing of this launch's, the wait on it moves to the end)
+  if (!a.overlap_prev) griddep_wait();
   griddep_launch();
   if (bad && threadIdx.x == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
 
@@ -805,6 +810,7 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
 #undef D_PF
 #undef D_OD
 #undef D_DR
+  if (a.overlap_prev) griddep_wait();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

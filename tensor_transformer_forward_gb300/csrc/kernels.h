@@ -271,6 +271,14 @@ struct AttnArgs {
   int splits;                // key splits per (sequence, rank, kv head) unit
   int tail_units;            // decode: the last tail_units units take tail_splits splits instead
   int tail_splits;
+  // decode launched right after a prefill attention launch of the same batch: the
+  // two touch disjoint data and both depend only on the QKV GEMM, which has
+  // completed once the decode launch starts (every prefill CTA with work releases
+  // its dependents only after its own wait on the QKV GEMM).  The decode CTAs then
+  // start at once on the SMs the prefill CTAs free, and wait on the prefill
+  // launch only before they exit, so a later kernel's wait on the decode launch
+  // still covers both.
+  int overlap_prev;
   int* status;
 };
 cudaError_t launch_attention_prefill(const AttnArgs& a, cudaStream_t s);
