@@ -640,13 +640,10 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   aa.part = reinterpret_cast<float*>(x->ws + x->r_apart.off);
   aa.counters = reinterpret_cast<int*>(x->ws + x->r_acnt.off);
   aa.status = dev_status;
-  if (b->num_prefill > 0) {
-    aa.seq_begin = 0; aa.seq_end = b->num_prefill; aa.splits = 1; aa.tail_units = 0; aa.tail_splits = 1;
-    Timed tm(x, TP_K_ATTN_PREFILL, s);
-    e = tpk::launch_attention_prefill(aa, s);
-    if (e != cudaSuccess) return cuda_fail(e);
-  }
-  if (b->num_prefill < b->num_seqs) {
+  // decode attention first (HBM-bound), then the prefill attention, whose CTAs take
+  // the SMs that the decode launch's last wave leaves free (AttnArgs::overlap_prev)
+  const bool has_decode = b->num_prefill < b->num_seqs;
+  if (has_decode) {
     aa.seq_begin = b->num_prefill; aa.seq_end = b->num_seqs;
     const int units = (b->num_seqs - b->num_prefill) * n * x->nkv_l;
     // split partials must fit the workspace region planned for them
@@ -655,9 +652,16 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
     const tpk::DecodeSplit ds =
         tpk::decode_split_plan(b->max_kv_len, units, x->num_sms, x->hd, x->nq_l / x->nkv_l, std::max(1, max_splits));
     aa.splits = ds.splits; aa.tail_units = ds.tail_units; aa.tail_splits = ds.tail_splits;
-    aa.overlap_prev = b->num_prefill > 0 ? 1 : 0;  // launched right after the prefill attention above
+    aa.overlap_prev = 0;
     Timed tm(x, TP_K_ATTN_DECODE, s);
     e = tpk::launch_attention_decode(aa, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (b->num_prefill > 0) {
+    aa.seq_begin = 0; aa.seq_end = b->num_prefill; aa.splits = 1; aa.tail_units = 0; aa.tail_splits = 1;
+    aa.overlap_prev = has_decode ? 1 : 0;  // launched right after the decode attention above
+    Timed tm(x, TP_K_ATTN_PREFILL, s);
+    e = tpk::launch_attention_prefill(aa, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
 

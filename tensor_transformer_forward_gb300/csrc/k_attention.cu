@@ -139,9 +139,7 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
   const int nchunks = k1 > k0 ? (k1 - k0 + C::CK - 1) / C::CK : 0;
   const __nv_bfloat16* kvb = reinterpret_cast<const __nv_bfloat16*>(a.kv);
   // the batch arrays are the host's; q and the cache come from earlier kernels
-  // (after a prefill attention launch, which reads and writes nothing of this
-  // launch's, the wait on it moves to the end: see AttnArgs::overlap_prev)
-  if (!a.overlap_prev) griddep_wait();
+  griddep_wait();
   griddep_launch();
   if (bad && threadIdx.x == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
 
@@ -318,7 +316,6 @@ __global__ void __launch_bounds__(160) attn_decode_kernel(AttnArgs a) {
       }
     }
   }
-  if (a.overlap_prev) griddep_wait();
   if (nsplit == 1) return;
   __threadfence();
   __syncthreads();
@@ -565,9 +562,9 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
   const int k1 = bad ? k0 : k1n;
   const int ntiles = k1 > k0 ? (k1 - k0 + C::BK - 1) / C::BK : 0;
   const uint32_t tmem = *tmem_slot;
-  // q and the cache come from the QKV GEMM (after a prefill attention launch, which
-  // reads and writes nothing of this launch's, the wait on it moves to the end)
-  if (!a.overlap_prev) griddep_wait();
+  // q and the cache come from the QKV GEMM; dependents are released only after
+  // this wait (a prefill attention launched next relies on it: see AttnArgs)
+  griddep_wait();
   griddep_launch();
   if (bad && threadIdx.x == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
 
@@ -810,7 +807,6 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
 #undef D_PF
 #undef D_OD
 #undef D_DR
-  if (a.overlap_prev) griddep_wait();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -1048,7 +1044,11 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  griddep_wait();  // q and the cache come from the QKV GEMM
+  // q and the cache come from the QKV GEMM; right after a decode attention launch
+  // of the same batch (which touches nothing of this launch's and released its
+  // dependents only after its own wait on the QKV GEMM) the wait on that launch
+  // moves to the end, so these CTAs start on the SMs its last wave leaves free
+  if (!a.overlap_prev) griddep_wait();
   griddep_launch();
 
   if (warp == 0) {
@@ -1289,6 +1289,7 @@ __global__ void __launch_bounds__(320, 1)
 #undef B_PF
 #undef B_OD
 #undef B_DR
+  if (a.overlap_prev) griddep_wait();  // this grid ends after the decode launch it overlapped
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

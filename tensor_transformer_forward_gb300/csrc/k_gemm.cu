@@ -1675,8 +1675,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
     }
     report_sat(p.status, sat);
     if constexpr (C::RESID_ROWS) cp_async_wait_all();  // no copy into the staging outlives the CTA
-    if constexpr (C::TMA_OUT || C::QKV_PAIR) {  // every store has landed before the CTA (and its staging) goes away
-      if (lane == 0) bulk_wait_all();
+    // every store has read its staging before the CTA (and its shared memory) goes
+    // away; the writes themselves complete on their own and are covered by the next
+    // kernel's wait on this grid
+    if constexpr (C::TMA_OUT || C::QKV_PAIR) {
+      if (lane == 0) bulk_wait_read();
       __syncwarp();
     }
   }

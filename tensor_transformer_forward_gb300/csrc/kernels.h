@@ -271,13 +271,13 @@ struct AttnArgs {
   int splits;                // key splits per (sequence, rank, kv head) unit
   int tail_units;            // decode: the last tail_units units take tail_splits splits instead
   int tail_splits;
-  // decode launched right after a prefill attention launch of the same batch: the
-  // two touch disjoint data and both depend only on the QKV GEMM, which has
-  // completed once the decode launch starts (every prefill CTA with work releases
-  // its dependents only after its own wait on the QKV GEMM).  The decode CTAs then
-  // start at once on the SMs the prefill CTAs free, and wait on the prefill
-  // launch only before they exit, so a later kernel's wait on the decode launch
-  // still covers both.
+  // prefill attention launched right after the decode attention launch of the same
+  // batch: the two touch disjoint data and both depend only on the QKV GEMM, which
+  // has completed once the prefill launch starts (every decode CTA releases its
+  // dependents only after its own wait on the QKV GEMM).  The prefill CTAs then
+  // start on the SMs the decode launch's last wave leaves free, and wait on the
+  // decode launch only before they exit, so a later kernel's wait on the prefill
+  // launch still covers both.
   int overlap_prev;
   int* status;
 };

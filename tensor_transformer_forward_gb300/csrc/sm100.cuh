@@ -92,8 +92,6 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the sources of all committed bulk stores have been read (the buffer may be reused)
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// all committed bulk stores have completed
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses
 // 16-byte aligned), completion as transaction bytes on the mbarrier.
