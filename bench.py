@@ -91,7 +91,7 @@ def workload_config(w: synth.Workload, n: int) -> dict:
 NCU_TRAFFIC = {
     # one layer of the mixed step (bench.py --quick --layers 1): the same decode
     # attention launch as each of the 28 layers' (128 sequences x 2049 keys, tp 2)
-    ("qwen3_0.6b_model_mixed", 2, "attn_decode"): (1082728192 + 5173248, "k_attention.cu", "c6fda36bbfdb82d5"),
+    ("qwen3_0.6b_model_mixed", 2, "attn_decode"): (1082728704 + 5169152, "k_attention.cu", "f842709ee3e5c4d5"),
     ("qwen3_0.6b_layer_prefill2048", 2, "gemm_lm_head"): (311221504 + 2994944, "k_gemm.cu",
                                                           "60871d5f8a01c0f8"),
     ("qwen3_0.6b_layer_decode64x4096", 2, "attn_decode"): (1078256384 + 3111168, "k_attention.cu",
