@@ -108,7 +108,10 @@ struct GemmCfg {
       : ((204800 - ROW16_BYTES - ((SWAP && EPI != EPI_ARGMAX) ? BN * 512 : 0)) / STAGE_BYTES) > 12
           ? 12
           : ((204800 - ROW16_BYTES - ((SWAP && EPI != EPI_ARGMAX) ? BN * 512 : 0)) / STAGE_BYTES);
-  static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+  // two accumulators of BN columns, each starting at a multiple of TM_STRIDE (the
+  // allocation is a power of two of at least 32 columns)
+  static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+  static constexpr int TM_STRIDE = TMEM_COLS / 2;
   static constexpr int QUEUE = 4;  // tile queue depth (weight-streaming argmax)
   // weight-streaming argmax: tiles from a dynamic queue; other swapped (few-token)
   // GEMMs: static round-robin over tiles x K splits
@@ -889,7 +892,7 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
         break;
       }
       tc_fence_after();
-      const uint32_t ta = lane_addr + static_cast<uint32_t>(b * BN);
+      const uint32_t ta = lane_addr + static_cast<uint32_t>(b * GemmCfg<BN, EPI, true, true>::TM_STRIDE);
       if constexpr (BN == 16) {
         float v[16];
         tc_ld16(ta, v);
@@ -1257,7 +1260,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+          const uint32_t d = tmem + static_cast<uint32_t>(b * C::TM_STRIDE);
           const int gs = g;
           for (; g < gend; ++g) {
             const int s = it % STAGES;
@@ -1332,11 +1335,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
         float v[32];
         if constexpr (BN == 16) {
           float v16[16];
-          tc_ld16(lane_addr + static_cast<uint32_t>(b * BN), v16);
+          tc_ld16(lane_addr + static_cast<uint32_t>(b * C::TM_STRIDE), v16);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = i < 16 ? v16[i] : 0.0f;
         } else {
-          tc_ld32(lane_addr + static_cast<uint32_t>(b * BN + c0), v);
+          tc_ld32(lane_addr + static_cast<uint32_t>(b * C::TM_STRIDE + c0), v);
         }
         const int ncol = min(min(32, BN), p.T - (t0 + c0));  // valid token columns (warp-uniform)
         if (p.logits && f_ok) {
@@ -1456,7 +1459,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
       if constexpr (C::QKV_PAIR) {
         const int b = seg & 1;
         const uint32_t use = (seg >> 1) & 1;
-        const uint32_t ta = lane_addr + static_cast<uint32_t>(b * BN);
+        const uint32_t ta = lane_addr + static_cast<uint32_t>(b * C::TM_STRIDE);
         const int w = (warp - 2) >> 2;
         uint8_t* stg = sStg + (warp - 2) * (2 * 32 * 128);
         const bool ok = p.qkv.hd == 128
@@ -1474,7 +1477,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
         const uint32_t use = (seg >> 1) & 1;
         if (!warp_all(mbar_wait(TFULL(b), use, abort_flag, p.status))) break;
         tc_fence_after();
-        const uint32_t ta = lane_addr + static_cast<uint32_t>(b * BN);
+        const uint32_t ta = lane_addr + static_cast<uint32_t>(b * C::TM_STRIDE);
         if constexpr (EPI == EPI_QKV) {
           if (BN >= 128 && p.qkv.hd == 128) {
             qkv_stream<BN, (BN >= 128 ? 128 : 64)>(p, ta, t, tp, f0, row_ok, cbase, cbase + BNH, rinv, sat);
@@ -1557,7 +1560,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t ta = lane_addr + static_cast<uint32_t>(b * BN + cbase);
+          const uint32_t ta = lane_addr + static_cast<uint32_t>(b * C::TM_STRIDE + cbase);
 #pragma unroll
           for (int c = 0; c < BNH / 32; ++c) {
             float v[32];
@@ -1780,7 +1783,13 @@ GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
     // up to 256 tokens against the whole vocab: weights on the M side, tokens as N,
     // so the weights stream from HBM once
     pl.swap = true;
-    pl.BN = pr.T <= 16 ? 16 : (pr.T <= 32 ? 32 : (pr.T <= 64 ? 64 : (pr.T <= 128 ? 128 : 256)));
+    pl.BN = pr.T <= 16 ? 16
+            : pr.T <= 32 ? 32
+            : pr.T <= 64 ? 64
+            : pr.T <= 128 ? 128
+            : pr.T <= 160 ? 160
+            : pr.T <= 192 ? 192
+                          : 256;
     pl.tiles_t = 1;
     pl.tiles_f = cdiv(pr.N, 128);
     pl.splits = 1;
@@ -2009,6 +2018,8 @@ cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partia
   TP_V(32, EPI_ARGMAX, false, true)
   TP_V(64, EPI_ARGMAX, false, true)
   TP_V(128, EPI_ARGMAX, false, true)
+  TP_V(160, EPI_ARGMAX, false, true)
+  TP_V(192, EPI_ARGMAX, false, true)
   TP_V(256, EPI_ARGMAX, false, true)
 #undef TP_V
 #undef TP_VP

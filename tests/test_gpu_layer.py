@@ -73,6 +73,16 @@ def test_32b_layer_tp16_replicated_kv():
     check_step(g, [0, 1, 2], head=False)
 
 
+@pytest.mark.parametrize("nseq", [150, 180, 256])
+def test_head_many_sequences_token_tiles(nseq):
+    """The vocab head for 129..256 sequences streams the weights once against one
+    token tile of 160, 192 or 256 columns (the rows past the last sequence are
+    zero fill and never read back); ids and logits of sampled sequences."""
+    w = synth.Workload("head_many", S06, (2,), (), tuple((i * 37) % 200 for i in range(nseq)), 1, True)
+    g = GpuStep(w, 2)
+    check_step(g, [0, nseq // 2, nseq - 1])
+
+
 def test_untied_head_uneven_vocab():
     """Untied LM head with a vocab that leaves the last rank a shorter slice
     (padded columns must never win the argmax)."""
