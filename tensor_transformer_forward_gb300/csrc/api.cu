@@ -161,7 +161,10 @@ WsPlan plan_ws(const tp_ctx* x, int64_t T, int64_t B, int64_t P) {
   take(w.qlo, T * n * x->nq_l * x->hd * 2);
   take(w.attn, T * n * x->nq_l * x->hd * 2);
   take(w.act, T * n * x->i_p * 2);
-  take(w.gpart, static_cast<size_t>(kMaxSms) * 128 * 128 * 4);
+  // split-K partials: 128 x 128 fp32 per SM, or the residual GEMMs' pair tiles (256
+  // tokens x 256 features, two K halves) over all tokens and the hidden size
+  const size_t pair_parts = static_cast<size_t>((T + 255) / 256) * ((H + 255) / 256) * 2 * 2 * 256 * 128 * 4;
+  take(w.gpart, std::max<size_t>(static_cast<size_t>(kMaxSms) * 128 * 128 * 4, pair_parts));
   take(w.gcnt, kGemmCounters * 4);
   const int64_t splits = std::min<int64_t>(kMaxDecodeSplits, std::max<int64_t>(1, (P + 255) / 256));
   take(w.apart, static_cast<size_t>(B) * n * x->nq_l * (x->hd + 2) * splits * 4);
@@ -235,7 +238,7 @@ void set_discard(const tp_ctx* x, tpk::GemmProblem& g, int k, const void* p, siz
 tp_status gemm(tp_ctx* x, int kind, const tpk::GemmProblem& pr, int32_t* dev_status, cudaStream_t s) {
   tpk::GemmPlan pl = tpk::plan_gemm(pr, x->num_sms);
   if (pl.partial_floats * 4 > x->r_gpart.bytes) return TP_ERR_UNSUPPORTED;
-  if (pl.splits > 1 && pl.tiles_t * pl.tiles_f > tpk::kArgmaxKeyOffset) return TP_ERR_UNSUPPORTED;
+  if (pl.splits > 1 && (pl.pair ? 2 : 1) * pl.tiles_t * pl.tiles_f > tpk::kArgmaxKeyOffset) return TP_ERR_UNSUPPORTED;
   Timed tm(x, kind, s);
   cudaError_t e = tpk::launch_gemm(pr, pl, at<float>(x->ws, x->r_gpart), at<int>(x->ws, x->r_gcnt), dev_status, s);
   if (e != cudaSuccess) return cuda_fail(e);

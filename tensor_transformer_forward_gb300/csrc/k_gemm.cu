@@ -160,11 +160,13 @@ __device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
 // After a wait gave up (TP_DEVFLAG_TIMEOUT is set, the results are not valid):
 // counts unit u and every later unit of this CTA in on their split-K tile
 // counters, so that each counter still returns to zero (the last to arrive
-// clears it) and the next launch starts clean.  One thread.
-__device__ __forceinline__ void drain_split_counters(const GemmParams& p, int u, int units) {
+// clears it) and the next launch starts clean.  One thread.  A CTA pair keeps
+// one counter per CTA of a tile (its 128 rows): counter 2 * tile + crank.
+__device__ __forceinline__ void drain_split_counters(const GemmParams& p, int u, int units, int ustep, int per_tile,
+                                                     int crank) {
   if (p.splits <= 1) return;
-  for (; u < units; u += gridDim.x) {
-    const int tile = u / p.splits;
+  for (; u < units; u += ustep) {
+    const int tile = (u / p.splits) * per_tile + crank;
     if (atomicAdd(p.counters + tile, 1) == p.splits - 1) p.counters[tile] = 0;
   }
 }
@@ -914,7 +916,7 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
     }
     // every epilogue thread takes the same path from here (named barriers follow)
     if (!named_bar_and(1, 128, ok)) {
-      if (threadIdx.x == 64) drain_split_counters(p, u, units);
+      if (threadIdx.x == 64) drain_split_counters(p, u, units, gridDim.x, 1, 0);
       break;
     }
     if (p.splits > 1) {
@@ -1575,11 +1577,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
         }
         // every epilogue thread takes the same path from here (named barriers follow)
         if (!named_bar_and(1, 32 * C::EW, ok)) {
-          if (threadIdx.x == 64) drain_split_counters(p, u, units);
+          if (threadIdx.x == 64) drain_split_counters(p, u, units, ustep, PAIR ? 2 : 1, static_cast<int>(crank));
           break;
         }
         if (p.splits > 1) {
-          const int tile = un.tt * p.tiles_f + un.tf;
+          // a pair's CTAs each sum their own 128 rows: one partial set per CTA of the tile
+          const int tile = (un.tt * p.tiles_f + un.tf) * (PAIR ? 2 : 1) + static_cast<int>(crank);
           float* part = p.partials + (static_cast<size_t>(tile) * p.splits + un.split) * (BN * 128);
           if (row_ok) {  // rows past the last token are never read
 #pragma unroll
@@ -1862,6 +1865,31 @@ GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
     pl.BN = 128;
     pl.tiles_f = cdiv(pr.N, 128);
   }
+  // Long-K residual (row-parallel) GEMMs on CTA pairs with 256-wide tiles and the
+  // K range (the rank segments) split in two: a 256-wide pair tile moves its
+  // operands at ~390 ns per K block against ~330 ns for a 128-wide one with half
+  // the MMA work, and the rank-sum's running sums cap the unsplit residual tiles
+  // at 128 columns.  The two halves meet in split-K partials (per CTA of the
+  // pair), the last to arrive adds them in split order.  Measured: 32B down_proj
+  // (1024 tokens, 400 K blocks) 370 -> 279 us; with 32 or 48 K blocks (0.6B
+  // o_proj / down_proj at 2176 tokens) the partials cost more than the main loop
+  // saves (22.8 -> 35.2 and 27.0 -> 37.1 us), so those keep 128-wide tiles.
+  if (pl.splits == 1 && pr.epi == EPI_RESID && pr.T >= 256 && total_kb >= 256) {
+    const int tt2 = cdiv(pr.T, 256), tf2 = cdiv(pr.N, 256);
+    if (tt2 * tf2 * 2 >= num_sms / 4) {
+      pl.pair = true;
+      pl.BN = 256;
+      pl.acc = true;
+      pl.splits = 2;
+      pl.tiles_t = tt2;
+      pl.tiles_f = tf2;
+      const int units = tt2 * tf2 * 2;
+      const int pairs = units < num_sms / 2 ? units : num_sms / 2;
+      pl.grid = 2 * pairs;
+      pl.partial_floats = static_cast<size_t>(tt2) * tf2 * 2 * pl.splits * 256 * 128;
+      return pl;
+    }
+  }
   // CTA pairs (256-token tiles, cta_group::2): unsplit token tiles with enough
   // pair tiles to keep at least half of the SM pairs busy
   if (pl.splits == 1 && (pr.epi == EPI_STORE || pr.epi == EPI_SILU || pr.epi == EPI_QKV || pr.epi == EPI_RESID) &&
@@ -1987,6 +2015,7 @@ cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partia
   TP_VP(256, EPI_QKV, false)
   TP_VP(128, EPI_RESID, false)
   TP_VP(128, EPI_RESID, true)
+  TP_VP(256, EPI_RESID, true)
   TP_V(256, EPI_STORE, false, false)
   TP_V(128, EPI_STORE, false, false)
   TP_V(64, EPI_STORE, false, false)

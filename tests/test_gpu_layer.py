@@ -73,6 +73,18 @@ def test_32b_layer_tp16_replicated_kv():
     check_step(g, [0, 1, 2], head=False)
 
 
+@pytest.mark.parametrize("n", [1, 2])
+def test_long_k_residual_gemm_split_in_two(n):
+    """down_proj with 256 K blocks (intermediate 16384) over 300 prefill tokens runs
+    on 256-wide CTA-pair tiles with its rank segments split in two halves that meet
+    in split-K partials; the residual it leaves against the oracle."""
+    s = synth.ModelShape(hidden=256, num_q_heads=4, num_kv_heads=2, head_dim=64, intermediate=16384, vocab=1000,
+                         num_layers=1)
+    w = synth.Workload("long_k_resid", s, (n,), ((300, 0),), (17,), 1, True)
+    g = GpuStep(w, n)
+    check_step(g, [0, 1])
+
+
 @pytest.mark.parametrize("nseq", [150, 180, 256])
 def test_head_many_sequences_token_tiles(nseq):
     """The vocab head for 129..256 sequences streams the weights once against one
