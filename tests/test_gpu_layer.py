@@ -75,12 +75,13 @@ def test_32b_layer_tp16_replicated_kv():
 
 @pytest.mark.parametrize("n", [1, 2])
 def test_long_k_residual_gemm_split_in_two(n):
-    """down_proj with 256 K blocks (intermediate 16384) over 300 prefill tokens runs
-    on 256-wide CTA-pair tiles with its rank segments split in two halves that meet
-    in split-K partials; the residual it leaves against the oracle."""
-    s = synth.ModelShape(hidden=256, num_q_heads=4, num_kv_heads=2, head_dim=64, intermediate=16384, vocab=1000,
+    """down_proj with 256 K blocks (intermediate 16384) over 1280 prefill tokens
+    (20 pair tiles of 256 x 256) runs on CTA pairs with its rank segments split in
+    K parts that meet in split-K partials; the residual it leaves against the
+    oracle."""
+    s = synth.ModelShape(hidden=1024, num_q_heads=8, num_kv_heads=4, head_dim=128, intermediate=16384, vocab=1000,
                          num_layers=1)
-    w = synth.Workload("long_k_resid", s, (n,), ((300, 0),), (17,), 1, True)
+    w = synth.Workload("long_k_resid", s, (n,), ((1280, 0),), (17,), 1, True)
     g = GpuStep(w, n)
     check_step(g, [0, 1])
 
