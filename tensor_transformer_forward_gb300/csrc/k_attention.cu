@@ -562,9 +562,7 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
   const int k1 = bad ? k0 : k1n;
   const int ntiles = k1 > k0 ? (k1 - k0 + C::BK - 1) / C::BK : 0;
   const uint32_t tmem = *tmem_slot;
-  // q and the cache come from the QKV GEMM; dependents are released only after
-  // this wait (a prefill attention launched next relies on it: see AttnArgs)
-  griddep_wait();
+  griddep_wait();  // q and the cache come from the QKV GEMM
   griddep_launch();
   if (bad && threadIdx.x == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
 
@@ -976,51 +974,59 @@ __global__ void __launch_bounds__(320, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  // barriers: 0 q_full | 1,2 k_full | 3,4 k_empty | 5,6 s_full | 7,8 s_empty | 9 p_full | 10 o_done | 11 drain
-  //           | 12,13 v_full | 14,15 v_empty
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  // barriers: q_full | k_full[S] | k_empty[S] | v_full[S] | v_empty[S] | s_full[2] | p_full[2] | o_done |
+  //           drain | q_free | o_read
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9 + 4 * STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
 #define B_Q (bar0)
 #define B_KF(s) (bar0 + 8u * (1 + (s)))
-#define B_KE(s) (bar0 + 8u * (3 + (s)))
-#define B_VF(s) (bar0 + 8u * (12 + (s)))
-#define B_VE(s) (bar0 + 8u * (14 + (s)))
-#define B_SF(b) (bar0 + 8u * (5 + (b)))
-#define B_PF(b) (bar0 + 8u * (7 + (b)))
-#define B_OD (bar0 + 8u * 10)
-#define B_DR (bar0 + 8u * 11)
+#define B_KE(s) (bar0 + 8u * (1 + STAGES + (s)))
+#define B_VF(s) (bar0 + 8u * (1 + 2 * STAGES + (s)))
+#define B_VE(s) (bar0 + 8u * (1 + 3 * STAGES + (s)))
+#define B_SF(b) (bar0 + 8u * (1 + 4 * STAGES + (b)))
+#define B_PF(b) (bar0 + 8u * (3 + 4 * STAGES + (b)))
+#define B_OD (bar0 + 8u * (5 + 4 * STAGES))
+#define B_DR (bar0 + 8u * (6 + 4 * STAGES))
+#define B_QE (bar0 + 8u * (7 + 4 * STAGES))
+#define B_OE (bar0 + 8u * (8 + 4 * STAGES))
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // linear grid, heaviest work first: the q-block index (from the last) varies slowest
+  // Work items: (query block, sequence, rank, q head), heaviest first (the query
+  // block index from the last varies slowest); CTA c takes items c, c + grid, ...
+  // Every role walks the same items and skips the same ones.
   const int heads = a.n * a.nq_l;
   const int nseq = a.seq_end - a.seq_begin;
   const int qblocks = (a.max_q_len + C::BQ - 1) / C::BQ;
-  const int rest = blockIdx.x % (heads * nseq);
-  const int b = a.seq_begin + rest / heads;
-  const int hg = rest % heads;
-  const int qlen = a.cu_q[b + 1] - a.cu_q[b];
-  const int q0 = (qblocks - 1 - static_cast<int>(blockIdx.x) / (heads * nseq)) * C::BQ;
-  if (q0 >= qlen) return;                                // uniform: before any barrier or TMEM use
-  {
-    // every cache block of the sequence's keys [0, ctx + qlen) must be inside the
-    // cache (block table entries checked by the CTA's threads together); else flag, skip
-    const int c0 = a.ctx_len[b];
-    if (__syncthreads_or(c0 < 0 || kv_blocks_bad(a.kvm, b, 0, c0 + qlen, threadIdx.x, blockDim.x))) {
-      griddep_wait();
-      if (threadIdx.x == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
-      return;
-    }
-  }
-  const int r = hg / a.nq_l, h = hg % a.nq_l;
-  const int g = h / (a.nq_l / a.nkv_l);
-  const int ctx = a.ctx_len[b];
-  const int tbase = a.cu_q[b];
-  const int kend = ctx + min(q0 + C::BQ, qlen);          // keys this CTA needs: [0, kend)
-  const int nblk = (kend + C::BKV - 1) / C::BKV;
+  const int n_items = qblocks * heads * nseq;
+  struct Item {
+    int b, r, h, g, qlen, q0, ctx, tbase, nblk;
+    bool bad;
+  };
+  // false: no queries in this block; bad: a cache block of the sequence's keys
+  // [0, ctx + qlen) lies outside the cache (the item is skipped and flagged)
+  auto item_at = [&](int i, Item& x) -> bool {
+    const int rest = i % (heads * nseq);
+    x.b = a.seq_begin + rest / heads;
+    const int hg = rest % heads;
+    x.qlen = a.cu_q[x.b + 1] - a.cu_q[x.b];
+    x.q0 = (qblocks - 1 - i / (heads * nseq)) * C::BQ;
+    if (x.q0 >= x.qlen) return false;
+    x.r = hg / a.nq_l;
+    x.h = hg % a.nq_l;
+    x.g = x.h / (a.nq_l / a.nkv_l);
+    x.ctx = a.ctx_len[x.b];
+    x.tbase = a.cu_q[x.b];
+    x.bad = x.ctx < 0 || kv_blocks_bad(a.kvm, x.b, 0, x.ctx + x.qlen, 0, 1);
+    const int kend = x.ctx + min(x.q0 + C::BQ, x.qlen);  // keys the item needs: [0, kend)
+    x.nblk = (kend + C::BKV - 1) / C::BKV;
+    return true;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(B_Q, 1);
+    mbar_init(B_QE, 1);
+    mbar_init(B_OE, 8);  // one arrival per softmax warp once it has read the output
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(B_KF(s), 1);
       mbar_init(B_KE(s), 1);
@@ -1044,49 +1050,65 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // q and the cache come from the QKV GEMM; right after a decode attention launch
-  // of the same batch (which touches nothing of this launch's and released its
-  // dependents only after its own wait on the QKV GEMM) the wait on that launch
-  // moves to the end, so these CTAs start on the SMs its last wave leaves free
-  if (!a.overlap_prev) griddep_wait();
+  griddep_wait();  // q and the cache come from the QKV GEMM
   griddep_launch();
 
   if (warp == 0) {
     // ---------------- TMA producers: lane 0 streams Q then K, lane 1 streams V ----------------
+    // The K / V rings and the Q tile run on across the CTA's items (jb counts
+    // every key block the CTA has streamed, it every item).
     if (lane < 2) {
       const bool is_k = lane == 0;
       if (is_k) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmQlo);
         tma_prefetch_desc(&tmKV);
-        const int qcol = r * a.w_rank + h * HD;
-        const int qlo_col = (r * a.nq_l + h) * HD;
-        mbar_arrive_expect_tx(B_Q, 2 * C::TILE_BYTES);
-        for (int s = 0; s < C::NSUB; ++s) {
-          tma_load_2d(smem_u32(smem + C::Q_OFF + s * C::SUB_BYTES), &tmQ, B_Q, qcol + s * 64, tbase + q0);
-          tma_load_2d(smem_u32(smem + C::Q_OFF + C::TILE_BYTES + s * C::SUB_BYTES), &tmQlo, B_Q, qlo_col + s * 64,
-                      tbase + q0);
-        }
       }
       uint8_t* ring = smem + C::KV_OFF + (is_k ? 0 : STAGES * C::TILE_BYTES);
-      int issued = 0;
-      // block of the next key block, looked up one block ahead (its load overlaps the wait)
-      int blk_next = nblk > 0 ? kv_block_checked(a.kvm, b, 0) : 0;
-      for (int j = 0; j < nblk; ++j) {
-        const int st = j % STAGES;
-        const uint32_t full = is_k ? B_KF(st) : B_VF(st);
-        const uint32_t empty = is_k ? B_KE(st) : B_VE(st);
-        const int blk = blk_next;
-        if (j + 1 < nblk) blk_next = kv_block_checked(a.kvm, b, (j + 1) * C::BKV);
-        if (!mbar_wait(empty, ((j / STAGES) & 1) ^ 1u, abort_flag, a.status)) break;
-        mbar_arrive_expect_tx(full, C::TILE_BYTES);
-        const int row = static_cast<int>(kv_row(a.kvm, a.nkv_l, r, is_k ? 0 : 1, blk, g, (j * C::BKV) % a.kvm.block_len));
-        for (int s = 0; s < C::NSUB; ++s)
-          tma_load_2d(smem_u32(ring + st * C::TILE_BYTES + s * C::SUB_BYTES), &tmKV, full, s * 64, row);
-        issued = j + 1;
+      int jb = 0, it = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+        Item x;
+        if (!item_at(i, x)) continue;
+        if (x.bad) {
+          if (is_k) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
+          continue;
+        }
+        if (is_k) {
+          // this item's q once the previous item's score MMAs have read the last one
+          if (!mbar_wait(B_QE, (it & 1) ^ 1u, abort_flag, a.status)) break;
+          const int qcol = x.r * a.w_rank + x.h * HD;
+          const int qlo_col = (x.r * a.nq_l + x.h) * HD;
+          mbar_arrive_expect_tx(B_Q, 2 * C::TILE_BYTES);
+          for (int s = 0; s < C::NSUB; ++s) {
+            tma_load_2d(smem_u32(smem + C::Q_OFF + s * C::SUB_BYTES), &tmQ, B_Q, qcol + s * 64, x.tbase + x.q0);
+            tma_load_2d(smem_u32(smem + C::Q_OFF + C::TILE_BYTES + s * C::SUB_BYTES), &tmQlo, B_Q,
+                        qlo_col + s * 64, x.tbase + x.q0);
+          }
+        }
+        // block of the next key block, looked up one block ahead (its load overlaps the wait)
+        int blk_next = kv_block_checked(a.kvm, x.b, 0);
+        for (int j = 0; j < x.nblk; ++j, ++jb) {
+          const int st = jb % STAGES;
+          const uint32_t full = is_k ? B_KF(st) : B_VF(st);
+          const uint32_t empty = is_k ? B_KE(st) : B_VE(st);
+          const int blk = blk_next;
+          if (j + 1 < x.nblk) blk_next = kv_block_checked(a.kvm, x.b, (j + 1) * C::BKV);
+          if (!mbar_wait(empty, ((jb / STAGES) & 1) ^ 1u, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full, C::TILE_BYTES);
+          const int row = static_cast<int>(
+              kv_row(a.kvm, a.nkv_l, x.r, is_k ? 0 : 1, blk, x.g, (j * C::BKV) % a.kvm.block_len));
+          for (int s = 0; s < C::NSUB; ++s)
+            tma_load_2d(smem_u32(ring + st * C::TILE_BYTES + s * C::SUB_BYTES), &tmKV, full, s * 64, row);
+        }
+        ++it;
       }
-      if (is_k) mbar_wait(B_Q, 0, nullptr, a.status);
-      for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j)
+      // every load issued has landed before the CTA may exit
+      if (is_k && it > 0) mbar_wait(B_Q, (it - 1) & 1, nullptr, a.status);
+      for (int j = (jb > STAGES ? jb - STAGES : 0); j < jb; ++j)
         mbar_wait(is_k ? B_KF(j % STAGES) : B_VF(j % STAGES), (j / STAGES) & 1, nullptr, a.status);
     }
   } else if (warp == 1) {
@@ -1094,12 +1116,23 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, C::BKV);      // S = Q K^T: both K-major
       const uint32_t id_o = idesc_bf16_f32(128, HD, true);    // O += P V: V MN-major
-      bool ok = mbar_wait(B_Q, 0, abort_flag, a.status);
+      bool ok = true;
+      int jb = 0, it = 0, drains = 0;
+      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+      Item x;
+      if (!item_at(i, x) || x.bad) continue;
+      const int nblk = x.nblk;
+      const int jb0 = jb;
+      ok = mbar_wait(B_Q, it & 1, abort_flag, a.status);
       tc_fence_after();
-      auto pv = [&](int j) -> bool {  // O += P(j) V(j), P(j) from TMEM (score buffer j & 1)
-        const int st = j % STAGES, sb = j & 1;
-        if (!mbar_wait(B_PF(sb), (j >> 1) & 1, abort_flag, a.status)) return false;
-        if (!mbar_wait(B_VF(st), (j / STAGES) & 1, abort_flag, a.status)) return false;
+      // O += P(j) V(j), P(j) from TMEM (score buffer of the CTA's key block jb0 + j);
+      // the first one overwrites O, so it waits until the previous item's output was read
+      auto pv = [&](int j) -> bool {
+        const int gj = jb0 + j;
+        const int st = gj % STAGES, sb = gj & 1;
+        if (j == 0 && !mbar_wait(B_OE, (it & 1) ^ 1u, abort_flag, a.status)) return false;
+        if (!mbar_wait(B_PF(sb), (gj >> 1) & 1, abort_flag, a.status)) return false;
+        if (!mbar_wait(B_VF(st), (gj / STAGES) & 1, abort_flag, a.status)) return false;
         tc_fence_after();
         const uint32_t vt = smem_u32(smem + C::KV_OFF + (STAGES + st) * C::TILE_BYTES);
         const uint32_t pa = tmem + C::S_COL + sb * 128;
@@ -1113,9 +1146,10 @@ __global__ void __launch_bounds__(320, 1)
         return true;
       };
       for (int j = 0; ok && j < nblk; ++j) {
-        const int st = j % STAGES, sb = j & 1;
-        // score buffer sb last held P(j-2), whose PV MMA was issued before this point
-        if (!mbar_wait(B_KF(st), (j / STAGES) & 1, abort_flag, a.status)) { ok = false; break; }
+        const int gj = jb0 + j;
+        const int st = gj % STAGES, sb = gj & 1;
+        // score buffer sb last held P(gj-2), whose PV MMA was issued before this point
+        if (!mbar_wait(B_KF(st), (gj / STAGES) & 1, abort_flag, a.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t qt = smem_u32(smem + C::Q_OFF);
         const uint32_t kt = smem_u32(smem + C::KV_OFF + st * C::TILE_BYTES);
@@ -1129,12 +1163,17 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
         tc_commit(B_SF(sb));
-        tc_commit(B_KE(st));  // the K stage is free once S(j) is done
+        tc_commit(B_KE(st));                 // the K stage is free once S(j) is done
+        if (j == nblk - 1) tc_commit(B_QE);  // and the Q tile once the item's last S is
         if (j > 0 && !pv(j - 1)) { ok = false; break; }
       }
-      if (ok) pv(nblk - 1);
-      tc_commit(B_DR);  // completes after every MMA above
-      mbar_wait(B_DR, 0, nullptr, a.status);
+      if (ok && !pv(nblk - 1)) ok = false;
+      tc_commit(B_DR);  // the item's output: completes after every MMA above
+      ++drains;
+      jb = jb0 + nblk;
+      ++it;
+      }
+      if (drains > 0) mbar_wait(B_DR, (drains - 1) & 1, nullptr, a.status);  // every MMA has completed
     }
   } else {
     // ---------------- softmax / output (warps 2..9) ----------------
@@ -1145,16 +1184,22 @@ __global__ void __launch_bounds__(320, 1)
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = q * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    constexpr int OH = HD / 2;                  // output dims per half
+    bool ok = true;
+    int jb = 0, it = 0;
+    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+    Item x;
+    if (!item_at(i, x) || x.bad) continue;
+    const int nblk = x.nblk, q0 = x.q0, qlen = x.qlen, ctx = x.ctx, tbase = x.tbase, r = x.r, h = x.h;
     const int qi = q0 + row;                    // query index within the sequence
     const bool row_ok = qi < qlen;
     const int last_key = ctx + qi;              // keys <= last_key are visible
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    constexpr int OH = HD / 2;                  // output dims per half
     float m_used = -INFINITY, l = 0.0f;
-    bool ok = true;
     for (int j = 0; j < nblk; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(B_SF(sb), (j >> 1) & 1, abort_flag, a.status)) ok = false;
+      const int gj = jb + j;
+      const int sb = gj & 1;
+      if (!mbar_wait(B_SF(sb), (gj >> 1) & 1, abort_flag, a.status)) ok = false;
       if (!named_bar_and(1, 256, ok)) { ok = false; break; }
       tc_fence_after();
       float sv[64];
@@ -1185,11 +1230,11 @@ __global__ void __launch_bounds__(320, 1)
       mx *= a.scale_log2;  // the scale is positive: max of the scaled scores
       // row max over both halves (TMEM columns 384 + 2 * (j & 1) + half); past this
       // barrier both halves have read their scores, so P may overwrite them
-      tc_st1(lane_addr + 384 + 2 * (j & 1) + half, mx);
+      tc_st1(lane_addr + 384 + 2 * (gj & 1) + half, mx);
       tc_fence_before();
       named_bar_sync(1, 256);
       tc_fence_after();
-      mx = fmaxf(mx, tc_ld1(lane_addr + 384 + 2 * (j & 1) + (half ^ 1)));
+      mx = fmaxf(mx, tc_ld1(lane_addr + 384 + 2 * (gj & 1) + (half ^ 1)));
       const bool rescale = mx > m_used + 8.0f;
       const float m_new = rescale ? mx : m_used;
       const float mb = m_new == -INFINITY ? 0.0f : m_new;
@@ -1225,7 +1270,7 @@ __global__ void __launch_bounds__(320, 1)
       // factor of 1.
       const bool touch_o = rescale && j > 0 && m_used != -INFINITY;
       const bool warp_touch = __any_sync(0xffffffffu, touch_o);
-      if (warp_touch && !warp_all(mbar_wait(B_OD, (j - 1) & 1, abort_flag, a.status))) ok = false;
+      if (warp_touch && !warp_all(mbar_wait(B_OD, (gj - 1) & 1, abort_flag, a.status))) ok = false;
       if (!ok) continue;  // warp-uniform here
       if (warp_touch) {
         tc_fence_after();
@@ -1247,8 +1292,8 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(B_PF(sb));
     }
-    // the MMA thread commits the drain barrier after the last PV
-    if (ok) ok = mbar_wait(B_DR, 0, abort_flag, a.status);
+    // the MMA thread commits the drain barrier after the item's last PV
+    if (ok) ok = mbar_wait(B_DR, it & 1, abort_flag, a.status);
     if (named_bar_and(1, 256, ok)) {
       tc_fence_after();
       // row sum over both halves (TMEM columns 388 + half)
@@ -1278,8 +1323,19 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       report_sat(a.status, sat);
+    } else {
+      ok = false;
+    }
+    // O has been read: the next item's first PV may overwrite it
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(B_OE);
+    jb += nblk;
+    ++it;
     }
   }
+#undef B_QE
+#undef B_OE
 #undef B_Q
 #undef B_KF
 #undef B_KE
@@ -1289,7 +1345,6 @@ __global__ void __launch_bounds__(320, 1)
 #undef B_PF
 #undef B_OD
 #undef B_DR
-  if (a.overlap_prev) griddep_wait();  // this grid ends after the decode launch it overlapped
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -1314,8 +1369,12 @@ static cudaError_t launch_prefill_hd(const AttnArgs& a, cudaStream_t s) {
     const cudaError_t e = smem_attr_per_device(attr, attn_prefill_tc_kernel<HD>, C::SMEM);
     if (e != cudaSuccess) return e;
   }
-  const unsigned grid = static_cast<unsigned>((a.max_q_len + C::BQ - 1) / C::BQ) * a.n * a.nq_l * (a.seq_end - a.seq_begin);
-  return launch_pdl(attn_prefill_tc_kernel<HD>, dim3(grid), dim3(320), C::SMEM, s, mq, mqlo, mkv, a);
+  // persistent: a.ctas CTAs walk the items (one per SM at most, fewer while a decode
+  // attention launch shares the GPU)
+  const int items = (a.max_q_len + C::BQ - 1) / C::BQ * a.n * a.nq_l * (a.seq_end - a.seq_begin);
+  const int ctas = a.ctas < items ? a.ctas : items;
+  if (ctas < 1) return cudaErrorInvalidValue;
+  return launch_pdl(attn_prefill_tc_kernel<HD>, dim3(ctas), dim3(320), C::SMEM, s, mq, mqlo, mkv, a);
 }
 
 cudaError_t launch_attention_prefill(const AttnArgs& a, cudaStream_t s) {

@@ -271,14 +271,7 @@ struct AttnArgs {
   int splits;                // key splits per (sequence, rank, kv head) unit
   int tail_units;            // decode: the last tail_units units take tail_splits splits instead
   int tail_splits;
-  // prefill attention launched right after the decode attention launch of the same
-  // batch: the two touch disjoint data and both depend only on the QKV GEMM, which
-  // has completed once the prefill launch starts (every decode CTA releases its
-  // dependents only after its own wait on the QKV GEMM).  The prefill CTAs then
-  // start on the SMs the decode launch's last wave leaves free, and wait on the
-  // decode launch only before they exit, so a later kernel's wait on the prefill
-  // launch still covers both.
-  int overlap_prev;
+  int ctas;                  // prefill: CTAs of the persistent launch (each walks work items)
   int* status;
 };
 cudaError_t launch_attention_prefill(const AttnArgs& a, cudaStream_t s);
