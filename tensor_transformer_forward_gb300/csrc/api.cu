@@ -176,7 +176,7 @@ WsPlan plan_ws(const tp_ctx* x, int64_t T, int64_t B, int64_t P) {
   take(w.gcnt, kGemmCounters * 4);
   const int64_t splits = std::min<int64_t>(kMaxDecodeSplits, std::max<int64_t>(1, (P + 255) / 256));
   take(w.apart, static_cast<size_t>(B) * n * x->nq_l * (x->hd + 2) * splits * 4);
-  take(w.acnt, static_cast<size_t>(B) * n * x->nkv_l * 4);
+  take(w.acnt, (static_cast<size_t>(B) * n * x->nkv_l + 2) * 4);  // split counters, then the decode tickets
   w.lm_tiles = static_cast<int>(div_ceil64(n * x->v_l, 64));
   take(w.amax_v, static_cast<size_t>(w.lm_tiles) * B * 4);
   take(w.amax_i, static_cast<size_t>(w.lm_tiles) * B * 4);
@@ -650,6 +650,7 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   aa.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(x->hd)));
   aa.part = reinterpret_cast<float*>(x->ws + x->r_apart.off);
   aa.counters = reinterpret_cast<int*>(x->ws + x->r_acnt.off);
+  aa.sched = aa.counters + static_cast<size_t>(x->ws_seqs) * n * x->nkv_l;
   aa.status = dev_status;
   // A mixed batch runs its two attention kernels side by side: the prefill
   // attention (tensor cores, a few persistent CTAs) on a second, higher-priority
@@ -658,6 +659,7 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   const bool has_decode = b->num_prefill < b->num_seqs;
   const bool side_by_side = b->num_prefill > 0 && has_decode;
   cudaStream_t ps = s;
+  const int pre_ctas = std::max(8, x->num_sms / 4);  // the prefill attention's CTAs beside the decode
   if (side_by_side) {
     if (!x->side) {
       int least = 0, greatest = 0;
@@ -676,7 +678,7 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
     // on the 28-layer mixed step: 16 / 24 / 30 / 38 / 48 / 76 CTAs gave 8.06 / 8.10 /
     // 7.96 / 7.89 / 8.05 / 8.00 ms); alone, one CTA per item, which the hardware
     // hands to SMs as they free up (heaviest items first)
-    aa.ctas = side_by_side ? std::max(8, x->num_sms / 4) : INT_MAX;
+    aa.ctas = side_by_side ? pre_ctas : INT_MAX;
     Timed tm(x, TP_K_ATTN_PREFILL, ps);
     e = tpk::launch_attention_prefill(aa, ps);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -690,9 +692,28 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
     const tpk::DecodeSplit ds =
         tpk::decode_split_plan(b->max_kv_len, units, x->num_sms, x->hd, x->nq_l / x->nkv_l, std::max(1, max_splits));
     aa.splits = ds.splits; aa.tail_units = ds.tail_units; aa.tail_splits = ds.tail_splits;
-    Timed tm(x, TP_K_ATTN_DECODE, s);
-    e = tpk::launch_attention_decode(aa, s);
-    if (e != cudaSuccess) return cuda_fail(e);
+    // the persistent decode kernel: one CTA per SM (two pipelines each) drawing
+    // items from a ticket counter.  Beside a prefill attention it leaves that
+    // kernel's SMs free, and a second launch on the prefill's stream takes them
+    // over once the prefill ends, drawing from the same counter.
+    const int items = (units - ds.tail_units) * ds.splits + ds.tail_units * ds.tail_splits;
+    const int want = std::max(1, std::min(x->num_sms, (items + 1) / 2));
+    const bool persistent = x->hd == 128;  // the tensor-core kernel (64-dim heads: a CTA per item)
+    const int side_ctas =
+        side_by_side && persistent ? std::min(pre_ctas, std::max(0, want - (x->num_sms - pre_ctas))) : 0;
+    aa.ctas = want - side_ctas;
+    aa.sched_ctas = want;
+    {
+      Timed tm(x, TP_K_ATTN_DECODE, s);
+      e = tpk::launch_attention_decode(aa, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (side_ctas > 0) {
+      aa.ctas = side_ctas;
+      x->launches += 1;  // counted, not timed: it runs inside the timed launch above
+      e = tpk::launch_attention_decode(aa, ps);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
   }
   if (side_by_side) {
     TP_CUDA(cudaEventRecord(x->join_ev, x->side));

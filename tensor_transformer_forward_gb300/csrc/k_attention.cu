@@ -368,7 +368,7 @@ static cudaError_t prepare_decode(int* ctas_per_sm) {
 }
 
 template <int HD, int G>
-static cudaError_t launch_decode_tc_hd(const AttnArgs& a, dim3 grid, cudaStream_t s);
+static cudaError_t launch_decode_tc_hd(const AttnArgs& a, cudaStream_t s);
 static cudaError_t decode_tc_ctas_per_sm(int G, int* per_sm);
 
 // Key splits per (sequence, rank, kv head).  CUDA-core kernel (64-dim heads): the
@@ -449,9 +449,10 @@ cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s) {
   const int units = seqs * a.n * a.nkv_l;
   if (a.splits < 1 || a.tail_units < 0 || a.tail_units > units || (a.tail_units > 0 && a.tail_splits < 1))
     return cudaErrorInvalidValue;
-  dim3 grid((units - a.tail_units) * a.splits + a.tail_units * (a.tail_units > 0 ? a.tail_splits : 0));
+  const int items = (units - a.tail_units) * a.splits + a.tail_units * (a.tail_units > 0 ? a.tail_splits : 0);
+  dim3 grid(items);
 #define TP_DEC_TC(HD_, G_) \
-  if (a.hd == HD_ && G == G_) return launch_decode_tc_hd<HD_, G_>(a, grid, s);
+  if (a.hd == HD_ && G == G_) return launch_decode_tc_hd<HD_, G_>(a, s);
 #define TP_DEC(HD_, G_) \
   if (a.hd == HD_ && G == G_) return launch_decode_hd<HD_, G_>(a, grid, s);
   TP_DEC_TC(128, 1) TP_DEC_TC(128, 2) TP_DEC_TC(128, 4) TP_DEC_TC(128, 8)
@@ -462,10 +463,25 @@ cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------
-// Decode on the tensor cores.  One CTA = (sequence, rank, local kv head, key
-// split), 192 threads: warp 0 streams 128-key K and V tiles of the split with TMA
-// (one stage each; two CTAs per SM overlap each other's loads), warp 1 allocates
-// TMEM and issues the MMAs, warps 2-5 run the softmax with one thread per key.
+// Decode on the tensor cores, persistent.  Work items are the (sequence, rank,
+// local kv head, key split) pieces of dec_cta, handed out in order from a ticket
+// counter; each CTA keeps drawing items until none are left, and its K / V
+// streams, MMAs and softmax run on from one item into the next without draining
+// (a CTA per item left every SM idle while one pair of CTAs ended and the next
+// started, and a last partial wave of items ran on part of the GPU).  256
+// threads, two CTAs per SM:
+//   warp 0    scheduler: draws the next ticket once the current item's last K
+//             tile is issued, checks the item's cache blocks, publishes it in a
+//             4-entry item ring, and writes its query rows into one of two Q
+//             buffers (bf16 high and low parts, the MMA's B operand)
+//   warp 1    TMEM allocation + one MMA-issuing thread
+//   warps 2-5 softmax, one thread per key of a 128-key tile; at the end of an
+//             item, O (one TMEM row per output dim) into a staging buffer
+//   warp 6    lane 0 streams K tiles, lane 1 V tiles (one stage each; the two
+//             CTAs of an SM overlap each other's loads)
+//   warp 7    writer: the staged output as fp16, or a split's partial and, for
+//             the last split of a unit to arrive, the merge of its splits in
+//             split order (so the softmax never waits on global memory)
 //   S^T = K Q^T   M = 128 keys, N = 16, K = head_dim: the B operand holds the
 //                 G query heads of the kv group as bf16 high parts (rows 0..G-1)
 //                 and bf16 low parts (rows G..2G-1), so S = S_hi + S_lo carries q
@@ -475,7 +491,10 @@ cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s) {
 //                 high parts (rows 0..G-1) and low parts (rows G..2G-1), summed
 //                 at the end, so P also keeps ~16 significant bits
 // S^T and P^T are double-buffered; the output is rescaled only when a head's
-// running max grows by more than 2^8.  Splits combine as in the kernel above.
+// running max grows by more than 2^8.  Ring phases count tiles and items over
+// the whole launch, so every role sees the same sequence of phases.  The result
+// does not depend on which CTA takes an item: an item's arithmetic is fixed, and
+// splits merge in split order.
 // ---------------------------------------------------------------------------
 template <int HD>
 struct DtcCfg {
@@ -486,317 +505,518 @@ struct DtcCfg {
   static constexpr int QSUB = 16 * 128;            // [16 rows][64 dims] bf16
   static constexpr int QT_BYTES = NSUB * QSUB;
   static constexpr int PT_BYTES = 2 * QSUB;        // [16 heads][128 keys] bf16 (two 64-key sub-tiles)
+  static constexpr int ST_BYTES = (8 * (HD + 2) * 4 + 15) / 16 * 16;  // staged output of up to 8 heads
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + KT_BYTES;
-  static constexpr int Q_OFF = V_OFF + KT_BYTES;
-  static constexpr int P_OFF = Q_OFF + QT_BYTES;   // two P^T buffers
+  static constexpr int Q_OFF = V_OFF + KT_BYTES;   // two Q^T buffers
+  static constexpr int P_OFF = Q_OFF + 2 * QT_BYTES;   // two P^T buffers
   static constexpr int RED_OFF = P_OFF + 2 * PT_BYTES;  // max then sum: [2][4 warps][8 heads] fp32 each
-  static constexpr int BAR_OFF = RED_OFF + 512;
-  static constexpr int SMEM = 1024 + BAR_OFF + 128;
-  static constexpr int S_COL = 0, O_COL = 32, TMEM_COLS = 64;
+  static constexpr int ST_OFF = RED_OFF + 512;     // two staging buffers
+  static constexpr int RING_OFF = ST_OFF + 2 * ST_BYTES;  // item ring: 4 x 32 bytes
+  static constexpr int BAR_OFF = RING_OFF + 128;
+  static constexpr int NBARS = 29;
+  static constexpr int PIPE_BYTES = (BAR_OFF + NBARS * 8 + 16 + 1023) / 1024 * 1024;  // one pipeline's share
+  static constexpr int SMEM = 1024 + 2 * PIPE_BYTES;
+  static constexpr int S_COL = 0, O_COL = 32, PIPE_COLS = 64, TMEM_COLS = 128;
+  static constexpr int THREADS = 512;  // two pipelines of 8 warps
+};
+
+// An item of the decode ring: its unit and split, the split's keys [k0, k1) and
+// tile count (k1 = k0 when its cache blocks failed the check), its sequence and
+// the token row of its query.
+struct DecItem {
+  int unit, split, nsplit, k0, k1, ntiles, b, t;
 };
 
 template <int HD, int G>
-__global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
-                                                             const __grid_constant__ CUtensorMap tmKV16,
-                                                             const AttnArgs a) {
+__global__ void __launch_bounds__(512, 1) attn_decode_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
+                                                                const __grid_constant__ CUtensorMap tmKV16,
+                                                                const AttnArgs a) {
   using C = DtcCfg<HD>;
   static_assert(2 * G <= 16, "hi and lo rows of the kv group fit N = 16");
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem0 = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int pipe = threadIdx.x >> 8;  // warps 0-7 pipeline 0, warps 8-15 pipeline 1
+  uint8_t* smem = smem0 + pipe * C::PIPE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  // barriers: 0 q_ready | 1 k_full | 2 k_empty | 3 v_full | 4 v_empty | 5,6 s_full | 7,8 p_full | 9 o_done | 10 drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  // barriers: 0-3 item full | 4-7 item empty | 8,9 q full | 10,11 q empty | 12 k full | 13 k empty |
+  // 14 v full | 15 v empty | 16,17 s full | 18,19 p full | 20 pv done | 21 item's o done |
+  // 22,23 staging full | 24,25 staging empty | 26 next-item request | 27 drain | 28 item's o read
+  // the TMEM address and the abort flag live in pipeline 0's share (one per CTA)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(reinterpret_cast<uint64_t*>(smem0 + C::BAR_OFF) + C::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
   float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
+  uint8_t* ring = smem + C::RING_OFF;
   const uint32_t bar0 = smem_u32(bars);
-#define D_QR (bar0)
-#define D_KF (bar0 + 8u * 1)
-#define D_KE (bar0 + 8u * 2)
-#define D_VF (bar0 + 8u * 3)
-#define D_VE (bar0 + 8u * 4)
-#define D_SF(b) (bar0 + 8u * (5 + (b)))
-#define D_PF(b) (bar0 + 8u * (7 + (b)))
-#define D_OD (bar0 + 8u * 9)
-#define D_DR (bar0 + 8u * 10)
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#define D_IF(s) (bar0 + 8u * (s))
+#define D_IE(s) (bar0 + 8u * (4 + (s)))
+#define D_QF(b) (bar0 + 8u * (8 + (b)))
+#define D_QE(b) (bar0 + 8u * (10 + (b)))
+#define D_KF (bar0 + 8u * 12)
+#define D_KE (bar0 + 8u * 13)
+#define D_VF (bar0 + 8u * 14)
+#define D_VE (bar0 + 8u * 15)
+#define D_SF(b) (bar0 + 8u * (16 + (b)))
+#define D_PF(b) (bar0 + 8u * (18 + (b)))
+#define D_OD (bar0 + 8u * 20)
+#define D_OF (bar0 + 8u * 21)
+#define D_STF(b) (bar0 + 8u * (22 + (b)))
+#define D_STE(b) (bar0 + 8u * (24 + (b)))
+#define D_NREQ (bar0 + 8u * 26)
+#define D_DR (bar0 + 8u * 27)
+#define D_OE (bar0 + 8u * 28)
+  const int warp = (threadIdx.x >> 5) & 7, lane = threadIdx.x & 31;  // warp within the pipeline
   const int per_seq = a.n * a.nkv_l;
-  const DecCta cta = dec_cta(a, blockIdx.x);
-  const int unit = cta.unit, split = cta.split, nsplit = cta.nsplit, pstride = dec_part_stride(a);
-  const int b = a.seq_begin + unit / per_seq;
-  const int r = (unit % per_seq) / a.nkv_l;
-  const int g = unit % a.nkv_l;
-  const int t = a.cu_q[b];
-  const int L = a.ctx_len[b] + 1;
-  // splits start on kKeyAlign-key boundaries (a page holds whole key tiles)
-  const int chunk = ((L + nsplit - 1) / nsplit + kKeyAlign - 1) / kKeyAlign * kKeyAlign;
-  const int k0 = split * chunk;
-  const int k1n = min(L, k0 + chunk);
-  // a split whose keys lie (partly) outside the cache reads nothing and flags the batch
-  const bool bad_mine = L < 1 || kv_blocks_bad(a.kvm, b, k0, k1n, threadIdx.x, blockDim.x);
+  const int units = (a.seq_end - a.seq_begin) * per_seq;
+  const int items = (units - a.tail_units) * a.splits + (a.tail_units > 0 ? a.tail_units * a.tail_splits : 0);
+  const int pstride = dec_part_stride(a);
 
-  if (threadIdx.x == 0) {
-    mbar_init(D_QR, 128);
+  if ((threadIdx.x & 255) == 0) {
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(D_IF(i), 1);
+      mbar_init(D_IE(i), 8);  // MMA, 4 softmax warps, K lane, V lane, writer
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(D_QF(i), 32);
+      mbar_init(D_QE(i), 1);
+      mbar_init(D_SF(i), 1);
+      mbar_init(D_PF(i), 4);
+      mbar_init(D_STF(i), 128);
+      mbar_init(D_STE(i), 32);
+    }
     mbar_init(D_KF, 1);
     mbar_init(D_KE, 1);
     mbar_init(D_VF, 1);
     mbar_init(D_VE, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(D_SF(i), 1);
-      mbar_init(D_PF(i), 4);
-    }
     mbar_init(D_OD, 1);
+    mbar_init(D_OF, 1);
+    mbar_init(D_NREQ, 1);
     mbar_init(D_DR, 1);
-    *abort_flag = 0;
-    *last_flag = 0;
+    mbar_init(D_OE, 4);
+    if (pipe == 0) *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (threadIdx.x >> 5 == 1) {  // both pipelines' columns, 64 each
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
+  // Zero the V tile and both Q^T buffers: rows 2G..15 of Q^T stay zero, and a
+  // first item of one short tile leaves V rows 16..127 unwritten (their P is 0,
+  // and 0 * NaN would not vanish); later short tiles find an earlier tile's rows
+  // there, which are finite cache values.
+  for (int i = threadIdx.x & 255; i < (C::KT_BYTES + 2 * C::QT_BYTES) / 16; i += 256)
+    *reinterpret_cast<uint4*>(smem + C::V_OFF + i * 16) = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   tc_fence_before();
-  const bool bad = __syncthreads_or(bad_mine);
+  __syncthreads();
   tc_fence_after();
-  const int k1 = bad ? k0 : k1n;
-  const int ntiles = k1 > k0 ? (k1 - k0 + C::BK - 1) / C::BK : 0;
-  const uint32_t tmem = *tmem_slot;
-  griddep_wait();  // q and the cache come from the QKV GEMM
-  griddep_launch();
-  if (bad && threadIdx.x == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
-
-  float m[G], l[G];  // running max (exp2 domain) and sum per head: the same in every softmax thread
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.0f;
-  }
+  const uint32_t tmem = *tmem_slot + pipe * C::PIPE_COLS;
+  const int nbar = 1 + pipe;  // the pipeline's named barrier for its softmax warps
 
   if (warp == 0) {
-    // ---------------- TMA: lane 0 streams K tiles, lane 1 V tiles ----------------
-    if (lane < 2) {
-      const bool is_k = lane == 0;
-      if (is_k) tma_prefetch_desc(&tmKV);
-      const uint32_t full = is_k ? D_KF : D_VF, empty = is_k ? D_KE : D_VE;
-      uint8_t* dst = smem + (is_k ? C::K_OFF : C::V_OFF);
-      int issued = 0;
-      // block of the next tile, looked up one tile ahead (its load overlaps the wait)
-      int blk_next = ntiles > 0 ? kv_block_checked(a.kvm, b, k0) : 0;
-      for (int j = 0; j < ntiles; ++j) {
-        const int key = k0 + j * C::BK;
-        const int blk = blk_next;
-        if (j + 1 < ntiles) blk_next = kv_block_checked(a.kvm, b, key + C::BK);
-        if (!mbar_wait(empty, (j & 1) ^ 1u, abort_flag, a.status)) break;
-        // a last tile of at most 16 keys loads 16 rows (the typical ctx + 1 tail)
-        const bool short_tail = j == ntiles - 1 && k1 - key <= 16;
-        mbar_arrive_expect_tx(full, short_tail ? C::KT_BYTES / 8 : C::KT_BYTES);
-        const int row = static_cast<int>(kv_row(a.kvm, a.nkv_l, r, is_k ? 0 : 1, blk, g, key % a.kvm.block_len));
-        for (int sub = 0; sub < C::NSUB; ++sub)
-          tma_load_2d(smem_u32(dst + sub * C::SUB_BYTES), short_tail ? &tmKV16 : &tmKV, full, sub * 64, row);
-        issued = j + 1;
+    // ---------------- scheduler: items, cache checks, query rows ----------------
+    // The first item is drawn and checked before the dependency wait (the batch
+    // tables do not come from the QKV GEMM); its query rows only after it.
+    int tk = 0;
+    if (lane == 0) tk = atomicAdd(a.sched, 1);
+    tk = __shfl_sync(0xffffffffu, tk, 0);
+    bool waited = false;
+    for (int it = 0;; ++it) {
+      DecItem e{-1, 0, 1, 0, 0, 0, 0, 0};
+      bool bad_l = false;
+      if (tk < items) {
+        const DecCta c = dec_cta(a, tk);
+        e.unit = c.unit;
+        e.split = c.split;
+        e.nsplit = c.nsplit;
+        e.b = a.seq_begin + c.unit / per_seq;
+        e.t = a.cu_q[e.b];
+        const int L = a.ctx_len[e.b] + 1;
+        // splits start on kKeyAlign-key boundaries (a page holds whole key tiles)
+        const int chunk = ((L + e.nsplit - 1) / e.nsplit + kKeyAlign - 1) / kKeyAlign * kKeyAlign;
+        e.k0 = e.split * chunk;
+        e.k1 = min(L, e.k0 + chunk);
+        // a split whose keys lie (partly) outside the cache reads nothing and flags the batch
+        bad_l = L < 1 || kv_blocks_bad(a.kvm, e.b, e.k0, e.k1, lane, 32);
       }
-      if (issued > 0) mbar_wait(full, (issued - 1) & 1, nullptr, a.status);  // the last tile has landed
+      const bool bad = __any_sync(0xffffffffu, bad_l);
+      if (bad || e.k1 < e.k0) e.k1 = e.k0;
+      e.ntiles = (e.k1 - e.k0 + C::BK - 1) / C::BK;
+      const int slot = it & 3;
+      if (it >= 4 && !warp_all(mbar_wait(D_IE(slot), ((it >> 2) - 1) & 1, abort_flag, a.status))) break;
+      if (lane == 0) {
+        *reinterpret_cast<DecItem*>(ring + slot * 32) = e;
+        mbar_arrive(D_IF(slot));
+      }
+      if (!waited) {
+        griddep_wait();  // q and the cache come from the QKV GEMM
+        griddep_launch();
+        waited = true;
+      }
+      if (bad && lane == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
+      if (e.unit < 0) break;
+      // query rows of the item into Q^T buffer it & 1, once the S MMAs of its
+      // previous user (item it - 2) are done: rows 0..G-1 = bf16(q_h), rows
+      // G..2G-1 = bf16(q_h - bf16(q_h)); 16-byte chunks in the 128-byte-swizzled
+      // K-major layout of the MMA's B operand
+      const int qb = it & 1;
+      if (it >= 2 && !warp_all(mbar_wait(D_QE(qb), ((it >> 1) - 1) & 1, abort_flag, a.status))) break;
+      {
+        const int r = (e.unit % per_seq) / a.nkv_l, g = e.unit % a.nkv_l;
+        const __half* qrow = reinterpret_cast<const __half*>(a.qkv) + static_cast<size_t>(e.t) * a.n * a.w_rank +
+                             static_cast<size_t>(r) * a.w_rank + static_cast<size_t>(g) * G * HD;
+        uint8_t* qt = smem + C::Q_OFF + qb * C::QT_BYTES;
+        for (int i = lane; i < 2 * G * (HD / 8); i += 32) {
+          const int rr = i / (HD / 8), c = i % (HD / 8);  // row, 8-dim chunk
+          const int h = rr < G ? rr : rr - G;
+          const uint4 u = __ldcg(reinterpret_cast<const uint4*>(qrow + h * HD + c * 8));
+          const float x[8] = {f16lo(u.x), f16hi(u.x), f16lo(u.y), f16hi(u.y),
+                              f16lo(u.z), f16hi(u.z), f16lo(u.w), f16hi(u.w)};
+          float y[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) y[k] = rr < G ? x[k] : x[k] - bf2f(f2bf(x[k]));
+          uint4 w;
+          w.x = pack_bf16x2(y[0], y[1]); w.y = pack_bf16x2(y[2], y[3]);
+          w.z = pack_bf16x2(y[4], y[5]); w.w = pack_bf16x2(y[6], y[7]);
+          *reinterpret_cast<uint4*>(qt + (c >> 3) * C::QSUB + rr * 128 + (((c & 7) ^ (rr & 7)) << 4)) = w;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(D_QF(qb));
+      }
+      // the next ticket a few K tiles before the item's K stream ends: late enough
+      // that the items left go to whichever pipelines free up first, early enough
+      // that the next item's first K tile follows the last one without a gap
+      if (!warp_all(mbar_wait(D_NREQ, it & 1, abort_flag, a.status))) break;
+      if (lane == 0) tk = atomicAdd(a.sched, 1);
+      tk = __shfl_sync(0xffffffffu, tk, 0);
+    }
+    if (!waited) {
+      griddep_wait();
+      griddep_launch();
     }
   } else if (warp == 1) {
+    griddep_wait();
+    griddep_launch();
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, 16);                 // K (K-major) x Q^T (K-major)
       const uint32_t id_o = idesc_bf16_f32(128, 16, false, true);    // V^T (MN-major) x P^T (K-major)
-      bool ok = mbar_wait(D_QR, 0, abort_flag, a.status);
-      tc_fence_after();
-      const uint32_t qt = smem_u32(smem + C::Q_OFF), kt = smem_u32(smem + C::K_OFF), vt = smem_u32(smem + C::V_OFF);
-      auto pv = [&](int j) -> bool {  // O^T += V(j)^T P(j)^T
-        const int pb = j & 1;
-        if (!mbar_wait(D_PF(pb), (j >> 1) & 1, abort_flag, a.status)) return false;
-        if (!mbar_wait(D_VF, j & 1, abort_flag, a.status)) return false;
+      const uint32_t kt = smem_u32(smem + C::K_OFF), vt = smem_u32(smem + C::V_OFF);
+      auto pv = [&](int g, bool first) -> bool {  // O^T (+)= V(g)^T P(g)^T, g counting tiles over the launch
+        const int pb = g & 1;
+        if (!mbar_wait(D_PF(pb), (g >> 1) & 1, abort_flag, a.status)) return false;
+        if (!mbar_wait(D_VF, g & 1, abort_flag, a.status)) return false;
         tc_fence_after();
         const uint32_t pt = smem_u32(smem + C::P_OFF + pb * C::PT_BYTES);
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk) {
           const uint64_t ad = sdesc_mn_sw128(vt + kk * 16 * 128, C::SUB_BYTES, 1024);
           const uint64_t bd = sdesc_k_sw128(pt + (kk >> 2) * C::QSUB) + 2ull * (kk & 3);
-          tc_mma_f16(tmem + C::O_COL, ad, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16(tmem + C::O_COL, ad, bd, id_o, (!first || kk > 0) ? 1u : 0u);
         }
         tc_commit(D_OD);
         tc_commit(D_VE);
         return true;
       };
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int sb = j & 1;
-        // score buffer sb last held S(j-2), read by the softmax before P(j-2) was ready
-        if (!mbar_wait(D_KF, j & 1, abort_flag, a.status)) { ok = false; break; }
+      int jt = 0;  // tiles of the items before this one
+      for (int it = 0;; ++it) {
+        const int slot = it & 3;
+        if (!mbar_wait(D_IF(slot), (it >> 2) & 1, abort_flag, a.status)) break;
+        const DecItem e = *reinterpret_cast<const DecItem*>(ring + slot * 32);
+        mbar_arrive(D_IE(slot));
+        if (e.unit < 0) break;
+        const int qb = it & 1;
+        if (!mbar_wait(D_QF(qb), (it >> 1) & 1, abort_flag, a.status)) break;
         tc_fence_after();
+        const uint32_t qt = smem_u32(smem + C::Q_OFF + qb * C::QT_BYTES);
+        bool ok = true;
+        for (int j = 0; j < e.ntiles; ++j) {
+          const int g = jt + j, sb = g & 1;
+          // score buffer sb last held S(g-2), read by the softmax before P(g-2) was ready
+          if (!mbar_wait(D_KF, g & 1, abort_flag, a.status)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint64_t ad = sdesc_k_sw128(kt + (kk >> 2) * C::SUB_BYTES) + 2ull * (kk & 3);
-          const uint64_t bd = sdesc_k_sw128(qt + (kk >> 2) * C::QSUB) + 2ull * (kk & 3);
-          tc_mma_f16(tmem + C::S_COL + sb * 16, ad, bd, id_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint64_t ad = sdesc_k_sw128(kt + (kk >> 2) * C::SUB_BYTES) + 2ull * (kk & 3);
+            const uint64_t bd = sdesc_k_sw128(qt + (kk >> 2) * C::QSUB) + 2ull * (kk & 3);
+            tc_mma_f16(tmem + C::S_COL + sb * 16, ad, bd, id_s, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(D_SF(sb));
+          tc_commit(D_KE);  // the K tile is free once S(g) is done
+          if (j > 0 && !pv(g - 1, j == 1)) { ok = false; break; }
         }
-        tc_commit(D_SF(sb));
-        tc_commit(D_KE);  // the K tile is free once S(j) is done
-        if (j > 0 && !pv(j - 1)) { ok = false; break; }
+        if (!ok) break;
+        tc_commit(D_QE(qb));  // the item's S MMAs (a commit with none outstanding arrives at once)
+        if (e.ntiles > 0 && !pv(jt + e.ntiles - 1, e.ntiles == 1)) break;
+        // the softmax has read the previous item's output: without this an item
+        // with no key tiles would complete the barrier a second time before the
+        // softmax waited for the first (a parity wait cannot tell them apart)
+        if (it > 0 && !mbar_wait(D_OE, (it - 1) & 1, abort_flag, a.status)) break;
+        tc_commit(D_OF);      // the item's output is complete in TMEM
+        jt += e.ntiles;
       }
-      if (ok && ntiles > 0) pv(ntiles - 1);
       tc_commit(D_DR);  // completes after every MMA above
       mbar_wait(D_DR, 0, nullptr, a.status);
     }
-  } else {
+  } else if (warp <= 5) {
+    griddep_wait();
+    griddep_launch();
     // ---------------- softmax, one thread per key of the tile (warps 2..5) ----------------
-    const int q = warp & 3;           // TMEM lane quarter
+    const int q = (threadIdx.x >> 5) & 3;  // TMEM lane quarter (warps 2-5 and 10-13 cover all four)
     const int row = q * 32 + lane;    // key of the tile / output dim
     const int wq = warp - 2;          // 0..3 for the cross-warp reductions
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    // Q^T: rows 0..G-1 = bf16(q_h), rows G..2G-1 = bf16(q_h - bf16(q_h)), the rest 0;
-    // 16-byte chunks in the 128-byte-swizzled K-major layout of the MMA's B operand
-    {
-      const __half* qrow = reinterpret_cast<const __half*>(a.qkv) + static_cast<size_t>(t) * a.n * a.w_rank +
-                           static_cast<size_t>(r) * a.w_rank + static_cast<size_t>(g) * G * HD;
-      for (int i = row; i < 16 * (HD / 8); i += 128) {
-        const int rr = i / (HD / 8), c = i % (HD / 8);  // row, 8-dim chunk
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (rr < 2 * G) {
-          const int h = rr < G ? rr : rr - G;
-          const uint4 u = *reinterpret_cast<const uint4*>(qrow + h * HD + c * 8);
-          const float x[8] = {f16lo(u.x), f16hi(u.x), f16lo(u.y), f16hi(u.y),
-                              f16lo(u.z), f16hi(u.z), f16lo(u.w), f16hi(u.w)};
-          float y[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) y[k] = rr < G ? x[k] : x[k] - bf2f(f2bf(x[k]));
-          w.x = pack_bf16x2(y[0], y[1]); w.y = pack_bf16x2(y[2], y[3]);
-          w.z = pack_bf16x2(y[4], y[5]); w.w = pack_bf16x2(y[6], y[7]);
-        }
-        *reinterpret_cast<uint4*>(smem + C::Q_OFF + (c >> 3) * C::QSUB + rr * 128 + (((c & 7) ^ (rr & 7)) << 4)) = w;
-      }
-      // A split of one short tile leaves V rows 16..127 unwritten: zero them (their
-      // P is 0, and 0 * NaN would not vanish).  Longer splits keep the previous
-      // tile's rows there, which are finite cache values.
-      if (ntiles == 1 && k1 - k0 <= 16) {
-        for (int i = row; i < C::NSUB * 112 * 8; i += 128) {
-          const int sub = i / (112 * 8), rem = i % (112 * 8);
-          *reinterpret_cast<uint4*>(smem + C::V_OFF + sub * C::SUB_BYTES + (16 + rem / 8) * 128 + (rem % 8) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(D_QR);
-    }
-    bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int sb = j & 1;
-      if (!warp_all(mbar_wait(D_SF(sb), (j >> 1) & 1, abort_flag, a.status))) ok = false;
-      tc_fence_after();
-      float sv[16];
-      tc_ld16(lane_addr + C::S_COL + sb * 16, sv);
-      const bool valid = k0 + j * C::BK + row < k1;
-      float sc[G], mw[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        sc[h] = valid ? (sv[h] + sv[G + h]) * a.scale_log2 : -INFINITY;
-        mw[h] = warp_max(sc[h]);
-      }
-      float* rmax = red + (j & 1) * 32;  // [4 warps][8 heads], alternating buffers
-      if (lane == 0) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) rmax[wq * 8 + h] = mw[h];
-      }
+    int jt = 0;
+    for (int it = 0;; ++it) {
+      const int slot = it & 3;
       // the barrier also agrees on failed waits (named barriers have no time limit)
-      if (!named_bar_and(1, 128, ok)) { ok = false; break; }
-      float mt[G], corr[G];
-      bool rescale = false;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        mt[h] = fmaxf(fmaxf(rmax[h], rmax[8 + h]), fmaxf(rmax[16 + h], rmax[24 + h]));
-        corr[h] = 1.0f;
-        if (mt[h] > m[h] + 8.0f) {  // uniform across the block
-          corr[h] = m[h] == -INFINITY ? 0.0f : exp2f(m[h] - mt[h]);
-          m[h] = mt[h];
-          rescale = true;
-        }
-      }
-      float p[G], pw[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        p[h] = exp2f(sc[h] - (m[h] == -INFINITY ? 0.0f : m[h]));
-        pw[h] = warp_sum(p[h]);
-      }
-      float* rsum = red + 64 + (j & 1) * 32;  // the same for the sums
-      if (lane == 0) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) rsum[wq * 8 + h] = pw[h];
-      }
-      // P^T(j): key `row` of head h at row h, column row of the [16][128] tile
-      uint8_t* pt = smem + C::P_OFF + (j & 1) * C::PT_BYTES + (row >> 6) * C::QSUB;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {  // bf16 high part in row h, bf16 low part in row G + h
-        const __nv_bfloat16 hi = f2bf(p[h]);
-        const __nv_bfloat16 lo = f2bf(p[h] - bf2f(hi));
-        const int rl = G + h;
-        *reinterpret_cast<__nv_bfloat16*>(pt + h * 128 + ((((row & 63) >> 3) ^ (h & 7)) << 4) + (row & 7) * 2) = hi;
-        *reinterpret_cast<__nv_bfloat16*>(pt + rl * 128 + ((((row & 63) >> 3) ^ (rl & 7)) << 4) + (row & 7) * 2) = lo;
-      }
-      named_bar_sync(1, 128);
-#pragma unroll
-      for (int h = 0; h < G; ++h) l[h] = l[h] * corr[h] + (rsum[h] + rsum[8 + h] + rsum[16 + h] + rsum[24 + h]);
-      if (rescale && j > 0) {
-        // O^T columns of the rescaled heads, once O += P(j-1) V(j-1) has completed
-        // (S(j) done implies PV(j-2) done: the barrier is at phase j-1 or j)
-        if (!warp_all(mbar_wait(D_OD, (j - 1) & 1, abort_flag, a.status))) ok = false;
-        if (ok) {
-          tc_fence_after();
-          float ov[16];
-          tc_ld16(lane_addr + C::O_COL, ov);
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            ov[h] *= corr[h];
-            ov[G + h] *= corr[h];
-          }
-          tc_st16(lane_addr + C::O_COL, ov);
-        }
-      }
-      if (!ok) continue;
-      fence_proxy_async_smem();
-      tc_fence_before();
+      const bool got = warp_all(mbar_wait(D_IF(slot), (it >> 2) & 1, abort_flag, a.status));
+      if (!named_bar_and(nbar, 128, got)) break;
+      const DecItem e = *reinterpret_cast<const DecItem*>(ring + slot * 32);
       __syncwarp();
-      if (lane == 0) mbar_arrive(D_PF(sb));
-    }
-    if (ok) ok = mbar_wait(D_DR, 0, abort_flag, a.status);
-    if (named_bar_and(1, 128, ok)) {
+      if (lane == 0) mbar_arrive(D_IE(slot));
+      if (e.unit < 0) break;
+      float m[G], l[G];  // running max (exp2 domain) and sum per head: the same in every softmax thread
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.0f;
+      }
+      bool ok = true;
+      for (int j = 0; j < e.ntiles; ++j) {
+        const int g = jt + j, sb = g & 1;
+        if (!warp_all(mbar_wait(D_SF(sb), (g >> 1) & 1, abort_flag, a.status))) ok = false;
+        tc_fence_after();
+        float sv[16];
+        tc_ld16(lane_addr + C::S_COL + sb * 16, sv);
+        const bool valid = e.k0 + j * C::BK + row < e.k1;
+        float sc[G], mw[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          sc[h] = valid ? (sv[h] + sv[G + h]) * a.scale_log2 : -INFINITY;
+          mw[h] = warp_max(sc[h]);
+        }
+        float* rmax = red + sb * 32;  // [4 warps][8 heads], alternating buffers
+        if (lane == 0) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) rmax[wq * 8 + h] = mw[h];
+        }
+        if (!named_bar_and(nbar, 128, ok)) { ok = false; break; }
+        float mt[G], corr[G];
+        bool rescale = false;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          mt[h] = fmaxf(fmaxf(rmax[h], rmax[8 + h]), fmaxf(rmax[16 + h], rmax[24 + h]));
+          corr[h] = 1.0f;
+          if (mt[h] > m[h] + 8.0f) {  // uniform across the block
+            corr[h] = m[h] == -INFINITY ? 0.0f : exp2f(m[h] - mt[h]);
+            m[h] = mt[h];
+            rescale = true;
+          }
+        }
+        float p[G], pw[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          p[h] = exp2f(sc[h] - (m[h] == -INFINITY ? 0.0f : m[h]));
+          pw[h] = warp_sum(p[h]);
+        }
+        float* rsum = red + 64 + sb * 32;  // the same for the sums
+        if (lane == 0) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) rsum[wq * 8 + h] = pw[h];
+        }
+        // P^T(g): key `row` of head h at row h, column row of the [16][128] tile
+        uint8_t* pt = smem + C::P_OFF + sb * C::PT_BYTES + (row >> 6) * C::QSUB;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {  // bf16 high part in row h, bf16 low part in row G + h
+          const __nv_bfloat16 hi = f2bf(p[h]);
+          const __nv_bfloat16 lo = f2bf(p[h] - bf2f(hi));
+          const int rl = G + h;
+          *reinterpret_cast<__nv_bfloat16*>(pt + h * 128 + ((((row & 63) >> 3) ^ (h & 7)) << 4) + (row & 7) * 2) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(pt + rl * 128 + ((((row & 63) >> 3) ^ (rl & 7)) << 4) + (row & 7) * 2) = lo;
+        }
+        named_bar_sync(nbar, 128);
+#pragma unroll
+        for (int h = 0; h < G; ++h) l[h] = l[h] * corr[h] + (rsum[h] + rsum[8 + h] + rsum[16 + h] + rsum[24 + h]);
+        if (rescale && j > 0) {
+          // O^T columns of the rescaled heads, once O += P(g-1) V(g-1) has completed
+          // (S(g) done implies PV(g-2) done: the barrier is at phase g-1 or g)
+          if (!warp_all(mbar_wait(D_OD, (g - 1) & 1, abort_flag, a.status))) ok = false;
+          if (ok) {
+            tc_fence_after();
+            float ov[16];
+            tc_ld16(lane_addr + C::O_COL, ov);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              ov[h] *= corr[h];
+              ov[G + h] *= corr[h];
+            }
+            tc_st16(lane_addr + C::O_COL, ov);
+          }
+        }
+        if (!ok) continue;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(D_PF(sb));
+      }
+      jt += e.ntiles;
+      // the item's output (one O^T row per output dim) into staging buffer it & 1,
+      // once the writer has emptied it (item it - 2)
+      const int ob = it & 1;
+      bool w = ok && warp_all(mbar_wait(D_OF, it & 1, abort_flag, a.status));
+      if (w && it >= 2) w = warp_all(mbar_wait(D_STE(ob), ((it >> 1) - 1) & 1, abort_flag, a.status));
+      if (!named_bar_and(nbar, 128, w)) break;
       tc_fence_after();
       float ov[16];
-      tc_ld16(lane_addr + C::O_COL, ov);  // O^T row `row` = output dim row of every head
-      if (ntiles == 0) {  // an empty split never wrote the accumulator
+      tc_ld16(lane_addr + C::O_COL, ov);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(D_OE);
+      float* st = reinterpret_cast<float*>(smem + C::ST_OFF + ob * C::ST_BYTES);
+      if (row < HD) {
 #pragma unroll
-        for (int h = 0; h < 16; ++h) ov[h] = 0.0f;
-      }
-#pragma unroll
-      for (int h = 0; h < G; ++h) ov[h] += ov[G + h];  // P V = P_hi V + P_lo V
-      const int d = row;
-      if (d < HD) {
-        if (nsplit == 1) {
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            __half* o = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
-                        (static_cast<size_t>(r) * a.nq_l + g * G + h) * HD + d;
-            uint32_t sat = 0;
-            *o = to_f16(l[h] > 0.0f ? ov[h] / l[h] : 0.0f, sat);
-            report_sat(a.status, sat);
-          }
-        } else {
-          float* part = a.part + (static_cast<size_t>(unit) * pstride + split) * G * (HD + 2);
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            part[h * (HD + 2) + d] = ov[h];
-            if (d == 0) {
-              part[h * (HD + 2) + HD] = m[h];
-              part[h * (HD + 2) + HD + 1] = l[h];
-            }
+        for (int h = 0; h < G; ++h) {
+          const float o = e.ntiles > 0 ? ov[h] + ov[G + h] : 0.0f;  // P V = P_hi V + P_lo V
+          st[h * (HD + 2) + row] = e.nsplit == 1 ? (l[h] > 0.0f ? o / l[h] : 0.0f) : o;
+          if (row == 0) {
+            st[h * (HD + 2) + HD] = m[h];
+            st[h * (HD + 2) + HD + 1] = l[h];
           }
         }
       }
+      mbar_arrive(D_STF(ob));
+    }
+  } else if (warp == 6) {
+    griddep_wait();
+    griddep_launch();
+    // ---------------- TMA: lane 0 streams K tiles, lane 1 V tiles ----------------
+    if (lane < 2) {
+      const bool is_k = lane == 0;
+      if (is_k) {
+        tma_prefetch_desc(&tmKV);
+        tma_prefetch_desc(&tmKV16);
+      }
+      const uint32_t full = is_k ? D_KF : D_VF, empty = is_k ? D_KE : D_VE;
+      uint8_t* dst = smem + (is_k ? C::K_OFF : C::V_OFF);
+      int issued = 0;  // tiles over the launch
+      for (int it = 0;; ++it) {
+        const int slot = it & 3;
+        if (!mbar_wait(D_IF(slot), (it >> 2) & 1, abort_flag, a.status)) break;
+        const DecItem e = *reinterpret_cast<const DecItem*>(ring + slot * 32);
+        mbar_arrive(D_IE(slot));
+        if (e.unit < 0) break;
+        const int r = (e.unit % per_seq) / a.nkv_l, g = e.unit % a.nkv_l;
+        bool ok = true;
+        // block of the next tile, looked up one tile ahead (its load overlaps the wait)
+        int blk_next = e.ntiles > 0 ? kv_block_checked(a.kvm, e.b, e.k0) : 0;
+        for (int j = 0; j < e.ntiles; ++j) {
+          const int key = e.k0 + j * C::BK;
+          const int blk = blk_next;
+          if (j + 1 < e.ntiles) blk_next = kv_block_checked(a.kvm, e.b, key + C::BK);
+          if (!mbar_wait(empty, (issued & 1) ^ 1u, abort_flag, a.status)) { ok = false; break; }
+          // a last tile of at most 16 keys loads 16 rows (the typical ctx + 1 tail)
+          const bool short_tail = j == e.ntiles - 1 && e.k1 - key <= 16;
+          mbar_arrive_expect_tx(full, short_tail ? C::KT_BYTES / 8 : C::KT_BYTES);
+          const int krow = static_cast<int>(kv_row(a.kvm, a.nkv_l, r, is_k ? 0 : 1, blk, g, key % a.kvm.block_len));
+          for (int sub = 0; sub < C::NSUB; ++sub)
+            tma_load_2d(smem_u32(dst + sub * C::SUB_BYTES), short_tail ? &tmKV16 : &tmKV, full, sub * 64, krow);
+          ++issued;
+          // the scheduler may draw the next item three tiles before this one's K
+          // stream ends (drawing, decoding and checking it takes about as long)
+          if (is_k && j == (e.ntiles > 3 ? e.ntiles - 3 : 0)) mbar_arrive(D_NREQ);
+        }
+        if (!ok) break;
+        if (is_k && e.ntiles == 0) mbar_arrive(D_NREQ);
+      }
+      if (issued > 0) mbar_wait(full, (issued - 1) & 1, nullptr, a.status);  // the last tile has landed
+    }
+  } else {
+    griddep_wait();
+    griddep_launch();
+    // ---------------- writer: outputs, split partials and merges (warp 7) ----------------
+    for (int it = 0;; ++it) {
+      const int slot = it & 3;
+      if (!warp_all(mbar_wait(D_IF(slot), (it >> 2) & 1, abort_flag, a.status))) break;
+      const DecItem e = *reinterpret_cast<const DecItem*>(ring + slot * 32);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(D_IE(slot));
+      if (e.unit < 0) break;
+      const int ob = it & 1;
+      if (!warp_all(mbar_wait(D_STF(ob), (it >> 1) & 1, abort_flag, a.status))) break;
+      const float* st = reinterpret_cast<const float*>(smem + C::ST_OFF + ob * C::ST_BYTES);
+      const int r = (e.unit % per_seq) / a.nkv_l, g = e.unit % a.nkv_l;
+      __half* obase = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(e.t) * a.n * a.nq_l * HD +
+                      (static_cast<size_t>(r) * a.nq_l + g * G) * HD;
+      if (e.nsplit == 1) {
+        uint32_t sat = 0;
+        for (int i = lane; i < G * HD / 8; i += 32) {
+          const int h = i / (HD / 8), c = i % (HD / 8);
+          const float* s8 = st + h * (HD + 2) + c * 8;
+          uint4 w;
+          w.x = pack_f16x2(s8[0], s8[1], sat); w.y = pack_f16x2(s8[2], s8[3], sat);
+          w.z = pack_f16x2(s8[4], s8[5], sat); w.w = pack_f16x2(s8[6], s8[7], sat);
+          *reinterpret_cast<uint4*>(obase + h * HD + c * 8) = w;
+        }
+        report_sat(a.status, sat);
+        mbar_arrive(D_STE(ob));
+        continue;
+      }
+      // a split: its partial (unnormalised O, m, l per head), then the last split
+      // of the unit to arrive (atomic counter, no waiting) merges them in split order
+      float* part = a.part + (static_cast<size_t>(e.unit) * pstride + e.split) * G * (HD + 2);
+      for (int i = lane; i < G * (HD + 2) / 2; i += 32)
+        reinterpret_cast<float2*>(part)[i] = reinterpret_cast<const float2*>(st)[i];
+      mbar_arrive(D_STE(ob));
+      __threadfence();
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) last = atomicAdd(a.counters + e.unit, 1) == e.nsplit - 1 ? 1 : 0;
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (!last) continue;
+      __threadfence();
+      const float* pbase = a.part + static_cast<size_t>(e.unit) * pstride * G * (HD + 2);
+      uint32_t sat = 0;
+      for (int i = lane; i < G * HD / 8; i += 32) {
+        const int h = i / (HD / 8), c = i % (HD / 8);
+        float mm = -INFINITY, ll = 0.0f, acc[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
+        for (int sp = 0; sp < e.nsplit; ++sp) {
+          const float* ps = pbase + (static_cast<size_t>(sp) * G + h) * (HD + 2);
+          const float m2 = __ldcg(ps + HD), l2 = __ldcg(ps + HD + 1);
+          float a2[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(ps + c * 8) + k);
+            a2[2 * k] = v.x;
+            a2[2 * k + 1] = v.y;
+          }
+          const float mn = fmaxf(mm, m2);
+          if (mn != -INFINITY) {
+            const float c1 = exp2f(mm - mn), c2 = exp2f(m2 - mn);
+            ll = ll * c1 + l2 * c2;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] = acc[k] * c1 + a2[k] * c2;
+            mm = mn;
+          }
+        }
+        float o[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[k] = ll > 0.0f ? acc[k] / ll : 0.0f;
+        uint4 w;
+        w.x = pack_f16x2(o[0], o[1], sat); w.y = pack_f16x2(o[2], o[3], sat);
+        w.z = pack_f16x2(o[4], o[5], sat); w.w = pack_f16x2(o[6], o[7], sat);
+        *reinterpret_cast<uint4*>(obase + h * HD + c * 8) = w;
+      }
+      report_sat(a.status, sat);
+      if (lane == 0) a.counters[e.unit] = 0;
     }
   }
-#undef D_QR
+#undef D_IF
+#undef D_IE
+#undef D_QF
+#undef D_QE
 #undef D_KF
 #undef D_KE
 #undef D_VF
@@ -804,43 +1024,27 @@ __global__ void __launch_bounds__(192) attn_decode_tc_kernel(const __grid_consta
 #undef D_SF
 #undef D_PF
 #undef D_OD
+#undef D_OF
+#undef D_STF
+#undef D_STE
+#undef D_NREQ
 #undef D_DR
+#undef D_OE
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (threadIdx.x >> 5 == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    tmem_dealloc(*tmem_slot, C::TMEM_COLS);
   }
-  if (nsplit == 1) return;
-  // the last CTA of this (sequence, rank, head) to finish merges the splits in order
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) *last_flag = (atomicAdd(a.counters + unit, 1) == nsplit - 1) ? 1 : 0;
-  __syncthreads();
-  if (!*last_flag) return;
-  __threadfence();
-  const float* pbase = a.part + static_cast<size_t>(unit) * pstride * G * (HD + 2);
-  for (int e = threadIdx.x; e < G * HD; e += blockDim.x) {
-    const int h = e / HD, d = e % HD;
-    float mm = -INFINITY, ll = 0.0f, aa = 0.0f;
-    for (int sp = 0; sp < nsplit; ++sp) {
-      const float* ps = pbase + (static_cast<size_t>(sp) * G + h) * (HD + 2);
-      const float m2 = __ldcg(ps + HD), l2 = __ldcg(ps + HD + 1), a2 = __ldcg(ps + d);
-      const float mn = fmaxf(mm, m2);
-      if (mn != -INFINITY) {
-        const float c1 = exp2f(mm - mn), c2 = exp2f(m2 - mn);
-        ll = ll * c1 + l2 * c2;
-        aa = aa * c1 + a2 * c2;
-        mm = mn;
-      }
+  // the last CTA to finish, over every launch drawing from the counter, resets it
+  // for the next step (every CTA has drawn its last tickets before it counts itself)
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.sched + 1, 1) == a.sched_ctas - 1) {
+      atomicExch(a.sched, 0);
+      atomicExch(a.sched + 1, 0);
     }
-    __half* o = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(t) * a.n * a.nq_l * HD +
-                (static_cast<size_t>(r) * a.nq_l + g * G + h) * HD + d;
-    uint32_t sat = 0;
-    *o = to_f16(ll > 0.0f ? aa / ll : 0.0f, sat);
-    report_sat(a.status, sat);
   }
-  if (threadIdx.x == 0) a.counters[unit] = 0;
 }
 
 template <int HD, int G>
@@ -851,12 +1055,12 @@ static cudaError_t prepare_decode_tc(int* ctas_per_sm) {
     cudaError_t e = cudaFuncSetAttribute(attn_decode_tc_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DtcCfg<HD>::SMEM);
     if (e != cudaSuccess) return e;
-    // all of the unified L1 / shared storage as shared memory: the occupancy below
-    // (and the split plan built on it) is then the one the launches get
+    // all of the unified L1 / shared storage as shared memory, so that two CTAs fit per SM
     e = cudaFuncSetAttribute(attn_decode_tc_kernel<HD, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_decode_tc_kernel<HD, G>, 192, DtcCfg<HD>::SMEM);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_decode_tc_kernel<HD, G>, DtcCfg<HD>::THREADS,
+                                                      DtcCfg<HD>::SMEM);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
     per_device_mark(pd, dev, occ);
@@ -874,17 +1078,21 @@ static cudaError_t decode_tc_ctas_per_sm(int G, int* per_sm) {
 }
 
 template <int HD, int G>
-static cudaError_t launch_decode_tc_hd(const AttnArgs& a, dim3 grid, cudaStream_t s) {
+static cudaError_t launch_decode_tc_hd(const AttnArgs& a, cudaStream_t s) {
   using C = DtcCfg<HD>;
   int per_sm = 0;
-  cudaError_t e0 = prepare_decode_tc<HD, G>(&per_sm);  // sets the shared-memory attribute once
+  cudaError_t e0 = prepare_decode_tc<HD, G>(&per_sm);  // sets the shared-memory attributes once
   if (e0 != cudaSuccess) return e0;
+  // persistent: a.ctas CTAs (one per SM: their shared memory fills it), each
+  // running two pipelines; CTAs that start late, e.g. on SMs another stream's
+  // kernel held, take whatever items are left
+  if (!a.sched || a.ctas < 1 || a.sched_ctas < a.ctas) return cudaErrorInvalidValue;
   const int64_t kv_rows = static_cast<int64_t>(a.n) * 2 * a.kvm.blocks * a.nkv_l * a.kvm.block_len;
   if (kv_rows >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
   CUtensorMap mkv, mkv16;
   if (!make_tmap_2d(&mkv, a.kv, kv_rows, HD, HD, 128, true)) return cudaErrorInvalidValue;
   if (!make_tmap_2d(&mkv16, a.kv, kv_rows, HD, HD, 16, true)) return cudaErrorInvalidValue;
-  return launch_pdl(attn_decode_tc_kernel<HD, G>, grid, dim3(192), C::SMEM, s, mkv, mkv16, a);
+  return launch_pdl(attn_decode_tc_kernel<HD, G>, dim3(a.ctas), dim3(C::THREADS), C::SMEM, s, mkv, mkv16, a);
 }
 
 // The split count of decode_splits for every unit, and a thinner last wave split further:
@@ -896,17 +1104,7 @@ static cudaError_t launch_decode_tc_hd(const AttnArgs& a, dim3 grid, cudaStream_
 DecodeSplit decode_split_plan(int max_kv_len, int num_units, int num_sms, int hd, int G, int max_splits) {
   DecodeSplit d{decode_splits(max_kv_len, num_units, num_sms, hd, G, max_splits), 0, 1};
   if (hd != 128 || d.splits != 1 || num_units <= 0) return d;
-  // resident CTAs per SM from the shared memory they take (the occupancy query
-  // reports one for this kernel, while two run side by side on every SM)
-  int dev = 0, smem_sm = 0, smem_rsv = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
-    return d;
-  int per_sm = smem_sm / (DtcCfg<128>::SMEM + smem_rsv);
-  if (per_sm > 2048 / 192) per_sm = 2048 / 192;  // threads
-  if (per_sm < 1) return d;
-  const int resident = num_sms * per_sm;
+  const int resident = 2 * num_sms;  // decode pipelines: two per CTA, one CTA per SM
   const int rem = num_units % resident;
   if (rem == 0 || num_units < resident || 2 * rem > resident) return d;
   int f = resident / rem;

@@ -271,7 +271,9 @@ struct AttnArgs {
   int splits;                // key splits per (sequence, rank, kv head) unit
   int tail_units;            // decode: the last tail_units units take tail_splits splits instead
   int tail_splits;
-  int ctas;                  // prefill: CTAs of the persistent launch (each walks work items)
+  int ctas;                  // CTAs of a persistent launch (each walks work items)
+  int* sched;                // decode: 2 ints (next ticket, CTAs done), zero between steps
+  int sched_ctas;            // decode: CTAs of all the launches that draw from sched
   int* status;
 };
 cudaError_t launch_attention_prefill(const AttnArgs& a, cudaStream_t s);

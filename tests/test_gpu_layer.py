@@ -46,6 +46,19 @@ def test_decode_thin_last_wave_split_further():
     check_step(g, [0, 1, 17, 37, 38, 39])
 
 
+def test_decode_persistent_ctas_take_many_items():
+    """200 decode sequences at tp 2 (1600 (sequence, rank, kv head) units) over
+    two layers: each resident decode CTA takes several items in turn, whole units
+    first and key splits of the last units (80 left after five rounds of 304,
+    three splits each); ragged lengths with a one-key context among the split
+    ones.  The second layer's launch draws from the ticket counter the first one
+    reset."""
+    ctxs = tuple((i * 397) % 900 for i in range(198)) + (0, 1500)
+    w = synth.Workload("decode_many", S06, (2,), (), ctxs, 2, False)
+    g = GpuStep(w, 2, head=False)
+    check_step(g, [0, 1, 57, 120, 189, 190, 197, 198, 199], head=False)
+
+
 @pytest.mark.parametrize("n", [1, 2])
 def test_prefill_with_cache_offset_and_ragged_lengths(n):
     """Prefill sequences with cached context (mask tril(S - T)) and lengths that
