@@ -673,7 +673,7 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
     ps = x->side;
   }
   if (b->num_prefill > 0) {
-    aa.seq_begin = 0; aa.seq_end = b->num_prefill; aa.splits = 1; aa.tail_units = 0; aa.tail_splits = 1;
+    aa.seq_begin = 0; aa.seq_end = b->num_prefill;
     // beside the decode attention a quarter of the SMs walk the work items (measured
     // on the 28-layer mixed step: 16 / 24 / 30 / 38 / 48 / 76 CTAs gave 8.06 / 8.10 /
     // 7.96 / 7.89 / 8.05 / 8.00 ms); alone, one CTA per item, which the hardware
@@ -691,12 +691,12 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
     const int max_splits = static_cast<int>(std::min<int64_t>(64, static_cast<int64_t>(x->r_apart.bytes) / per_split));
     const tpk::DecodeSplit ds =
         tpk::decode_split_plan(b->max_kv_len, units, x->num_sms, x->hd, x->nq_l / x->nkv_l, std::max(1, max_splits));
-    aa.splits = ds.splits; aa.tail_units = ds.tail_units; aa.tail_splits = ds.tail_splits;
+    aa.plan = ds;
     // the persistent decode kernel: one CTA per SM (two pipelines each) drawing
     // items from a ticket counter.  Beside a prefill attention it leaves that
     // kernel's SMs free, and a second launch on the prefill's stream takes them
     // over once the prefill ends, drawing from the same counter.
-    const int items = (units - ds.tail_units) * ds.splits + ds.tail_units * ds.tail_splits;
+    const int items = tpk::plan_items(ds);
     const int want = std::max(1, std::min(x->num_sms, (items + 1) / 2));
     const bool persistent = x->hd == 128;  // the tensor-core kernel (64-dim heads: a CTA per item)
     const int side_ctas =

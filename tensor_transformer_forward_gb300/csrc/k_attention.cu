@@ -51,32 +51,31 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   return r;
 }
 
-// CTA i of a decode launch (1D grid): its (sequence, rank, kv head) unit, its key
-// split and the unit's split count.  Units [0, U - tail_units) have `splits`
-// splits, the rest tail_splits; a unit's CTAs are consecutive.
+// Item i of a decode launch: its (sequence, rank, kv head) unit, its key split
+// and the unit's split count, walking the plan's levels in order (a unit's
+// items are consecutive).
 struct DecCta {
   int unit, split, nsplit;
 };
 __device__ __forceinline__ DecCta dec_cta(const AttnArgs& a, int i) {
-  const int units = (a.seq_end - a.seq_begin) * a.n * a.nkv_l;
-  const int u1 = units - a.tail_units;
-  DecCta c;
-  if (i < u1 * a.splits) {
-    c.unit = i / a.splits;
-    c.split = i % a.splits;
-    c.nsplit = a.splits;
-  } else {
-    const int j = i - u1 * a.splits;
-    c.unit = u1 + j / a.tail_splits;
-    c.split = j % a.tail_splits;
-    c.nsplit = a.tail_splits;
+  DecCta c{0, 0, 1};
+  int u0 = 0;
+#pragma unroll
+  for (int l = 0; l < kDecLevels; ++l) {
+    const int s = a.plan.splits[l], n = a.plan.units[l] * s;
+    if (i < n) {
+      c.unit = u0 + i / s;
+      c.split = i % s;
+      c.nsplit = s;
+      return c;
+    }
+    i -= n;
+    u0 += a.plan.units[l];
   }
   return c;
 }
-// partials per unit in the split workspace (the larger of the two split counts)
-__device__ __forceinline__ int dec_part_stride(const AttnArgs& a) {
-  return a.tail_units > 0 && a.tail_splits > a.splits ? a.tail_splits : a.splits;
-}
+// partials per unit in the split workspace
+__device__ __forceinline__ int dec_part_stride(const AttnArgs& a) { return plan_max_splits(a.plan); }
 
 // ---------------------------------------------------------------------------
 // Decode (one new token per sequence): flash-decoding split over the keys.
@@ -447,10 +446,10 @@ cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s) {
   if (seqs <= 0) return cudaSuccess;
   const int G = a.nq_l / a.nkv_l;
   const int units = seqs * a.n * a.nkv_l;
-  if (a.splits < 1 || a.tail_units < 0 || a.tail_units > units || (a.tail_units > 0 && a.tail_splits < 1))
-    return cudaErrorInvalidValue;
-  const int items = (units - a.tail_units) * a.splits + a.tail_units * (a.tail_units > 0 ? a.tail_splits : 0);
-  dim3 grid(items);
+  for (int l = 0; l < kDecLevels; ++l)
+    if (a.plan.units[l] < 0 || a.plan.splits[l] < 1) return cudaErrorInvalidValue;
+  if (plan_units(a.plan) != units) return cudaErrorInvalidValue;
+  dim3 grid(plan_items(a.plan));
 #define TP_DEC_TC(HD_, G_) \
   if (a.hd == HD_ && G == G_) return launch_decode_tc_hd<HD_, G_>(a, s);
 #define TP_DEC(HD_, G_) \
@@ -496,7 +495,7 @@ cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s) {
 // does not depend on which CTA takes an item: an item's arithmetic is fixed, and
 // splits merge in split order.
 // ---------------------------------------------------------------------------
-template <int HD>
+template <int HD, int G>
 struct DtcCfg {
   static constexpr int BK = 128;                   // keys per tile
   static constexpr int NSUB = HD / 64;             // 64-dim sub-tiles
@@ -505,18 +504,32 @@ struct DtcCfg {
   static constexpr int QSUB = 16 * 128;            // [16 rows][64 dims] bf16
   static constexpr int QT_BYTES = NSUB * QSUB;
   static constexpr int PT_BYTES = 2 * QSUB;        // [16 heads][128 keys] bf16 (two 64-key sub-tiles)
-  static constexpr int ST_BYTES = (8 * (HD + 2) * 4 + 15) / 16 * 16;  // staged output of up to 8 heads
+  // K and V stream through rings of 16 KB slots: a K tile is two slots of 64
+  // head dims ([128 keys][64 dims]), a V tile two slots of 64 keys ([64 keys]
+  // [2 x 64 dims]).  Three slots per ring (where both pipelines' share fits: up
+  // to 4 heads per kv group) keep 1.5 tiles of each in flight per pipeline, so a
+  // pipeline does not wait a whole load latency per tile for the V slot its
+  // last PV MMA frees.
+  static constexpr int SLOT = 16384;
+  static constexpr int VSUB = 8192;                // [64 keys][64 dims] of a V slot
+  static constexpr int KSLOTS = G <= 4 ? 3 : 2;
+  static constexpr int VSLOTS = G <= 4 ? 3 : 2;
+  // a pipeline's operand tiles (1024-byte aligned: 128-byte swizzle atoms)
   static constexpr int K_OFF = 0;
-  static constexpr int V_OFF = K_OFF + KT_BYTES;
-  static constexpr int Q_OFF = V_OFF + KT_BYTES;   // two Q^T buffers
-  static constexpr int P_OFF = Q_OFF + 2 * QT_BYTES;   // two P^T buffers
-  static constexpr int RED_OFF = P_OFF + 2 * PT_BYTES;  // max then sum: [2][4 warps][8 heads] fp32 each
+  static constexpr int V_OFF = K_OFF + KSLOTS * SLOT;
+  static constexpr int Q_OFF = V_OFF + VSLOTS * SLOT;   // Q^T
+  static constexpr int P_OFF = Q_OFF + QT_BYTES;   // two P^T buffers
+  static constexpr int BIG = P_OFF + 2 * PT_BYTES;
+  // the rest of a pipeline's share, after both pipelines' operand tiles
+  static constexpr int ST_BYTES = (G * (HD + 2) * 4 + 15) / 16 * 16;  // staged output of the G heads
+  static constexpr int RED_OFF = 0;                // max then sum: [2][4 warps][8 heads] fp32 each
   static constexpr int ST_OFF = RED_OFF + 512;     // two staging buffers
   static constexpr int RING_OFF = ST_OFF + 2 * ST_BYTES;  // item ring: 4 x 32 bytes
   static constexpr int BAR_OFF = RING_OFF + 128;
-  static constexpr int NBARS = 29;
-  static constexpr int PIPE_BYTES = (BAR_OFF + NBARS * 8 + 16 + 1023) / 1024 * 1024;  // one pipeline's share
-  static constexpr int SMEM = 1024 + 2 * PIPE_BYTES;
+  static constexpr int NBARS = 23 + 2 * KSLOTS + 2 * VSLOTS;
+  static constexpr int SMALL = (BAR_OFF + NBARS * 8 + 8 + 15) / 16 * 16;  // + TMEM address, abort flag
+  static constexpr int SMEM = 1024 + 2 * BIG + 2 * SMALL;
+  static_assert(SMEM <= 232448, "two pipelines fit one SM's shared memory");
   static constexpr int S_COL = 0, O_COL = 32, PIPE_COLS = 64, TMEM_COLS = 128;
   static constexpr int THREADS = 512;  // two pipelines of 8 warps
 };
@@ -530,45 +543,49 @@ struct DecItem {
 
 template <int HD, int G>
 __global__ void __launch_bounds__(512, 1) attn_decode_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
+                                                                const __grid_constant__ CUtensorMap tmKV64,
                                                                 const __grid_constant__ CUtensorMap tmKV16,
                                                                 const AttnArgs a) {
-  using C = DtcCfg<HD>;
+  using C = DtcCfg<HD, G>;
   static_assert(2 * G <= 16, "hi and lo rows of the kv group fit N = 16");
+  static_assert(HD == 128, "a K tile is two 64-dim slots");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem0 = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int pipe = threadIdx.x >> 8;  // warps 0-7 pipeline 0, warps 8-15 pipeline 1
-  uint8_t* smem = smem0 + pipe * C::PIPE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  // barriers: 0-3 item full | 4-7 item empty | 8,9 q full | 10,11 q empty | 12 k full | 13 k empty |
-  // 14 v full | 15 v empty | 16,17 s full | 18,19 p full | 20 pv done | 21 item's o done |
-  // 22,23 staging full | 24,25 staging empty | 26 next-item request | 27 drain | 28 item's o read
+  uint8_t* smem = smem0 + pipe * C::BIG;                       // operand tiles
+  uint8_t* sm2 = smem0 + 2 * C::BIG + pipe * C::SMALL;          // the rest
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm2 + C::BAR_OFF);
+  // barriers: 0-3 item full | 4-7 item empty | 8 q full | 9 q empty | 10,11 s full | 12,13 p full |
+  // 14 pv done | 15 item's o done | 16,17 staging full | 18,19 staging empty | 20 next-item request |
+  // 21 drain | 22 item's o read | then full and empty per K slot, per V slot
   // the TMEM address and the abort flag live in pipeline 0's share (one per CTA)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(reinterpret_cast<uint64_t*>(smem0 + C::BAR_OFF) + C::NBARS);
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(reinterpret_cast<uint64_t*>(smem0 + 2 * C::BIG + C::BAR_OFF) + C::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
-  uint8_t* ring = smem + C::RING_OFF;
+  float* red = reinterpret_cast<float*>(sm2 + C::RED_OFF);
+  uint8_t* ring = sm2 + C::RING_OFF;
   const uint32_t bar0 = smem_u32(bars);
 #define D_IF(s) (bar0 + 8u * (s))
 #define D_IE(s) (bar0 + 8u * (4 + (s)))
-#define D_QF(b) (bar0 + 8u * (8 + (b)))
-#define D_QE(b) (bar0 + 8u * (10 + (b)))
-#define D_KF (bar0 + 8u * 12)
-#define D_KE (bar0 + 8u * 13)
-#define D_VF (bar0 + 8u * 14)
-#define D_VE (bar0 + 8u * 15)
-#define D_SF(b) (bar0 + 8u * (16 + (b)))
-#define D_PF(b) (bar0 + 8u * (18 + (b)))
-#define D_OD (bar0 + 8u * 20)
-#define D_OF (bar0 + 8u * 21)
-#define D_STF(b) (bar0 + 8u * (22 + (b)))
-#define D_STE(b) (bar0 + 8u * (24 + (b)))
-#define D_NREQ (bar0 + 8u * 26)
-#define D_DR (bar0 + 8u * 27)
-#define D_OE (bar0 + 8u * 28)
+#define D_QF (bar0 + 8u * 8)
+#define D_QE (bar0 + 8u * 9)
+#define D_SF(b) (bar0 + 8u * (10 + (b)))
+#define D_PF(b) (bar0 + 8u * (12 + (b)))
+#define D_OD (bar0 + 8u * 14)
+#define D_OF (bar0 + 8u * 15)
+#define D_STF(b) (bar0 + 8u * (16 + (b)))
+#define D_STE(b) (bar0 + 8u * (18 + (b)))
+#define D_NREQ (bar0 + 8u * 20)
+#define D_DR (bar0 + 8u * 21)
+#define D_OE (bar0 + 8u * 22)
+#define D_KF(s) (bar0 + 8u * (23 + (s)))
+#define D_KE(s) (bar0 + 8u * (23 + C::KSLOTS + (s)))
+#define D_VF(s) (bar0 + 8u * (23 + 2 * C::KSLOTS + (s)))
+#define D_VE(s) (bar0 + 8u * (23 + 2 * C::KSLOTS + C::VSLOTS + (s)))
   const int warp = (threadIdx.x >> 5) & 7, lane = threadIdx.x & 31;  // warp within the pipeline
   const int per_seq = a.n * a.nkv_l;
   const int units = (a.seq_end - a.seq_begin) * per_seq;
-  const int items = (units - a.tail_units) * a.splits + (a.tail_units > 0 ? a.tail_units * a.tail_splits : 0);
+  const int items = plan_items(a.plan);
   const int pstride = dec_part_stride(a);
 
   if ((threadIdx.x & 255) == 0) {
@@ -576,18 +593,22 @@ __global__ void __launch_bounds__(512, 1) attn_decode_tc_kernel(const __grid_con
       mbar_init(D_IF(i), 1);
       mbar_init(D_IE(i), 8);  // MMA, 4 softmax warps, K lane, V lane, writer
     }
+    for (int i = 0; i < C::KSLOTS; ++i) {
+      mbar_init(D_KF(i), 1);
+      mbar_init(D_KE(i), 1);
+    }
+    for (int i = 0; i < C::VSLOTS; ++i) {
+      mbar_init(D_VF(i), 1);
+      mbar_init(D_VE(i), 1);
+    }
+    mbar_init(D_QF, 32);
+    mbar_init(D_QE, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(D_QF(i), 32);
-      mbar_init(D_QE(i), 1);
       mbar_init(D_SF(i), 1);
       mbar_init(D_PF(i), 4);
       mbar_init(D_STF(i), 128);
       mbar_init(D_STE(i), 32);
     }
-    mbar_init(D_KF, 1);
-    mbar_init(D_KE, 1);
-    mbar_init(D_VF, 1);
-    mbar_init(D_VE, 1);
     mbar_init(D_OD, 1);
     mbar_init(D_OF, 1);
     mbar_init(D_NREQ, 1);
@@ -600,11 +621,11 @@ __global__ void __launch_bounds__(512, 1) attn_decode_tc_kernel(const __grid_con
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
-  // Zero the V tile and both Q^T buffers: rows 2G..15 of Q^T stay zero, and a
-  // first item of one short tile leaves V rows 16..127 unwritten (their P is 0,
-  // and 0 * NaN would not vanish); later short tiles find an earlier tile's rows
-  // there, which are finite cache values.
-  for (int i = threadIdx.x & 255; i < (C::KT_BYTES + 2 * C::QT_BYTES) / 16; i += 256)
+  // Zero the V slots and Q^T: rows 2G..15 of Q^T stay zero, and a short tile
+  // (at most 16 keys) loads 16 V rows only, so a first item of one short tile
+  // would leave unwritten rows (their P is 0, and 0 * NaN would not vanish);
+  // later short tiles find earlier tiles' rows there, which are finite cache values.
+  for (int i = threadIdx.x & 255; i < (C::VSLOTS * C::SLOT + C::QT_BYTES) / 16; i += 256)
     *reinterpret_cast<uint4*>(smem + C::V_OFF + i * 16) = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   tc_fence_before();
@@ -655,33 +676,46 @@ __global__ void __launch_bounds__(512, 1) attn_decode_tc_kernel(const __grid_con
       }
       if (bad && lane == 0) raise_flag(a.status, TP_DEVFLAG_BAD_TOKEN);
       if (e.unit < 0) break;
-      // query rows of the item into Q^T buffer it & 1, once the S MMAs of its
-      // previous user (item it - 2) are done: rows 0..G-1 = bf16(q_h), rows
-      // G..2G-1 = bf16(q_h - bf16(q_h)); 16-byte chunks in the 128-byte-swizzled
-      // K-major layout of the MMA's B operand
-      const int qb = it & 1;
-      if (it >= 2 && !warp_all(mbar_wait(D_QE(qb), ((it >> 1) - 1) & 1, abort_flag, a.status))) break;
+      // the item's query into registers at once, into Q^T once the previous
+      // item's S MMAs are done: rows 0..G-1 = bf16(q_h), rows G..2G-1 =
+      // bf16(q_h - bf16(q_h)); 16-byte chunks in the 128-byte-swizzled K-major
+      // layout of the MMA's B operand
       {
+        constexpr int NQC = (G * (HD / 8) + 31) / 32;  // 8-dim chunks per lane
         const int r = (e.unit % per_seq) / a.nkv_l, g = e.unit % a.nkv_l;
         const __half* qrow = reinterpret_cast<const __half*>(a.qkv) + static_cast<size_t>(e.t) * a.n * a.w_rank +
                              static_cast<size_t>(r) * a.w_rank + static_cast<size_t>(g) * G * HD;
-        uint8_t* qt = smem + C::Q_OFF + qb * C::QT_BYTES;
-        for (int i = lane; i < 2 * G * (HD / 8); i += 32) {
-          const int rr = i / (HD / 8), c = i % (HD / 8);  // row, 8-dim chunk
-          const int h = rr < G ? rr : rr - G;
-          const uint4 u = __ldcg(reinterpret_cast<const uint4*>(qrow + h * HD + c * 8));
-          const float x[8] = {f16lo(u.x), f16hi(u.x), f16lo(u.y), f16hi(u.y),
-                              f16lo(u.z), f16hi(u.z), f16lo(u.w), f16hi(u.w)};
-          float y[8];
+        uint4 qv[NQC];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) y[k] = rr < G ? x[k] : x[k] - bf2f(f2bf(x[k]));
-          uint4 w;
-          w.x = pack_bf16x2(y[0], y[1]); w.y = pack_bf16x2(y[2], y[3]);
-          w.z = pack_bf16x2(y[4], y[5]); w.w = pack_bf16x2(y[6], y[7]);
-          *reinterpret_cast<uint4*>(qt + (c >> 3) * C::QSUB + rr * 128 + (((c & 7) ^ (rr & 7)) << 4)) = w;
+        for (int k = 0; k < NQC; ++k) {
+          const int i = lane + 32 * k;
+          qv[k] = i < G * (HD / 8) ? __ldcg(reinterpret_cast<const uint4*>(qrow + i * 8)) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (it >= 1 && !warp_all(mbar_wait(D_QE, (it - 1) & 1, abort_flag, a.status))) break;
+        uint8_t* qt = smem + C::Q_OFF;
+#pragma unroll
+        for (int k = 0; k < NQC; ++k) {
+          const int i = lane + 32 * k;
+          if (i < G * (HD / 8)) {
+            const int h = i / (HD / 8), c = i % (HD / 8);  // head, 8-dim chunk
+            const uint4 u = qv[k];
+            const float x[8] = {f16lo(u.x), f16hi(u.x), f16lo(u.y), f16hi(u.y),
+                                f16lo(u.z), f16hi(u.z), f16lo(u.w), f16hi(u.w)};
+            float lo[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) lo[j] = x[j] - bf2f(f2bf(x[j]));
+            uint4 w;
+            w.x = pack_bf16x2(x[0], x[1]); w.y = pack_bf16x2(x[2], x[3]);
+            w.z = pack_bf16x2(x[4], x[5]); w.w = pack_bf16x2(x[6], x[7]);
+            const int rl = G + h;
+            *reinterpret_cast<uint4*>(qt + (c >> 3) * C::QSUB + h * 128 + (((c & 7) ^ (h & 7)) << 4)) = w;
+            w.x = pack_bf16x2(lo[0], lo[1]); w.y = pack_bf16x2(lo[2], lo[3]);
+            w.z = pack_bf16x2(lo[4], lo[5]); w.w = pack_bf16x2(lo[6], lo[7]);
+            *reinterpret_cast<uint4*>(qt + (c >> 3) * C::QSUB + rl * 128 + (((c & 7) ^ (rl & 7)) << 4)) = w;
+          }
         }
         fence_proxy_async_smem();
-        mbar_arrive(D_QF(qb));
+        mbar_arrive(D_QF);
       }
       // the next ticket a few K tiles before the item's K stream ends: late enough
       // that the items left go to whichever pipelines free up first, early enough
@@ -704,18 +738,24 @@ __global__ void __launch_bounds__(512, 1) attn_decode_tc_kernel(const __grid_con
       const uint32_t kt = smem_u32(smem + C::K_OFF), vt = smem_u32(smem + C::V_OFF);
       auto pv = [&](int g, bool first) -> bool {  // O^T (+)= V(g)^T P(g)^T, g counting tiles over the launch
         const int pb = g & 1;
+        const int v0 = (2 * g) % C::VSLOTS, v1 = (2 * g + 1) % C::VSLOTS;  // the tile's two key halves
         if (!mbar_wait(D_PF(pb), (g >> 1) & 1, abort_flag, a.status)) return false;
-        if (!mbar_wait(D_VF, g & 1, abort_flag, a.status)) return false;
-        tc_fence_after();
         const uint32_t pt = smem_u32(smem + C::P_OFF + pb * C::PT_BYTES);
+        // each key half as soon as it has landed; its slot frees when its MMAs are done
+        for (int h = 0; h < 2; ++h) {
+          const int vs = h ? v1 : v0;
+          if (!mbar_wait(D_VF(vs), ((2 * g + h) / C::VSLOTS) & 1, abort_flag, a.status)) return false;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < C::BK / 16; ++kk) {
-          const uint64_t ad = sdesc_mn_sw128(vt + kk * 16 * 128, C::SUB_BYTES, 1024);
-          const uint64_t bd = sdesc_k_sw128(pt + (kk >> 2) * C::QSUB) + 2ull * (kk & 3);
-          tc_mma_f16(tmem + C::O_COL, ad, bd, id_o, (!first || kk > 0) ? 1u : 0u);
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = 4 * h + k4;
+            const uint64_t ad = sdesc_mn_sw128(vt + vs * C::SLOT + k4 * 16 * 128, C::VSUB, 1024);
+            const uint64_t bd = sdesc_k_sw128(pt + h * C::QSUB) + 2ull * k4;
+            tc_mma_f16(tmem + C::O_COL, ad, bd, id_o, (!first || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(D_VE(vs));
         }
         tc_commit(D_OD);
-        tc_commit(D_VE);
         return true;
       };
       int jt = 0;  // tiles of the items before this one
@@ -725,28 +765,38 @@ __global__ void __launch_bounds__(512, 1) attn_decode_tc_kernel(const __grid_con
         const DecItem e = *reinterpret_cast<const DecItem*>(ring + slot * 32);
         mbar_arrive(D_IE(slot));
         if (e.unit < 0) break;
-        const int qb = it & 1;
-        if (!mbar_wait(D_QF(qb), (it >> 1) & 1, abort_flag, a.status)) break;
+        if (!mbar_wait(D_QF, it & 1, abort_flag, a.status)) break;
         tc_fence_after();
-        const uint32_t qt = smem_u32(smem + C::Q_OFF + qb * C::QT_BYTES);
+        const uint32_t qt = smem_u32(smem + C::Q_OFF);
         bool ok = true;
         for (int j = 0; j < e.ntiles; ++j) {
           const int g = jt + j, sb = g & 1;
-          // score buffer sb last held S(g-2), read by the softmax before P(g-2) was ready
-          if (!mbar_wait(D_KF, g & 1, abort_flag, a.status)) { ok = false; break; }
-          tc_fence_after();
+          const int k0s = (2 * g) % C::KSLOTS, k1s = (2 * g + 1) % C::KSLOTS;  // the tile's two dim halves
+          // score buffer sb last held S(g-2), read by the softmax before P(g-2) was ready;
+          // each head-dim half as soon as it has landed, its slot free when its MMAs are done
+          for (int h = 0; h < 2 && ok; ++h) {
+            const int ks = h ? k1s : k0s;
+            if (!mbar_wait(D_KF(ks), ((2 * g + h) / C::KSLOTS) & 1, abort_flag, a.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint64_t ad = sdesc_k_sw128(kt + (kk >> 2) * C::SUB_BYTES) + 2ull * (kk & 3);
-            const uint64_t bd = sdesc_k_sw128(qt + (kk >> 2) * C::QSUB) + 2ull * (kk & 3);
-            tc_mma_f16(tmem + C::S_COL + sb * 16, ad, bd, id_s, kk > 0 ? 1u : 0u);
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const int kk = 4 * h + k4;
+              const uint64_t ad = sdesc_k_sw128(kt + ks * C::SLOT) + 2ull * k4;
+              const uint64_t bd = sdesc_k_sw128(qt + h * C::QSUB) + 2ull * k4;
+              tc_mma_f16(tmem + C::S_COL + sb * 16, ad, bd, id_s, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(D_KE(ks));
           }
+          if (!ok) break;
           tc_commit(D_SF(sb));
-          tc_commit(D_KE);  // the K tile is free once S(g) is done
+          if (j == e.ntiles - 1) tc_commit(D_QE);  // Q^T is free once the item's last S is done
           if (j > 0 && !pv(g - 1, j == 1)) { ok = false; break; }
         }
         if (!ok) break;
-        tc_commit(D_QE(qb));  // the item's S MMAs (a commit with none outstanding arrives at once)
+        if (e.ntiles == 0) tc_commit(D_QE);  // no S MMAs: arrives once the earlier MMAs are done
         if (e.ntiles > 0 && !pv(jt + e.ntiles - 1, e.ntiles == 1)) break;
         // the softmax has read the previous item's output: without this an item
         // with no key tiles would complete the barrier a second time before the
@@ -873,7 +923,7 @@ __global__ void __launch_bounds__(512, 1) attn_decode_tc_kernel(const __grid_con
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(D_OE);
-      float* st = reinterpret_cast<float*>(smem + C::ST_OFF + ob * C::ST_BYTES);
+      float* st = reinterpret_cast<float*>(sm2 + C::ST_OFF + ob * C::ST_BYTES);
       if (row < HD) {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -893,13 +943,10 @@ __global__ void __launch_bounds__(512, 1) attn_decode_tc_kernel(const __grid_con
     // ---------------- TMA: lane 0 streams K tiles, lane 1 V tiles ----------------
     if (lane < 2) {
       const bool is_k = lane == 0;
-      if (is_k) {
-        tma_prefetch_desc(&tmKV);
-        tma_prefetch_desc(&tmKV16);
-      }
-      const uint32_t full = is_k ? D_KF : D_VF, empty = is_k ? D_KE : D_VE;
-      uint8_t* dst = smem + (is_k ? C::K_OFF : C::V_OFF);
-      int issued = 0;  // tiles over the launch
+      tma_prefetch_desc(is_k ? &tmKV : &tmKV64);
+      tma_prefetch_desc(&tmKV16);
+      const int nsl = is_k ? C::KSLOTS : C::VSLOTS;
+      int issued = 0;  // slots filled over the launch (two per tile)
       for (int it = 0;; ++it) {
         const int slot = it & 3;
         if (!mbar_wait(D_IF(slot), (it >> 2) & 1, abort_flag, a.status)) break;
@@ -914,14 +961,33 @@ __global__ void __launch_bounds__(512, 1) attn_decode_tc_kernel(const __grid_con
           const int key = e.k0 + j * C::BK;
           const int blk = blk_next;
           if (j + 1 < e.ntiles) blk_next = kv_block_checked(a.kvm, e.b, key + C::BK);
-          if (!mbar_wait(empty, (issued & 1) ^ 1u, abort_flag, a.status)) { ok = false; break; }
           // a last tile of at most 16 keys loads 16 rows (the typical ctx + 1 tail)
           const bool short_tail = j == e.ntiles - 1 && e.k1 - key <= 16;
-          mbar_arrive_expect_tx(full, short_tail ? C::KT_BYTES / 8 : C::KT_BYTES);
           const int krow = static_cast<int>(kv_row(a.kvm, a.nkv_l, r, is_k ? 0 : 1, blk, g, key % a.kvm.block_len));
-          for (int sub = 0; sub < C::NSUB; ++sub)
-            tma_load_2d(smem_u32(dst + sub * C::SUB_BYTES), short_tail ? &tmKV16 : &tmKV, full, sub * 64, krow);
-          ++issued;
+          // K: slot h = head dims [64h, 64h + 64) of the 128 keys; V: slot h = keys
+          // [64h, 64h + 64) with both dim halves (a short tile fills half 0 only)
+          for (int h = 0; h < 2; ++h) {
+            const int sl = issued % nsl;
+            const uint32_t full = is_k ? D_KF(sl) : D_VF(sl), empty = is_k ? D_KE(sl) : D_VE(sl);
+            uint8_t* dst = smem + (is_k ? C::K_OFF : C::V_OFF) + sl * C::SLOT;
+            if (!mbar_wait(empty, ((issued / nsl) & 1) ^ 1u, abort_flag, a.status)) { ok = false; break; }
+            ++issued;
+            if (is_k) {
+              mbar_arrive_expect_tx(full, short_tail ? C::SLOT / 8 : C::SLOT);
+              tma_load_2d(smem_u32(dst), short_tail ? &tmKV16 : &tmKV, full, h * 64, krow);
+            } else if (!short_tail) {
+              mbar_arrive_expect_tx(full, C::SLOT);
+              for (int sub = 0; sub < 2; ++sub)
+                tma_load_2d(smem_u32(dst + sub * C::VSUB), &tmKV64, full, sub * 64, krow + 64 * h);
+            } else if (h == 0) {
+              mbar_arrive_expect_tx(full, C::SLOT / 4);
+              for (int sub = 0; sub < 2; ++sub)
+                tma_load_2d(smem_u32(dst + sub * C::VSUB), &tmKV16, full, sub * 64, krow);
+            } else {
+              mbar_arrive(full);  // keys 64..127 of a short tile: none (P is 0 there)
+            }
+          }
+          if (!ok) break;
           // the scheduler may draw the next item three tiles before this one's K
           // stream ends (drawing, decoding and checking it takes about as long)
           if (is_k && j == (e.ntiles > 3 ? e.ntiles - 3 : 0)) mbar_arrive(D_NREQ);
@@ -929,7 +995,10 @@ __global__ void __launch_bounds__(512, 1) attn_decode_tc_kernel(const __grid_con
         if (!ok) break;
         if (is_k && e.ntiles == 0) mbar_arrive(D_NREQ);
       }
-      if (issued > 0) mbar_wait(full, (issued - 1) & 1, nullptr, a.status);  // the last tile has landed
+      // every slot's last load has landed before the CTA may exit (a consumer that
+      // gave up early leaves them unwaited)
+      for (int q = issued > nsl ? issued - nsl : 0; q < issued; ++q)
+        mbar_wait(is_k ? D_KF(q % nsl) : D_VF(q % nsl), (q / nsl) & 1, nullptr, a.status);
     }
   } else {
     griddep_wait();
@@ -944,7 +1013,7 @@ __global__ void __launch_bounds__(512, 1) attn_decode_tc_kernel(const __grid_con
       if (e.unit < 0) break;
       const int ob = it & 1;
       if (!warp_all(mbar_wait(D_STF(ob), (it >> 1) & 1, abort_flag, a.status))) break;
-      const float* st = reinterpret_cast<const float*>(smem + C::ST_OFF + ob * C::ST_BYTES);
+      const float* st = reinterpret_cast<const float*>(sm2 + C::ST_OFF + ob * C::ST_BYTES);
       const int r = (e.unit % per_seq) / a.nkv_l, g = e.unit % a.nkv_l;
       __half* obase = reinterpret_cast<__half*>(a.out) + static_cast<size_t>(e.t) * a.n * a.nq_l * HD +
                       (static_cast<size_t>(r) * a.nq_l + g * G) * HD;
@@ -982,23 +1051,36 @@ __global__ void __launch_bounds__(512, 1) attn_decode_tc_kernel(const __grid_con
         float mm = -INFINITY, ll = 0.0f, acc[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
-        for (int sp = 0; sp < e.nsplit; ++sp) {
-          const float* ps = pbase + (static_cast<size_t>(sp) * G + h) * (HD + 2);
-          const float m2 = __ldcg(ps + HD), l2 = __ldcg(ps + HD + 1);
-          float a2[8];
+        // four splits' partials loaded at once (one L2 round trip), then added in split order
+        for (int s0 = 0; s0 < e.nsplit; s0 += 4) {
+          float m2[4], l2[4], a2[4][8];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 v = __ldcg(reinterpret_cast<const float2*>(ps + c * 8) + k);
-            a2[2 * k] = v.x;
-            a2[2 * k + 1] = v.y;
+          for (int q = 0; q < 4; ++q) {
+            m2[q] = -INFINITY;
+            l2[q] = 0.0f;
+            if (s0 + q < e.nsplit) {
+              const float* ps = pbase + (static_cast<size_t>(s0 + q) * G + h) * (HD + 2);
+              m2[q] = __ldcg(ps + HD);
+              l2[q] = __ldcg(ps + HD + 1);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float2 v = __ldcg(reinterpret_cast<const float2*>(ps + c * 8) + k);
+                a2[q][2 * k] = v.x;
+                a2[q][2 * k + 1] = v.y;
+              }
+            }
           }
-          const float mn = fmaxf(mm, m2);
-          if (mn != -INFINITY) {
-            const float c1 = exp2f(mm - mn), c2 = exp2f(m2 - mn);
-            ll = ll * c1 + l2 * c2;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) acc[k] = acc[k] * c1 + a2[k] * c2;
-            mm = mn;
+          for (int q = 0; q < 4; ++q) {
+            if (s0 + q >= e.nsplit) break;
+            const float mn = fmaxf(mm, m2[q]);
+            if (mn != -INFINITY) {
+              const float c1 = exp2f(mm - mn), c2 = exp2f(m2[q] - mn);
+              ll = ll * c1 + l2[q] * c2;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) acc[k] = acc[k] * c1 + a2[q][k] * c2;
+              mm = mn;
+            }
           }
         }
         float o[8];
@@ -1053,14 +1135,14 @@ static cudaError_t prepare_decode_tc(int* ctas_per_sm) {
   int dev = -1, occ = 0;
   if (!per_device_ready(pd, &dev, &occ)) {
     cudaError_t e = cudaFuncSetAttribute(attn_decode_tc_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         DtcCfg<HD>::SMEM);
+                                         DtcCfg<HD, G>::SMEM);
     if (e != cudaSuccess) return e;
     // all of the unified L1 / shared storage as shared memory, so that two CTAs fit per SM
     e = cudaFuncSetAttribute(attn_decode_tc_kernel<HD, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_decode_tc_kernel<HD, G>, DtcCfg<HD>::THREADS,
-                                                      DtcCfg<HD>::SMEM);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_decode_tc_kernel<HD, G>, DtcCfg<HD, G>::THREADS,
+                                                      DtcCfg<HD, G>::SMEM);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
     per_device_mark(pd, dev, occ);
@@ -1079,7 +1161,7 @@ static cudaError_t decode_tc_ctas_per_sm(int G, int* per_sm) {
 
 template <int HD, int G>
 static cudaError_t launch_decode_tc_hd(const AttnArgs& a, cudaStream_t s) {
-  using C = DtcCfg<HD>;
+  using C = DtcCfg<HD, G>;
   int per_sm = 0;
   cudaError_t e0 = prepare_decode_tc<HD, G>(&per_sm);  // sets the shared-memory attributes once
   if (e0 != cudaSuccess) return e0;
@@ -1089,32 +1171,50 @@ static cudaError_t launch_decode_tc_hd(const AttnArgs& a, cudaStream_t s) {
   if (!a.sched || a.ctas < 1 || a.sched_ctas < a.ctas) return cudaErrorInvalidValue;
   const int64_t kv_rows = static_cast<int64_t>(a.n) * 2 * a.kvm.blocks * a.nkv_l * a.kvm.block_len;
   if (kv_rows >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
-  CUtensorMap mkv, mkv16;
+  CUtensorMap mkv, mkv64, mkv16;  // boxes of 128, 64 and 16 rows x 64 dims
   if (!make_tmap_2d(&mkv, a.kv, kv_rows, HD, HD, 128, true)) return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&mkv64, a.kv, kv_rows, HD, HD, 64, true)) return cudaErrorInvalidValue;
   if (!make_tmap_2d(&mkv16, a.kv, kv_rows, HD, HD, 16, true)) return cudaErrorInvalidValue;
-  return launch_pdl(attn_decode_tc_kernel<HD, G>, dim3(a.ctas), dim3(C::THREADS), C::SMEM, s, mkv, mkv16, a);
+  return launch_pdl(attn_decode_tc_kernel<HD, G>, dim3(a.ctas), dim3(C::THREADS), C::SMEM, s, mkv, mkv64, mkv16, a);
 }
 
-// The split count of decode_splits for every unit, and a thinner last wave split further:
-// with one split per unit, when the units of the last partial wave fill at most
-// half of the resident CTAs, each of them takes f = resident / units-in-the-wave
-// splits (at most 4, each at least two key tiles) so that the wave keeps enough
-// loads in flight to hold the HBM rate (measured on 128 sequences x 2049 keys,
-// tp 2: 1024 units on 304 resident CTAs leave 112 for the last wave).
+// The decode split plan.  A few units: every unit in decode_splits parts (one
+// level).  Otherwise, on the persistent tensor-core kernel, the units in levels
+// of 1, 2, 4 and 8 splits, sized by guided self-scheduling: items of a level are
+// handed out while the work left is at least kDecodeGuide x (pipelines) x (item
+// size), so that the items still to come when a pipeline runs dry are small
+// against the work left, and the pipelines end close together.  Split counts
+// are rounded so that every split of a full-length unit holds whole key tiles
+// (17 tiles in 8 parts of 3 tiles: 6 splits).
+constexpr double kDecodeGuide = 0.5;
 DecodeSplit decode_split_plan(int max_kv_len, int num_units, int num_sms, int hd, int G, int max_splits) {
-  DecodeSplit d{decode_splits(max_kv_len, num_units, num_sms, hd, G, max_splits), 0, 1};
-  if (hd != 128 || d.splits != 1 || num_units <= 0) return d;
-  const int resident = 2 * num_sms;  // decode pipelines: two per CTA, one CTA per SM
-  const int rem = num_units % resident;
-  if (rem == 0 || num_units < resident || 2 * rem > resident) return d;
-  int f = resident / rem;
-  const int tiles = (max_kv_len + 127) / 128;
-  if (f > tiles / 2) f = tiles / 2;
-  if (f > 4) f = 4;
-  if (f > max_splits) f = max_splits;
-  if (f < 2) return d;
-  d.tail_units = rem;
-  d.tail_splits = f;
+  DecodeSplit d{};
+  for (int l = 0; l < kDecLevels; ++l) d.splits[l] = 1;
+  d.splits[0] = decode_splits(max_kv_len, num_units, num_sms, hd, G, max_splits);
+  d.units[0] = num_units > 0 ? num_units : 0;
+  if (hd != 128 || d.splits[0] != 1 || num_units <= 0) return d;
+  const int nt = (max_kv_len + 127) / 128;  // key tiles of a full-length unit
+  const double pipes = 2.0 * num_sms;       // decode pipelines: two per CTA, one CTA per SM
+  double left = static_cast<double>(num_units) * nt;
+  int u = 0;
+  const int want[kDecLevels] = {1, 2, 4, 8};
+  for (int l = 0; l < kDecLevels; ++l) {
+    int f = want[l] < max_splits ? want[l] : max_splits;
+    if (f > nt) f = nt;
+    if (f < 1) f = 1;
+    const int chunk = (nt + f - 1) / f;  // tiles per split
+    const int ns = (nt + chunk - 1) / chunk;
+    d.splits[l] = ns;
+    int n = num_units - u;
+    if (l + 1 < kDecLevels) {
+      const double stop = kDecodeGuide * pipes * chunk;  // work left when this level's items get too big
+      const double fit = (left - stop) / nt;
+      n = fit <= 0.0 ? 0 : (fit >= n ? n : static_cast<int>(fit + 0.999999));
+    }
+    d.units[l] = n;
+    u += n;
+    left -= static_cast<double>(n) * nt;
+  }
   return d;
 }
 

@@ -253,6 +253,32 @@ cudaError_t launch_row_stats(const void* x, int64_t rows, int H, void* xh, float
                              cudaStream_t s);
 
 
+// Decode split plan: the units (sequence, rank, kv head) in consecutive levels,
+// level l holding units[l] units whose keys are split in splits[l] parts each (a
+// split covers whole 128-key tiles); items are handed out level by level, so
+// the pieces get smaller as the work runs out.
+constexpr int kDecLevels = 4;
+struct DecodeSplit {
+  int units[kDecLevels];
+  int splits[kDecLevels];
+};
+__host__ __device__ inline int plan_items(const DecodeSplit& d) {
+  int n = 0;
+  for (int l = 0; l < kDecLevels; ++l) n += d.units[l] * d.splits[l];
+  return n;
+}
+__host__ __device__ inline int plan_units(const DecodeSplit& d) {
+  int n = 0;
+  for (int l = 0; l < kDecLevels; ++l) n += d.units[l];
+  return n;
+}
+// the largest split count of a level that holds units (partials per unit in the workspace)
+__host__ __device__ inline int plan_max_splits(const DecodeSplit& d) {
+  int m = 1;
+  for (int l = 0; l < kDecLevels; ++l)
+    if (d.units[l] > 0 && d.splits[l] > m) m = d.splits[l];
+  return m;
+}
 struct AttnArgs {
   const void* qkv;           // [T, n * w_rank] (q post-RoPE: bf16 high part for prefill tokens, fp16 for decode)
   const void* q_lo;          // [T, n * nq_l * hd] bf16 low part of q (prefill tokens)
@@ -268,9 +294,7 @@ struct AttnArgs {
   float scale_log2;          // log2(e) / sqrt(hd)
   float* part;               // split-KV partials (decode)
   int* counters;
-  int splits;                // key splits per (sequence, rank, kv head) unit
-  int tail_units;            // decode: the last tail_units units take tail_splits splits instead
-  int tail_splits;
+  DecodeSplit plan;          // decode: the units' key splits
   int ctas;                  // CTAs of a persistent launch (each walks work items)
   int* sched;                // decode: 2 ints (next ticket, CTAs done), zero between steps
   int sched_ctas;            // decode: CTAs of all the launches that draw from sched
@@ -278,12 +302,6 @@ struct AttnArgs {
 };
 cudaError_t launch_attention_prefill(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s);
-// Decode split plan: every unit's keys in `splits` parts, except the last
-// tail_units units, in tail_splits parts (a last wave too thin to keep HBM busy,
-// split further); tail_units 0 when no such wave.
-struct DecodeSplit {
-  int splits, tail_units, tail_splits;
-};
 DecodeSplit decode_split_plan(int max_kv_len, int num_units, int num_sms, int hd, int G, int max_splits);
 
 cudaError_t launch_final_norm_select(const void* hidden, int H, const int32_t* cu_q, int B, const void* w,
