@@ -77,9 +77,15 @@ struct GemmParams {
 // half of the BN weight rows (BN / 2), so a K block moves 32 KB (BN = 256) into
 // and out of each SM's shared memory instead of 48 KB; each CTA's epilogue
 // handles its 128 rows from its own TMEM.
-template <int BN, int EPI = EPI_STORE, bool ACC = false, bool SWAP = false, bool PAIR = false>
+// XCH: a cluster of two such pairs on one 256 x 256 residual tile, each pair over
+// one half of the K range (a rank segment at tp 2); each CTA sends the columns it
+// does not finish to the other pair's CTA of the same rows through distributed
+// shared memory and finishes the other 128 columns, adding the two halves in
+// split order.
+template <int BN, int EPI = EPI_STORE, bool ACC = false, bool SWAP = false, bool PAIR = false, bool XCH = false>
 struct GemmCfg {
-  static constexpr int CL = PAIR ? 2 : 1;  // CTAs per cluster
+  static_assert(!XCH || (PAIR && EPI == EPI_RESID && BN == 256), "the exchange: residual 256-wide pair tiles");
+  static constexpr int CL = XCH ? 4 : (PAIR ? 2 : 1);  // CTAs per cluster
   // epilogue warps: 8 (two per TMEM lane quarter, splitting the columns) where the
   // columns split into independent halves, else 4
   static constexpr int EW =
@@ -119,7 +125,7 @@ struct GemmCfg {
   // swapped epilogues other than the argmax stage the summed tile token-major in
   // fp32 ([BN tokens][128 features]) and write whole token rows from there
   static constexpr int TROW_BYTES = (SWAP && EPI != EPI_ARGMAX) ? BN * 128 * 4 : 0;
-  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * QUEUE + 1;
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * QUEUE + 1 + 2;  // ... PRO, XRDY, XFULL
   // outputs leave through TMA stores (fp16) / TMA reduce-adds (fp32 residual) from one
   // 32-row x 128-byte staging box per epilogue warp
   static constexpr bool TMA_OUT = !SWAP && (EPI == EPI_STORE || EPI == EPI_SILU || EPI == EPI_RESID);
@@ -1036,19 +1042,24 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& p, uint32_t tmem
   report_sat(p.status, sat);
 }
 
-template <int BN, int EPI, bool ACC, bool SWAP, bool PAIR>
-__global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
+template <int BN, int EPI, bool ACC, bool SWAP, bool PAIR, bool XCH>
+__global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR, XCH>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2,
                    const __grid_constant__ CUtensorMap tmKV, const GemmParams p) {
-  using C = GemmCfg<BN, EPI, ACC, SWAP, PAIR>;
+  using C = GemmCfg<BN, EPI, ACC, SWAP, PAIR, XCH>;
   constexpr int STAGES = C::STAGES;
   static_assert(!PAIR || (!SWAP && EPI != EPI_ARGMAX), "CTA pairs: token tiles only");
-  // rank in the CTA pair (0 issues the MMAs for both); 0 without pairs
+  // rank in the cluster; a pair is ranks 2k and 2k + 1, the even one (its leader)
+  // issuing the MMAs for both; 0 without pairs
   const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
-  // a pair takes every unit its cluster index selects (both CTAs the same units)
-  const int u0 = static_cast<int>(blockIdx.x) / C::CL;
-  const int ustep = static_cast<int>(gridDim.x) / C::CL;
+  const uint32_t prank = crank & 1u, lead = crank & ~1u;
+  // a pair takes every unit its cluster index selects (both CTAs the same units);
+  // with the exchange, pair k of a cluster takes split k of the cluster's tile
+  const int u0 = XCH ? static_cast<int>(blockIdx.x) / 4 * 2 + static_cast<int>(crank >> 1)
+                     : static_cast<int>(blockIdx.x) / C::CL;
+  const int ustep = XCH ? static_cast<int>(gridDim.x) / 4 * 2 : static_cast<int>(gridDim.x) / C::CL;
+  const uint16_t pmask = static_cast<uint16_t>(3u << lead);  // this pair's CTAs (multicast commits)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -1083,10 +1094,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
 #define QFULL(k) (bar0 + 8u * (2 * STAGES + 5 + (k)))
 #define QEMPTY(k) (bar0 + 8u * (2 * STAGES + 5 + C::QUEUE + (k)))
 #define PRO (bar0 + 8u * (2 * STAGES + 5 + 2 * C::QUEUE))
+#define XRDY (bar0 + 8u * (2 * STAGES + 6 + 2 * C::QUEUE))
+#define XFULL (bar0 + 8u * (2 * STAGES + 7 + 2 * C::QUEUE))
   volatile int* queue = reinterpret_cast<volatile int*>(tmem_slot + 4);  // [QUEUE] tile ids
   // an epilogue warp hands an accumulator back to the MMA issuer (a pair's leader)
   auto tempty_arrive = [&](uint32_t bar) {
-    if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(bar, 0));
+    if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(bar, lead));
     else mbar_arrive(bar);
   };
 
@@ -1105,6 +1118,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
       mbar_init(QEMPTY(k), 5);  // the MMA thread and the 4 epilogue warps
     }
     mbar_init(PRO, 1);
+    mbar_init(XRDY, 1);                  // the other pair's CTA: its stage memory is free
+    mbar_init(XFULL, XCH ? 32 * C::EW : 1);  // its epilogue threads: their columns are here
     *abort_flag = 0;
     *last_flag = 0;
     fence_barrier_init();
@@ -1165,13 +1180,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
       auto load = [&](const Unit& un, int g, int s, bool x_part, bool w_part) {
         const int r = g / p.kb_seg, kb = g - r * p.kb_seg;
         // this CTA's token rows and (pairs) its half of the tile's weight rows
-        const int t0 = un.tt * TM_T + static_cast<int>(crank) * 128;
-        const int f0 = un.tf * TM_F + static_cast<int>(crank) * (BN / 2);
+        const int t0 = un.tt * TM_T + static_cast<int>(prank) * 128;
+        const int f0 = un.tf * TM_F + static_cast<int>(prank) * (BN / 2);
         const uint32_t xdst = smem_u32(SWAP ? sB + s * C::B_BYTES : sA + s * C::A_BYTES);
         const uint32_t wdst = smem_u32(SWAP ? sA + s * C::A_BYTES : sB + s * C::B_BYTES);
         if constexpr (PAIR) {
           // both CTAs' loads complete on the leader's full barrier, which expects both
-          const uint32_t cbar = mapa_shared(FULL(s), 0);
+          const uint32_t cbar = mapa_shared(FULL(s), lead);
           if (x_part) tma_load_2d_pair(xdst, &tmX, cbar, r * p.x_k_seg + kb * 64, t0);
           if (w_part) tma_load_2d_pair(wdst, &tmW, cbar, kb * 64, r * p.w_row_seg + f0);
         } else {
@@ -1181,7 +1196,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
       };
       auto expect = [&](int s) {
         if constexpr (PAIR) {
-          if (crank == 0) mbar_arrive_expect_tx(FULL(s), 2 * C::STAGE_BYTES);
+          if (prank == 0) mbar_arrive_expect_tx(FULL(s), 2 * C::STAGE_BYTES);
         } else {
           mbar_arrive_expect_tx(FULL(s), C::STAGE_BYTES);
         }
@@ -1234,13 +1249,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
       // every load issued has landed before the CTA may exit (a pair's loads land on
       // the leader's barriers: the leader waits for both CTAs', and the peer stays
       // until the final cluster barrier, which the leader reaches after this)
-      if (crank == 0)
+      if (prank == 0)
         for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
           mbar_wait(FULL(j % STAGES), (j / STAGES) & 1, nullptr, p.status);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (a pair's leader issues for both CTAs) ----------------
-    if (lane == 0 && crank == 0) {
+    if (lane == 0 && prank == 0) {
       const uint32_t idesc = idesc_f16_f32(PAIR ? 256 : 128, BN);
       int it = 0, seg = 0, qk = 0;
       bool ok = true;
@@ -1280,12 +1295,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
               if constexpr (PAIR) tc_mma_f16_pair(d, ad + 2ull * kk, bd + 2ull * kk, idesc, (g > gs || kk > 0) ? 1u : 0u);
               else tc_mma_f16(d, ad + 2ull * kk, bd + 2ull * kk, idesc, (g > gs || kk > 0) ? 1u : 0u);
             }
-            if constexpr (PAIR) tc_commit_pair_mc(EMPTY(s));  // frees the stage in both CTAs
+            if constexpr (PAIR) tc_commit_pair_mc(EMPTY(s), pmask);  // frees the stage in both CTAs
             else tc_commit(EMPTY(s));
             ++it;
           }
           if (!ok) break;
-          if constexpr (PAIR) tc_commit_pair_mc(TFULL(b));  // both CTAs' epilogues
+          if constexpr (PAIR) tc_commit_pair_mc(TFULL(b), pmask);  // both CTAs' epilogues
           else tc_commit(TFULL(b));
           ++seg;
         }
@@ -1409,6 +1424,89 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
         }
       }
     }
+  } else if constexpr (XCH) {
+    // ---------------- epilogue of the K-split exchange (warps 2..9) ----------------
+    // This CTA's 128 rows of the 256 x 256 tile, its split's K half complete in
+    // TMEM buffer 0.  Split `me` finishes columns [128 me, 128 me + 128) and sends
+    // the other 128 to the other pair's CTA of the same rows (cluster rank ^ 2),
+    // into that CTA's stage memory once the MMAs reading it are done: fp32,
+    // [32 column groups of 4][128 rows][4], so a warp's 16-byte stores and loads
+    // are contiguous.  The two warps of a lane quarter take 64 columns each.
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int ws = (warp - 2) >> 2;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    uint8_t* box = sOut + (warp - 2) * (C::NXB * 4096 + 2048);
+    uint8_t* box16 = box + C::NXB * 4096;
+    uint32_t sat = 0;
+    const int me = static_cast<int>(crank >> 1);
+    const uint32_t peer = crank ^ 2u;
+    const int fin = me * 128 + ws * 64;        // this thread's finished columns
+    const int snd = (1 - me) * 128 + ws * 64;  // and the ones it sends
+    const uint32_t rbuf = smem_u32(smem);
+    if (u0 < units) {
+      const Unit un = unit_of(p, u0);
+      const int t = un.tt * C::TM_T + static_cast<int>(prank) * 128 + row;
+      const int tbox = un.tt * C::TM_T + static_cast<int>(prank) * 128 + q * 32;
+      const int f0 = un.tf * BN;
+      const bool row_ok = t < p.T;
+      if (p.row_ss_out != nullptr) {  // old residual of the first finished chunks, while the MMA runs
+#pragma unroll
+        for (int k = 0; k < C::NXB; ++k) prefetch_rows32(p, box + k * 4096, t, row_ok, f0 + fin + 32 * k, lane);
+      }
+      bool ok = warp_all(mbar_wait(TFULL(0), 0, abort_flag, p.status));
+      // this pair's MMAs are done: this CTA's stage memory may take the peer's columns
+      if (ok && threadIdx.x == 64) mbar_arrive_cluster(mapa_shared(XRDY, peer));
+      ok = ok && warp_all(mbar_wait_cl(XRDY, 0, abort_flag, p.status));
+      tc_fence_after();
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float v[32];
+          tc_ld32(lane_addr + static_cast<uint32_t>(snd + 32 * c), v);
+          const int cg0 = (ws * 64 + 32 * c) >> 2;  // the peer's column group of v[0]
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            st_cluster_v4(mapa_shared(rbuf + static_cast<uint32_t>(((cg0 + k) * 128 + row) * 16), peer), v[4 * k],
+                          v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        }
+      }
+      // every epilogue thread arrives (after a failure too, so that the peer's bounded wait ends)
+      mbar_arrive_cluster(mapa_shared(XFULL, peer));
+      ok = ok && warp_all(mbar_wait_cl(XFULL, 0, abort_flag, p.status));
+      if (ok) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          float v[32];
+          tc_ld32(lane_addr + static_cast<uint32_t>(fin + 32 * c), v);
+          const int cg0 = (ws * 64 + 32 * c) >> 2;
+          const float* rb = reinterpret_cast<const float*>(smem);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float4 o = *reinterpret_cast<const float4*>(rb + ((cg0 + k) * 128 + row) * 4);
+            // split 0's half plus split 1's (the rank order at tp 2)
+            v[4 * k] = me == 0 ? v[4 * k] + o.x : o.x + v[4 * k];
+            v[4 * k + 1] = me == 0 ? v[4 * k + 1] + o.y : o.y + v[4 * k + 1];
+            v[4 * k + 2] = me == 0 ? v[4 * k + 2] + o.z : o.z + v[4 * k + 2];
+            v[4 * k + 3] = me == 0 ? v[4 * k + 3] + o.w : o.w + v[4 * k + 3];
+          }
+          if (p.row_ss_out != nullptr) {  // uniform: read-add-store and the next norm's inputs
+            if (c == 0) cp_async_wait_all();
+            resid_rows32<C>(p, &tmO, &tmO2, c < C::NXB ? box + c * 4096 : box, box16, t, row_ok, f0 + fin + 32 * c,
+                            tbox, lane, v, c < C::NXB, sat);
+          } else {
+            box_acquire(lane);
+            stage_f32x32(box, lane, v);
+            box_release(&tmO, box, f0 + fin + 32 * c, tbox, true, lane);
+          }
+        }
+      }
+    }
+    report_sat(p.status, sat);
+    cp_async_wait_all();  // no copy into the staging outlives the CTA
+    if (lane == 0) bulk_wait_read();
+    __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..), tokens on the M side ----------------
     // A warp reads TMEM lanes 32*(warp % 4) .. +31 (one token row per thread);
@@ -1437,8 +1535,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
     int seg = 0;
     for (int u = u0; u < units; u += ustep) {
       const Unit un = unit_of(p, u);
-      const int t = un.tt * C::TM_T + static_cast<int>(crank) * 128 + row;
-      const int tbox = un.tt * C::TM_T + static_cast<int>(crank) * 128 + q * 32;  // first row of this warp's boxes
+      const int t = un.tt * C::TM_T + static_cast<int>(prank) * 128 + row;
+      const int tbox = un.tt * C::TM_T + static_cast<int>(prank) * 128 + q * 32;  // first row of this warp's boxes
       const int f0 = un.tf * BN;
       const bool row_ok = t < p.T;
       float rinv = 1.0f;  // deferred RMSNorm of the input row (QKV, gate_up)
@@ -1577,12 +1675,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
         }
         // every epilogue thread takes the same path from here (named barriers follow)
         if (!named_bar_and(1, 32 * C::EW, ok)) {
-          if (threadIdx.x == 64) drain_split_counters(p, u, units, ustep, PAIR ? 2 : 1, static_cast<int>(crank));
+          if (threadIdx.x == 64) drain_split_counters(p, u, units, ustep, PAIR ? 2 : 1, static_cast<int>(prank));
           break;
         }
         if (p.splits > 1) {
           // a pair's CTAs each sum their own 128 rows: one partial set per CTA of the tile
-          const int tile = (un.tt * p.tiles_f + un.tf) * (PAIR ? 2 : 1) + static_cast<int>(crank);
+          const int tile = (un.tt * p.tiles_f + un.tf) * (PAIR ? 2 : 1) + static_cast<int>(prank);
           float* part = p.partials + (static_cast<size_t>(tile) * p.splits + un.split) * (BN * 128);
           if (row_ok) {  // rows past the last token are never read
 #pragma unroll
@@ -1697,6 +1795,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, ACC, SWAP, PAIR>::THREADS, 1)
 #undef QFULL
 #undef QEMPTY
 #undef PRO
+#undef XRDY
+#undef XFULL
   tc_fence_before();
   __syncthreads();
   // a pair: the leader's MMAs into this CTA's TMEM and shared memory, and the
@@ -1778,6 +1878,35 @@ static inline int cdiv(long long a, long long b) { return static_cast<int>((a + 
 // tile width of a CTA pair (TMEM: two accumulators of BN columns per CTA): 256,
 // or 128 for the rank-sum epilogue (its running sums in registers hold BN at 128)
 constexpr int kPairMaxBN = 256;
+
+// 4-CTA clusters of the exchange kernel resident at once on the current device
+// (cluster placement follows the GPU's SM groups, so fewer than SMs / 4 can fit);
+// 0 when the query fails.
+static int xch_max_clusters() {
+  static PerDevice pd;
+  int dev = -1, n = 0;
+  if (per_device_ready(pd, &dev, &n)) return n;
+  auto kern = gemm_tc_kernel<256, EPI_RESID, true, false, true, true>;
+  using Cfg = GemmCfg<256, EPI_RESID, true, false, true, true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(4 * 64);
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 4;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  per_device_mark(pd, dev, n);
+  return n;
+}
 
 GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
   GemmPlan pl{};
@@ -1865,6 +1994,28 @@ GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
     pl.BN = 128;
     pl.tiles_f = cdiv(pr.N, 128);
   }
+  // Residual GEMMs with one or two rank segments whose 256 x 256 tiles fit one
+  // wave of 4-CTA clusters: the two pairs of a cluster take one K half each (a
+  // rank segment at tp 2) and meet through distributed shared memory, no
+  // partials in global memory.  A 256-wide pair tile moves its operands at
+  // ~390 ns per K block against ~330 ns for the 128-wide one with the whole K.
+  if (pl.splits == 1 && pr.epi == EPI_RESID && pr.T >= 256 && pr.n_seg <= 2 && total_kb % 2 == 0 &&
+      total_kb >= 16) {
+    const int tt2 = cdiv(pr.T, 256), tf2 = cdiv(pr.N, 256);
+    const int tiles2 = tt2 * tf2;
+    if (4 * tiles2 >= num_sms / 2 && tiles2 <= xch_max_clusters()) {
+      pl.pair = true;
+      pl.xch = true;
+      pl.BN = 256;
+      pl.acc = true;
+      pl.splits = 2;
+      pl.tiles_t = tt2;
+      pl.tiles_f = tf2;
+      pl.grid = 4 * tiles2;
+      pl.partial_floats = 0;
+      return pl;
+    }
+  }
   // Long-K residual (row-parallel) GEMMs on CTA pairs with 256-wide tiles and the
   // K range (the rank segments) split in two: a 256-wide pair tile moves its
   // operands at ~390 ns per K block against ~330 ns for a 128-wide one with half
@@ -1915,11 +2066,11 @@ GemmPlan plan_gemm(const GemmProblem& pr, int num_sms) {
 
 int gemm_num_tiles_f(const GemmProblem& pr, const GemmPlan& plan) { return plan.tiles_f; }
 
-template <int BN, int EPI, bool ACC, bool SWAP, bool PAIR = false>
+template <int BN, int EPI, bool ACC, bool SWAP, bool PAIR = false, bool XCH = false>
 static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, const GemmProblem& pr,
                                   const GemmParams& gp, int grid, cudaStream_t s) {
-  auto kern = gemm_tc_kernel<BN, EPI, ACC, SWAP, PAIR>;
-  using Cfg = GemmCfg<BN, EPI, ACC, SWAP, PAIR>;
+  auto kern = gemm_tc_kernel<BN, EPI, ACC, SWAP, PAIR, XCH>;
+  using Cfg = GemmCfg<BN, EPI, ACC, SWAP, PAIR, XCH>;
   constexpr int smem = Cfg::SMEM;
   static PerDevice attr;  // per instantiation and device
   {
@@ -1949,7 +2100,7 @@ static cudaError_t launch_variant(const CUtensorMap& mx, const CUtensorMap& mw, 
       return cudaErrorInvalidValue;
   }
   if constexpr (PAIR)
-    return launch_pdl_cluster(kern, 2, dim3(grid), dim3(Cfg::THREADS), smem, s, mx, mw, mo, mo2, mkv, gp);
+    return launch_pdl_cluster(kern, Cfg::CL, dim3(grid), dim3(Cfg::THREADS), smem, s, mx, mw, mo, mo2, mkv, gp);
   return launch_pdl(kern, dim3(grid), dim3(Cfg::THREADS), smem, s, mx, mw, mo, mo2, mkv, gp);
 }
 
@@ -2008,8 +2159,13 @@ cudaError_t launch_gemm(const GemmProblem& pr, const GemmPlan& pl, float* partia
   if (pl.BN == BN_ && pr.epi == EPI_ && pl.acc == ACC_ && pl.swap == SW_ && !pl.pair)         \
     return launch_variant<BN_, EPI_, ACC_, SW_>(mx, mw, pr, gp, g, stream);
 #define TP_VP(BN_, EPI_, ACC_)                                                               \
-  if (pl.BN == BN_ && pr.epi == EPI_ && pl.acc == ACC_ && !pl.swap && pl.pair)               \
+  if (pl.BN == BN_ && pr.epi == EPI_ && pl.acc == ACC_ && !pl.swap && pl.pair && !pl.xch)    \
     return launch_variant<BN_, EPI_, ACC_, false, true>(mx, mw, pr, gp, g, stream);
+  if (pl.xch) {
+    if (pl.BN != 256 || pr.epi != EPI_RESID || !pl.pair || pl.splits != 2 || g != 4 * pl.tiles_t * pl.tiles_f)
+      return cudaErrorInvalidValue;
+    return launch_variant<256, EPI_RESID, true, false, true, true>(mx, mw, pr, gp, g, stream);
+  }
   TP_VP(256, EPI_STORE, false)
   TP_VP(256, EPI_SILU, false)
   TP_VP(256, EPI_QKV, false)

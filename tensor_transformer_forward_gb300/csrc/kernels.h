@@ -221,6 +221,8 @@ struct GemmPlan {
   bool swap;        // weights on the MMA's M side (few tokens): tiles of 128 features x BN tokens
   bool pair;        // CTA pairs (clusters of 2): tiles of 256 tokens x BN features, cta_group::2 MMAs
   bool acc;         // running sum in registers (multi-segment or split-K)
+  bool xch;         // residual pair tiles, K in two halves on two pairs of a 4-CTA cluster
+                    // exchanging partials through distributed shared memory
   int tiles_t, tiles_f, splits;
   int grid;
   size_t partial_floats;  // workspace floats for split-K partials

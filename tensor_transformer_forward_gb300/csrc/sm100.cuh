@@ -324,6 +324,39 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
+// Wait on this CTA's mbarrier with cluster-scope acquire: writes another CTA of
+// the cluster made to this CTA's shared memory before its (release.cluster)
+// arrival are visible after it.  Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort, int* status) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((it & 63u) == 63u) {
+      if (abort && *abort) return false;
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > TP_WAIT_LIMIT_NS) {
+        if (abort) *abort = 1;
+        raise_flag(status, TP_DEVFLAG_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+// 16-byte store into the shared memory of a CTA of the cluster (shared::cluster address).
+__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
 // 2D tiled load into this CTA's shared memory whose completion (transaction bytes)
 // is signalled on an mbarrier of either CTA of the pair (cbar: shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cbar, int c0,

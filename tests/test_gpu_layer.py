@@ -86,12 +86,14 @@ def test_32b_layer_tp16_replicated_kv():
     check_step(g, [0, 1, 2], head=False)
 
 
-@pytest.mark.parametrize("n", [1, 2])
+@pytest.mark.parametrize("n", [1, 2, 4])
 def test_long_k_residual_gemm_split_in_two(n):
-    """down_proj with 256 K blocks (intermediate 16384) over 1280 prefill tokens
-    (20 pair tiles of 256 x 256) runs on CTA pairs with its rank segments split in
-    K parts that meet in split-K partials; the residual it leaves against the
-    oracle."""
+    """down_proj with 256 K blocks (intermediate 16384) over 1297 tokens (24 tiles
+    of 256 x 256).  At tp 1 and 2 (one or two rank segments) o_proj and down_proj
+    run on 4-CTA clusters whose two CTA pairs take one K half each and exchange
+    their partials through distributed shared memory; at tp 4 down_proj runs on
+    CTA pairs with the rank segments split in two halves that meet in split-K
+    partials in global memory.  The residual they leave against the oracle."""
     s = synth.ModelShape(hidden=1024, num_q_heads=8, num_kv_heads=4, head_dim=128, intermediate=16384, vocab=1000,
                          num_layers=1)
     w = synth.Workload("long_k_resid", s, (n,), ((1280, 0),), (17,), 1, True)
