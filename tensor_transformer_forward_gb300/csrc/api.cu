@@ -659,7 +659,7 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   const bool has_decode = b->num_prefill < b->num_seqs;
   const bool side_by_side = b->num_prefill > 0 && has_decode;
   cudaStream_t ps = s;
-  const int pre_ctas = std::max(8, x->num_sms / 4);  // the prefill attention's CTAs beside the decode
+  const int pre_ctas = std::max(8, x->num_sms * 3 / 8);  // the prefill attention's CTAs beside the decode
   if (side_by_side) {
     if (!x->side) {
       int least = 0, greatest = 0;
@@ -674,10 +674,11 @@ tp_status tp_decoder_layer_forward(tp_ctx* x, const void* shards, const tp_batch
   }
   if (b->num_prefill > 0) {
     aa.seq_begin = 0; aa.seq_end = b->num_prefill;
-    // beside the decode attention a quarter of the SMs walk the work items (measured
-    // on the 28-layer mixed step: 16 / 24 / 30 / 38 / 48 / 76 CTAs gave 8.06 / 8.10 /
-    // 7.96 / 7.89 / 8.05 / 8.00 ms); alone, one CTA per item, which the hardware
-    // hands to SMs as they free up (heaviest items first)
+    // beside the decode attention 3/8 of the SMs walk the work items (measured on
+    // the 28-layer mixed step, 128 decode + 4 x 512 prefill tokens, beside the
+    // persistent decode kernel: 16 / 24 / 30 / 38 / 48 / 57 / 76 CTAs gave 7.61 /
+    // 7.51 / 7.48 / 7.45 / 7.42 / 7.42 / 7.44 ms); alone, one CTA per item, which
+    // the hardware hands to SMs as they free up (heaviest items first)
     aa.ctas = side_by_side ? pre_ctas : INT_MAX;
     Timed tm(x, TP_K_ATTN_PREFILL, ps);
     e = tpk::launch_attention_prefill(aa, ps);
