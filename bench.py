@@ -93,21 +93,27 @@ NCU_TRAFFIC = {
     # attention as each of the 28 layers' (128 sequences x 2049 keys, tp 2); the
     # main and the side launch of the layer summed (serialised under ncu, the main
     # launch finds every item)
-    ("qwen3_0.6b_model_mixed", 2, "attn_decode"): (1082750720 + 3527424 + 71168, "k_attention.cu", "35d704b99f046794"),
-    ("qwen3_0.6b_layer_prefill2048", 2, "gemm_lm_head"): (311223040 + 3034624, "k_gemm.cu", "b4660ecfc2cf31a9"),
-    ("qwen3_0.6b_layer_decode64x4096", 2, "attn_decode"): (1078377984 + 3269376, "k_attention.cu", "35d704b99f046794"),
-    ("qwen3_32b_layer_tp16_decode32x2048", 16, "gemm_lm_head"): (1558449920 + 3330048, "k_gemm.cu", "b4660ecfc2cf31a9"),
+    ("qwen3_0.6b_model_mixed", 2, "attn_decode"): (1082750720 + 3527424 + 71168, "k_attention.cu", "bae1123ac46e89e3"),
+    ("qwen3_0.6b_layer_prefill2048", 2, "gemm_lm_head"): (311223040 + 3034624, "k_gemm.cu", "baf27ff4fbfd0bf7"),
+    ("qwen3_0.6b_layer_decode64x4096", 2, "attn_decode"): (1078377984 + 3269376, "k_attention.cu", "bae1123ac46e89e3"),
+    ("qwen3_32b_layer_tp16_decode32x2048", 16, "gemm_lm_head"): (1558449920 + 3330048, "k_gemm.cu", "baf27ff4fbfd0bf7"),
 }
 KERNEL_HEADERS = ("kernels.h", "sm100.cuh", "common.cuh")
 
 
 def source_hash(cu_file: str) -> str:
+    """Hash of the kernel source and the headers it includes, code only: line
+    comments and blank lines do not change a kernel, so they do not count."""
     import hashlib
+    import re
     d = os.path.join(ROOT, "tensor_transformer_forward_gb300", "csrc")
     m = hashlib.sha256()
     for f in (cu_file,) + KERNEL_HEADERS:
-        with open(os.path.join(d, f), "rb") as fh:
-            m.update(fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            for line in fh:
+                code = re.sub(r"(^|\s)//.*$", "", line.rstrip("\n")).rstrip()
+                if code:
+                    m.update(code.encode() + b"\n")
     return m.hexdigest()[:16]
 
 

@@ -467,17 +467,20 @@ cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s) {
 // counter; each CTA keeps drawing items until none are left, and its K / V
 // streams, MMAs and softmax run on from one item into the next without draining
 // (a CTA per item left every SM idle while one pair of CTAs ended and the next
-// started, and a last partial wave of items ran on part of the GPU).  256
-// threads, two CTAs per SM:
-//   warp 0    scheduler: draws the next ticket once the current item's last K
-//             tile is issued, checks the item's cache blocks, publishes it in a
-//             4-entry item ring, and writes its query rows into one of two Q
-//             buffers (bf16 high and low parts, the MMA's B operand)
-//   warp 1    TMEM allocation + one MMA-issuing thread
+// started, and a last partial wave of items ran on part of the GPU).  One CTA
+// per SM (its shared memory fills the SM, so a launch can leave whole SMs to
+// another kernel), 512 threads: two independent pipelines of 8 warps, each
+// drawing its own items.  A pipeline's warps:
+//   warp 0    scheduler: draws the next ticket three K tiles before the current
+//             item's K stream ends, checks the item's cache blocks, publishes
+//             it in a 4-entry item ring, loads its query into registers and
+//             writes it as Q^T (bf16 high and low parts, the MMA's B operand)
+//             once the previous item's S MMAs are done
+//   warp 1    (pipeline 0: TMEM allocation for both) one MMA-issuing thread
 //   warps 2-5 softmax, one thread per key of a 128-key tile; at the end of an
 //             item, O (one TMEM row per output dim) into a staging buffer
-//   warp 6    lane 0 streams K tiles, lane 1 V tiles (one stage each; the two
-//             CTAs of an SM overlap each other's loads)
+//   warp 6    lane 0 streams K, lane 1 V through rings of 16 KB slots (two
+//             per tile; see DtcCfg)
 //   warp 7    writer: the staged output as fp16, or a split's partial and, for
 //             the last split of a unit to arrive, the merge of its splits in
 //             split order (so the softmax never waits on global memory)

@@ -60,6 +60,24 @@ def test_ncu_traffic_only_while_the_kernel_source_is_unchanged(monkeypatch):
     assert bench.ncu_traffic("no such workload", 2, "gemm_lm_head") is None
 
 
+def test_source_hash_counts_code_not_comments(tmp_path, monkeypatch):
+    """The hash that ties a traffic capture to a kernel ignores line comments and
+    blank lines and follows any change to the code itself."""
+    import shutil
+    import bench
+    src = os.path.join(bench.ROOT, "tensor_transformer_forward_gb300", "csrc")
+    dst = tmp_path / "tensor_transformer_forward_gb300" / "csrc"
+    shutil.copytree(src, dst)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.source_hash("k_gemm.cu")
+    p = dst / "k_gemm.cu"
+    text = p.read_text()
+    p.write_text(text.replace("\n", "\n// a comment line\n\n", 1))
+    assert bench.source_hash("k_gemm.cu") == h0
+    p.write_text(text.replace("namespace tpk {", "namespace tpk {\nconstexpr int kAnotherConstant = 1;", 1))
+    assert bench.source_hash("k_gemm.cu") != h0
+
+
 def test_reference_arm_prints_the_contract_line():
     """`bench.py --impl reference` (the oracle on the host cores) prints one JSON
     line with the keys the driver reads, on the tiny workload, without a GPU."""
