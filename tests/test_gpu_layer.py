@@ -161,6 +161,19 @@ def test_decode_large_weights_64dim_heads_few_tokens():
     check_step(g, list(range(5)))
 
 
+@pytest.mark.parametrize("q_heads,kv_heads", [(16, 2), (8, 8)])
+def test_decode_query_groups_of_eight_and_one(q_heads, kv_heads):
+    """The tensor-core decode attention with 8 query heads per kv head at tp 2 (the
+    smallest rings: two 16 KB slots each for K and V) and with one (multi-head
+    attention); ragged contexts (one key, a partial last tile, 2200 keys) and a
+    prefill sequence beside them."""
+    s = synth.ModelShape(hidden=512, num_q_heads=q_heads, num_kv_heads=kv_heads, head_dim=128, intermediate=768,
+                         vocab=1000, num_layers=1)
+    w = synth.Workload("decode_groups", s, (2,), ((40, 0),), (0, 130, 2200, 511, 77), 1, False)
+    g = GpuStep(w, 2)
+    check_step(g, list(range(6)))
+
+
 @pytest.mark.parametrize("prefill,decode", [(((130, 0),), (3, 70)), (((9, 0),), (3, 70, 200))])
 def test_hidden_not_a_multiple_of_128(prefill, decode):
     """hidden 4160 = 32.5 x 128: the residual epilogues' last feature tile lies half
