@@ -332,6 +332,22 @@ const char* tp_last_cuda_error(void);
  * *flag (device int32) is non-zero, gives up after limit_ns and sets TP_ERR_TIMEOUT. */
 tp_status tp_debug_wait_probe(const int32_t* flag, int32_t* dev_status, int64_t limit_ns, void* stream);
 
+/* The decode attention's split plan, as tp_decoder_layer_forward makes it for the decode
+ * sequences of a step; host only, nothing is launched ("Tensor parallelism from scratch",
+ * "The cost of communication": decode steps are bound by reading the cache, so its units of
+ * work are cut to keep every SM streaming to the end).  The step's num_units (sequence,
+ * rank, kv head) units go in up to four levels taken in order: level l holds units_out[l]
+ * units whose keys are split in splits_out[l] parts; on 128-dim heads every split is
+ * whole 128-key tiles and later levels are split finer (guided self-scheduling: the items
+ * get smaller as the work left runs out).  max_kv_len: the step's longest context
+ * (tp_batch.max_kv_len); num_sms: the device's SMs; head_dim: 64 or 128; group: q heads
+ * per kv head (1, 2, 4 or 8); max_splits: the most splits the workspace holds partials
+ * for.  units_out, splits_out: host int32[4].  TP_ERR_INVALID_ARG on a null pointer or a
+ * value out of range (max_kv_len, num_units, num_sms, max_splits < 1).  Without a GPU the
+ * occupancy query behind the first level's split count gives way to one CTA per SM. */
+tp_status tp_debug_decode_plan(int32_t max_kv_len, int32_t num_units, int32_t num_sms, int32_t head_dim,
+                               int32_t group, int32_t max_splits, int32_t* units_out, int32_t* splits_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -101,6 +101,7 @@ def _load() -> ctypes.CDLL:
         "tp_profile_begin": ([P, ctypes.c_uint32, I32], I32),
         "tp_profile_end": ([P, ctypes.POINTER(F32), pI32], I32),
         "tp_debug_wait_probe": ([P, P, I64, P], I32),
+        "tp_debug_decode_plan": ([I32, I32, I32, I32, I32, I32, pI32, pI32], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -115,7 +116,7 @@ EXPORTED = ("tp_create", "tp_destroy", "tp_status_string", "tp_last_cuda_error",
             "tp_workspace_init", "tp_embed_vocab_parallel", "tp_decoder_layer_forward", "tp_lm_head_argmax",
             "tp_read_status", "tp_rank_sum_count", "tp_debug_wait_probe", "tp_workspace_part", "tp_launch_count",
             "tp_profile_begin", "tp_profile_end", "tp_lm_head_argmax_static", "tp_keep_intermediates",
-            "tp_decode_advance", "tp_hidden_written")
+            "tp_decode_advance", "tp_hidden_written", "tp_debug_decode_plan")
 KERNELS = ("embed", "rmsnorm", "gemm_qkv", "rope", "attn_prefill", "attn_decode", "gemm_o", "gemm_gate_up",
            "gemm_down", "final_norm", "gemm_lm_head", "argmax", "decode_advance")
 
@@ -439,3 +440,13 @@ def tp_read_status(status: torch.Tensor) -> int:
 def tp_debug_wait_probe(flag: torch.Tensor, status: torch.Tensor, limit_ns: int) -> None:
     _check(_lib.tp_debug_wait_probe(_dev(flag, "flag", torch.int32), _dev(status, "status", torch.int32),
                                     int(limit_ns), _stream()), "tp_debug_wait_probe")
+
+
+def tp_debug_decode_plan(max_kv_len: int, num_units: int, num_sms: int, head_dim: int, group: int,
+                         max_splits: int):
+    """The decode attention's split plan (host only): ([units per level], [splits per level])."""
+    units = (ctypes.c_int32 * 4)()
+    splits = (ctypes.c_int32 * 4)()
+    _check(_lib.tp_debug_decode_plan(int(max_kv_len), int(num_units), int(num_sms), int(head_dim), int(group),
+                                     int(max_splits), units, splits), "tp_debug_decode_plan")
+    return list(units), list(splits)

@@ -945,4 +945,18 @@ tp_status tp_debug_wait_probe(const int32_t* flag, int32_t* dev_status, int64_t 
   return TP_OK;
 }
 
+tp_status tp_debug_decode_plan(int32_t max_kv_len, int32_t num_units, int32_t num_sms, int32_t head_dim,
+                               int32_t group, int32_t max_splits, int32_t* units_out, int32_t* splits_out) {
+  static_assert(tpk::kDecLevels == 4, "the header promises four levels");
+  if (!units_out || !splits_out || max_kv_len < 1 || num_units < 1 || num_sms < 1 || max_splits < 1 ||
+      (head_dim != 64 && head_dim != 128) || (group != 1 && group != 2 && group != 4 && group != 8))
+    return TP_ERR_INVALID_ARG;
+  const tpk::DecodeSplit d = tpk::decode_split_plan(max_kv_len, num_units, num_sms, head_dim, group, max_splits);
+  for (int l = 0; l < tpk::kDecLevels; ++l) {
+    units_out[l] = d.units[l];
+    splits_out[l] = d.splits[l];
+  }
+  return TP_OK;
+}
+
 }  // extern "C"
