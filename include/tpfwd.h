@@ -334,8 +334,9 @@ tp_status tp_debug_wait_probe(const int32_t* flag, int32_t* dev_status, int64_t 
 
 /* The decode attention's split plan, as tp_decoder_layer_forward makes it for the decode
  * sequences of a step; host only, nothing is launched ("Tensor parallelism from scratch",
- * "The cost of communication": decode steps are bound by reading the cache, so its units of
- * work are cut to keep every SM streaming to the end).  The step's num_units (sequence,
+ * "The cost of communication", bounds a decode step below by the time to read memory; the
+ * decode attention reads the KV cache, so its units of work are cut to keep every SM
+ * streaming to the end).  The step's num_units (sequence,
  * rank, kv head) units go in up to four levels taken in order: level l holds units_out[l]
  * units whose keys are split in splits_out[l] parts; on 128-dim heads every split is
  * whole 128-key tiles and later levels are split finer (guided self-scheduling: the items

@@ -1,8 +1,9 @@
 """The decode attention's split plan (host logic, no GPU): how a decode step's
 (sequence, rank, kv head) units are cut into work items for the persistent
-kernel.  Decode is bound by reading the KV cache ("Tensor parallelism from
-scratch", "The cost of communication"), so the plan's job is to keep every
-pipeline streaming until the cache has been read: these tests pin its
+kernel.  A decode step is bounded below by the time to read memory ("Tensor
+parallelism from scratch", "The cost of communication"), and the decode
+attention reads the KV cache, so the plan's job is to keep every pipeline
+streaming until the cache has been read: these tests pin its
 structure and check, on a list-scheduling model of the pipelines, that the cut
 finishes no later than whole units would and close to the even share."""
 
