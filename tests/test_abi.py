@@ -161,3 +161,28 @@ def test_static_scratch_entry_point_refuses_sizes_beyond_its_array_before_device
     b.num_seqs, b.num_tokens = 65, 65
     assert L.tp_lm_head_argmax_static(small.handle, fake, ctypes.byref(b), fake, fake, None, fake, None) == inval
     assert ctx.launch_count() == 0 and small.launch_count() == 0
+
+
+@pytest.mark.parametrize("s,n", [(synth.TINY, 2), (synth.QWEN3_06B, 1), (synth.QWEN3_06B, 2), (synth.QWEN3_32B, 16)])
+def test_workspace_holds_the_declared_intermediates_and_grows_with_its_limits(s, n):
+    """tp_workspace_bytes against what the header says the workspace holds: the
+    four per-token intermediates (fp16 layer output [T, H], the merged projection
+    [T, n, (nq_l + 2 nkv_l) hd] in 16-bit, the attention output [T, n nq_l hd] and
+    SiLU * up [T, n I_p] in fp16) and the fp32 RoPE (cos, sin) table of every
+    position; never smaller when a limit grows, and by at least the per-token
+    parts for every further 128-token tile and by about the table's rows for
+    more positions (regions are padded)."""
+    from tensor_transformer_forward_gb300 import Context
+    ctx = Context(_cfg(s, n))
+    nq_l, nkv_l, hd = s.num_q_heads // n, max(1, s.num_kv_heads // n), s.head_dim
+    per_token = 2 * s.hidden + 2 * n * (nq_l + 2 * nkv_l) * hd + 2 * n * nq_l * hd + 2 * n * (s.intermediate // n)
+    for T, S, P in [(1, 1, 1), (64, 64, 4097), (2048, 1, 2049), (2176, 132, 2049)]:
+        b = ctx.workspace_bytes(T, S, P)
+        assert b >= T * per_token + P * hd * 4, (T, S, P, b)
+        assert ctx.workspace_bytes(2 * T, S, P) >= b
+        if T % 128 == 0:
+            assert ctx.workspace_bytes(2 * T, S, P) - b >= T * per_token
+        assert ctx.workspace_bytes(T, 2 * S, P) >= b
+        assert ctx.workspace_bytes(T, S, 2 * P) >= b
+        if P >= 1024:  # the table is padded too: allow up to 128 positions of it
+            assert ctx.workspace_bytes(T, S, 2 * P) - b >= (P - 128) * hd * 4
